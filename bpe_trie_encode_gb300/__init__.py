@@ -1,0 +1,198 @@
+"""bpe_trie_encode_gb300 -- byte-level BPE training and greedy trie encoding on
+one GB300 (sm_103a).
+
+The work happens in ``libbpetrie.so`` (hand-written CUDA kernels behind the C
+ABI of ``include/bpetrie.h``); this package marshals torch tensors to it.
+PyTorch is used only for device memory and streams.
+
+    import torch, bpe_trie_encode_gb300 as bt
+    ctx = bt.Context()
+    sym = ctx.pretokenize(torch.frombuffer(text, dtype=torch.uint8).cuda())
+    merges, final = ctx.train(sym, 4096)
+    trie = ctx.trie_build(*bt.vocab_from_merges(merges))
+    ids, id_off = ctx.encode(trie, data_u8_cuda, doc_off_i64_cuda)
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import _capi
+from ._capi import (BPE_MAX_MERGES, BPE_OPT_CHUNK, BPE_OPT_GRAPH, BPE_OPT_PROFILE,  # noqa: F401
+                    BPE_OPT_TABLE_LOG2, BPE_WORD_START, BpeError)
+
+__all__ = ["Context", "Trie", "BpeError", "vocab_from_merges", "BPE_WORD_START", "BPE_MAX_MERGES"]
+
+
+def _stream_ptr(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need_cuda(t: torch.Tensor, dtype: torch.dtype, name: str, device: torch.device) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the context is on {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.contiguous()
+
+
+class Trie:
+    """A double-array trie uploaded to the GPU (see ``Context.trie_build``)."""
+
+    def __init__(self, handle: int, device: torch.device, n_tok: int):
+        self._h = ctypes.c_void_p(handle)
+        self.device = device
+        self.n_tok = n_tok
+
+    def info(self) -> dict:
+        n_nodes, n_slots, max_len = ctypes.c_uint64(), ctypes.c_uint64(), ctypes.c_uint32()
+        _capi.load().trie_info(self._h, ctypes.byref(n_nodes), ctypes.byref(n_slots), ctypes.byref(max_len))
+        return {"n_tok": self.n_tok, "n_nodes": n_nodes.value, "n_slots": n_slots.value,
+                "max_token_len": max_len.value}
+
+    def close(self):
+        if self._h:
+            _capi.load().trie_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Context:
+    """A library context on one CUDA device.  Calls are ordered on the torch
+    current stream of that device at the time of each call."""
+
+    def __init__(self, device=None):
+        if not torch.cuda.is_available():
+            raise RuntimeError("bpe_trie_encode_gb300 needs a CUDA GPU")
+        self.lib = _capi.load()
+        self.device = torch.device("cuda", torch.cuda.current_device() if device is None
+                                   else torch.device(device).index or 0)
+        h = ctypes.c_void_p()
+        rc = self.lib.bpe_ctx_create(ctypes.byref(h), self.device.index, ctypes.c_void_p(_stream_ptr(self.device)))
+        if rc != 0:
+            raise BpeError(rc, "bpe_ctx_create failed")
+        self._h = h
+
+    # -- plumbing -----------------------------------------------------------
+    def _sync_stream(self):
+        self.lib.bpe_ctx_set_stream(self._h, ctypes.c_void_p(_stream_ptr(self.device)))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self.lib.bpe_ctx_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_option(self, option: int, value: int) -> None:
+        _capi.check(self._h, self.lib.bpe_ctx_set_option(self._h, option, value))
+
+    def stats(self) -> dict:
+        s = _capi.bpe_stats()
+        _capi.check(self._h, self.lib.bpe_last_stats(self._h, ctypes.byref(s)))
+        out = {s.k[i].name.decode(): {"launches": s.k[i].launches, "bytes": s.k[i].bytes, "ms": s.k[i].ms}
+               for i in range(s.n)}
+        out["kernel_launches"] = s.kernel_launches
+        return out
+
+    # -- the C ABI --------------------------------------------------------
+    def pretokenize(self, data: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+        """uint8 bytes -> int32 tensor holding the uint32 symbols (bit 16 =
+        WORD_START).  Asynchronous on the current stream."""
+        data = _need_cuda(data, torch.uint8, "data", self.device)
+        n = data.numel()
+        if out is None:
+            out = torch.empty(n, dtype=torch.int32, device=self.device)
+        out = _need_cuda(out, torch.int32, "out", self.device)
+        if out.numel() < n:
+            raise ValueError("out too small")
+        self._sync_stream()
+        _capi.check(self._h, self.lib.bpe_pretokenize(self._h, ctypes.c_void_p(data.data_ptr()), n,
+                                                      ctypes.c_void_p(out.data_ptr())))
+        return out[:n]
+
+    def train(self, symbols: torch.Tensor, n_merges: int, final: bool = True):
+        """BPE merge loop.  Returns (merges uint32 [n_done, 4] = (left, right,
+        new_id, count), final symbols int32 tensor or None)."""
+        symbols = _need_cuda(symbols, torch.int32, "symbols", self.device)
+        n = symbols.numel()
+        merges = (_capi.bpe_merge * max(n_merges, 1))()
+        n_done = ctypes.c_uint32(0)
+        n_final = ctypes.c_uint64(0)
+        fin = torch.empty(max(n, 1), dtype=torch.int32, device=self.device) if final else None
+        self._sync_stream()
+        rc = self.lib.bpe_train(self._h, ctypes.c_void_p(symbols.data_ptr() if n else 0), n, n_merges,
+                                merges, ctypes.byref(n_done),
+                                ctypes.c_void_p(fin.data_ptr()) if fin is not None else None,
+                                ctypes.byref(n_final))
+        _capi.check(self._h, rc)
+        m = np.frombuffer(merges, dtype=np.uint32).reshape(-1, 4)[: n_done.value].copy()
+        return m, (fin[: n_final.value] if fin is not None else None)
+
+    def trie_build(self, vocab_bytes, vocab_off) -> Trie:
+        """Double-array trie of token strings vocab_bytes[off[t]:off[t+1]]."""
+        vb = np.ascontiguousarray(np.frombuffer(bytes(vocab_bytes), dtype=np.uint8)
+                                  if isinstance(vocab_bytes, (bytes, bytearray)) else vocab_bytes,
+                                  dtype=np.uint8)
+        off = np.ascontiguousarray(vocab_off, dtype=np.uint64)
+        n_tok = off.size - 1
+        h = ctypes.c_void_p()
+        _capi.check(self._h, self.lib.trie_build(self._h, ctypes.c_void_p(vb.ctypes.data if vb.size else 0),
+                                                 ctypes.c_void_p(off.ctypes.data), n_tok, ctypes.byref(h)))
+        return Trie(h.value, self.device, n_tok)
+
+    def encode(self, trie: Trie, data: torch.Tensor, doc_off: torch.Tensor | None = None,
+               capacity: int | None = None, ids_out: torch.Tensor | None = None):
+        """Greedy longest-match ids.  data: uint8 CUDA tensor; doc_off: int64
+        CUDA tensor of n_docs+1 ascending offsets (default: one document).
+        Returns (ids int32 [n_ids], id_off int64 [n_docs+1])."""
+        data = _need_cuda(data, torch.uint8, "data", self.device)
+        if doc_off is None:
+            doc_off = torch.tensor([0, data.numel()], dtype=torch.int64, device=self.device)
+        doc_off = _need_cuda(doc_off, torch.int64, "doc_off", self.device)
+        n_docs = doc_off.numel() - 1
+        if ids_out is None:
+            cap = data.numel() if capacity is None else capacity
+            ids_out = torch.empty(max(cap, 1), dtype=torch.int32, device=self.device)
+        else:
+            ids_out = _need_cuda(ids_out, torch.int32, "ids_out", self.device)
+            cap = ids_out.numel() if capacity is None else min(capacity, ids_out.numel())
+        id_off = torch.empty(max(n_docs + 1, 1), dtype=torch.int64, device=self.device)
+        n_ids = ctypes.c_uint64(0)
+        if data.numel() == 0:   # keep a valid device pointer for empty input
+            data = torch.empty(16, dtype=torch.uint8, device=self.device)
+        self._sync_stream()
+        rc = self.lib.trie_encode(self._h, trie._h, ctypes.c_void_p(data.data_ptr()),
+                                  ctypes.c_void_p(doc_off.data_ptr()), max(n_docs, 0),
+                                  ctypes.c_void_p(ids_out.data_ptr()), cap,
+                                  ctypes.c_void_p(id_off.data_ptr()), ctypes.byref(n_ids))
+        if rc == -6:
+            raise BpeError(rc, f"{n_ids.value} ids needed, capacity {cap}")
+        _capi.check(self._h, rc)
+        return ids_out[: n_ids.value], id_off[: n_docs + 1]
+
+
+def vocab_from_merges(merges):
+    """Token byte strings of ids 0 .. 255 + len(merges) (host bookkeeping for
+    trie_build): bytes(b) = [b], bytes(256 + k) = bytes(left) + bytes(right).
+    Returns (uint8 array, uint64 offsets)."""
+    m = np.asarray(merges, dtype=np.uint32).reshape(-1, 4)
+    toks = [bytes([b]) for b in range(256)]
+    for l, r in m[:, :2].tolist():
+        toks.append(toks[l] + toks[r])
+    off = np.zeros(len(toks) + 1, dtype=np.uint64)
+    off[1:] = np.cumsum([len(t) for t in toks])
+    return np.frombuffer(b"".join(toks), dtype=np.uint8), off

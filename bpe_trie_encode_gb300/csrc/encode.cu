@@ -1,0 +1,521 @@
+// encode.cu -- greedy longest-match encoding over the double-array trie
+// ([GPU-BPE] "What it does", 4. trie-based inference; the inference pipeline
+// trie_tokenizer_chunked -> trie_prefix_sum -> trie_tokenizer_compact).
+//
+// Every document is cut into chunks of C bytes; one thread parses one chunk.
+// The exact result is the sequential greedy parse of each document, so a
+// chunk must start where the previous chunk's last token ends, which is only
+// known after that chunk is parsed.  The kernels resolve this without a
+// sequential pass in the common case:
+//
+//   k_chunk_index   first chunk of every document (one CTA, exclusive scan)
+//   k_spec          each thread parses its chunk speculatively from the chunk's
+//                   first byte, remembering which positions start a token
+//                   (bitmap in shared memory) and where the parse leaves the
+//                   chunk (spec exit).  After a barrier each thread re-parses
+//                   its chunk from the previous chunk's spec exit (the nominal
+//                   entry) until that path meets a remembered token start --
+//                   from there both paths are the same.  It records the
+//                   chunk's token count and exit for the nominal entry, and
+//                   flags the chunk when that exit differs from its own spec
+//                   exit (the next chunk's nominal entry is then wrong).
+//                   The first chunk of a CTA gets its nominal entry from a halo
+//                   thread that parses the chunk before it.
+//   k_repair        only when some chunk was flagged (rare: the two parses of a
+//                   chunk never meet inside it): one thread walks the flagged
+//                   chains in order, re-parsing chunks from their true entries
+//                   until an exit agrees with the nominal entry again.
+//   k_emit          exclusive scan of the chunk counts (CTA scan + decoupled
+//                   look-back over tiles taken in ticket order) and a final
+//                   parse of every chunk from its true entry that writes ids at
+//                   their global offsets.
+//   k_doc_offsets   per-document id offsets.
+//
+// One trie step is: slot = base + byte, valid when check[slot] == node.  The
+// root's 256 children are in a shared-memory LUT ([GPU-BPE] "Line by line",
+// 3) root LUT), so the first byte of every token costs no global load.
+#include <algorithm>
+
+#include "device.cuh"
+#include "internal.h"
+#include "trie.h"
+
+namespace bpe {
+namespace {
+
+constexpr int kSpecThreads = 256;          // 255 owned chunks + 1 halo chunk per CTA
+constexpr int kEmitThreads = 256;
+constexpr int kMaxChunk = 1024;            // bytes per chunk (bitmap bound)
+constexpr unsigned kSpinLimit = 1u << 22;
+
+struct EncState {
+    unsigned long long n_chunks;
+    unsigned long long total;
+    uint32_t err;        // DERR_* bits
+    uint32_t any_flag;   // some chunk's exit disagreed with the next nominal entry
+    uint32_t ticket;
+    uint32_t bad_doc_off;
+    unsigned long long span;   // doc_off[n_docs] - doc_off[0]
+};
+
+struct EncParams {
+    const uint8_t *bytes;
+    const uint64_t *doc_off;
+    uint32_t n_docs;
+    uint32_t chunk;              // C
+    const unsigned long long *chunk_start;   // n_docs + 1
+    const int2 *slot;
+    const int32_t *tid;
+    const int4 *root;
+    uint32_t *count;             // per chunk: tokens starting in the chunk (true path)
+    uint32_t *exit_rel;          // per chunk: true exit - chunk start
+    uint32_t *spec_rel;          // per chunk: spec exit - chunk start
+    uint32_t *flag;              // bitmap of flagged chunks
+    unsigned long long *prefix;  // per chunk: global index of its first id
+    unsigned long long *status;  // look-back words per emit tile
+    int32_t *ids;
+    unsigned long long cap;
+    unsigned long long *id_off;
+    EncState *st;
+};
+
+// -------------------------------------------------------------- matching ---
+
+struct Match {
+    uint32_t len;
+    int32_t id;
+};
+
+// Longest token prefixing bytes[p, end) (p < end).
+__device__ __forceinline__ Match match_at(const EncParams &P, const int4 *lut, uint64_t p, uint64_t end) {
+    const int4 r = lut[__ldg(P.bytes + p)];
+    int32_t node = r.x;
+    uint32_t y = (uint32_t)r.y;
+    Match m{1u, r.z};
+    int32_t best_node = -1;
+    uint64_t q = p + 1;
+    while (q < end) {
+        const uint32_t base = y & ~kTermBit;
+        if (base == 0) break;                       // no children
+        const int32_t t = (int32_t)(base + __ldg(P.bytes + q));
+        const int2 v = __ldg(P.slot + t);
+        if (v.x != node) break;
+        node = t;
+        y = (uint32_t)v.y;
+        ++q;
+        if (y & kTermBit) {
+            m.len = (uint32_t)(q - p);
+            best_node = node;
+        }
+    }
+    if (best_node >= 0) m.id = __ldg(P.tid + best_node);
+    return m;
+}
+
+__device__ __forceinline__ void load_lut(const EncParams &P, int4 *lut) {
+    for (int c = threadIdx.x; c < 256; c += blockDim.x) lut[c] = P.root[c];
+}
+
+// document of a chunk: last d with chunk_start[d] <= k
+__device__ __forceinline__ uint32_t doc_of_chunk(const EncParams &P, unsigned long long k) {
+    uint32_t lo = 0, hi = P.n_docs;   // answer in [0, n_docs)
+    while (hi - lo > 1) {
+        const uint32_t mid = (lo + hi) >> 1;
+        if (P.chunk_start[mid] <= k) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+struct ChunkGeo {
+    uint64_t cs, ce, de;   // chunk start, chunk end, document end
+    bool doc_first;
+};
+
+__device__ __forceinline__ ChunkGeo chunk_geo(const EncParams &P, unsigned long long k) {
+    const uint32_t d = doc_of_chunk(P, k);
+    const uint64_t ds = P.doc_off[d], de = P.doc_off[d + 1];
+    const uint64_t j = k - P.chunk_start[d];
+    ChunkGeo g;
+    g.cs = ds + j * P.chunk;
+    g.ce = min(g.cs + P.chunk, de);
+    g.de = de;
+    g.doc_first = (j == 0);
+    return g;
+}
+
+// ---------------------------------------------------------- chunk index ---
+
+__global__ void __launch_bounds__(1024) k_chunk_index(EncParams P, unsigned long long *chunk_start) {
+    __shared__ unsigned long long s_w[32];
+    __shared__ unsigned long long s_carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s_carry = 0;
+    __syncthreads();
+    for (uint64_t base = 0; base < P.n_docs; base += 1024) {
+        const uint64_t d = base + tid;
+        unsigned long long v = 0;
+        if (d < P.n_docs) {
+            const uint64_t a = P.doc_off[d], b = P.doc_off[d + 1];
+            if (b < a) {
+                atomicOr(&P.st->err, DERR_OOB);
+                P.st->bad_doc_off = (uint32_t)d;
+            } else {
+                v = (b - a + P.chunk - 1) / P.chunk;
+            }
+        }
+        unsigned long long x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_w[warp] = x;
+        __syncthreads();
+        unsigned long long wpre = 0, tot = 0;
+        for (int w = 0; w < 32; w++) {
+            if (w < warp) wpre += s_w[w];
+            tot += s_w[w];
+        }
+        const unsigned long long carry = s_carry;
+        if (d < P.n_docs) chunk_start[d] = carry + wpre + x - v;
+        __syncthreads();
+        if (tid == 0) s_carry = carry + tot;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        chunk_start[P.n_docs] = s_carry;
+        P.st->n_chunks = s_carry;
+        P.st->span = P.doc_off[P.n_docs] - P.doc_off[0];
+    }
+}
+
+// ------------------------------------------------ speculative parse + fix ---
+
+__global__ void __launch_bounds__(kSpecThreads) k_spec(EncParams P, unsigned long long n_chunks) {
+    extern __shared__ uint32_t s_bits[];   // kSpecThreads x (C/32) token-start bitmaps
+    __shared__ int4 lut[256];
+    __shared__ unsigned long long s_exit[kSpecThreads];
+    load_lut(P, lut);
+    __syncthreads();
+    const int tid = threadIdx.x;
+    const uint32_t words = P.chunk >> 5;
+    uint32_t *bits = s_bits + tid * words;
+    const long long k = (long long)blockIdx.x * (kSpecThreads - 1) + tid - 1;
+    const bool live = k >= 0 && (unsigned long long)k < n_chunks;
+
+    ChunkGeo g{0, 0, 0, true};
+    uint32_t spec_count = 0;
+    uint64_t spec_exit = 0;
+    if (live) {
+        g = chunk_geo(P, (unsigned long long)k);
+        for (uint32_t w = 0; w < words; w++) bits[w] = 0;
+        uint64_t p = g.cs;
+        while (p < g.ce) {
+            const uint32_t o = (uint32_t)(p - g.cs);
+            bits[o >> 5] |= 1u << (o & 31);
+            p += match_at(P, lut, p, g.de).len;
+            ++spec_count;
+        }
+        spec_exit = p;
+    }
+    s_exit[tid] = spec_exit;
+    __syncthreads();
+    if (!live || tid == 0) return;   // the halo thread only supplied its exit
+
+    uint32_t count;
+    uint64_t exit;
+    if (g.doc_first) {
+        count = spec_count;
+        exit = spec_exit;
+    } else {
+        uint64_t q = s_exit[tid - 1];        // nominal entry: previous chunk's spec exit
+        uint32_t c = 0;
+        exit = q;
+        for (;;) {
+            if (q >= g.ce) {
+                exit = q;
+                break;
+            }
+            const uint32_t o = (uint32_t)(q - g.cs);
+            if ((bits[o >> 5] >> (o & 31)) & 1u) {
+                // the paths meet at q: the rest of the chunk is the spec path
+                uint32_t rest = __popc(bits[o >> 5] >> (o & 31));
+                for (uint32_t w = (o >> 5) + 1; w < words; w++) rest += __popc(bits[w]);
+                c += rest;
+                exit = spec_exit;
+                break;
+            }
+            q += match_at(P, lut, q, g.de).len;
+            ++c;
+        }
+        count = c;
+    }
+    P.count[k] = count;
+    P.exit_rel[k] = (uint32_t)(exit - g.cs);
+    P.spec_rel[k] = (uint32_t)(spec_exit - g.cs);
+    if (exit != spec_exit) {
+        atomicOr(P.flag + (k >> 5), 1u << (k & 31));
+        P.st->any_flag = 1u;
+    }
+}
+
+// ---------------------------------------------------------------- repair ---
+
+// Parse [e, ce) of a chunk fully; returns the count and sets *exit.
+__device__ uint32_t parse_from(const EncParams &P, const int4 *lut, uint64_t e, uint64_t ce, uint64_t de,
+                               uint64_t *exit) {
+    uint32_t c = 0;
+    while (e < ce) {
+        e += match_at(P, lut, e, de).len;
+        ++c;
+    }
+    *exit = e;
+    return c;
+}
+
+__global__ void k_repair(EncParams P, unsigned long long n_chunks) {
+    __shared__ int4 lut[256];
+    if (!P.st->any_flag) return;
+    load_lut(P, lut);
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    unsigned long long k = 0;
+    for (;;) {
+        // next flagged chunk at or after k
+        unsigned long long w = k >> 5;
+        const unsigned long long nw = (n_chunks + 31) >> 5;
+        uint32_t bitsw = w < nw ? (P.flag[w] & (~0u << (k & 31))) : 0u;
+        while (w < nw && bitsw == 0) {
+            ++w;
+            if (w < nw) bitsw = P.flag[w];
+        }
+        if (w >= nw) break;
+        const unsigned long long f = (w << 5) + (unsigned long long)(__ffs(bitsw) - 1);
+        if (f >= n_chunks) break;
+        // chunk f has a true entry; its exit (true) disagrees with the next nominal entry
+        ChunkGeo gf = chunk_geo(P, f);
+        uint64_t e = gf.cs + P.exit_rel[f];
+        unsigned long long c = f + 1;
+        for (; c < n_chunks; c++) {
+            const ChunkGeo g = chunk_geo(P, c);
+            if (g.doc_first) break;           // next document: entry resets, chunk c is fine
+            uint64_t x;
+            P.count[c] = parse_from(P, lut, e, g.ce, g.de, &x);
+            P.exit_rel[c] = (uint32_t)(x - g.cs);
+            if (x == g.cs + P.spec_rel[c]) {  // agrees with the next nominal entry again
+                ++c;
+                break;
+            }
+            e = x;
+        }
+        k = c;   // chunks before c are settled; c itself keeps its own flag
+    }
+}
+
+// ------------------------------------------------------------ scan + emit ---
+
+__global__ void __launch_bounds__(kEmitThreads) k_emit(EncParams P, unsigned long long n_chunks) {
+    __shared__ int4 lut[256];
+    __shared__ uint32_t s_w[kEmitThreads / 32];
+    __shared__ unsigned long long s_tile, s_off;
+    load_lut(P, lut);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned long long ntiles = (n_chunks + kEmitThreads - 1) / kEmitThreads;
+    for (;;) {
+        if (tid == 0) s_tile = atomicAdd(&P.st->ticket, 1u);
+        __syncthreads();
+        const unsigned long long t = s_tile;
+        if (t >= ntiles) break;
+        const unsigned long long k = t * kEmitThreads + tid;
+        const uint32_t cnt = k < n_chunks ? P.count[k] : 0u;
+        const uint32_t incl = warp_incl_sum(cnt, lane);
+        if (lane == 31) s_w[warp] = incl;
+        __syncthreads();
+        uint32_t wpre = 0, tsum = 0;
+        for (int w = 0; w < kEmitThreads / 32; w++) {
+            if (w < warp) wpre += s_w[w];
+            tsum += s_w[w];
+        }
+        if (tid == 0) {
+            unsigned long long off = 0;
+            if (t > 0) {
+                st_relaxed(P.status + t, 1ull | ((unsigned long long)tsum << 2));
+                long long j = (long long)t - 1;
+                unsigned spins = 0;
+                for (;;) {
+                    const unsigned long long w = ld_relaxed(P.status + j);
+                    const uint32_t fl = (uint32_t)(w & 3ull);
+                    if (fl == 0) {
+                        if (++spins > kSpinLimit) {
+                            atomicOr(&P.st->err, DERR_TIMEOUT);
+                            break;
+                        }
+                        if (spins > 64) __nanosleep(64);
+                        continue;
+                    }
+                    off += w >> 2;
+                    if (fl == 2) break;
+                    --j;
+                }
+            }
+            st_relaxed(P.status + t, 2ull | ((off + tsum) << 2));
+            if (t == ntiles - 1) P.st->total = off + tsum;
+            s_off = off;
+        }
+        __syncthreads();
+        if (k < n_chunks) {
+            unsigned long long o = s_off + wpre + incl - cnt;
+            P.prefix[k] = o;
+            const ChunkGeo g = chunk_geo(P, k);
+            uint64_t e = g.doc_first ? g.cs : (g.cs - P.chunk) + P.exit_rel[k - 1];
+            while (e < g.ce) {
+                const Match m = match_at(P, lut, e, g.de);
+                if (o < P.cap) P.ids[o] = m.id;
+                ++o;
+                e += m.len;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+__global__ void k_doc_offsets(EncParams P, unsigned long long n_chunks) {
+    const uint64_t d = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
+    if (d > P.n_docs) return;
+    const unsigned long long c = P.chunk_start[d];
+    P.id_off[d] = c < n_chunks ? P.prefix[c] : P.st->total;
+}
+
+}  // namespace
+}  // namespace bpe
+
+using namespace bpe;
+
+extern "C" int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_bytes, const uint64_t *d_doc_off,
+                           uint32_t n_docs, int32_t *d_ids_out, uint64_t ids_capacity, uint64_t *d_id_off_out,
+                           uint64_t *n_ids) {
+    if (!ctx) return BPE_ERR_INVALID_ARG;
+    if (!trie || !n_ids) return fail(ctx, BPE_ERR_INVALID_ARG, "trie_encode: null trie or n_ids");
+    if (trie->device != ctx->device) return fail(ctx, BPE_ERR_INVALID_ARG, "trie_encode: trie on another device");
+    if (n_docs && (!d_doc_off || !d_bytes)) return fail(ctx, BPE_ERR_INVALID_ARG, "trie_encode: null input");
+    if (ids_capacity && !d_ids_out) return fail(ctx, BPE_ERR_INVALID_ARG, "trie_encode: null ids with capacity");
+    BPE_CUDA(ctx, cudaSetDevice(ctx->device), "cudaSetDevice");
+    cudaStream_t s = ctx->stream;
+    stats_reset(ctx);
+    *n_ids = 0;
+    if (n_docs == 0) {
+        if (d_id_off_out) BPE_CUDA(ctx, cudaMemsetAsync(d_id_off_out, 0, 8, s), "id_off");
+        BPE_CUDA(ctx, cudaStreamSynchronize(s), "sync");
+        return BPE_OK;
+    }
+    const uint32_t C = (uint32_t)std::min(ctx->chunk, kMaxChunk);
+    int rc;
+    void *cstart, *state, *pin;
+    if ((rc = ensure(ctx, S_ENC_CHUNK_START, ((uint64_t)n_docs + 1) * 8, &cstart)) ||
+        (rc = ensure(ctx, S_ENC_STATE, sizeof(EncState), &state)) ||
+        (rc = ensure_pinned(ctx, sizeof(EncState), &pin)))
+        return rc;
+    EncState *h = (EncState *)pin;
+    const bool profile = ctx->profile != 0;
+    if (profile && (rc = ensure_events(ctx, 6))) return rc;
+
+    EncParams P{};
+    P.bytes = d_bytes;
+    P.doc_off = d_doc_off;
+    P.n_docs = n_docs;
+    P.chunk = C;
+    P.chunk_start = (const unsigned long long *)cstart;
+    P.slot = trie->d_slot;
+    P.tid = trie->d_tid;
+    P.root = trie->d_root;
+    P.ids = d_ids_out;
+    P.cap = ids_capacity;
+    P.st = (EncState *)state;
+
+    // phase 1: chunk index (needs the chunk count on the host to size the rest)
+    BPE_CUDA(ctx, cudaStreamSynchronize(s), "sync");
+    BPE_CUDA(ctx, cudaMemsetAsync(state, 0, sizeof(EncState), s), "state clear");
+    if (profile) cudaEventRecord(ctx->events[0], s);
+    k_chunk_index<<<1, 1024, 0, s>>>(P, (unsigned long long *)cstart);
+    if (profile) cudaEventRecord(ctx->events[1], s);
+    BPE_CUDA(ctx, cudaGetLastError(), "k_chunk_index launch");
+    BPE_CUDA(ctx, cudaMemcpyAsync(h, state, sizeof(EncState), cudaMemcpyDeviceToHost, s), "state read");
+    BPE_CUDA(ctx, cudaStreamSynchronize(s), "chunk index sync");
+    if (h->err & DERR_OOB)
+        return fail(ctx, BPE_ERR_INVALID_ARG, "trie_encode: document offsets descend at document %u", h->bad_doc_off);
+    const unsigned long long nc = h->n_chunks;
+    if (nc == 0) {
+        if (d_id_off_out) BPE_CUDA(ctx, cudaMemsetAsync(d_id_off_out, 0, ((uint64_t)n_docs + 1) * 8, s), "id_off");
+        BPE_CUDA(ctx, cudaStreamSynchronize(s), "sync");
+        return BPE_OK;
+    }
+
+    void *info, *flag, *status, *prefix, *idoff_tmp = nullptr;
+    const unsigned long long spec_blocks = (nc + kSpecThreads - 2) / (kSpecThreads - 1);
+    const unsigned long long emit_tiles = (nc + kEmitThreads - 1) / kEmitThreads;
+    if ((rc = ensure(ctx, S_ENC_CHUNK_INFO, nc * 12, &info)) ||
+        (rc = ensure(ctx, S_ENC_NOTOK, ((nc + 31) / 32) * 4, &flag)) ||
+        (rc = ensure(ctx, S_ENC_STATUS, emit_tiles * 8, &status)) ||
+        (rc = ensure(ctx, S_ENC_PREFIX, nc * 8 + ((uint64_t)n_docs + 1) * 8, &prefix)))
+        return rc;
+    P.chunk_start = (const unsigned long long *)cstart;   // (ensure may not move it: distinct slot)
+    P.count = (uint32_t *)info;
+    P.exit_rel = P.count + nc;
+    P.spec_rel = P.exit_rel + nc;
+    P.flag = (uint32_t *)flag;
+    P.status = (unsigned long long *)status;
+    P.prefix = (unsigned long long *)prefix;
+    idoff_tmp = (unsigned long long *)prefix + nc;
+    P.id_off = d_id_off_out ? (unsigned long long *)d_id_off_out : (unsigned long long *)idoff_tmp;
+
+    BPE_CUDA(ctx, cudaMemsetAsync(flag, 0, ((nc + 31) / 32) * 4, s), "flag clear");
+    BPE_CUDA(ctx, cudaMemsetAsync(status, 0, emit_tiles * 8, s), "status clear");
+    const size_t spec_smem = (size_t)kSpecThreads * (C / 32) * 4;
+    BPE_CUDA(ctx, cudaFuncSetAttribute(k_spec, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)spec_smem),
+             "k_spec smem");
+    int eb = 1;
+    BPE_CUDA(ctx, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&eb, k_emit, kEmitThreads, 0), "occupancy");
+    const unsigned long long emit_grid = std::min<unsigned long long>(emit_tiles, (unsigned long long)ctx->sm_count * std::max(eb, 1));
+
+    if (profile) cudaEventRecord(ctx->events[2], s);
+    k_spec<<<(unsigned)spec_blocks, kSpecThreads, spec_smem, s>>>(P, nc);
+    if (profile) cudaEventRecord(ctx->events[3], s);
+    k_repair<<<1, 256, 0, s>>>(P, nc);
+    if (profile) cudaEventRecord(ctx->events[4], s);
+    k_emit<<<(unsigned)emit_grid, kEmitThreads, 0, s>>>(P, nc);
+    if (profile) cudaEventRecord(ctx->events[5], s);
+    k_doc_offsets<<<(unsigned)((n_docs + 1 + 255) / 256), 256, 0, s>>>(P, nc);
+    BPE_CUDA(ctx, cudaGetLastError(), "trie_encode launch");
+    BPE_CUDA(ctx, cudaMemcpyAsync(h, state, sizeof(EncState), cudaMemcpyDeviceToHost, s), "state read");
+    BPE_CUDA(ctx, cudaStreamSynchronize(s), "trie_encode sync");
+    if (h->err & DERR_TIMEOUT) return fail(ctx, BPE_ERR_TIMEOUT, "trie_encode: look-back wait gave up");
+
+    const uint64_t total = h->total;
+    *n_ids = total;
+
+    // statistics: the spec parse and the emit pass each read the input once;
+    // emit writes 4 bytes per id
+    const int a = stats_slot(ctx, "encode_spec"), b = stats_slot(ctx, "encode_emit");
+    ctx->stats.k[a].launches = 1;
+    ctx->stats.k[b].launches = 1;
+    const uint64_t in_bytes = h->span;
+    ctx->stats.kernel_launches = 5;
+    ctx->stats.k[a].bytes = (double)in_bytes;
+    ctx->stats.k[b].bytes = (double)in_bytes + 4.0 * (double)total;
+    if (profile) {
+        float x = 0, y = 0, z = 0;
+        cudaEventElapsedTime(&x, ctx->events[2], ctx->events[3]);
+        cudaEventElapsedTime(&y, ctx->events[4], ctx->events[5]);
+        cudaEventElapsedTime(&z, ctx->events[3], ctx->events[4]);
+        ctx->stats.k[a].ms = x;
+        ctx->stats.k[b].ms = y;
+        const int c = stats_slot(ctx, "encode_repair");
+        ctx->stats.k[c].launches = 1;
+        ctx->stats.k[c].ms = z;
+        cudaGetLastError();
+    }
+    if (total > ids_capacity)
+        return fail(ctx, BPE_ERR_CAPACITY, "trie_encode: %llu ids exceed the capacity %llu",
+                    (unsigned long long)total, (unsigned long long)ids_capacity);
+    return BPE_OK;
+}

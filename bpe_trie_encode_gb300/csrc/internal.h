@@ -1,0 +1,90 @@
+// internal.h -- context, scratch pool and error plumbing shared by the
+// translation units of libbpetrie.so.  Host-side only (no device code).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <string>
+#include <vector>
+
+#include "bpetrie.h"
+
+namespace bpe {
+
+// Named scratch slots of the context's pool.
+enum Slot {
+    S_TRAIN_BUF0, S_TRAIN_BUF1, S_TABLE_KEY, S_TABLE_CNT, S_LIST0, S_LIST1,
+    S_STATUS0, S_STATUS1, S_BEST, S_STATE, S_NHIST,
+    S_ENC_CHUNK_START, S_ENC_CHUNK_INFO, S_ENC_NOTOK, S_ENC_STATUS, S_ENC_PREFIX, S_ENC_STATE,
+    S_NUM
+};
+
+struct Scratch {
+    void *p = nullptr;
+    size_t cap = 0;
+};
+
+struct TrainGraph {
+    cudaGraphExec_t exec = nullptr;
+    // what the capture baked in; a mismatch forces a new capture
+    std::vector<uintptr_t> key;
+};
+
+struct bpe_ctx_impl;
+
+}  // namespace bpe
+
+struct bpe_ctx {
+    int device = 0;
+    cudaStream_t stream = nullptr;
+    cudaStream_t capture_stream = nullptr;  // private stream used only to capture graphs
+    int sm_count = 0;
+    std::string err;
+    bpe::Scratch scratch[bpe::S_NUM];
+    void *pinned = nullptr;                 // small pinned host staging area
+    size_t pinned_cap = 0;
+    // options
+    int table_log2 = 0;
+    int use_graph = 1;
+    int profile = 0;
+    int chunk = 128;
+    // cached graph of merge iterations
+    bpe::TrainGraph graph;
+    // profiling events (grown on demand)
+    std::vector<cudaEvent_t> events;
+    bpe_stats stats{};
+    uint64_t pretok_launches = 0;   // running count of pre-tokenize launches
+};
+
+namespace bpe {
+
+// Set ctx->err from a printf-style message and return `code`.
+int fail(bpe_ctx *ctx, int code, const char *fmt, ...);
+
+// Map a CUDA error to BPE_ERR_CUDA (or OOM) with context.
+int cuda_fail(bpe_ctx *ctx, cudaError_t e, const char *what);
+
+// Make scratch slot `s` at least `bytes` large (growth x1.5, contents are
+// not preserved).  Waits for the context stream before freeing old storage.
+int ensure(bpe_ctx *ctx, Slot s, size_t bytes, void **out);
+
+// Pinned host staging of at least `bytes`.
+int ensure_pinned(bpe_ctx *ctx, size_t bytes, void **out);
+
+// Make sure ctx->events holds at least n timing events.
+int ensure_events(bpe_ctx *ctx, size_t n);
+
+// Stats helpers.
+void stats_reset(bpe_ctx *ctx);
+int stats_slot(bpe_ctx *ctx, const char *name);
+
+}  // namespace bpe
+
+#define BPE_CUDA(ctx, call, what)                                  \
+    do {                                                           \
+        cudaError_t e__ = (call);                                  \
+        if (e__ != cudaSuccess) return bpe::cuda_fail(ctx, e__, what); \
+    } while (0)

@@ -1,0 +1,188 @@
+/*
+ * bpetrie.h -- byte-level BPE training and greedy trie encoding on one GPU.
+ *
+ * C ABI of libbpetrie.so (sm_103a).  Plain pointers and sizes only.
+ *
+ * Sources (web pages; section names as printed there):
+ *   [GPU-BPE]  "bpe -- GPU BPE Tokenizer Pipeline" (llm.istanbul, learn/tr/13_bpe)
+ *   [UNIGRAM]  "Improving Unigram tokenizer CPU performance" (perplexity.ai hub)
+ *
+ * Conventions for every call
+ *   - d_ pointers are device pointers on the context's device; h_ pointers are
+ *     host pointers.  The caller owns every input and output buffer; the
+ *     library owns the context, its scratch pool and tries.
+ *   - Work is ordered on the context's stream.  A call returns only after its
+ *     work is complete when it returns a host-side result (n_done, n_ids...);
+ *     bpe_pretokenize returns as soon as its kernel is queued.
+ *   - Return value: BPE_OK (0) or a negative BPE_ERR_* code; the message of
+ *     the last failure is available from bpe_last_error().  On failure no
+ *     output beyond what the code describes is meaningful.
+ *   - Symbols are uint32: bits 0-15 a token id, bit 16 BPE_WORD_START
+ *     ([GPU-BPE] "What it does", 1. GPU pre-tokenization), bits 17-31 zero.
+ */
+#ifndef BPETRIE_H
+#define BPETRIE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BPE_WORD_START 0x10000u
+#define BPE_MAX_MERGES 65280u          /* ids 256 .. 65535 fit in 16 bits */
+#define BPE_MAX_TRAIN_SYMBOLS (1ull << 30)
+
+enum {
+    BPE_OK = 0,
+    BPE_ERR_INVALID_ARG = -1,  /* null pointer, bad size, malformed vocabulary */
+    BPE_ERR_OOM = -2,          /* device or host allocation failed */
+    BPE_ERR_CUDA = -3,         /* a CUDA runtime call failed */
+    BPE_ERR_TABLE_FULL = -4,   /* the global pair table overflowed (raise BPE_OPT_TABLE_LOG2) */
+    BPE_ERR_ID_OVERFLOW = -5,  /* n_merges > BPE_MAX_MERGES */
+    BPE_ERR_CAPACITY = -6,     /* output buffer too small; required size reported */
+    BPE_ERR_TIMEOUT = -7,      /* a bounded device-side wait gave up */
+    BPE_ERR_CHECKED_OOB = -8   /* a device bounds check failed (internal error) */
+};
+
+typedef struct bpe_ctx bpe_ctx;
+typedef struct bpe_trie bpe_trie;
+
+/* One learned merge: the pair (left, right) becomes new_id = 256 + k; count
+ * is the pair's number of occurrences when it was chosen.  Ids carry no
+ * WORD_START bit. */
+typedef struct {
+    uint32_t left, right, new_id, count;
+} bpe_merge;
+
+/* ------------------------------------------------------------- context --- */
+
+/* Create a context on `device` that orders its work on `cuda_stream` (a
+ * cudaStream_t; NULL means the legacy default stream).  The context keeps a
+ * persistent scratch pool that grows by 1.5x when a call needs more
+ * ([GPU-BPE] "Host architecture", 2. persistent buffer pool).
+ * Errors: INVALID_ARG (out NULL, bad device), CUDA. */
+int bpe_ctx_create(bpe_ctx **out, int device, void *cuda_stream);
+
+/* Change the stream later calls are ordered on. */
+int bpe_ctx_set_stream(bpe_ctx *ctx, void *cuda_stream);
+
+/* Release the context and its scratch (waits for its stream first). */
+void bpe_ctx_destroy(bpe_ctx *ctx);
+
+/* Message of the last failed call on this context ("" if none).  The string
+ * lives until the next call on the context. */
+const char *bpe_last_error(const bpe_ctx *ctx);
+
+/* Tuning and measurement options (bpe_ctx_set_option):
+ *   BPE_OPT_TABLE_LOG2   log2 of the global pair-table slots (12..28;
+ *                        0 = automatic from the stream length)
+ *   BPE_OPT_GRAPH        1 = replay merge iterations from CUDA graphs
+ *                        (default), 0 = launch every kernel from the host
+ *   BPE_OPT_PROFILE      1 = record a CUDA event after every kernel of
+ *                        bpe_train / trie_encode so bpe_last_stats() reports
+ *                        per-kernel device time (implies host launches)
+ *   BPE_OPT_CHUNK        trie_encode bytes per chunk (64..4096, multiple
+ *                        of 32; default 128) */
+enum { BPE_OPT_TABLE_LOG2 = 1, BPE_OPT_GRAPH = 2, BPE_OPT_PROFILE = 3, BPE_OPT_CHUNK = 4 };
+int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value);
+
+/* Statistics of the last bpe_train or trie_encode call on this context.
+ * Per kernel family: launches, algorithmic DRAM bytes (the bytes the method
+ * must move: 4 per symbol read or written, input bytes, 4 per id written)
+ * and, with BPE_OPT_PROFILE, summed device milliseconds between the events
+ * bracketing each launch (0 otherwise). */
+typedef struct {
+    char name[32];
+    uint64_t launches;
+    double bytes;
+    double ms;
+} bpe_kernel_stat;
+enum { BPE_MAX_STATS = 8 };
+typedef struct {
+    int n;
+    uint64_t kernel_launches;   /* every kernel launch of the call, graph nodes included */
+    bpe_kernel_stat k[BPE_MAX_STATS];
+} bpe_stats;
+int bpe_last_stats(const bpe_ctx *ctx, bpe_stats *out);
+
+/* -------------------------------------------------------- pre-tokenize --- */
+
+/* [GPU-BPE] "What it does", 1. GPU pre-tokenization, and "Line by line",
+ * 1) bpe_word_boundary.  symbols[i] = bytes[i] | WORD_START when i == 0 or
+ * class(bytes[i]) != class(bytes[i-1]); classes: Newline 0x0A, Space 0x20,
+ * Digit '0'-'9', Letter a-z A-Z and every byte >= 0x80, Punct otherwise.
+ * d_bytes: n bytes; d_symbols_out: n uint32 (may not alias d_bytes).
+ * n == 0 is a no-op.  Asynchronous.  Errors: INVALID_ARG, CUDA. */
+int bpe_pretokenize(bpe_ctx *ctx, const uint8_t *d_bytes, uint64_t n, uint32_t *d_symbols_out);
+
+/* --------------------------------------------------------------- train --- */
+
+/* The BPE merge loop ([GPU-BPE] "What is this?" and "What it does" 2.-3.;
+ * the 9-dispatch training pipeline).  For k = 0 .. n_merges-1: count every
+ * adjacent pair (i, i+1) whose right symbol has no WORD_START (overlapping
+ * occurrences all count), choose the highest count (ties: lowest left id,
+ * then lowest right id), stop if that count is 0, otherwise replace the
+ * pair's occurrences left to right, non-overlapping, by 256 + k keeping the
+ * left symbol's WORD_START bit, and compact the stream.
+ *
+ * d_symbols: n input symbols (read only; n < BPE_MAX_TRAIN_SYMBOLS).
+ * h_merges_out: host array with room for n_merges entries; the first
+ *   *n_done are written.
+ * d_symbols_final (nullable): device array with room for n symbols; receives
+ *   the stream after *n_done merges, *n_final (nullable) its length.
+ * Blocks until done.  Errors: INVALID_ARG, ID_OVERFLOW (n_merges >
+ * BPE_MAX_MERGES), OOM, TABLE_FULL, TIMEOUT, CUDA. */
+int bpe_train(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_merges,
+              bpe_merge *h_merges_out, uint32_t *n_done,
+              uint32_t *d_symbols_final, uint64_t *n_final);
+
+/* ---------------------------------------------------------------- trie --- */
+
+/* Build a flattened double-array trie ([UNIGRAM], the double-array passage:
+ * child = base[node] + byte, valid when check[child] == node; token id kept
+ * in the node) over a vocabulary, and upload it to the context's device.
+ * Token t is the byte string h_vocab_bytes[h_vocab_off[t] .. h_vocab_off[t+1]);
+ * the id of a token is its index.  Every single byte 0..255 must be a token
+ * (byte-level vocabularies always are; greedy matching then never fails);
+ * when two tokens have the same bytes the lower id is kept.  Empty strings
+ * are ignored.  The trie is usable with any context on the same device.
+ * Errors: INVALID_ARG (missing single byte, offsets not ascending), OOM, CUDA. */
+int trie_build(bpe_ctx *ctx, const uint8_t *h_vocab_bytes, const uint64_t *h_vocab_off,
+               uint32_t n_tok, bpe_trie **out);
+
+/* Host-only: the double-array layout trie_build would upload, written to
+ * caller arrays of `capacity` entries (check = parent slot, -1 free, -2 root;
+ * base = child offset | 0x80000000 when the slot is a token; tid = token id
+ * or -1).  *n_slots receives the layout size; BPE_ERR_CAPACITY when it
+ * exceeds capacity (call with capacity 0 to size the arrays).  Needs no GPU.
+ * Errors: INVALID_ARG (as trie_build), CAPACITY. */
+int trie_layout(const uint8_t *h_vocab_bytes, const uint64_t *h_vocab_off, uint32_t n_tok,
+                int32_t *check_out, int32_t *base_out, int32_t *tid_out, uint64_t capacity,
+                uint64_t *n_slots);
+
+/* Sizes of a built trie (any pointer may be NULL). */
+int trie_info(const bpe_trie *trie, uint64_t *n_nodes, uint64_t *n_slots, uint32_t *max_token_len);
+
+void trie_free(bpe_trie *trie);
+
+/* Greedy longest-match encoding ([GPU-BPE] "What it does", 4. trie-based
+ * inference, and the 3-dispatch inference pipeline).  Each document
+ * d_bytes[d_doc_off[d] .. d_doc_off[d+1]) is encoded independently from its
+ * first byte: at position p the id of the longest token that prefixes the
+ * rest of the document is emitted and p advances by its length.
+ *
+ * d_doc_off: n_docs+1 ascending uint64 (device); d_ids_out: ids_capacity
+ * int32; d_id_off_out (nullable): n_docs+1 uint64, d_id_off_out[d] = index
+ * of document d's first id, [n_docs] = total.  *n_ids (host) receives the
+ * total.  When the total exceeds ids_capacity no id beyond the capacity is
+ * written, *n_ids holds the required size and BPE_ERR_CAPACITY is returned.
+ * Blocks until done.  Errors: INVALID_ARG, CAPACITY, OOM, TIMEOUT, CUDA. */
+int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_bytes,
+                const uint64_t *d_doc_off, uint32_t n_docs, int32_t *d_ids_out,
+                uint64_t ids_capacity, uint64_t *d_id_off_out, uint64_t *n_ids);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BPETRIE_H */

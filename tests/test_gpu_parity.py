@@ -1,0 +1,344 @@
+"""GPU parity: the CUDA path against the CPU oracle, bit for bit.
+
+Small cases are compared element by element with the oracle run live; the
+five workloads are compared with the oracle's recorded results
+(tests/golden/workloads.json, written by tests/golden/make_golden.py), by
+SHA-256 of the full outputs.  All calls go through the C ABI.
+"""
+import hashlib
+import json
+import os
+import random
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+import synth  # noqa: E402
+
+WS = 0x10000
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def sha(a) -> str:
+    return hashlib.sha256(np.ascontiguousarray(a).tobytes()).hexdigest()
+
+
+@pytest.fixture(scope="module")
+def golden():
+    with open(os.path.join(GOLDEN, "workloads.json")) as f:
+        return json.load(f)
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    import bpe_trie_encode_gb300 as bt
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    c = bt.Context(0)
+    yield c
+    c.close()
+
+
+def dev_u8(a) -> "torch.Tensor":
+    a = np.frombuffer(a, dtype=np.uint8) if isinstance(a, (bytes, bytearray)) else a
+    return torch.from_numpy(np.ascontiguousarray(a).copy()).cuda()
+
+
+def dev_sym(a) -> "torch.Tensor":
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint32).view(np.int32).copy()).cuda()
+
+
+def host_u32(t) -> np.ndarray:
+    return t.cpu().numpy().view(np.uint32)
+
+
+def rand_bytes(rng, n, alphabet):
+    return bytes(rng.choice(alphabet) for _ in range(n))
+
+
+# ------------------------------------------------------------- pretokenize --
+@pytest.mark.parametrize("n", [0, 1, 2, 15, 16, 17, 31, 33, 1000, (1 << 20) + 7])
+def test_pretokenize_sizes(ctx, n):
+    rng = np.random.default_rng(n)
+    data = rng.integers(0, 256, n, dtype=np.uint8)
+    data[rng.random(n) < 0.3] = ord("a")   # runs of one class
+    got = host_u32(ctx.pretokenize(dev_u8(data)))
+    assert np.array_equal(got, oracle.pretokenize(data))
+
+
+def test_pretokenize_unaligned_and_all_bytes(ctx):
+    data = np.arange(256 * 40, dtype=np.uint32).astype(np.uint8)
+    d = dev_u8(np.concatenate([[7], data]))
+    got = host_u32(ctx.pretokenize(d[1:]))            # 1-byte offset: scalar path
+    assert np.array_equal(got, oracle.pretokenize(data))
+
+
+def test_pretokenize_corpus(ctx, golden):
+    text = synth.corpus("med")
+    assert sha(text) == golden["med"]["corpus_sha256"], "generator output differs on this machine"
+    got = host_u32(ctx.pretokenize(dev_u8(text)))
+    assert sha(got) == golden["med"]["symbols_sha256"]
+
+
+# ------------------------------------------------------------------- train --
+def check_train(ctx, sym, n_merges, **kw):
+    m, f = ctx.train(dev_sym(sym), n_merges)
+    wm, wf = oracle.train_stream(sym, n_merges)
+    assert np.array_equal(m, wm), (m[:5], wm[:5])
+    assert np.array_equal(host_u32(f), wf)
+    return m
+
+
+def test_train_worked_examples(ctx):
+    with open(os.path.join(GOLDEN, "worked_examples.json")) as f:
+        ex = json.load(f)
+    for e in ex["train"]:
+        sym = oracle.pretokenize(e["text"].encode())
+        m, fin = ctx.train(dev_sym(sym), e["n_merges"])
+        assert m.tolist() == e["merges"], e["name"]
+        assert [[x & 0xFFFF, x >> 16] for x in host_u32(fin).tolist()] == e["final"], e["name"]
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_train_random_small(ctx, seed):
+    rng = random.Random(seed)
+    alphabets = [b"ab", b"aab ", b"abc a.\n1", b"a", b"ab1 ", bytes(range(97, 123)) + b" ."]
+    n = rng.choice([2, 3, 5, 100, 2047, 2048, 2049, 4096 + 3, 9000])
+    text = rand_bytes(rng, n, alphabets[seed % len(alphabets)])
+    check_train(ctx, oracle.pretokenize(text), 60)
+
+
+@pytest.mark.parametrize("n", [2048 * 3 - 1, 2048 * 3, 2048 * 3 + 1, 1_000_001])
+def test_train_identical_runs_cross_tiles(ctx, n):
+    # one run of identical letters spans many 2048-symbol tiles: leftmost-first
+    # pairing must carry its parity across every tile boundary
+    text = b"a" * n + b" " + b"a" * (n // 3) + b".bb" + b"b" * 4097
+    check_train(ctx, oracle.pretokenize(text), 12)
+
+
+def test_train_alternating_and_ties(ctx):
+    check_train(ctx, oracle.pretokenize(b"ab" * 50000 + b" " + b"ba" * 777), 20)
+    check_train(ctx, oracle.pretokenize(b"ab cd ef gh ba dc fe hg"), 10)
+
+
+def test_train_degenerate(ctx):
+    m, f = ctx.train(dev_sym(oracle.pretokenize(b"a")), 5)
+    assert m.shape == (0, 4) and host_u32(f).tolist() == [97 | WS]
+    m, f = ctx.train(dev_sym(oracle.pretokenize(b"abc")), 0)
+    assert m.shape == (0, 4) and host_u32(f).size == 3
+    m, f = ctx.train(dev_sym(oracle.pretokenize(b"a1 .\n")), 5)   # no countable pair
+    assert m.shape == (0, 4)
+
+
+def test_train_rejects_too_many_merges(ctx):
+    import bpe_trie_encode_gb300 as bt
+    with pytest.raises(bt.BpeError) as e:
+        ctx.train(dev_sym(oracle.pretokenize(b"abc")), 65281)
+    assert e.value.name == "ID_OVERFLOW"
+
+
+def test_train_table_full_is_reported(ctx):
+    import bpe_trie_encode_gb300 as bt
+    rng = np.random.default_rng(5)
+    data = rng.integers(97, 123, 200000, dtype=np.uint8)   # ~676 distinct pairs ... grows
+    sym = oracle.pretokenize(data)
+    ctx.set_option(bt.BPE_OPT_TABLE_LOG2, 12)
+    try:
+        with pytest.raises(bt.BpeError) as e:
+            ctx.train(dev_sym(sym), 400)
+        assert e.value.name == "TABLE_FULL"
+    finally:
+        ctx.set_option(bt.BPE_OPT_TABLE_LOG2, 0)
+    check_train(ctx, sym[:5000], 30)   # the context is still usable
+
+
+@pytest.mark.parametrize("mode", ["graph", "eager", "profile"])
+def test_train_launch_modes_agree(ctx, golden, mode):
+    import bpe_trie_encode_gb300 as bt
+    sym = oracle.pretokenize(synth.corpus("tiny"))
+    ctx.set_option(bt.BPE_OPT_GRAPH, 1 if mode == "graph" else 0)
+    ctx.set_option(bt.BPE_OPT_PROFILE, 1 if mode == "profile" else 0)
+    try:
+        m, f = ctx.train(dev_sym(sym), 256)
+    finally:
+        ctx.set_option(bt.BPE_OPT_GRAPH, 1)
+        ctx.set_option(bt.BPE_OPT_PROFILE, 0)
+    g = golden["tiny"]
+    assert sha(m.astype(np.uint32)) == g["merges_sha256"]
+    assert sha(host_u32(f)) == g["final_sha256"]
+    if mode == "profile":
+        st = ctx.stats()
+        assert st["pair_count"]["ms"] > 0 and st["merge_compact"]["launches"] == 256
+
+
+def train_workload(ctx, golden, name, checkpoints):
+    g = golden[name]
+    text = synth.corpus(name)
+    assert sha(text) == g["corpus_sha256"], "generator output differs on this machine"
+    sym = ctx.pretokenize(dev_u8(text))
+    assert sha(host_u32(sym)) == g["symbols_sha256"]
+    m, f = ctx.train(sym, g["n_merges"])
+    assert m.shape[0] == g["n_done"]
+    assert m[:8].tolist() == g["merges_head"]
+    assert sha(m.astype(np.uint32)) == g["merges_sha256"]
+    assert f.numel() == g["n_final"] and sha(host_u32(f)) == g["final_sha256"]
+    for k in checkpoints:
+        _, fk = ctx.train(sym, k)
+        ck = g["checkpoints"][str(k)]
+        assert fk.numel() == ck["n"] and sha(host_u32(fk)) == ck["sha256"], k
+    return m
+
+
+def test_train_tiny_workload(ctx, golden):
+    train_workload(ctx, golden, "tiny", [0, 1, 2, 10, 100])
+
+
+def test_train_med_workload(ctx, golden):
+    train_workload(ctx, golden, "med", [1, 2, 10, 100, 1000])
+
+
+@pytest.fixture(scope="module")
+def large_merges(ctx, golden):
+    """The large workload's merge table from the GPU, accepted only when it is
+    bit-identical (by hash) to the oracle's recorded table."""
+    return train_workload(ctx, golden, "large", [10, 1000])
+
+
+def test_train_large_workload(large_merges, golden):
+    assert large_merges.shape[0] == golden["large"]["n_done"]
+
+
+# ------------------------------------------------------------------ encode --
+def vocab_arrays(tokens):
+    vb = b"".join(tokens)
+    off = np.cumsum([0] + [len(t) for t in tokens]).astype(np.uint64)
+    return np.frombuffer(vb, dtype=np.uint8).copy(), off
+
+
+def check_encode(ctx, vb, off, docs, chunk=None):
+    import bpe_trie_encode_gb300 as bt
+    data = b"".join(docs)
+    doc_off = np.cumsum([0] + [len(d) for d in docs]).astype(np.int64)
+    trie = ctx.trie_build(vb, off)
+    if chunk:
+        ctx.set_option(bt.BPE_OPT_CHUNK, chunk)
+    try:
+        ids, id_off = ctx.encode(trie, dev_u8(data) if data else torch.empty(0, dtype=torch.uint8, device="cuda"),
+                                 torch.from_numpy(doc_off).cuda())
+    finally:
+        ctx.set_option(bt.BPE_OPT_CHUNK, 128)
+    wids, woff = oracle.Trie(vb, off).encode(data, doc_off.astype(np.uint64))
+    assert np.array_equal(ids.cpu().numpy(), wids)
+    assert np.array_equal(id_off.cpu().numpy().astype(np.uint64), woff)
+    return ids
+
+
+def test_encode_worked_examples(ctx):
+    with open(os.path.join(GOLDEN, "worked_examples.json")) as f:
+        ex = json.load(f)
+    for e in ex["encode"]:
+        toks = [bytes([b]) for b in range(256)] + [s.encode() for s in e["vocab_extra"]]
+        vb, off = vocab_arrays(toks)
+        ids = check_encode(ctx, vb, off, [e["text"].encode()])
+        assert ids.cpu().tolist() == e["ids"], e["name"]
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_encode_random_vocab_ragged_docs(ctx, seed):
+    rng = random.Random(seed)
+    alpha = b"ab c" if seed % 2 else bytes(range(97, 103)) + b" ."
+    toks = [bytes([b]) for b in range(256)]
+    toks += [rand_bytes(rng, rng.randrange(2, 40), alpha) for _ in range(rng.randrange(5, 3000))]
+    vb, off = vocab_arrays(toks)
+    docs = [rand_bytes(rng, rng.choice([0, 1, 5, 127, 128, 129, 1000, 5000]), alpha) for _ in range(rng.randrange(1, 40))]
+    check_encode(ctx, vb, off, docs)
+
+
+@pytest.mark.parametrize("chunk", [64, 128, 256, 1024])
+def test_encode_chunk_sizes_agree(ctx, chunk):
+    rng = random.Random(11)
+    toks = [bytes([b]) for b in range(256)] + [rand_bytes(rng, rng.randrange(2, 30), b"abc ") for _ in range(500)]
+    vb, off = vocab_arrays(toks)
+    docs = [rand_bytes(rng, 20000, b"abc ") for _ in range(3)]
+    check_encode(ctx, vb, off, docs, chunk=chunk)
+
+
+def test_encode_tokens_longer_than_chunks(ctx):
+    # tokens of 300 bytes make the previous chunk's last token cover whole chunks
+    toks = [bytes([b]) for b in range(256)] + [b"x" * 300, b"x" * 299 + b"y", b"xy" * 100]
+    vb, off = vocab_arrays(toks)
+    docs = [b"x" * 5000 + b"y" + b"xy" * 700, b"x" * 299 + b"y" * 3]
+    check_encode(ctx, vb, off, docs)
+
+
+def test_encode_parses_that_never_meet(ctx):
+    # with tokens {a, aa} parses started one byte apart never share a boundary:
+    # every chunk needs the repair walk
+    toks = [bytes([b]) for b in range(256)] + [b"aa", b"ab"]
+    vb, off = vocab_arrays(toks)
+    check_encode(ctx, vb, off, [b"a" * 100001 + b"b", b"a" * 1000, b"ba" * 3000])
+
+
+def test_encode_capacity_error(ctx):
+    import bpe_trie_encode_gb300 as bt
+    toks = [bytes([b]) for b in range(256)]
+    vb, off = vocab_arrays(toks)
+    trie = ctx.trie_build(vb, off)
+    with pytest.raises(bt.BpeError) as e:
+        ctx.encode(trie, dev_u8(b"hello world"), capacity=5)
+    assert e.value.name == "CAPACITY" and "11 ids" in str(e.value)
+
+
+def test_encode_rejects_bad_inputs(ctx):
+    import bpe_trie_encode_gb300 as bt
+    with pytest.raises(bt.BpeError):
+        ctx.trie_build(*vocab_arrays([b"a", b"b"]))
+    trie = ctx.trie_build(*vocab_arrays([bytes([b]) for b in range(256)]))
+    with pytest.raises(bt.BpeError) as e:
+        ctx.encode(trie, dev_u8(b"abcdef"), torch.tensor([0, 4, 2], dtype=torch.int64, device="cuda"))
+    assert e.value.name == "INVALID_ARG"
+
+
+def test_encode_learned_vocab_tiny(ctx, golden):
+    sym = oracle.pretokenize(synth.corpus("tiny"))
+    wm, _ = oracle.train_words(sym, 256)
+    vb, off = oracle.vocab_from_merges(wm)
+    text = synth.lexicon("tiny").corpus(42, 300000)
+    check_encode(ctx, vb, off, [text.tobytes()[:100000], text.tobytes()[100000:]])
+
+
+def test_encode_large_vocab_workload(ctx, large_merges, golden):
+    """1 GiB of text with the 32,256-token vocabulary learned on the large
+    corpus (the merge table was verified against the oracle's by hash)."""
+    g = golden["enc"]
+    vb, off = oracle.vocab_from_merges(large_merges)
+    assert sha(np.asarray(vb, dtype=np.uint8)) == g["vocab_sha256"]
+    text = synth.corpus("enc")
+    assert sha(text) == g["text_sha256"]
+    trie = ctx.trie_build(vb, off)
+    d = dev_u8(text)
+    del text
+    ids, id_off = ctx.encode(trie, d)
+    assert ids.numel() == g["n_ids"]
+    assert sha(ids.cpu().numpy()) == g["ids_sha256"]
+    assert sha(id_off.cpu().numpy().astype(np.uint64)) == g["id_off_sha256"]
+
+
+def test_encode_batch_workload(ctx, golden):
+    """512 documents of >= 64 KiB, 250,000-token substring vocabulary."""
+    g = golden["batch"]
+    big = synth.corpus("large")
+    vb, off = synth.substring_vocab(big)
+    del big
+    assert sha(vb) == g["vocab_sha256"] and sha(off) == g["vocab_off_sha256"]
+    data, doc_off = synth.batch_documents()
+    assert sha(data) == g["text_sha256"]
+    trie = ctx.trie_build(vb, off)
+    ids, id_off = ctx.encode(trie, dev_u8(data), torch.from_numpy(doc_off.astype(np.int64)).cuda())
+    assert ids.numel() == g["n_ids"]
+    assert sha(ids.cpu().numpy()) == g["ids_sha256"]
+    assert sha(id_off.cpu().numpy().astype(np.uint64)) == g["id_off_sha256"]
