@@ -72,7 +72,7 @@ def test_pretokenize_sizes(ctx, n):
 
 def test_pretokenize_unaligned_and_all_bytes(ctx):
     data = np.arange(256 * 40, dtype=np.uint32).astype(np.uint8)
-    d = dev_u8(np.concatenate([[7], data]))
+    d = dev_u8(np.concatenate([np.array([7], dtype=np.uint8), data]))
     got = host_u32(ctx.pretokenize(d[1:]))            # 1-byte offset: scalar path
     assert np.array_equal(got, oracle.pretokenize(data))
 
