@@ -1,0 +1,507 @@
+#!/usr/bin/env python
+"""Benchmark: BPE training merges/s and trie-encode GB/s on one GB300.
+
+One step is one pass of the whole hot path over one batch of synthetic input:
+  train leg   pre-tokenize the medium corpus (16 MiB, seed 1, 20,000-word
+              Turkish-mix lexicon) and run 4,096 merges (pair count, argmax,
+              merge, compaction per merge)
+  encode leg  greedy longest-match encode of 1 GiB of fresh text (seed 3) with
+              the 32,256-token vocabulary learned on the large corpus (trained
+              on the GPU during set-up, checked against the oracle's table)
+``value`` is the train leg's merges/s (the medium training workload is the
+headline configuration); the encode leg is reported in ``encode``.  Inputs are
+resident in HBM when the timed region starts; L2 is flushed between steps.
+Kernel durations come from CUDA events recorded after every kernel on the
+launching stream (the library's profile option) inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle (single-threaded C) on the same
+workload: each step runs the oracle's training on the medium corpus and its
+greedy encode on a 64 MiB sample of the encode text.
+N > 1 (torchrun) runs independent replicas, one per GPU ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import platform
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "BPE train merges/s + trie_encode GB/s on 1 GB300; % of HBM roofline"
+TRAIN = {"tiny": 256, "med": 4096, "large": 32000}
+ENC_REF_SAMPLE = 64 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--train", default="med", choices=sorted(TRAIN))
+    ap.add_argument("--encode", default="enc", choices=["enc", "batch", "none"])
+    ap.add_argument("--merges", type=int, default=None, help="override the merge count (profiling cases)")
+    ap.add_argument("--encode-bytes", type=int, default=None, help="encode only a prefix (profiling cases)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
+
+
+# ----------------------------------------------------------------- clocks ---
+class Clocks:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.lines: list[str] = []
+        self.proc = None
+        self.th = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.idx)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.th:
+            self.th.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- helpers ------
+def sha(a) -> str:
+    import numpy as np
+    return hashlib.sha256(np.ascontiguousarray(a).tobytes()).hexdigest()
+
+
+def golden():
+    try:
+        with open(os.path.join(ROOT, "tests", "golden", "workloads.json")) as f:
+            return json.load(f)
+    except Exception:
+        return {}
+
+
+def traffic_record():
+    """Per-launch DRAM bytes of each kernel from a committed ncu summary,
+    valid only while the kernel's source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+    except Exception:
+        return {}
+    out = {}
+    for name, r in rec.get("kernels", {}).items():
+        src = os.path.join(ROOT, r["source"])
+        try:
+            h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        except Exception:
+            continue
+        if h == r.get("source_sha256"):
+            out[name] = r
+    return out
+
+
+def roofline(stats: dict, families: list[str], peak: float, peak_kind: str, traffic: dict):
+    fam = max(families, key=lambda f: stats.get(f, {}).get("ms", 0.0))
+    s = stats[fam]
+    achieved = s["bytes"] / (s["ms"] / 1e3) / 1e9 if s["ms"] > 0 else 0.0
+    per_launch_bytes = s["bytes"] / max(s["launches"], 1)
+    t = traffic.get(fam)
+    tr = None
+    if t:
+        # ncu measured a (possibly smaller) case: scale its DRAM bytes by the
+        # algorithmic bytes of that case to this launch's algorithmic bytes
+        tr = t["dram_bytes"] * per_launch_bytes / t["algorithmic_bytes"] if t.get("scale") else t["dram_bytes"]
+    return {"kernel": fam, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_kind": f"of {peak_kind}",
+            "traffic": round(tr, 1) if tr is not None else None,
+            "algorithmic_bytes_per_launch": round(per_launch_bytes, 1),
+            "avg_launch_ms": round(s["ms"] / max(s["launches"], 1), 6)}
+
+
+# ---------------------------------------------------------------- ours ------
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import bpe_trie_encode_gb300 as bt
+    import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    ctx = bt.Context(local_rank)
+    g = golden()
+    peak, peak_kind = peaks()
+    n_merges = args.merges or TRAIN[args.train]
+
+    # ---- set-up (untimed)
+    text = synth.corpus(args.train)
+    h_text = torch.from_numpy(text.copy()).pin_memory()
+    d_text = h_text.to(dev)
+    d_sym = torch.empty(text.size, dtype=torch.int32, device=dev)
+    enc = None
+    vocab_check = None
+    if args.encode != "none":
+        if args.encode == "enc":
+            m_big = large_merges_for_reference()       # the oracle's table (stored copy, hash checked)
+            vocab_check = "the oracle's merge table of the large corpus"
+            vb, voff = bt.vocab_from_merges(m_big)
+            etext = synth.corpus("enc", args.encode_bytes)
+            doc_off = np.array([0, etext.size], dtype=np.int64)
+            wl = (f"{etext.size} B text (seed 3), 32,256-token vocabulary learned on the large corpus, "
+                  "one document")
+        else:
+            big = synth.corpus("large")
+            vb, voff = synth.substring_vocab(big)
+            del big
+            etext, doc_off = synth.batch_documents()
+            doc_off = doc_off.astype(np.int64)
+            vocab_check = "generator vocabulary"
+            wl = "512 documents of >= 64 KiB (seed 4), 250,000-token substring vocabulary"
+        trie = ctx.trie_build(vb, voff)
+        h_enc = torch.from_numpy(etext).pin_memory()
+        enc = {"trie": trie, "vb": vb, "voff": voff, "h": h_enc, "d": h_enc.to(dev), "h_off": torch.from_numpy(doc_off).pin_memory(),
+               "d_off": torch.from_numpy(doc_off).to(dev), "workload": wl, "bytes": int(etext.size),
+               "ids": torch.empty(int(etext.size), dtype=torch.int32, device=dev)}
+        del etext
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(timed: bool, acc: dict):
+        flush.fill_(1)                         # L2 flush between steps (> 129 MB written)
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        ctx.pretokenize(d_text, out=d_sym)
+        m, _ = ctx.train(d_sym, n_merges, final=False)
+        st_train = ctx.stats()
+        e1.record(stream)
+        st_enc = None
+        n_ids = 0
+        if enc:
+            ids, _ = ctx.encode(enc["trie"], enc["d"], enc["d_off"], ids_out=enc["ids"])
+            n_ids = ids.numel()
+            st_enc = ctx.stats()
+        e2.record(stream)
+        torch.cuda.synchronize(dev)
+        if timed:
+            acc["train_ms"] += e0.elapsed_time(e1)
+            acc["enc_ms"] += e1.elapsed_time(e2)
+            acc["merges"] += m.shape[0]
+            acc["launches"] += 1 + st_train["kernel_launches"] + (st_enc["kernel_launches"] if st_enc else 0)
+            for st in (st_train, st_enc):
+                for k, v in (st or {}).items():
+                    if k == "kernel_launches":
+                        continue
+                    a = acc["kern"].setdefault(k, {"launches": 0, "bytes": 0.0, "ms": 0.0})
+                    for f in ("launches", "bytes", "ms"):
+                        a[f] += v[f]
+            acc["n_ids"] = n_ids
+
+    ctx.set_option(bt.BPE_OPT_PROFILE, 1)
+    dummy = {"train_ms": 0, "enc_ms": 0, "merges": 0, "launches": 0, "kern": {}}
+    for _ in range(args.warmup):
+        step(False, dummy)
+    acc = {"train_ms": 0.0, "enc_ms": 0.0, "merges": 0, "launches": 0, "kern": {}, "n_ids": 0}
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = Clocks(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    for _ in range(args.steps):
+        step(True, acc)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    ctx.set_option(bt.BPE_OPT_PROFILE, 0)
+
+    t = torch.tensor([acc["train_ms"], acc["enc_ms"]], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    train_ms, enc_ms = float(t[0]), float(t[1])
+    merges_total = acc["merges"] * world
+    value = merges_total / (train_ms / 1e3)
+
+    # ---- end to end through host buffers (graph replay, no profiling)
+    e2e = None
+    if not args.no_e2e:
+        h_merges_bytes = n_merges * 16
+        tr_ms = en_ms = 0.0
+        d2h_ids = 0
+        for i in range(args.warmup + args.steps):
+            flush.fill_(1)
+            torch.cuda.synchronize(dev)
+            a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            a.record(stream)
+            dt = h_text.to(dev, non_blocking=True)
+            ctx.pretokenize(dt, out=d_sym)
+            m, _ = ctx.train(d_sym, n_merges, final=False)     # merge table returns to host
+            b.record(stream)
+            if enc:
+                de = enc["h"].to(dev, non_blocking=True)
+                do = enc["h_off"].to(dev, non_blocking=True)
+                ids, id_off = ctx.encode(enc["trie"], de, do, ids_out=enc["ids"])
+                h_ids = ids.to("cpu")
+                h_io = id_off.to("cpu")
+                d2h_ids = h_ids.numel() * 4 + h_io.numel() * 8
+            c.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= args.warmup:
+                tr_ms += a.elapsed_time(b)
+                en_ms += b.elapsed_time(c)
+        t2 = torch.tensor([tr_ms, en_ms], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(t2, op=dist.ReduceOp.MAX)
+        tr_ms, en_ms = float(t2[0]), float(t2[1])
+        e2e = {"value": round(args.steps * m.shape[0] * world / (tr_ms / 1e3), 2), "unit": "merges/s",
+               "h2d_bytes_per_step": int(text.size + (enc["bytes"] + enc["h_off"].numel() * 8 if enc else 0)),
+               "d2h_bytes_per_step": int(h_merges_bytes + d2h_ids)}
+        if enc:
+            e2e["encode"] = {"value": round(args.steps * enc["bytes"] * world / (en_ms / 1e3) / 1e9, 3),
+                             "unit": "GB/s"}
+
+    # ---- CPU baseline: the oracle as it stands, rank 0, N == 1 only
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args, text, enc, n_merges)
+
+    if rank != 0:
+        return None
+    traffic = traffic_record()
+    kern = acc["kern"]
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "merges/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round((train_ms + enc_ms) / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "data": "synthetic (seeded generator)",
+        "config": {"workload": f"{args.train} training: {text.size} B corpus, {n_merges} merges; "
+                               f"encode leg: {enc['workload'] if enc else 'none'}",
+                   "train_corpus_bytes": int(text.size), "n_merges": n_merges,
+                   "l2": "flushed between steps (256 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "vocab": vocab_check},
+        "train": {"value": round(value, 2), "unit": "merges/s", "ms_per_step": round(train_ms / args.steps, 3),
+                  "roofline": roofline(kern, ["pair_count", "merge_compact"], peak, peak_kind, traffic)},
+        "roofline": roofline(kern, ["pair_count", "merge_compact"], peak, peak_kind, traffic),
+        "gpu_launches": acc["launches"],
+        "kernels": {k: {"launches": v["launches"], "ms": round(v["ms"], 3),
+                        "GB/s": round(v["bytes"] / (v["ms"] / 1e3) / 1e9, 1) if v["ms"] else None}
+                    for k, v in kern.items()},
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if enc:
+        gbs = args.steps * enc["bytes"] * world / (enc_ms / 1e3) / 1e9
+        out["encode"] = {"value": round(gbs, 3), "unit": "GB/s", "ms_per_step": round(enc_ms / args.steps, 3),
+                         "workload": enc["workload"], "n_ids": acc["n_ids"],
+                         "roofline": roofline(kern, ["encode_spec", "encode_emit"], peak, peak_kind, traffic)}
+    return out
+
+
+def cpu_baseline(args, text, enc, n_merges):
+    """The oracle as it stands, single-threaded, on a bounded sample: the full
+    training workload (about 10 s of CPU) and the first 64 MiB of the encode
+    text with the same vocabulary."""
+    import numpy as np
+
+    import oracle
+
+    t0 = time.perf_counter()
+    sym = oracle.pretokenize(text)
+    m, _ = oracle.train_words(sym, n_merges)
+    dt = time.perf_counter() - t0
+    out = {"value": round(m.shape[0] / dt, 2), "unit": "merges/s", "cores": 1, "kind": "oracle",
+           "sample": f"{args.train} training, full ({text.size} B, {n_merges} merges), "
+                     f"word-frequency oracle, single thread, {cpu_model()}",
+           "seconds": round(dt, 2)}
+    if enc:
+        sample = enc["h"][:ENC_REF_SAMPLE].numpy()
+        trie = oracle.Trie(enc["vb"], enc["voff"])
+        t0 = time.perf_counter()
+        trie.encode(sample)
+        dt = time.perf_counter() - t0
+        out["encode"] = {"value": round(sample.size / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+                         "sample": f"first {sample.size} B of the encode text, same vocabulary"}
+    return out
+
+
+def large_merges_for_reference():
+    """The oracle's merge table of the large corpus: the stored copy written by
+    tests/golden/make_golden.py (checked by hash), else a fresh oracle run."""
+    import numpy as np
+
+    import oracle
+    import synth
+    g = golden().get("large", {})
+    p = os.path.join(ROOT, "tests", "golden", "large_merges.npy")
+    if os.path.exists(p) and g:
+        lr = np.load(p).astype(np.uint32)
+        m = np.zeros((lr.shape[0], 4), dtype=np.uint32)
+        m[:, :2] = lr[:, :2]
+        m[:, 2] = 256 + np.arange(lr.shape[0], dtype=np.uint32)
+        m[:, 3] = lr[:, 2]
+        if sha(m) == g.get("merges_sha256"):
+            return m
+    m, _ = oracle.train_words(oracle.pretokenize(synth.corpus("large")), TRAIN["large"])
+    return m
+
+
+def encode_reference_sample(args):
+    """(vocab bytes, offsets, sample text, doc offsets) for the oracle's encode leg."""
+    import numpy as np
+
+    import oracle
+    import synth
+    if args.encode == "enc":
+        vb, voff = oracle.vocab_from_merges(large_merges_for_reference())
+        text = synth.corpus("enc", ENC_REF_SAMPLE)
+        doc_off = np.array([0, text.size], dtype=np.uint64)
+    else:
+        big = synth.corpus("large")
+        vb, voff = synth.substring_vocab(big)
+        text, doc_off = synth.batch_documents(64)
+    return vb, voff, text, doc_off
+
+
+# ---------------------------------------------------------- reference -------
+def run_reference(args, rank, world):
+    import numpy as np
+
+    import oracle
+    import synth
+    if rank != 0:
+        return None
+    n_merges = TRAIN[args.train]
+    text = synth.corpus(args.train)
+    enc = None
+    if args.encode != "none":
+        vb, voff, etext, doc_off = encode_reference_sample(args)
+        enc = (oracle.Trie(vb, voff), etext, doc_off)
+
+    def step():
+        t0 = time.perf_counter()
+        m, _ = oracle.train_words(oracle.pretokenize(text), n_merges)
+        t1 = time.perf_counter()
+        if enc:
+            enc[0].encode(enc[1], enc[2])
+        t2 = time.perf_counter()
+        return t1 - t0, t2 - t1, m.shape[0]
+
+    for _ in range(args.warmup):
+        step()
+    tr = en = 0.0
+    merges = 0
+    for _ in range(args.steps):
+        a, b, m = step()
+        tr += a
+        en += b
+        merges += m
+    value = merges / tr
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "merges/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round((tr + en) / args.steps * 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+           "data": "synthetic (seeded generator)",
+           "config": {"workload": f"{args.train} training: {text.size} B corpus, {n_merges} merges; "
+                                  f"encode leg: {args.encode} ({'64 MiB sample' if args.encode == 'enc' else '64 documents'})",
+                      "parallelism": "CPU oracle, rank 0 only"},
+           "cpu_baseline": {"value": round(value, 2), "unit": "merges/s", "cores": 1, "kind": "oracle",
+                            "sample": f"full {args.train} training per step, single-threaded C oracle, {cpu_model()}"},
+           "e2e": {"value": round(value, 2), "unit": "merges/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    if enc:
+        out["encode"] = {"value": round(args.steps * enc[1].size / en / 1e9, 4), "unit": "GB/s",
+                         "sample_bytes": int(enc[1].size)}
+    return out
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        import torch
+        import torch.distributed as dist
+        if world > 1:
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        out = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            dist.destroy_process_group()
+    if out is not None and rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

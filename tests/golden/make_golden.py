@@ -12,7 +12,8 @@ Workloads (see ``synth`` for the text recipe):
   tiny   64 KiB corpus, 256 merges (full-stream oracle and word-frequency
          oracle must agree; both are recorded)
   med    16 MiB corpus, 4,096 merges
-  large  256 MiB corpus, 32,000 merges
+  large  256 MiB corpus, 32,000 merges (the table itself is also stored,
+         as large_merges.npy: rows of left, right, count)
   enc    1 GiB text, greedy encode with the vocabulary learned on ``large``
   batch  512 documents, 250,000-token substring vocabulary, per-document ids
 """
@@ -127,6 +128,9 @@ def main(names):
             rec, merges = train_record(name)
             if name == "large":
                 merges_large = merges
+                # (left, right, count) as uint32 for consumers that need the table
+                np.save(os.path.join(os.path.dirname(OUT), "large_merges.npy"),
+                        merges[:, [0, 1, 3]].astype(np.uint32))
         else:
             rec = encode_record(name, merges_large)
         data[name] = rec
