@@ -35,6 +35,7 @@
 // root's 256 children are in a shared-memory LUT ([GPU-BPE] "Line by line",
 // 3) root LUT), so the first byte of every token costs no global load.
 #include <algorithm>
+#include <mutex>
 
 #include "device.cuh"
 #include "internal.h"
@@ -518,4 +519,144 @@ extern "C" int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_
         return fail(ctx, BPE_ERR_CAPACITY, "trie_encode: %llu ids exceed the capacity %llu",
                     (unsigned long long)total, (unsigned long long)ids_capacity);
     return BPE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// trie_encode_noalloc: the same kernels, with every scratch buffer carved out
+// of one fixed device array instead of the context's pool, for callers that
+// must not allocate device memory.  The array is part of the library's
+// module: each GPU that loads the library holds it until the process exits.
+namespace bpe {
+namespace {
+
+constexpr uint32_t kNaMaxDocs = 65536;
+constexpr uint64_t kNaMaxChunks = 524288;          // 128-byte chunks: up to 64 MiB of text
+constexpr uint32_t kNaChunk = 128;
+constexpr size_t na_align(size_t x) { return (x + 255) & ~size_t(255); }
+constexpr size_t kNaOffState = 0;
+constexpr size_t kNaOffChunkStart = na_align(sizeof(EncState));
+constexpr size_t kNaOffInfo = na_align(kNaOffChunkStart + 8 * ((size_t)kNaMaxDocs + 1));
+constexpr size_t kNaOffFlag = na_align(kNaOffInfo + 12 * kNaMaxChunks);
+constexpr size_t kNaOffStatus = na_align(kNaOffFlag + kNaMaxChunks / 8);
+constexpr size_t kNaOffPrefix = na_align(kNaOffStatus + 8 * (kNaMaxChunks / kEmitThreads + 1));
+constexpr size_t kNaOffIdOff = na_align(kNaOffPrefix + 8 * kNaMaxChunks);
+constexpr size_t kNaBytes = na_align(kNaOffIdOff + 8 * ((size_t)kNaMaxDocs + 1));   // about 11.6 MB
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaBytes];
+
+// Device address of g_noalloc_scratch per device, looked up once with that
+// device current (the host-side name is only a stand-in, never a device
+// address).
+std::mutex g_na_mu;
+void *g_na_addr[256] = {};
+
+cudaError_t noalloc_scratch(int device, unsigned char **out) {
+    std::lock_guard<std::mutex> lock(g_na_mu);
+    if (device < 0 || device >= 256) return cudaErrorInvalidDevice;
+    if (!g_na_addr[device]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_na_addr[device] = p;
+    }
+    *out = (unsigned char *)g_na_addr[device];
+    return cudaSuccess;
+}
+
+struct DeviceGuard {   // restores the caller's current device
+    int prev = -1;
+    explicit DeviceGuard(int d) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        cudaSetDevice(d);
+    }
+    ~DeviceGuard() {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+int noalloc_body(const bpe_trie *trie, const uint8_t *d_bytes, const uint64_t *d_doc_off, uint32_t n_docs,
+                 int32_t *d_ids_out, uint64_t ids_capacity, uint64_t *d_id_off_out, uint64_t *n_ids,
+                 cudaStream_t s) {
+    unsigned char *base = nullptr;
+    if (noalloc_scratch(trie->device, &base) != cudaSuccess) return BPE_ERR_CUDA;
+    EncParams P{};
+    P.bytes = d_bytes;
+    P.doc_off = d_doc_off;
+    P.n_docs = n_docs;
+    P.chunk = kNaChunk;
+    P.chunk_start = (const unsigned long long *)(base + kNaOffChunkStart);
+    P.slot = trie->d_slot;
+    P.tid = trie->d_tid;
+    P.root = trie->d_root;
+    P.ids = d_ids_out;
+    P.cap = ids_capacity;
+    P.st = (EncState *)(base + kNaOffState);
+    P.count = (uint32_t *)(base + kNaOffInfo);
+    P.exit_rel = P.count + kNaMaxChunks;
+    P.spec_rel = P.exit_rel + kNaMaxChunks;
+    P.flag = (uint32_t *)(base + kNaOffFlag);
+    P.status = (unsigned long long *)(base + kNaOffStatus);
+    P.prefix = (unsigned long long *)(base + kNaOffPrefix);
+    P.id_off = d_id_off_out ? (unsigned long long *)d_id_off_out : (unsigned long long *)(base + kNaOffIdOff);
+
+    // the array keeps the previous call's contents: zero what must start at zero
+    if (cudaMemsetAsync(P.st, 0, sizeof(EncState), s) != cudaSuccess) return BPE_ERR_CUDA;
+    k_chunk_index<<<1, 1024, 0, s>>>(P, (unsigned long long *)(base + kNaOffChunkStart));
+    EncState h;
+    if (cudaMemcpyAsync(&h, P.st, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return BPE_ERR_CUDA;
+    if (h.err & DERR_OOB) return BPE_ERR_INVALID_ARG;
+    const unsigned long long nc = h.n_chunks;
+    if (nc > kNaMaxChunks) return BPE_ERR_INVALID_ARG;
+    if (nc == 0) {
+        if (d_id_off_out && cudaMemsetAsync(d_id_off_out, 0, 8 * ((size_t)n_docs + 1), s) != cudaSuccess)
+            return BPE_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return BPE_ERR_CUDA;
+        *n_ids = 0;
+        return BPE_OK;
+    }
+    const unsigned long long spec_blocks = (nc + kSpecThreads - 2) / (kSpecThreads - 1);
+    const unsigned long long emit_tiles = (nc + kEmitThreads - 1) / kEmitThreads;
+    if (cudaMemsetAsync(P.flag, 0, ((nc + 31) / 32) * 4, s) != cudaSuccess ||
+        cudaMemsetAsync(P.status, 0, emit_tiles * 8, s) != cudaSuccess)
+        return BPE_ERR_CUDA;
+    int sms = 0, eb = 1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, trie->device) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&eb, k_emit, kEmitThreads, 0) != cudaSuccess)
+        return BPE_ERR_CUDA;
+    const unsigned long long emit_grid =
+        std::min<unsigned long long>(emit_tiles, (unsigned long long)sms * std::max(eb, 1));
+    const size_t spec_smem = (size_t)kSpecThreads * (kNaChunk / 32) * 4;
+    k_spec<<<(unsigned)spec_blocks, kSpecThreads, spec_smem, s>>>(P, nc);
+    k_repair<<<1, 256, 0, s>>>(P, nc);
+    k_emit<<<(unsigned)emit_grid, kEmitThreads, 0, s>>>(P, nc);
+    k_doc_offsets<<<(unsigned)((n_docs + 1 + 255) / 256), 256, 0, s>>>(P, nc);
+    if (cudaGetLastError() != cudaSuccess) return BPE_ERR_CUDA;
+    if (cudaMemcpyAsync(&h, P.st, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return BPE_ERR_CUDA;
+    if (h.err & DERR_TIMEOUT) return BPE_ERR_TIMEOUT;
+    *n_ids = h.total;
+    return h.total > ids_capacity ? BPE_ERR_CAPACITY : BPE_OK;
+}
+
+}  // namespace
+}  // namespace bpe
+
+extern "C" int trie_encode_noalloc(const bpe_trie *trie, const uint8_t *d_bytes, const uint64_t *d_doc_off,
+                                   uint32_t n_docs, int32_t *d_ids_out, uint64_t ids_capacity,
+                                   uint64_t *d_id_off_out, uint64_t *n_ids, void *cuda_stream) {
+    if (!trie || !n_ids) return BPE_ERR_INVALID_ARG;
+    *n_ids = 0;
+    if (n_docs > bpe::kNaMaxDocs) return BPE_ERR_INVALID_ARG;
+    if (n_docs && (!d_doc_off || !d_bytes)) return BPE_ERR_INVALID_ARG;
+    if (ids_capacity && !d_ids_out) return BPE_ERR_INVALID_ARG;
+    bpe::DeviceGuard guard(trie->device);
+    cudaStream_t s = (cudaStream_t)cuda_stream;
+    if (n_docs == 0) {
+        if (d_id_off_out && cudaMemsetAsync(d_id_off_out, 0, 8, s) != cudaSuccess) return BPE_ERR_CUDA;
+        return cudaStreamSynchronize(s) == cudaSuccess ? BPE_OK : BPE_ERR_CUDA;
+    }
+    return bpe::noalloc_body(trie, d_bytes, d_doc_off, n_docs, d_ids_out, ids_capacity, d_id_off_out, n_ids, s);
 }

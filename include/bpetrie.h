@@ -182,6 +182,35 @@ int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_bytes,
                 const uint64_t *d_doc_off, uint32_t n_docs, int32_t *d_ids_out,
                 uint64_t ids_capacity, uint64_t *d_id_off_out, uint64_t *n_ids);
 
+/* Encoding that allocates nothing.  The pages have no counterpart: this entry
+ * point exists for callers of the library that cannot allocate device memory,
+ * for example a plug-in that receives only a stream and raw device pointers
+ * from a host application which owns all device memory through its own
+ * allocator or a fixed budget, or a latency-critical path that must not
+ * trigger the device-wide synchronisation that cudaFree implies.
+ *
+ * Same inputs, outputs, result and errors as trie_encode, but no context is
+ * used and nothing is allocated (no cudaMalloc, cudaFree, pinned host memory
+ * or allocating library routine): the scratch lives in one fixed array inside
+ * the library, about 11.6 MB, which every GPU that loads the library holds
+ * until the process exits.  The work is ordered on `cuda_stream` (a
+ * cudaStream_t, NULL = legacy default stream); the trie's device is made
+ * current for the call and the caller's current device is restored.
+ *
+ * Limits: n_docs <= 65,536 and at most 524,288 chunks of 128 bytes, where a
+ * document of L bytes uses ceil(L / 128) chunks (up to 64 MiB of text in
+ * all).  A larger input returns BPE_ERR_INVALID_ARG before any id is written.
+ * The first call on a device looks up the array's device address, once per
+ * device with that device current; make that first call before any stream
+ * capture.  Every call shares the array, which keeps the last call's contents
+ * (each call clears what must start at zero), so calls that overlap on the GPU
+ * -- on different streams or threads -- race: the caller must serialise them.
+ * Blocks until done.  Errors: INVALID_ARG, CAPACITY (with *n_ids = required
+ * size), TIMEOUT, CUDA; there is no context, so no message is kept. */
+int trie_encode_noalloc(const bpe_trie *trie, const uint8_t *d_bytes, const uint64_t *d_doc_off,
+                        uint32_t n_docs, int32_t *d_ids_out, uint64_t ids_capacity,
+                        uint64_t *d_id_off_out, uint64_t *n_ids, void *cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif
