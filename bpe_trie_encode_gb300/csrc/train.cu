@@ -2,41 +2,48 @@
 // "What it does" 2.-3., and the training pipeline clear_table -> pair_count
 // -> find_max -> setup_merge -> merge_reduce -> scan -> finalize_compact).
 //
-// One merge iteration k is two kernels:
+// Pair counts are kept exactly, for every pair ever seen, in one global table
+// for the whole call:
 //
-//   k_count  pair counting.  Each CTA sums the pairs of its share of the
-//            stream in a shared-memory hash table (Murmur3 finaliser,
-//            triangular probing) and flushes it to one global table with
-//            atomics when it fills up and once at the end ([GPU-BPE] "What it
-//            does", 2. two-level pair counting).  The flush also performs the
-//            argmax: atomicAdd returns a key's running total, the largest
-//            (count, -key) a CTA saw goes through one atomicMax into best[k].
-//            The last add of the winning key sees its final count, and no
-//            running total exceeds a final one, so best[k] is the exact
-//            argmax with the tie-break count desc, left asc, right asc.  No
-//            separate table scan, no clear_table dispatch.
-//   k_merge  merge + compaction in one pass over the stream ([GPU-BPE] "What
-//            it does", 3.; "Line by line", 2) subgroup scan).  Tiles of 2048
-//            symbols are taken in ticket order; a tile publishes its
-//            aggregate, looks back for its predecessors' prefix (decoupled
-//            look-back) and scatters its surviving symbols.  The carried
-//            state is a 1-bit transducer plus the kept count, which handles
-//            leftmost-first merging inside runs of identical symbols that
-//            cross tiles (see below).  The same kernel clears the slots of
-//            the global table that k_count used.
+//   k_count   (merge 0 only) counts every adjacent pair of the stream.  Each
+//             CTA sums pairs in a shared-memory hash table (Murmur3
+//             finaliser, triangular probing) and flushes it to the global
+//             table when half full and once at the end ([GPU-BPE] "What it
+//             does", 2. two-level pair counting).  atomicAdd returns each
+//             key's running total; since counts only grow here, the largest
+//             (count, -key) any flush sees is the argmax, which one
+//             atomicMax per CTA records in best[0].
+//   k_argmax  (merge k >= 1) max over the dense (key, count) arrays ->
+//             best[k], tie-break count desc, left asc, right asc.
+//   k_merge   merge + compaction + count update in one pass over the stream
+//             ([GPU-BPE] "What it does", 3.; "Line by line", 2) subgroup
+//             scan).  Tiles of 4,096 symbols are taken in ticket order; a tile
+//             scans its items, publishes its aggregate, finds its prefix with
+//             a warp-wide decoupled look-back and scatters the surviving
+//             symbols.  Every pair the merge destroys or creates goes, as a
+//             -1 or +1, through a shared-memory table of deltas into the
+//             global counts, so the next argmax sees exact counts without a
+//             full recount.
 //
-// Stream state lives on the device (iteration counter, stream lengths, stop
-// flag = best[k] with count 0), so iterations can be replayed from a CUDA
-// graph with no host round trip.
+// Merge k's stream length, the stop flag (best[k] == 0) and the merge index
+// live on the device, so iterations replay from a CUDA graph with no host
+// round trip.
 //
-// Leftmost-first merging, the definition: position i is a *valid start* when
-// id(s[i]) == l, id(s[i+1]) == r and s[i+1] has no WORD_START.  Let c(i) be
-// the number of consecutive valid starts ending at i (0 if i is not one).
-// The left-to-right replacement merges exactly the starts with c(i) odd
-// (for l != r every valid start has c(i) == 1; for l == r a run alternates).
-// Position i is consumed when i-1 merges.  Per position the parity of c is a
-// function of the parity before it: "negate" for a valid start, "zero"
-// otherwise -- a 1-bit transducer, composable and therefore scannable.
+// Leftmost-first merging, the definition used: position i is a *valid start*
+// when id(s[i]) == l, id(s[i+1]) == r and s[i+1] has no WORD_START.  Let c(i)
+// be the number of consecutive valid starts ending at i (0 if none).  The
+// left-to-right replacement merges exactly the starts with c(i) odd (for
+// l != r every valid start has c(i) == 1; inside a run of l == r they
+// alternate), and position i is consumed when i-1 merges.  Per position the
+// parity of c is a function of the parity before it -- "negate" at a valid
+// start, "zero" elsewhere -- so a tile is summarised by a 1-bit transducer
+// plus its kept count for each incoming parity; these summaries compose, so
+// they scan, within a tile and across tiles.
+//
+// Count deltas of one merge (exact): an old pair (j, j+1) (counted when
+// s[j+1] has no WORD_START) disappears iff j-1, j or j+1 merges; in the new
+// stream, the pair formed by a kept position j and the next kept position
+// j + 1 + m(j) is new iff either side merged.
 #include <algorithm>
 #include <cstring>
 
@@ -48,68 +55,97 @@ namespace {
 
 constexpr int kCountThreads = 512;
 constexpr int kCountSlots = 8192;                 // shared table slots per CTA (64 KiB)
-constexpr int kCountTile = kCountThreads * 4;     // symbols per CTA step
-constexpr int kMergeThreads = 512;
+constexpr int kCountItems = 8;
+constexpr int kCountTile = kCountThreads * kCountItems;
+constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
-constexpr int kMergeTile = kMergeThreads * 4;     // symbols per tile
+constexpr int kMergeItems = 16;
+constexpr int kMergeTile = kMergeThreads * kMergeItems;  // 4,096 symbols per tile
+constexpr int kDeltaSlots = 1024;                 // shared delta table per merge CTA (8 KiB)
+constexpr int kTileHalo = 16;                     // symbols staged past a tile
+// Shared-memory tile layout: one padding word after every 16 symbols, so a
+// thread reading its 16 consecutive symbols hits 32 different banks.
+constexpr int kTileWords = (kMergeTile + kTileHalo) + (kMergeTile + kTileHalo) / 16;
+__device__ __forceinline__ int padded(int i) { return i + (i >> 4); }
+static_assert(kMergeItems == 16, "the padded tile layout assumes 16 symbols per thread");
+constexpr int kArgmaxThreads = 256;
 constexpr int kGraphIters = 32;                   // merge iterations per captured graph
 constexpr int kPadSymbols = 64;                   // readable slack past the stream end
 constexpr unsigned kSpinLimit = 1u << 22;         // look-back spins before giving up
 constexpr int kInFlight = 3;                      // graph launches in flight before polling
+constexpr unsigned long long kEmptySlot = ~0ull;
 
 struct TrainState {
-    uint32_t k_base;        // merges before the current graph replay
+    uint32_t k_base;          // merges before the current graph replay
     uint32_t n_merges;
-    uint32_t err;           // DERR_* bits
-    uint32_t pad0;
+    uint32_t err;             // DERR_* bits
+    uint32_t dense_len;       // entries of the dense key/count arrays
     unsigned long long n[2];  // stream length, by merge parity
-    uint32_t list_len[2];     // used global-table slots, by merge parity
     uint32_t ticket[2];       // tile tickets, by merge parity
 };
 
 struct TrainParams {
     uint32_t *buf[2];
-    uint32_t *tkey;
-    uint32_t *tcnt;
+    unsigned long long *tslot;   // hash slots: key << 32 | dense index
     uint32_t tmask;
-    uint32_t *list[2];
+    uint32_t *dkey;              // dense keys (l << 16 | r)
+    uint32_t *dcnt;              // dense counts
+    uint32_t dcap;
     unsigned long long *status[2];
-    unsigned long long *best;   // per merge: count << 32 | ~key ; 0 = stop
-    unsigned long long *nhist;  // stream length after k merges
+    unsigned long long *best;    // per merge: count << 32 | ~key ; 0 = stop
+    unsigned long long *nhist;   // stream length after k merges
+    uint32_t *dhist;             // dense entries scanned by argmax k
     TrainState *st;
 };
-
-// ------------------------------------------------------------ pair count ---
 
 __device__ __forceinline__ unsigned long long pack_best(uint32_t count, uint32_t key) {
     return ((unsigned long long)count << 32) | (unsigned long long)(~key);
 }
 
-// Add c to key in the global table; returns the key's new total.
-__device__ __forceinline__ uint32_t table_add(const TrainParams &p, uint32_t *list, uint32_t *list_len, uint32_t key,
-                              uint32_t c) {
+__device__ __forceinline__ uint32_t pair_key(uint32_t a, uint32_t b) { return ((a & 0xFFFFu) << 16) | (b & 0xFFFFu); }
+
+// The global count table, as the kernels hand it around.
+struct Table {
+    unsigned long long *tslot;
+    uint32_t *dkey, *dcnt;
+    TrainState *st;
+    uint32_t tmask, dcap;
+};
+__device__ __forceinline__ Table table_of(const TrainParams &p) {
+    Table t;
+    t.tslot = p.tslot; t.dkey = p.dkey; t.dcnt = p.dcnt; t.st = p.st; t.tmask = p.tmask; t.dcap = p.dcap;
+    return t;
+}
+
+// Add delta (two's complement) to key's global count; returns the new total.
+__device__ __forceinline__ uint32_t global_add(const Table p, uint32_t key, uint32_t delta) {
     uint32_t h = fmix32(key) & p.tmask;
     for (uint32_t probe = 1; probe <= 128; ++probe) {
-        uint32_t cur = __ldcg(p.tkey + h);
-        if (cur == kEmptyKey) {
-            cur = atomicCAS(p.tkey + h, kEmptyKey, key);
-            if (cur == kEmptyKey) {
-                uint32_t at = atomicAdd(list_len, 1u);
-                list[at] = h;
-                cur = key;
+        unsigned long long cur = __ldcg(p.tslot + h);
+        if (cur == kEmptySlot) {
+            const uint32_t idx = atomicAdd(&p.st->dense_len, 1u);
+            if (idx >= p.dcap) {
+                atomicOr(&p.st->err, DERR_TABLE_FULL);
+                return 0;
             }
+            p.dkey[idx] = key;
+            const unsigned long long want = ((unsigned long long)key << 32) | idx;
+            cur = atomicCAS(p.tslot + h, kEmptySlot, want);
+            if (cur == kEmptySlot) cur = want;
+            else p.dkey[idx] = kEmptyKey;   // lost the race: the entry stays a hole with count 0
         }
-        if (cur == key) return atomicAdd(p.tcnt + h, c) + c;
+        if ((uint32_t)(cur >> 32) == key) return atomicAdd(p.dcnt + (uint32_t)cur, delta) + delta;
         h = (h + probe) & p.tmask;
     }
     atomicOr(&p.st->err, DERR_TABLE_FULL);
     return 0;
 }
 
-__device__ __forceinline__ void smem_add(uint32_t *skey, uint32_t *scnt, uint32_t *socc, const TrainParams &p,
-                                         uint32_t *list, uint32_t *list_len, uint32_t key,
-                                         unsigned long long &mybest) {
-    uint32_t h = fmix32(key) & (kCountSlots - 1);
+// Shared-memory accumulation; returns true when the key found no room in a
+// crowded neighbourhood (the caller then adds it globally).
+template <int SLOTS>
+__device__ __forceinline__ bool smem_add(uint32_t *skey, uint32_t *sval, uint32_t *socc, uint32_t key, uint32_t delta) {
+    uint32_t h = fmix32(key) & (SLOTS - 1);
 #pragma unroll 1
     for (uint32_t probe = 1; probe <= 16; ++probe) {
         uint32_t cur = ((volatile uint32_t *)skey)[h];
@@ -121,18 +157,17 @@ __device__ __forceinline__ void smem_add(uint32_t *skey, uint32_t *scnt, uint32_
             }
         }
         if (cur == key) {
-            atomicAdd(scnt + h, 1u);
-            return;
+            atomicAdd(sval + h, delta);
+            return false;
         }
-        h = (h + probe) & (kCountSlots - 1);
+        h = (h + probe) & (SLOTS - 1);
     }
-    // local table crowded around this key: count it globally right away
-    uint32_t tot = table_add(p, list, list_len, key, 1u);
-    unsigned long long b = pack_best(tot, key);
-    mybest = b > mybest ? b : mybest;
+    return true;
 }
 
-__global__ void __launch_bounds__(kCountThreads) k_count(TrainParams p, uint32_t it) {
+// ------------------------------------------------------------ pair count ---
+
+__global__ void __launch_bounds__(kCountThreads) k_count(TrainParams p) {
     extern __shared__ uint32_t smem[];
     uint32_t *skey = smem;
     uint32_t *scnt = smem + kCountSlots;
@@ -140,15 +175,10 @@ __global__ void __launch_bounds__(kCountThreads) k_count(TrainParams p, uint32_t
     __shared__ unsigned long long sbest[kCountThreads / 32];
 
     TrainState *st = p.st;
-    const uint32_t k = st->k_base + it;
-    if (k >= st->n_merges || st->err) return;
-    if (k > 0 && (p.best[k - 1] >> 32) == 0) return;  // training has stopped
-    const uint64_t n = st->n[k & 1];
-    const uint32_t *s = (k & 1) ? p.buf[1] : p.buf[0];
-    uint32_t *list = (k & 1) ? p.list[1] : p.list[0];
-    uint32_t *list_len = &st->list_len[k & 1];
-    const int tid = threadIdx.x;
-    if (blockIdx.x == 0 && tid == 0) st->list_len[(k + 1) & 1] = 0;
+    if (st->n_merges == 0 || st->err) return;
+    const uint64_t n = st->n[0];
+    const uint32_t *s = p.buf[0];
+    const int tid = threadIdx.x, lane = tid & 31;
 
     for (int j = tid; j < kCountSlots; j += kCountThreads) {
         skey[j] = kEmptyKey;
@@ -158,79 +188,247 @@ __global__ void __launch_bounds__(kCountThreads) k_count(TrainParams p, uint32_t
     __syncthreads();
 
     unsigned long long mybest = 0;
-    for (uint64_t base = (uint64_t)blockIdx.x * kCountTile; base < n; base += (uint64_t)gridDim.x * kCountTile) {
-        const uint64_t pos = base + 4ull * tid;
-        if (pos + 1 < n) {
-            // 128-bit load of 4 symbols plus the next one (the buffer is padded)
-            const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(s + pos));
-            const uint32_t a[5] = {v.x, v.y, v.z, v.w, __ldcs(s + pos + 4)};
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                if (pos + j + 1 < n && !(a[j + 1] & kWordStart)) {
-                    const uint32_t key = ((a[j] & 0xFFFFu) << 16) | (a[j + 1] & 0xFFFFu);
-                    smem_add(skey, scnt, &socc, p, list, list_len, key, mybest);
-                }
-            }
-        }
-        if (__syncthreads_or(tid == 0 && socc > kCountSlots / 2)) {
-            for (int j = tid; j < kCountSlots; j += kCountThreads) {
-                const uint32_t key = skey[j];
-                if (key != kEmptyKey) {
-                    const uint32_t tot = table_add(p, list, list_len, key, scnt[j]);
-                    const unsigned long long b = pack_best(tot, key);
-                    mybest = b > mybest ? b : mybest;
+    auto flush = [&](bool clear) {
+        for (int j = tid; j < kCountSlots; j += kCountThreads) {
+            const uint32_t key = skey[j];
+            if (key != kEmptyKey) {
+                const uint32_t tot = global_add(table_of(p), key, scnt[j]);
+                const unsigned long long b = pack_best(tot, key);
+                mybest = b > mybest ? b : mybest;
+                if (clear) {
                     skey[j] = kEmptyKey;
                     scnt[j] = 0;
                 }
             }
+        }
+    };
+    for (uint64_t base = (uint64_t)blockIdx.x * kCountTile; base < n; base += (uint64_t)gridDim.x * kCountTile) {
+        const uint64_t pos = base + (uint64_t)kCountItems * tid;
+        uint32_t a[kCountItems + 1];
+        uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+        if (pos < n) {   // the buffer is padded: 8 symbols past pos are readable
+            v0 = __ldcs(reinterpret_cast<const uint4 *>(s + pos));
+            v1 = __ldcs(reinterpret_cast<const uint4 *>(s + pos + 4));
+        }
+        a[0] = v0.x; a[1] = v0.y; a[2] = v0.z; a[3] = v0.w;
+        a[4] = v1.x; a[5] = v1.y; a[6] = v1.z; a[7] = v1.w;
+        uint32_t nx = __shfl_down_sync(kFull, v0.x, 1);
+        if (lane == 31) nx = (pos + kCountItems < n) ? __ldcs(s + pos + kCountItems) : kWordStart;
+        a[8] = nx;
+#pragma unroll
+        for (int j = 0; j < kCountItems; j++) {
+            if (pos + j + 1 < n && !(a[j + 1] & kWordStart)) {
+                const uint32_t key = pair_key(a[j], a[j + 1]);
+                if (smem_add<kCountSlots>(skey, scnt, &socc, key, 1u)) {
+                    const uint32_t tot = global_add(table_of(p), key, 1u);
+                    const unsigned long long b = pack_best(tot, key);
+                    mybest = b > mybest ? b : mybest;
+                }
+            }
+        }
+        if (__syncthreads_or(tid == 0 && socc > kCountSlots / 2)) {
+            flush(true);
             if (tid == 0) socc = 0;
             __syncthreads();
         }
     }
     __syncthreads();
-    for (int j = tid; j < kCountSlots; j += kCountThreads) {
-        const uint32_t key = skey[j];
-        if (key != kEmptyKey) {
-            const uint32_t tot = table_add(p, list, list_len, key, scnt[j]);
-            const unsigned long long b = pack_best(tot, key);
-            mybest = b > mybest ? b : mybest;
-        }
-    }
+    flush(false);
     mybest = warp_max_u64(mybest);
-    if ((tid & 31) == 0) sbest[tid >> 5] = mybest;
+    if (lane == 0) sbest[tid >> 5] = mybest;
     __syncthreads();
     if (tid < 32) {
         unsigned long long b = tid < kCountThreads / 32 ? sbest[tid] : 0ull;
         b = warp_max_u64(b);
-        if (tid == 0 && b) atomicMax(p.best + k, b);
+        if (tid == 0 && b) atomicMax(p.best, b);
+    }
+}
+
+// ---------------------------------------------------------------- argmax ---
+
+__global__ void __launch_bounds__(kArgmaxThreads) k_argmax(TrainParams p, uint32_t it) {
+    __shared__ unsigned long long sbest[kArgmaxThreads / 32];
+    TrainState *st = p.st;
+    const uint32_t k = st->k_base + it;
+    if (k == 0 || k >= st->n_merges || st->err) return;
+    if ((p.best[k - 1] >> 32) == 0) return;   // training has stopped
+    const uint32_t D = st->dense_len;
+    if (blockIdx.x == 0 && threadIdx.x == 0) p.dhist[k] = D;
+    unsigned long long b = 0;
+    for (uint32_t i = blockIdx.x * kArgmaxThreads + threadIdx.x; i < D; i += gridDim.x * kArgmaxThreads) {
+        const uint32_t c = __ldcg(p.dcnt + i);
+        if (c != 0) {
+            const unsigned long long v = pack_best(c, __ldcg(p.dkey + i));
+            b = v > b ? v : b;
+        }
+    }
+    b = warp_max_u64(b);
+    if ((threadIdx.x & 31) == 0) sbest[threadIdx.x >> 5] = b;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        unsigned long long x = threadIdx.x < kArgmaxThreads / 32 ? sbest[threadIdx.x] : 0ull;
+        x = warp_max_u64(x);
+        if (threadIdx.x == 0 && x) atomicMax(p.best + k, x);
     }
 }
 
 // -------------------------------------------------------- merge + compact ---
 
 // 1-bit transducers: bit x of f is f(x).
-constexpr uint32_t kFId = 2u, kFNeg = 1u, kFZero = 0u;
+constexpr uint32_t kFId = 2u;   // identity; 1 = negate, 0 = constant zero
 __device__ __forceinline__ uint32_t fapply(uint32_t f, uint32_t x) { return (f >> x) & 1u; }
-// g after f
-__device__ __forceinline__ uint32_t fcomp(uint32_t g, uint32_t f) {
+__device__ __forceinline__ uint32_t fcomp(uint32_t g, uint32_t f) {   // g after f
     return fapply(g, f & 1u) | (fapply(g, (f >> 1) & 1u) << 1);
 }
 
+// A summary of consecutive items packed in 32 bits: transducer f (2 bits),
+// kept symbols for incoming parity 0 (15 bits) and 1 (15 bits).
+constexpr uint32_t kSumId = kFId;
+__device__ __forceinline__ uint32_t sum_pack(uint32_t f, uint32_t k0, uint32_t k1) { return f | (k0 << 2) | (k1 << 17); }
+// b after a
+__device__ __forceinline__ uint32_t sum_comp(uint32_t b, uint32_t a) {
+    const uint32_t fa = a & 3u, fb = b & 3u;
+    const uint32_t a0 = (a >> 2) & 0x7FFFu, a1 = a >> 17, b0 = (b >> 2) & 0x7FFFu, b1 = b >> 17;
+    return sum_pack(fcomp(fb, fa), a0 + (fapply(fa, 0) ? b1 : b0), a1 + (fapply(fa, 1) ? b1 : b0));
+}
+
 // Look-back status words.
-//   aggregate: 1 | F << 2 | kept(carry 0) << 4 | kept(carry 1) << 34
+//   aggregate: 1 | f << 2 | kept(parity 0) << 4 | kept(parity 1) << 34
 //   inclusive: 2 | parity << 2 | prefix << 4
-__device__ __forceinline__ unsigned long long agg_word(uint32_t f, uint32_t k0, uint32_t k1) {
-    return 1ull | ((unsigned long long)f << 2) | ((unsigned long long)k0 << 4) | ((unsigned long long)k1 << 34);
+__device__ __forceinline__ unsigned long long agg_word(uint32_t sum) {
+    return 1ull | ((unsigned long long)(sum & 3u) << 2) | ((unsigned long long)((sum >> 2) & 0x7FFFu) << 4) |
+           ((unsigned long long)(sum >> 17) << 34);
 }
 __device__ __forceinline__ unsigned long long inc_word(uint32_t par, unsigned long long prefix) {
     return 2ull | ((unsigned long long)par << 2) | (prefix << 4);
 }
 
-__global__ void __launch_bounds__(kMergeThreads) k_merge(TrainParams p, uint32_t it) {
-    __shared__ uint32_t s_wfun[kMergeWarps];
+// Summary of many tiles in 64 bits: f (2 bits) | kept(parity 0) << 2 (31 bits)
+// | kept(parity 1) << 33 (31 bits).  Identity: f = identity, counts 0.
+__device__ __forceinline__ unsigned long long lsum_from_agg(unsigned long long w) {
+    return ((w >> 2) & 3ull) | (((w >> 4) & 0x3FFFFFFFull) << 2) | (((w >> 34) & 0x3FFFFFFFull) << 33);
+}
+// b after a
+__device__ __forceinline__ unsigned long long lsum_comp(unsigned long long b, unsigned long long a) {
+    const uint32_t fa = (uint32_t)a & 3u, fb = (uint32_t)b & 3u;
+    const unsigned long long a0 = (a >> 2) & 0x7FFFFFFFull, a1 = a >> 33, b0 = (b >> 2) & 0x7FFFFFFFull, b1 = b >> 33;
+    const unsigned long long k0 = a0 + (fapply(fa, 0) ? b1 : b0), k1 = a1 + (fapply(fa, 1) ? b1 : b0);
+    return (unsigned long long)fcomp(fb, fa) | (k0 << 2) | (k1 << 33);
+}
+
+// Warp-wide decoupled look-back for tile t (all 32 lanes call it).  Lane L
+// reads the 8 status words of tiles jhi-8L-7 .. jhi-8L, so one round trip
+// covers 256 predecessors; summaries are composed by a tree reduction.
+// Returns false when the bounded wait gives up.
+__device__ __forceinline__ bool lookback(const unsigned long long *status, uint64_t t, int lane, uint32_t *carry,
+                         unsigned long long *off) {
+    constexpr int kPer = 8;
+    unsigned long long g = kFId;   // tiles newer than the current window, composed
+    long long jhi = (long long)t - 1;
+    unsigned spins = 0;
+    for (;;) {
+        unsigned long long w[kPer];
+#pragma unroll
+        for (int q = 0; q < kPer; q++) {   // q = 0 is the newest tile of this lane
+            const long long j = jhi - kPer * lane - q;
+            w[q] = (j >= 0) ? ld_relaxed(status + j) : inc_word(0, 0);
+        }
+        int qi = kPer;                      // newest inclusive of this lane
+        bool ready = true;
+#pragma unroll
+        for (int q = kPer - 1; q >= 0; q--)
+            if ((w[q] & 3ull) == 2) qi = q;
+#pragma unroll
+        for (int q = 0; q < kPer; q++)
+            if (q <= qi && (w[q] & 3ull) == 0) ready = false;
+        const unsigned incl_m = __ballot_sync(kFull, qi < kPer);
+        const int Ls = incl_m ? __ffs(incl_m) - 1 : 32;   // first lane holding an inclusive
+        const unsigned need = (Ls >= 31) ? kFull : ((2u << Ls) - 1u);
+        if (__ballot_sync(kFull, !ready) & need) {
+            if (++spins > kSpinLimit) return false;
+            if (spins > 16) __nanosleep(32);
+            continue;
+        }
+        // this lane's aggregates, oldest first (those newer than its inclusive)
+        unsigned long long mine = kFId;
+#pragma unroll
+        for (int q = kPer - 1; q >= 0; q--)
+            if (q < qi) mine = lsum_comp(lsum_from_agg(w[q]), mine);
+        // ordered tree reduction over lanes 0 .. Ls-1 (higher lane = older)
+        const int span = Ls < 32 ? Ls : 32;
+        unsigned long long x = (lane < span) ? mine : (unsigned long long)kFId;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const unsigned long long y = __shfl_down_sync(kFull, x, d);
+            if (lane + d < span) x = lsum_comp(x, y);
+        }
+        const unsigned long long newer = __shfl_sync(kFull, x, 0);   // lanes 0 .. span-1 composed
+        if (Ls < 32) {
+            // inclusive of lane Ls at its qi, then its newer aggregates, then lanes < Ls, then g
+            unsigned long long wi = 0, part = 0;
+            int q_i = __shfl_sync(kFull, qi, Ls);
+            part = __shfl_sync(kFull, mine, Ls);
+#pragma unroll
+            for (int q = 0; q < kPer; q++) {
+                const unsigned long long v = __shfl_sync(kFull, w[q], Ls);
+                if (q == q_i) wi = v;
+            }
+            uint32_t par = (uint32_t)(wi >> 2) & 1u;
+            unsigned long long o = wi >> 4;
+            const unsigned long long chain = lsum_comp(g, lsum_comp(newer, part));
+            o += par ? (chain >> 33) : ((chain >> 2) & 0x7FFFFFFFull);
+            *carry = fapply((uint32_t)chain & 3u, par);
+            *off = o;
+            return true;
+        }
+        g = lsum_comp(g, newer);
+        jhi -= 32 * kPer;
+    }
+}
+
+// Count deltas of one thread's 16 positions (rare: only where a merge happened
+// nearby).  mm: bit j = m(pos+j) for j = 0..17; mprev = m(pos-1); sym(j) reads
+// symbol pos+j from the padded tile.
+__device__ __noinline__ void thread_deltas(const Table p, uint32_t *dkey, uint32_t *dval, uint32_t *socc,
+                                           const uint32_t *mys, uint64_t pos, uint64_t n, uint32_t mm,
+                                           uint32_t mprev, uint32_t new_id) {
+    auto sym = [&](int j) { return mys[j < 16 ? j : j + 1]; };
+    auto add = [&](uint32_t kk, uint32_t d) {
+        if (smem_add<kDeltaSlots>(dkey, dval, socc, kk, d)) global_add(p, kk, d);
+    };
+    const uint32_t mext = (mm << 1) | mprev;           // bit j: m(pos+j-1)
+    // old pairs (j, j+1) touched by a merge at j-1, j or j+1
+    uint32_t told = (mext | mm | (mm >> 1)) & 0xFFFFu;
+    while (told) {
+        const int j = __ffs(told) - 1;
+        told &= told - 1;
+        if (pos + j + 1 >= n) break;
+        const uint32_t b = sym(j + 1);
+        if (!(b & kWordStart)) add(pair_key(sym(j), b), 0xFFFFFFFFu);
+    }
+    // new pairs at kept positions j whose own or next kept symbol merged
+    uint32_t tnew = ~mext & (mm | (mm >> 1)) & 0xFFFFu;
+    while (tnew) {
+        const int j = __ffs(tnew) - 1;
+        tnew &= tnew - 1;
+        if (pos + j >= n) break;
+        const uint32_t mj = (mm >> j) & 1u;
+        const int nk = j + 1 + (int)mj;
+        if (pos + nk >= n) continue;
+        const uint32_t b = sym(nk);
+        if (b & kWordStart) continue;
+        const uint32_t mk = (mm >> nk) & 1u;
+        add(pair_key(mj ? new_id : sym(j), mk ? new_id : b), 1u);
+    }
+}
+
+__global__ void __launch_bounds__(kMergeThreads, 4) k_merge(TrainParams p, uint32_t it) {
+    extern __shared__ uint32_t dsm[];
+    uint32_t *stile = dsm;                                // the tile and its halo (padded)
+    uint32_t *dkey = dsm + kTileWords;                    // shared delta table
+    uint32_t *dval = dkey + kDeltaSlots;
     __shared__ uint32_t s_wsum[kMergeWarps];
-    __shared__ uint32_t s_tile;
-    __shared__ uint32_t s_carry;
+    __shared__ uint32_t s_tile, s_carry, s_docc, s_tilesum;
     __shared__ unsigned long long s_off;
 
     TrainState *st = p.st;
@@ -246,121 +444,123 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge(TrainParams p, uint32_t
     unsigned long long *status = (k & 1) ? p.status[1] : p.status[0];
     unsigned long long *next_status = (k & 1) ? p.status[0] : p.status[1];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (blockIdx.x == 0 && tid == 0) st->ticket[(k + 1) & 1] = 0;
-
-    // clear the global-table slots k_count used in this iteration
-    const uint32_t used = st->list_len[k & 1];
-    const uint32_t *list = (k & 1) ? p.list[1] : p.list[0];
-    for (uint32_t j = blockIdx.x * kMergeThreads + tid; j < used; j += gridDim.x * kMergeThreads) {
-        const uint32_t h = list[j];
-        p.tkey[h] = kEmptyKey;
-        p.tcnt[h] = 0;
-    }
-
     const uint64_t ntiles = (n + kMergeTile - 1) / kMergeTile;
-    for (;;) {
-        if (tid == 0) s_tile = atomicAdd(&st->ticket[k & 1], 1u);
-        __syncthreads();
-        const uint64_t t = s_tile;
-        if (t >= ntiles) break;
-        if (tid == 0) next_status[t] = 0ull;
 
-        const uint64_t pos = t * kMergeTile + 4ull * tid;
-        uint32_t a[5] = {0, 0, 0, 0, 0};
-        if (pos < n) {
-            const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(in + pos));
-            a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
-            a[4] = __ldcs(in + pos + 4);
-        }
-        uint32_t valid = 0, fthr = kFId;
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const bool vj = (pos + j + 1 < n) && (a[j] & 0xFFFFu) == l && (a[j + 1] & 0xFFFFu) == r &&
-                            !(a[j + 1] & kWordStart);
-            valid |= (uint32_t)vj << j;
-            fthr = fcomp(vj ? kFNeg : kFZero, fthr);
-        }
-        // exclusive scan of transducers (warp shuffles, then across warps)
-        uint32_t fin = fthr;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const uint32_t o = __shfl_up_sync(kFull, fin, d);
-            if (lane >= d) fin = fcomp(fin, o);
-        }
-        uint32_t fex = __shfl_up_sync(kFull, fin, 1);
-        if (lane == 0) fex = kFId;
-        if (lane == 31) s_wfun[warp] = fin;
-        __syncthreads();
-        uint32_t wpre = kFId, tilef = kFId;
-        for (int w = 0; w < kMergeWarps; w++) {   // 16 composes, identical in every thread
-            const uint32_t g = s_wfun[w];
-            if (w < warp) wpre = fcomp(g, wpre);
-            tilef = fcomp(g, tilef);
-        }
-        fex = fcomp(fex, wpre);
+    // one tile per CTA, in ticket order (a tile only waits on tiles that run)
+    if (tid == 0) {
+        s_tile = atomicAdd(&st->ticket[k & 1], 1u);
+        s_docc = 0;
+        if (blockIdx.x == 0) st->ticket[(k + 1) & 1] = 0;
+    }
+    __syncthreads();
+    const uint64_t t = s_tile;
+    if (t >= ntiles) return;
+    if (tid == 0) next_status[t] = 0ull;
+    const uint64_t base = t * kMergeTile;
+    const uint32_t tile_len = (n - base < (uint64_t)kMergeTile) ? (uint32_t)(n - base) : (uint32_t)kMergeTile;
 
-        // kept symbols under both possible carries, packed 16 | 16 bits
-        uint32_t packed = 0;
+    // coalesced 128-bit loads of the tile and its halo into shared memory
+#pragma unroll
+    for (int q = 0; q < (kMergeTile + kTileHalo) / (4 * kMergeThreads) + 1; q++) {
+        const int i4 = tid + q * kMergeThreads;
+        if (i4 < (kMergeTile + kTileHalo) / 4) {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (base + 4ull * i4 < n) v = __ldcs(reinterpret_cast<const uint4 *>(in + base + 4ull * i4));
+            uint32_t *d = stile + padded(4 * i4);   // 4 symbols never straddle a padding word
+            d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+        }
+    }
+    __syncthreads();
+
+    // valid starts among this thread's 16 positions and the 2 after them
+    const uint64_t pos = base + (uint64_t)kMergeItems * tid;
+    const uint32_t *mys = stile + padded(kMergeItems * tid);
+    uint32_t valid = 0;   // bit j: position pos + j is a valid start, j = 0 .. 17
+    {
+        uint32_t isl = 0, isr = 0;   // id == l ; id == r without WORD_START
+#pragma unroll
+        for (int j = 0; j < kMergeItems + 3; j++) {
+            const uint32_t x = mys[j < 16 ? j : j + 1];
+            isl |= (uint32_t)((x & 0xFFFFu) == l) << j;
+            isr |= (uint32_t)((x & 0x1FFFFu) == r) << j;
+        }
+        valid = isl & (isr >> 1) & 0x3FFFFu;
+        const uint64_t lim = n - pos;   // positions pos+j with j + 1 < lim
+        if (lim < kMergeItems + 3) valid &= (lim >= 1) ? ((1u << (uint32_t)(lim - 1)) - 1u) : 0u;
+    }
+    // A tile takes the full path when it owns a valid start, or when the next
+    // tile's first position is one: the merge there removes the pair (last,
+    // first) and creates (last, new symbol), deltas this tile owes.
+    const bool any = __syncthreads_or((valid & (tid == kMergeThreads - 1 ? 0x1FFFFu : 0xFFFFu)) != 0);
+
+    uint32_t excl = kSumId;   // summary of this tile's items before this thread
+    if (!any) {
+        // no valid start owned by the tile: parity is 0 after every item, only
+        // the first symbol can be consumed (by a merge at the end of the tile before)
+        if (tid == 0) s_tilesum = sum_pack(0u, tile_len, tile_len - 1);
+    } else {
+        for (int j = tid; j < kDeltaSlots; j += kMergeThreads) {   // fenced by the barriers below
+            dkey[j] = kEmptyKey;
+            dval[j] = 0;
+        }
+        uint32_t kept[2], fout[2];
 #pragma unroll
         for (uint32_t c = 0; c < 2; c++) {
-            uint32_t par = fapply(fex, c), kept = 0;
+            uint32_t par = c, kc = 0;
 #pragma unroll
-            for (int j = 0; j < 4; j++) {
-                if (pos + j < n) kept += par ^ 1u;
+            for (int j = 0; j < kMergeItems; j++) {
+                if (pos + j < n) kc += par ^ 1u;
                 par = ((valid >> j) & 1u) ? (par ^ 1u) : 0u;
             }
-            packed |= kept << (16 * c);
+            kept[c] = kc;
+            fout[c] = par;
         }
-        const uint32_t pin = warp_incl_sum(packed, lane);
-        if (lane == 31) s_wsum[warp] = pin;
+        const uint32_t mine = sum_pack(fout[0] | (fout[1] << 1), kept[0], kept[1]);
+        uint32_t incl = mine;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t o = __shfl_up_sync(kFull, incl, d);
+            if (lane >= d) incl = sum_comp(incl, o);
+        }
+        excl = __shfl_up_sync(kFull, incl, 1);
+        if (lane == 0) excl = kSumId;
+        if (lane == 31) s_wsum[warp] = incl;
         __syncthreads();
-        uint32_t wsum = 0, tsum = 0;
-        for (int w = 0; w < kMergeWarps; w++) {
-            const uint32_t g = s_wsum[w];
-            if (w < warp) wsum += g;
-            tsum += g;
-        }
-        const uint32_t pex = pin - packed + wsum;
-
-        if (tid == 0) {
-            const uint32_t k0 = tsum & 0xFFFFu, k1 = tsum >> 16;
-            uint32_t carry = 0;
-            unsigned long long off = 0;
-            if (t > 0) {
-                st_relaxed(status + t, agg_word(tilef, k0, k1));
-                uint32_t gf = kFId;
-                unsigned long long g0 = 0, g1 = 0;
-                uint64_t j = t - 1;
-                unsigned spins = 0;
-                for (;;) {
-                    const unsigned long long w = ld_relaxed(status + j);
-                    const uint32_t flag = (uint32_t)(w & 3ull);
-                    if (flag == 0) {
-                        if (++spins > kSpinLimit) {
-                            atomicOr(&st->err, DERR_TIMEOUT);
-                            break;
-                        }
-                        if (spins > 64) __nanosleep(64);
-                        continue;
-                    }
-                    if (flag == 2) {
-                        const uint32_t par = (uint32_t)(w >> 2) & 1u;
-                        off = (w >> 4) + (par ? g1 : g0);
-                        carry = fapply(gf, par);
-                        break;
-                    }
-                    const uint32_t af = (uint32_t)(w >> 2) & 3u;
-                    const unsigned long long a0 = (w >> 4) & 0x3FFFFFFFull, a1 = (w >> 34) & 0x3FFFFFFFull;
-                    const unsigned long long n0 = a0 + (fapply(af, 0) ? g1 : g0);
-                    const unsigned long long n1 = a1 + (fapply(af, 1) ? g1 : g0);
-                    gf = fcomp(gf, af);
-                    g0 = n0;
-                    g1 = n1;
-                    --j;
-                }
+        if (warp == 0) {   // exclusive scan of the 8 warp totals
+            uint32_t w = lane < kMergeWarps ? s_wsum[lane] : kSumId, wi = w;
+#pragma unroll
+            for (int d = 1; d < kMergeWarps; d <<= 1) {
+                const uint32_t o = __shfl_up_sync(kFull, wi, d);
+                if (lane >= d) wi = sum_comp(wi, o);
             }
-            const unsigned long long total = off + (carry ? k1 : k0);
-            st_relaxed(status + t, inc_word(fapply(tilef, carry), total));
+            uint32_t we = __shfl_up_sync(kFull, wi, 1);
+            if (lane == 0) we = kSumId;
+            __syncwarp();
+            if (lane < kMergeWarps) s_wsum[lane] = we;
+            if (lane == kMergeWarps - 1) s_tilesum = wi;
+        }
+        __syncthreads();
+        excl = sum_comp(excl, s_wsum[warp]);
+    }
+    __syncthreads();
+    const uint32_t tile = s_tilesum;
+
+    // warp 0: publish the aggregate, look back over 256 predecessors per round trip
+    if (warp == 0) {
+        uint32_t carry = 0;
+        unsigned long long off = 0;
+        if (t > 0) {
+            if (lane == 0) st_relaxed(status + t, agg_word(tile));
+            if (!lookback(status, t, lane, &carry, &off)) {
+                if (lane == 0) atomicOr(&st->err, DERR_TIMEOUT);
+                carry = 0;
+                off = 0;
+            }
+        }
+        if (lane == 0) {
+            const uint32_t t0 = (tile >> 2) & 0x7FFFu, t1 = tile >> 17;
+            const unsigned long long total = off + (carry ? t1 : t0);
+            st_relaxed(status + t, inc_word(fapply(tile & 3u, carry), total));
             if (t == ntiles - 1) {
                 st->n[(k + 1) & 1] = total;
                 p.nhist[k + 1] = total;
@@ -368,18 +568,50 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge(TrainParams p, uint32_t
             s_carry = carry;
             s_off = off;
         }
-        __syncthreads();
+    }
+    __syncthreads();
+    const uint32_t carry = s_carry;
+    const unsigned long long obase = s_off;
 
-        const uint32_t carry = s_carry;
-        uint64_t o = s_off + ((pex >> (16 * carry)) & 0xFFFFu);
-        uint32_t par = fapply(fex, carry);
+    if (!any) {
+        // shifted copy; a merge at the end of the previous tile consumed symbol 0
+        for (uint32_t i = tid; i + carry < tile_len; i += kMergeThreads) out[obase + i] = stile[padded(i + carry)];
+        if (carry && tid == 0 && base + 1 < n && !(stile[1] & kWordStart))
+            global_add(table_of(p), pair_key(stile[0], stile[1]), 0xFFFFFFFFu);
+        return;
+    }
+
+    // merge flags m(pos-1 .. pos+17) under the real carry
+    uint32_t par = fapply(excl & 3u, carry);
+    const uint32_t mprev = par;   // m(pos-1)
+    uint32_t mm = 0;              // bit j: m(pos+j)
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const uint32_t npar = ((valid >> j) & 1u) ? (par ^ 1u) : 0u;
-            if (pos + j < n && !par) out[o++] = npar ? (new_id | (a[j] & kWordStart)) : a[j];
-            par = npar;
+    for (int j = 0; j < kMergeItems + 2; j++) {
+        par = ((valid >> j) & 1u) ? (par ^ 1u) : 0u;
+        mm |= par << j;
+    }
+    if ((mm | mprev) & 0x1FFFFu)   // some merge touches this thread's pairs
+        thread_deltas(table_of(p), dkey, dval, &s_docc, mys, pos, n, mm, mprev, new_id);
+    const uint32_t mext = (mm << 1) | mprev;   // bit j: position pos+j consumed
+    uint32_t outv[kMergeItems];
+#pragma unroll
+    for (int j = 0; j < kMergeItems; j++) {
+        const uint32_t x = mys[j];
+        outv[j] = ((mm >> j) & 1u) ? (new_id | (x & kWordStart)) : x;
+    }
+    uint32_t e = carry ? (excl >> 17) : ((excl >> 2) & 0x7FFFu);   // tile-local output index
+    const uint32_t tile_kept = carry ? (tile >> 17) : ((tile >> 2) & 0x7FFFu);
+    __syncthreads();   // every symbol of the tile is in registers: the tile buffer is free
+#pragma unroll
+    for (int j = 0; j < kMergeItems; j++)
+        if (pos + j < n && !((mext >> j) & 1u)) stile[padded(e++)] = outv[j];
+    __syncthreads();
+    for (uint32_t i = tid; i < tile_kept; i += kMergeThreads) out[obase + i] = stile[padded(i)];
+    if (s_docc) {
+        for (int j = tid; j < kDeltaSlots; j += kMergeThreads) {
+            const uint32_t kk = dkey[j];
+            if (kk != kEmptyKey && dval[j]) global_add(table_of(p), kk, dval[j]);
         }
-        __syncthreads();   // shared words are reused by the next tile
     }
 }
 
@@ -393,41 +625,38 @@ uint32_t ceil_log2(uint64_t x) {
 
 struct Launch {
     TrainParams p;
-    unsigned count_grid, merge_grid;
-    size_t count_smem;
+    unsigned count_grid, merge_grid, argmax_grid;
+    size_t count_smem, merge_smem;
 };
 
 int occupancy(bpe_ctx *ctx, int *count_blocks, int *merge_blocks) {
-    static int cached_count = 0, cached_merge = 0;
-    if (!cached_count) {
-        const size_t smem = 2 * kCountSlots * sizeof(uint32_t);
-        BPE_CUDA(ctx, cudaFuncSetAttribute(k_count, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
-                 "k_count smem attribute");
-        BPE_CUDA(ctx, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_count, k_count, kCountThreads, smem),
-                 "k_count occupancy");
-        BPE_CUDA(ctx, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached_merge, k_merge, kMergeThreads, 0),
-                 "k_merge occupancy");
-        if (cached_count < 1) cached_count = 1;
-        if (cached_merge < 1) cached_merge = 1;
-    }
-    *count_blocks = cached_count;
-    *merge_blocks = cached_merge;
+    const size_t csm = 2 * kCountSlots * sizeof(uint32_t),
+                 msm = (kTileWords + 2 * kDeltaSlots) * sizeof(uint32_t);
+    BPE_CUDA(ctx, cudaFuncSetAttribute(k_count, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm),
+             "k_count smem attribute");
+    BPE_CUDA(ctx, cudaFuncSetAttribute(k_merge, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msm),
+             "k_merge smem attribute");
+    BPE_CUDA(ctx, cudaOccupancyMaxActiveBlocksPerMultiprocessor(count_blocks, k_count, kCountThreads, csm),
+             "k_count occupancy");
+    BPE_CUDA(ctx, cudaOccupancyMaxActiveBlocksPerMultiprocessor(merge_blocks, k_merge, kMergeThreads, msm),
+             "k_merge occupancy");
+    *count_blocks = std::max(*count_blocks, 1);
+    *merge_blocks = std::max(*merge_blocks, 1);
     return BPE_OK;
 }
 
-int launch_iteration(bpe_ctx *ctx, const Launch &L, uint32_t it, cudaStream_t s) {
-    k_count<<<L.count_grid, kCountThreads, L.count_smem, s>>>(L.p, it);
-    k_merge<<<L.merge_grid, kMergeThreads, 0, s>>>(L.p, it);
-    return BPE_OK;
+void launch_iteration(const Launch &L, uint32_t it, cudaStream_t s) {
+    k_argmax<<<L.argmax_grid, kArgmaxThreads, 0, s>>>(L.p, it);
+    k_merge<<<L.merge_grid, kMergeThreads, L.merge_smem, s>>>(L.p, it);
 }
 
 // Capture (or reuse) a graph of kGraphIters iterations plus the k_base advance.
 int get_graph(bpe_ctx *ctx, const Launch &L, cudaGraphExec_t *out) {
     std::vector<uintptr_t> key = {
-        (uintptr_t)L.p.buf[0], (uintptr_t)L.p.buf[1], (uintptr_t)L.p.tkey, (uintptr_t)L.p.tcnt,
-        (uintptr_t)L.p.tmask, (uintptr_t)L.p.list[0], (uintptr_t)L.p.list[1], (uintptr_t)L.p.status[0],
-        (uintptr_t)L.p.status[1], (uintptr_t)L.p.best, (uintptr_t)L.p.nhist, (uintptr_t)L.p.st,
-        (uintptr_t)L.count_grid, (uintptr_t)L.merge_grid};
+        (uintptr_t)L.p.buf[0], (uintptr_t)L.p.buf[1], (uintptr_t)L.p.tslot, (uintptr_t)L.p.tmask,
+        (uintptr_t)L.p.dkey, (uintptr_t)L.p.dcnt, (uintptr_t)L.p.dcap, (uintptr_t)L.p.status[0],
+        (uintptr_t)L.p.status[1], (uintptr_t)L.p.best, (uintptr_t)L.p.nhist, (uintptr_t)L.p.dhist,
+        (uintptr_t)L.p.st, (uintptr_t)L.merge_grid, (uintptr_t)L.argmax_grid};
     if (ctx->graph.exec && ctx->graph.key == key) {
         *out = ctx->graph.exec;
         return BPE_OK;
@@ -438,7 +667,7 @@ int get_graph(bpe_ctx *ctx, const Launch &L, cudaGraphExec_t *out) {
     }
     cudaStream_t cs = ctx->capture_stream;
     BPE_CUDA(ctx, cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal), "begin capture");
-    for (uint32_t i = 0; i < kGraphIters; i++) launch_iteration(ctx, L, i, cs);
+    for (uint32_t i = 0; i < kGraphIters; i++) launch_iteration(L, i, cs);
     k_advance<<<1, 1, 0, cs>>>(L.p.st, kGraphIters);
     cudaGraph_t g = nullptr;
     cudaError_t e = cudaStreamEndCapture(cs, &g);
@@ -458,25 +687,28 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     cudaStream_t s = ctx->stream;
     const uint64_t T = 1ull << table_log2;
     const uint64_t ntiles = (n + kMergeTile - 1) / kMergeTile;
-    void *buf0, *buf1, *tkey, *tcnt, *l0, *l1, *st0, *st1, *best, *state, *nhist;
+    void *buf0, *buf1, *tslot, *dense, *st0, *st1, *best, *state, *nhist, *dhist;
     int rc;
     if ((rc = ensure(ctx, S_TRAIN_BUF0, (n + kPadSymbols) * 4, &buf0)) ||
         (rc = ensure(ctx, S_TRAIN_BUF1, (n + kPadSymbols) * 4, &buf1)) ||
-        (rc = ensure(ctx, S_TABLE_KEY, T * 4, &tkey)) || (rc = ensure(ctx, S_TABLE_CNT, T * 4, &tcnt)) ||
-        (rc = ensure(ctx, S_LIST0, T * 4, &l0)) || (rc = ensure(ctx, S_LIST1, T * 4, &l1)) ||
+        (rc = ensure(ctx, S_TABLE_KEY, T * 8, &tslot)) || (rc = ensure(ctx, S_TABLE_CNT, T * 8, &dense)) ||
         (rc = ensure(ctx, S_STATUS0, ntiles * 8, &st0)) || (rc = ensure(ctx, S_STATUS1, ntiles * 8, &st1)) ||
         (rc = ensure(ctx, S_BEST, (uint64_t)n_merges * 8, &best)) ||
         (rc = ensure(ctx, S_STATE, sizeof(TrainState), &state)) ||
-        (rc = ensure(ctx, S_NHIST, ((uint64_t)n_merges + 1) * 8, &nhist)))
+        (rc = ensure(ctx, S_NHIST, ((uint64_t)n_merges + 1) * 8, &nhist)) ||
+        (rc = ensure(ctx, S_LIST0, ((uint64_t)n_merges + 1) * 4, &dhist)))
         return rc;
+    uint32_t *dkey = (uint32_t *)dense, *dcnt = dkey + T;   // dense keys, then dense counts
     const uint32_t G = kGraphIters;
     void *pin;
-    const size_t pin_bytes = sizeof(TrainState) + 8 * kInFlight + (uint64_t)n_merges * 8 + ((uint64_t)n_merges + 1) * 8;
+    const size_t pin_bytes = sizeof(TrainState) + 8 * kInFlight + (uint64_t)n_merges * 8 +
+                             ((uint64_t)n_merges + 1) * 8 + ((uint64_t)n_merges + 1) * 4;
     if ((rc = ensure_pinned(ctx, pin_bytes, &pin))) return rc;
     TrainState *h_state = (TrainState *)pin;
     unsigned long long *h_poll = (unsigned long long *)(h_state + 1);
     unsigned long long *h_best = h_poll + kInFlight;
     unsigned long long *h_nhist = h_best + n_merges;
+    uint32_t *h_dhist = (uint32_t *)(h_nhist + n_merges + 1);
 
     // Make sure nothing still reads the pinned area from an earlier call.
     BPE_CUDA(ctx, cudaStreamSynchronize(s), "train: stream sync");
@@ -486,10 +718,11 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     h_nhist[0] = n;
     BPE_CUDA(ctx, cudaMemcpyAsync(state, h_state, sizeof *h_state, cudaMemcpyHostToDevice, s), "state upload");
     BPE_CUDA(ctx, cudaMemcpyAsync(nhist, h_nhist, 8, cudaMemcpyHostToDevice, s), "nhist upload");
-    BPE_CUDA(ctx, cudaMemsetAsync(tkey, 0xFF, T * 4, s), "table clear");
-    BPE_CUDA(ctx, cudaMemsetAsync(tcnt, 0, T * 4, s), "table clear");
+    BPE_CUDA(ctx, cudaMemsetAsync(tslot, 0xFF, T * 8, s), "table clear");
+    BPE_CUDA(ctx, cudaMemsetAsync(dcnt, 0, T * 4, s), "count clear");
     BPE_CUDA(ctx, cudaMemsetAsync(st0, 0, ntiles * 8, s), "status clear");
     BPE_CUDA(ctx, cudaMemsetAsync(best, 0, (uint64_t)n_merges * 8, s), "best clear");
+    BPE_CUDA(ctx, cudaMemsetAsync(dhist, 0, ((uint64_t)n_merges + 1) * 4, s), "dhist clear");
     BPE_CUDA(ctx, cudaMemcpyAsync(buf0, d_symbols, n * 4, cudaMemcpyDeviceToDevice, s), "input copy");
 
     int cb, mb;
@@ -497,31 +730,37 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     Launch L;
     L.p.buf[0] = (uint32_t *)buf0;
     L.p.buf[1] = (uint32_t *)buf1;
-    L.p.tkey = (uint32_t *)tkey;
-    L.p.tcnt = (uint32_t *)tcnt;
+    L.p.tslot = (unsigned long long *)tslot;
     L.p.tmask = (uint32_t)(T - 1);
-    L.p.list[0] = (uint32_t *)l0;
-    L.p.list[1] = (uint32_t *)l1;
+    L.p.dkey = dkey;
+    L.p.dcnt = dcnt;
+    L.p.dcap = (uint32_t)T;
     L.p.status[0] = (unsigned long long *)st0;
     L.p.status[1] = (unsigned long long *)st1;
     L.p.best = (unsigned long long *)best;
     L.p.nhist = (unsigned long long *)nhist;
+    L.p.dhist = (uint32_t *)dhist;
     L.p.st = (TrainState *)state;
     const uint64_t count_work = (n + kCountTile - 1) / kCountTile;
     L.count_grid = (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(count_work, (uint64_t)ctx->sm_count * cb));
-    L.merge_grid = (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(ntiles, (uint64_t)ctx->sm_count * mb));
+    L.merge_grid = (unsigned)std::max<uint64_t>(1, ntiles);   // one tile per CTA; spare CTAs exit
+    L.argmax_grid = (unsigned)ctx->sm_count * 2;
     L.count_smem = 2 * kCountSlots * sizeof(uint32_t);
+    L.merge_smem = (kTileWords + 2 * kDeltaSlots) * sizeof(uint32_t);
 
     const bool profile = ctx->profile != 0;
     const bool graph = ctx->use_graph && !profile;
-    if (profile && (rc = ensure_events(ctx, 2 * (size_t)n_merges + 1 + kInFlight))) return rc;
+    // profile events: 0 before k_count, 1 after it; merge k: 2+2k after argmax, 3+2k after merge
+    const size_t n_prof = profile ? 2 + 2 * (size_t)n_merges : 0;
+    if ((rc = ensure_events(ctx, n_prof + kInFlight))) return rc;
     std::vector<cudaEvent_t> poll_ev(kInFlight);
-    if (!profile && (rc = ensure_events(ctx, kInFlight))) return rc;
-    for (int i = 0; i < kInFlight; i++) poll_ev[i] = ctx->events[profile ? 2 * (size_t)n_merges + 1 + i : i];
+    for (int i = 0; i < kInFlight; i++) poll_ev[i] = ctx->events[n_prof + i];
 
     cudaGraphExec_t exec = nullptr;
     if (graph && (rc = get_graph(ctx, L, &exec))) return rc;
     if (profile) BPE_CUDA(ctx, cudaEventRecord(ctx->events[0], s), "event");
+    k_count<<<L.count_grid, kCountThreads, L.count_smem, s>>>(L.p);
+    if (profile) BPE_CUDA(ctx, cudaEventRecord(ctx->events[1], s), "event");
 
     // Launch windows of G merges; keep at most kInFlight windows queued so a
     // stop (a merge with count 0) is noticed without a full drain.
@@ -540,10 +779,10 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
             BPE_CUDA(ctx, cudaGraphLaunch(exec, s), "graph launch");
         } else {
             for (uint32_t k = launched; k < end; k++) {
-                k_count<<<L.count_grid, kCountThreads, L.count_smem, s>>>(L.p, k);
-                if (profile) cudaEventRecord(ctx->events[1 + 2 * (size_t)k], s);
-                k_merge<<<L.merge_grid, kMergeThreads, 0, s>>>(L.p, k);
+                k_argmax<<<L.argmax_grid, kArgmaxThreads, 0, s>>>(L.p, k);
                 if (profile) cudaEventRecord(ctx->events[2 + 2 * (size_t)k], s);
+                k_merge<<<L.merge_grid, kMergeThreads, L.merge_smem, s>>>(L.p, k);
+                if (profile) cudaEventRecord(ctx->events[3 + 2 * (size_t)k], s);
             }
         }
         BPE_CUDA(ctx, cudaGetLastError(), "train launch");
@@ -558,6 +797,8 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     BPE_CUDA(ctx, cudaMemcpyAsync(h_best, best, (uint64_t)n_merges * 8, cudaMemcpyDeviceToHost, s), "best read");
     BPE_CUDA(ctx, cudaMemcpyAsync(h_nhist, nhist, ((uint64_t)n_merges + 1) * 8, cudaMemcpyDeviceToHost, s),
              "nhist read");
+    BPE_CUDA(ctx, cudaMemcpyAsync(h_dhist, dhist, ((uint64_t)n_merges + 1) * 4, cudaMemcpyDeviceToHost, s),
+             "dhist read");
     BPE_CUDA(ctx, cudaStreamSynchronize(s), "train sync");
 
     if (h_state->err & DERR_TABLE_FULL) {
@@ -586,25 +827,29 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
 
     // statistics: algorithmic bytes per kernel family and (profiled) device time
     stats_reset(ctx);
-    ctx->stats.kernel_launches = graph ? (uint64_t)window * (2 * kGraphIters + 1) : 2ull * launched;
-    const uint32_t ran = std::min<uint32_t>(n_merges, done + 1);   // the stopping count ran too
-    const int sc = stats_slot(ctx, "pair_count"), sm = stats_slot(ctx, "merge_compact");
-    for (uint32_t k = 0; k < ran; k++) {
-        ctx->stats.k[sc].launches++;
-        ctx->stats.k[sc].bytes += 4.0 * (double)h_nhist[k];
-        if (k < done) {
-            ctx->stats.k[sm].launches++;
-            ctx->stats.k[sm].bytes += 4.0 * (double)h_nhist[k] + 4.0 * (double)h_nhist[k + 1];
-        }
+    ctx->stats.kernel_launches = 1 + (graph ? (uint64_t)window * (2 * kGraphIters + 1) : 2ull * launched);
+    const int sc = stats_slot(ctx, "pair_count"), sa = stats_slot(ctx, "argmax"), sm = stats_slot(ctx, "merge_compact");
+    ctx->stats.k[sc].launches = 1;
+    ctx->stats.k[sc].bytes = 4.0 * (double)n;
+    const uint32_t ran = std::min<uint32_t>(n_merges, done + 1);   // the argmax that found 0 ran too
+    for (uint32_t k = 1; k < ran; k++) {
+        ctx->stats.k[sa].launches++;
+        ctx->stats.k[sa].bytes += 8.0 * (double)h_dhist[k];
+    }
+    for (uint32_t k = 0; k < done; k++) {
+        ctx->stats.k[sm].launches++;
+        ctx->stats.k[sm].bytes += 4.0 * (double)h_nhist[k] + 4.0 * (double)h_nhist[k + 1];
     }
     if (profile) {
+        float x = 0;
+        if (cudaEventElapsedTime(&x, ctx->events[0], ctx->events[1]) == cudaSuccess) ctx->stats.k[sc].ms = x;
         for (uint32_t k = 0; k < launched; k++) {
             float a = 0, b = 0;
-            if (cudaEventElapsedTime(&a, ctx->events[2 * (size_t)k], ctx->events[1 + 2 * (size_t)k]) == cudaSuccess &&
-                k < ran)
-                ctx->stats.k[sc].ms += a;
-            if (cudaEventElapsedTime(&b, ctx->events[1 + 2 * (size_t)k], ctx->events[2 + 2 * (size_t)k]) == cudaSuccess &&
-                k < done)
+            cudaEvent_t before = ctx->events[k ? 3 + 2 * (size_t)(k - 1) : 1];
+            if (k >= 1 && k < ran && cudaEventElapsedTime(&a, before, ctx->events[2 + 2 * (size_t)k]) == cudaSuccess)
+                ctx->stats.k[sa].ms += a;
+            if (k < done &&
+                cudaEventElapsedTime(&b, ctx->events[2 + 2 * (size_t)k], ctx->events[3 + 2 * (size_t)k]) == cudaSuccess)
                 ctx->stats.k[sm].ms += b;
         }
         cudaGetLastError();
