@@ -153,8 +153,8 @@ extern "C" int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value) {
         ctx->profile = value ? 1 : 0;
         return BPE_OK;
     case BPE_OPT_CHUNK:
-        if (value < 64 || value > 4096 || value % 32)
-            return fail(ctx, BPE_ERR_INVALID_ARG, "chunk %lld not in 64..4096 or not a multiple of 32",
+        if (value < 64 || value > 256 || value % 32)
+            return fail(ctx, BPE_ERR_INVALID_ARG, "chunk %lld not in 64..256 or not a multiple of 32",
                         (long long)value);
         ctx->chunk = (int)value;
         return BPE_OK;

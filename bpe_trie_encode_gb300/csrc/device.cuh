@@ -33,6 +33,15 @@ __device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long lon
     return v;
 }
 
+// Weak 64-bit load served by L2 (no L1, no ordering): independent loads of
+// look-back status words overlap; each word is one aligned 64-bit value, so a
+// reader sees it either before or after its single store.
+__device__ __forceinline__ unsigned long long ld_l2(const unsigned long long *a) {
+    unsigned long long v;
+    asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(v) : "l"(a));
+    return v;
+}
+
 __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) {

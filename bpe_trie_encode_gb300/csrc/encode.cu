@@ -46,7 +46,7 @@ namespace {
 
 constexpr int kSpecThreads = 256;          // 255 owned chunks + 1 halo chunk per CTA
 constexpr int kEmitThreads = 256;
-constexpr int kMaxChunk = 1024;            // bytes per chunk (bitmap bound)
+constexpr int kMaxChunk = 256;             // bytes per chunk (staging and bitmap bound)
 constexpr unsigned kSpinLimit = 1u << 22;
 
 struct EncState {
@@ -56,7 +56,8 @@ struct EncState {
     uint32_t any_flag;   // some chunk's exit disagreed with the next nominal entry
     uint32_t ticket;
     uint32_t bad_doc_off;
-    unsigned long long span;   // doc_off[n_docs] - doc_off[0]
+    unsigned long long span;     // doc_off[n_docs] - doc_off[0]
+    unsigned long long text_lo;  // doc_off[0]
 };
 
 struct EncParams {
@@ -144,6 +145,113 @@ __device__ __forceinline__ ChunkGeo chunk_geo(const EncParams &P, unsigned long 
     return g;
 }
 
+// ------------------------------------------------------------- parsing ---
+
+// Sequential reads of a lane's bytes, four at a time: one aligned 32-bit load
+// through L1 serves the next bytes (the word never leaves the allocation: it
+// holds at least one byte of the text).
+struct ByteWin {
+    const uint8_t *g;
+    uintptr_t at = ~uintptr_t(0);
+    uint32_t w = 0;
+    __device__ __forceinline__ uint32_t operator()(uint64_t p) {
+        const uintptr_t a = (uintptr_t)(g + p), al = a & ~uintptr_t(3);
+        if (al != at) {
+            at = al;
+            w = __ldg(reinterpret_cast<const uint32_t *>(al));
+        }
+        return (w >> (8 * (uint32_t)(a - al))) & 0xFFu;
+    }
+};
+
+// Greedy longest-match parse of the tokens that start in [p, ce) of a
+// document ending at de.  Every loop iteration takes one trie step on every
+// lane -- from the root through the shared LUT, or from a node through the
+// double array -- so the lanes of a warp run the same instructions whatever
+// their token lengths; a token ends when a step fails.
+//   MODE 0 (speculative): mark token starts in bits (offsets from cs)
+//   MODE 1 (resync): stop early where a token start is already marked
+//   MODE 2 (emit): write ids to ids[o ...] (below cap)
+// Returns the position after the last token; *cnt = tokens parsed (MODE 1:
+// tokens up to the meeting point, *met = whether it met the marked path).
+template <int MODE>
+__device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 *lut, uint64_t p, uint64_t ce,
+                                                 uint64_t de, uint64_t cs, uint32_t *bits, uint32_t *cnt,
+                                                 unsigned long long o, bool *met) {
+    uint32_t c = 0;
+    if (MODE == 1) *met = false;
+    if (p < ce && MODE == 1) {
+        const uint32_t off = (uint32_t)(p - cs);
+        if ((bits[off >> 5] >> (off & 31)) & 1u) {
+            *met = true;
+            *cnt = 0;
+            return p;
+        }
+    }
+    ByteWin byte{P.bytes};
+    int32_t node = -1;            // -1: at the root
+    uint32_t y = 0, blen = 0;     // base|TERM of node; length of the best token so far
+    int32_t bnode = -1, btid = 0; // best token: its slot (id in tid[]) or, at depth 1, its id
+    uint64_t q = p;
+    while (p < ce) {
+        const bool root = node < 0;
+        const uint32_t base = y & ~kTermBit;
+        bool ok = false;
+        int32_t nt = 0;
+        uint32_t ny = 0;
+        if (q < de && (root || base != 0)) {
+            const uint32_t ch = byte(q);
+            if (root) {
+                const int4 r = lut[ch];
+                nt = r.x;
+                ny = (uint32_t)r.y;
+                btid = r.z;
+                ok = true;
+            } else {
+                nt = (int32_t)(base + ch);
+                const int2 v = __ldg(P.slot + nt);
+                ny = (uint32_t)v.y;
+                ok = (v.x == node);
+            }
+        }
+        if (ok) {
+            node = nt;
+            y = ny;
+            ++q;
+            if (ny & kTermBit) {
+                blen = (uint32_t)(q - p);
+                bnode = root ? -1 : nt;
+            }
+        } else {   // the token [p, p + blen) ends here (every byte is a token: blen >= 1)
+            if (MODE == 0) {
+                const uint32_t off = (uint32_t)(p - cs);
+                bits[off >> 5] |= 1u << (off & 31);
+            }
+            if (MODE == 2 && o < P.cap) P.ids[o] = bnode >= 0 ? __ldg(P.tid + bnode) : btid;
+            ++o;
+            ++c;
+            p += blen;
+            if (MODE == 1 && p < ce) {
+                const uint32_t off = (uint32_t)(p - cs);
+                if ((bits[off >> 5] >> (off & 31)) & 1u) {
+                    *met = true;
+                    break;
+                }
+            }
+            node = -1;
+            y = 0;
+            blen = 0;
+            bnode = -1;
+            q = p;
+        }
+    }
+    *cnt = c;
+    return p;
+}
+
+__host__ __device__ __forceinline__ size_t spec_smem_for(uint32_t C) { return (size_t)kSpecThreads * (C / 32) * 4; }
+__host__ __device__ __forceinline__ size_t emit_smem_for(uint32_t) { return 0; }
+
 // ---------------------------------------------------------- chunk index ---
 
 __global__ void __launch_bounds__(1024) k_chunk_index(EncParams P, unsigned long long *chunk_start) {
@@ -187,37 +295,32 @@ __global__ void __launch_bounds__(1024) k_chunk_index(EncParams P, unsigned long
         chunk_start[P.n_docs] = s_carry;
         P.st->n_chunks = s_carry;
         P.st->span = P.doc_off[P.n_docs] - P.doc_off[0];
+        P.st->text_lo = P.doc_off[0];
     }
 }
 
 // ------------------------------------------------ speculative parse + fix ---
 
-__global__ void __launch_bounds__(kSpecThreads) k_spec(EncParams P, unsigned long long n_chunks) {
+__global__ void __launch_bounds__(kSpecThreads) k_spec(EncParams P, unsigned long long n_chunks, uint64_t text_end) {
     extern __shared__ uint32_t s_bits[];   // kSpecThreads x (C/32) token-start bitmaps
     __shared__ int4 lut[256];
     __shared__ unsigned long long s_exit[kSpecThreads];
-    load_lut(P, lut);
-    __syncthreads();
     const int tid = threadIdx.x;
     const uint32_t words = P.chunk >> 5;
     uint32_t *bits = s_bits + tid * words;
     const long long k = (long long)blockIdx.x * (kSpecThreads - 1) + tid - 1;
     const bool live = k >= 0 && (unsigned long long)k < n_chunks;
+    load_lut(P, lut);
 
     ChunkGeo g{0, 0, 0, true};
+    if (live) g = chunk_geo(P, (unsigned long long)k);
+    __syncthreads();
+
     uint32_t spec_count = 0;
     uint64_t spec_exit = 0;
     if (live) {
-        g = chunk_geo(P, (unsigned long long)k);
         for (uint32_t w = 0; w < words; w++) bits[w] = 0;
-        uint64_t p = g.cs;
-        while (p < g.ce) {
-            const uint32_t o = (uint32_t)(p - g.cs);
-            bits[o >> 5] |= 1u << (o & 31);
-            p += match_at(P, lut, p, g.de).len;
-            ++spec_count;
-        }
-        spec_exit = p;
+        spec_exit = parse_tokens<0>(P, lut, g.cs, g.ce, g.de, g.cs, bits, &spec_count, 0, nullptr);
     }
     s_exit[tid] = spec_exit;
     __syncthreads();
@@ -229,25 +332,19 @@ __global__ void __launch_bounds__(kSpecThreads) k_spec(EncParams P, unsigned lon
         count = spec_count;
         exit = spec_exit;
     } else {
-        uint64_t q = s_exit[tid - 1];        // nominal entry: previous chunk's spec exit
+        // re-parse from the nominal entry (previous chunk's spec exit) until the
+        // two paths meet; from there the rest of the chunk is the spec path
+        bool met = false;
         uint32_t c = 0;
-        exit = q;
-        for (;;) {
-            if (q >= g.ce) {
-                exit = q;
-                break;
-            }
+        const uint64_t q = parse_tokens<1>(P, lut, s_exit[tid - 1], g.ce, g.de, g.cs, bits, &c, 0, &met);
+        if (met) {
             const uint32_t o = (uint32_t)(q - g.cs);
-            if ((bits[o >> 5] >> (o & 31)) & 1u) {
-                // the paths meet at q: the rest of the chunk is the spec path
-                uint32_t rest = __popc(bits[o >> 5] >> (o & 31));
-                for (uint32_t w = (o >> 5) + 1; w < words; w++) rest += __popc(bits[w]);
-                c += rest;
-                exit = spec_exit;
-                break;
-            }
-            q += match_at(P, lut, q, g.de).len;
-            ++c;
+            uint32_t rest = __popc(bits[o >> 5] >> (o & 31));
+            for (uint32_t w = (o >> 5) + 1; w < words; w++) rest += __popc(bits[w]);
+            c += rest;
+            exit = spec_exit;
+        } else {
+            exit = q;
         }
         count = c;
     }
@@ -315,68 +412,73 @@ __global__ void k_repair(EncParams P, unsigned long long n_chunks) {
 
 // ------------------------------------------------------------ scan + emit ---
 
-__global__ void __launch_bounds__(kEmitThreads) k_emit(EncParams P, unsigned long long n_chunks) {
+__global__ void __launch_bounds__(kEmitThreads) k_emit(EncParams P, unsigned long long n_chunks, uint64_t text_end) {
     __shared__ int4 lut[256];
     __shared__ uint32_t s_w[kEmitThreads / 32];
     __shared__ unsigned long long s_tile, s_off;
     load_lut(P, lut);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned long long ntiles = (n_chunks + kEmitThreads - 1) / kEmitThreads;
-    for (;;) {
-        if (tid == 0) s_tile = atomicAdd(&P.st->ticket, 1u);
-        __syncthreads();
-        const unsigned long long t = s_tile;
-        if (t >= ntiles) break;
-        const unsigned long long k = t * kEmitThreads + tid;
-        const uint32_t cnt = k < n_chunks ? P.count[k] : 0u;
-        const uint32_t incl = warp_incl_sum(cnt, lane);
-        if (lane == 31) s_w[warp] = incl;
-        __syncthreads();
-        uint32_t wpre = 0, tsum = 0;
-        for (int w = 0; w < kEmitThreads / 32; w++) {
-            if (w < warp) wpre += s_w[w];
-            tsum += s_w[w];
-        }
-        if (tid == 0) {
-            unsigned long long off = 0;
-            if (t > 0) {
-                st_relaxed(P.status + t, 1ull | ((unsigned long long)tsum << 2));
-                long long j = (long long)t - 1;
-                unsigned spins = 0;
-                for (;;) {
-                    const unsigned long long w = ld_relaxed(P.status + j);
-                    const uint32_t fl = (uint32_t)(w & 3ull);
-                    if (fl == 0) {
-                        if (++spins > kSpinLimit) {
-                            atomicOr(&P.st->err, DERR_TIMEOUT);
-                            break;
-                        }
-                        if (spins > 64) __nanosleep(64);
-                        continue;
+    if (tid == 0) s_tile = atomicAdd(&P.st->ticket, 1u);   // tiles in ticket order
+    __syncthreads();
+    const unsigned long long t = s_tile;
+    if (t >= ntiles) return;
+    const unsigned long long k = t * kEmitThreads + tid;
+    const bool live = k < n_chunks;
+    ChunkGeo g{0, 0, 0, true};
+    if (live) g = chunk_geo(P, k);
+    const uint32_t cnt = live ? P.count[k] : 0u;
+    const uint32_t incl = warp_incl_sum(cnt, lane);
+    if (lane == 31) s_w[warp] = incl;
+    __syncthreads();
+    uint32_t wpre = 0, tsum = 0;
+#pragma unroll
+    for (int w = 0; w < kEmitThreads / 32; w++) {
+        if (w < warp) wpre += s_w[w];
+        tsum += s_w[w];
+    }
+    if (warp == 0) {   // publish, then look back 32 predecessors per round trip
+        unsigned long long off = 0;
+        if (t > 0) {
+            if (lane == 0) st_relaxed(P.status + t, 1ull | ((unsigned long long)tsum << 2));
+            long long jhi = (long long)t - 1;
+            unsigned spins = 0;
+            for (;;) {
+                const long long j = jhi - lane;
+                const unsigned long long w = (j >= 0) ? ld_l2(P.status + j) : 2ull;
+                const uint32_t fl = (uint32_t)(w & 3ull);
+                const unsigned incl_m = __ballot_sync(kFull, fl == 2);
+                const int L = incl_m ? __ffs(incl_m) - 1 : 31;
+                const unsigned need = (L == 31) ? kFull : ((2u << L) - 1u);
+                if (__ballot_sync(kFull, fl == 0) & need) {
+                    if (++spins > kSpinLimit) {
+                        if (lane == 0) atomicOr(&P.st->err, DERR_TIMEOUT);
+                        break;
                     }
-                    off += w >> 2;
-                    if (fl == 2) break;
-                    --j;
+                    if (spins > 32) __nanosleep(64);
+                    continue;
                 }
+                unsigned long long v = (lane <= L) ? (w >> 2) : 0ull;
+#pragma unroll
+                for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
+                off += v;
+                if (incl_m) break;
+                jhi -= 32;
             }
+        }
+        if (lane == 0) {
             st_relaxed(P.status + t, 2ull | ((off + tsum) << 2));
             if (t == ntiles - 1) P.st->total = off + tsum;
             s_off = off;
         }
-        __syncthreads();
-        if (k < n_chunks) {
-            unsigned long long o = s_off + wpre + incl - cnt;
-            P.prefix[k] = o;
-            const ChunkGeo g = chunk_geo(P, k);
-            uint64_t e = g.doc_first ? g.cs : (g.cs - P.chunk) + P.exit_rel[k - 1];
-            while (e < g.ce) {
-                const Match m = match_at(P, lut, e, g.de);
-                if (o < P.cap) P.ids[o] = m.id;
-                ++o;
-                e += m.len;
-            }
-        }
-        __syncthreads();
+    }
+    __syncthreads();
+    if (live) {
+        const unsigned long long o = s_off + wpre + incl - cnt;
+        P.prefix[k] = o;
+        const uint64_t e = g.doc_first ? g.cs : (g.cs - P.chunk) + P.exit_rel[k - 1];
+        uint32_t c = 0;
+        parse_tokens<2>(P, lut, e, g.ce, g.de, g.cs, nullptr, &c, o, nullptr);
     }
 }
 
@@ -445,6 +547,7 @@ extern "C" int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_
     if (h->err & DERR_OOB)
         return fail(ctx, BPE_ERR_INVALID_ARG, "trie_encode: document offsets descend at document %u", h->bad_doc_off);
     const unsigned long long nc = h->n_chunks;
+    const uint64_t text_end = h->text_lo + h->span;   // end of the last document
     if (nc == 0) {
         if (d_id_off_out) BPE_CUDA(ctx, cudaMemsetAsync(d_id_off_out, 0, ((uint64_t)n_docs + 1) * 8, s), "id_off");
         BPE_CUDA(ctx, cudaStreamSynchronize(s), "sync");
@@ -471,19 +574,20 @@ extern "C" int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_
 
     BPE_CUDA(ctx, cudaMemsetAsync(flag, 0, ((nc + 31) / 32) * 4, s), "flag clear");
     BPE_CUDA(ctx, cudaMemsetAsync(status, 0, emit_tiles * 8, s), "status clear");
-    const size_t spec_smem = (size_t)kSpecThreads * (C / 32) * 4;
+    const size_t spec_smem = spec_smem_for(C), emit_smem = emit_smem_for(C);
     BPE_CUDA(ctx, cudaFuncSetAttribute(k_spec, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)spec_smem),
              "k_spec smem");
-    int eb = 1;
-    BPE_CUDA(ctx, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&eb, k_emit, kEmitThreads, 0), "occupancy");
-    const unsigned long long emit_grid = std::min<unsigned long long>(emit_tiles, (unsigned long long)ctx->sm_count * std::max(eb, 1));
+    BPE_CUDA(ctx, cudaFuncSetAttribute(k_emit, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)emit_smem),
+             "k_emit smem");
+
+    const unsigned long long emit_grid = emit_tiles;   // one tile per CTA, ticket order
 
     if (profile) cudaEventRecord(ctx->events[2], s);
-    k_spec<<<(unsigned)spec_blocks, kSpecThreads, spec_smem, s>>>(P, nc);
+    k_spec<<<(unsigned)spec_blocks, kSpecThreads, spec_smem, s>>>(P, nc, text_end);
     if (profile) cudaEventRecord(ctx->events[3], s);
     k_repair<<<1, 256, 0, s>>>(P, nc);
     if (profile) cudaEventRecord(ctx->events[4], s);
-    k_emit<<<(unsigned)emit_grid, kEmitThreads, 0, s>>>(P, nc);
+    k_emit<<<(unsigned)emit_grid, kEmitThreads, emit_smem, s>>>(P, nc, text_end);
     if (profile) cudaEventRecord(ctx->events[5], s);
     k_doc_offsets<<<(unsigned)((n_docs + 1 + 255) / 256), 256, 0, s>>>(P, nc);
     BPE_CUDA(ctx, cudaGetLastError(), "trie_encode launch");
@@ -621,16 +725,14 @@ int noalloc_body(const bpe_trie *trie, const uint8_t *d_bytes, const uint64_t *d
     if (cudaMemsetAsync(P.flag, 0, ((nc + 31) / 32) * 4, s) != cudaSuccess ||
         cudaMemsetAsync(P.status, 0, emit_tiles * 8, s) != cudaSuccess)
         return BPE_ERR_CUDA;
-    int sms = 0, eb = 1;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, trie->device) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&eb, k_emit, kEmitThreads, 0) != cudaSuccess)
+    const size_t spec_smem = spec_smem_for(kNaChunk), emit_smem = emit_smem_for(kNaChunk);
+    if (cudaFuncSetAttribute(k_spec, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)spec_smem) != cudaSuccess ||
+        cudaFuncSetAttribute(k_emit, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)emit_smem) != cudaSuccess)
         return BPE_ERR_CUDA;
-    const unsigned long long emit_grid =
-        std::min<unsigned long long>(emit_tiles, (unsigned long long)sms * std::max(eb, 1));
-    const size_t spec_smem = (size_t)kSpecThreads * (kNaChunk / 32) * 4;
-    k_spec<<<(unsigned)spec_blocks, kSpecThreads, spec_smem, s>>>(P, nc);
+    const uint64_t text_end = h.span + h.text_lo;
+    k_spec<<<(unsigned)spec_blocks, kSpecThreads, spec_smem, s>>>(P, nc, text_end);
     k_repair<<<1, 256, 0, s>>>(P, nc);
-    k_emit<<<(unsigned)emit_grid, kEmitThreads, 0, s>>>(P, nc);
+    k_emit<<<(unsigned)emit_tiles, kEmitThreads, emit_smem, s>>>(P, nc, text_end);
     k_doc_offsets<<<(unsigned)((n_docs + 1 + 255) / 256), 256, 0, s>>>(P, nc);
     if (cudaGetLastError() != cudaSuccess) return BPE_ERR_CUDA;
     if (cudaMemcpyAsync(&h, P.st, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess ||

@@ -331,7 +331,7 @@ __device__ __forceinline__ bool lookback(const unsigned long long *status, uint6
 #pragma unroll
         for (int q = 0; q < kPer; q++) {   // q = 0 is the newest tile of this lane
             const long long j = jhi - kPer * lane - q;
-            w[q] = (j >= 0) ? ld_relaxed(status + j) : inc_word(0, 0);
+            w[q] = (j >= 0) ? ld_l2(status + j) : inc_word(0, 0);
         }
         int qi = kPer;                      // newest inclusive of this lane
         bool ready = true;

@@ -82,7 +82,7 @@ const char *bpe_last_error(const bpe_ctx *ctx);
  *   BPE_OPT_PROFILE      1 = record a CUDA event after every kernel of
  *                        bpe_train / trie_encode so bpe_last_stats() reports
  *                        per-kernel device time (implies host launches)
- *   BPE_OPT_CHUNK        trie_encode bytes per chunk (64..4096, multiple
+ *   BPE_OPT_CHUNK        trie_encode bytes per chunk (64..256, multiple
  *                        of 32; default 128) */
 enum { BPE_OPT_TABLE_LOG2 = 1, BPE_OPT_GRAPH = 2, BPE_OPT_PROFILE = 3, BPE_OPT_CHUNK = 4 };
 int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value);

@@ -258,7 +258,7 @@ def test_encode_random_vocab_ragged_docs(ctx, seed):
     check_encode(ctx, vb, off, docs)
 
 
-@pytest.mark.parametrize("chunk", [64, 128, 256, 1024])
+@pytest.mark.parametrize("chunk", [64, 96, 128, 256])
 def test_encode_chunk_sizes_agree(ctx, chunk):
     rng = random.Random(11)
     toks = [bytes([b]) for b in range(256)] + [rand_bytes(rng, rng.randrange(2, 30), b"abc ") for _ in range(500)]
