@@ -857,6 +857,579 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     return BPE_OK;
 }
 
+// ----------------------------------------------- word-frequency training ---
+//
+// No pair is counted across a WORD_START and no merge crosses one, so the
+// stream is a sequence of words (a word starts at index 0 and at every
+// WORD_START symbol) and the merge loop can run over the distinct words,
+// each weighted by its number of occurrences: the pair counts, the argmax,
+// the merges and -- expanded back over the occurrences -- the final stream
+// are exactly those of the full-stream loop.
+//
+//   k_wstarts_count / k_scan_top / k_wstarts_write   word start positions
+//   k_whash / k_wverify     distinct words through a hash table of 64-bit
+//                           content hashes; a verification pass compares
+//                           every occurrence with its representative, a
+//                           collision makes the host retry with a new seed
+//   k_wassign / k_wgather   one compact copy of each distinct word
+//   k_wcount                initial weighted pair counts (+ argmax of merge 0)
+//   k_wmerge                per merge: every word holding the pair is merged
+//                           left to right in place by one thread, and its
+//                           pairs before and after go as -freq / +freq deltas
+//                           into the count table (k_argmax finds the next pair)
+//   k_wexpand               the final stream from the occurrences
+
+constexpr int kWThreads = 256;
+constexpr int kWItems = 16;
+constexpr int kWBlock = kWThreads * kWItems;   // positions per scan block
+constexpr uint32_t kWErrCollision = 8u;
+
+struct WSlot {
+    unsigned long long key;   // content hash | 1; 0 = empty
+    uint32_t freq;
+    uint32_t rep_inv;         // ~(first occurrence)
+};
+
+struct WordParams {
+    const uint32_t *sym;      // the input stream
+    uint64_t n;
+    uint32_t *wstart;         // word starts, n_occ + 1 entries
+    uint32_t *occ_slot;       // table slot of each occurrence
+    WSlot *table;
+    uint32_t tmask;
+    uint32_t *uid;            // per table slot: distinct word id
+    uint32_t *urep, *ufreq, *ulen, *uoff;   // per distinct word
+    uint32_t *wsym;           // compact words
+    uint32_t *bsum;           // scan block sums
+    uint32_t *counter;        // [0] = n_occ, [1] = n_uniq, [2] = err, [3] = total of the last scan
+};
+
+// Block-wide exclusive scan of one value per thread (kWThreads threads).
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *s_w, uint32_t *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t incl = warp_incl_sum(v, lane);
+    if (lane == 31) s_w[warp] = incl;
+    __syncthreads();
+    uint32_t pre = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kWThreads / 32; w++) {
+        const uint32_t x = s_w[w];
+        pre += (w < warp) ? x : 0u;
+        tot += x;
+    }
+    __syncthreads();
+    *total = tot;
+    return pre + incl - v;
+}
+
+__device__ __forceinline__ bool is_word_start(const uint32_t *sym, uint64_t i) { return i == 0 || (sym[i] & kWordStart); }
+
+__global__ void __launch_bounds__(kWThreads) k_wstarts_count(WordParams W) {
+    __shared__ uint32_t s_w[kWThreads / 32];
+    const uint64_t base = (uint64_t)blockIdx.x * kWBlock + (uint64_t)threadIdx.x * kWItems;
+    uint32_t c = 0;
+    for (int j = 0; j < kWItems; j++)
+        if (base + j < W.n && is_word_start(W.sym, base + j)) ++c;
+    uint32_t tot;
+    block_excl_scan(c, s_w, &tot);
+    if (threadIdx.x == 0) W.bsum[blockIdx.x] = tot;
+}
+
+// Exclusive scan of nb block sums in place by one CTA; total -> *total.
+__global__ void __launch_bounds__(1024) k_scan_top(uint32_t *bsum, uint32_t nb, uint32_t *total) {
+    __shared__ uint32_t s_w[32];
+    __shared__ uint32_t s_carry;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) s_carry = 0;
+    __syncthreads();
+    for (uint32_t b0 = 0; b0 < nb; b0 += 1024) {
+        const uint32_t i = b0 + threadIdx.x;
+        const uint32_t v = i < nb ? bsum[i] : 0u;
+        const uint32_t incl = warp_incl_sum(v, lane);
+        if (lane == 31) s_w[warp] = incl;
+        __syncthreads();
+        uint32_t pre = 0, tot = 0;
+        for (int w = 0; w < 32; w++) {
+            pre += (w < warp) ? s_w[w] : 0u;
+            tot += s_w[w];
+        }
+        const uint32_t carry = s_carry;
+        if (i < nb) bsum[i] = carry + pre + incl - v;
+        __syncthreads();
+        if (threadIdx.x == 0) s_carry = carry + tot;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) *total = s_carry;
+}
+
+__global__ void __launch_bounds__(kWThreads) k_wstarts_write(WordParams W, uint32_t n_occ) {
+    __shared__ uint32_t s_w[kWThreads / 32];
+    const uint64_t base = (uint64_t)blockIdx.x * kWBlock + (uint64_t)threadIdx.x * kWItems;
+    uint32_t c = 0;
+    for (int j = 0; j < kWItems; j++)
+        if (base + j < W.n && is_word_start(W.sym, base + j)) ++c;
+    uint32_t tot;
+    uint32_t o = W.bsum[blockIdx.x] + block_excl_scan(c, s_w, &tot);
+    for (int j = 0; j < kWItems; j++)
+        if (base + j < W.n && is_word_start(W.sym, base + j)) W.wstart[o++] = (uint32_t)(base + j);
+    if (blockIdx.x == 0 && threadIdx.x == 0) W.wstart[n_occ] = (uint32_t)W.n;
+}
+
+__device__ __forceinline__ unsigned long long word_hash(const uint32_t *w, uint32_t len, unsigned long long seed) {
+    unsigned long long h = seed ^ (0x9E3779B97F4A7C15ull * (len + 1));
+    for (uint32_t i = 0; i < len; i++) {
+        h ^= w[i];
+        h *= 0x100000001B3ull;
+        h ^= h >> 29;
+    }
+    h ^= h >> 33;       // a 64-bit finaliser (splitmix64's)
+    h *= 0xFF51AFD7ED558CCDull;
+    h ^= h >> 33;
+    h *= 0xC4CEB9FE1A85EC53ull;
+    h ^= h >> 33;
+    return h | 1ull;
+}
+
+__global__ void k_whash(WordParams W, uint32_t n_occ, unsigned long long seed) {
+    const uint32_t o = blockIdx.x * blockDim.x + threadIdx.x;
+    if (o >= n_occ) return;
+    const uint32_t a = W.wstart[o], b = W.wstart[o + 1];
+    const unsigned long long h = word_hash(W.sym + a, b - a, seed);
+    uint32_t s = (uint32_t)(h >> 20) & W.tmask;
+    for (uint32_t probe = 1; probe <= 256; ++probe) {
+        const unsigned long long cur = atomicCAS(&W.table[s].key, 0ull, h);
+        if (cur == 0ull || cur == h) {
+            atomicAdd(&W.table[s].freq, 1u);
+            atomicMax(&W.table[s].rep_inv, ~o);
+            W.occ_slot[o] = s;
+            return;
+        }
+        s = (s + probe) & W.tmask;
+    }
+    atomicOr(&W.counter[2], DERR_TABLE_FULL);
+    W.occ_slot[o] = 0;
+}
+
+__global__ void k_wverify(WordParams W, uint32_t n_occ) {
+    const uint32_t o = blockIdx.x * blockDim.x + threadIdx.x;
+    if (o >= n_occ) return;
+    const uint32_t rep = ~W.table[W.occ_slot[o]].rep_inv;
+    if (rep == o) return;
+    const uint32_t a = W.wstart[o], len = W.wstart[o + 1] - a;
+    const uint32_t ra = W.wstart[rep], rlen = W.wstart[rep + 1] - ra;
+    bool same = (len == rlen);
+    for (uint32_t i = 0; same && i < len; i++) same = (W.sym[a + i] == W.sym[ra + i]);
+    if (!same) atomicOr(&W.counter[2], kWErrCollision);
+}
+
+__global__ void k_wassign(WordParams W, uint32_t tsize) {
+    for (uint32_t s = blockIdx.x * blockDim.x + threadIdx.x; s < tsize; s += gridDim.x * blockDim.x) {
+        const WSlot e = W.table[s];
+        if (e.key == 0ull) continue;
+        const uint32_t u = atomicAdd(&W.counter[1], 1u);
+        const uint32_t rep = ~e.rep_inv;
+        W.uid[s] = u;
+        W.urep[u] = rep;
+        W.ufreq[u] = e.freq;
+        W.ulen[u] = W.wstart[rep + 1] - W.wstart[rep];
+    }
+}
+
+// exclusive scan of len[0..n) into off (block part; k_scan_top completes it)
+__global__ void __launch_bounds__(kWThreads) k_lens_partial(const uint32_t *len, uint32_t n, uint32_t *bsum) {
+    __shared__ uint32_t s_w[kWThreads / 32];
+    const uint64_t base = (uint64_t)blockIdx.x * kWBlock + (uint64_t)threadIdx.x * kWItems;
+    uint32_t c = 0;
+    for (int j = 0; j < kWItems; j++)
+        if (base + j < n) c += len[base + j];
+    uint32_t tot;
+    block_excl_scan(c, s_w, &tot);
+    if (threadIdx.x == 0) bsum[blockIdx.x] = tot;
+}
+__global__ void __launch_bounds__(kWThreads) k_lens_final(const uint32_t *len, uint32_t n, const uint32_t *bsum,
+                                                          uint32_t *off) {
+    __shared__ uint32_t s_w[kWThreads / 32];
+    const uint64_t base = (uint64_t)blockIdx.x * kWBlock + (uint64_t)threadIdx.x * kWItems;
+    uint32_t c = 0;
+    for (int j = 0; j < kWItems; j++)
+        if (base + j < n) c += len[base + j];
+    uint32_t tot;
+    uint32_t o = bsum[blockIdx.x] + block_excl_scan(c, s_w, &tot);
+    for (int j = 0; j < kWItems; j++)
+        if (base + j < n) {
+            off[base + j] = o;
+            o += len[base + j];
+        }
+}
+
+__global__ void k_wgather(WordParams W, uint32_t U) {
+    const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
+    if (u >= U) return;
+    const uint32_t a = W.wstart[W.urep[u]], len = W.ulen[u], o = W.uoff[u];
+    for (uint32_t i = 0; i < len; i++) W.wsym[o + i] = W.sym[a + i];
+}
+
+// Per-thread word loop with a shared delta table flushed at the end.
+template <bool COUNT>
+__device__ __forceinline__ void word_deltas(const TrainParams &p, const WordParams &W, uint32_t U, uint32_t k,
+                                            uint32_t l, uint32_t r, uint32_t new_id, uint32_t *dkey, uint32_t *dval,
+                                            uint32_t *s_docc, unsigned long long &mybest) {
+    const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
+    auto add = [&](uint32_t kk, uint32_t d) {
+        if (smem_add<kDeltaSlots>(dkey, dval, s_docc, kk, d)) {
+            const uint32_t tot = global_add(table_of(p), kk, d);
+            if (COUNT) {
+                const unsigned long long b = pack_best(tot, kk);
+                mybest = b > mybest ? b : mybest;
+            }
+        }
+    };
+    if (u < U) {
+        uint32_t *w = W.wsym + W.uoff[u];
+        const uint32_t len = W.ulen[u], f = W.ufreq[u];
+        if (COUNT) {
+            for (uint32_t i = 0; i + 1 < len; i++) add(pair_key(w[i], w[i + 1]), f);
+        } else if (len >= 2) {
+            bool hit = false;
+            for (uint32_t i = 0; i + 1 < len && !hit; i++)
+                hit = (w[i] & 0xFFFFu) == l && (w[i + 1] & 0xFFFFu) == r;
+            if (hit) {
+                const uint32_t neg = 0u - f;
+                for (uint32_t i = 0; i + 1 < len; i++) add(pair_key(w[i], w[i + 1]), neg);
+                uint32_t o = 0;   // left to right, non-overlapping, in place (o <= i)
+                for (uint32_t i = 0; i < len;) {
+                    if (i + 1 < len && (w[i] & 0xFFFFu) == l && (w[i + 1] & 0xFFFFu) == r) {
+                        w[o++] = new_id | (w[i] & kWordStart);
+                        i += 2;
+                    } else {
+                        w[o++] = w[i++];
+                    }
+                }
+                W.ulen[u] = o;
+                for (uint32_t i = 0; i + 1 < o; i++) add(pair_key(w[i], w[i + 1]), f);
+            }
+        }
+    }
+    __syncthreads();
+    if (*s_docc) {
+        for (int j = threadIdx.x; j < kDeltaSlots; j += blockDim.x) {
+            const uint32_t kk = dkey[j];
+            if (kk != kEmptyKey && dval[j]) {
+                const uint32_t tot = global_add(table_of(p), kk, dval[j]);
+                if (COUNT) {
+                    const unsigned long long b = pack_best(tot, kk);
+                    mybest = b > mybest ? b : mybest;
+                }
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kWThreads) k_wcount(TrainParams p, WordParams W) {
+    __shared__ uint32_t dkey[kDeltaSlots], dval[kDeltaSlots], s_docc;
+    __shared__ unsigned long long sbest[kWThreads / 32];
+    for (int j = threadIdx.x; j < kDeltaSlots; j += blockDim.x) {
+        dkey[j] = kEmptyKey;
+        dval[j] = 0;
+    }
+    if (threadIdx.x == 0) s_docc = 0;
+    __syncthreads();
+    unsigned long long mybest = 0;
+    word_deltas<true>(p, W, W.counter[1], 0, 0, 0, 0, dkey, dval, &s_docc, mybest);
+    mybest = warp_max_u64(mybest);
+    if ((threadIdx.x & 31) == 0) sbest[threadIdx.x >> 5] = mybest;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        unsigned long long b = threadIdx.x < kWThreads / 32 ? sbest[threadIdx.x] : 0ull;
+        b = warp_max_u64(b);
+        if (threadIdx.x == 0 && b) atomicMax(p.best, b);
+    }
+}
+
+__global__ void __launch_bounds__(kWThreads) k_wmerge(TrainParams p, WordParams W, uint32_t it) {
+    __shared__ uint32_t dkey[kDeltaSlots], dval[kDeltaSlots], s_docc;
+    TrainState *st = p.st;
+    const uint32_t k = st->k_base + it;
+    if (k >= st->n_merges || st->err) return;
+    const unsigned long long bw = p.best[k];
+    if ((bw >> 32) == 0) return;   // training has stopped
+    const uint32_t key = ~(uint32_t)bw;
+    for (int j = threadIdx.x; j < kDeltaSlots; j += blockDim.x) {
+        dkey[j] = kEmptyKey;
+        dval[j] = 0;
+    }
+    if (threadIdx.x == 0) s_docc = 0;
+    __syncthreads();
+    unsigned long long unused = 0;
+    word_deltas<false>(p, W, W.counter[1], k, key >> 16, key & 0xFFFFu, 256u + k, dkey, dval, &s_docc, unused);
+}
+
+// final stream: occurrence o's word, at its scanned offset
+__global__ void k_occ_len(WordParams W, uint32_t n_occ, uint32_t *olen) {
+    const uint32_t o = blockIdx.x * blockDim.x + threadIdx.x;
+    if (o < n_occ) olen[o] = W.ulen[W.uid[W.occ_slot[o]]];
+}
+__global__ void k_wexpand(WordParams W, uint32_t n_occ, const uint32_t *ooff, uint32_t *out) {
+    const uint32_t o = blockIdx.x * blockDim.x + threadIdx.x;
+    if (o >= n_occ) return;
+    const uint32_t u = W.uid[W.occ_slot[o]];
+    const uint32_t *w = W.wsym + W.uoff[u];
+    const uint32_t len = W.ulen[u], at = ooff[o];
+    for (uint32_t i = 0; i < len; i++) out[at + i] = w[i];
+}
+
+// exclusive scan of a device u32 array (n <= 2^30) into off; returns the total
+int scan_u32(bpe_ctx *ctx, const uint32_t *len, uint32_t n, uint32_t *off, uint32_t *bsum, uint32_t *d_total,
+             uint32_t *h_total) {
+    cudaStream_t s = ctx->stream;
+    const uint32_t nb = (n + kWBlock - 1) / kWBlock;
+    if (nb == 0) {
+        *h_total = 0;
+        return BPE_OK;
+    }
+    k_lens_partial<<<nb, kWThreads, 0, s>>>(len, n, bsum);
+    k_scan_top<<<1, 1024, 0, s>>>(bsum, nb, d_total);
+    k_lens_final<<<nb, kWThreads, 0, s>>>(len, n, bsum, off);
+    BPE_CUDA(ctx, cudaMemcpyAsync(h_total, d_total, 4, cudaMemcpyDeviceToHost, s), "scan total");
+    BPE_CUDA(ctx, cudaStreamSynchronize(s), "scan sync");
+    return BPE_OK;
+}
+
+int train_words_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_merges, uint32_t table_log2,
+                     bpe_merge *h_merges_out, uint32_t *n_done, uint32_t *d_symbols_final, uint64_t *n_final,
+                     bool *table_full) {
+    *table_full = false;
+    cudaStream_t s = ctx->stream;
+    int rc;
+    void *bsum, *wstart, *occ_slot, *table, *uidv, *uinfo, *wsym, *state, *best, *tslot, *dense, *dhist, *cnt;
+    const uint32_t nb = (uint32_t)((n + kWBlock - 1) / kWBlock);
+    if ((rc = ensure(ctx, S_W_BSUM, ((uint64_t)nb + 1024) * 4 + 64, &bsum)) ||
+        (rc = ensure(ctx, S_STATE, sizeof(TrainState) + 64, &state)))
+        return rc;
+    cnt = (uint32_t *)bsum + nb + 1024;   // 4 counters
+    void *pin;
+    const size_t pin_bytes = sizeof(TrainState) + 64 + 8 * kInFlight + (uint64_t)n_merges * 8 + ((uint64_t)n_merges + 1) * 4;
+    if ((rc = ensure_pinned(ctx, pin_bytes, &pin))) return rc;
+    uint32_t *h_cnt = (uint32_t *)pin;                     // 16 words
+    TrainState *h_state = (TrainState *)(h_cnt + 16);
+    unsigned long long *h_poll = (unsigned long long *)(h_state + 1);
+    unsigned long long *h_best = h_poll + kInFlight;
+    uint32_t *h_dhist = (uint32_t *)(h_best + n_merges);
+    BPE_CUDA(ctx, cudaStreamSynchronize(s), "train: stream sync");
+
+    WordParams W{};
+    W.sym = d_symbols;
+    W.n = n;
+    W.bsum = (uint32_t *)bsum;
+    W.counter = (uint32_t *)cnt;
+    BPE_CUDA(ctx, cudaMemsetAsync(cnt, 0, 16, s), "counters");
+    // 1. word starts
+    k_wstarts_count<<<nb, kWThreads, 0, s>>>(W);
+    k_scan_top<<<1, 1024, 0, s>>>(W.bsum, nb, W.counter);
+    BPE_CUDA(ctx, cudaMemcpyAsync(h_cnt, cnt, 16, cudaMemcpyDeviceToHost, s), "count read");
+    BPE_CUDA(ctx, cudaStreamSynchronize(s), "word count sync");
+    const uint32_t n_occ = h_cnt[0];
+    if ((rc = ensure(ctx, S_W_START, ((uint64_t)n_occ + 1) * 4, &wstart)) ||
+        (rc = ensure(ctx, S_W_OCCSLOT, (uint64_t)n_occ * 4 + 4, &occ_slot)))
+        return rc;
+    W.wstart = (uint32_t *)wstart;
+    W.occ_slot = (uint32_t *)occ_slot;
+    k_wstarts_write<<<nb, kWThreads, 0, s>>>(W, n_occ);
+    // 2. distinct words (retry on a hash collision or a full table)
+    uint32_t tlog = 16;
+    while ((1u << tlog) < 2u * std::min<uint32_t>(n_occ, 1u << 26) && tlog < 27) tlog++;
+    uint32_t U = 0;
+    for (int attempt = 0;; attempt++) {
+        const uint64_t tsize = 1ull << tlog;
+        if ((rc = ensure(ctx, S_W_TABLE, tsize * sizeof(WSlot), &table)) ||
+            (rc = ensure(ctx, S_W_UID, tsize * 4, &uidv)))
+            return rc;
+        W.table = (WSlot *)table;
+        W.tmask = (uint32_t)(tsize - 1);
+        W.uid = (uint32_t *)uidv;
+        BPE_CUDA(ctx, cudaMemsetAsync(table, 0, tsize * sizeof(WSlot), s), "word table clear");
+        BPE_CUDA(ctx, cudaMemsetAsync(cnt, 0, 16, s), "counters");
+        const unsigned long long seed = 0x243F6A8885A308D3ull * (attempt + 1);
+        const uint32_t gb = (n_occ + 255) / 256;
+        if (gb) {
+            k_whash<<<gb, 256, 0, s>>>(W, n_occ, seed);
+            k_wverify<<<gb, 256, 0, s>>>(W, n_occ);
+        }
+        BPE_CUDA(ctx, cudaMemcpyAsync(h_cnt, cnt, 16, cudaMemcpyDeviceToHost, s), "count read");
+        BPE_CUDA(ctx, cudaStreamSynchronize(s), "word hash sync");
+        if (h_cnt[2] == 0) break;
+        if (attempt >= 4) return fail(ctx, BPE_ERR_TABLE_FULL, "bpe_train: distinct-word table failed");
+        if (h_cnt[2] & DERR_TABLE_FULL) tlog = std::min<uint32_t>(tlog + 2, 28);
+    }
+    {
+        const uint64_t tsize = 1ull << tlog;
+        const uint32_t Umax = std::min<uint32_t>(n_occ, (uint32_t)tsize);
+        if ((rc = ensure(ctx, S_W_UINFO, ((uint64_t)Umax + 1) * 16, &uinfo))) return rc;
+        W.urep = (uint32_t *)uinfo;
+        W.ufreq = W.urep + Umax + 1;
+        W.ulen = W.ufreq + Umax + 1;
+        W.uoff = W.ulen + Umax + 1;
+        k_wassign<<<std::max<uint32_t>(1, std::min<uint64_t>(tsize / 256, 4096)), 256, 0, s>>>(W, (uint32_t)tsize);
+        BPE_CUDA(ctx, cudaMemcpyAsync(h_cnt, cnt, 16, cudaMemcpyDeviceToHost, s), "count read");
+        BPE_CUDA(ctx, cudaStreamSynchronize(s), "assign sync");
+        U = h_cnt[1];
+    }
+    uint32_t usym = 0;
+    if ((rc = scan_u32(ctx, W.ulen, U, W.uoff, W.bsum, W.counter + 3, &usym))) return rc;
+    if ((rc = ensure(ctx, S_W_SYM, (uint64_t)usym * 4 + 16, &wsym))) return rc;
+    W.wsym = (uint32_t *)wsym;
+    if (U) k_wgather<<<(U + 255) / 256, 256, 0, s>>>(W, U);
+
+    // 3. the merge loop over distinct words
+    const uint64_t T = 1ull << table_log2;
+    if ((rc = ensure(ctx, S_TABLE_KEY, T * 8, &tslot)) || (rc = ensure(ctx, S_TABLE_CNT, T * 8, &dense)) ||
+        (rc = ensure(ctx, S_BEST, (uint64_t)n_merges * 8, &best)) ||
+        (rc = ensure(ctx, S_LIST0, ((uint64_t)n_merges + 1) * 4, &dhist)))
+        return rc;
+    uint32_t *dkey = (uint32_t *)dense, *dcnt = dkey + T;
+    memset(h_state, 0, sizeof *h_state);
+    h_state->n_merges = n_merges;
+    BPE_CUDA(ctx, cudaMemcpyAsync(state, h_state, sizeof *h_state, cudaMemcpyHostToDevice, s), "state upload");
+    BPE_CUDA(ctx, cudaMemsetAsync(tslot, 0xFF, T * 8, s), "table clear");
+    BPE_CUDA(ctx, cudaMemsetAsync(dcnt, 0, T * 4, s), "count clear");
+    BPE_CUDA(ctx, cudaMemsetAsync(best, 0, (uint64_t)n_merges * 8, s), "best clear");
+    BPE_CUDA(ctx, cudaMemsetAsync(dhist, 0, ((uint64_t)n_merges + 1) * 4, s), "dhist clear");
+    TrainParams P{};
+    P.tslot = (unsigned long long *)tslot;
+    P.tmask = (uint32_t)(T - 1);
+    P.dkey = dkey;
+    P.dcnt = dcnt;
+    P.dcap = (uint32_t)T;
+    P.best = (unsigned long long *)best;
+    P.dhist = (uint32_t *)dhist;
+    P.st = (TrainState *)state;
+    const unsigned wgrid = std::max<uint32_t>(1, (U + kWThreads - 1) / kWThreads);
+    const unsigned agrid = (unsigned)ctx->sm_count * 2;
+    const bool profile = ctx->profile != 0;
+    const bool graph = ctx->use_graph && !profile;
+    const size_t n_prof = profile ? 2 + 2 * (size_t)n_merges : 0;
+    if ((rc = ensure_events(ctx, n_prof + kInFlight))) return rc;
+    std::vector<cudaEvent_t> poll_ev(kInFlight);
+    for (int i = 0; i < kInFlight; i++) poll_ev[i] = ctx->events[n_prof + i];
+
+    cudaGraphExec_t exec = nullptr;
+    if (graph) {
+        std::vector<uintptr_t> key = {0x57u /* word loop */, (uintptr_t)P.tslot, (uintptr_t)P.tmask, (uintptr_t)P.dkey,
+                                      (uintptr_t)P.dcnt, (uintptr_t)P.best, (uintptr_t)P.dhist, (uintptr_t)P.st,
+                                      (uintptr_t)W.wsym, (uintptr_t)W.ulen, (uintptr_t)W.counter, wgrid, agrid};
+        if (!(ctx->graph.exec && ctx->graph.key == key)) {
+            if (ctx->graph.exec) cudaGraphExecDestroy(ctx->graph.exec);
+            ctx->graph.exec = nullptr;
+            cudaStream_t cs = ctx->capture_stream;
+            BPE_CUDA(ctx, cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal), "begin capture");
+            for (uint32_t i = 0; i < kGraphIters; i++) {
+                k_argmax<<<agrid, kArgmaxThreads, 0, cs>>>(P, i);
+                k_wmerge<<<wgrid, kWThreads, 0, cs>>>(P, W, i);
+            }
+            k_advance<<<1, 1, 0, cs>>>(P.st, kGraphIters);
+            cudaGraph_t g = nullptr;
+            cudaError_t e = cudaStreamEndCapture(cs, &g);
+            if (e != cudaSuccess) return cuda_fail(ctx, e, "end capture");
+            e = cudaGraphInstantiate(&ctx->graph.exec, g, 0);
+            cudaGraphDestroy(g);
+            if (e != cudaSuccess) return cuda_fail(ctx, e, "graph instantiate");
+            ctx->graph.key = key;
+        }
+        exec = ctx->graph.exec;
+    }
+    if (profile) BPE_CUDA(ctx, cudaEventRecord(ctx->events[0], s), "event");
+    k_wcount<<<wgrid, kWThreads, 0, s>>>(P, W);
+    if (profile) BPE_CUDA(ctx, cudaEventRecord(ctx->events[1], s), "event");
+    uint32_t launched = 0;
+    uint64_t window = 0;
+    bool stopped = false;
+    while (launched < n_merges && !stopped) {
+        if (window >= (uint64_t)kInFlight) {
+            const int slot = (int)(window % kInFlight);
+            BPE_CUDA(ctx, cudaEventSynchronize(poll_ev[slot]), "poll sync");
+            if ((h_poll[slot] >> 32) == 0) stopped = true;
+            if (stopped) break;
+        }
+        const uint32_t end = std::min<uint32_t>(n_merges, launched + kGraphIters);
+        if (graph) {
+            BPE_CUDA(ctx, cudaGraphLaunch(exec, s), "graph launch");
+        } else {
+            for (uint32_t k = launched; k < end; k++) {
+                k_argmax<<<agrid, kArgmaxThreads, 0, s>>>(P, k);
+                if (profile) cudaEventRecord(ctx->events[2 + 2 * (size_t)k], s);
+                k_wmerge<<<wgrid, kWThreads, 0, s>>>(P, W, k);
+                if (profile) cudaEventRecord(ctx->events[3 + 2 * (size_t)k], s);
+            }
+        }
+        BPE_CUDA(ctx, cudaGetLastError(), "train launch");
+        const int slot = (int)(window % kInFlight);
+        BPE_CUDA(ctx, cudaMemcpyAsync(h_poll + slot, P.best + (end - 1), 8, cudaMemcpyDeviceToHost, s), "poll copy");
+        BPE_CUDA(ctx, cudaEventRecord(poll_ev[slot], s), "poll event");
+        launched = end;
+        window++;
+    }
+    BPE_CUDA(ctx, cudaMemcpyAsync(h_state, state, sizeof *h_state, cudaMemcpyDeviceToHost, s), "state read");
+    BPE_CUDA(ctx, cudaMemcpyAsync(h_best, best, (uint64_t)n_merges * 8, cudaMemcpyDeviceToHost, s), "best read");
+    BPE_CUDA(ctx, cudaMemcpyAsync(h_dhist, dhist, ((uint64_t)n_merges + 1) * 4, cudaMemcpyDeviceToHost, s),
+             "dhist read");
+    BPE_CUDA(ctx, cudaStreamSynchronize(s), "train sync");
+    if (h_state->err & DERR_TABLE_FULL) {
+        *table_full = true;
+        return fail(ctx, BPE_ERR_TABLE_FULL, "bpe_train: pair table of 2^%u slots overflowed", table_log2);
+    }
+    uint32_t done = 0;
+    while (done < n_merges && (h_best[done] >> 32) != 0) done++;
+    for (uint32_t k = 0; k < done; k++) {
+        const uint32_t key = ~(uint32_t)h_best[k];
+        h_merges_out[k].left = key >> 16;
+        h_merges_out[k].right = key & 0xFFFFu;
+        h_merges_out[k].new_id = 256u + k;
+        h_merges_out[k].count = (uint32_t)(h_best[k] >> 32);
+    }
+    *n_done = done;
+
+    // 4. the final stream (expanded over the occurrences) and its length
+    void *ooff;
+    if ((rc = ensure(ctx, S_W_OUTOFF, (uint64_t)n_occ * 8 + 16, &ooff))) return rc;
+    uint32_t *olen = (uint32_t *)ooff, *ooffs = olen + n_occ + 1;
+    if (n_occ) k_occ_len<<<(n_occ + 255) / 256, 256, 0, s>>>(W, n_occ, olen);
+    uint32_t total = 0;
+    if ((rc = scan_u32(ctx, olen, n_occ, ooffs, W.bsum, W.counter + 3, &total))) return rc;
+    if (n_final) *n_final = total;
+    if (d_symbols_final && n_occ) {
+        k_wexpand<<<(n_occ + 255) / 256, 256, 0, s>>>(W, n_occ, ooffs, d_symbols_final);
+        BPE_CUDA(ctx, cudaStreamSynchronize(s), "expand sync");
+    }
+
+    stats_reset(ctx);
+    ctx->stats.kernel_launches = 1 + (graph ? (uint64_t)window * (2 * kGraphIters + 1) : 2ull * launched);
+    const int sc = stats_slot(ctx, "word_count"), sa = stats_slot(ctx, "argmax"), sm = stats_slot(ctx, "word_merge");
+    ctx->stats.k[sc].launches = 1;
+    ctx->stats.k[sc].bytes = 8.0 * (double)usym;
+    const uint32_t ran = std::min<uint32_t>(n_merges, done + 1);
+    for (uint32_t k = 1; k < ran; k++) {
+        ctx->stats.k[sa].launches++;
+        ctx->stats.k[sa].bytes += 8.0 * (double)h_dhist[k];
+    }
+    ctx->stats.k[sm].launches = done;
+    ctx->stats.k[sm].bytes = 4.0 * (double)usym * done;   // every word read once per merge (upper bound)
+    if (profile) {
+        float x = 0;
+        if (cudaEventElapsedTime(&x, ctx->events[0], ctx->events[1]) == cudaSuccess) ctx->stats.k[sc].ms = x;
+        for (uint32_t k = 0; k < launched; k++) {
+            float a = 0, b = 0;
+            cudaEvent_t before = ctx->events[k ? 3 + 2 * (size_t)(k - 1) : 1];
+            if (k >= 1 && k < ran && cudaEventElapsedTime(&a, before, ctx->events[2 + 2 * (size_t)k]) == cudaSuccess)
+                ctx->stats.k[sa].ms += a;
+            if (k < done &&
+                cudaEventElapsedTime(&b, ctx->events[2 + 2 * (size_t)k], ctx->events[3 + 2 * (size_t)k]) == cudaSuccess)
+                ctx->stats.k[sm].ms += b;
+        }
+        cudaGetLastError();
+    }
+    return BPE_OK;
+}
+
 }  // namespace
 }  // namespace bpe
 
@@ -890,7 +1463,11 @@ extern "C" int bpe_train(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, ui
     if (automatic) lg = std::min<uint32_t>(22, std::max<uint32_t>(16, ceil_log2(n)));
     for (;;) {
         bool full = false;
-        int rc = train_once(ctx, d_symbols, n, n_merges, lg, h_merges_out, n_done, d_symbols_final, n_final, &full);
+        int rc = ctx->train_words
+                     ? train_words_once(ctx, d_symbols, n, n_merges, lg, h_merges_out, n_done, d_symbols_final,
+                                        n_final, &full)
+                     : train_once(ctx, d_symbols, n, n_merges, lg, h_merges_out, n_done, d_symbols_final, n_final,
+                                  &full);
         if (rc == BPE_OK || !full || !automatic || lg >= 28) return rc;
         lg += 2;   // automatic size was too small: retry with a larger table
     }

@@ -83,8 +83,13 @@ const char *bpe_last_error(const bpe_ctx *ctx);
  *                        bpe_train / trie_encode so bpe_last_stats() reports
  *                        per-kernel device time (implies host launches)
  *   BPE_OPT_CHUNK        trie_encode bytes per chunk (64..256, multiple
- *                        of 32; default 128) */
-enum { BPE_OPT_TABLE_LOG2 = 1, BPE_OPT_GRAPH = 2, BPE_OPT_PROFILE = 3, BPE_OPT_CHUNK = 4 };
+ *                        of 32; default 128)
+ *   BPE_OPT_TRAIN_WORDS  1 = bpe_train runs the merge loop over distinct
+ *                        words weighted by their number of occurrences
+ *                        (the same merges and final stream: no count or merge
+ *                        crosses a WORD_START); 0 = over the full symbol
+ *                        stream (default) */
+enum { BPE_OPT_TABLE_LOG2 = 1, BPE_OPT_GRAPH = 2, BPE_OPT_PROFILE = 3, BPE_OPT_CHUNK = 4, BPE_OPT_TRAIN_WORDS = 5 };
 int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value);
 
 /* Statistics of the last bpe_train or trie_encode call on this context.

@@ -342,3 +342,47 @@ def test_encode_batch_workload(ctx, golden):
     assert ids.numel() == g["n_ids"]
     assert sha(ids.cpu().numpy()) == g["ids_sha256"]
     assert sha(id_off.cpu().numpy().astype(np.uint64)) == g["id_off_sha256"]
+
+
+# --------------------------------------------- word-frequency training path --
+@pytest.fixture
+def words_ctx(ctx):
+    import bpe_trie_encode_gb300 as bt
+    ctx.set_option(bt.BPE_OPT_TRAIN_WORDS, 1)
+    yield ctx
+    ctx.set_option(bt.BPE_OPT_TRAIN_WORDS, 0)
+
+
+def test_words_worked_examples(words_ctx):
+    test_train_worked_examples(words_ctx)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_words_random_small(words_ctx, seed):
+    test_train_random_small(words_ctx, seed)
+
+
+@pytest.mark.parametrize("n", [2048 * 3 + 1, 1_000_001])
+def test_words_identical_runs(words_ctx, n):
+    test_train_identical_runs_cross_tiles(words_ctx, n)
+
+
+def test_words_alternating_ties_degenerate(words_ctx):
+    test_train_alternating_and_ties(words_ctx)
+    test_train_degenerate(words_ctx)
+
+
+def test_words_many_distinct_words(words_ctx):
+    # every word distinct: the distinct-word table holds one entry per occurrence
+    rng = np.random.default_rng(3)
+    words = [bytes(rng.integers(97, 123, rng.integers(1, 9)).astype(np.uint8)) for _ in range(40000)]
+    check_train(words_ctx, oracle.pretokenize(b" ".join(words)), 50)
+
+
+def test_words_tiny_med_workloads(words_ctx, golden):
+    train_workload(words_ctx, golden, "tiny", [0, 1, 10, 100])
+    train_workload(words_ctx, golden, "med", [1, 100, 1000])
+
+
+def test_words_large_workload(words_ctx, golden):
+    train_workload(words_ctx, golden, "large", [1000])
