@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--encode-bytes", type=int, default=None, help="encode only a prefix (profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the extra legs (word-frequency, large, batch)")
     return ap.parse_args()
 
 
@@ -183,6 +184,88 @@ def roofline(stats: dict, families: list[str], peak: float, peak_kind: str, traf
             "traffic": round(tr, 1) if tr is not None else None,
             "algorithmic_bytes_per_launch": round(per_launch_bytes, 1),
             "avg_launch_ms": round(s["ms"] / max(s["launches"], 1), 6)}
+
+
+def timed(stream, fn):
+    """Run fn() between two CUDA events on the stream; returns (result, ms)."""
+    import torch
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    r = fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return r, a.elapsed_time(b)
+
+
+def extra_legs(args, ctx, dev, stream, flush, d_text, d_sym, n_merges, peak, peak_kind):
+    import numpy as np
+    import torch
+
+    import bpe_trie_encode_gb300 as bt
+    import synth
+    out = {}
+    # word-frequency training of the same medium corpus
+    ctx.set_option(bt.BPE_OPT_TRAIN_WORDS, 1)
+    ctx.set_option(bt.BPE_OPT_PROFILE, 1)
+    ms_all, merges, kern = 0.0, 0, {}
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        (m, _), ms = timed(stream, lambda: (ctx.pretokenize(d_text, out=d_sym), ctx.train(d_sym, n_merges, final=False))[1])
+        if i >= args.warmup:
+            ms_all += ms
+            merges += m.shape[0]
+            for k2, v in ctx.stats().items():
+                if k2 != "kernel_launches":
+                    a = kern.setdefault(k2, {"launches": 0, "ms": 0.0})
+                    a["launches"] += v["launches"]
+                    a["ms"] += v["ms"]
+    out["train_words"] = {"value": round(merges / (ms_all / 1e3), 2), "unit": "merges/s",
+                          "ms_per_step": round(ms_all / args.steps, 3),
+                          "workload": f"{args.train} training by distinct words (identical merges)",
+                          "kernels": {k2: {"launches": v["launches"], "ms": round(v["ms"], 3)} for k2, v in kern.items()}}
+    # the large training workload (256 MiB, 32,000 merges), word-frequency path, one timed run
+    big = synth.corpus("large")
+    d_big = torch.from_numpy(big).to(dev)
+    d_bsym = torch.empty(big.size, dtype=torch.int32, device=dev)
+    ctx.set_option(bt.BPE_OPT_PROFILE, 0)
+    ctx.pretokenize(d_big, out=d_bsym)
+    ctx.train(d_bsym, 200, final=False)          # warm-up
+    flush.fill_(1)
+    torch.cuda.synchronize()
+    (m, _), ms = timed(stream, lambda: (ctx.pretokenize(d_big, out=d_bsym), ctx.train(d_bsym, 32000, final=False))[1])
+    out["train_large_words"] = {"value": round(m.shape[0] / (ms / 1e3), 2), "unit": "merges/s", "ms": round(ms, 3),
+                                "workload": f"large training: {big.size} B corpus, {m.shape[0]} merges, distinct words"}
+    ctx.set_option(bt.BPE_OPT_TRAIN_WORDS, 0)
+    del d_bsym
+    # the batch encode workload: 512 documents, 250,000-token substring vocabulary
+    vb, voff = synth.substring_vocab(big)
+    del big, d_big
+    data, doc_off = synth.batch_documents()
+    trie = ctx.trie_build(vb, voff)
+    d_data = torch.from_numpy(data).to(dev)
+    d_off = torch.from_numpy(doc_off.astype(np.int64)).to(dev)
+    ids = torch.empty(data.size, dtype=torch.int32, device=dev)
+    ctx.set_option(bt.BPE_OPT_PROFILE, 1)
+    ms_all, kern = 0.0, {}
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        (r, _), ms = timed(stream, lambda: (ctx.encode(trie, d_data, d_off, ids_out=ids), None))
+        if i >= args.warmup:
+            ms_all += ms
+            for k2, v in ctx.stats().items():
+                if k2 != "kernel_launches":
+                    a = kern.setdefault(k2, {"launches": 0, "bytes": 0.0, "ms": 0.0})
+                    for f in ("launches", "bytes", "ms"):
+                        a[f] += v[f]
+    ctx.set_option(bt.BPE_OPT_PROFILE, 0)
+    out["encode_batch"] = {"value": round(args.steps * data.size / (ms_all / 1e3) / 1e9, 3), "unit": "GB/s",
+                           "ms_per_step": round(ms_all / args.steps, 3),
+                           "workload": f"{doc_off.size - 1} documents, {data.size} B, 250,000-token substring vocabulary",
+                           "n_ids": int(r[0].numel()), "trie": trie.info(),
+                           "roofline": roofline(kern, ["encode_spec", "encode_emit"], peak, peak_kind, {})}
+    return out
 
 
 # ---------------------------------------------------------------- ours ------
@@ -328,6 +411,12 @@ def run_ours(args, rank, world, local_rank):
             e2e["encode"] = {"value": round(args.steps * enc["bytes"] * world / (en_ms / 1e3) / 1e9, 3),
                              "unit": "GB/s"}
 
+    # ---- extra legs: the word-frequency trainer (same merges), the large
+    # training workload, the batch encode workload
+    extra = {}
+    if not args.no_extra:
+        extra = extra_legs(args, ctx, dev, stream, flush, d_text, d_sym, n_merges, peak, peak_kind)
+
     # ---- CPU baseline: the oracle as it stands, rank 0, N == 1 only
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -360,6 +449,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
+    out.update(extra)
     if enc:
         gbs = args.steps * enc["bytes"] * world / (enc_ms / 1e3) / 1e9
         out["encode"] = {"value": round(gbs, 3), "unit": "GB/s", "ms_per_step": round(enc_ms / args.steps, 3),

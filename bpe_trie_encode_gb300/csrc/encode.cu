@@ -21,10 +21,15 @@
 //                   exit (the next chunk's nominal entry is then wrong).
 //                   The first chunk of a CTA gets its nominal entry from a halo
 //                   thread that parses the chunk before it.
-//   k_repair        only when some chunk was flagged (rare: the two parses of a
-//                   chunk never meet inside it): one thread walks the flagged
-//                   chains in order, re-parsing chunks from their true entries
-//                   until an exit agrees with the nominal entry again.
+//   k_repair_walk   only when some chunk was flagged (rare: the two parses of a
+//                   chunk never meet inside it): one thread per flagged chunk
+//                   re-parses the chunks after it, from that chunk's exit,
+//                   until an exit agrees with the next nominal entry again,
+//                   and keeps the chain privately.
+//   k_repair_apply  one CTA sorts the flagged chunks and, in order, writes the
+//                   chains of those whose own entry is true (a flagged chunk
+//                   inside an applied chain is skipped); with more flags than
+//                   the list holds it walks the chains sequentially instead.
 //   k_emit          exclusive scan of the chunk counts (CTA scan + decoupled
 //                   look-back over tiles taken in ticket order) and a final
 //                   parse of every chunk from its true entry that writes ids at
@@ -54,6 +59,7 @@ struct EncState {
     unsigned long long total;
     uint32_t err;        // DERR_* bits
     uint32_t any_flag;   // some chunk's exit disagreed with the next nominal entry
+    uint32_t flist_len;  // flagged chunks appended to the list
     uint32_t ticket;
     uint32_t bad_doc_off;
     unsigned long long span;     // doc_off[n_docs] - doc_off[0]
@@ -73,6 +79,9 @@ struct EncParams {
     uint32_t *exit_rel;          // per chunk: true exit - chunk start
     uint32_t *spec_rel;          // per chunk: spec exit - chunk start
     uint32_t *flag;              // bitmap of flagged chunks
+    uint32_t *flist;             // flagged chunks, unordered (flist_cap entries; 0 = none kept)
+    uint32_t flist_cap;
+    uint32_t *wpriv;             // per flagged chunk: its repair walk (kWalkWords words)
     unsigned long long *prefix;  // per chunk: global index of its first id
     unsigned long long *status;  // look-back words per emit tile
     int32_t *ids;
@@ -354,6 +363,8 @@ __global__ void __launch_bounds__(kSpecThreads) k_spec(EncParams P, unsigned lon
     if (exit != spec_exit) {
         atomicOr(P.flag + (k >> 5), 1u << (k & 31));
         P.st->any_flag = 1u;
+        const uint32_t i = atomicAdd(&P.st->flist_len, 1u);
+        if (i < P.flist_cap) P.flist[i] = (uint32_t)k;
     }
 }
 
@@ -371,42 +382,127 @@ __device__ uint32_t parse_from(const EncParams &P, const int4 *lut, uint64_t e, 
     return c;
 }
 
-__global__ void k_repair(EncParams P, unsigned long long n_chunks) {
+// Sequential repair from flagged chunk f (whose entry is true): re-parse the
+// chunks after it from their true entries until an exit agrees with the next
+// chunk's nominal entry again or the document ends.  Returns the last chunk
+// rewritten (f if none).
+__device__ unsigned long long repair_chain(const EncParams &P, const int4 *lut, unsigned long long f,
+                                           unsigned long long n_chunks) {
+    const ChunkGeo gf = chunk_geo(P, f);
+    uint64_t e = gf.cs + P.exit_rel[f];
+    unsigned long long c = f + 1;
+    for (; c < n_chunks; c++) {
+        const ChunkGeo g = chunk_geo(P, c);
+        if (g.doc_first) break;           // next document: entry resets
+        uint64_t x;
+        P.count[c] = parse_from(P, lut, e, g.ce, g.de, &x);
+        P.exit_rel[c] = (uint32_t)(x - g.cs);
+        if (x == g.cs + P.spec_rel[c]) return c;   // agrees with the next nominal entry
+        e = x;
+    }
+    return c - 1;
+}
+
+constexpr int kWalkMax = 8;                    // chunks a parallel walker records
+constexpr int kWalkWords = 2 + 2 * kWalkMax;   // length, "continues", (count, exit) pairs
+constexpr uint32_t kFlagListCap = 4096;
+
+// One walker per flagged chunk, all in parallel: the chain as it would be if
+// the chunk's entry is true, recorded privately (up to kWalkMax chunks).
+__global__ void k_repair_walk(EncParams P, unsigned long long n_chunks) {
     __shared__ int4 lut[256];
-    if (!P.st->any_flag) return;
+    const uint32_t L = P.st->flist_len;
+    if (L == 0 || L > P.flist_cap) return;
     load_lut(P, lut);
     __syncthreads();
-    if (threadIdx.x != 0) return;
-    unsigned long long k = 0;
-    for (;;) {
-        // next flagged chunk at or after k
-        unsigned long long w = k >> 5;
-        const unsigned long long nw = (n_chunks + 31) >> 5;
-        uint32_t bitsw = w < nw ? (P.flag[w] & (~0u << (k & 31))) : 0u;
-        while (w < nw && bitsw == 0) {
-            ++w;
-            if (w < nw) bitsw = P.flag[w];
-        }
-        if (w >= nw) break;
-        const unsigned long long f = (w << 5) + (unsigned long long)(__ffs(bitsw) - 1);
-        if (f >= n_chunks) break;
-        // chunk f has a true entry; its exit (true) disagrees with the next nominal entry
-        ChunkGeo gf = chunk_geo(P, f);
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < L; i += gridDim.x * blockDim.x) {
+        const unsigned long long f = P.flist[i];
+        uint32_t *w = P.wpriv + (size_t)i * kWalkWords;
+        const ChunkGeo gf = chunk_geo(P, f);
         uint64_t e = gf.cs + P.exit_rel[f];
-        unsigned long long c = f + 1;
-        for (; c < n_chunks; c++) {
+        uint32_t m = 0, more = 0;
+        for (unsigned long long c = f + 1; c < n_chunks; c++) {
             const ChunkGeo g = chunk_geo(P, c);
-            if (g.doc_first) break;           // next document: entry resets, chunk c is fine
-            uint64_t x;
-            P.count[c] = parse_from(P, lut, e, g.ce, g.de, &x);
-            P.exit_rel[c] = (uint32_t)(x - g.cs);
-            if (x == g.cs + P.spec_rel[c]) {  // agrees with the next nominal entry again
-                ++c;
+            if (g.doc_first) break;
+            if (m == kWalkMax) {
+                more = 1;
                 break;
             }
+            uint64_t x;
+            w[2 + 2 * m] = parse_from(P, lut, e, g.ce, g.de, &x);
+            w[3 + 2 * m] = (uint32_t)(x - g.cs);
+            ++m;
+            if (x == g.cs + P.spec_rel[c]) break;
             e = x;
         }
-        k = c;   // chunks before c are settled; c itself keeps its own flag
+        w[0] = m;
+        w[1] = more;
+    }
+}
+
+// Apply the walks of flagged chunks whose entry is true: in chunk order, a
+// flagged chunk inside the chain of an earlier applied one has a wrong entry
+// and is skipped.  With more flags than the list holds, repair sequentially.
+__global__ void __launch_bounds__(1024) k_repair_apply(EncParams P, unsigned long long n_chunks) {
+    __shared__ int4 lut[256];
+    __shared__ unsigned long long keys[kFlagListCap];
+    const uint32_t L = P.st->flist_len;
+    if (L == 0) return;
+    load_lut(P, lut);
+    if (L > P.flist_cap) {   // sequential repair over the flag bitmap
+        __syncthreads();
+        if (threadIdx.x != 0) return;
+        const unsigned long long nw = (n_chunks + 31) >> 5;
+        unsigned long long k = 0;
+        for (;;) {
+            unsigned long long w = k >> 5;
+            uint32_t bitsw = w < nw ? (P.flag[w] & (~0u << (k & 31))) : 0u;
+            while (w < nw && bitsw == 0) {
+                ++w;
+                if (w < nw) bitsw = P.flag[w];
+            }
+            if (w >= nw) break;
+            const unsigned long long f = (w << 5) + (unsigned long long)(__ffs(bitsw) - 1);
+            if (f >= n_chunks) break;
+            k = repair_chain(P, lut, f, n_chunks) + 1;
+        }
+        return;
+    }
+    uint32_t n2 = 1;
+    while (n2 < L) n2 <<= 1;
+    for (uint32_t i = threadIdx.x; i < n2; i += blockDim.x)
+        keys[i] = i < L ? (((unsigned long long)P.flist[i] << 12) | i) : ~0ull;
+    __syncthreads();
+    for (uint32_t k = 2; k <= n2; k <<= 1) {   // bitonic sort by chunk index
+        for (uint32_t j = k >> 1; j > 0; j >>= 1) {
+            for (uint32_t t = threadIdx.x; t < n2; t += blockDim.x) {
+                const uint32_t x = t ^ j;
+                if (x > t) {
+                    const bool up = (t & k) == 0;
+                    const unsigned long long a = keys[t], b = keys[x];
+                    if ((a > b) == up) {
+                        keys[t] = b;
+                        keys[x] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    if (threadIdx.x != 0) return;
+    long long cur_end = -1;   // last chunk settled by an applied chain
+    for (uint32_t q = 0; q < L; q++) {
+        const unsigned long long f = keys[q] >> 12;
+        const uint32_t i = (uint32_t)(keys[q] & 0xFFFu);
+        if ((long long)f <= cur_end) continue;
+        const uint32_t *w = P.wpriv + (size_t)i * kWalkWords;
+        const uint32_t m = w[0];
+        for (uint32_t r = 0; r < m; r++) {
+            P.count[f + 1 + r] = w[2 + 2 * r];
+            P.exit_rel[f + 1 + r] = w[3 + 2 * r];
+        }
+        cur_end = (long long)(f + m);
+        if (w[1]) cur_end = (long long)repair_chain(P, lut, f + m, n_chunks);   // a long chain goes on
     }
 }
 
@@ -560,7 +656,8 @@ extern "C" int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_
     if ((rc = ensure(ctx, S_ENC_CHUNK_INFO, nc * 12, &info)) ||
         (rc = ensure(ctx, S_ENC_NOTOK, ((nc + 31) / 32) * 4, &flag)) ||
         (rc = ensure(ctx, S_ENC_STATUS, emit_tiles * 8, &status)) ||
-        (rc = ensure(ctx, S_ENC_PREFIX, nc * 8 + ((uint64_t)n_docs + 1) * 8, &prefix)))
+        (rc = ensure(ctx, S_ENC_PREFIX, nc * 8 + ((uint64_t)n_docs + 1) * 8 +
+                                                (uint64_t)kFlagListCap * (1 + kWalkWords) * 4, &prefix)))
         return rc;
     P.chunk_start = (const unsigned long long *)cstart;   // (ensure may not move it: distinct slot)
     P.count = (uint32_t *)info;
@@ -570,6 +667,9 @@ extern "C" int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_
     P.status = (unsigned long long *)status;
     P.prefix = (unsigned long long *)prefix;
     idoff_tmp = (unsigned long long *)prefix + nc;
+    P.flist = (uint32_t *)((unsigned long long *)idoff_tmp + n_docs + 1);
+    P.flist_cap = kFlagListCap;
+    P.wpriv = P.flist + kFlagListCap;
     P.id_off = d_id_off_out ? (unsigned long long *)d_id_off_out : (unsigned long long *)idoff_tmp;
 
     BPE_CUDA(ctx, cudaMemsetAsync(flag, 0, ((nc + 31) / 32) * 4, s), "flag clear");
@@ -585,7 +685,8 @@ extern "C" int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_
     if (profile) cudaEventRecord(ctx->events[2], s);
     k_spec<<<(unsigned)spec_blocks, kSpecThreads, spec_smem, s>>>(P, nc, text_end);
     if (profile) cudaEventRecord(ctx->events[3], s);
-    k_repair<<<1, 256, 0, s>>>(P, nc);
+    k_repair_walk<<<16, 256, 0, s>>>(P, nc);
+    k_repair_apply<<<1, 1024, 0, s>>>(P, nc);
     if (profile) cudaEventRecord(ctx->events[4], s);
     k_emit<<<(unsigned)emit_grid, kEmitThreads, emit_smem, s>>>(P, nc, text_end);
     if (profile) cudaEventRecord(ctx->events[5], s);
@@ -604,7 +705,7 @@ extern "C" int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_
     ctx->stats.k[a].launches = 1;
     ctx->stats.k[b].launches = 1;
     const uint64_t in_bytes = h->span;
-    ctx->stats.kernel_launches = 5;
+    ctx->stats.kernel_launches = 6;
     ctx->stats.k[a].bytes = (double)in_bytes;
     ctx->stats.k[b].bytes = (double)in_bytes + 4.0 * (double)total;
     if (profile) {
@@ -644,7 +745,8 @@ constexpr size_t kNaOffFlag = na_align(kNaOffInfo + 12 * kNaMaxChunks);
 constexpr size_t kNaOffStatus = na_align(kNaOffFlag + kNaMaxChunks / 8);
 constexpr size_t kNaOffPrefix = na_align(kNaOffStatus + 8 * (kNaMaxChunks / kEmitThreads + 1));
 constexpr size_t kNaOffIdOff = na_align(kNaOffPrefix + 8 * kNaMaxChunks);
-constexpr size_t kNaBytes = na_align(kNaOffIdOff + 8 * ((size_t)kNaMaxDocs + 1));   // about 11.6 MB
+constexpr size_t kNaOffFlist = na_align(kNaOffIdOff + 8 * ((size_t)kNaMaxDocs + 1));
+constexpr size_t kNaBytes = na_align(kNaOffFlist + 4 * (size_t)kFlagListCap * (1 + kWalkWords));   // about 11.9 MB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaBytes];
 
@@ -702,6 +804,9 @@ int noalloc_body(const bpe_trie *trie, const uint8_t *d_bytes, const uint64_t *d
     P.status = (unsigned long long *)(base + kNaOffStatus);
     P.prefix = (unsigned long long *)(base + kNaOffPrefix);
     P.id_off = d_id_off_out ? (unsigned long long *)d_id_off_out : (unsigned long long *)(base + kNaOffIdOff);
+    P.flist = (uint32_t *)(base + kNaOffFlist);
+    P.flist_cap = kFlagListCap;
+    P.wpriv = P.flist + kFlagListCap;
 
     // the array keeps the previous call's contents: zero what must start at zero
     if (cudaMemsetAsync(P.st, 0, sizeof(EncState), s) != cudaSuccess) return BPE_ERR_CUDA;
@@ -731,7 +836,8 @@ int noalloc_body(const bpe_trie *trie, const uint8_t *d_bytes, const uint64_t *d
         return BPE_ERR_CUDA;
     const uint64_t text_end = h.span + h.text_lo;
     k_spec<<<(unsigned)spec_blocks, kSpecThreads, spec_smem, s>>>(P, nc, text_end);
-    k_repair<<<1, 256, 0, s>>>(P, nc);
+    k_repair_walk<<<16, 256, 0, s>>>(P, nc);
+    k_repair_apply<<<1, 1024, 0, s>>>(P, nc);
     k_emit<<<(unsigned)emit_tiles, kEmitThreads, emit_smem, s>>>(P, nc, text_end);
     k_doc_offsets<<<(unsigned)((n_docs + 1 + 255) / 256), 256, 0, s>>>(P, nc);
     if (cudaGetLastError() != cudaSuccess) return BPE_ERR_CUDA;

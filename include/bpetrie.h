@@ -197,7 +197,7 @@ int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_bytes,
  * Same inputs, outputs, result and errors as trie_encode, but no context is
  * used and nothing is allocated (no cudaMalloc, cudaFree, pinned host memory
  * or allocating library routine): the scratch lives in one fixed array inside
- * the library, about 11.6 MB, which every GPU that loads the library holds
+ * the library, about 11.9 MB, which every GPU that loads the library holds
  * until the process exits.  The work is ordered on `cuda_stream` (a
  * cudaStream_t, NULL = legacy default stream); the trie's device is made
  * current for the call and the caller's current device is restored.

@@ -283,6 +283,33 @@ def test_encode_parses_that_never_meet(ctx):
     check_encode(ctx, vb, off, [b"a" * 100001 + b"b", b"a" * 1000, b"ba" * 3000])
 
 
+def parity_shift_docs(rng, n_docs, lengths, c_rate):
+    """Documents over {a, c} for the vocabulary {c, a, aa}: a 'c' moves the
+    parse of the 'a' runs after it to the other parity, so a speculative parse
+    from an even chunk start never meets the true one.  Chunks are flagged
+    where the parity flips, and chains run until the next flip."""
+    docs = []
+    for _ in range(n_docs):
+        n = rng.choice(lengths)
+        docs.append(bytes(99 if (i == 0 or rng.random() < c_rate) else 97 for i in range(n)))
+    return docs
+
+
+PARITY_VOCAB = [bytes([b]) for b in range(256)] + [b"aa"]
+
+
+@pytest.mark.parametrize("n_docs,lengths,c_rate", [
+    (3000, [129, 300, 513], 0.0),      # one flag per document, under the flag list's capacity
+    (5000, [300], 0.0),                # more flags than the list holds: sequential repair
+    (4, [3000, 20000], 0.0),           # chains much longer than a walker records
+    (64, [1, 2, 127, 128, 129, 5000], 0.004),   # flips at random: flagged chunks inside chains
+])
+def test_encode_repair_paths(ctx, n_docs, lengths, c_rate):
+    rng = random.Random(n_docs * 7 + len(lengths))
+    vb, off = vocab_arrays(PARITY_VOCAB)
+    check_encode(ctx, vb, off, parity_shift_docs(rng, n_docs, lengths, c_rate))
+
+
 def test_encode_capacity_error(ctx):
     import bpe_trie_encode_gb300 as bt
     toks = [bytes([b]) for b in range(256)]

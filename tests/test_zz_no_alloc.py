@@ -34,6 +34,11 @@ def _noalloc(lib, trie, data, doc_off, cap):
     return rc, ids[: n.value], id_off
 
 
+def _vocab(tokens):
+    vb = np.frombuffer(b"".join(tokens), dtype=np.uint8).copy()
+    return vb, np.cumsum([0] + [len(t) for t in tokens]).astype(np.uint64)
+
+
 def test_noalloc_encode_matches_trie_encode():
     import bpe_trie_encode_gb300 as bt
     from bpe_trie_encode_gb300 import _capi
@@ -54,6 +59,19 @@ def test_noalloc_encode_matches_trie_encode():
         doc_off = torch.tensor(np.cumsum([0] + [len(d) for d in docs]), dtype=torch.int64, device="cuda")
         want_ids, want_off = ctx.encode(trie, data, doc_off)
         rc, ids, id_off = _noalloc(lib, trie, data, doc_off, data.numel())
+        assert rc == 0
+        assert torch.equal(ids, want_ids)
+        assert torch.equal(id_off, want_off)
+
+    # documents whose parses flip parity at their first byte flag one chunk
+    # each: the repair runs from the flag list, then past its capacity
+    ptrie = ctx.trie_build(*_vocab([bytes([b]) for b in range(256)] + [b"aa"]))
+    for n_docs in (3000, 5000, 300):
+        docs = [b"c" + b"a" * (299 + d % 7) for d in range(n_docs)]
+        data = torch.from_numpy(np.frombuffer(b"".join(docs), dtype=np.uint8).copy()).cuda()
+        doc_off = torch.tensor(np.cumsum([0] + [len(d) for d in docs]), dtype=torch.int64, device="cuda")
+        want_ids, want_off = ctx.encode(ptrie, data, doc_off)
+        rc, ids, id_off = _noalloc(lib, ptrie, data, doc_off, data.numel())
         assert rc == 0
         assert torch.equal(ids, want_ids)
         assert torch.equal(id_off, want_off)
