@@ -11,8 +11,10 @@ One step is one pass of the whole hot path over one batch of synthetic input:
 ``value`` is the train leg's merges/s (the medium training workload is the
 headline configuration); the encode leg is reported in ``encode``.  Inputs are
 resident in HBM when the timed region starts; L2 is flushed between steps.
-Kernel durations come from CUDA events recorded after every kernel on the
-launching stream (the library's profile option) inside the timed region.
+The timed steps replay merge windows from CUDA graphs, as a caller runs them.
+Kernel durations (roofline, per-kernel table) come from the same steps run
+again with a CUDA event recorded after every kernel on the launching stream
+(the library's profile option, host launches).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -206,20 +208,23 @@ def extra_legs(args, ctx, dev, stream, flush, d_text, d_sym, n_merges, peak, pea
     out = {}
     # word-frequency training of the same medium corpus
     ctx.set_option(bt.BPE_OPT_TRAIN_WORDS, 1)
-    ctx.set_option(bt.BPE_OPT_PROFILE, 1)
     ms_all, merges, kern = 0.0, 0, {}
-    for i in range(args.warmup + args.steps):
-        flush.fill_(1)
-        torch.cuda.synchronize()
-        (m, _), ms = timed(stream, lambda: (ctx.pretokenize(d_text, out=d_sym), ctx.train(d_sym, n_merges, final=False))[1])
-        if i >= args.warmup:
-            ms_all += ms
-            merges += m.shape[0]
-            for k2, v in ctx.stats().items():
-                if k2 != "kernel_launches":
-                    a = kern.setdefault(k2, {"launches": 0, "ms": 0.0})
-                    a["launches"] += v["launches"]
-                    a["ms"] += v["ms"]
+    for prof in (False, True):   # timed graph replay, then one profiled step for the kernel split
+        ctx.set_option(bt.BPE_OPT_PROFILE, 1 if prof else 0)
+        for i in range(1 if prof else args.warmup + args.steps):
+            flush.fill_(1)
+            torch.cuda.synchronize()
+            (m, _), ms = timed(stream, lambda: (ctx.pretokenize(d_text, out=d_sym),
+                                                ctx.train(d_sym, n_merges, final=False))[1])
+            if prof:
+                for k2, v in ctx.stats().items():
+                    if k2 != "kernel_launches":
+                        a = kern.setdefault(k2, {"launches": 0, "ms": 0.0})
+                        a["launches"] += v["launches"]
+                        a["ms"] += v["ms"]
+            elif i >= args.warmup:
+                ms_all += ms
+                merges += m.shape[0]
     out["train_words"] = {"value": round(merges / (ms_all / 1e3), 2), "unit": "merges/s",
                           "ms_per_step": round(ms_all / args.steps, 3),
                           "workload": f"{args.train} training by distinct words (identical merges)",
@@ -347,7 +352,7 @@ def run_ours(args, rank, world, local_rank):
                         a[f] += v[f]
             acc["n_ids"] = n_ids
 
-    ctx.set_option(bt.BPE_OPT_PROFILE, 1)
+    # timed steps: graph replay, as a caller runs it
     dummy = {"train_ms": 0, "enc_ms": 0, "merges": 0, "launches": 0, "kern": {}}
     for _ in range(args.warmup):
         step(False, dummy)
@@ -364,7 +369,15 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     clk = clocks.stop() if clocks else None
+    # per-kernel device time for the roofline: the same steps again with a
+    # CUDA event after every kernel on the launching stream (host launches)
+    ctx.set_option(bt.BPE_OPT_PROFILE, 1)
+    prof = {"train_ms": 0.0, "enc_ms": 0.0, "merges": 0, "launches": 0, "kern": {}, "n_ids": 0}
+    step(False, dummy)
+    for _ in range(max(1, min(args.steps, 2))):
+        step(True, prof)
     ctx.set_option(bt.BPE_OPT_PROFILE, 0)
+    acc["kern"] = prof["kern"]
 
     t = torch.tensor([acc["train_ms"], acc["enc_ms"]], dtype=torch.float64, device=dev)
     if world > 1:
@@ -442,6 +455,8 @@ def run_ours(args, rank, world, local_rank):
                   "roofline": roofline(kern, ["pair_count", "merge_compact"], peak, peak_kind, traffic)},
         "roofline": roofline(kern, ["pair_count", "merge_compact"], peak, peak_kind, traffic),
         "gpu_launches": acc["launches"],
+        "timing": ("value, e2e: CUDA-graph replay as a caller runs it; roofline and kernels: per-kernel CUDA "
+                   "events on the launching stream in a separate profiled pass of the same steps"),
         "kernels": {k: {"launches": v["launches"], "ms": round(v["ms"], 3),
                         "GB/s": round(v["bytes"] / (v["ms"] / 1e3) / 1e9, 1) if v["ms"] else None}
                     for k, v in kern.items()},

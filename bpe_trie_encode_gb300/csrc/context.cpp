@@ -155,6 +155,12 @@ extern "C" int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value) {
     case BPE_OPT_TRAIN_WORDS:
         ctx->train_words = value ? 1 : 0;
         return BPE_OK;
+    case BPE_OPT_MERGE_LOOKBACK:
+        ctx->merge_lookback = value ? 1 : 0;
+        return BPE_OK;
+    case BPE_OPT_PERSISTENT:
+        ctx->persistent = value ? 1 : 0;
+        return BPE_OK;
     case BPE_OPT_CHUNK:
         if (value < 64 || value > 256 || value % 32)
             return fail(ctx, BPE_ERR_INVALID_ARG, "chunk %lld not in 64..256 or not a multiple of 32",

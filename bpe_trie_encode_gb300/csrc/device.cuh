@@ -33,6 +33,16 @@ __device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long lon
     return v;
 }
 
+// Acquire / release 32-bit words at GPU scope (grid barrier).
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *a) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t *a, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
 // Weak 64-bit load served by L2 (no L1, no ordering): independent loads of
 // look-back status words overlap; each word is one aligned 64-bit value, so a
 // reader sees it either before or after its single store.

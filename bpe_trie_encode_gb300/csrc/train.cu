@@ -61,7 +61,13 @@ constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
 constexpr int kMergeItems = 16;
 constexpr int kMergeTile = kMergeThreads * kMergeItems;  // 4,096 symbols per tile
-constexpr int kDeltaSlots = 1024;                 // shared delta table per merge CTA (8 KiB)
+// Warp-contiguous layout of a tile for l != r: warp w owns the 512 positions
+// from wb = base + 512 w, in 4 rounds of 128; in round q lane L holds the 4
+// positions p0 = wb + 128 q + 4 L .. p0 + 3 (one coalesced 128-bit load).
+constexpr int kRounds = 4;
+constexpr int kWarpSpan = 128 * kRounds;   // 512 positions per warp and tile
+static_assert(kWarpSpan * kMergeWarps == kMergeTile, "tile geometry");
+constexpr int kDeltaSlots = 2048;                 // shared delta table per merge CTA (16 KiB)
 constexpr int kTileHalo = 16;                     // symbols staged past a tile
 // Shared-memory tile layout: one padding word after every 16 symbols, so a
 // thread reading its 16 consecutive symbols hits 32 different banks.
@@ -70,6 +76,8 @@ __device__ __forceinline__ int padded(int i) { return i + (i >> 4); }
 static_assert(kMergeItems == 16, "the padded tile layout assumes 16 symbols per thread");
 constexpr int kArgmaxThreads = 256;
 constexpr int kGraphIters = 32;                   // merge iterations per captured graph
+constexpr int kLoopIters = 64;                    // merge iterations per persistent launch
+constexpr int kBarGroups = 16;                    // first level of the grid barrier
 constexpr int kPadSymbols = 64;                   // readable slack past the stream end
 constexpr unsigned kSpinLimit = 1u << 22;         // look-back spins before giving up
 constexpr int kInFlight = 3;                      // graph launches in flight before polling
@@ -82,6 +90,11 @@ struct TrainState {
     uint32_t dense_len;       // entries of the dense key/count arrays
     unsigned long long n[2];  // stream length, by merge parity
     uint32_t ticket[2];       // tile tickets, by merge parity
+    uint32_t msum_done;       // k_msum CTAs finished (the last one scans)
+    // grid barrier of the persistent merge loop: kBarGroups arrival counters,
+    // the groups' counter and the release generation, each on its own
+    // 128-byte line so arrivals and polling do not queue at one L2 slice
+    alignas(128) uint32_t bar[32 * (kBarGroups + 2)];
 };
 
 struct TrainParams {
@@ -92,6 +105,8 @@ struct TrainParams {
     uint32_t *dcnt;              // dense counts
     uint32_t dcap;
     unsigned long long *status[2];
+    unsigned long long *rsum;    // two-pass merge: per-range summaries
+    unsigned long long *rpre;    // two-pass merge: entering flag | offset << 1 per range
     unsigned long long *best;    // per merge: count << 32 | ~key ; 0 = stop
     unsigned long long *nhist;   // stream length after k merges
     uint32_t *dhist;             // dense entries scanned by argmax k
@@ -254,12 +269,23 @@ __global__ void __launch_bounds__(kArgmaxThreads) k_argmax(TrainParams p, uint32
     if ((p.best[k - 1] >> 32) == 0) return;   // training has stopped
     const uint32_t D = st->dense_len;
     if (blockIdx.x == 0 && threadIdx.x == 0) p.dhist[k] = D;
+    // four counts per 128-bit load (entries past D are 0); a key is read only
+    // for the largest count of the four (and its ties)
     unsigned long long b = 0;
-    for (uint32_t i = blockIdx.x * kArgmaxThreads + threadIdx.x; i < D; i += gridDim.x * kArgmaxThreads) {
-        const uint32_t c = __ldcg(p.dcnt + i);
-        if (c != 0) {
-            const unsigned long long v = pack_best(c, __ldcg(p.dkey + i));
-            b = v > b ? v : b;
+    const uint32_t D4 = (D + 3) / 4;
+    for (uint32_t i = blockIdx.x * kArgmaxThreads + threadIdx.x; i < D4; i += gridDim.x * kArgmaxThreads) {
+        const uint4 c = __ldcg(reinterpret_cast<const uint4 *>(p.dcnt) + i);
+        uint32_t cm = c.x > c.y ? c.x : c.y;
+        cm = cm > c.z ? cm : c.z;
+        cm = cm > c.w ? cm : c.w;
+        if (cm == 0 || cm < (uint32_t)(b >> 32)) continue;
+        const uint32_t cs[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            if (cs[j] == cm) {
+                const unsigned long long v = pack_best(cm, __ldcg(p.dkey + 4 * i + j));
+                b = v > b ? v : b;
+            }
         }
     }
     b = warp_max_u64(b);
@@ -422,6 +448,187 @@ __device__ __noinline__ void thread_deltas(const Table p, uint32_t *dkey, uint32
     }
 }
 
+// Stage a tile (kMergeTile symbols from base) and its halo into padded shared
+// memory with coalesced 128-bit loads; symbols at or past n read as 0.
+__device__ __forceinline__ void stage_tile(uint32_t *stile, const uint32_t *in, uint64_t base, uint64_t n, int tid) {
+#pragma unroll
+    for (int q = 0; q < (kMergeTile + kTileHalo) / (4 * kMergeThreads) + 1; q++) {
+        const int i4 = tid + q * kMergeThreads;
+        if (i4 < (kMergeTile + kTileHalo) / 4) {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (base + 4ull * i4 < n) v = __ldcg(reinterpret_cast<const uint4 *>(in + base + 4ull * i4));
+            uint32_t *d = stile + padded(4 * i4);   // 4 symbols never straddle a padding word
+            d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+        }
+    }
+}
+
+// Valid starts among a thread's 16 positions and the 2 after them (bit j:
+// position pos + j, j = 0 .. 17), from the staged tile.
+__device__ __forceinline__ uint32_t staged_valid(const uint32_t *mys, uint64_t pos, uint64_t n, uint32_t l, uint32_t r) {
+    uint32_t isl = 0, isr = 0;   // id == l ; id == r without WORD_START
+#pragma unroll
+    for (int j = 0; j < kMergeItems + 3; j++) {
+        const uint32_t x = mys[j < 16 ? j : j + 1];
+        isl |= (uint32_t)((x & 0xFFFFu) == l) << j;
+        isr |= (uint32_t)((x & 0x1FFFFu) == r) << j;
+    }
+    uint32_t valid = isl & (isr >> 1) & 0x3FFFFu;
+    if (pos >= n) return 0u;
+    const uint64_t lim = n - pos;   // positions pos+j with j + 1 < lim
+    if (lim < kMergeItems + 3) valid &= (1u << (uint32_t)(lim - 1)) - 1u;
+    return valid;
+}
+
+// Summary of one thread's 16 positions given their valid starts.
+__device__ __forceinline__ uint32_t thread_summary(uint32_t valid, uint64_t pos, uint64_t n) {
+    uint32_t kept[2], fout[2];
+#pragma unroll
+    for (uint32_t c = 0; c < 2; c++) {
+        uint32_t par = c, kc = 0;
+#pragma unroll
+        for (int j = 0; j < kMergeItems; j++) {
+            if (pos + j < n) kc += par ^ 1u;
+            par = ((valid >> j) & 1u) ? (par ^ 1u) : 0u;
+        }
+        kept[c] = kc;
+        fout[c] = par;
+    }
+    return sum_pack(fout[0] | (fout[1] << 1), kept[0], kept[1]);
+}
+
+// Summary of a tile that owns no valid start: parity is 0 after every item,
+// and only the first symbol can be consumed (by a merge just before the tile).
+__device__ __forceinline__ uint32_t plain_tile_summary(uint32_t tile_len) {
+    return sum_pack(0u, tile_len, tile_len - 1);
+}
+
+// In-tile ordered exclusive scan of the threads' summaries (all threads call
+// it).  Returns the summary of the tile's items before this thread and leaves
+// the tile's summary in *s_tilesum; ends with a barrier.
+__device__ __forceinline__ uint32_t tile_scan(uint32_t mine, int lane, int warp, uint32_t *s_wsum,
+                                              uint32_t *s_tilesum) {
+    uint32_t incl = mine;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t o = __shfl_up_sync(kFull, incl, d);
+        if (lane >= d) incl = sum_comp(incl, o);
+    }
+    uint32_t excl = __shfl_up_sync(kFull, incl, 1);
+    if (lane == 0) excl = kSumId;
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {   // exclusive scan of the warp totals
+        uint32_t w = lane < kMergeWarps ? s_wsum[lane] : kSumId, wi = w;
+#pragma unroll
+        for (int d = 1; d < kMergeWarps; d <<= 1) {
+            const uint32_t o = __shfl_up_sync(kFull, wi, d);
+            if (lane >= d) wi = sum_comp(wi, o);
+        }
+        uint32_t we = __shfl_up_sync(kFull, wi, 1);
+        if (lane == 0) we = kSumId;
+        __syncwarp();
+        if (lane < kMergeWarps) s_wsum[lane] = we;
+        if (lane == kMergeWarps - 1) *s_tilesum = wi;
+    }
+    __syncthreads();
+    return sum_comp(excl, s_wsum[warp]);
+}
+
+// A staged tile that owns no valid start: a shifted copy (a merge at the end
+// of the previous tile consumed symbol 0, removing the pair it began).
+__device__ __forceinline__ void emit_plain(const TrainParams &p, const uint32_t *stile, uint32_t carry,
+                                           unsigned long long obase, uint64_t base, uint64_t n, uint32_t tile_len,
+                                           uint32_t *out, int tid) {
+    for (uint32_t i = tid; i + carry < tile_len; i += kMergeThreads) out[obase + i] = stile[padded(i + carry)];
+    if (carry && tid == 0 && base + 1 < n && !(stile[1] & kWordStart))
+        global_add(table_of(p), pair_key(stile[0], stile[1]), 0xFFFFFFFFu);
+}
+
+// Merge and compact a staged tile given each thread's merge flags (mm: bit j
+// = m(pos+j), j = 0 .. 17; mprev = m(pos-1)), its tile-local output index e
+// and the tile's kept count: count deltas, then the surviving symbols in
+// order from out + obase.  Needs the delta table cleared (by a barrier ago).
+__device__ __forceinline__ void emit_full(const TrainParams &p, uint32_t *stile, uint32_t *dkey, uint32_t *dval,
+                                          uint32_t *s_docc, uint32_t mm, uint32_t mprev, uint32_t e,
+                                          uint32_t tile_kept, unsigned long long obase, uint64_t pos, uint64_t n,
+                                          uint32_t new_id, uint32_t *out, int tid) {
+    const uint32_t *mys = stile + padded(kMergeItems * tid);
+    if ((mm | mprev) & 0x1FFFFu)   // some merge touches this thread's pairs
+        thread_deltas(table_of(p), dkey, dval, s_docc, mys, pos, n, mm, mprev, new_id);
+    const uint32_t mext = (mm << 1) | mprev;   // bit j: position pos+j consumed
+    uint32_t outv[kMergeItems];
+#pragma unroll
+    for (int j = 0; j < kMergeItems; j++) {
+        const uint32_t x = mys[j];
+        outv[j] = ((mm >> j) & 1u) ? (new_id | (x & kWordStart)) : x;
+    }
+    __syncthreads();   // every symbol of the tile is in registers: the tile buffer is free
+#pragma unroll
+    for (int j = 0; j < kMergeItems; j++)
+        if (pos + j < n && !((mext >> j) & 1u)) stile[padded(e++)] = outv[j];
+    __syncthreads();
+    for (uint32_t i = tid; i < tile_kept; i += kMergeThreads) out[obase + i] = stile[padded(i)];
+}
+
+// Add a CTA's shared delta table to the global counts (after a barrier).
+__device__ __forceinline__ void flush_deltas(const TrainParams &p, const uint32_t *dkey, const uint32_t *dval,
+                                             const uint32_t *s_docc) {
+    if (!*s_docc) return;
+    for (int j = threadIdx.x; j < kDeltaSlots; j += kMergeThreads) {
+        const uint32_t kk = dkey[j];
+        if (kk != kEmptyKey && dval[j]) global_add(table_of(p), kk, dval[j]);
+    }
+}
+
+// Merge flags of a thread's positions under the transducer scan (any l, r):
+// m(pos-1) from the summary of the tile's items before the thread, then each
+// valid start flips the parity and anything else clears it.
+__device__ __forceinline__ uint32_t run_flags(uint32_t valid, uint32_t excl, uint32_t carry, uint32_t *mprev) {
+    uint32_t par = fapply(excl & 3u, carry);
+    *mprev = par;
+    uint32_t mm = 0;
+#pragma unroll
+    for (int j = 0; j < kMergeItems + 2; j++) {
+        par = ((valid >> j) & 1u) ? (par ^ 1u) : 0u;
+        mm |= par << j;
+    }
+    return mm;
+}
+
+// Common prologue of the merge kernels: the merge to apply, or false when
+// there is none (past the requested merges, an error, or training stopped).
+struct MergeOp {
+    uint32_t k, l, r, new_id;
+    uint64_t n;
+    const uint32_t *in;
+    uint32_t *out;
+};
+// Merge k's operands, or false when training has stopped (best[k] == 0).
+// Every word read here may have been written earlier in the same launch by
+// the persistent loop, so the loads bypass L1.
+__device__ __forceinline__ bool merge_op_at(const TrainParams &p, uint32_t k, MergeOp *op) {
+    const unsigned long long bw = __ldcg(p.best + k);
+    if ((bw >> 32) == 0) return false;
+    const uint32_t key = ~(uint32_t)bw;
+    op->k = k;
+    op->l = key >> 16;
+    op->r = key & 0xFFFFu;
+    op->new_id = 256u + k;
+    op->n = __ldcg(&p.st->n[k & 1]);
+    op->in = (k & 1) ? p.buf[1] : p.buf[0];
+    op->out = (k & 1) ? p.buf[0] : p.buf[1];
+    return true;
+}
+__device__ __forceinline__ bool merge_op(const TrainParams &p, uint32_t it, MergeOp *op) {
+    const TrainState *st = p.st;
+    const uint32_t k = st->k_base + it;
+    if (k >= st->n_merges || st->err) return false;
+    return merge_op_at(p, k, op);
+}
+
+// Single pass with decoupled look-back: one tile per CTA in ticket order (a
+// tile only waits on tiles that already run).
 __global__ void __launch_bounds__(kMergeThreads, 4) k_merge(TrainParams p, uint32_t it) {
     extern __shared__ uint32_t dsm[];
     uint32_t *stile = dsm;                                // the tile and its halo (padded)
@@ -431,22 +638,16 @@ __global__ void __launch_bounds__(kMergeThreads, 4) k_merge(TrainParams p, uint3
     __shared__ uint32_t s_tile, s_carry, s_docc, s_tilesum;
     __shared__ unsigned long long s_off;
 
+    MergeOp op;
+    if (!merge_op(p, it, &op)) return;
     TrainState *st = p.st;
-    const uint32_t k = st->k_base + it;
-    if (k >= st->n_merges || st->err) return;
-    const unsigned long long bw = p.best[k];
-    if ((bw >> 32) == 0) return;  // nothing to merge: training has stopped
-    const uint32_t key = ~(uint32_t)bw;
-    const uint32_t l = key >> 16, r = key & 0xFFFFu, new_id = 256u + k;
-    const uint64_t n = st->n[k & 1];
-    const uint32_t *in = (k & 1) ? p.buf[1] : p.buf[0];
-    uint32_t *out = (k & 1) ? p.buf[0] : p.buf[1];
+    const uint32_t k = op.k;
+    const uint64_t n = op.n;
     unsigned long long *status = (k & 1) ? p.status[1] : p.status[0];
     unsigned long long *next_status = (k & 1) ? p.status[0] : p.status[1];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint64_t ntiles = (n + kMergeTile - 1) / kMergeTile;
 
-    // one tile per CTA, in ticket order (a tile only waits on tiles that run)
     if (tid == 0) {
         s_tile = atomicAdd(&st->ticket[k & 1], 1u);
         s_docc = 0;
@@ -458,89 +659,23 @@ __global__ void __launch_bounds__(kMergeThreads, 4) k_merge(TrainParams p, uint3
     if (tid == 0) next_status[t] = 0ull;
     const uint64_t base = t * kMergeTile;
     const uint32_t tile_len = (n - base < (uint64_t)kMergeTile) ? (uint32_t)(n - base) : (uint32_t)kMergeTile;
-
-    // coalesced 128-bit loads of the tile and its halo into shared memory
-#pragma unroll
-    for (int q = 0; q < (kMergeTile + kTileHalo) / (4 * kMergeThreads) + 1; q++) {
-        const int i4 = tid + q * kMergeThreads;
-        if (i4 < (kMergeTile + kTileHalo) / 4) {
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (base + 4ull * i4 < n) v = __ldcs(reinterpret_cast<const uint4 *>(in + base + 4ull * i4));
-            uint32_t *d = stile + padded(4 * i4);   // 4 symbols never straddle a padding word
-            d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
-        }
-    }
+    stage_tile(stile, op.in, base, n, tid);
     __syncthreads();
-
-    // valid starts among this thread's 16 positions and the 2 after them
     const uint64_t pos = base + (uint64_t)kMergeItems * tid;
-    const uint32_t *mys = stile + padded(kMergeItems * tid);
-    uint32_t valid = 0;   // bit j: position pos + j is a valid start, j = 0 .. 17
-    {
-        uint32_t isl = 0, isr = 0;   // id == l ; id == r without WORD_START
-#pragma unroll
-        for (int j = 0; j < kMergeItems + 3; j++) {
-            const uint32_t x = mys[j < 16 ? j : j + 1];
-            isl |= (uint32_t)((x & 0xFFFFu) == l) << j;
-            isr |= (uint32_t)((x & 0x1FFFFu) == r) << j;
-        }
-        valid = isl & (isr >> 1) & 0x3FFFFu;
-        const uint64_t lim = n - pos;   // positions pos+j with j + 1 < lim
-        if (lim < kMergeItems + 3) valid &= (lim >= 1) ? ((1u << (uint32_t)(lim - 1)) - 1u) : 0u;
-    }
+    const uint32_t valid = staged_valid(stile + padded(kMergeItems * tid), pos, n, op.l, op.r);
     // A tile takes the full path when it owns a valid start, or when the next
     // tile's first position is one: the merge there removes the pair (last,
     // first) and creates (last, new symbol), deltas this tile owes.
     const bool any = __syncthreads_or((valid & (tid == kMergeThreads - 1 ? 0x1FFFFu : 0xFFFFu)) != 0);
-
-    uint32_t excl = kSumId;   // summary of this tile's items before this thread
+    uint32_t excl = kSumId;
     if (!any) {
-        // no valid start owned by the tile: parity is 0 after every item, only
-        // the first symbol can be consumed (by a merge at the end of the tile before)
-        if (tid == 0) s_tilesum = sum_pack(0u, tile_len, tile_len - 1);
+        if (tid == 0) s_tilesum = plain_tile_summary(tile_len);
     } else {
         for (int j = tid; j < kDeltaSlots; j += kMergeThreads) {   // fenced by the barriers below
             dkey[j] = kEmptyKey;
             dval[j] = 0;
         }
-        uint32_t kept[2], fout[2];
-#pragma unroll
-        for (uint32_t c = 0; c < 2; c++) {
-            uint32_t par = c, kc = 0;
-#pragma unroll
-            for (int j = 0; j < kMergeItems; j++) {
-                if (pos + j < n) kc += par ^ 1u;
-                par = ((valid >> j) & 1u) ? (par ^ 1u) : 0u;
-            }
-            kept[c] = kc;
-            fout[c] = par;
-        }
-        const uint32_t mine = sum_pack(fout[0] | (fout[1] << 1), kept[0], kept[1]);
-        uint32_t incl = mine;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const uint32_t o = __shfl_up_sync(kFull, incl, d);
-            if (lane >= d) incl = sum_comp(incl, o);
-        }
-        excl = __shfl_up_sync(kFull, incl, 1);
-        if (lane == 0) excl = kSumId;
-        if (lane == 31) s_wsum[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {   // exclusive scan of the 8 warp totals
-            uint32_t w = lane < kMergeWarps ? s_wsum[lane] : kSumId, wi = w;
-#pragma unroll
-            for (int d = 1; d < kMergeWarps; d <<= 1) {
-                const uint32_t o = __shfl_up_sync(kFull, wi, d);
-                if (lane >= d) wi = sum_comp(wi, o);
-            }
-            uint32_t we = __shfl_up_sync(kFull, wi, 1);
-            if (lane == 0) we = kSumId;
-            __syncwarp();
-            if (lane < kMergeWarps) s_wsum[lane] = we;
-            if (lane == kMergeWarps - 1) s_tilesum = wi;
-        }
-        __syncthreads();
-        excl = sum_comp(excl, s_wsum[warp]);
+        excl = tile_scan(thread_summary(valid, pos, n), lane, warp, s_wsum, &s_tilesum);
     }
     __syncthreads();
     const uint32_t tile = s_tilesum;
@@ -571,47 +706,591 @@ __global__ void __launch_bounds__(kMergeThreads, 4) k_merge(TrainParams p, uint3
     }
     __syncthreads();
     const uint32_t carry = s_carry;
-    const unsigned long long obase = s_off;
-
     if (!any) {
-        // shifted copy; a merge at the end of the previous tile consumed symbol 0
-        for (uint32_t i = tid; i + carry < tile_len; i += kMergeThreads) out[obase + i] = stile[padded(i + carry)];
-        if (carry && tid == 0 && base + 1 < n && !(stile[1] & kWordStart))
-            global_add(table_of(p), pair_key(stile[0], stile[1]), 0xFFFFFFFFu);
+        emit_plain(p, stile, carry, s_off, base, n, tile_len, op.out, tid);
         return;
     }
-
-    // merge flags m(pos-1 .. pos+17) under the real carry
-    uint32_t par = fapply(excl & 3u, carry);
-    const uint32_t mprev = par;   // m(pos-1)
-    uint32_t mm = 0;              // bit j: m(pos+j)
-#pragma unroll
-    for (int j = 0; j < kMergeItems + 2; j++) {
-        par = ((valid >> j) & 1u) ? (par ^ 1u) : 0u;
-        mm |= par << j;
-    }
-    if ((mm | mprev) & 0x1FFFFu)   // some merge touches this thread's pairs
-        thread_deltas(table_of(p), dkey, dval, &s_docc, mys, pos, n, mm, mprev, new_id);
-    const uint32_t mext = (mm << 1) | mprev;   // bit j: position pos+j consumed
-    uint32_t outv[kMergeItems];
-#pragma unroll
-    for (int j = 0; j < kMergeItems; j++) {
-        const uint32_t x = mys[j];
-        outv[j] = ((mm >> j) & 1u) ? (new_id | (x & kWordStart)) : x;
-    }
-    uint32_t e = carry ? (excl >> 17) : ((excl >> 2) & 0x7FFFu);   // tile-local output index
+    uint32_t mprev;
+    const uint32_t mm = run_flags(valid, excl, carry, &mprev);
+    const uint32_t e = carry ? (excl >> 17) : ((excl >> 2) & 0x7FFFu);
     const uint32_t tile_kept = carry ? (tile >> 17) : ((tile >> 2) & 0x7FFFu);
-    __syncthreads();   // every symbol of the tile is in registers: the tile buffer is free
+    emit_full(p, stile, dkey, dval, &s_docc, mm, mprev, e, tile_kept, s_off, pos, n, op.new_id, op.out, tid);
+    flush_deltas(p, dkey, dval, &s_docc);
+}
+
+// ---- two-pass merge: per-range summaries, then apply (no inter-CTA wait) ---
+//
+// Both kernels give CTA b the same contiguous range of tiles.  k_msum
+// summarises each range (the tile summaries composed in order); the last CTA
+// to finish scans the range summaries into each range's entering merge flag
+// and output offset, and the new stream length.  k_mapply then merges its
+// range tile by tile, carrying flag and offset from one tile to the next with
+// the tile summaries its own in-tile scans produce.
+
+__device__ __forceinline__ unsigned long long lsum_from_sum(uint32_t s) {
+    return (unsigned long long)(s & 3u) | ((unsigned long long)((s >> 2) & 0x7FFFu) << 2) |
+           ((unsigned long long)(s >> 17) << 33);
+}
+
+// l != r: the stream is split into 512-symbol warp spans, balanced over the
+// CTAs (ranges differ by at most one span); [r0, re) are the range's positions.
+__device__ __forceinline__ void span_range(uint64_t n, uint64_t *r0, uint64_t *re) {
+    const uint64_t nspans = (n + kWarpSpan - 1) / kWarpSpan;
+    const uint64_t a = nspans * blockIdx.x / gridDim.x, b = nspans * (blockIdx.x + 1) / gridDim.x;
+    *r0 = a * kWarpSpan;
+    *re = b * kWarpSpan < n ? b * kWarpSpan : n;
+    if (*r0 > *re) *r0 = *re;
+}
+
+__device__ __forceinline__ void tile_range(uint64_t ntiles, uint64_t *t0, uint64_t *t1) {
+    const uint64_t per = (ntiles + gridDim.x - 1) / gridDim.x;
+    const uint64_t a = (uint64_t)blockIdx.x * per;
+    *t0 = a < ntiles ? a : ntiles;
+    *t1 = a + per < ntiles ? a + per : ntiles;
+}
+
+// When l != r no two valid starts are adjacent (the position after one holds
+// r, not l), so every valid start merges: a merge flag is the valid bit
+// itself, and a range's summary is "the last position's valid bit" with kept
+// count len - (valid starts before its last position), one less when its
+// first symbol is consumed.
+// Only l == r needs the transducer scan.
+
+
+__device__ __forceinline__ uint32_t is_l(uint32_t x, uint32_t l) { return (x & 0xFFFFu) == l ? 1u : 0u; }
+__device__ __forceinline__ uint32_t is_r(uint32_t x, uint32_t r) { return (x & 0x1FFFFu) == r ? 1u : 0u; }
+
+// Valid-start bits (bit j: position p0 + j) of a lane's 4 positions for all
+// rounds, with the 4 symbols per round in x[].  nx0: the symbol after the
+// warp's span (read by lane 31).
+__device__ __forceinline__ void quad_valid(const uint4 *x, uint32_t nx0, uint64_t wb, uint64_t n, uint32_t l,
+                                           uint32_t r, int lane, uint32_t *v4) {
+    uint32_t isl[kRounds], isr[kRounds];
 #pragma unroll
-    for (int j = 0; j < kMergeItems; j++)
-        if (pos + j < n && !((mext >> j) & 1u)) stile[padded(e++)] = outv[j];
-    __syncthreads();
-    for (uint32_t i = tid; i < tile_kept; i += kMergeThreads) out[obase + i] = stile[padded(i)];
-    if (s_docc) {
-        for (int j = tid; j < kDeltaSlots; j += kMergeThreads) {
-            const uint32_t kk = dkey[j];
-            if (kk != kEmptyKey && dval[j]) global_add(table_of(p), kk, dval[j]);
+    for (int q = 0; q < kRounds; q++) {
+        isl[q] = is_l(x[q].x, l) | (is_l(x[q].y, l) << 1) | (is_l(x[q].z, l) << 2) | (is_l(x[q].w, l) << 3);
+        isr[q] = is_r(x[q].x, r) | (is_r(x[q].y, r) << 1) | (is_r(x[q].z, r) << 2) | (is_r(x[q].w, r) << 3);
+    }
+#pragma unroll
+    for (int q = 0; q < kRounds; q++) {
+        uint32_t rn = __shfl_down_sync(kFull, isr[q], 1) & 1u;   // position p0 + 4
+        const uint32_t rw = q + 1 < kRounds ? __shfl_sync(kFull, isr[q + 1 < kRounds ? q + 1 : q], 0) & 1u
+                                            : is_r(nx0, r);
+        if (lane == 31) rn = rw;
+        uint32_t v = isl[q] & ((isr[q] >> 1) | (rn << 3));
+        const uint64_t p0 = wb + 128ull * q + 4ull * lane;
+        if (p0 >= n) v = 0;
+        else if (n - p0 < 5) v &= (1u << (uint32_t)(n - p0 - 1)) - 1u;   // p0 + j + 1 < n
+        v4[q] = v;
+    }
+}
+
+// Count deltas of a lane's 4 positions p0 .. p0+3 (rare: only where a merge
+// happened nearby), those before re (the end of the CTA's range) only.  mext
+// bit j: m(p0 - 1 + j), j = 0 .. 6; sq[j]: symbol p0 + j, j = 0 .. 5.  For l != r every occurrence of the pair lr merges and
+// none is created, so its count ends at exactly 0: its -1s are skipped and the
+// count is cleared once instead (the hottest key would otherwise take one
+// atomic per merge).
+__device__ __noinline__ void quad_deltas(const Table p, uint32_t *dkey, uint32_t *dval, uint32_t *socc,
+                                         const uint32_t *sq, uint64_t p0, uint64_t re, uint64_t n, uint32_t mext,
+                                         uint32_t new_id, uint32_t lr) {
+    auto add = [&](uint32_t kk, uint32_t d) {
+        if (smem_add<kDeltaSlots>(dkey, dval, socc, kk, d)) global_add(p, kk, d);
+    };
+    const uint32_t mm = mext >> 1;   // bit j: m(p0 + j)
+    // old pairs (j, j+1) touched by a merge at j-1, j or j+1
+    uint32_t told = (mext | mm | (mm >> 1)) & 0xFu;
+    while (told) {
+        const int j = __ffs(told) - 1;
+        told &= told - 1;
+        if (p0 + j >= re || p0 + j + 1 >= n) break;   // pairs owned by positions of this range
+        const uint32_t b = sq[j + 1];
+        const uint32_t kk = pair_key(sq[j], b);
+        if (!(b & kWordStart) && kk != lr) add(kk, 0xFFFFFFFFu);   // (l, r) itself is zeroed once
+    }
+    // new pairs at kept positions j whose own or next kept symbol merged
+    uint32_t tnew = ~mext & (mm | (mm >> 1)) & 0xFu;
+    while (tnew) {
+        const int j = __ffs(tnew) - 1;
+        tnew &= tnew - 1;
+        if (p0 + j >= re) break;
+        const uint32_t mj = (mm >> j) & 1u;
+        const int nk = j + 1 + (int)mj;
+        if (p0 + nk >= n) continue;
+        const uint32_t b = sq[nk];
+        if (b & kWordStart) continue;
+        const uint32_t mk = (mm >> nk) & 1u;
+        add(pair_key(mj ? new_id : sq[j], mk ? new_id : b), 1u);
+    }
+}
+
+// Merge and compact one tile for l != r (every valid start merges, so the
+// merge flags are the valid bits and no carry between tiles is needed: the
+// flag before a warp's span is read from the data).  Survivors are packed
+// into the warp's 512-word buffer wout, then copied to out + obase + (the
+// warp's offset in the tile).  Returns the tile's kept count.  Deltas go to
+// the CTA's shared table (cleared before, flushed by the caller).
+__device__ __forceinline__ uint32_t apply_tile_distinct(const TrainParams &p, const MergeOp &op, uint64_t base,
+                                                        uint64_t re, unsigned long long obase, uint32_t *wout,
+                                                        uint32_t *s_wtot, uint32_t *dkey, uint32_t *dval,
+                                                        uint32_t *s_docc, int lane, int warp) {
+    const uint64_t n = op.n;
+    const uint64_t wb = base + (uint64_t)kWarpSpan * warp;
+    const bool live = wb < re;   // the warp's span lies in the CTA's range (re is span-aligned or n)
+    uint4 x[kRounds];
+#pragma unroll
+    for (int q = 0; q < kRounds; q++) {
+        const uint64_t p0 = wb + 128ull * q + 4ull * lane;
+        x[q] = (live && p0 < n) ? __ldcg(reinterpret_cast<const uint4 *>(op.in + p0)) : make_uint4(0, 0, 0, 0);
+    }
+    // symbols past the span (lane 31) and before it (lane 0)
+    uint32_t nx0 = 0, nx1 = 0, nx2 = 0, pv = 0;
+    if (live && lane == 31) {
+        const uint64_t e = wb + kWarpSpan;
+        nx0 = e < n ? __ldcg(op.in + e) : 0u;
+        nx1 = e + 1 < n ? __ldcg(op.in + e + 1) : 0u;
+        nx2 = e + 2 < n ? __ldcg(op.in + e + 2) : 0u;
+    }
+    if (live && lane == 0 && wb > 0 && wb < n) pv = __ldcg(op.in + wb - 1);
+    uint32_t v4[kRounds];
+    quad_valid(x, nx0, wb, live ? n : 0, op.l, op.r, lane, v4);
+
+    uint32_t packed = 0, kept4[kRounds], mext[kRounds];
+#pragma unroll
+    for (int q = 0; q < kRounds; q++) {
+        const uint64_t p0 = wb + 128ull * q + 4ull * lane;
+        // m(p0 - 1): the previous lane's last position, across rounds and spans
+        uint32_t mp = (__shfl_up_sync(kFull, v4[q], 1) >> 3) & 1u;
+        const uint32_t mw = q > 0 ? (__shfl_sync(kFull, v4[q > 0 ? q - 1 : 0], 31) >> 3) & 1u
+                                  : ((wb > 0 && wb < n) ? (is_l(pv, op.l) & is_r(x[0].x, op.r)) : 0u);
+        if (lane == 0) mp = mw;
+        // m(p0 + 4), m(p0 + 5): the next lane's first positions
+        uint32_t mn = __shfl_down_sync(kFull, v4[q], 1) & 3u;
+        uint32_t mnw;
+        if (q + 1 < kRounds) {
+            mnw = __shfl_sync(kFull, v4[q + 1 < kRounds ? q + 1 : q], 0) & 3u;
+        } else {
+            const uint64_t e = wb + kWarpSpan;
+            mnw = (e + 1 < n ? (is_l(nx0, op.l) & is_r(nx1, op.r)) : 0u) |
+                  ((e + 2 < n ? (is_l(nx1, op.l) & is_r(nx2, op.r)) : 0u) << 1);
         }
+        if (lane == 31) mn = mnw;
+        mext[q] = mp | (v4[q] << 1) | (mn << 5);
+        uint32_t kb = ~(mp | (v4[q] << 1)) & 0xFu;   // kept positions
+        if (p0 >= re) kb = 0;
+        else if (re - p0 < 4) kb &= (1u << (uint32_t)(re - p0)) - 1u;
+        kept4[q] = kb;
+        packed |= (uint32_t)__popc(kb) << (8 * q);
+    }
+    // one scan gives every round's lane offsets (8-bit fields, at most 128 each)
+    const uint32_t incl = warp_incl_sum(packed, lane);
+    const uint32_t excl = incl - packed;
+    const uint32_t tot = __shfl_sync(kFull, incl, 31);
+    uint32_t rbase = 0;
+#pragma unroll
+    for (int q = 0; q < kRounds; q++) {
+        uint32_t o = rbase + ((excl >> (8 * q)) & 0xFFu);
+        const uint32_t xs[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            if ((kept4[q] >> j) & 1u) wout[o++] = ((v4[q] >> j) & 1u) ? (op.new_id | (xs[j] & kWordStart)) : xs[j];
+        rbase += (tot >> (8 * q)) & 0xFFu;
+    }
+    // count deltas where a merge is near
+#pragma unroll
+    for (int q = 0; q < kRounds; q++) {
+        uint32_t s4 = __shfl_down_sync(kFull, x[q].x, 1), s5 = __shfl_down_sync(kFull, x[q].y, 1);
+        const uint32_t w4 = q + 1 < kRounds ? __shfl_sync(kFull, x[q + 1 < kRounds ? q + 1 : q].x, 0) : nx0;
+        const uint32_t w5 = q + 1 < kRounds ? __shfl_sync(kFull, x[q + 1 < kRounds ? q + 1 : q].y, 0) : nx1;
+        if (lane == 31) {
+            s4 = w4;
+            s5 = w5;
+        }
+        if (live && (mext[q] & 0x3Fu)) {
+            const uint32_t sq[6] = {x[q].x, x[q].y, x[q].z, x[q].w, s4, s5};
+            quad_deltas(table_of(p), dkey, dval, s_docc, sq, wb + 128ull * q + 4ull * lane, re, n, mext[q],
+                        op.new_id, pair_key(op.l, op.r));
+        }
+    }
+    if (lane == 0) s_wtot[warp] = rbase;
+    __syncthreads();
+    uint32_t wpre = 0, tile_kept = 0;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; w++) {
+        const uint32_t t = s_wtot[w];
+        wpre += w < warp ? t : 0u;
+        tile_kept += t;
+    }
+    __syncwarp();
+    for (uint32_t i = lane; i < rbase; i += 32) op.out[obase + wpre + i] = wout[i];
+    return tile_kept;
+}
+
+// Shared words of the two-pass merge.
+struct MergeShared {
+    uint32_t wsum[kMergeWarps];
+    unsigned long long lw[kMergeWarps];
+    uint32_t lastv, docc, tilesum;
+    int last;
+};
+
+// Summary of this CTA's range of tiles (valid in thread 0): for l != r the
+// last position's valid bit and the kept counts, else the tile summaries
+// composed in order.
+__device__ __forceinline__ unsigned long long range_summary(const MergeOp &op, MergeShared &sh) {
+    const uint64_t n = op.n;
+    const uint32_t *in = op.in;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint64_t ntiles = (n + kMergeTile - 1) / kMergeTile;
+    const bool distinct = op.l != op.r;
+    uint64_t t0, t1, r0, re;
+    tile_range(ntiles, &t0, &t1);
+    span_range(n, &r0, &re);
+    if (tid == 0) sh.lastv = 0;
+    __syncthreads();
+
+    unsigned long long acc = kFId;   // l == r: this range's tiles so far, composed
+    uint32_t cnt = 0;                // l != r: valid starts so far
+    if (distinct) {
+        // groups of 8 spans (one per warp), two groups' loads in flight
+        for (uint64_t g = r0; g < re; g += 2 * kMergeTile) {
+            uint4 x[2][kRounds];
+            uint32_t nx0[2];
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const uint64_t wb = g + (uint64_t)h * kMergeTile + (uint64_t)kWarpSpan * warp;
+                const bool live = wb < re;
+#pragma unroll
+                for (int q = 0; q < kRounds; q++) {
+                    const uint64_t p0 = wb + 128ull * q + 4ull * lane;
+                    x[h][q] = (live && p0 < n) ? __ldcg(reinterpret_cast<const uint4 *>(in + p0)) : make_uint4(0, 0, 0, 0);
+                }
+                nx0[h] = (live && lane == 31 && wb + kWarpSpan < n) ? __ldcg(in + wb + kWarpSpan) : 0u;
+            }
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const uint64_t wb = g + (uint64_t)h * kMergeTile + (uint64_t)kWarpSpan * warp;
+                if (wb >= re) continue;   // warp-uniform
+                uint32_t v4[kRounds];
+                quad_valid(x[h], nx0[h], wb, n, op.l, op.r, lane, v4);
+#pragma unroll
+                for (int q = 0; q < kRounds; q++) {
+                    const uint64_t p0 = wb + 128ull * q + 4ull * lane;
+                    uint32_t v = v4[q];
+                    if (p0 >= re) v = 0;
+                    else if (re - p0 < 4) v &= (1u << (uint32_t)(re - p0)) - 1u;   // positions of this range
+                    cnt += __popc(v);
+                    if (p0 < re && re - p0 <= 4) sh.lastv = (v4[q] >> (re - p0 - 1)) & 1u;
+                }
+            }
+        }
+    }
+    for (uint64_t t = distinct ? t1 : t0; t < t1; t++) {
+        const uint64_t base = t * kMergeTile;
+        const uint64_t pos = base + (uint64_t)kMergeItems * tid;
+        uint32_t isl = 0, isr = 0;
+        if (pos < n) {   // the buffer is padded: 16 symbols past pos are readable
+            const uint4 *src = reinterpret_cast<const uint4 *>(in + pos);
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const uint4 v = __ldcg(src + q);
+                const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    isl |= (uint32_t)((x[j] & 0xFFFFu) == op.l) << (4 * q + j);
+                    isr |= (uint32_t)((x[j] & 0x1FFFFu) == op.r) << (4 * q + j);
+                }
+            }
+        }
+        uint32_t nxt = __shfl_down_sync(kFull, isr, 1) & 1u;   // position pos + 16
+        if (lane == 31)
+            nxt = (pos + kMergeItems < n) ? (uint32_t)((__ldcg(in + pos + kMergeItems) & 0x1FFFFu) == op.r) : 0u;
+        uint32_t valid = isl & ((isr >> 1) | (nxt << 15)) & 0xFFFFu;
+        if (pos >= n) valid = 0;
+        else if (n - pos < kMergeItems + 1) valid &= (1u << (uint32_t)(n - pos - 1)) - 1u;   // pos+j+1 < n
+        const uint32_t tile_len = (n - base < (uint64_t)kMergeTile) ? (uint32_t)(n - base) : (uint32_t)kMergeTile;
+        uint32_t ts;
+        if (!__syncthreads_or(valid != 0)) {
+            ts = plain_tile_summary(tile_len);
+        } else {
+            // ordered reduction: lane L ends with lanes [L, L + 2d) composed
+            uint32_t x = thread_summary(valid, pos, n);
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t y = __shfl_down_sync(kFull, x, d);
+                if (lane + d < 32) x = sum_comp(y, x);
+            }
+            if (lane == 0) sh.wsum[warp] = x;
+            __syncthreads();
+            ts = sh.wsum[0];
+#pragma unroll
+            for (int w = 1; w < kMergeWarps; w++) ts = sum_comp(sh.wsum[w], ts);
+            __syncthreads();   // wsum is reused by the next tile
+        }
+        acc = lsum_comp(lsum_from_sum(ts), acc);
+    }
+    if (distinct) {
+        cnt = __reduce_add_sync(kFull, cnt);
+        if (lane == 0) sh.wsum[warp] = cnt;
+        __syncthreads();
+        if (tid == 0) {
+            uint32_t v = 0;
+            for (int w = 0; w < kMergeWarps; w++) v += sh.wsum[w];
+            const unsigned long long len = re - r0;
+            if (len) {   // a valid start at the last position consumes the next range's first symbol
+                const unsigned long long k0 = len - v + sh.lastv;
+                acc = (sh.lastv ? 3ull : 0ull) | (k0 << 2) | ((k0 ? k0 - 1 : 0ull) << 33);
+            }
+        }
+        __syncthreads();   // wsum is reused
+    }
+    return acc;
+}
+
+// Ordered exclusive scan of the threads' 64-bit summaries (all threads call
+// it; ends with a barrier): the composition of the threads before this one.
+__device__ __forceinline__ unsigned long long block_excl_lsum(unsigned long long mine, MergeShared &sh) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned long long incl = mine;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const unsigned long long o = __shfl_up_sync(kFull, incl, d);
+        if (lane >= d) incl = lsum_comp(incl, o);
+    }
+    unsigned long long excl = __shfl_up_sync(kFull, incl, 1);
+    if (lane == 0) excl = kFId;
+    if (lane == 31) sh.lw[warp] = incl;
+    __syncthreads();
+    unsigned long long wpre = kFId;
+    for (int w = 0; w < warp; w++) wpre = lsum_comp(sh.lw[w], wpre);
+    __syncthreads();   // lw is reused
+    return lsum_comp(excl, wpre);
+}
+
+// Entering merge flag and offset of range b from the G range summaries, and
+// (by range G-1's owner thread) the new stream length.  Thread t takes the
+// ranges [t*per, (t+1)*per).  write_all: also store every range's prefix.
+__device__ __forceinline__ void scan_ranges(const TrainParams &p, uint32_t k, uint32_t G, bool write_all, uint32_t b_want,
+                                            MergeShared &sh, uint32_t *carry_out, unsigned long long *off_out) {
+    const int tid = threadIdx.x;
+    const uint32_t per = (G + kMergeThreads - 1) / kMergeThreads;
+    const uint32_t b0 = tid * per < G ? tid * per : G, b1 = b0 + per < G ? b0 + per : G;
+    unsigned long long mine = kFId;
+    for (uint32_t b = b0; b < b1; b++) mine = lsum_comp(__ldcg(p.rsum + b), mine);
+    const unsigned long long excl = block_excl_lsum(mine, sh);
+    // walk this thread's ranges from the stream start's state (flag 0, offset 0)
+    uint32_t carry = fapply((uint32_t)excl & 3u, 0u);
+    unsigned long long off = (excl >> 2) & 0x7FFFFFFFull;
+    for (uint32_t b = b0; b < b1; b++) {
+        if (write_all) p.rpre[b] = (off << 1) | carry;
+        if (b == b_want) {
+            sh.lw[0] = (off << 1) | carry;
+        }
+        const unsigned long long sb = __ldcg(p.rsum + b);
+        off += carry ? (sb >> 33) : ((sb >> 2) & 0x7FFFFFFFull);
+        carry = fapply((uint32_t)sb & 3u, carry);
+    }
+    if (b0 < b1 && b1 == G && (write_all || b_want == 0)) {
+        p.st->n[(k + 1) & 1] = off;
+        p.nhist[k + 1] = off;
+    }
+    __syncthreads();
+    const unsigned long long pre = sh.lw[0];
+    *carry_out = (uint32_t)pre & 1u;
+    *off_out = pre >> 1;
+    __syncthreads();   // lw is reused
+}
+
+// Merge and compact this CTA's range of tiles, entering with the merge flag
+// carry and output offset off; count deltas go through one shared table,
+// flushed once at the end.
+__device__ __forceinline__ void apply_range(const TrainParams &p, const MergeOp &op, uint32_t carry,
+                                            unsigned long long off, uint32_t *dsm, MergeShared &sh) {
+    uint32_t *stile = dsm;   // l == r: the staged tile; l != r: the warps' output buffers
+    uint32_t *dkey = dsm + kTileWords;
+    uint32_t *dval = dkey + kDeltaSlots;
+    const uint64_t n = op.n;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint64_t ntiles = (n + kMergeTile - 1) / kMergeTile;
+    const bool distinct = op.l != op.r;
+    uint64_t t0, t1, r0, re;
+    tile_range(ntiles, &t0, &t1);
+    span_range(n, &r0, &re);
+    if (distinct && blockIdx.x == 0 && tid == 0)   // every occurrence of (l, r) merges: its count ends at 0
+        global_add(table_of(p), pair_key(op.l, op.r), 0u - (uint32_t)(__ldcg(p.best + op.k) >> 32));
+    if (distinct ? r0 >= re : t0 >= t1) return;
+    if (tid == 0) sh.docc = 0;
+    for (int j = tid; j < kDeltaSlots; j += kMergeThreads) {
+        dkey[j] = kEmptyKey;
+        dval[j] = 0;
+    }
+    __syncthreads();
+    if (distinct) {
+        uint32_t *wout = stile + kWarpSpan * warp;
+        for (uint64_t g = r0; g < re; g += kMergeTile) {
+            off += apply_tile_distinct(p, op, g, re, off, wout, sh.wsum, dkey, dval, &sh.docc, lane, warp);
+            __syncthreads();   // the output buffers and shared words are reused
+        }
+    } else {
+        for (uint64_t t = t0; t < t1; t++) {
+            const uint64_t base = t * kMergeTile;
+            const uint32_t tile_len = (n - base < (uint64_t)kMergeTile) ? (uint32_t)(n - base) : (uint32_t)kMergeTile;
+            stage_tile(stile, op.in, base, n, tid);
+            __syncthreads();
+            const uint64_t pos = base + (uint64_t)kMergeItems * tid;
+            const uint32_t valid = staged_valid(stile + padded(kMergeItems * tid), pos, n, op.l, op.r);
+            // the full path also when the next tile's first position merges: the
+            // pair (last, first) it removes and (last, new) it creates are ours
+            const bool any = __syncthreads_or((valid & (tid == kMergeThreads - 1 ? 0x1FFFFu : 0xFFFFu)) != 0);
+            if (!any) {
+                emit_plain(p, stile, carry, off, base, n, tile_len, op.out, tid);
+                off += tile_len - carry;
+                carry = 0;
+                __syncthreads();   // the tile buffer is reused
+                continue;
+            }
+            const uint32_t excl = tile_scan(thread_summary(valid, pos, n), lane, warp, sh.wsum, &sh.tilesum);
+            const uint32_t tile = sh.tilesum;
+            uint32_t mprev;
+            const uint32_t mm = run_flags(valid, excl, carry, &mprev);
+            const uint32_t e = carry ? (excl >> 17) : ((excl >> 2) & 0x7FFFu);
+            const uint32_t tile_kept = carry ? (tile >> 17) : ((tile >> 2) & 0x7FFFu);
+            emit_full(p, stile, dkey, dval, &sh.docc, mm, mprev, e, tile_kept, off, pos, n, op.new_id, op.out, tid);
+            off += tile_kept;
+            carry = fapply(tile & 3u, carry);
+            __syncthreads();   // the tile buffer and shared words are reused
+        }
+    }
+    flush_deltas(p, dkey, dval, &sh.docc);
+}
+
+__global__ void __launch_bounds__(kMergeThreads) k_msum(TrainParams p, uint32_t it) {
+    __shared__ MergeShared sh;
+    MergeOp op;
+    if (!merge_op(p, it, &op)) return;
+    TrainState *st = p.st;
+    const unsigned long long acc = range_summary(op, sh);
+    if (threadIdx.x == 0) p.rsum[blockIdx.x] = acc;
+    // the last CTA to finish scans the range summaries
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) sh.last = atomicAdd(&st->msum_done, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!sh.last) return;
+    __threadfence();
+    uint32_t c;
+    unsigned long long o;
+    scan_ranges(p, op.k, gridDim.x, true, 0, sh, &c, &o);
+    if (threadIdx.x == 0) st->msum_done = 0;
+}
+
+__global__ void __launch_bounds__(kMergeThreads, 4) k_mapply(TrainParams p, uint32_t it) {
+    extern __shared__ uint32_t dsm[];
+    __shared__ MergeShared sh;
+    MergeOp op;
+    if (!merge_op(p, it, &op)) return;
+    const unsigned long long pre = p.rpre[blockIdx.x];
+    apply_range(p, op, (uint32_t)pre & 1u, pre >> 1, dsm, sh);
+}
+
+// ------------------------------------------- persistent two-pass merge loop ---
+//
+// One cooperative launch runs merges [k_begin, k_end): argmax, range
+// summaries and apply, separated by grid barriers (all CTAs are resident).
+// Each CTA finds its own range's prefix from the G summaries, so a merge
+// costs three barriers and no kernel launch.
+
+// Grid barrier with a bounded wait: false (and DERR_TIMEOUT) when it gives up.
+// Two levels: CTA b arrives at counter b % kBarGroups; the last arrival of a
+// group arrives at the groups' counter, whose last arrival bumps the
+// generation the others poll.
+__device__ __forceinline__ bool grid_sync(TrainState *st, int *s_ok) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t *grp = st->bar, *top = st->bar + 32 * kBarGroups, *gen_w = top + 32;
+        const uint32_t G = gridDim.x, g = blockIdx.x % kBarGroups;
+        const uint32_t ngroups = G < (uint32_t)kBarGroups ? G : (uint32_t)kBarGroups;
+        const uint32_t gsize = (G - g + kBarGroups - 1) / kBarGroups;   // CTAs b < G with b % kBarGroups == g
+        const uint32_t gen = ld_acquire_u32(gen_w);
+        __threadfence();
+        int ok = 1;
+        if (atomicAdd(grp + 32 * g, 1u) == gsize - 1) {
+            atomicExch(grp + 32 * g, 0u);
+            if (atomicAdd(top, 1u) == ngroups - 1) {
+                atomicExch(top, 0u);
+                __threadfence();
+                st_release_u32(gen_w, gen + 1);
+            }
+        }
+        unsigned spins = 0;
+        while (ld_acquire_u32(gen_w) == gen) {
+            if (++spins > kSpinLimit) {
+                atomicOr(&st->err, DERR_TIMEOUT);
+                ok = 0;
+                break;
+            }
+            if (spins > 4) __nanosleep(100);
+        }
+        __threadfence();
+        *s_ok = ok;
+    }
+    __syncthreads();
+    return *s_ok != 0;
+}
+
+// Block max of (count, ~key) over the dense table, folded into best[k].
+__device__ __forceinline__ void argmax_into(const TrainParams &p, uint32_t k, unsigned long long *sbest) {
+    const uint32_t D = __ldcg(&p.st->dense_len);
+    if (blockIdx.x == 0 && threadIdx.x == 0) p.dhist[k] = D;
+    unsigned long long b = 0;
+    const uint32_t D4 = (D + 3) / 4;
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < D4; i += gridDim.x * blockDim.x) {
+        const uint4 c = __ldcg(reinterpret_cast<const uint4 *>(p.dcnt) + i);
+        uint32_t cm = c.x > c.y ? c.x : c.y;
+        cm = cm > c.z ? cm : c.z;
+        cm = cm > c.w ? cm : c.w;
+        if (cm == 0 || cm < (uint32_t)(b >> 32)) continue;
+        const uint32_t cs[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            if (cs[j] == cm) {
+                const unsigned long long v = pack_best(cm, __ldcg(p.dkey + 4 * i + j));
+                b = v > b ? v : b;
+            }
+        }
+    }
+    b = warp_max_u64(b);
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) sbest[warp] = b;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        unsigned long long x = threadIdx.x < blockDim.x / 32 ? sbest[threadIdx.x] : 0ull;
+        x = warp_max_u64(x);
+        if (threadIdx.x == 0 && x) atomicMax(p.best + k, x);
+    }
+}
+
+__global__ void __launch_bounds__(kMergeThreads, 4) k_train_loop(TrainParams p, uint32_t k_begin, uint32_t k_end) {
+    extern __shared__ uint32_t dsm[];
+    __shared__ MergeShared sh;
+    __shared__ unsigned long long sbest[kMergeWarps];
+    __shared__ int s_ok;
+    TrainState *st = p.st;
+    for (uint32_t k = k_begin; k < k_end; k++) {
+        if (k > 0) argmax_into(p, k, sbest);   // merge 0's pair comes from the count pass
+        if (!grid_sync(st, &s_ok)) return;
+        // after the barrier every CTA reads the same best[k] and err (nothing
+        // writes them until the next barrier)
+        MergeOp op;
+        if (__ldcg(&st->err) || !merge_op_at(p, k, &op)) return;
+        const unsigned long long acc = range_summary(op, sh);
+        if (threadIdx.x == 0) __stcg(p.rsum + blockIdx.x, acc);
+        if (!grid_sync(st, &s_ok)) return;
+        uint32_t carry;
+        unsigned long long off;
+        scan_ranges(p, k, gridDim.x, false, blockIdx.x, sh, &carry, &off);
+        apply_range(p, op, carry, off, dsm, sh);
+        if (!grid_sync(st, &s_ok)) return;
     }
 }
 
@@ -627,6 +1306,7 @@ struct Launch {
     TrainParams p;
     unsigned count_grid, merge_grid, argmax_grid;
     size_t count_smem, merge_smem;
+    bool lookback;   // single pass with decoupled look-back, else two passes
 };
 
 int occupancy(bpe_ctx *ctx, int *count_blocks, int *merge_blocks) {
@@ -636,18 +1316,29 @@ int occupancy(bpe_ctx *ctx, int *count_blocks, int *merge_blocks) {
              "k_count smem attribute");
     BPE_CUDA(ctx, cudaFuncSetAttribute(k_merge, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msm),
              "k_merge smem attribute");
+    BPE_CUDA(ctx, cudaFuncSetAttribute(k_mapply, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msm),
+             "k_mapply smem attribute");
     BPE_CUDA(ctx, cudaOccupancyMaxActiveBlocksPerMultiprocessor(count_blocks, k_count, kCountThreads, csm),
              "k_count occupancy");
-    BPE_CUDA(ctx, cudaOccupancyMaxActiveBlocksPerMultiprocessor(merge_blocks, k_merge, kMergeThreads, msm),
-             "k_merge occupancy");
+    BPE_CUDA(ctx, cudaOccupancyMaxActiveBlocksPerMultiprocessor(merge_blocks, k_mapply, kMergeThreads, msm),
+             "k_mapply occupancy");
     *count_blocks = std::max(*count_blocks, 1);
     *merge_blocks = std::max(*merge_blocks, 1);
     return BPE_OK;
 }
 
+void launch_merge(const Launch &L, uint32_t it, cudaStream_t s) {
+    if (L.lookback) {
+        k_merge<<<L.merge_grid, kMergeThreads, L.merge_smem, s>>>(L.p, it);
+    } else {
+        k_msum<<<L.merge_grid, kMergeThreads, 0, s>>>(L.p, it);
+        k_mapply<<<L.merge_grid, kMergeThreads, L.merge_smem, s>>>(L.p, it);
+    }
+}
+
 void launch_iteration(const Launch &L, uint32_t it, cudaStream_t s) {
     k_argmax<<<L.argmax_grid, kArgmaxThreads, 0, s>>>(L.p, it);
-    k_merge<<<L.merge_grid, kMergeThreads, L.merge_smem, s>>>(L.p, it);
+    launch_merge(L, it, s);
 }
 
 // Capture (or reuse) a graph of kGraphIters iterations plus the k_base advance.
@@ -655,8 +1346,9 @@ int get_graph(bpe_ctx *ctx, const Launch &L, cudaGraphExec_t *out) {
     std::vector<uintptr_t> key = {
         (uintptr_t)L.p.buf[0], (uintptr_t)L.p.buf[1], (uintptr_t)L.p.tslot, (uintptr_t)L.p.tmask,
         (uintptr_t)L.p.dkey, (uintptr_t)L.p.dcnt, (uintptr_t)L.p.dcap, (uintptr_t)L.p.status[0],
-        (uintptr_t)L.p.status[1], (uintptr_t)L.p.best, (uintptr_t)L.p.nhist, (uintptr_t)L.p.dhist,
-        (uintptr_t)L.p.st, (uintptr_t)L.merge_grid, (uintptr_t)L.argmax_grid};
+        (uintptr_t)L.p.status[1], (uintptr_t)L.p.rsum, (uintptr_t)L.p.rpre, (uintptr_t)L.p.best,
+        (uintptr_t)L.p.nhist, (uintptr_t)L.p.dhist, (uintptr_t)L.p.st, (uintptr_t)L.merge_grid,
+        (uintptr_t)L.argmax_grid, (uintptr_t)L.lookback};
     if (ctx->graph.exec && ctx->graph.key == key) {
         *out = ctx->graph.exec;
         return BPE_OK;
@@ -698,8 +1390,33 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
         (rc = ensure(ctx, S_NHIST, ((uint64_t)n_merges + 1) * 8, &nhist)) ||
         (rc = ensure(ctx, S_LIST0, ((uint64_t)n_merges + 1) * 4, &dhist)))
         return rc;
+    int cb, mb;
+    if ((rc = occupancy(ctx, &cb, &mb))) return rc;
+    const bool lookback = ctx->merge_lookback != 0;
+    const bool profile = ctx->profile != 0;
+    const bool graph = ctx->use_graph && !profile;
+    // merge windows replay from CUDA graphs, or (BPE_OPT_PERSISTENT, two-pass
+    // merge only) from one persistent cooperative launch per window
+    int coop = 0, pb = 0;
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, ctx->device);
+    const bool persistent = ctx->persistent && graph && !lookback && coop;
+    if (persistent) {
+        const size_t msm = (kTileWords + 2 * kDeltaSlots) * sizeof(uint32_t);
+        BPE_CUDA(ctx, cudaFuncSetAttribute(k_train_loop, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msm),
+                 "k_train_loop smem attribute");
+        BPE_CUDA(ctx, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&pb, k_train_loop, kMergeThreads, msm),
+                 "k_train_loop occupancy");
+        if (pb < 1) return fail(ctx, BPE_ERR_CUDA, "bpe_train: the persistent merge loop does not fit on an SM");
+    }
+    // persistent: every CTA resident (at least one per SM, for the argmax);
+    // otherwise one range per CTA, at most as many ranges as tiles
+    const uint64_t range_grid =
+        persistent ? std::min<uint64_t>((uint64_t)ctx->sm_count * pb, std::max<uint64_t>(ntiles, ctx->sm_count))
+                   : std::max<uint64_t>(1, std::min<uint64_t>(ntiles, (uint64_t)ctx->sm_count * mb));
+    void *ranges;
+    if ((rc = ensure(ctx, S_LIST1, range_grid * 16, &ranges))) return rc;
     uint32_t *dkey = (uint32_t *)dense, *dcnt = dkey + T;   // dense keys, then dense counts
-    const uint32_t G = kGraphIters;
+    const uint32_t G = persistent ? kLoopIters : kGraphIters;
     void *pin;
     const size_t pin_bytes = sizeof(TrainState) + 8 * kInFlight + (uint64_t)n_merges * 8 +
                              ((uint64_t)n_merges + 1) * 8 + ((uint64_t)n_merges + 1) * 4;
@@ -725,9 +1442,10 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     BPE_CUDA(ctx, cudaMemsetAsync(dhist, 0, ((uint64_t)n_merges + 1) * 4, s), "dhist clear");
     BPE_CUDA(ctx, cudaMemcpyAsync(buf0, d_symbols, n * 4, cudaMemcpyDeviceToDevice, s), "input copy");
 
-    int cb, mb;
-    if ((rc = occupancy(ctx, &cb, &mb))) return rc;
     Launch L;
+    L.lookback = lookback;
+    L.p.rsum = (unsigned long long *)ranges;
+    L.p.rpre = L.p.rsum + range_grid;
     L.p.buf[0] = (uint32_t *)buf0;
     L.p.buf[1] = (uint32_t *)buf1;
     L.p.tslot = (unsigned long long *)tslot;
@@ -743,13 +1461,12 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     L.p.st = (TrainState *)state;
     const uint64_t count_work = (n + kCountTile - 1) / kCountTile;
     L.count_grid = (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(count_work, (uint64_t)ctx->sm_count * cb));
-    L.merge_grid = (unsigned)std::max<uint64_t>(1, ntiles);   // one tile per CTA; spare CTAs exit
+    // look-back: one tile per CTA (spare CTAs exit); two passes: one range per CTA
+    L.merge_grid = lookback ? (unsigned)std::max<uint64_t>(1, ntiles) : (unsigned)range_grid;
     L.argmax_grid = (unsigned)ctx->sm_count * 2;
     L.count_smem = 2 * kCountSlots * sizeof(uint32_t);
     L.merge_smem = (kTileWords + 2 * kDeltaSlots) * sizeof(uint32_t);
 
-    const bool profile = ctx->profile != 0;
-    const bool graph = ctx->use_graph && !profile;
     // profile events: 0 before k_count, 1 after it; merge k: 2+2k after argmax, 3+2k after merge
     const size_t n_prof = profile ? 2 + 2 * (size_t)n_merges : 0;
     if ((rc = ensure_events(ctx, n_prof + kInFlight))) return rc;
@@ -757,7 +1474,7 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     for (int i = 0; i < kInFlight; i++) poll_ev[i] = ctx->events[n_prof + i];
 
     cudaGraphExec_t exec = nullptr;
-    if (graph && (rc = get_graph(ctx, L, &exec))) return rc;
+    if (graph && !persistent && (rc = get_graph(ctx, L, &exec))) return rc;
     if (profile) BPE_CUDA(ctx, cudaEventRecord(ctx->events[0], s), "event");
     k_count<<<L.count_grid, kCountThreads, L.count_smem, s>>>(L.p);
     if (profile) BPE_CUDA(ctx, cudaEventRecord(ctx->events[1], s), "event");
@@ -774,14 +1491,19 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
             if ((h_poll[slot] >> 32) == 0) stopped = true;
             if (stopped) break;
         }
-        const uint32_t end = std::min<uint32_t>(n_merges, launched + G);
-        if (graph) {
+        uint32_t end = std::min<uint32_t>(n_merges, launched + G);
+        if (persistent) {
+            void *args[] = {&L.p, &launched, &end};
+            BPE_CUDA(ctx, cudaLaunchCooperativeKernel((const void *)k_train_loop, L.merge_grid, kMergeThreads, args,
+                                                      L.merge_smem, s),
+                     "persistent merge launch");
+        } else if (graph) {
             BPE_CUDA(ctx, cudaGraphLaunch(exec, s), "graph launch");
         } else {
             for (uint32_t k = launched; k < end; k++) {
                 k_argmax<<<L.argmax_grid, kArgmaxThreads, 0, s>>>(L.p, k);
                 if (profile) cudaEventRecord(ctx->events[2 + 2 * (size_t)k], s);
-                k_merge<<<L.merge_grid, kMergeThreads, L.merge_smem, s>>>(L.p, k);
+                launch_merge(L, k, s);
                 if (profile) cudaEventRecord(ctx->events[3 + 2 * (size_t)k], s);
             }
         }
@@ -806,7 +1528,7 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
         return fail(ctx, BPE_ERR_TABLE_FULL, "bpe_train: pair table of 2^%u slots overflowed", table_log2);
     }
     if (h_state->err & DERR_TIMEOUT)
-        return fail(ctx, BPE_ERR_TIMEOUT, "bpe_train: decoupled look-back wait gave up");
+        return fail(ctx, BPE_ERR_TIMEOUT, "bpe_train: a look-back or grid-barrier wait gave up");
     uint32_t done = 0;
     while (done < n_merges && (h_best[done] >> 32) != 0) done++;
     for (uint32_t k = 0; k < done; k++) {
@@ -827,7 +1549,10 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
 
     // statistics: algorithmic bytes per kernel family and (profiled) device time
     stats_reset(ctx);
-    ctx->stats.kernel_launches = 1 + (graph ? (uint64_t)window * (2 * kGraphIters + 1) : 2ull * launched);
+    const uint64_t per_merge = lookback ? 2 : 3;
+    ctx->stats.kernel_launches =
+        1 + (persistent ? (uint64_t)window
+                        : graph ? (uint64_t)window * (per_merge * kGraphIters + 1) : per_merge * launched);
     const int sc = stats_slot(ctx, "pair_count"), sa = stats_slot(ctx, "argmax"), sm = stats_slot(ctx, "merge_compact");
     ctx->stats.k[sc].launches = 1;
     ctx->stats.k[sc].bytes = 4.0 * (double)n;
@@ -1402,7 +2127,8 @@ int train_words_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32
     }
 
     stats_reset(ctx);
-    ctx->stats.kernel_launches = 1 + (graph ? (uint64_t)window * (2 * kGraphIters + 1) : 2ull * launched);
+    const uint64_t per_merge = 2;   // argmax + word merge
+    ctx->stats.kernel_launches = 1 + (graph ? (uint64_t)window * (per_merge * kGraphIters + 1) : per_merge * launched);
     const int sc = stats_slot(ctx, "word_count"), sa = stats_slot(ctx, "argmax"), sm = stats_slot(ctx, "word_merge");
     ctx->stats.k[sc].launches = 1;
     ctx->stats.k[sc].bytes = 8.0 * (double)usym;

@@ -88,8 +88,25 @@ const char *bpe_last_error(const bpe_ctx *ctx);
  *                        words weighted by their number of occurrences
  *                        (the same merges and final stream: no count or merge
  *                        crosses a WORD_START); 0 = over the full symbol
- *                        stream (default) */
-enum { BPE_OPT_TABLE_LOG2 = 1, BPE_OPT_GRAPH = 2, BPE_OPT_PROFILE = 3, BPE_OPT_CHUNK = 4, BPE_OPT_TRAIN_WORDS = 5 };
+ *                        stream (default)
+ *   BPE_OPT_MERGE_LOOKBACK  full-stream merge and compaction: 1 = one pass,
+ *                        tiles finding their output offsets by decoupled
+ *                        look-back; 0 = two passes, range summaries then
+ *                        apply (default; no CTA waits on another).  Both
+ *                        give the same results.
+ *   BPE_OPT_PERSISTENT   1 = the two-pass merge loop runs as one cooperative
+ *                        launch per window of merges (all CTAs resident,
+ *                        phases separated by grid barriers) instead of a CUDA
+ *                        graph of per-phase kernels; default 0 */
+enum {
+    BPE_OPT_TABLE_LOG2 = 1,
+    BPE_OPT_GRAPH = 2,
+    BPE_OPT_PROFILE = 3,
+    BPE_OPT_CHUNK = 4,
+    BPE_OPT_TRAIN_WORDS = 5,
+    BPE_OPT_MERGE_LOOKBACK = 6,
+    BPE_OPT_PERSISTENT = 7
+};
 int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value);
 
 /* Statistics of the last bpe_train or trie_encode call on this context.

@@ -112,12 +112,37 @@ def test_train_random_small(ctx, seed):
     check_train(ctx, oracle.pretokenize(text), 60)
 
 
-@pytest.mark.parametrize("n", [2048 * 3 - 1, 2048 * 3, 2048 * 3 + 1, 1_000_001])
+@pytest.mark.parametrize("n", [4096 * 3 - 1, 4096 * 3, 4096 * 3 + 1, 1_000_001, 5_000_001])
 def test_train_identical_runs_cross_tiles(ctx, n):
-    # one run of identical letters spans many 2048-symbol tiles: leftmost-first
-    # pairing must carry its parity across every tile boundary
+    # one run of identical letters spans many 4096-symbol tiles (at 5M, several
+    # tiles per CTA range): leftmost-first pairing must carry its parity across
+    # every tile and range boundary
     text = b"a" * n + b" " + b"a" * (n // 3) + b".bb" + b"b" * 4097
     check_train(ctx, oracle.pretokenize(text), 12)
+
+
+@pytest.mark.parametrize("mode", ["lookback", "persistent"])
+@pytest.mark.parametrize("case", ["runs", "random", "tiny"])
+def test_train_merge_variants_agree(ctx, golden, case, mode):
+    # the single-pass merge (decoupled look-back) and the persistent two-pass
+    # loop give the same merges and stream
+    import bpe_trie_encode_gb300 as bt
+    opt = bt.BPE_OPT_MERGE_LOOKBACK if mode == "lookback" else bt.BPE_OPT_PERSISTENT
+    ctx.set_option(opt, 1)
+    try:
+        if case == "runs":
+            text = b"a" * 1_000_001 + b" " + b"a" * 4097 + b".bb" + b"b" * 4097
+            check_train(ctx, oracle.pretokenize(text), 12)
+        elif case == "random":
+            for seed in range(4):
+                rng = random.Random(100 + seed)
+                check_train(ctx, oracle.pretokenize(rand_bytes(rng, 9000 + 4096 * seed, b"aab c.")), 60)
+        else:
+            m, f = ctx.train(dev_sym(oracle.pretokenize(synth.corpus("tiny"))), 256)
+            assert sha(m.astype(np.uint32)) == golden["tiny"]["merges_sha256"]
+            assert sha(host_u32(f)) == golden["tiny"]["final_sha256"]
+    finally:
+        ctx.set_option(opt, 0)
 
 
 def test_train_alternating_and_ties(ctx):
