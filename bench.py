@@ -273,6 +273,27 @@ def extra_legs(args, ctx, dev, stream, flush, d_text, d_sym, n_merges, peak, pea
     return out
 
 
+# ------------------------------------------------------------ ranks ---------
+def reduce_ranks(times_ms: list, units: list, world: int, device) -> tuple[list, list]:
+    """Whole-job figures over all ranks: the slowest rank's time for each
+    entry of times_ms and the sum of units (merges, bytes) over ranks.  The
+    tensors live on ``device`` (the GPU for NCCL, the CPU for gloo)."""
+    if world <= 1:
+        return [float(x) for x in times_ms], [float(x) for x in units]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x) for x in times_ms], dtype=torch.float64, device=device)
+    u = torch.tensor([float(x) for x in units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return [float(x) for x in t.cpu()], [float(x) for x in u.cpu()]
+
+
+def throughput(units: float, ms: float) -> float:
+    """Units per second from a duration in milliseconds (0 for no time)."""
+    return units / (ms / 1e3) if ms > 0 else 0.0
+
+
 # ---------------------------------------------------------------- ours ------
 def run_ours(args, rank, world, local_rank):
     import numpy as np
@@ -379,12 +400,9 @@ def run_ours(args, rank, world, local_rank):
     ctx.set_option(bt.BPE_OPT_PROFILE, 0)
     acc["kern"] = prof["kern"]
 
-    t = torch.tensor([acc["train_ms"], acc["enc_ms"]], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    train_ms, enc_ms = float(t[0]), float(t[1])
-    merges_total = acc["merges"] * world
-    value = merges_total / (train_ms / 1e3)
+    (train_ms, enc_ms), (merges_total, enc_bytes_total) = reduce_ranks(
+        [acc["train_ms"], acc["enc_ms"]], [acc["merges"], enc["bytes"] * args.steps if enc else 0], world, dev)
+    value = throughput(merges_total, train_ms)
 
     # ---- end to end through host buffers (graph replay, no profiling)
     e2e = None
@@ -413,16 +431,13 @@ def run_ours(args, rank, world, local_rank):
             if i >= args.warmup:
                 tr_ms += a.elapsed_time(b)
                 en_ms += b.elapsed_time(c)
-        t2 = torch.tensor([tr_ms, en_ms], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(t2, op=dist.ReduceOp.MAX)
-        tr_ms, en_ms = float(t2[0]), float(t2[1])
-        e2e = {"value": round(args.steps * m.shape[0] * world / (tr_ms / 1e3), 2), "unit": "merges/s",
+        (tr_ms, en_ms), (e2e_merges, e2e_bytes) = reduce_ranks(
+            [tr_ms, en_ms], [args.steps * m.shape[0], args.steps * enc["bytes"] if enc else 0], world, dev)
+        e2e = {"value": round(throughput(e2e_merges, tr_ms), 2), "unit": "merges/s",
                "h2d_bytes_per_step": int(text.size + (enc["bytes"] + enc["h_off"].numel() * 8 if enc else 0)),
                "d2h_bytes_per_step": int(h_merges_bytes + d2h_ids)}
         if enc:
-            e2e["encode"] = {"value": round(args.steps * enc["bytes"] * world / (en_ms / 1e3) / 1e9, 3),
-                             "unit": "GB/s"}
+            e2e["encode"] = {"value": round(throughput(e2e_bytes, en_ms) / 1e9, 3), "unit": "GB/s"}
 
     # ---- extra legs: the word-frequency trainer (same merges), the large
     # training workload, the batch encode workload
@@ -466,7 +481,7 @@ def run_ours(args, rank, world, local_rank):
     }
     out.update(extra)
     if enc:
-        gbs = args.steps * enc["bytes"] * world / (enc_ms / 1e3) / 1e9
+        gbs = throughput(enc_bytes_total, enc_ms) / 1e9
         out["encode"] = {"value": round(gbs, 3), "unit": "GB/s", "ms_per_step": round(enc_ms / args.steps, 3),
                          "workload": enc["workload"], "n_ids": acc["n_ids"],
                          "roofline": roofline(kern, ["encode_spec", "encode_emit"], peak, peak_kind, traffic)}
