@@ -82,6 +82,9 @@ struct EncParams {
     uint32_t *flist;             // flagged chunks, unordered (flist_cap entries; 0 = none kept)
     uint32_t flist_cap;
     uint32_t *wpriv;             // per flagged chunk: its repair walk (kWalkWords words)
+    uint32_t *sbits;             // per chunk: C/32 words, token starts of the speculative parse
+    int32_t *sids;               // per chunk: C words, the speculative parse's ids in order
+                                 // (both null: the emit pass re-parses every chunk)
     unsigned long long *prefix;  // per chunk: global index of its first id
     unsigned long long *status;  // look-back words per emit tile
     int32_t *ids;
@@ -178,18 +181,24 @@ struct ByteWin {
 // lane -- from the root through the shared LUT, or from a node through the
 // double array -- so the lanes of a warp run the same instructions whatever
 // their token lengths; a token ends when a step fails.
-//   MODE 0 (speculative): mark token starts in bits (offsets from cs)
+//   MODE 0 (speculative): mark token starts in bits (offsets from cs) and,
+//          when sid is not null, store each token to sid[0 ...]: its id when
+//          it is one byte long (from the root LUT), else 0x80000000 | its
+//          trie slot, so the id lookup leaves the parse's critical path
 //   MODE 1 (resync): stop early where a token start is already marked
 //   MODE 2 (emit): write ids to ids[o ...] (below cap)
-// Returns the position after the last token; *cnt = tokens parsed (MODE 1:
-// tokens up to the meeting point, *met = whether it met the marked path).
+//   MODE 3 (emit head): MODE 2's writes, stopping like MODE 1
+// Returns the position after the last token; *cnt = tokens parsed (MODE 1
+// and 3: tokens up to the meeting point, *met = whether it met the marked
+// path).
 template <int MODE>
 __device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 *lut, uint64_t p, uint64_t ce,
                                                  uint64_t de, uint64_t cs, uint32_t *bits, uint32_t *cnt,
-                                                 unsigned long long o, bool *met) {
+                                                 unsigned long long o, bool *met, int32_t *sid = nullptr) {
+    constexpr bool kMeet = MODE == 1 || MODE == 3, kWrite = MODE == 2 || MODE == 3;
     uint32_t c = 0;
-    if (MODE == 1) *met = false;
-    if (p < ce && MODE == 1) {
+    if (kMeet) *met = false;
+    if (p < ce && kMeet) {
         const uint32_t off = (uint32_t)(p - cs);
         if ((bits[off >> 5] >> (off & 31)) & 1u) {
             *met = true;
@@ -235,12 +244,13 @@ __device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 
             if (MODE == 0) {
                 const uint32_t off = (uint32_t)(p - cs);
                 bits[off >> 5] |= 1u << (off & 31);
+                if (sid) sid[c] = bnode >= 0 ? (int32_t)(0x80000000u | (uint32_t)bnode) : btid;
             }
-            if (MODE == 2 && o < P.cap) P.ids[o] = bnode >= 0 ? __ldg(P.tid + bnode) : btid;
+            if (kWrite && o < P.cap) P.ids[o] = bnode >= 0 ? __ldg(P.tid + bnode) : btid;
             ++o;
             ++c;
             p += blen;
-            if (MODE == 1 && p < ce) {
+            if (kMeet && p < ce) {
                 const uint32_t off = (uint32_t)(p - cs);
                 if ((bits[off >> 5] >> (off & 31)) & 1u) {
                     *met = true;
@@ -259,7 +269,10 @@ __device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 
 }
 
 __host__ __device__ __forceinline__ size_t spec_smem_for(uint32_t C) { return (size_t)kSpecThreads * (C / 32) * 4; }
-__host__ __device__ __forceinline__ size_t emit_smem_for(uint32_t) { return 0; }
+__host__ __device__ __forceinline__ size_t emit_smem_for(uint32_t C) { return (size_t)kEmitThreads * (C / 32) * 4; }
+// Stored speculative ids take 4 bytes per input byte; above this the emit
+// pass re-parses instead (also when the allocation fails).
+constexpr uint64_t kMaxSpecIdBytes = 16ull << 30;
 
 // ---------------------------------------------------------- chunk index ---
 
@@ -310,7 +323,7 @@ __global__ void __launch_bounds__(1024) k_chunk_index(EncParams P, unsigned long
 
 // ------------------------------------------------ speculative parse + fix ---
 
-__global__ void __launch_bounds__(kSpecThreads) k_spec(EncParams P, unsigned long long n_chunks, uint64_t text_end) {
+__global__ void __launch_bounds__(kSpecThreads, 8) k_spec(EncParams P, unsigned long long n_chunks, uint64_t text_end) {
     extern __shared__ uint32_t s_bits[];   // kSpecThreads x (C/32) token-start bitmaps
     __shared__ int4 lut[256];
     __shared__ unsigned long long s_exit[kSpecThreads];
@@ -329,7 +342,10 @@ __global__ void __launch_bounds__(kSpecThreads) k_spec(EncParams P, unsigned lon
     uint64_t spec_exit = 0;
     if (live) {
         for (uint32_t w = 0; w < words; w++) bits[w] = 0;
-        spec_exit = parse_tokens<0>(P, lut, g.cs, g.ce, g.de, g.cs, bits, &spec_count, 0, nullptr);
+        int32_t *sid = P.sids ? P.sids + (size_t)k * P.chunk : nullptr;
+        spec_exit = parse_tokens<0>(P, lut, g.cs, g.ce, g.de, g.cs, bits, &spec_count, 0, nullptr, sid);
+        if (P.sbits)
+            for (uint32_t w = 0; w < words; w++) P.sbits[(size_t)k * words + w] = bits[w];
     }
     s_exit[tid] = spec_exit;
     __syncthreads();
@@ -509,7 +525,10 @@ __global__ void __launch_bounds__(1024) k_repair_apply(EncParams P, unsigned lon
 // ------------------------------------------------------------ scan + emit ---
 
 __global__ void __launch_bounds__(kEmitThreads) k_emit(EncParams P, unsigned long long n_chunks, uint64_t text_end) {
+    extern __shared__ uint32_t s_bits[];   // kEmitThreads x (C/32): each chunk's spec token starts
     __shared__ int4 lut[256];
+    __shared__ unsigned long long s_csrc[kEmitThreads], s_cdst[kEmitThreads];   // per chunk: copy source, target
+    __shared__ uint32_t s_cbeg[kEmitThreads];                                  // per chunk: start in the warp's range
     __shared__ uint32_t s_w[kEmitThreads / 32];
     __shared__ unsigned long long s_tile, s_off;
     load_lut(P, lut);
@@ -569,12 +588,75 @@ __global__ void __launch_bounds__(kEmitThreads) k_emit(EncParams P, unsigned lon
         }
     }
     __syncthreads();
+    const unsigned long long o = s_off + wpre + incl - cnt;
+    if (live) P.prefix[k] = o;
+    if (!P.sids) {   // re-parse the chunk from its true entry
+        if (live) {
+            const uint64_t e = g.doc_first ? g.cs : (g.cs - P.chunk) + P.exit_rel[k - 1];
+            uint32_t c = 0;
+            parse_tokens<2>(P, lut, e, g.ce, g.de, g.cs, nullptr, &c, o, nullptr);
+        }
+        return;
+    }
+    // Parse from the true entry only until the path meets a token start of the
+    // speculative parse; the rest of the chunk's ids are the stored ones.
+    uint32_t src_t = 0, n_copy = 0, c_head = 0;
     if (live) {
-        const unsigned long long o = s_off + wpre + incl - cnt;
-        P.prefix[k] = o;
+        const uint32_t words = P.chunk >> 5;
+        uint32_t *bits = s_bits + tid * words;
+        uint32_t n_spec = 0;
+        for (uint32_t w = 0; w < words; w++) {
+            bits[w] = P.sbits[(size_t)k * words + w];
+            n_spec += __popc(bits[w]);
+        }
         const uint64_t e = g.doc_first ? g.cs : (g.cs - P.chunk) + P.exit_rel[k - 1];
-        uint32_t c = 0;
-        parse_tokens<2>(P, lut, e, g.ce, g.de, g.cs, nullptr, &c, o, nullptr);
+        bool met = false;
+        const uint64_t q = parse_tokens<3>(P, lut, e, g.ce, g.de, g.cs, bits, &c_head, o, &met);
+        if (met) {   // spec tokens before offset q - cs are skipped
+            const uint32_t off = (uint32_t)(q - g.cs);
+            uint32_t before = 0;
+            for (uint32_t w = 0; w < (off >> 5); w++) before += __popc(bits[w]);
+            before += __popc(bits[off >> 5] & ((1u << (off & 31)) - 1u));
+            src_t = before;
+            n_copy = n_spec - before;
+        }
+    }
+    // The warp's 32 tails form one range of W ids: lane L copies ids L, L+32,
+    // ... (coalesced reads and writes, four in flight), finding each id's
+    // chunk by a binary search over the tails' starts.
+    const unsigned long long dst = o + c_head;
+    const uint32_t tincl = warp_incl_sum(n_copy, lane);
+    const uint32_t W = __shfl_sync(kFull, tincl, 31);
+    unsigned long long *wsrc = s_csrc + warp * 32, *wdst = s_cdst + warp * 32;
+    uint32_t *wbeg = s_cbeg + warp * 32;
+    wbeg[lane] = tincl - n_copy;
+    wsrc[lane] = (unsigned long long)k * P.chunk + src_t;
+    wdst[lane] = dst;
+    __syncwarp();
+    for (uint32_t w0 = 0; w0 < W; w0 += 4 * 32) {
+        int32_t v[4];
+        unsigned long long d[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            const uint32_t w = w0 + u * 32 + lane;
+            d[u] = ~0ull;
+            if (w < W) {
+                int j = 0;   // last lane whose tail starts at or before w
+#pragma unroll
+                for (int step = 16; step > 0; step >>= 1)
+                    if (wbeg[j + step] <= w) j += step;
+                const uint32_t r = w - wbeg[j];
+                v[u] = __ldcs(P.sids + wsrc[j] + r);
+                d[u] = wdst[j] + r;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            if (d[u] != ~0ull && d[u] < P.cap) {
+                const int32_t x = v[u];
+                P.ids[d[u]] = x < 0 ? __ldg(P.tid + (x & 0x7FFFFFFF)) : x;
+            }
+        }
     }
 }
 
@@ -671,6 +753,17 @@ extern "C" int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_
     P.flist_cap = kFlagListCap;
     P.wpriv = P.flist + kFlagListCap;
     P.id_off = d_id_off_out ? (unsigned long long *)d_id_off_out : (unsigned long long *)idoff_tmp;
+    // the speculative parse's ids and token starts, so emit copies instead of re-parsing
+    const uint64_t sid_bytes = nc * (uint64_t)C * 4, sbit_bytes = nc * (uint64_t)(C / 32) * 4;
+    if (sid_bytes <= kMaxSpecIdBytes) {
+        void *sids = nullptr, *sbits = nullptr;
+        if (ensure(ctx, S_ENC_SIDS, sid_bytes, &sids) == BPE_OK && ensure(ctx, S_ENC_SBITS, sbit_bytes, &sbits) == BPE_OK) {
+            P.sids = (int32_t *)sids;
+            P.sbits = (uint32_t *)sbits;
+        } else {
+            ctx->err.clear();   // no room: the emit pass re-parses
+        }
+    }
 
     BPE_CUDA(ctx, cudaMemsetAsync(flag, 0, ((nc + 31) / 32) * 4, s), "flag clear");
     BPE_CUDA(ctx, cudaMemsetAsync(status, 0, emit_tiles * 8, s), "status clear");

@@ -18,7 +18,8 @@ namespace bpe {
 enum Slot {
     S_TRAIN_BUF0, S_TRAIN_BUF1, S_TABLE_KEY, S_TABLE_CNT, S_LIST0, S_LIST1,
     S_STATUS0, S_STATUS1, S_BEST, S_STATE, S_NHIST,
-    S_ENC_CHUNK_START, S_ENC_CHUNK_INFO, S_ENC_NOTOK, S_ENC_STATUS, S_ENC_PREFIX, S_ENC_STATE,
+    S_ENC_CHUNK_START, S_ENC_CHUNK_INFO, S_ENC_NOTOK, S_ENC_STATUS, S_ENC_PREFIX, S_ENC_STATE, S_ENC_SIDS,
+    S_ENC_SBITS,
     S_W_BSUM, S_W_START, S_W_OCCSLOT, S_W_TABLE, S_W_UID, S_W_UINFO, S_W_SYM, S_W_OUTOFF,
     S_NUM
 };
