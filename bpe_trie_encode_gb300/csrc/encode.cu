@@ -53,6 +53,7 @@ constexpr int kSpecThreads = 256;          // 255 owned chunks + 1 halo chunk pe
 constexpr int kEmitThreads = 256;
 constexpr int kMaxChunk = 256;             // bytes per chunk (staging and bitmap bound)
 constexpr unsigned kSpinLimit = 1u << 22;
+constexpr uint32_t kBS = 256;   // stride between a thread's bitmap words (one column per thread: no bank conflicts)
 
 struct EncState {
     unsigned long long n_chunks;
@@ -161,18 +162,19 @@ __device__ __forceinline__ ChunkGeo chunk_geo(const EncParams &P, unsigned long 
 
 // Sequential reads of a lane's bytes, four at a time: one aligned 32-bit load
 // through L1 serves the next bytes (the word never leaves the allocation: it
-// holds at least one byte of the text).
+// holds at least one byte of the text).  Offsets are 32-bit, from g.
 struct ByteWin {
     const uint8_t *g;
-    uintptr_t at = ~uintptr_t(0);
+    uint32_t at = 0xFFFFFFFFu;   // low word of the loaded word's address (never 4-aligned at start)
     uint32_t w = 0;
-    __device__ __forceinline__ uint32_t operator()(uint64_t p) {
-        const uintptr_t a = (uintptr_t)(g + p), al = a & ~uintptr_t(3);
+    __device__ __forceinline__ uint32_t operator()(uint32_t q) {
+        const uintptr_t a = (uintptr_t)(g + q);
+        const uint32_t al = (uint32_t)a & ~3u;
         if (al != at) {
             at = al;
-            w = __ldg(reinterpret_cast<const uint32_t *>(al));
+            w = __ldg(reinterpret_cast<const uint32_t *>(a & ~uintptr_t(3)));
         }
-        return (w >> (8 * (uint32_t)(a - al))) & 0xFFu;
+        return (w >> (8 * ((uint32_t)a & 3u))) & 0xFFu;
     }
 };
 
@@ -180,7 +182,9 @@ struct ByteWin {
 // document ending at de.  Every loop iteration takes one trie step on every
 // lane -- from the root through the shared LUT, or from a node through the
 // double array -- so the lanes of a warp run the same instructions whatever
-// their token lengths; a token ends when a step fails.
+// their token lengths; a token ends when a step fails.  Positions are kept
+// as 32-bit offsets from the chunk start cs (p >= cs; a parse never runs
+// 2^31 bytes past it).
 //   MODE 0 (speculative): mark token starts in bits (offsets from cs) and,
 //          when sid is not null, store each token to sid[0 ...]: its id when
 //          it is one byte long (from the root LUT), else 0x80000000 | its
@@ -192,25 +196,27 @@ struct ByteWin {
 // and 3: tokens up to the meeting point, *met = whether it met the marked
 // path).
 template <int MODE>
-__device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 *lut, uint64_t p, uint64_t ce,
-                                                 uint64_t de, uint64_t cs, uint32_t *bits, uint32_t *cnt,
+__device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 *lut, uint64_t p_abs, uint64_t ce_abs,
+                                                 uint64_t de_abs, uint64_t cs, uint32_t *bits, uint32_t *cnt,
                                                  unsigned long long o, bool *met, int32_t *sid = nullptr) {
     constexpr bool kMeet = MODE == 1 || MODE == 3, kWrite = MODE == 2 || MODE == 3;
+    uint32_t p = (uint32_t)(p_abs - cs);
+    const uint32_t ce = (uint32_t)(ce_abs - cs);
+    const uint32_t de = de_abs - cs < 0x7FFFFFFFull ? (uint32_t)(de_abs - cs) : 0x7FFFFFFFu;
     uint32_t c = 0;
     if (kMeet) *met = false;
     if (p < ce && kMeet) {
-        const uint32_t off = (uint32_t)(p - cs);
-        if ((bits[off >> 5] >> (off & 31)) & 1u) {
+        if ((bits[(p >> 5) * kBS] >> (p & 31)) & 1u) {
             *met = true;
             *cnt = 0;
-            return p;
+            return p_abs;
         }
     }
-    ByteWin byte{P.bytes};
+    ByteWin byte{P.bytes + cs};
     int32_t node = -1;            // -1: at the root
     uint32_t y = 0, blen = 0;     // base|TERM of node; length of the best token so far
     int32_t bnode = -1, btid = 0; // best token: its slot (id in tid[]) or, at depth 1, its id
-    uint64_t q = p;
+    uint32_t q = p;
     while (p < ce) {
         const bool root = node < 0;
         const uint32_t base = y & ~kTermBit;
@@ -237,13 +243,12 @@ __device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 
             y = ny;
             ++q;
             if (ny & kTermBit) {
-                blen = (uint32_t)(q - p);
+                blen = q - p;
                 bnode = root ? -1 : nt;
             }
         } else {   // the token [p, p + blen) ends here (every byte is a token: blen >= 1)
             if (MODE == 0) {
-                const uint32_t off = (uint32_t)(p - cs);
-                bits[off >> 5] |= 1u << (off & 31);
+                bits[(p >> 5) * kBS] |= 1u << (p & 31);
                 if (sid) sid[c] = bnode >= 0 ? (int32_t)(0x80000000u | (uint32_t)bnode) : btid;
             }
             if (kWrite && o < P.cap) P.ids[o] = bnode >= 0 ? __ldg(P.tid + bnode) : btid;
@@ -251,8 +256,7 @@ __device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 
             ++c;
             p += blen;
             if (kMeet && p < ce) {
-                const uint32_t off = (uint32_t)(p - cs);
-                if ((bits[off >> 5] >> (off & 31)) & 1u) {
+                if ((bits[(p >> 5) * kBS] >> (p & 31)) & 1u) {
                     *met = true;
                     break;
                 }
@@ -265,7 +269,7 @@ __device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 
         }
     }
     *cnt = c;
-    return p;
+    return cs + p;
 }
 
 __host__ __device__ __forceinline__ size_t spec_smem_for(uint32_t C) { return (size_t)kSpecThreads * (C / 32) * 4; }
@@ -329,7 +333,7 @@ __global__ void __launch_bounds__(kSpecThreads, 8) k_spec(EncParams P, unsigned 
     __shared__ unsigned long long s_exit[kSpecThreads];
     const int tid = threadIdx.x;
     const uint32_t words = P.chunk >> 5;
-    uint32_t *bits = s_bits + tid * words;
+    uint32_t *bits = s_bits + tid;
     const long long k = (long long)blockIdx.x * (kSpecThreads - 1) + tid - 1;
     const bool live = k >= 0 && (unsigned long long)k < n_chunks;
     load_lut(P, lut);
@@ -341,11 +345,11 @@ __global__ void __launch_bounds__(kSpecThreads, 8) k_spec(EncParams P, unsigned 
     uint32_t spec_count = 0;
     uint64_t spec_exit = 0;
     if (live) {
-        for (uint32_t w = 0; w < words; w++) bits[w] = 0;
+        for (uint32_t w = 0; w < words; w++) bits[w * kBS] = 0;
         int32_t *sid = P.sids ? P.sids + (size_t)k * P.chunk : nullptr;
         spec_exit = parse_tokens<0>(P, lut, g.cs, g.ce, g.de, g.cs, bits, &spec_count, 0, nullptr, sid);
         if (P.sbits)
-            for (uint32_t w = 0; w < words; w++) P.sbits[(size_t)k * words + w] = bits[w];
+            for (uint32_t w = 0; w < words; w++) P.sbits[(size_t)k * words + w] = bits[w * kBS];
     }
     s_exit[tid] = spec_exit;
     __syncthreads();
@@ -364,8 +368,8 @@ __global__ void __launch_bounds__(kSpecThreads, 8) k_spec(EncParams P, unsigned 
         const uint64_t q = parse_tokens<1>(P, lut, s_exit[tid - 1], g.ce, g.de, g.cs, bits, &c, 0, &met);
         if (met) {
             const uint32_t o = (uint32_t)(q - g.cs);
-            uint32_t rest = __popc(bits[o >> 5] >> (o & 31));
-            for (uint32_t w = (o >> 5) + 1; w < words; w++) rest += __popc(bits[w]);
+            uint32_t rest = __popc(bits[(o >> 5) * kBS] >> (o & 31));
+            for (uint32_t w = (o >> 5) + 1; w < words; w++) rest += __popc(bits[w * kBS]);
             c += rest;
             exit = spec_exit;
         } else {
@@ -603,11 +607,11 @@ __global__ void __launch_bounds__(kEmitThreads) k_emit(EncParams P, unsigned lon
     uint32_t src_t = 0, n_copy = 0, c_head = 0;
     if (live) {
         const uint32_t words = P.chunk >> 5;
-        uint32_t *bits = s_bits + tid * words;
+        uint32_t *bits = s_bits + tid;
         uint32_t n_spec = 0;
         for (uint32_t w = 0; w < words; w++) {
-            bits[w] = P.sbits[(size_t)k * words + w];
-            n_spec += __popc(bits[w]);
+            bits[w * kBS] = P.sbits[(size_t)k * words + w];
+            n_spec += __popc(bits[w * kBS]);
         }
         const uint64_t e = g.doc_first ? g.cs : (g.cs - P.chunk) + P.exit_rel[k - 1];
         bool met = false;
@@ -615,8 +619,8 @@ __global__ void __launch_bounds__(kEmitThreads) k_emit(EncParams P, unsigned lon
         if (met) {   // spec tokens before offset q - cs are skipped
             const uint32_t off = (uint32_t)(q - g.cs);
             uint32_t before = 0;
-            for (uint32_t w = 0; w < (off >> 5); w++) before += __popc(bits[w]);
-            before += __popc(bits[off >> 5] & ((1u << (off & 31)) - 1u));
+            for (uint32_t w = 0; w < (off >> 5); w++) before += __popc(bits[w * kBS]);
+            before += __popc(bits[(off >> 5) * kBS] & ((1u << (off & 31)) - 1u));
             src_t = before;
             n_copy = n_spec - before;
         }
