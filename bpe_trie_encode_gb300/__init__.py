@@ -20,9 +20,9 @@ import numpy as np
 import torch
 
 from . import _capi
-from ._capi import (BPE_MAX_MERGES, BPE_OPT_CHUNK, BPE_OPT_GRAPH, BPE_OPT_MERGE_LOOKBACK,  # noqa: F401
-                    BPE_OPT_PERSISTENT, BPE_OPT_PROFILE, BPE_OPT_TABLE_LOG2, BPE_OPT_TRAIN_WORDS, BPE_WORD_START,
-                    BpeError)
+from ._capi import (BPE_MAX_MERGES, BPE_MERGE_LOOKBACK, BPE_MERGE_TILES, BPE_MERGE_TWO_PASS,  # noqa: F401
+                    BPE_OPT_CHUNK, BPE_OPT_GRAPH, BPE_OPT_MERGE, BPE_OPT_PERSISTENT, BPE_OPT_PROFILE,
+                    BPE_OPT_TABLE_LOG2, BPE_OPT_TRAIN_WORDS, BPE_WORD_START, BpeError)
 
 __all__ = ["Context", "Trie", "BpeError", "vocab_from_merges", "BPE_WORD_START", "BPE_MAX_MERGES"]
 

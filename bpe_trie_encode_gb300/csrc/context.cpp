@@ -155,8 +155,10 @@ extern "C" int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value) {
     case BPE_OPT_TRAIN_WORDS:
         ctx->train_words = value ? 1 : 0;
         return BPE_OK;
-    case BPE_OPT_MERGE_LOOKBACK:
-        ctx->merge_lookback = value ? 1 : 0;
+    case BPE_OPT_MERGE:
+        if (value != BPE_MERGE_TILES && value != BPE_MERGE_LOOKBACK && value != BPE_MERGE_TWO_PASS)
+            return fail(ctx, BPE_ERR_INVALID_ARG, "unknown merge variant %lld", (long long)value);
+        ctx->merge_mode = (int)value;
         return BPE_OK;
     case BPE_OPT_PERSISTENT:
         ctx->persistent = value ? 1 : 0;

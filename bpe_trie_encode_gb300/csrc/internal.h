@@ -54,7 +54,7 @@ struct bpe_ctx {
     int profile = 0;
     int chunk = 128;
     int train_words = 0;
-    int merge_lookback = 0;
+    int merge_mode = 0;   // BPE_MERGE_*
     int persistent = 0;
     // cached graph of merge iterations
     bpe::TrainGraph graph;

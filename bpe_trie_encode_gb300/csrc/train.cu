@@ -91,6 +91,7 @@ struct TrainState {
     unsigned long long n[2];  // stream length, by merge parity
     uint32_t ticket[2];       // tile tickets, by merge parity
     uint32_t msum_done;       // k_msum CTAs finished (the last one scans)
+    uint32_t gactive[2];      // gapped tiles: tiles in use, by merge parity
     // grid barrier of the persistent merge loop: kBarGroups arrival counters,
     // the groups' counter and the release generation, each on its own
     // 128-byte line so arrivals and polling do not queue at one L2 slice
@@ -111,6 +112,12 @@ struct TrainParams {
     unsigned long long *nhist;   // stream length after k merges
     uint32_t *dhist;             // dense entries scanned by argmax k
     TrainState *st;
+    // gapped tiles: tile t's live symbols sit at buf + t * kMergeTile
+    uint32_t *glen[2];           // live symbols per tile, by merge parity
+    uint32_t *gsum;              // summary pass: tile summaries
+    uint32_t *gcarry;            // summary pass: merge flag entering each tile
+    unsigned long long *goff;    // summary pass: output offset of each tile (compacting merges)
+    uint32_t gtiles;
 };
 
 __device__ __forceinline__ unsigned long long pack_best(uint32_t count, uint32_t key) {
@@ -413,10 +420,11 @@ __device__ __forceinline__ bool lookback(const unsigned long long *status, uint6
 }
 
 // Count deltas of one thread's 16 positions (rare: only where a merge happened
-// nearby).  mm: bit j = m(pos+j) for j = 0..17; mprev = m(pos-1); sym(j) reads
-// symbol pos+j from the padded tile.
+// nearby), those before re only.  mm: bit j = m(pos+j) for j = 0..17; mprev =
+// m(pos-1); sym(j) reads symbol pos+j from the padded tile; symbols exist
+// below n.
 __device__ __noinline__ void thread_deltas(const Table p, uint32_t *dkey, uint32_t *dval, uint32_t *socc,
-                                           const uint32_t *mys, uint64_t pos, uint64_t n, uint32_t mm,
+                                           const uint32_t *mys, uint64_t pos, uint64_t re, uint64_t n, uint32_t mm,
                                            uint32_t mprev, uint32_t new_id) {
     auto sym = [&](int j) { return mys[j < 16 ? j : j + 1]; };
     auto add = [&](uint32_t kk, uint32_t d) {
@@ -428,7 +436,7 @@ __device__ __noinline__ void thread_deltas(const Table p, uint32_t *dkey, uint32
     while (told) {
         const int j = __ffs(told) - 1;
         told &= told - 1;
-        if (pos + j + 1 >= n) break;
+        if (pos + j >= re || pos + j + 1 >= n) break;   // pairs owned by positions before re
         const uint32_t b = sym(j + 1);
         if (!(b & kWordStart)) add(pair_key(sym(j), b), 0xFFFFFFFFu);
     }
@@ -437,7 +445,7 @@ __device__ __noinline__ void thread_deltas(const Table p, uint32_t *dkey, uint32
     while (tnew) {
         const int j = __ffs(tnew) - 1;
         tnew &= tnew - 1;
-        if (pos + j >= n) break;
+        if (pos + j >= re) break;
         const uint32_t mj = (mm >> j) & 1u;
         const int nk = j + 1 + (int)mj;
         if (pos + nk >= n) continue;
@@ -480,16 +488,19 @@ __device__ __forceinline__ uint32_t staged_valid(const uint32_t *mys, uint64_t p
     return valid;
 }
 
-// Summary of one thread's 16 positions given their valid starts.
-__device__ __forceinline__ uint32_t thread_summary(uint32_t valid, uint64_t pos, uint64_t n) {
+// Summary of one thread's 16 positions given their valid starts; positions
+// at or past re (not this tile's) are left out.
+__device__ __forceinline__ uint32_t thread_summary(uint32_t valid, uint64_t pos, uint64_t re) {
     uint32_t kept[2], fout[2];
 #pragma unroll
     for (uint32_t c = 0; c < 2; c++) {
         uint32_t par = c, kc = 0;
 #pragma unroll
         for (int j = 0; j < kMergeItems; j++) {
-            if (pos + j < n) kc += par ^ 1u;
-            par = ((valid >> j) & 1u) ? (par ^ 1u) : 0u;
+            if (pos + j < re) {
+                kc += par ^ 1u;
+                par = ((valid >> j) & 1u) ? (par ^ 1u) : 0u;
+            }
         }
         kept[c] = kc;
         fout[c] = par;
@@ -548,14 +559,15 @@ __device__ __forceinline__ void emit_plain(const TrainParams &p, const uint32_t 
 // Merge and compact a staged tile given each thread's merge flags (mm: bit j
 // = m(pos+j), j = 0 .. 17; mprev = m(pos-1)), its tile-local output index e
 // and the tile's kept count: count deltas, then the surviving symbols in
-// order from out + obase.  Needs the delta table cleared (by a barrier ago).
+// order from out + obase.  Positions before re are the tile's own; symbols
+// exist below n.  Needs the delta table cleared (by a barrier ago).
 __device__ __forceinline__ void emit_full(const TrainParams &p, uint32_t *stile, uint32_t *dkey, uint32_t *dval,
                                           uint32_t *s_docc, uint32_t mm, uint32_t mprev, uint32_t e,
-                                          uint32_t tile_kept, unsigned long long obase, uint64_t pos, uint64_t n,
-                                          uint32_t new_id, uint32_t *out, int tid) {
+                                          uint32_t tile_kept, unsigned long long obase, uint64_t pos, uint64_t re,
+                                          uint64_t n, uint32_t new_id, uint32_t *out, int tid) {
     const uint32_t *mys = stile + padded(kMergeItems * tid);
     if ((mm | mprev) & 0x1FFFFu)   // some merge touches this thread's pairs
-        thread_deltas(table_of(p), dkey, dval, s_docc, mys, pos, n, mm, mprev, new_id);
+        thread_deltas(table_of(p), dkey, dval, s_docc, mys, pos, re, n, mm, mprev, new_id);
     const uint32_t mext = (mm << 1) | mprev;   // bit j: position pos+j consumed
     uint32_t outv[kMergeItems];
 #pragma unroll
@@ -566,7 +578,7 @@ __device__ __forceinline__ void emit_full(const TrainParams &p, uint32_t *stile,
     __syncthreads();   // every symbol of the tile is in registers: the tile buffer is free
 #pragma unroll
     for (int j = 0; j < kMergeItems; j++)
-        if (pos + j < n && !((mext >> j) & 1u)) stile[padded(e++)] = outv[j];
+        if (pos + j < re && !((mext >> j) & 1u)) stile[padded(e++)] = outv[j];
     __syncthreads();
     for (uint32_t i = tid; i < tile_kept; i += kMergeThreads) out[obase + i] = stile[padded(i)];
 }
@@ -714,7 +726,7 @@ __global__ void __launch_bounds__(kMergeThreads, 4) k_merge(TrainParams p, uint3
     const uint32_t mm = run_flags(valid, excl, carry, &mprev);
     const uint32_t e = carry ? (excl >> 17) : ((excl >> 2) & 0x7FFFu);
     const uint32_t tile_kept = carry ? (tile >> 17) : ((tile >> 2) & 0x7FFFu);
-    emit_full(p, stile, dkey, dval, &s_docc, mm, mprev, e, tile_kept, s_off, pos, n, op.new_id, op.out, tid);
+    emit_full(p, stile, dkey, dval, &s_docc, mm, mprev, e, tile_kept, s_off, pos, n, n, op.new_id, op.out, tid);
     flush_deltas(p, dkey, dval, &s_docc);
 }
 
@@ -1155,7 +1167,7 @@ __device__ __forceinline__ void apply_range(const TrainParams &p, const MergeOp 
             const uint32_t mm = run_flags(valid, excl, carry, &mprev);
             const uint32_t e = carry ? (excl >> 17) : ((excl >> 2) & 0x7FFFu);
             const uint32_t tile_kept = carry ? (tile >> 17) : ((tile >> 2) & 0x7FFFu);
-            emit_full(p, stile, dkey, dval, &sh.docc, mm, mprev, e, tile_kept, off, pos, n, op.new_id, op.out, tid);
+            emit_full(p, stile, dkey, dval, &sh.docc, mm, mprev, e, tile_kept, off, pos, n, n, op.new_id, op.out, tid);
             off += tile_kept;
             carry = fapply(tile & 3u, carry);
             __syncthreads();   // the tile buffer and shared words are reused
@@ -1294,6 +1306,444 @@ __global__ void __launch_bounds__(kMergeThreads, 4) k_train_loop(TrainParams p, 
     }
 }
 
+// ------------------------------------------------------- gapped tile stream ---
+//
+// BPE_MERGE_TILES.  The stream is kept as fixed 4,096-slot tiles,
+// each holding its live symbols at its start (a count per tile); the stream
+// is the tiles' live parts in order.  A merge compacts each tile into the
+// same tile of the other buffer, so no global offset is needed: for l != r
+// one kernel does the whole merge, each tile reading the symbols around it
+// from its neighbours' live parts.  For l == r a summary pass first gives
+// each tile the merge flag entering it.  The contiguous stream is gathered
+// once, at the end.
+
+constexpr int kGapStage = 4 + kMergeTile + 16;   // [3] = symbol before the tile, [4 ..] = tile + halo
+
+struct GapHalo {
+    uint32_t prev, has_prev, nnext;
+    uint32_t nx[3];
+};
+
+// The last live symbol before tile t and the first (up to 3) after it,
+// skipping empty tiles.
+__device__ __forceinline__ void gap_halo(const uint32_t *in, const uint32_t *lin, uint32_t T, uint32_t t,
+                                         GapHalo *h) {
+    h->has_prev = 0;
+    h->prev = 0;
+    for (uint32_t u = t; u-- > 0;) {
+        const uint32_t lu = __ldcg(lin + u);
+        if (lu) {
+            h->prev = __ldcg(in + (uint64_t)u * kMergeTile + lu - 1);
+            h->has_prev = 1;
+            break;
+        }
+    }
+    h->nnext = 0;
+    for (uint32_t u = t + 1; u < T && h->nnext < 3; u++) {
+        const uint32_t lu = __ldcg(lin + u);
+        for (uint32_t i = 0; i < lu && h->nnext < 3; i++) h->nx[h->nnext++] = __ldcg(in + (uint64_t)u * kMergeTile + i);
+    }
+}
+
+// Stage tile t's len live symbols and the halo symbols after them into the
+// padded layout of the transducer path (tile-local positions).  Ends with a
+// barrier.
+__device__ __forceinline__ void stage_gapped_padded(uint32_t *stile, const uint32_t *tin, uint32_t len,
+                                                    const GapHalo &h) {
+    constexpr int kQuads = (kMergeTile + kTileHalo) / 4 / kMergeThreads + 1;
+    uint4 v[kQuads];
+#pragma unroll
+    for (int u = 0; u < kQuads; u++) {   // all loads in flight before the first store
+        const uint32_t i4 = threadIdx.x + u * blockDim.x;
+        v[u] = 4 * i4 < len ? __ldcg(reinterpret_cast<const uint4 *>(tin) + i4) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kQuads; u++) {
+        const uint32_t i4 = threadIdx.x + u * blockDim.x;
+        if (i4 < (kMergeTile + kTileHalo) / 4) {
+            uint32_t *d = stile + padded(4 * i4);
+            d[0] = v[u].x; d[1] = v[u].y; d[2] = v[u].z; d[3] = v[u].w;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        for (uint32_t j = 0; j < h.nnext; j++) stile[padded(len + j)] = h.nx[j];
+    __syncthreads();
+}
+
+__device__ __forceinline__ uint32_t bit_if(bool b, int j) { return b ? (1u << j) : 0u; }
+
+// l != r, one tile: warp w takes tile positions [512 w, 512 w + 512) in four
+// rounds of 128 (lane L: 4 positions from 128 q + 4 L), reading the staged
+// tile (sdat[3]: the symbol before the tile, sdat[4 + i]: symbol i, halo after
+// len).  Every read of sdat happens before the one barrier in here; after it
+// each warp packs its survivors into its own part of sout and copies them to
+// tout.  Returns the tile's kept count.
+__device__ __forceinline__ uint32_t gap_tile_distinct(const TrainParams &p, const MergeOp &op, const uint32_t *sdat,
+                                                      uint32_t len, uint32_t E, bool has_prev, uint32_t *sout,
+                                                      uint32_t *tout, uint32_t *s_wtot, uint32_t *dkey,
+                                                      uint32_t *dval, uint32_t *s_docc, int lane, int warp) {
+    const uint32_t w0 = (uint32_t)kWarpSpan * warp;
+    uint32_t packed = 0, kept4[kRounds] = {0, 0, 0, 0}, mext[kRounds] = {0, 0, 0, 0};
+    uint4 xs[kRounds], xn[kRounds];
+#pragma unroll
+    for (int q = 0; q < kRounds; q++) {
+        const uint32_t p0 = w0 + 128u * q + 4u * lane;
+        xs[q] = make_uint4(0, 0, 0, 0);
+        xn[q] = make_uint4(0, 0, 0, 0);
+        if (p0 >= len) continue;
+        xs[q] = *reinterpret_cast<const uint4 *>(sdat + 4 + p0);
+        xn[q] = *reinterpret_cast<const uint4 *>(sdat + 8 + p0);
+        const uint32_t sp = sdat[3 + p0];   // symbol p0 - 1
+        const uint32_t sym[8] = {sp, xs[q].x, xs[q].y, xs[q].z, xs[q].w, xn[q].x, xn[q].y, xn[q].z};
+        // bit j: m(p0 - 1 + j) = valid(p0 - 1 + j), j = 0 .. 6 (l != r: every valid start merges)
+        uint32_t m = 0;
+#pragma unroll
+        for (int j = 0; j < 7; j++) {
+            const uint32_t i1 = p0 + j;   // position of the right symbol of the pair starting at p0 - 1 + j
+            const bool exists = i1 < E && (j > 0 || p0 > 0 || has_prev);
+            m |= bit_if(exists && is_l(sym[j], op.l) && is_r(sym[j + 1], op.r), j);
+        }
+        mext[q] = m;
+        uint32_t kb = ~m & 0xFu;   // position p0 + j is consumed when p0 + j - 1 merged
+        if (len - p0 < 4) kb &= (1u << (len - p0)) - 1u;
+        kept4[q] = kb;
+        packed |= (uint32_t)__popc(kb) << (8 * q);
+    }
+    const uint32_t incl = warp_incl_sum(packed, lane);
+    const uint32_t excl = incl - packed;
+    const uint32_t tot = __shfl_sync(kFull, incl, 31);
+    uint32_t wkept = 0;
+#pragma unroll
+    for (int q = 0; q < kRounds; q++) wkept += (tot >> (8 * q)) & 0xFFu;
+    if (lane == 0) s_wtot[warp] = wkept;
+    // count deltas where a merge is near (positions of this tile only)
+#pragma unroll
+    for (int q = 0; q < kRounds; q++) {
+        if (mext[q] & 0x3Fu) {
+            const uint32_t sq[6] = {xs[q].x, xs[q].y, xs[q].z, xs[q].w, xn[q].x, xn[q].y};
+            quad_deltas(table_of(p), dkey, dval, s_docc, sq, w0 + 128u * q + 4u * lane, len, E, mext[q], op.new_id,
+                        pair_key(op.l, op.r));
+        }
+    }
+    __syncthreads();
+    uint32_t wpre = 0, tile_kept = 0;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; w++) {
+        const uint32_t t = s_wtot[w];
+        wpre += w < warp ? t : 0u;
+        tile_kept += t;
+    }
+    uint32_t rbase = wpre;
+#pragma unroll
+    for (int q = 0; q < kRounds; q++) {
+        uint32_t o = rbase + ((excl >> (8 * q)) & 0xFFu);
+        const uint32_t x4[4] = {xs[q].x, xs[q].y, xs[q].z, xs[q].w};
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            if ((kept4[q] >> j) & 1u) sout[o++] = ((mext[q] >> (j + 1)) & 1u) ? (op.new_id | (x4[j] & kWordStart)) : x4[j];
+        rbase += (tot >> (8 * q)) & 0xFFu;
+    }
+    __syncwarp();
+    for (uint32_t i = wpre + lane; i < wpre + wkept; i += 32) tout[i] = sout[i];
+    return tile_kept;
+}
+
+// l == r, one tile entering with merge flag carry: the transducer path over
+// the padded staging (kept apart so its registers do not weigh on the l != r
+// path).  Returns the tile's kept count; ends after its last barrier.
+__device__ __noinline__ uint32_t gap_tile_runs(const TrainParams &p, const MergeOp &op, const uint32_t *tin,
+                                               uint32_t *tout, uint32_t len, const GapHalo &h, uint32_t carry,
+                                               uint32_t *stile, uint32_t *dkey, uint32_t *dval, MergeShared &sh,
+                                               uint32_t *prev_out) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    stage_gapped_padded(stile, tin, len, h);
+    const uint32_t E = len + h.nnext;
+    const uint64_t pos = (uint64_t)kMergeItems * tid;
+    const uint32_t valid = staged_valid(stile + padded(kMergeItems * tid), pos, E, op.l, op.r);
+    // the full path also when the first position after the tile merges: the
+    // pair (last, next) it removes and (last, new) it creates are ours
+    const uint32_t upto = len >= pos ? (len - pos + 1 >= 18 ? 0x3FFFFu : (1u << (len - pos + 1)) - 1u) : 0u;
+    const bool any = __syncthreads_or((valid & upto) != 0);
+    *prev_out = stile[padded(len - 1)];
+    uint32_t tile_kept;
+    if (!any) {
+        emit_plain(p, stile, carry, 0, 0, E, len, tout, tid);
+        tile_kept = len - carry;
+    } else {
+        const uint32_t excl = tile_scan(thread_summary(valid, pos, len), lane, warp, sh.wsum, &sh.tilesum);
+        const uint32_t tile = sh.tilesum;
+        uint32_t mprev;
+        const uint32_t mm = run_flags(valid, excl, carry, &mprev);
+        const uint32_t e = carry ? (excl >> 17) : ((excl >> 2) & 0x7FFFu);
+        tile_kept = carry ? (tile >> 17) : ((tile >> 2) & 0x7FFFu);
+        emit_full(p, stile, dkey, dval, &sh.docc, mm, mprev, e, tile_kept, 0, pos, len, E, op.new_id, tout, tid);
+    }
+    __syncthreads();
+    return tile_kept;
+}
+
+// A merge compacts the stream back into full tiles (its output at global
+// offsets) when the live symbols fill less than 70% of the tiles in use, so
+// the work per merge follows the live symbols, not the tiles.  Both merge
+// kernels evaluate this on the same stored values.
+__device__ __forceinline__ bool gap_pack(const TrainParams &p, uint32_t k, uint32_t active) {
+    const unsigned long long nk = __ldcg(p.nhist + k);
+    return nk * 10 < (unsigned long long)active * kMergeTile * 7;
+}
+
+// The summary pass, for merges that need it (l == r, or compacting): each
+// tile's summary (the transducer over its live symbols); the last CTA scans
+// them into each tile's entering merge flag and output offset, the new stream
+// length and, for a compacting merge, the new number of tiles in use.
+__global__ void __launch_bounds__(kMergeThreads) k_gsum(TrainParams p, uint32_t it) {
+    extern __shared__ uint32_t dsm[];
+    __shared__ MergeShared sh;
+    __shared__ uint32_t s_tilesum;
+    MergeOp op;
+    if (!merge_op(p, it, &op)) return;
+    const uint32_t Ta = __ldcg(&p.st->gactive[op.k & 1]);
+    const bool pack = gap_pack(p, op.k, Ta);
+    if (op.l != op.r && !pack) return;
+    const uint32_t T = p.gtiles, t = blockIdx.x;
+    const uint32_t *lin = (op.k & 1) ? p.glen[1] : p.glen[0];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t len = t < Ta ? __ldcg(lin + t) : 0u;
+    uint32_t ts = kSumId;
+    if (len) {
+        __shared__ GapHalo s_h;
+        if (tid == 0) gap_halo(op.in, lin, Ta, t, &s_h);
+        __syncthreads();
+        const GapHalo h = s_h;
+        uint32_t *stile = dsm;
+        stage_gapped_padded(stile, op.in + (uint64_t)t * kMergeTile, len, h);
+        const uint32_t E = len + h.nnext;
+        const uint64_t pos = (uint64_t)kMergeItems * tid;
+        const uint32_t valid = staged_valid(stile + padded(kMergeItems * tid), pos, E, op.l, op.r);
+        tile_scan(thread_summary(valid, pos, len), lane, warp, sh.wsum, &s_tilesum);
+        ts = s_tilesum;
+    }
+    if (tid == 0) p.gsum[t] = ts;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) sh.last = atomicAdd(&p.st->msum_done, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!sh.last) return;
+    __threadfence();
+    // scan the tile summaries: thread t takes tiles [t*per, (t+1)*per)
+    const uint32_t per = (T + kMergeThreads - 1) / kMergeThreads;
+    const uint32_t b0 = tid * per < T ? tid * per : T, b1 = b0 + per < T ? b0 + per : T;
+    unsigned long long mine = kFId;
+    for (uint32_t b = b0; b < b1; b++) mine = lsum_comp(lsum_from_sum(__ldcg(p.gsum + b)), mine);
+    const unsigned long long ex = block_excl_lsum(mine, sh);
+    uint32_t carry = fapply((uint32_t)ex & 3u, 0u);
+    unsigned long long off = (ex >> 2) & 0x7FFFFFFFull;
+    for (uint32_t b = b0; b < b1; b++) {
+        p.gcarry[b] = carry;
+        p.goff[b] = off;
+        const uint32_t sb = __ldcg(p.gsum + b);
+        off += carry ? (sb >> 17) : ((sb >> 2) & 0x7FFFu);
+        carry = fapply(sb & 3u, carry);
+    }
+    if (b0 < b1 && b1 == T) {
+        p.st->n[(op.k + 1) & 1] = off;
+        p.nhist[op.k + 1] = off;
+        p.st->gactive[(op.k + 1) & 1] = pack ? (uint32_t)((off + kMergeTile - 1) / kMergeTile) : Ta;
+    }
+    if (tid == 0) p.st->msum_done = 0;
+}
+
+// One merge over the gapped tiles: CTA b compacts its contiguous range of
+// tiles, each into its twin in the other buffer.  The range's live counts are
+// read once; the symbol before a tile carries over from the tile before it,
+// and the (up to 3) symbols after it are read with the tile itself.
+constexpr int kGapMaxRange = 1024;   // tiles per CTA range (T / grid is far below)
+
+__global__ void __launch_bounds__(kMergeThreads, 4) k_gmerge(TrainParams p, uint32_t it) {
+    extern __shared__ uint32_t dsm[];
+    uint32_t *sdat = dsm;                         // staged tile (linear) or, for l == r, the padded tile
+    uint32_t *sout = dsm + kGapStage;             // l != r: survivors in order
+    uint32_t *dkey = dsm + kGapStage + kMergeTile;
+    uint32_t *dval = dkey + kDeltaSlots;
+    __shared__ MergeShared sh;
+    __shared__ GapHalo s_h;
+    __shared__ uint32_t s_len[kGapMaxRange + 1];
+    MergeOp op;
+    if (!merge_op(p, it, &op)) return;
+    const uint32_t T = __ldcg(&p.st->gactive[op.k & 1]);   // tiles in use (those after hold nothing)
+    const bool pack = gap_pack(p, op.k, T);                 // compacting merge: the summary pass ran
+    const bool distinct = op.l != op.r;
+    const uint32_t *lin = (op.k & 1) ? p.glen[1] : p.glen[0];
+    uint32_t *lout = (op.k & 1) ? p.glen[0] : p.glen[1];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (blockIdx.x == 0 && tid == 0) {
+        if (distinct) {   // every occurrence of (l, r) merges: its count ends at 0
+            const uint32_t cnt = (uint32_t)(__ldcg(p.best + op.k) >> 32);
+            global_add(table_of(p), pair_key(op.l, op.r), 0u - cnt);
+            if (!pack) {   // the stream loses cnt symbols (a compacting merge's pass wrote the length)
+                const unsigned long long nn = __ldcg(p.nhist + op.k) - cnt;
+                p.st->n[(op.k + 1) & 1] = nn;
+                p.nhist[op.k + 1] = nn;
+            }
+        }
+        if (!pack) p.st->gactive[(op.k + 1) & 1] = T;
+    }
+    // a compacting merge leaves full tiles: the first n' / 4096 hold 4,096 symbols
+    const unsigned long long n_new = pack ? __ldcg(p.nhist + op.k + 1) : 0ull;
+    uint64_t t0, t1;
+    tile_range(T, &t0, &t1);
+    if (t0 >= t1) return;
+    const uint32_t nt = (uint32_t)(t1 - t0);
+    for (uint32_t i = tid; i <= nt; i += kMergeThreads) s_len[i] = (t0 + i < T) ? __ldcg(lin + t0 + i) : 0u;
+    if (tid == 0) {
+        sh.docc = 0;
+        gap_halo(op.in, lin, T, (uint32_t)t0, &s_h);   // the symbol before the range
+    }
+    if (pack)   // the new live counts of this range's tiles
+        for (uint32_t i = tid; i < (uint32_t)(t1 - t0); i += kMergeThreads) {
+            const unsigned long long b = (t0 + i) * (unsigned long long)kMergeTile;
+            lout[t0 + i] = b >= n_new ? 0u : (n_new - b < kMergeTile ? (uint32_t)(n_new - b) : (uint32_t)kMergeTile);
+        }
+    for (int j = tid; j < kDeltaSlots; j += kMergeThreads) {
+        dkey[j] = kEmptyKey;
+        dval[j] = 0;
+    }
+    __syncthreads();
+    uint32_t prev = s_h.prev, has_prev = s_h.has_prev;
+    for (uint32_t i = 0; i < nt; i++) {
+        const uint32_t t = (uint32_t)t0 + i, len = s_len[i];
+        // gapped: into the twin tile; compacting: at the tile's global offset
+        uint32_t *tout = op.out + (pack ? __ldcg(p.goff + t) : (uint64_t)t * kMergeTile);
+        if (len == 0) {
+            if (tid == 0 && !pack) lout[t] = 0;
+            continue;
+        }
+        const uint32_t *tin = op.in + (uint64_t)t * kMergeTile;
+        const uint32_t ln = s_len[i + 1];
+        uint32_t tile_kept;
+        if (distinct) {
+            // stage the live symbols exactly (the last quad element by element),
+            // while thread 0 writes the symbols around the tile
+            constexpr int kQuads = kMergeTile / 4 / kMergeThreads;   // 16-byte loads per thread
+            uint4 v[kQuads];
+#pragma unroll
+            for (int u = 0; u < kQuads; u++) {   // all loads in flight before the first store
+                const uint32_t i4 = tid + u * kMergeThreads;
+                v[u] = 4 * i4 < len ? __ldcg(reinterpret_cast<const uint4 *>(tin) + i4) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kQuads; u++) {
+                const uint32_t i4 = tid + u * kMergeThreads;
+                if (4 * i4 + 4 <= len) {
+                    *reinterpret_cast<uint4 *>(sdat + 4 + 4 * i4) = v[u];
+                } else if (4 * i4 < len) {
+                    const uint32_t e4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                    for (uint32_t j = 0; j < 4; j++)
+                        if (4 * i4 + j < len) sdat[4 + 4 * i4 + j] = e4[j];
+                }
+            }
+            if (tid == 0) {
+                uint32_t nx[3] = {0, 0, 0}, nn = 0;
+                if (t + 1 < T && ln >= 3) {   // the next tile holds the three symbols after this one
+                    const uint32_t *q = op.in + (uint64_t)(t + 1) * kMergeTile;
+                    nx[0] = __ldcg(q);
+                    nx[1] = __ldcg(q + 1);
+                    nx[2] = __ldcg(q + 2);
+                    nn = 3;
+                } else {
+                    GapHalo w;
+                    gap_halo(op.in, lin, T, t, &w);
+                    nn = w.nnext;
+                    for (int j = 0; j < 3; j++) nx[j] = w.nx[j];
+                }
+                sdat[3] = prev;
+                for (uint32_t j = 0; j < 3; j++) sdat[4 + len + j] = nx[j];
+                s_h.nnext = nn;
+                s_h.has_prev = has_prev;
+            }
+            __syncthreads();
+            const uint32_t E = len + s_h.nnext;
+            const bool hp = s_h.has_prev != 0;
+            prev = sdat[4 + len - 1];
+            tile_kept = gap_tile_distinct(p, op, sdat, len, E, hp, sout, tout, sh.wsum, dkey, dval, &sh.docc, lane,
+                                          warp);
+        } else {
+            if (tid == 0) {
+                GapHalo h;
+                h.prev = prev;
+                h.has_prev = has_prev;
+                if (t + 1 < T && ln >= 3) {
+                    const uint32_t *q = op.in + (uint64_t)(t + 1) * kMergeTile;
+                    h.nx[0] = __ldcg(q);
+                    h.nx[1] = __ldcg(q + 1);
+                    h.nx[2] = __ldcg(q + 2);
+                    h.nnext = 3;
+                } else {
+                    GapHalo w;
+                    gap_halo(op.in, lin, T, t, &w);
+                    h.nnext = w.nnext;
+                    for (int j = 0; j < 3; j++) h.nx[j] = w.nx[j];
+                }
+                s_h = h;
+            }
+            __syncthreads();
+            const GapHalo h = s_h;
+            tile_kept = gap_tile_runs(p, op, tin, tout, len, h, __ldcg(p.gcarry + t), sdat, dkey, dval, sh, &prev);
+        }
+        has_prev = 1;
+        if (tid == 0 && !pack) lout[t] = tile_kept;
+    }
+    __syncthreads();
+    flush_deltas(p, dkey, dval, &sh.docc);
+}
+
+// Live symbols per tile at the start: the contiguous input.
+__global__ void k_ginit(uint32_t *len0, uint32_t T, unsigned long long n) {
+    const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < T) {
+        const unsigned long long b = (unsigned long long)t * kMergeTile;
+        len0[t] = n - b < (unsigned long long)kMergeTile ? (uint32_t)(n - b) : (uint32_t)kMergeTile;
+    }
+}
+
+// Exclusive scan of the tiles' live counts (one CTA).
+__global__ void __launch_bounds__(1024) k_gscan(const uint32_t *len, uint32_t T, unsigned long long *off) {
+    __shared__ unsigned long long s_w[32];
+    __shared__ unsigned long long s_carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s_carry = 0;
+    __syncthreads();
+    for (uint32_t base = 0; base < T; base += 1024) {
+        const uint32_t t = base + tid;
+        const unsigned long long v = t < T ? len[t] : 0ull;
+        unsigned long long x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_w[warp] = x;
+        __syncthreads();
+        unsigned long long wpre = 0, tot = 0;
+        for (int w = 0; w < 32; w++) {
+            if (w < warp) wpre += s_w[w];
+            tot += s_w[w];
+        }
+        if (t < T) off[t] = s_carry + wpre + x - v;
+        __syncthreads();
+        if (tid == 0) s_carry += tot;
+        __syncthreads();
+    }
+}
+
+// The contiguous stream: tile t's live symbols to out + off[t].
+__global__ void k_gcopy(const uint32_t *buf, const uint32_t *len, const unsigned long long *off, uint32_t *out) {
+    const uint32_t t = blockIdx.x, l = len[t];
+    const uint32_t *src = buf + (uint64_t)t * kMergeTile;
+    for (uint32_t i = threadIdx.x; i < l; i += blockDim.x) out[off[t] + i] = src[i];
+}
+
 __global__ void k_advance(TrainState *st, uint32_t by) { st->k_base += by; }
 
 uint32_t ceil_log2(uint64_t x) {
@@ -1305,9 +1755,13 @@ uint32_t ceil_log2(uint64_t x) {
 struct Launch {
     TrainParams p;
     unsigned count_grid, merge_grid, argmax_grid;
-    size_t count_smem, merge_smem;
-    bool lookback;   // single pass with decoupled look-back, else two passes
+    size_t count_smem, merge_smem, gmerge_smem, gsum_smem;
+    unsigned gmerge_grid;
+    int mode;   // BPE_MERGE_TWO_PASS, BPE_MERGE_LOOKBACK or BPE_MERGE_TILES
 };
+
+constexpr size_t kGmergeSmem = (size_t)(kGapStage + kMergeTile + 2 * kDeltaSlots) * sizeof(uint32_t);
+constexpr size_t kGsumSmem = (size_t)kTileWords * sizeof(uint32_t);
 
 int occupancy(bpe_ctx *ctx, int *count_blocks, int *merge_blocks) {
     const size_t csm = 2 * kCountSlots * sizeof(uint32_t),
@@ -1318,6 +1772,10 @@ int occupancy(bpe_ctx *ctx, int *count_blocks, int *merge_blocks) {
              "k_merge smem attribute");
     BPE_CUDA(ctx, cudaFuncSetAttribute(k_mapply, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msm),
              "k_mapply smem attribute");
+    BPE_CUDA(ctx, cudaFuncSetAttribute(k_gmerge, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGmergeSmem),
+             "k_gmerge smem attribute");
+    BPE_CUDA(ctx, cudaFuncSetAttribute(k_gsum, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGsumSmem),
+             "k_gsum smem attribute");
     BPE_CUDA(ctx, cudaOccupancyMaxActiveBlocksPerMultiprocessor(count_blocks, k_count, kCountThreads, csm),
              "k_count occupancy");
     BPE_CUDA(ctx, cudaOccupancyMaxActiveBlocksPerMultiprocessor(merge_blocks, k_mapply, kMergeThreads, msm),
@@ -1328,7 +1786,10 @@ int occupancy(bpe_ctx *ctx, int *count_blocks, int *merge_blocks) {
 }
 
 void launch_merge(const Launch &L, uint32_t it, cudaStream_t s) {
-    if (L.lookback) {
+    if (L.mode == BPE_MERGE_TILES) {
+        k_gsum<<<L.p.gtiles, kMergeThreads, L.gsum_smem, s>>>(L.p, it);   // returns at once unless l == r
+        k_gmerge<<<L.gmerge_grid, kMergeThreads, L.gmerge_smem, s>>>(L.p, it);
+    } else if (L.mode == BPE_MERGE_LOOKBACK) {
         k_merge<<<L.merge_grid, kMergeThreads, L.merge_smem, s>>>(L.p, it);
     } else {
         k_msum<<<L.merge_grid, kMergeThreads, 0, s>>>(L.p, it);
@@ -1348,7 +1809,9 @@ int get_graph(bpe_ctx *ctx, const Launch &L, cudaGraphExec_t *out) {
         (uintptr_t)L.p.dkey, (uintptr_t)L.p.dcnt, (uintptr_t)L.p.dcap, (uintptr_t)L.p.status[0],
         (uintptr_t)L.p.status[1], (uintptr_t)L.p.rsum, (uintptr_t)L.p.rpre, (uintptr_t)L.p.best,
         (uintptr_t)L.p.nhist, (uintptr_t)L.p.dhist, (uintptr_t)L.p.st, (uintptr_t)L.merge_grid,
-        (uintptr_t)L.argmax_grid, (uintptr_t)L.lookback};
+        (uintptr_t)L.argmax_grid, (uintptr_t)L.mode, (uintptr_t)L.p.glen[0], (uintptr_t)L.p.glen[1],
+        (uintptr_t)L.p.gsum, (uintptr_t)L.p.gcarry, (uintptr_t)L.p.goff, (uintptr_t)L.p.gtiles,
+        (uintptr_t)L.gmerge_grid};
     if (ctx->graph.exec && ctx->graph.key == key) {
         *out = ctx->graph.exec;
         return BPE_OK;
@@ -1392,14 +1855,15 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
         return rc;
     int cb, mb;
     if ((rc = occupancy(ctx, &cb, &mb))) return rc;
-    const bool lookback = ctx->merge_lookback != 0;
+    const int mode = ctx->merge_mode;
+    const bool lookback = mode == BPE_MERGE_LOOKBACK, gapped = mode == BPE_MERGE_TILES;
     const bool profile = ctx->profile != 0;
     const bool graph = ctx->use_graph && !profile;
     // merge windows replay from CUDA graphs, or (BPE_OPT_PERSISTENT, two-pass
     // merge only) from one persistent cooperative launch per window
     int coop = 0, pb = 0;
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, ctx->device);
-    const bool persistent = ctx->persistent && graph && !lookback && coop;
+    const bool persistent = ctx->persistent && graph && mode == BPE_MERGE_TWO_PASS && coop;
     if (persistent) {
         const size_t msm = (kTileWords + 2 * kDeltaSlots) * sizeof(uint32_t);
         BPE_CUDA(ctx, cudaFuncSetAttribute(k_train_loop, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msm),
@@ -1414,7 +1878,7 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
         persistent ? std::min<uint64_t>((uint64_t)ctx->sm_count * pb, std::max<uint64_t>(ntiles, ctx->sm_count))
                    : std::max<uint64_t>(1, std::min<uint64_t>(ntiles, (uint64_t)ctx->sm_count * mb));
     void *ranges;
-    if ((rc = ensure(ctx, S_LIST1, range_grid * 16, &ranges))) return rc;
+    if ((rc = ensure(ctx, S_LIST1, range_grid * 16 + ntiles * 8, &ranges))) return rc;   // ranges, then tile offsets
     uint32_t *dkey = (uint32_t *)dense, *dcnt = dkey + T;   // dense keys, then dense counts
     const uint32_t G = persistent ? kLoopIters : kGraphIters;
     void *pin;
@@ -1432,6 +1896,7 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     memset(h_state, 0, sizeof *h_state);
     h_state->n_merges = n_merges;
     h_state->n[0] = n;
+    h_state->gactive[0] = (uint32_t)ntiles;
     h_nhist[0] = n;
     BPE_CUDA(ctx, cudaMemcpyAsync(state, h_state, sizeof *h_state, cudaMemcpyHostToDevice, s), "state upload");
     BPE_CUDA(ctx, cudaMemcpyAsync(nhist, h_nhist, 8, cudaMemcpyHostToDevice, s), "nhist upload");
@@ -1443,7 +1908,24 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     BPE_CUDA(ctx, cudaMemcpyAsync(buf0, d_symbols, n * 4, cudaMemcpyDeviceToDevice, s), "input copy");
 
     Launch L;
-    L.lookback = lookback;
+    L.mode = mode;
+    // gapped tiles: live counts by parity (st0), l == r summaries and flags (st1)
+    L.p.glen[0] = (uint32_t *)st0;
+    L.p.glen[1] = (uint32_t *)st0 + ntiles;
+    L.p.gsum = (uint32_t *)st1;
+    L.p.gcarry = (uint32_t *)st1 + ntiles;
+    L.p.goff = (unsigned long long *)ranges + 2 * range_grid;
+    L.p.gtiles = (uint32_t)ntiles;
+    L.gmerge_smem = kGmergeSmem;
+    L.gsum_smem = kGsumSmem;
+    {   // one range of tiles per CTA, every CTA resident
+        int gb = 1;
+        BPE_CUDA(ctx, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&gb, k_gmerge, kMergeThreads, kGmergeSmem),
+                 "k_gmerge occupancy");
+        uint64_t g = std::min<uint64_t>(ntiles, (uint64_t)ctx->sm_count * std::max(gb, 1));
+        g = std::max<uint64_t>(g, (ntiles + kGapMaxRange - 1) / kGapMaxRange);
+        L.gmerge_grid = (unsigned)std::max<uint64_t>(1, g);
+    }
     L.p.rsum = (unsigned long long *)ranges;
     L.p.rpre = L.p.rsum + range_grid;
     L.p.buf[0] = (uint32_t *)buf0;
@@ -1475,6 +1957,7 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
 
     cudaGraphExec_t exec = nullptr;
     if (graph && !persistent && (rc = get_graph(ctx, L, &exec))) return rc;
+    if (gapped) k_ginit<<<(unsigned)((ntiles + 255) / 256), 256, 0, s>>>(L.p.glen[0], (uint32_t)ntiles, n);
     if (profile) BPE_CUDA(ctx, cudaEventRecord(ctx->events[0], s), "event");
     k_count<<<L.count_grid, kCountThreads, L.count_smem, s>>>(L.p);
     if (profile) BPE_CUDA(ctx, cudaEventRecord(ctx->events[1], s), "event");
@@ -1542,8 +2025,17 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     const uint64_t nf = h_nhist[done];
     if (n_final) *n_final = nf;
     if (d_symbols_final) {
-        BPE_CUDA(ctx, cudaMemcpyAsync(d_symbols_final, L.p.buf[done & 1], nf * 4, cudaMemcpyDeviceToDevice, s),
-                 "final copy");
+        if (gapped) {   // gather the tiles' live symbols
+            void *goff;
+            if ((rc = ensure(ctx, S_W_OUTOFF, ntiles * 8, &goff))) return rc;
+            k_gscan<<<1, 1024, 0, s>>>(L.p.glen[done & 1], (uint32_t)ntiles, (unsigned long long *)goff);
+            k_gcopy<<<(unsigned)ntiles, 256, 0, s>>>(L.p.buf[done & 1], L.p.glen[done & 1],
+                                                      (const unsigned long long *)goff, d_symbols_final);
+            BPE_CUDA(ctx, cudaGetLastError(), "gather launch");
+        } else {
+            BPE_CUDA(ctx, cudaMemcpyAsync(d_symbols_final, L.p.buf[done & 1], nf * 4, cudaMemcpyDeviceToDevice, s),
+                     "final copy");
+        }
         BPE_CUDA(ctx, cudaStreamSynchronize(s), "final sync");
     }
 
@@ -1551,8 +2043,8 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     stats_reset(ctx);
     const uint64_t per_merge = lookback ? 2 : 3;
     ctx->stats.kernel_launches =
-        1 + (persistent ? (uint64_t)window
-                        : graph ? (uint64_t)window * (per_merge * kGraphIters + 1) : per_merge * launched);
+        1 + (gapped ? 1 : 0) + (d_symbols_final && gapped ? 2 : 0) +
+        (persistent ? (uint64_t)window : graph ? (uint64_t)window * (per_merge * kGraphIters + 1) : per_merge * launched);
     const int sc = stats_slot(ctx, "pair_count"), sa = stats_slot(ctx, "argmax"), sm = stats_slot(ctx, "merge_compact");
     ctx->stats.k[sc].launches = 1;
     ctx->stats.k[sc].bytes = 4.0 * (double)n;

@@ -89,12 +89,20 @@ const char *bpe_last_error(const bpe_ctx *ctx);
  *                        (the same merges and final stream: no count or merge
  *                        crosses a WORD_START); 0 = over the full symbol
  *                        stream (default)
- *   BPE_OPT_MERGE_LOOKBACK  full-stream merge and compaction: 1 = one pass,
- *                        tiles finding their output offsets by decoupled
- *                        look-back; 0 = two passes, range summaries then
- *                        apply (default; no CTA waits on another).  Both
- *                        give the same results.
- *   BPE_OPT_PERSISTENT   1 = the two-pass merge loop runs as one cooperative
+ *   BPE_OPT_MERGE        full-stream merge and compaction (all give the same
+ *                        results):
+ *                        BPE_MERGE_TWO_PASS (default): per merge, range
+ *                          summaries (the last CTA scans them into offsets),
+ *                          then each range merges and compacts; no CTA waits
+ *                          on another
+ *                        BPE_MERGE_LOOKBACK: one pass, each tile finding its
+ *                          output offset by decoupled look-back
+ *                        BPE_MERGE_TILES: the stream is kept as 4,096-slot
+ *                          tiles with a live count each; a merge compacts
+ *                          every tile into its twin in the other buffer (no
+ *                          global offsets), compacting into full tiles when
+ *                          they fall below 70% full; gathered at the end
+ *   BPE_OPT_PERSISTENT   1 = with BPE_MERGE_TWO_PASS, the merge loop runs as one cooperative
  *                        launch per window of merges (all CTAs resident,
  *                        phases separated by grid barriers) instead of a CUDA
  *                        graph of per-phase kernels; default 0 */
@@ -104,9 +112,10 @@ enum {
     BPE_OPT_PROFILE = 3,
     BPE_OPT_CHUNK = 4,
     BPE_OPT_TRAIN_WORDS = 5,
-    BPE_OPT_MERGE_LOOKBACK = 6,
+    BPE_OPT_MERGE = 6,
     BPE_OPT_PERSISTENT = 7
 };
+enum { BPE_MERGE_TWO_PASS = 0, BPE_MERGE_LOOKBACK = 1, BPE_MERGE_TILES = 2 };
 int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value);
 
 /* Statistics of the last bpe_train or trie_encode call on this context.

@@ -121,14 +121,16 @@ def test_train_identical_runs_cross_tiles(ctx, n):
     check_train(ctx, oracle.pretokenize(text), 12)
 
 
-@pytest.mark.parametrize("mode", ["lookback", "persistent"])
-@pytest.mark.parametrize("case", ["runs", "random", "tiny"])
+@pytest.mark.parametrize("mode", ["lookback", "tiles", "persistent"])
+@pytest.mark.parametrize("case", ["runs", "random", "tiny", "med"])
 def test_train_merge_variants_agree(ctx, golden, case, mode):
-    # the single-pass merge (decoupled look-back) and the persistent two-pass
-    # loop give the same merges and stream
+    # the single-pass merge (decoupled look-back), the gapped-tile merge and
+    # the persistent two-pass loop give the same merges and stream as the
+    # default two-pass merge
     import bpe_trie_encode_gb300 as bt
-    opt = bt.BPE_OPT_MERGE_LOOKBACK if mode == "lookback" else bt.BPE_OPT_PERSISTENT
-    ctx.set_option(opt, 1)
+    ctx.set_option(bt.BPE_OPT_MERGE, {"lookback": bt.BPE_MERGE_LOOKBACK, "tiles": bt.BPE_MERGE_TILES,
+                                      "persistent": bt.BPE_MERGE_TWO_PASS}[mode])
+    ctx.set_option(bt.BPE_OPT_PERSISTENT, 1 if mode == "persistent" else 0)
     try:
         if case == "runs":
             text = b"a" * 1_000_001 + b" " + b"a" * 4097 + b".bb" + b"b" * 4097
@@ -137,12 +139,21 @@ def test_train_merge_variants_agree(ctx, golden, case, mode):
             for seed in range(4):
                 rng = random.Random(100 + seed)
                 check_train(ctx, oracle.pretokenize(rand_bytes(rng, 9000 + 4096 * seed, b"aab c.")), 60)
-        else:
+        elif case == "tiny":
             m, f = ctx.train(dev_sym(oracle.pretokenize(synth.corpus("tiny"))), 256)
             assert sha(m.astype(np.uint32)) == golden["tiny"]["merges_sha256"]
             assert sha(host_u32(f)) == golden["tiny"]["final_sha256"]
+        else:   # the medium workload with checkpoints: streams after 1, 100 and 1,000 merges
+            g = golden["med"]
+            sym = ctx.pretokenize(dev_u8(synth.corpus("med")))
+            m, f = ctx.train(sym, g["n_merges"])
+            assert sha(m.astype(np.uint32)) == g["merges_sha256"] and sha(host_u32(f)) == g["final_sha256"]
+            for k in (1, 100, 1000):
+                _, fk = ctx.train(sym, k)
+                assert sha(host_u32(fk)) == g["checkpoints"][str(k)]["sha256"], k
     finally:
-        ctx.set_option(opt, 0)
+        ctx.set_option(bt.BPE_OPT_MERGE, bt.BPE_MERGE_TWO_PASS)
+        ctx.set_option(bt.BPE_OPT_PERSISTENT, 0)
 
 
 def test_train_alternating_and_ties(ctx):
