@@ -186,6 +186,46 @@ class Context:
         return ids_out[: n_ids.value], id_off[: n_docs + 1]
 
 
+class Stream:
+    """Streaming encode of one document arriving in slices (trie_stream_*):
+    push() returns the ids that no later byte can change; the last push
+    returns the rest.  The ids of all pushes, concatenated, equal
+    Context.encode on the whole document."""
+
+    def __init__(self, ctx: "Context", trie: Trie):
+        self.ctx, self.trie = ctx, trie
+        self._h = ctypes.c_void_p()
+        _capi.check(ctx._h, ctx.lib.trie_stream_open(ctx._h, trie._h, ctypes.byref(self._h)))
+
+    def push(self, data: torch.Tensor, last: bool = False, ids_out: torch.Tensor | None = None) -> torch.Tensor:
+        data = _need_cuda(data, torch.uint8, "data", self.ctx.device)
+        cap = data.numel() + self.trie.info()["max_token_len"] + 16   # one id per carried or new byte
+        if ids_out is None:
+            ids_out = torch.empty(cap, dtype=torch.int32, device=self.ctx.device)
+        else:
+            ids_out = _need_cuda(ids_out, torch.int32, "ids_out", self.ctx.device)
+        n_ids = ctypes.c_uint64(0)
+        ptr = data.data_ptr() if data.numel() else 0
+        self.ctx._sync_stream()
+        rc = self.ctx.lib.trie_stream_push(self._h, ctypes.c_void_p(ptr), data.numel(), 1 if last else 0,
+                                           ctypes.c_void_p(ids_out.data_ptr()), ids_out.numel(), ctypes.byref(n_ids))
+        if rc == -6:
+            raise BpeError(rc, f"{n_ids.value} ids needed, capacity {ids_out.numel()}")
+        _capi.check(self.ctx._h, rc)
+        return ids_out[: n_ids.value]
+
+    def close(self):
+        if self._h:
+            self.ctx.lib.trie_stream_close(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def vocab_from_merges(merges):
     """Token byte strings of ids 0 .. 255 + len(merges) (host bookkeeping for
     trie_build): bytes(b) = [b], bytes(256 + k) = bytes(left) + bytes(right).

@@ -127,6 +127,30 @@ __device__ __forceinline__ Match match_at(const EncParams &P, const int4 *lut, u
     return m;
 }
 
+// The longest token prefixing bytes[p, end) when that match is final: false
+// when the trie walk ran into end with children still possible (more bytes
+// could make the match longer).
+__device__ __forceinline__ bool match_final(const EncParams &P, const int4 *lut, uint64_t p, uint64_t end,
+                                            uint32_t *len) {
+    const int4 r = lut[__ldg(P.bytes + p)];
+    int32_t node = r.x;
+    uint32_t y = (uint32_t)r.y;
+    *len = 1u;
+    uint64_t q = p + 1;
+    for (;;) {
+        const uint32_t base = y & ~kTermBit;
+        if (base == 0) return true;                 // no children: final
+        if (q >= end) return false;                 // the next byte decides
+        const int32_t t = (int32_t)(base + __ldg(P.bytes + q));
+        const int2 v = __ldg(P.slot + t);
+        if (v.x != node) return true;               // mismatch: final
+        node = t;
+        y = (uint32_t)v.y;
+        ++q;
+        if (y & kTermBit) *len = (uint32_t)(q - p);
+    }
+}
+
 __device__ __forceinline__ void load_lut(const EncParams &P, int4 *lut) {
     for (int c = threadIdx.x; c < 256; c += blockDim.x) lut[c] = P.root[c];
 }
@@ -671,6 +695,42 @@ __global__ void k_doc_offsets(EncParams P, unsigned long long n_chunks) {
     P.id_off[d] = c < n_chunks ? P.prefix[c] : P.st->total;
 }
 
+// Streaming ([GPU-BPE] "Host architecture", 3. multi-pass slicing, with the
+// parse carried across slices): the prefix of one document's parse [0, end)
+// that no later byte can change.  A token starting max_len or more bytes
+// before the end is final (its walk stops within max_len bytes); from the
+// last chunk exit at or before end - max_len the tokens are walked again
+// until the first whose walk reached the end.  out[0]: number of final ids;
+// out[1]: position of the first token that is not final (end if none).
+__global__ void k_stream_cut(EncParams P, unsigned long long n_chunks, uint64_t end, uint32_t max_len,
+                             unsigned long long *out) {
+    __shared__ int4 lut[256];
+    load_lut(P, lut);
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    const uint64_t safe = end > max_len ? end - max_len : 0;
+    long long lo = -1, hi = (long long)n_chunks;   // last chunk c with exit(c) <= safe
+    while (hi - lo > 1) {
+        const long long mid = (lo + hi) / 2;
+        if ((uint64_t)mid * P.chunk + P.exit_rel[mid] <= safe) lo = mid;
+        else hi = mid;
+    }
+    uint64_t b = 0;
+    unsigned long long ids = 0;
+    if (lo >= 0) {
+        b = (uint64_t)lo * P.chunk + P.exit_rel[lo];
+        ids = P.prefix[lo] + P.count[lo];
+    }
+    while (b < end) {
+        uint32_t len;
+        if (!match_final(P, lut, b, end, &len)) break;
+        b += len;
+        ++ids;
+    }
+    out[0] = ids;
+    out[1] = b;
+}
+
 }  // namespace
 }  // namespace bpe
 
@@ -820,6 +880,126 @@ extern "C" int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_
     if (total > ids_capacity)
         return fail(ctx, BPE_ERR_CAPACITY, "trie_encode: %llu ids exceed the capacity %llu",
                     (unsigned long long)total, (unsigned long long)ids_capacity);
+    return BPE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Streaming encode of one document arriving in slices.  Each push encodes the
+// carried bytes followed by the new slice as one document, hands back the ids
+// no later byte can change and carries the bytes of the rest (fewer than the
+// longest token) to the next push; the last push makes everything final.
+
+struct bpe_stream {
+    bpe_ctx *ctx = nullptr;
+    const bpe_trie *trie = nullptr;
+    uint8_t *d_buf = nullptr;          // carried bytes, then the slice
+    size_t cap = 0;
+    uint8_t *d_carry = nullptr;        // the carried bytes between pushes
+    uint32_t carry = 0;
+    uint64_t *d_off = nullptr;         // {0, total}: the one document
+    unsigned long long *d_cut = nullptr;
+    unsigned long long *h_cut = nullptr;   // pinned: final ids, cut position; then {0, total}
+};
+
+extern "C" int trie_stream_open(bpe_ctx *ctx, const bpe_trie *trie, bpe_stream **out) {
+    if (!ctx || !trie || !out) return BPE_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (trie->device != ctx->device) return fail(ctx, BPE_ERR_INVALID_ARG, "trie_stream_open: trie on another device");
+    BPE_CUDA(ctx, cudaSetDevice(ctx->device), "cudaSetDevice");
+    bpe_stream *st = new bpe_stream();
+    st->ctx = ctx;
+    st->trie = trie;
+    cudaError_t e = cudaMalloc(&st->d_carry, (size_t)trie->max_len + 16);
+    if (e == cudaSuccess) e = cudaMalloc(&st->d_off, 2 * sizeof(uint64_t));
+    if (e == cudaSuccess) e = cudaMalloc(&st->d_cut, 2 * sizeof(unsigned long long));
+    if (e == cudaSuccess) e = cudaMallocHost(&st->h_cut, 4 * sizeof(unsigned long long));
+    if (e != cudaSuccess) {
+        trie_stream_close(st);
+        return cuda_fail(ctx, e, "trie_stream_open");
+    }
+    *out = st;
+    return BPE_OK;
+}
+
+extern "C" void trie_stream_close(bpe_stream *st) {
+    if (!st) return;
+    if (st->ctx) {
+        cudaSetDevice(st->ctx->device);
+        cudaStreamSynchronize(st->ctx->stream);
+    }
+    if (st->d_buf) cudaFree(st->d_buf);
+    if (st->d_carry) cudaFree(st->d_carry);
+    if (st->d_off) cudaFree(st->d_off);
+    if (st->d_cut) cudaFree(st->d_cut);
+    if (st->h_cut) cudaFreeHost(st->h_cut);
+    delete st;
+}
+
+extern "C" int trie_stream_push(bpe_stream *st, const uint8_t *d_bytes, uint64_t n, int last, int32_t *d_ids_out,
+                                uint64_t ids_capacity, uint64_t *n_ids) {
+    if (!st || !n_ids) return BPE_ERR_INVALID_ARG;
+    bpe_ctx *ctx = st->ctx;
+    *n_ids = 0;
+    if (n && !d_bytes) return fail(ctx, BPE_ERR_INVALID_ARG, "trie_stream_push: null bytes");
+    BPE_CUDA(ctx, cudaSetDevice(ctx->device), "cudaSetDevice");
+    cudaStream_t s = ctx->stream;
+    const uint64_t total = (uint64_t)st->carry + n;
+    if (st->cap < total + 16) {   // grow the staging buffer (x1.5, like the context's pool)
+        BPE_CUDA(ctx, cudaStreamSynchronize(s), "stream grow sync");
+        if (st->d_buf) cudaFree(st->d_buf);
+        st->d_buf = nullptr;
+        st->cap = 0;
+        const size_t want = (size_t)(total + total / 2 + 256);
+        BPE_CUDA(ctx, cudaMalloc(&st->d_buf, want), "trie_stream_push: staging buffer");
+        st->cap = want;
+    }
+    if (st->carry)
+        BPE_CUDA(ctx, cudaMemcpyAsync(st->d_buf, st->d_carry, st->carry, cudaMemcpyDeviceToDevice, s), "carry copy");
+    if (n) BPE_CUDA(ctx, cudaMemcpyAsync(st->d_buf + st->carry, d_bytes, n, cudaMemcpyDeviceToDevice, s), "slice copy");
+    if (total == 0) {
+        BPE_CUDA(ctx, cudaStreamSynchronize(s), "sync");
+        return BPE_OK;
+    }
+    BPE_CUDA(ctx, cudaStreamSynchronize(s), "stream sync");   // h_cut is reused below
+    st->h_cut[2] = 0;
+    st->h_cut[3] = total;
+    BPE_CUDA(ctx, cudaMemcpyAsync(st->d_off, st->h_cut + 2, 2 * sizeof(uint64_t), cudaMemcpyHostToDevice, s),
+             "offsets");
+    uint64_t all = 0;
+    int rc = trie_encode(ctx, st->trie, st->d_buf, st->d_off, 1, d_ids_out, ids_capacity, nullptr, &all);
+    if (rc) {
+        *n_ids = all;
+        return rc;
+    }
+    if (last) {
+        st->carry = 0;
+        *n_ids = all;
+        return BPE_OK;
+    }
+    // the final prefix of the parse: the chunk arrays of that encode are still in the pool
+    const uint32_t C = (uint32_t)std::min(ctx->chunk, kMaxChunk);
+    const unsigned long long nc = (total + C - 1) / C;
+    EncParams P{};
+    P.bytes = st->d_buf;
+    P.chunk = C;
+    P.slot = st->trie->d_slot;
+    P.tid = st->trie->d_tid;
+    P.root = st->trie->d_root;
+    P.count = (uint32_t *)ctx->scratch[S_ENC_CHUNK_INFO].p;
+    P.exit_rel = P.count + nc;
+    P.prefix = (unsigned long long *)ctx->scratch[S_ENC_PREFIX].p;
+    k_stream_cut<<<1, 256, 0, s>>>(P, nc, total, st->trie->max_len, st->d_cut);
+    BPE_CUDA(ctx, cudaGetLastError(), "k_stream_cut launch");
+    BPE_CUDA(ctx, cudaMemcpyAsync(st->h_cut, st->d_cut, 2 * sizeof(unsigned long long), cudaMemcpyDeviceToHost, s),
+             "cut read");
+    BPE_CUDA(ctx, cudaStreamSynchronize(s), "cut sync");
+    const uint64_t cut = st->h_cut[1];
+    st->carry = (uint32_t)(total - cut);   // below the longest token
+    if (st->carry)
+        BPE_CUDA(ctx, cudaMemcpyAsync(st->d_carry, st->d_buf + cut, st->carry, cudaMemcpyDeviceToDevice, s),
+                 "carry keep");
+    *n_ids = st->h_cut[0];
+    ctx->stats.kernel_launches += 1;
     return BPE_OK;
 }
 

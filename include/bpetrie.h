@@ -213,6 +213,27 @@ int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_bytes,
                 const uint64_t *d_doc_off, uint32_t n_docs, int32_t *d_ids_out,
                 uint64_t ids_capacity, uint64_t *d_id_off_out, uint64_t *n_ids);
 
+/* Streaming encode of one document that arrives in slices ([GPU-BPE] "Host
+ * architecture", 3. multi-pass slicing; the parse is carried across slices so
+ * the ids equal trie_encode's on the whole document).
+ *
+ * trie_stream_open: a stream bound to ctx (its device, stream and pool) and
+ * trie; both must outlive it.  trie_stream_push: encode the bytes carried from
+ * the previous push followed by d_bytes[0 .. n) (device), write the ids that
+ * no later byte can change to d_ids_out[0 .. *n_ids) and carry the rest of
+ * the bytes (fewer than the longest token) to the next push; with last != 0
+ * every id is final and the stream is ready for a new document.  The ids of
+ * the carried tail may also be written past *n_ids, so ids_capacity must
+ * hold one id per carried or new byte; when it does not, BPE_ERR_CAPACITY is
+ * returned with the required size in *n_ids and the carry is kept (the push
+ * can be repeated).  Blocks until done.  Errors: INVALID_ARG, CAPACITY, OOM,
+ * TIMEOUT, CUDA.  trie_stream_close releases the stream (NULL is ignored). */
+typedef struct bpe_stream bpe_stream;
+int trie_stream_open(bpe_ctx *ctx, const bpe_trie *trie, bpe_stream **out);
+int trie_stream_push(bpe_stream *stream, const uint8_t *d_bytes, uint64_t n, int last, int32_t *d_ids_out,
+                     uint64_t ids_capacity, uint64_t *n_ids);
+void trie_stream_close(bpe_stream *stream);
+
 /* Encoding that allocates nothing.  The pages have no counterpart: this entry
  * point exists for callers of the library that cannot allocate device memory,
  * for example a plug-in that receives only a stream and raw device pointers

@@ -346,6 +346,64 @@ def test_encode_repair_paths(ctx, n_docs, lengths, c_rate):
     check_encode(ctx, vb, off, parity_shift_docs(rng, n_docs, lengths, c_rate))
 
 
+def stream_encode(ctx, vb, off, text, cuts, trie=None):
+    import bpe_trie_encode_gb300 as bt
+    trie = trie or ctx.trie_build(vb, off)
+    st = bt.Stream(ctx, trie)
+    out = []
+    bounds = [0] + sorted(cuts) + [len(text)]
+    for i in range(len(bounds) - 1):
+        piece = text[bounds[i]:bounds[i + 1]]
+        d = dev_u8(piece) if piece else torch.empty(0, dtype=torch.uint8, device="cuda")
+        out.append(st.push(d, last=(i == len(bounds) - 2)).cpu().numpy())
+    st.close()
+    return np.concatenate(out) if out else np.zeros(0, np.int32)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_encode_stream_slices_equal_whole_document(ctx, seed):
+    # the ids of a document pushed in slices (empty, single-byte, shorter than
+    # the longest token, cutting tokens) equal the oracle's on the whole text
+    rng = random.Random(1000 + seed)
+    alpha = b"ab c" if seed % 2 else bytes(range(97, 103)) + b" ."
+    toks = [bytes([b]) for b in range(256)]
+    toks += [rand_bytes(rng, rng.randrange(2, 60), alpha) for _ in range(rng.randrange(50, 2000))]
+    vb, off = vocab_arrays(toks)
+    text = rand_bytes(rng, rng.choice([0, 1, 7, 3000, 70000]), alpha)
+    cuts = sorted(rng.randrange(0, len(text) + 1) for _ in range(rng.randrange(0, 40)))
+    cuts += [c for c in cuts[:3]]   # repeated cuts: empty slices
+    ids = stream_encode(ctx, vb, off, text, cuts)
+    want, _ = oracle.Trie(vb, off).encode(text, np.array([0, len(text)], dtype=np.uint64))
+    assert np.array_equal(ids, want)
+
+
+def test_encode_stream_long_tokens_and_reuse(ctx):
+    import bpe_trie_encode_gb300 as bt
+    toks = [bytes([b]) for b in range(256)] + [b"x" * 300, b"x" * 299 + b"y", b"xy" * 100, b"aa"]
+    vb, off = vocab_arrays(toks)
+    trie = ctx.trie_build(vb, off)
+    o = oracle.Trie(vb, off)
+    st = bt.Stream(ctx, trie)
+    for text, step in ((b"x" * 5000 + b"y" + b"xy" * 700, 7), (b"c" + b"a" * 2000, 5), (b"x" * 299, 1000)):
+        got = []
+        for i in range(0, len(text), step):   # slices far shorter than the longest token
+            got.append(st.push(dev_u8(text[i:i + step])).cpu().numpy())
+        got.append(st.push(torch.empty(0, dtype=torch.uint8, device="cuda"), last=True).cpu().numpy())
+        want, _ = o.encode(text, np.array([0, len(text)], dtype=np.uint64))
+        assert np.array_equal(np.concatenate(got), want)   # the stream is reused after each last push
+    st.close()
+
+
+def test_encode_stream_learned_vocab_megabytes(ctx, golden):
+    merges, _ = oracle.train_words(oracle.pretokenize(synth.corpus("tiny")), 256)
+    vb, off = oracle.vocab_from_merges(merges)
+    text = synth.corpus("med")[: 6 << 20].tobytes()
+    cuts = list(range(1 << 20, len(text), (1 << 20) + 12345))
+    ids = stream_encode(ctx, vb, off, text, cuts)
+    want, _ = oracle.Trie(vb, off).encode(text, np.array([0, len(text)], dtype=np.uint64))
+    assert np.array_equal(ids, want)
+
+
 def test_encode_capacity_error(ctx):
     import bpe_trie_encode_gb300 as bt
     toks = [bytes([b]) for b in range(256)]
