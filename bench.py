@@ -408,6 +408,9 @@ def run_ours(args, rank, world, local_rank):
     e2e = None
     if not args.no_e2e:
         h_merges_bytes = n_merges * 16
+        if enc:   # pinned host outputs of the end-to-end encode
+            h_ids_buf = torch.empty(enc["bytes"], dtype=torch.int32, pin_memory=True)
+            h_ioff_buf = torch.empty(enc["h_off"].numel(), dtype=torch.int64)
         tr_ms = en_ms = 0.0
         d2h_ids = 0
         for i in range(args.warmup + args.steps):
@@ -419,12 +422,9 @@ def run_ours(args, rank, world, local_rank):
             ctx.pretokenize(dt, out=d_sym)
             m, _ = ctx.train(d_sym, n_merges, final=False)     # merge table returns to host
             b.record(stream)
-            if enc:
-                de = enc["h"].to(dev, non_blocking=True)
-                do = enc["h_off"].to(dev, non_blocking=True)
-                ids, id_off = ctx.encode(enc["trie"], de, do, ids_out=enc["ids"])
-                h_ids = ids.to("cpu")
-                h_io = id_off.to("cpu")
+            if enc:   # host buffers in and out through trie_encode_host (copies overlap the encode)
+                h_ids, h_io = bt.encode_host(ctx, enc["trie"], enc["h"], enc["h_off"], ids_out=h_ids_buf,
+                                             id_off_out=h_ioff_buf)
                 d2h_ids = h_ids.numel() * 4 + h_io.numel() * 8
             c.record(stream)
             torch.cuda.synchronize(dev)

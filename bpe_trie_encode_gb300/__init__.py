@@ -186,6 +186,34 @@ class Context:
         return ids_out[: n_ids.value], id_off[: n_docs + 1]
 
 
+def encode_host(ctx: "Context", trie: "Trie", data, doc_off=None, ids_out=None, id_off_out=None,
+                slice_bytes: int = 0):
+    """Greedy longest-match ids from host memory (trie_encode_host: the
+    copies overlap the encode).  data: uint8 CPU tensor (pinned for overlap);
+    doc_off: int64 CPU tensor of n_docs+1 offsets (default: one document).
+    Returns (ids int32 CPU tensor, id_off int64 CPU tensor)."""
+    if not isinstance(data, torch.Tensor) or data.device.type != "cpu" or data.dtype != torch.uint8:
+        raise TypeError("data must be a uint8 CPU tensor")
+    if doc_off is None:
+        doc_off = torch.tensor([0, data.numel()], dtype=torch.int64)
+    doc_off = doc_off.to(torch.int64).contiguous()
+    n_docs = doc_off.numel() - 1
+    if ids_out is None:
+        ids_out = torch.empty(max(data.numel(), 1), dtype=torch.int32, pin_memory=True)
+    if id_off_out is None:
+        id_off_out = torch.empty(max(n_docs + 1, 1), dtype=torch.int64)
+    n = ctypes.c_uint64(0)
+    ctx._sync_stream()
+    rc = ctx.lib.trie_encode_host(ctx._h, trie._h, ctypes.c_void_p(data.data_ptr() if data.numel() else 0),
+                                  ctypes.c_void_p(doc_off.data_ptr()), max(n_docs, 0),
+                                  ctypes.c_void_p(ids_out.data_ptr()), ids_out.numel(),
+                                  ctypes.c_void_p(id_off_out.data_ptr()), ctypes.byref(n), slice_bytes)
+    if rc == -6:
+        raise BpeError(rc, f"{n.value} ids needed, capacity {ids_out.numel()}")
+    _capi.check(ctx._h, rc)
+    return ids_out[: n.value], id_off_out[: n_docs + 1]
+
+
 class Stream:
     """Streaming encode of one document arriving in slices (trie_stream_*):
     push() returns the ids that no later byte can change; the last push

@@ -30,6 +30,7 @@ EXPORTS = [
     "bpe_ctx_set_option", "bpe_last_stats", "bpe_pretokenize", "bpe_train",
     "trie_build", "trie_layout", "trie_info", "trie_free", "trie_encode",
     "trie_encode_noalloc", "trie_stream_open", "trie_stream_push", "trie_stream_close",
+    "trie_encode_host",
 ]
 
 
@@ -88,6 +89,7 @@ def load() -> ctypes.CDLL:
             "trie_stream_open": (i32, [vp, vp, P(vp)]),
             "trie_stream_push": (i32, [vp, vp, u64, i32, vp, u64, P(u64)]),
             "trie_stream_close": (None, [vp]),
+            "trie_encode_host": (i32, [vp, vp, vp, vp, u32, vp, u64, vp, P(u64), u64]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

@@ -688,6 +688,17 @@ __global__ void __launch_bounds__(kEmitThreads) k_emit(EncParams P, unsigned lon
     }
 }
 
+// Small transfers done by one CTA instead of a copy engine, so they never
+// queue behind a large host transfer on another stream (the host side is
+// pinned memory, which the device addresses directly).
+__global__ void k_copy_small(const uint8_t *src, uint8_t *dst, uint32_t n) {
+    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
+}
+__global__ void k_set_doc(uint64_t *off, uint64_t total) {
+    off[0] = 0;
+    off[1] = total;
+}
+
 __global__ void k_doc_offsets(EncParams P, unsigned long long n_chunks) {
     const uint64_t d = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
     if (d > P.n_docs) return;
@@ -784,7 +795,7 @@ extern "C" int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_
     k_chunk_index<<<1, 1024, 0, s>>>(P, (unsigned long long *)cstart);
     if (profile) cudaEventRecord(ctx->events[1], s);
     BPE_CUDA(ctx, cudaGetLastError(), "k_chunk_index launch");
-    BPE_CUDA(ctx, cudaMemcpyAsync(h, state, sizeof(EncState), cudaMemcpyDeviceToHost, s), "state read");
+    k_copy_small<<<1, 128, 0, s>>>((const uint8_t *)state, (uint8_t *)h, (uint32_t)sizeof(EncState));   // state read
     BPE_CUDA(ctx, cudaStreamSynchronize(s), "chunk index sync");
     if (h->err & DERR_OOB)
         return fail(ctx, BPE_ERR_INVALID_ARG, "trie_encode: document offsets descend at document %u", h->bad_doc_off);
@@ -849,7 +860,7 @@ extern "C" int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_
     if (profile) cudaEventRecord(ctx->events[5], s);
     k_doc_offsets<<<(unsigned)((n_docs + 1 + 255) / 256), 256, 0, s>>>(P, nc);
     BPE_CUDA(ctx, cudaGetLastError(), "trie_encode launch");
-    BPE_CUDA(ctx, cudaMemcpyAsync(h, state, sizeof(EncState), cudaMemcpyDeviceToHost, s), "state read");
+    k_copy_small<<<1, 128, 0, s>>>((const uint8_t *)state, (uint8_t *)h, (uint32_t)sizeof(EncState));   // state read
     BPE_CUDA(ctx, cudaStreamSynchronize(s), "trie_encode sync");
     if (h->err & DERR_TIMEOUT) return fail(ctx, BPE_ERR_TIMEOUT, "trie_encode: look-back wait gave up");
 
@@ -935,6 +946,53 @@ extern "C" void trie_stream_close(bpe_stream *st) {
     delete st;
 }
 
+// Encode the document doc[0 .. total) (the carried bytes, then the slice) and
+// keep the bytes after the final prefix of its parse as the next carry.
+static int stream_encode(bpe_stream *st, const uint8_t *doc, uint64_t total, int last, int32_t *d_ids_out,
+                         uint64_t ids_capacity, uint64_t *n_ids) {
+    bpe_ctx *ctx = st->ctx;
+    cudaStream_t s = ctx->stream;
+    if (total == 0) {
+        BPE_CUDA(ctx, cudaStreamSynchronize(s), "sync");
+        return BPE_OK;
+    }
+    k_set_doc<<<1, 1, 0, s>>>(st->d_off, total);
+    uint64_t all = 0;
+    int rc = trie_encode(ctx, st->trie, doc, st->d_off, 1, d_ids_out, ids_capacity, nullptr, &all);
+    if (rc) {
+        *n_ids = all;
+        return rc;
+    }
+    if (last) {
+        st->carry = 0;
+        *n_ids = all;
+        return BPE_OK;
+    }
+    // the final prefix of the parse: the chunk arrays of that encode are still in the pool
+    const uint32_t C = (uint32_t)std::min(ctx->chunk, kMaxChunk);
+    const unsigned long long nc = (total + C - 1) / C;
+    EncParams P{};
+    P.bytes = doc;
+    P.chunk = C;
+    P.slot = st->trie->d_slot;
+    P.tid = st->trie->d_tid;
+    P.root = st->trie->d_root;
+    P.count = (uint32_t *)ctx->scratch[S_ENC_CHUNK_INFO].p;
+    P.exit_rel = P.count + nc;
+    P.prefix = (unsigned long long *)ctx->scratch[S_ENC_PREFIX].p;
+    k_stream_cut<<<1, 256, 0, s>>>(P, nc, total, st->trie->max_len, st->d_cut);
+    BPE_CUDA(ctx, cudaGetLastError(), "k_stream_cut launch");
+    k_copy_small<<<1, 32, 0, s>>>((const uint8_t *)st->d_cut, (uint8_t *)st->h_cut, 2 * sizeof(unsigned long long));
+    BPE_CUDA(ctx, cudaStreamSynchronize(s), "cut sync");
+    const uint64_t cut = st->h_cut[1];
+    st->carry = (uint32_t)(total - cut);   // below the longest token
+    if (st->carry)
+        k_copy_small<<<1, 256, 0, s>>>(doc + cut, st->d_carry, st->carry);   // carry keep
+    *n_ids = st->h_cut[0];
+    ctx->stats.kernel_launches += 1;
+    return BPE_OK;
+}
+
 extern "C" int trie_stream_push(bpe_stream *st, const uint8_t *d_bytes, uint64_t n, int last, int32_t *d_ids_out,
                                 uint64_t ids_capacity, uint64_t *n_ids) {
     if (!st || !n_ids) return BPE_ERR_INVALID_ARG;
@@ -956,52 +1014,22 @@ extern "C" int trie_stream_push(bpe_stream *st, const uint8_t *d_bytes, uint64_t
     if (st->carry)
         BPE_CUDA(ctx, cudaMemcpyAsync(st->d_buf, st->d_carry, st->carry, cudaMemcpyDeviceToDevice, s), "carry copy");
     if (n) BPE_CUDA(ctx, cudaMemcpyAsync(st->d_buf + st->carry, d_bytes, n, cudaMemcpyDeviceToDevice, s), "slice copy");
-    if (total == 0) {
-        BPE_CUDA(ctx, cudaStreamSynchronize(s), "sync");
-        return BPE_OK;
-    }
-    BPE_CUDA(ctx, cudaStreamSynchronize(s), "stream sync");   // h_cut is reused below
-    st->h_cut[2] = 0;
-    st->h_cut[3] = total;
-    BPE_CUDA(ctx, cudaMemcpyAsync(st->d_off, st->h_cut + 2, 2 * sizeof(uint64_t), cudaMemcpyHostToDevice, s),
-             "offsets");
-    uint64_t all = 0;
-    int rc = trie_encode(ctx, st->trie, st->d_buf, st->d_off, 1, d_ids_out, ids_capacity, nullptr, &all);
-    if (rc) {
-        *n_ids = all;
-        return rc;
-    }
-    if (last) {
-        st->carry = 0;
-        *n_ids = all;
-        return BPE_OK;
-    }
-    // the final prefix of the parse: the chunk arrays of that encode are still in the pool
-    const uint32_t C = (uint32_t)std::min(ctx->chunk, kMaxChunk);
-    const unsigned long long nc = (total + C - 1) / C;
-    EncParams P{};
-    P.bytes = st->d_buf;
-    P.chunk = C;
-    P.slot = st->trie->d_slot;
-    P.tid = st->trie->d_tid;
-    P.root = st->trie->d_root;
-    P.count = (uint32_t *)ctx->scratch[S_ENC_CHUNK_INFO].p;
-    P.exit_rel = P.count + nc;
-    P.prefix = (unsigned long long *)ctx->scratch[S_ENC_PREFIX].p;
-    k_stream_cut<<<1, 256, 0, s>>>(P, nc, total, st->trie->max_len, st->d_cut);
-    BPE_CUDA(ctx, cudaGetLastError(), "k_stream_cut launch");
-    BPE_CUDA(ctx, cudaMemcpyAsync(st->h_cut, st->d_cut, 2 * sizeof(unsigned long long), cudaMemcpyDeviceToHost, s),
-             "cut read");
-    BPE_CUDA(ctx, cudaStreamSynchronize(s), "cut sync");
-    const uint64_t cut = st->h_cut[1];
-    st->carry = (uint32_t)(total - cut);   // below the longest token
-    if (st->carry)
-        BPE_CUDA(ctx, cudaMemcpyAsync(st->d_carry, st->d_buf + cut, st->carry, cudaMemcpyDeviceToDevice, s),
-                 "carry keep");
-    *n_ids = st->h_cut[0];
-    ctx->stats.kernel_launches += 1;
-    return BPE_OK;
+    return stream_encode(st, st->d_buf, total, last, d_ids_out, ids_capacity, n_ids);
 }
+
+namespace bpe {
+// The slice already sits in device memory with at least the trie's longest
+// token length of writable bytes before it: the carry goes there, so the
+// slice itself is not copied.
+int stream_push_in_place(bpe_stream *st, uint8_t *d_slice, uint64_t n, int last, int32_t *d_ids_out,
+                         uint64_t ids_capacity, uint64_t *n_ids) {
+    *n_ids = 0;
+    uint8_t *doc = d_slice - st->carry;
+    if (st->carry)
+        k_copy_small<<<1, 256, 0, st->ctx->stream>>>(st->d_carry, doc, st->carry);   // carry copy
+    return stream_encode(st, doc, (uint64_t)st->carry + n, last, d_ids_out, ids_capacity, n_ids);
+}
+}  // namespace bpe
 
 // ---------------------------------------------------------------------------
 // trie_encode_noalloc: the same kernels, with every scratch buffer carved out

@@ -19,7 +19,7 @@ enum Slot {
     S_TRAIN_BUF0, S_TRAIN_BUF1, S_TABLE_KEY, S_TABLE_CNT, S_LIST0, S_LIST1,
     S_STATUS0, S_STATUS1, S_BEST, S_STATE, S_NHIST,
     S_ENC_CHUNK_START, S_ENC_CHUNK_INFO, S_ENC_NOTOK, S_ENC_STATUS, S_ENC_PREFIX, S_ENC_STATE, S_ENC_SIDS,
-    S_ENC_SBITS,
+    S_ENC_SBITS, S_HOST_IN0, S_HOST_IN1, S_HOST_OUT0, S_HOST_OUT1, S_HOST_OFF0, S_HOST_OFF1,
     S_W_BSUM, S_W_START, S_W_OCCSLOT, S_W_TABLE, S_W_UID, S_W_UINFO, S_W_SYM, S_W_OUTOFF,
     S_NUM
 };
@@ -85,6 +85,11 @@ int ensure_events(bpe_ctx *ctx, size_t n);
 // Stats helpers.
 void stats_reset(bpe_ctx *ctx);
 int stats_slot(bpe_ctx *ctx, const char *name);
+
+// Streaming push of a slice with writable headroom of the trie's longest
+// token length before it (the carried bytes are placed there).
+int stream_push_in_place(bpe_stream *st, uint8_t *d_slice, uint64_t n, int last, int32_t *d_ids_out,
+                         uint64_t ids_capacity, uint64_t *n_ids);
 
 }  // namespace bpe
 

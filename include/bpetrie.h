@@ -234,6 +234,23 @@ int trie_stream_push(bpe_stream *stream, const uint8_t *d_bytes, uint64_t n, int
                      uint64_t ids_capacity, uint64_t *n_ids);
 void trie_stream_close(bpe_stream *stream);
 
+/* Greedy encoding from host buffers, with the transfers overlapped ("Async
+ * batching", three streams ordered by events: host to device, compute,
+ * device to host; two device buffer slots).  Same result as trie_encode on
+ * the same documents.  Whole documents are grouped into units of about
+ * slice_bytes (0: 128 MiB) and encoded together; a longer document is streamed
+ * in slices of slice_bytes with the parse carried across them.
+ *
+ * h_bytes, h_doc_off (n_docs+1 ascending offsets): host input (pinned memory
+ * lets the copies overlap the encode); h_ids_out: ids_capacity int32 (host,
+ * pinned for the same reason); h_id_off_out (nullable): n_docs+1 uint64.
+ * *n_ids receives the total; past ids_capacity nothing is written and
+ * BPE_ERR_CAPACITY is returned with the required size.  Blocks until done.
+ * Errors: INVALID_ARG, CAPACITY, OOM, TIMEOUT, CUDA. */
+int trie_encode_host(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *h_bytes, const uint64_t *h_doc_off,
+                     uint32_t n_docs, int32_t *h_ids_out, uint64_t ids_capacity, uint64_t *h_id_off_out,
+                     uint64_t *n_ids, uint64_t slice_bytes);
+
 /* Encoding that allocates nothing.  The pages have no counterpart: this entry
  * point exists for callers of the library that cannot allocate device memory,
  * for example a plug-in that receives only a stream and raw device pointers

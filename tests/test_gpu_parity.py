@@ -404,6 +404,26 @@ def test_encode_stream_learned_vocab_megabytes(ctx, golden):
     assert np.array_equal(ids, want)
 
 
+@pytest.mark.parametrize("slice_bytes", [4096, 5000, 1 << 20])
+def test_encode_host_pipeline(ctx, slice_bytes):
+    # host buffers in, host buffers out: groups of whole documents and
+    # documents longer than a slice, with empty documents mixed in
+    import bpe_trie_encode_gb300 as bt
+    rng = random.Random(slice_bytes)
+    alpha = b"ab c."
+    toks = [bytes([b]) for b in range(256)] + [rand_bytes(rng, rng.randrange(2, 40), alpha) for _ in range(800)]
+    vb, off = vocab_arrays(toks)
+    docs = [rand_bytes(rng, rng.choice([0, 1, 100, 3000, 20000, 70000]), alpha) for _ in range(60)]
+    data = b"".join(docs)
+    doc_off = np.cumsum([0] + [len(d) for d in docs]).astype(np.int64)
+    trie = ctx.trie_build(vb, off)
+    h = torch.from_numpy(np.frombuffer(data, dtype=np.uint8).copy()).pin_memory()
+    ids, id_off = bt.encode_host(ctx, trie, h, torch.from_numpy(doc_off), slice_bytes=slice_bytes)
+    wids, woff = oracle.Trie(vb, off).encode(data, doc_off.astype(np.uint64))
+    assert np.array_equal(ids.numpy(), wids)
+    assert np.array_equal(id_off.numpy().astype(np.uint64), woff)
+
+
 def test_encode_capacity_error(ctx):
     import bpe_trie_encode_gb300 as bt
     toks = [bytes([b]) for b in range(256)]
@@ -447,6 +467,13 @@ def test_encode_large_vocab_workload(ctx, large_merges, golden):
     assert ids.numel() == g["n_ids"]
     assert sha(ids.cpu().numpy()) == g["ids_sha256"]
     assert sha(id_off.cpu().numpy().astype(np.uint64)) == g["id_off_sha256"]
+    # the same from host memory: 64 MiB slices streamed with the parse carried across them
+    import bpe_trie_encode_gb300 as bt
+    h = d.cpu().pin_memory()
+    del d, ids
+    hids, hoff = bt.encode_host(ctx, trie, h)
+    assert hids.numel() == g["n_ids"] and sha(hids.numpy()) == g["ids_sha256"]
+    assert sha(hoff.numpy().astype(np.uint64)) == g["id_off_sha256"]
 
 
 def test_encode_batch_workload(ctx, golden):
