@@ -270,6 +270,21 @@ def extra_legs(args, ctx, dev, stream, flush, d_text, d_sym, n_merges, peak, pea
                            "workload": f"{doc_off.size - 1} documents, {data.size} B, 250,000-token substring vocabulary",
                            "n_ids": int(r[0].numel()), "trie": trie.info(),
                            "roofline": roofline(kern, ["encode_spec", "encode_emit"], peak, peak_kind, {})}
+    # the same batch through the bitmap-node trie layout, against the double array above
+    ctx.set_option(bt.BPE_OPT_TRIE_LAYOUT, bt.BPE_TRIE_BITMAP)
+    ms_bm = 0.0
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        (r2, _), ms = timed(stream, lambda: (ctx.encode(trie, d_data, d_off, ids_out=ids), None))
+        if i >= args.warmup:
+            ms_bm += ms
+    ctx.set_option(bt.BPE_OPT_TRIE_LAYOUT, bt.BPE_TRIE_DOUBLE_ARRAY)
+    out["encode_batch_bitmap_layout"] = {
+        "value": round(args.steps * data.size / (ms_bm / 1e3) / 1e9, 3), "unit": "GB/s",
+        "ms_per_step": round(ms_bm / args.steps, 3), "n_ids": int(r2[0].numel()),
+        "vs_double_array": round(ms_all / ms_bm, 3),
+        "workload": "the batch encode above with 64-byte bitmap nodes instead of the double array"}
     return out
 
 

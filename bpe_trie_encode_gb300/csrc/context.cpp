@@ -160,6 +160,11 @@ extern "C" int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value) {
             return fail(ctx, BPE_ERR_INVALID_ARG, "unknown merge variant %lld", (long long)value);
         ctx->merge_mode = (int)value;
         return BPE_OK;
+    case BPE_OPT_TRIE_LAYOUT:
+        if (value != BPE_TRIE_DOUBLE_ARRAY && value != BPE_TRIE_BITMAP)
+            return fail(ctx, BPE_ERR_INVALID_ARG, "unknown trie layout %lld", (long long)value);
+        ctx->trie_layout = (int)value;
+        return BPE_OK;
     case BPE_OPT_PERSISTENT:
         ctx->persistent = value ? 1 : 0;
         return BPE_OK;

@@ -74,6 +74,7 @@ struct EncParams {
     uint32_t chunk;              // C
     const unsigned long long *chunk_start;   // n_docs + 1
     const int2 *slot;
+    const BmNode *bm;            // bitmap-node layout (null unless that layout is used)
     const int32_t *tid;
     const int4 *root;
     uint32_t *count;             // per chunk: tokens starting in the chunk (true path)
@@ -101,7 +102,27 @@ struct Match {
     int32_t id;
 };
 
+// One trie step below the root: node -> its child on byte ch (at base + ch).
+// L = 0, double array: the child slot's check must name node.  L = 1, bitmap
+// nodes: node's bitmap has bit ch (both loads independent).  *ny: the
+// child's base | TERM.
+template <int L>
+__device__ __forceinline__ bool trie_step(const EncParams &P, int32_t node, uint32_t base, uint32_t ch, int32_t *nt,
+                                          uint32_t *ny) {
+    const int32_t t = (int32_t)(base + ch);
+    *nt = t;
+    if (L == 0) {
+        const int2 v = __ldg(P.slot + t);
+        *ny = (uint32_t)v.y;
+        return v.x == node;
+    }
+    const unsigned long long w = __ldg(&P.bm[node].bits[ch >> 6]);
+    *ny = __ldg(&P.bm[t].by);
+    return (w >> (ch & 63)) & 1ull;
+}
+
 // Longest token prefixing bytes[p, end) (p < end).
+template <int L = 0>
 __device__ __forceinline__ Match match_at(const EncParams &P, const int4 *lut, uint64_t p, uint64_t end) {
     const int4 r = lut[__ldg(P.bytes + p)];
     int32_t node = r.x;
@@ -112,11 +133,11 @@ __device__ __forceinline__ Match match_at(const EncParams &P, const int4 *lut, u
     while (q < end) {
         const uint32_t base = y & ~kTermBit;
         if (base == 0) break;                       // no children
-        const int32_t t = (int32_t)(base + __ldg(P.bytes + q));
-        const int2 v = __ldg(P.slot + t);
-        if (v.x != node) break;
+        int32_t t;
+        uint32_t ny;
+        if (!trie_step<L>(P, node, base, __ldg(P.bytes + q), &t, &ny)) break;
         node = t;
-        y = (uint32_t)v.y;
+        y = ny;
         ++q;
         if (y & kTermBit) {
             m.len = (uint32_t)(q - p);
@@ -130,6 +151,7 @@ __device__ __forceinline__ Match match_at(const EncParams &P, const int4 *lut, u
 // The longest token prefixing bytes[p, end) when that match is final: false
 // when the trie walk ran into end with children still possible (more bytes
 // could make the match longer).
+template <int L = 0>
 __device__ __forceinline__ bool match_final(const EncParams &P, const int4 *lut, uint64_t p, uint64_t end,
                                             uint32_t *len) {
     const int4 r = lut[__ldg(P.bytes + p)];
@@ -141,11 +163,11 @@ __device__ __forceinline__ bool match_final(const EncParams &P, const int4 *lut,
         const uint32_t base = y & ~kTermBit;
         if (base == 0) return true;                 // no children: final
         if (q >= end) return false;                 // the next byte decides
-        const int32_t t = (int32_t)(base + __ldg(P.bytes + q));
-        const int2 v = __ldg(P.slot + t);
-        if (v.x != node) return true;               // mismatch: final
+        int32_t t;
+        uint32_t ny;
+        if (!trie_step<L>(P, node, base, __ldg(P.bytes + q), &t, &ny)) return true;   // mismatch: final
         node = t;
-        y = (uint32_t)v.y;
+        y = ny;
         ++q;
         if (y & kTermBit) *len = (uint32_t)(q - p);
     }
@@ -219,7 +241,7 @@ struct ByteWin {
 // Returns the position after the last token; *cnt = tokens parsed (MODE 1
 // and 3: tokens up to the meeting point, *met = whether it met the marked
 // path).
-template <int MODE>
+template <int MODE, int L = 0>
 __device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 *lut, uint64_t p_abs, uint64_t ce_abs,
                                                  uint64_t de_abs, uint64_t cs, uint32_t *bits, uint32_t *cnt,
                                                  unsigned long long o, bool *met, int32_t *sid = nullptr) {
@@ -256,10 +278,7 @@ __device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 
                 btid = r.z;
                 ok = true;
             } else {
-                nt = (int32_t)(base + ch);
-                const int2 v = __ldg(P.slot + nt);
-                ny = (uint32_t)v.y;
-                ok = (v.x == node);
+                ok = trie_step<L>(P, node, base, ch, &nt, &ny);
             }
         }
         if (ok) {
@@ -351,6 +370,7 @@ __global__ void __launch_bounds__(1024) k_chunk_index(EncParams P, unsigned long
 
 // ------------------------------------------------ speculative parse + fix ---
 
+template <int L>
 __global__ void __launch_bounds__(kSpecThreads, 8) k_spec(EncParams P, unsigned long long n_chunks, uint64_t text_end) {
     extern __shared__ uint32_t s_bits[];   // kSpecThreads x (C/32) token-start bitmaps
     __shared__ int4 lut[256];
@@ -371,7 +391,7 @@ __global__ void __launch_bounds__(kSpecThreads, 8) k_spec(EncParams P, unsigned 
     if (live) {
         for (uint32_t w = 0; w < words; w++) bits[w * kBS] = 0;
         int32_t *sid = P.sids ? P.sids + (size_t)k * P.chunk : nullptr;
-        spec_exit = parse_tokens<0>(P, lut, g.cs, g.ce, g.de, g.cs, bits, &spec_count, 0, nullptr, sid);
+        spec_exit = parse_tokens<0, L>(P, lut, g.cs, g.ce, g.de, g.cs, bits, &spec_count, 0, nullptr, sid);
         if (P.sbits)
             for (uint32_t w = 0; w < words; w++) P.sbits[(size_t)k * words + w] = bits[w * kBS];
     }
@@ -389,7 +409,7 @@ __global__ void __launch_bounds__(kSpecThreads, 8) k_spec(EncParams P, unsigned 
         // two paths meet; from there the rest of the chunk is the spec path
         bool met = false;
         uint32_t c = 0;
-        const uint64_t q = parse_tokens<1>(P, lut, s_exit[tid - 1], g.ce, g.de, g.cs, bits, &c, 0, &met);
+        const uint64_t q = parse_tokens<1, L>(P, lut, s_exit[tid - 1], g.ce, g.de, g.cs, bits, &c, 0, &met);
         if (met) {
             const uint32_t o = (uint32_t)(q - g.cs);
             uint32_t rest = __popc(bits[(o >> 5) * kBS] >> (o & 31));
@@ -415,11 +435,12 @@ __global__ void __launch_bounds__(kSpecThreads, 8) k_spec(EncParams P, unsigned 
 // ---------------------------------------------------------------- repair ---
 
 // Parse [e, ce) of a chunk fully; returns the count and sets *exit.
+template <int L>
 __device__ uint32_t parse_from(const EncParams &P, const int4 *lut, uint64_t e, uint64_t ce, uint64_t de,
                                uint64_t *exit) {
     uint32_t c = 0;
     while (e < ce) {
-        e += match_at(P, lut, e, de).len;
+        e += match_at<L>(P, lut, e, de).len;
         ++c;
     }
     *exit = e;
@@ -430,6 +451,7 @@ __device__ uint32_t parse_from(const EncParams &P, const int4 *lut, uint64_t e, 
 // chunks after it from their true entries until an exit agrees with the next
 // chunk's nominal entry again or the document ends.  Returns the last chunk
 // rewritten (f if none).
+template <int L>
 __device__ unsigned long long repair_chain(const EncParams &P, const int4 *lut, unsigned long long f,
                                            unsigned long long n_chunks) {
     const ChunkGeo gf = chunk_geo(P, f);
@@ -439,7 +461,7 @@ __device__ unsigned long long repair_chain(const EncParams &P, const int4 *lut, 
         const ChunkGeo g = chunk_geo(P, c);
         if (g.doc_first) break;           // next document: entry resets
         uint64_t x;
-        P.count[c] = parse_from(P, lut, e, g.ce, g.de, &x);
+        P.count[c] = parse_from<L>(P, lut, e, g.ce, g.de, &x);
         P.exit_rel[c] = (uint32_t)(x - g.cs);
         if (x == g.cs + P.spec_rel[c]) return c;   // agrees with the next nominal entry
         e = x;
@@ -453,6 +475,7 @@ constexpr uint32_t kFlagListCap = 4096;
 
 // One walker per flagged chunk, all in parallel: the chain as it would be if
 // the chunk's entry is true, recorded privately (up to kWalkMax chunks).
+template <int LY>
 __global__ void k_repair_walk(EncParams P, unsigned long long n_chunks) {
     __shared__ int4 lut[256];
     const uint32_t L = P.st->flist_len;
@@ -473,7 +496,7 @@ __global__ void k_repair_walk(EncParams P, unsigned long long n_chunks) {
                 break;
             }
             uint64_t x;
-            w[2 + 2 * m] = parse_from(P, lut, e, g.ce, g.de, &x);
+            w[2 + 2 * m] = parse_from<LY>(P, lut, e, g.ce, g.de, &x);
             w[3 + 2 * m] = (uint32_t)(x - g.cs);
             ++m;
             if (x == g.cs + P.spec_rel[c]) break;
@@ -487,6 +510,7 @@ __global__ void k_repair_walk(EncParams P, unsigned long long n_chunks) {
 // Apply the walks of flagged chunks whose entry is true: in chunk order, a
 // flagged chunk inside the chain of an earlier applied one has a wrong entry
 // and is skipped.  With more flags than the list holds, repair sequentially.
+template <int LY>
 __global__ void __launch_bounds__(1024) k_repair_apply(EncParams P, unsigned long long n_chunks) {
     __shared__ int4 lut[256];
     __shared__ unsigned long long keys[kFlagListCap];
@@ -508,7 +532,7 @@ __global__ void __launch_bounds__(1024) k_repair_apply(EncParams P, unsigned lon
             if (w >= nw) break;
             const unsigned long long f = (w << 5) + (unsigned long long)(__ffs(bitsw) - 1);
             if (f >= n_chunks) break;
-            k = repair_chain(P, lut, f, n_chunks) + 1;
+            k = repair_chain<LY>(P, lut, f, n_chunks) + 1;
         }
         return;
     }
@@ -546,12 +570,13 @@ __global__ void __launch_bounds__(1024) k_repair_apply(EncParams P, unsigned lon
             P.exit_rel[f + 1 + r] = w[3 + 2 * r];
         }
         cur_end = (long long)(f + m);
-        if (w[1]) cur_end = (long long)repair_chain(P, lut, f + m, n_chunks);   // a long chain goes on
+        if (w[1]) cur_end = (long long)repair_chain<LY>(P, lut, f + m, n_chunks);   // a long chain goes on
     }
 }
 
 // ------------------------------------------------------------ scan + emit ---
 
+template <int L>
 __global__ void __launch_bounds__(kEmitThreads) k_emit(EncParams P, unsigned long long n_chunks, uint64_t text_end) {
     extern __shared__ uint32_t s_bits[];   // kEmitThreads x (C/32): each chunk's spec token starts
     __shared__ int4 lut[256];
@@ -591,8 +616,8 @@ __global__ void __launch_bounds__(kEmitThreads) k_emit(EncParams P, unsigned lon
                 const unsigned long long w = (j >= 0) ? ld_l2(P.status + j) : 2ull;
                 const uint32_t fl = (uint32_t)(w & 3ull);
                 const unsigned incl_m = __ballot_sync(kFull, fl == 2);
-                const int L = incl_m ? __ffs(incl_m) - 1 : 31;
-                const unsigned need = (L == 31) ? kFull : ((2u << L) - 1u);
+                const int li = incl_m ? __ffs(incl_m) - 1 : 31;   // first lane holding an inclusive prefix
+                const unsigned need = (li == 31) ? kFull : ((2u << li) - 1u);
                 if (__ballot_sync(kFull, fl == 0) & need) {
                     if (++spins > kSpinLimit) {
                         if (lane == 0) atomicOr(&P.st->err, DERR_TIMEOUT);
@@ -601,7 +626,7 @@ __global__ void __launch_bounds__(kEmitThreads) k_emit(EncParams P, unsigned lon
                     if (spins > 32) __nanosleep(64);
                     continue;
                 }
-                unsigned long long v = (lane <= L) ? (w >> 2) : 0ull;
+                unsigned long long v = (lane <= li) ? (w >> 2) : 0ull;
 #pragma unroll
                 for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
                 off += v;
@@ -622,7 +647,7 @@ __global__ void __launch_bounds__(kEmitThreads) k_emit(EncParams P, unsigned lon
         if (live) {
             const uint64_t e = g.doc_first ? g.cs : (g.cs - P.chunk) + P.exit_rel[k - 1];
             uint32_t c = 0;
-            parse_tokens<2>(P, lut, e, g.ce, g.de, g.cs, nullptr, &c, o, nullptr);
+            parse_tokens<2, L>(P, lut, e, g.ce, g.de, g.cs, nullptr, &c, o, nullptr);
         }
         return;
     }
@@ -639,7 +664,7 @@ __global__ void __launch_bounds__(kEmitThreads) k_emit(EncParams P, unsigned lon
         }
         const uint64_t e = g.doc_first ? g.cs : (g.cs - P.chunk) + P.exit_rel[k - 1];
         bool met = false;
-        const uint64_t q = parse_tokens<3>(P, lut, e, g.ce, g.de, g.cs, bits, &c_head, o, &met);
+        const uint64_t q = parse_tokens<3, L>(P, lut, e, g.ce, g.de, g.cs, bits, &c_head, o, &met);
         if (met) {   // spec tokens before offset q - cs are skipped
             const uint32_t off = (uint32_t)(q - g.cs);
             uint32_t before = 0;
@@ -713,6 +738,7 @@ __global__ void k_doc_offsets(EncParams P, unsigned long long n_chunks) {
 // last chunk exit at or before end - max_len the tokens are walked again
 // until the first whose walk reached the end.  out[0]: number of final ids;
 // out[1]: position of the first token that is not final (end if none).
+template <int L>
 __global__ void k_stream_cut(EncParams P, unsigned long long n_chunks, uint64_t end, uint32_t max_len,
                              unsigned long long *out) {
     __shared__ int4 lut[256];
@@ -734,7 +760,7 @@ __global__ void k_stream_cut(EncParams P, unsigned long long n_chunks, uint64_t 
     }
     while (b < end) {
         uint32_t len;
-        if (!match_final(P, lut, b, end, &len)) break;
+        if (!match_final<L>(P, lut, b, end, &len)) break;
         b += len;
         ++ids;
     }
@@ -742,6 +768,38 @@ __global__ void k_stream_cut(EncParams P, unsigned long long n_chunks, uint64_t 
     out[1] = b;
 }
 
+// The bitmap-node layout from the double array ([UNIGRAM] "Bitmap and inline
+// packing"): node i gets base | TERM and, for every slot j whose check names
+// i, bit j - base(i) of its child bitmap.
+__global__ void k_build_bm(const int2 *slot, unsigned long long n_slots, BmNode *bm) {
+    for (unsigned long long i = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x; i < n_slots;
+         i += (unsigned long long)gridDim.x * blockDim.x) {
+        const int2 v = slot[i];
+        bm[i].by = (uint32_t)v.y;
+        if (v.x >= 0) {   // a child of slot v.x
+            const uint32_t c = (uint32_t)(i - (slot[v.x].y & ~kTermBit));
+            atomicOr(&bm[v.x].bits[c >> 6], 1ull << (c & 63));
+        }
+    }
+}
+
+}  // namespace
+
+int trie_bitmap_nodes(bpe_ctx *ctx, const bpe_trie *trie) {
+    if (trie->d_bm) return BPE_OK;
+    bpe_trie *t = const_cast<bpe_trie *>(trie);   // built once, on first use
+    void *p = nullptr;
+    BPE_CUDA(ctx, cudaMalloc(&p, trie->n_slots * sizeof(BmNode)), "bitmap nodes");
+    BPE_CUDA(ctx, cudaMemsetAsync(p, 0, trie->n_slots * sizeof(BmNode), ctx->stream), "bitmap nodes clear");
+    k_build_bm<<<(unsigned)std::min<unsigned long long>((trie->n_slots + 255) / 256, 65535), 256, 0, ctx->stream>>>(
+        trie->d_slot, trie->n_slots, (BmNode *)p);
+    BPE_CUDA(ctx, cudaGetLastError(), "k_build_bm launch");
+    BPE_CUDA(ctx, cudaStreamSynchronize(ctx->stream), "bitmap nodes sync");
+    t->d_bm = p;
+    return BPE_OK;
+}
+
+namespace {
 }  // namespace
 }  // namespace bpe
 
@@ -843,20 +901,27 @@ extern "C" int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_
     BPE_CUDA(ctx, cudaMemsetAsync(flag, 0, ((nc + 31) / 32) * 4, s), "flag clear");
     BPE_CUDA(ctx, cudaMemsetAsync(status, 0, emit_tiles * 8, s), "status clear");
     const size_t spec_smem = spec_smem_for(C), emit_smem = emit_smem_for(C);
-    BPE_CUDA(ctx, cudaFuncSetAttribute(k_spec, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)spec_smem),
+    const bool bm = ctx->trie_layout == BPE_TRIE_BITMAP;
+    if (bm) {
+        if ((rc = trie_bitmap_nodes(ctx, trie))) return rc;
+        P.bm = (const BmNode *)trie->d_bm;
+    }
+    auto spec_fn = bm ? k_spec<1> : k_spec<0>;
+    auto emit_fn = bm ? k_emit<1> : k_emit<0>;
+    BPE_CUDA(ctx, cudaFuncSetAttribute(spec_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)spec_smem),
              "k_spec smem");
-    BPE_CUDA(ctx, cudaFuncSetAttribute(k_emit, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)emit_smem),
+    BPE_CUDA(ctx, cudaFuncSetAttribute(emit_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)emit_smem),
              "k_emit smem");
 
     const unsigned long long emit_grid = emit_tiles;   // one tile per CTA, ticket order
 
     if (profile) cudaEventRecord(ctx->events[2], s);
-    k_spec<<<(unsigned)spec_blocks, kSpecThreads, spec_smem, s>>>(P, nc, text_end);
+    spec_fn<<<(unsigned)spec_blocks, kSpecThreads, spec_smem, s>>>(P, nc, text_end);
     if (profile) cudaEventRecord(ctx->events[3], s);
-    k_repair_walk<<<16, 256, 0, s>>>(P, nc);
-    k_repair_apply<<<1, 1024, 0, s>>>(P, nc);
+    (bm ? k_repair_walk<1> : k_repair_walk<0>)<<<16, 256, 0, s>>>(P, nc);
+    (bm ? k_repair_apply<1> : k_repair_apply<0>)<<<1, 1024, 0, s>>>(P, nc);
     if (profile) cudaEventRecord(ctx->events[4], s);
-    k_emit<<<(unsigned)emit_grid, kEmitThreads, emit_smem, s>>>(P, nc, text_end);
+    emit_fn<<<(unsigned)emit_grid, kEmitThreads, emit_smem, s>>>(P, nc, text_end);
     if (profile) cudaEventRecord(ctx->events[5], s);
     k_doc_offsets<<<(unsigned)((n_docs + 1 + 255) / 256), 256, 0, s>>>(P, nc);
     BPE_CUDA(ctx, cudaGetLastError(), "trie_encode launch");
@@ -980,7 +1045,9 @@ static int stream_encode(bpe_stream *st, const uint8_t *doc, uint64_t total, int
     P.count = (uint32_t *)ctx->scratch[S_ENC_CHUNK_INFO].p;
     P.exit_rel = P.count + nc;
     P.prefix = (unsigned long long *)ctx->scratch[S_ENC_PREFIX].p;
-    k_stream_cut<<<1, 256, 0, s>>>(P, nc, total, st->trie->max_len, st->d_cut);
+    P.bm = (const BmNode *)st->trie->d_bm;   // built by the encode above when that layout is on
+    (ctx->trie_layout == BPE_TRIE_BITMAP ? k_stream_cut<1> : k_stream_cut<0>)<<<1, 256, 0, s>>>(
+        P, nc, total, st->trie->max_len, st->d_cut);
     BPE_CUDA(ctx, cudaGetLastError(), "k_stream_cut launch");
     k_copy_small<<<1, 32, 0, s>>>((const uint8_t *)st->d_cut, (uint8_t *)st->h_cut, 2 * sizeof(unsigned long long));
     BPE_CUDA(ctx, cudaStreamSynchronize(s), "cut sync");
@@ -1136,14 +1203,14 @@ int noalloc_body(const bpe_trie *trie, const uint8_t *d_bytes, const uint64_t *d
         cudaMemsetAsync(P.status, 0, emit_tiles * 8, s) != cudaSuccess)
         return BPE_ERR_CUDA;
     const size_t spec_smem = spec_smem_for(kNaChunk), emit_smem = emit_smem_for(kNaChunk);
-    if (cudaFuncSetAttribute(k_spec, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)spec_smem) != cudaSuccess ||
-        cudaFuncSetAttribute(k_emit, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)emit_smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(k_spec<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)spec_smem) != cudaSuccess ||
+        cudaFuncSetAttribute(k_emit<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)emit_smem) != cudaSuccess)
         return BPE_ERR_CUDA;
     const uint64_t text_end = h.span + h.text_lo;
-    k_spec<<<(unsigned)spec_blocks, kSpecThreads, spec_smem, s>>>(P, nc, text_end);
-    k_repair_walk<<<16, 256, 0, s>>>(P, nc);
-    k_repair_apply<<<1, 1024, 0, s>>>(P, nc);
-    k_emit<<<(unsigned)emit_tiles, kEmitThreads, emit_smem, s>>>(P, nc, text_end);
+    k_spec<0><<<(unsigned)spec_blocks, kSpecThreads, spec_smem, s>>>(P, nc, text_end);
+    k_repair_walk<0><<<16, 256, 0, s>>>(P, nc);
+    k_repair_apply<0><<<1, 1024, 0, s>>>(P, nc);
+    k_emit<0><<<(unsigned)emit_tiles, kEmitThreads, emit_smem, s>>>(P, nc, text_end);
     k_doc_offsets<<<(unsigned)((n_docs + 1 + 255) / 256), 256, 0, s>>>(P, nc);
     if (cudaGetLastError() != cudaSuccess) return BPE_ERR_CUDA;
     if (cudaMemcpyAsync(&h, P.st, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess ||

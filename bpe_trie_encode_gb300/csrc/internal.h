@@ -56,6 +56,7 @@ struct bpe_ctx {
     int train_words = 0;
     int merge_mode = 0;   // BPE_MERGE_*
     int persistent = 0;
+    int trie_layout = 0;   // BPE_TRIE_*
     // cached graph of merge iterations
     bpe::TrainGraph graph;
     // profiling events (grown on demand)
@@ -85,6 +86,9 @@ int ensure_events(bpe_ctx *ctx, size_t n);
 // Stats helpers.
 void stats_reset(bpe_ctx *ctx);
 int stats_slot(bpe_ctx *ctx, const char *name);
+
+// The bitmap-node layout of a trie, built on its first use (kept with the trie).
+int trie_bitmap_nodes(bpe_ctx *ctx, const bpe_trie *trie);
 
 // Streaming push of a slice with writable headroom of the trie's longest
 // token length before it (the carried bytes are placed there).

@@ -15,7 +15,19 @@ struct bpe_trie {
     int2 *d_slot = nullptr;    // {check, base | TERM}, n_slots entries
     int32_t *d_tid = nullptr;  // token id per slot (-1: none)
     int4 *d_root = nullptr;    // 256 x {slot, base|TERM, tid, 0} of the depth-1 nodes
+    // bitmap-node layout, built on first use: per slot one 64-byte node
+    // {256-bit child bitmap, base|TERM} (the slot numbering of the double array)
+    void *d_bm = nullptr;
 };
+
+namespace bpe {
+struct alignas(64) BmNode {
+    unsigned long long bits[4];   // bit c: this node has a child on byte c (at base + c)
+    uint32_t by;                  // base | TERM, as in the double array
+    uint32_t pad[7];
+};
+static_assert(sizeof(BmNode) == 64, "one cache line per node");
+}
 
 namespace bpe {
 constexpr uint32_t kTermBit = 0x80000000u;

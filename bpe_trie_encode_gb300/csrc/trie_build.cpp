@@ -294,5 +294,6 @@ extern "C" void trie_free(bpe_trie *T) {
     if (T->d_slot) cudaFree(T->d_slot);
     if (T->d_tid) cudaFree(T->d_tid);
     if (T->d_root) cudaFree(T->d_root);
+    if (T->d_bm) cudaFree(T->d_bm);
     delete T;
 }

@@ -102,6 +102,14 @@ const char *bpe_last_error(const bpe_ctx *ctx);
  *                          every tile into its twin in the other buffer (no
  *                          global offsets), compacting into full tiles when
  *                          they fall below 70% full; gathered at the end
+ *   BPE_OPT_TRIE_LAYOUT  the trie layout trie_encode walks (same results):
+ *                        BPE_TRIE_DOUBLE_ARRAY (default): a step loads the
+ *                          child slot {check, base|TERM} and compares check;
+ *                        BPE_TRIE_BITMAP: 64-byte nodes with a 256-bit child
+ *                          bitmap ([UNIGRAM] "Bitmap and inline packing"), a
+ *                          step tests the parent's bit and loads the child's
+ *                          base|TERM; built on a trie's first use (n_slots x
+ *                          64 bytes, kept until trie_free)
  *   BPE_OPT_PERSISTENT   1 = with BPE_MERGE_TWO_PASS, the merge loop runs as one cooperative
  *                        launch per window of merges (all CTAs resident,
  *                        phases separated by grid barriers) instead of a CUDA
@@ -113,8 +121,10 @@ enum {
     BPE_OPT_CHUNK = 4,
     BPE_OPT_TRAIN_WORDS = 5,
     BPE_OPT_MERGE = 6,
-    BPE_OPT_PERSISTENT = 7
+    BPE_OPT_PERSISTENT = 7,
+    BPE_OPT_TRIE_LAYOUT = 8
 };
+enum { BPE_TRIE_DOUBLE_ARRAY = 0, BPE_TRIE_BITMAP = 1 };
 enum { BPE_MERGE_TWO_PASS = 0, BPE_MERGE_LOOKBACK = 1, BPE_MERGE_TILES = 2 };
 int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value);
 

@@ -492,6 +492,33 @@ def test_encode_batch_workload(ctx, golden):
     assert sha(id_off.cpu().numpy().astype(np.uint64)) == g["id_off_sha256"]
 
 
+# ------------------------------------------------ bitmap-node trie layout --
+@pytest.fixture
+def bitmap_ctx(ctx):
+    import bpe_trie_encode_gb300 as bt
+    ctx.set_option(bt.BPE_OPT_TRIE_LAYOUT, bt.BPE_TRIE_BITMAP)
+    yield ctx
+    ctx.set_option(bt.BPE_OPT_TRIE_LAYOUT, bt.BPE_TRIE_DOUBLE_ARRAY)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_bitmap_layout_random_vocab(bitmap_ctx, seed):
+    test_encode_random_vocab_ragged_docs(bitmap_ctx, seed)
+
+
+def test_bitmap_layout_edges(bitmap_ctx):
+    # long tokens across chunks, parses that never meet (repair), the stream cut
+    test_encode_tokens_longer_than_chunks(bitmap_ctx)
+    test_encode_parses_that_never_meet(bitmap_ctx)
+    test_encode_repair_paths(bitmap_ctx, 64, [1, 2, 127, 128, 129, 5000], 0.004)
+    test_encode_stream_long_tokens_and_reuse(bitmap_ctx)
+    test_encode_worked_examples(bitmap_ctx)
+
+
+def test_bitmap_layout_batch_workload(bitmap_ctx, golden):
+    test_encode_batch_workload(bitmap_ctx, golden)
+
+
 # --------------------------------------------- word-frequency training path --
 @pytest.fixture
 def words_ctx(ctx):
