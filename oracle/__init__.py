@@ -87,6 +87,9 @@ def _load():
         lib.orc_pair_counts.argtypes = [vp, u64, vp, vp, u64]
         lib.orc_encode.restype = i32
         lib.orc_encode.argtypes = [vp, vp, vp, u32, vp, u64, vp, vp]
+        lib.orc_unigram_encode.restype = i32
+        lib.orc_unigram_encode.argtypes = [vp, vp, ctypes.c_int32, ctypes.c_double, vp, vp, u32,
+                                           vp, u64, vp, vp]
         _lib = lib
         return lib
 
@@ -242,4 +245,27 @@ class Trie:
                                   _p(id_off), ctypes.byref(n))
         if rc:
             raise OracleError(f"oracle encode failed ({rc})")
+        return ids[: n.value].copy(), id_off
+
+    def unigram_encode(self, data, scores, unk_id: int, unk_score: float, doc_off=None):
+        """Most likely segmentation of each document under per-token f64 scores
+        ([UNIGRAM] "Unigram tokenization"): (ids int32, id_off uint64).  Tokens
+        end only on UTF-8 character boundaries; a character no token starts
+        becomes one ``unk_id`` scored ``unk_score``."""
+        b = _u8(data)
+        sc = np.ascontiguousarray(scores, dtype=np.float64)
+        if sc.size != self._off.size - 1:
+            raise OracleError("one score per token")
+        doc = (np.array([0, b.size], dtype=np.uint64) if doc_off is None
+               else np.ascontiguousarray(doc_off, dtype=np.uint64))
+        n_docs = doc.size - 1
+        cap = b.size
+        ids = np.empty(max(cap, 1), dtype=np.int32)
+        id_off = np.zeros(n_docs + 1, dtype=np.uint64)
+        n = ctypes.c_uint64(0)
+        rc = self._lib.orc_unigram_encode(self.h, _p(sc) if sc.size else None, unk_id, unk_score,
+                                          _p(b) if b.size else None, _p(doc), n_docs, _p(ids), cap,
+                                          _p(id_off), ctypes.byref(n))
+        if rc:
+            raise OracleError(f"oracle unigram encode failed ({rc})")
         return ids[: n.value].copy(), id_off

@@ -26,7 +26,9 @@
  *   - greedy encoding emits, at each position, the longest vocabulary string
  *     that prefixes the rest of the document; duplicate strings keep the
  *     lowest id; a position no token matches is an error.
+ *   - Unigram (Viterbi) segmentation: see orc_unigram_encode.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -536,4 +538,83 @@ int64_t orc_pair_counts(const uint32_t *sym, uint64_t n, uint32_t *keys_out,
     }
     free(keys);
     return d;
+}
+
+/* ------------------------------------------------------------------------
+ * Unigram (Viterbi) segmentation ([UNIGRAM] "Unigram tokenization": the most
+ * likely path, best[i] = max over tokens t = x[j..i) of best[j] + score(t)).
+ * Per document, following the page's recurrence:
+ *   best[0] = 0, best[i] = -inf otherwise;
+ *   for each position i in order that is reachable and not a UTF-8
+ *   continuation byte (10xxxxxx): walk the trie from i; every token t ending
+ *   at j relaxes best[j] with best[i] + score[t] when strictly larger
+ *   (ties keep the earlier start);
+ *   then backtrack from the document end.
+ * Readings of what the page leaves open:
+ *   - a token counts only when it ends at a character boundary (j is the end
+ *     or byte j is not a continuation byte): a path through the middle of a
+ *     character could never be continued;
+ *   - "no token matched" means no such token: then <unk> (id unk_id, score
+ *     unk_score) spans i .. the next character boundary, so every document
+ *     has a path.
+ * Scores are f64 (the page's node holds an f64 score).  ids / id_off as in
+ * orc_encode.
+ * ---------------------------------------------------------------------- */
+static int is_cont(uint8_t b) { return (b & 0xC0) == 0x80; }
+
+int orc_unigram_encode(const orc_trie *T, const double *score, int32_t unk_id, double unk_score,
+                       const uint8_t *bytes, const uint64_t *doc_off, uint32_t n_docs,
+                       int32_t *ids, uint64_t cap, uint64_t *id_off, uint64_t *n_ids) {
+    uint64_t m = 0;
+    for (uint32_t d = 0; d < n_docs; d++) {
+        if (id_off) id_off[d] = m;
+        const uint64_t s = doc_off[d], e = doc_off[d + 1];
+        if (e < s) return ORC_EARG;
+        const uint64_t n = e - s;
+        const uint8_t *x = bytes + s;
+        double *best = (double *)malloc(sizeof(double) * (n + 1));
+        uint64_t *from = (uint64_t *)malloc(sizeof(uint64_t) * (n + 1));
+        int32_t *tok = (int32_t *)malloc(sizeof(int32_t) * (n + 1));
+        if (!best || !from || !tok) { free(best); free(from); free(tok); return ORC_ENOMEM; }
+        for (uint64_t i = 0; i <= n; i++) best[i] = -INFINITY;
+        best[0] = 0.0;
+        for (uint64_t i = 0; i < n; i++) {
+            if (best[i] == -INFINITY || is_cont(x[i])) continue;
+            int matched = 0;
+            uint32_t node = 0;
+            for (uint64_t q = i; q < n; q++) {
+                node = trie_find(T, node, x[q]);
+                if (node == UINT32_MAX) break;
+                const uint64_t j = q + 1;
+                const int32_t t = T->nodes[node].tid;
+                if (t < 0 || (j < n && is_cont(x[j]))) continue;
+                matched = 1;
+                const double cand = best[i] + score[t];
+                if (cand > best[j]) { best[j] = cand; from[j] = i; tok[j] = t; }
+            }
+            if (!matched) {
+                uint64_t j = i + 1;
+                while (j < n && is_cont(x[j])) j++;
+                const double cand = best[i] + unk_score;
+                if (cand > best[j]) { best[j] = cand; from[j] = i; tok[j] = unk_id; }
+            }
+        }
+        if (best[n] == -INFINITY) {   /* cannot happen: every character has an edge */
+            free(best); free(from); free(tok);
+            return ORC_ENOMATCH;
+        }
+        /* backtrack: count, then write in order */
+        uint64_t k = 0;
+        for (uint64_t j = n; j > 0; j = from[j]) k++;
+        uint64_t w = m + k;
+        for (uint64_t j = n; j > 0; j = from[j]) {
+            w--;
+            if (w < cap && ids) ids[w] = tok[j];
+        }
+        m += k;
+        free(best); free(from); free(tok);
+    }
+    if (id_off) id_off[n_docs] = m;
+    *n_ids = m;
+    return m > cap ? ORC_ECAP : ORC_OK;
 }

@@ -16,7 +16,8 @@ enc   1 GiB text from the large lexicon, text seed 3
 batch 512 documents of >= 64 KiB from the large lexicon, text seed 4,
       document d drawn from its own sub-stream d; vocabulary: 256 bytes plus
       distinct substrings (2..48 bytes, log-uniform length) of the large
-      corpus drawn with seed 5, 250,000 tokens in all
+      corpus drawn with seed 5, 250,000 tokens in all; Unigram scores for it:
+      Zipf log-probabilities over a seed-6 random ranking (``unigram_scores``)
 ====  =====================================================================
 """
 from __future__ import annotations
@@ -58,6 +59,7 @@ BATCH_VOCAB_SEED = 5
 BATCH_VOCAB_SIZE = 250000
 BATCH_VOCAB_MIN_LEN = 2
 BATCH_VOCAB_MAX_LEN = 48
+UNIGRAM_SCORE_SEED = 6
 
 
 def build(force: bool = False) -> str:
@@ -95,6 +97,8 @@ def _load():
         lib.syn_document.argtypes = [vp, u64, u64, u64, vp, u64]
         lib.syn_substring_vocab.restype = u32
         lib.syn_substring_vocab.argtypes = [vp, u64, u64, u32, u32, u32, vp, u64, vp]
+        lib.syn_unigram_scores.restype = i32
+        lib.syn_unigram_scores.argtypes = [u32, u64, vp]
         lib.syn_ln_export.restype = ctypes.c_double
         lib.syn_ln_export.argtypes = [ctypes.c_double]
         lib.syn_exp_export.restype = ctypes.c_double
@@ -194,6 +198,20 @@ def substring_vocab(text: np.ndarray, n_tok: int = BATCH_VOCAB_SIZE,
         raise ValueError("substring vocabulary needs >= 256 tokens and text >= 2 bytes")
     off = off[: n + 1].copy()
     return data[: int(off[-1])].copy(), off
+
+
+def unigram_scores(n_tok: int, seed: int = UNIGRAM_SCORE_SEED) -> np.ndarray:
+    """Seeded synthetic Unigram log-probabilities (float64, one per token):
+    a Zipf law over a random ranking of the tokens, normalised to sum 1."""
+    out = np.empty(max(n_tok, 1), dtype=np.float64)
+    if _load().syn_unigram_scores(n_tok, seed, _ptr(out)) != 0:
+        raise ValueError("unigram scores need n_tok >= 1")
+    return out[:n_tok]
+
+
+def unigram_unk_score(scores: np.ndarray) -> float:
+    """Score of the unknown-character fallback: 10 below the lowest token."""
+    return float(np.min(scores)) - 10.0
 
 
 def ln(x: float) -> float:

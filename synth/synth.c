@@ -302,3 +302,27 @@ uint32_t syn_substring_vocab(const uint8_t *text, uint64_t text_len, uint64_t se
 /* Exposed for a determinism check of the float helpers. */
 double syn_ln_export(double x) { return syn_ln(x); }
 double syn_exp_export(double x) { return syn_exp(x); }
+
+/*
+ * Synthetic Unigram log-probabilities for n_tok tokens: a Zipf law over a
+ * seeded random ranking, score[t] = ln(1 / ((rank(t) + 1) * H)) with H the
+ * harmonic number of n_tok, so that exp(score) sums to 1.  Returns 0 on
+ * success, -1 when n_tok is 0.
+ */
+int syn_unigram_scores(uint32_t n_tok, uint64_t seed, double *score) {
+    if (n_tok == 0) return -1;
+    uint32_t *rank = (uint32_t *)malloc(sizeof(uint32_t) * n_tok);
+    if (!rank) return -1;
+    for (uint32_t t = 0; t < n_tok; t++) rank[t] = t;
+    syn_rng r = rng_make(seed, 5);
+    for (uint32_t t = n_tok - 1; t > 0; t--) {          /* Fisher-Yates */
+        uint32_t k = rng_below(&r, t + 1);
+        uint32_t x = rank[t]; rank[t] = rank[k]; rank[k] = x;
+    }
+    double H = 0.0;
+    for (uint32_t k = n_tok; k > 0; k--) H += 1.0 / (double)k;
+    const double lnH = syn_ln(H);
+    for (uint32_t t = 0; t < n_tok; t++) score[t] = -(lnH + syn_ln((double)rank[t] + 1.0));
+    free(rank);
+    return 0;
+}
