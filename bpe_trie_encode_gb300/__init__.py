@@ -11,6 +11,8 @@ PyTorch is used only for device memory and streams.
     merges, final = ctx.train(sym, 4096)
     trie = ctx.trie_build(*bt.vocab_from_merges(merges))
     ids, id_off = ctx.encode(trie, data_u8_cuda, doc_off_i64_cuda)
+    uni = ctx.unigram(trie, scores_f64, unk_id, unk_score)       # Viterbi model
+    ids, id_off = ctx.unigram_encode(uni, data_u8_cuda, doc_off_i64_cuda)
 """
 from __future__ import annotations
 
@@ -22,10 +24,10 @@ import torch
 from . import _capi
 from ._capi import (BPE_MAX_MERGES, BPE_MERGE_LOOKBACK, BPE_MERGE_TILES, BPE_MERGE_TWO_PASS,  # noqa: F401
                     BPE_OPT_CHUNK, BPE_OPT_GRAPH, BPE_OPT_MERGE, BPE_OPT_PERSISTENT, BPE_OPT_PROFILE,
-                    BPE_OPT_TABLE_LOG2, BPE_OPT_TRAIN_WORDS, BPE_OPT_TRIE_LAYOUT, BPE_TRIE_BITMAP,
+                    BPE_OPT_TABLE_LOG2, BPE_OPT_TRAIN_WORDS, BPE_OPT_TRIE_LAYOUT, BPE_OPT_UNI_CHUNK, BPE_TRIE_BITMAP,
                     BPE_TRIE_DOUBLE_ARRAY, BPE_WORD_START, BpeError)
 
-__all__ = ["Context", "Trie", "BpeError", "vocab_from_merges", "BPE_WORD_START", "BPE_MAX_MERGES"]
+__all__ = ["Context", "Trie", "Unigram", "BpeError", "vocab_from_merges", "BPE_WORD_START", "BPE_MAX_MERGES"]
 
 
 def _stream_ptr(device: torch.device) -> int:
@@ -185,6 +187,66 @@ class Context:
             raise BpeError(rc, f"{n_ids.value} ids needed, capacity {cap}")
         _capi.check(self._h, rc)
         return ids_out[: n_ids.value], id_off[: n_docs + 1]
+
+
+    def unigram(self, trie: Trie, scores, unk_id: int, unk_score: float) -> "Unigram":
+        """A Unigram (Viterbi) model over ``trie``: one f64 score per token
+        (host array), the id and score of the <unk> fallback."""
+        sc = np.ascontiguousarray(scores, dtype=np.float64)
+        h = ctypes.c_void_p()
+        _capi.check(self._h, self.lib.unigram_create(self._h, trie._h,
+                                                     ctypes.c_void_p(sc.ctypes.data if sc.size else 0),
+                                                     sc.size, int(unk_id), float(unk_score), ctypes.byref(h)))
+        return Unigram(h.value, self.device, trie)
+
+    def unigram_encode(self, model: "Unigram", data: torch.Tensor, doc_off: torch.Tensor | None = None,
+                       capacity: int | None = None, ids_out: torch.Tensor | None = None):
+        """Most likely segmentation of each document (Viterbi).  Arguments and
+        result as ``encode``."""
+        data = _need_cuda(data, torch.uint8, "data", self.device)
+        if doc_off is None:
+            doc_off = torch.tensor([0, data.numel()], dtype=torch.int64, device=self.device)
+        doc_off = _need_cuda(doc_off, torch.int64, "doc_off", self.device)
+        n_docs = doc_off.numel() - 1
+        if ids_out is None:
+            cap = data.numel() if capacity is None else capacity
+            ids_out = torch.empty(max(cap, 1), dtype=torch.int32, device=self.device)
+        else:
+            ids_out = _need_cuda(ids_out, torch.int32, "ids_out", self.device)
+            cap = ids_out.numel() if capacity is None else min(capacity, ids_out.numel())
+        id_off = torch.empty(max(n_docs + 1, 1), dtype=torch.int64, device=self.device)
+        n_ids = ctypes.c_uint64(0)
+        if data.numel() == 0:
+            data = torch.empty(16, dtype=torch.uint8, device=self.device)
+        self._sync_stream()
+        rc = self.lib.unigram_encode(self._h, model._h, ctypes.c_void_p(data.data_ptr()),
+                                     ctypes.c_void_p(doc_off.data_ptr()), max(n_docs, 0),
+                                     ctypes.c_void_p(ids_out.data_ptr()), cap,
+                                     ctypes.c_void_p(id_off.data_ptr()), ctypes.byref(n_ids))
+        if rc == -6:
+            raise BpeError(rc, f"{n_ids.value} ids needed, capacity {cap}")
+        _capi.check(self._h, rc)
+        return ids_out[: n_ids.value], id_off[: n_docs + 1]
+
+
+class Unigram:
+    """A Unigram model on the GPU (see ``Context.unigram``); keeps its trie alive."""
+
+    def __init__(self, handle: int, device: torch.device, trie: Trie):
+        self._h = ctypes.c_void_p(handle)
+        self.device = device
+        self.trie = trie
+
+    def close(self):
+        if self._h:
+            _capi.load().unigram_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def encode_host(ctx: "Context", trie: "Trie", data, doc_off=None, ids_out=None, id_off_out=None,

@@ -21,7 +21,7 @@ ERRORS = {
 BPE_WORD_START = 0x10000
 BPE_MAX_MERGES = 65280
 BPE_OPT_TABLE_LOG2, BPE_OPT_GRAPH, BPE_OPT_PROFILE, BPE_OPT_CHUNK, BPE_OPT_TRAIN_WORDS = 1, 2, 3, 4, 5
-BPE_OPT_MERGE, BPE_OPT_PERSISTENT, BPE_OPT_TRIE_LAYOUT = 6, 7, 8
+BPE_OPT_MERGE, BPE_OPT_PERSISTENT, BPE_OPT_TRIE_LAYOUT, BPE_OPT_UNI_CHUNK = 6, 7, 8, 9
 BPE_TRIE_DOUBLE_ARRAY, BPE_TRIE_BITMAP = 0, 1
 BPE_MERGE_TWO_PASS, BPE_MERGE_LOOKBACK, BPE_MERGE_TILES = 0, 1, 2
 
@@ -31,7 +31,7 @@ EXPORTS = [
     "bpe_ctx_set_option", "bpe_last_stats", "bpe_pretokenize", "bpe_train",
     "trie_build", "trie_layout", "trie_info", "trie_free", "trie_encode",
     "trie_encode_noalloc", "trie_stream_open", "trie_stream_push", "trie_stream_close",
-    "trie_encode_host",
+    "trie_encode_host", "unigram_create", "unigram_encode", "unigram_free",
 ]
 
 
@@ -91,6 +91,9 @@ def load() -> ctypes.CDLL:
             "trie_stream_push": (i32, [vp, vp, u64, i32, vp, u64, P(u64)]),
             "trie_stream_close": (None, [vp]),
             "trie_encode_host": (i32, [vp, vp, vp, vp, u32, vp, u64, vp, P(u64), u64]),
+            "unigram_create": (i32, [vp, vp, vp, u32, ctypes.c_int32, ctypes.c_double, P(vp)]),
+            "unigram_encode": (i32, [vp, vp, vp, vp, u32, vp, u64, vp, P(u64)]),
+            "unigram_free": (None, [vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

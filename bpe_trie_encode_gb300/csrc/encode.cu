@@ -811,6 +811,9 @@ extern "C" int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_
     if (!ctx) return BPE_ERR_INVALID_ARG;
     if (!trie || !n_ids) return fail(ctx, BPE_ERR_INVALID_ARG, "trie_encode: null trie or n_ids");
     if (trie->device != ctx->device) return fail(ctx, BPE_ERR_INVALID_ARG, "trie_encode: trie on another device");
+    if (trie->missing_byte >= 0)
+        return fail(ctx, BPE_ERR_INVALID_ARG, "trie_encode: byte 0x%02X is not a token of the vocabulary",
+                    trie->missing_byte);
     if (n_docs && (!d_doc_off || !d_bytes)) return fail(ctx, BPE_ERR_INVALID_ARG, "trie_encode: null input");
     if (ids_capacity && !d_ids_out) return fail(ctx, BPE_ERR_INVALID_ARG, "trie_encode: null ids with capacity");
     BPE_CUDA(ctx, cudaSetDevice(ctx->device), "cudaSetDevice");
@@ -981,6 +984,9 @@ extern "C" int trie_stream_open(bpe_ctx *ctx, const bpe_trie *trie, bpe_stream *
     if (!ctx || !trie || !out) return BPE_ERR_INVALID_ARG;
     *out = nullptr;
     if (trie->device != ctx->device) return fail(ctx, BPE_ERR_INVALID_ARG, "trie_stream_open: trie on another device");
+    if (trie->missing_byte >= 0)
+        return fail(ctx, BPE_ERR_INVALID_ARG, "trie_stream_open: byte 0x%02X is not a token of the vocabulary",
+                    trie->missing_byte);
     BPE_CUDA(ctx, cudaSetDevice(ctx->device), "cudaSetDevice");
     bpe_stream *st = new bpe_stream();
     st->ctx = ctx;
@@ -1229,6 +1235,7 @@ extern "C" int trie_encode_noalloc(const bpe_trie *trie, const uint8_t *d_bytes,
                                    uint64_t *d_id_off_out, uint64_t *n_ids, void *cuda_stream) {
     if (!trie || !n_ids) return BPE_ERR_INVALID_ARG;
     *n_ids = 0;
+    if (trie->missing_byte >= 0) return BPE_ERR_INVALID_ARG;   // greedy needs every single byte
     if (n_docs > bpe::kNaMaxDocs) return BPE_ERR_INVALID_ARG;
     if (n_docs && (!d_doc_off || !d_bytes)) return BPE_ERR_INVALID_ARG;
     if (ids_capacity && !d_ids_out) return BPE_ERR_INVALID_ARG;

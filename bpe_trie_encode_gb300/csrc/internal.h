@@ -21,6 +21,7 @@ enum Slot {
     S_ENC_CHUNK_START, S_ENC_CHUNK_INFO, S_ENC_NOTOK, S_ENC_STATUS, S_ENC_PREFIX, S_ENC_STATE, S_ENC_SIDS,
     S_ENC_SBITS, S_HOST_IN0, S_HOST_IN1, S_HOST_OUT0, S_HOST_OUT1, S_HOST_OFF0, S_HOST_OFF1,
     S_W_BSUM, S_W_START, S_W_OCCSLOT, S_W_TABLE, S_W_UID, S_W_UINFO, S_W_SYM, S_W_OUTOFF,
+    S_UNI_START, S_UNI_STATE, S_UNI_BACK, S_UNI_GBACK, S_UNI_CHUNK, S_UNI_FLAG, S_UNI_PREFIX, S_UNI_STATUS,
     S_NUM
 };
 
@@ -57,6 +58,7 @@ struct bpe_ctx {
     int merge_mode = 0;   // BPE_MERGE_*
     int persistent = 0;
     int trie_layout = 0;   // BPE_TRIE_*
+    int uni_chunk = 0;     // unigram_encode chunk bytes (0: default)
     // cached graph of merge iterations
     bpe::TrainGraph graph;
     // profiling events (grown on demand)

@@ -12,6 +12,7 @@ struct bpe_trie {
     uint64_t n_nodes = 0;
     uint64_t n_slots = 0;
     uint32_t max_len = 0;
+    int missing_byte = -1;     // lowest single byte that is not a token (-1: none; greedy encoding needs none)
     int2 *d_slot = nullptr;    // {check, base | TERM}, n_slots entries
     int32_t *d_tid = nullptr;  // token id per slot (-1: none)
     int4 *d_root = nullptr;    // 256 x {slot, base|TERM, tid, 0} of the depth-1 nodes

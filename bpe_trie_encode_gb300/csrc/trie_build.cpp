@@ -74,6 +74,7 @@ struct Layout {
     std::vector<int4> root;
     uint64_t n_nodes = 0;
     uint32_t max_len = 0;
+    int missing_byte = -1;   // lowest byte that is not a token, -1 if none
 };
 
 // Host-side construction; ctx (nullable) only receives error messages.
@@ -133,14 +134,13 @@ int build_layout(bpe_ctx *ctx, const uint8_t *h_vocab_bytes, const uint64_t *h_v
         prev_len = len;
     }
 
-    // every single byte must be a token (greedy matching then never fails)
+    // whether every single byte is a token (greedy matching then never fails)
     {
         std::vector<int> seen(256, 0);
         for (uint32_t c = nodes[0].first_child; c; c = nodes[c].next_sibling)
             if (nodes[c].tid >= 0) seen[nodes[c].label] = 1;
-        for (int b = 0; b < 256; b++)
-            if (!seen[b])
-                return fail(ctx, BPE_ERR_INVALID_ARG, "trie_build: byte 0x%02X is not a token of the vocabulary", b);
+        for (int b = 255; b >= 0; b--)
+            if (!seen[b]) L.missing_byte = b;
     }
 
     // 3. double-array placement in breadth-first order
@@ -249,6 +249,7 @@ extern "C" int trie_build(bpe_ctx *ctx, const uint8_t *h_vocab_bytes, const uint
     T->n_nodes = L.n_nodes;
     T->n_slots = (uint64_t)used;
     T->max_len = L.max_len;
+    T->missing_byte = L.missing_byte;
     cudaError_t e = cudaMalloc(&T->d_slot, sizeof(int2) * used);
     if (e == cudaSuccess) e = cudaMalloc(&T->d_tid, sizeof(int32_t) * used);
     if (e == cudaSuccess) e = cudaMalloc(&T->d_root, sizeof(int4) * 256);

@@ -1,0 +1,1268 @@
+// unigram.cu -- Unigram (Viterbi) encoding over the double-array trie
+// ([UNIGRAM] "Unigram tokenization": best[j] = max over tokens t = x[i..j) of
+// best[i] + score(t), continuation bytes skipped, <unk> where nothing
+// matches, a backtrack from the end; the token id and score live with the
+// trie node, [UNIGRAM] "Baseline" and "Bitmap and inline packing").
+//
+// The recurrence is sequential along a document; the GPU splits every
+// document into chunks of C bytes, one thread per chunk, and makes the
+// sequential result exact by speculation and repair.  Scores are summed in
+// 64-bit fixed point, so sums are associative and a path's decisions do not
+// depend on the constant its values start from.
+//
+//   k_uni_index   first chunk of every document, longest document
+//   k_uni_fwd     each thread runs the recurrence from the first character
+//                 boundary G bytes before its chunk (value 0 there, nothing
+//                 reachable before) through its chunk, and stores the back
+//                 pointer (token length, id) of every position: those of the
+//                 chunk in the output array, those of the guard privately.
+//   k_uni_check   the chunk's guard ran the recurrence from a wrong start
+//                 value, but if the back-pointer chains of every reachable
+//                 position of the last E bytes before the chunk (E = longest
+//                 edge) meet at one position z, and the guard's back pointers
+//                 equal the previous chunk's from z on, the guard's values
+//                 there are the true ones plus one constant -- and so are the
+//                 chunk's.  A chunk for which that fails is flagged.
+//   k_uni_frepair one thread per document with a flagged chunk re-runs the
+//                 recurrence, in order, from the chunk before each flagged
+//                 one through the chunks after it until a chunk passes the
+//                 check against the repaired back pointers.
+//   k_uni_bspec   each thread backtracks speculatively from a reachable
+//                 position H bytes past its chunk's end; back-pointer chains
+//                 merge, so where the chain first steps to or below the
+//                 chunk's end (sx) is usually where the true path does.  It
+//                 counts the tokens starting in the chunk and records the
+//                 chain's last position in the chunk (bot).
+//   k_uni_brepair the true sx of a chunk is the next chunk's bot (the
+//                 document end for the last chunk); one thread per document
+//                 re-walks, right to left, the chunks where they differ.
+//   k_uni_emit    exclusive scan of the counts (decoupled look-back) and a
+//                 walk of every chunk from its true sx that writes its ids.
+//   k_uni_docoff  per-document id offsets.
+//
+// A back pointer is (length << 24) | id, id 0xFFFFFF for <unk>; 0 marks an
+// unreachable position and kRoot the start of a speculative run.
+#include <algorithm>
+#include <cmath>
+#include <vector>
+
+#include "device.cuh"
+#include "internal.h"
+#include "trie.h"
+
+struct bpe_unigram {
+    bpe_ctx *ctx = nullptr;
+    const bpe_trie *trie = nullptr;
+    int device = 0;
+    int32_t unk_id = 0;
+    long long unk = 0;          // unk_score in fixed-point units
+    long long max_abs = 0;      // largest |score| in units (over tokens and unk)
+    int q = 0;                  // units are 2^-q
+    uint32_t span = 0;          // E: longest edge (token or <unk>) the kernels take
+    void *d_leaf = nullptr;     // per trie slot: {score units, token id}
+};
+
+namespace bpe {
+namespace {
+
+constexpr int kUniThreads = 128;
+constexpr uint32_t kRoot = 0x00FFFFFFu;    // speculative start (length 0 never occurs otherwise)
+constexpr uint32_t kUnkTid = 0x00FFFFFFu;
+constexpr long long kNeg = -0x7FFFFFFFFFFFFFFFll - 1;   // -inf
+constexpr uint32_t kUniDefaultChunk = 512;
+constexpr unsigned kUniSpinLimit = 1u << 22;
+enum : uint32_t { UERR_SPAN = 8u, UERR_OOB = 4u, UERR_TIMEOUT = 2u, UERR_CONT_START = 16u };
+
+struct __align__(16) Leaf {
+    long long score;
+    int32_t tid;
+    int32_t pad;
+};
+
+struct UniState {
+    unsigned long long n_chunks;
+    unsigned long long total;
+    unsigned long long max_doc;
+    unsigned long long span;      // doc_off[n_docs] - doc_off[0]
+    unsigned long long text_lo;   // doc_off[0]
+    uint32_t err;
+    uint32_t any_fflag, any_bflag;
+    uint32_t ticket;
+    uint32_t bad_doc;
+    uint32_t fwd_repairs, bwd_repairs;   // chunks re-run by the repair passes
+    uint32_t flist_len;
+};
+
+struct UniParams {
+    const uint8_t *bytes;
+    const uint64_t *doc_off;
+    uint32_t n_docs;
+    uint32_t chunk;     // C
+    uint32_t guard;     // G: guard bytes before a chunk (> E, <= 256, a multiple of 32)
+    uint32_t grec;      // words per chunk of the guard record: G back pointers, G/32 crossing bits
+    uint32_t E;         // longest edge
+    uint32_t ahead;     // H: backtrack start past the chunk end
+    const unsigned long long *chunk_start;   // n_docs + 1
+    const int2 *slot;
+    const int4 *root;
+    const Leaf *leaf;
+    long long unk;
+    int32_t unk_id;
+    unsigned long long text_lo;   // doc_off[0]
+    uint32_t *back;     // per position (offset from text_lo), span + 1 words
+    uint32_t *gback;    // per chunk grec words: the guard's back pointers and crossing bits
+    uint32_t *fflag, *bflag;   // bitmaps over chunks
+    uint32_t *okn;             // bitmap: a flagged chunk's parallel repair was valid for its successor too
+    uint32_t *okp;             // bitmap: a flagged chunk's parallel re-walk was valid for its predecessor too
+    uint32_t *flist;           // flagged chunks (unordered; flist_cap entries kept)
+    uint32_t flist_cap;
+    uint32_t *sx, *bot, *count;   // per chunk (sx, bot relative to the chunk start)
+    unsigned long long *prefix;
+    unsigned long long *status;
+    int32_t *ids;
+    unsigned long long cap;
+    unsigned long long *id_off;
+    UniState *st;
+};
+
+__device__ __forceinline__ bool is_cont(uint32_t b) { return (b & 0xC0u) == 0x80u; }
+__device__ __forceinline__ uint32_t byte_at(const UniParams &P, uint64_t p) { return __ldg(P.bytes + p); }
+__device__ __forceinline__ uint32_t &back_at(const UniParams &P, uint64_t p) {
+    return P.back[p - P.text_lo];
+}
+
+// Root LUT with the depth-1 nodes that exist: entry x < 0 when byte c has no
+// node below the root (the root is slot 0, its children's check is 0).
+__device__ __forceinline__ void load_uni_lut(const UniParams &P, int4 *lut) {
+    for (int c = threadIdx.x; c < 256; c += blockDim.x) {
+        int4 r = P.root[c];
+        if (__ldg(&P.slot[r.x].x) != 0) r.x = -1;
+        lut[c] = r;
+    }
+}
+
+__device__ __forceinline__ uint32_t doc_of_chunk(const UniParams &P, unsigned long long k) {
+    uint32_t lo = 0, hi = P.n_docs;
+    while (hi - lo > 1) {
+        const uint32_t mid = (lo + hi) >> 1;
+        if (P.chunk_start[mid] <= k) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+struct UGeo {
+    uint64_t ds, de, cs, ce;
+    bool first, last;   // first / last chunk of its document
+};
+
+__device__ __forceinline__ UGeo uni_geo(const UniParams &P, unsigned long long k) {
+    const uint32_t d = doc_of_chunk(P, k);
+    UGeo g;
+    g.ds = P.doc_off[d];
+    g.de = P.doc_off[d + 1];
+    const uint64_t j = k - P.chunk_start[d];
+    g.cs = g.ds + j * P.chunk;
+    g.ce = min(g.cs + P.chunk, g.de);
+    g.first = j == 0;
+    g.last = g.ce == g.de;
+    return g;
+}
+
+// One run of the recurrence over positions [from, to) of a document ending
+// at de, on a ring of R values and back pointers.  The caller has set the
+// ring for the positions it starts from.  Position i is final when the run
+// reaches it: its back pointer goes to sink(i, bp).  A reachable character
+// start then relaxes every token that ends at a character boundary (trie
+// walk) or, when there is none, the <unk> edge to the next boundary; every
+// relaxed edge i -> j is reported to edge(i, j).  Each loop iteration takes
+// one trie step on every lane (finalising a position first where a walk has
+// ended), so the lanes of a warp do not wait for each other's long walks.  A
+// run of E continuation bytes could only be crossed by a longer edge: it
+// raises UERR_SPAN (whichever run sees its last E bytes).
+template <int R, typename Sink, typename Edge>
+__device__ __forceinline__ void uni_run(const UniParams &P, const int4 *lut, long long *best, uint32_t *bk,
+                                        uint64_t from, uint64_t to, uint64_t de, Sink sink, Edge edge) {
+    uint32_t cont_run = 0;
+    uint64_t i = from;
+    int32_t node = -1;   // < 0: no walk in progress at i
+    uint32_t y = 0, len = 0;
+    long long b = 0;
+    bool matched = false;
+    auto relax = [&](uint64_t j, long long cand, uint32_t bp) {
+        const uint32_t sj = (uint32_t)j & (R - 1);
+        if (cand > best[sj]) {
+            best[sj] = cand;
+            bk[sj] = bp;
+        }
+        edge(i, j);
+    };
+    auto unk_edge = [&]() {
+        uint64_t j = i + 1;
+        while (j < de && is_cont(byte_at(P, j)) && j - i <= P.E) ++j;
+        if (j - i > P.E) {
+            atomicOr(&P.st->err, UERR_SPAN);
+            j = i + P.E;   // keep the ring consistent; the call fails
+        }
+        relax(j, b + P.unk, ((uint32_t)(j - i) << 24) | kUnkTid);
+    };
+    for (;;) {
+        if (node < 0) {
+            if (i >= to) break;
+            const uint32_t si = (uint32_t)i & (R - 1);
+            b = best[si];
+            const uint32_t bp = bk[si];
+            best[si] = kNeg;
+            bk[si] = 0;
+            sink(i, b == kNeg ? 0u : bp);
+            const uint32_t c0 = byte_at(P, i);
+            cont_run = is_cont(c0) ? cont_run + 1 : 0u;
+            if (cont_run >= P.E) atomicOr(&P.st->err, UERR_SPAN);
+            if (b == kNeg || is_cont(c0)) {
+                ++i;
+                continue;
+            }
+            const int4 r = lut[c0];
+            matched = false;
+            if (r.x < 0) {
+                unk_edge();
+                ++i;
+                continue;
+            }
+            node = r.x;
+            y = (uint32_t)r.y;
+            len = 1;
+        }
+        // the node for x[i .. i+len): its token, then one step down
+        const uint64_t j = i + len;
+        const uint32_t nb = j < de ? byte_at(P, j) : 0u;
+        if ((y & kTermBit) && (j == de || !is_cont(nb))) {
+            const Leaf lf = P.leaf[node];
+            relax(j, b + lf.score, (len << 24) | (uint32_t)lf.tid);
+            matched = true;
+        }
+        const uint32_t base = y & ~kTermBit;
+        bool down = j < de && base != 0 && len < P.E;
+        if (down) {
+            const int32_t t = (int32_t)(base + nb);
+            const int2 v = __ldg(P.slot + t);
+            down = v.x == node;
+            if (down) {
+                node = t;
+                y = (uint32_t)v.y;
+                ++len;
+            }
+        }
+        if (!down) {
+            if (!matched) unk_edge();
+            node = -1;
+            ++i;
+        }
+    }
+}
+
+template <int R>
+__device__ __forceinline__ void ring_clear(long long *best, uint32_t *bk) {
+#pragma unroll 8
+    for (int s = 0; s < R; s++) {
+        best[s] = kNeg;
+        bk[s] = 0;
+    }
+}
+
+// First character boundary at or after p (p < de), or de.
+__device__ __forceinline__ uint64_t next_boundary(const UniParams &P, uint64_t p, uint64_t de) {
+    while (p < de && is_cont(byte_at(P, p))) ++p;
+    return p;
+}
+
+// ---------------------------------------------------------- chunk index ---
+
+// chunk_start (exclusive scan of ceil(len / C) per document), the longest
+// document, the chunk count and the text span.
+__global__ void __launch_bounds__(1024) k_uni_index(UniParams P, unsigned long long *chunk_start) {
+    __shared__ unsigned long long s_w[32];
+    __shared__ unsigned long long s_carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s_carry = 0;
+    __syncthreads();
+    unsigned long long longest = 0;
+    for (uint64_t base = 0; base < P.n_docs; base += 1024) {
+        const uint64_t d = base + tid;
+        unsigned long long v = 0;
+        if (d < P.n_docs) {
+            const uint64_t a = P.doc_off[d], b = P.doc_off[d + 1];
+            if (b < a) {
+                atomicOr(&P.st->err, UERR_OOB);
+                P.st->bad_doc = (uint32_t)d;
+            } else {
+                v = (b - a + P.chunk - 1) / P.chunk;
+                longest = max(longest, (unsigned long long)(b - a));
+            }
+        }
+        unsigned long long x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_w[warp] = x;
+        __syncthreads();
+        unsigned long long wpre = 0, tot = 0;
+        for (int w = 0; w < 32; w++) {
+            if (w < warp) wpre += s_w[w];
+            tot += s_w[w];
+        }
+        const unsigned long long carry = s_carry;
+        if (d < P.n_docs) chunk_start[d] = carry + wpre + x - v;
+        __syncthreads();
+        if (tid == 0) s_carry = carry + tot;
+        __syncthreads();
+    }
+    longest = warp_max_u64(longest);
+    if (lane == 0 && longest) atomicMax(&P.st->max_doc, longest);
+    if (tid == 0) {
+        chunk_start[P.n_docs] = s_carry;
+        P.st->n_chunks = s_carry;
+        P.st->span = P.doc_off[P.n_docs] - P.doc_off[0];
+        P.st->text_lo = P.doc_off[0];
+    }
+}
+
+// ------------------------------------------------------------- forward ---
+
+// Where chunk k's run starts: the document start when the chunk lies within
+// G bytes of it (then the run is exact), else cs - G.
+__device__ __forceinline__ uint64_t run_from(const UniParams &P, const UGeo &g) {
+    return (g.cs - g.ds <= P.guard) ? g.ds : g.cs - P.guard;
+}
+
+template <int R>
+__device__ __forceinline__ uint64_t start_run(const UniParams &P, const UGeo &g, uint64_t from, long long *best,
+                                              uint32_t *bk) {
+    ring_clear<R>(best, bk);
+    const uint64_t s0 = from == g.ds ? g.ds : next_boundary(P, from, g.de);
+    best[(uint32_t)s0 & (R - 1)] = 0;
+    bk[(uint32_t)s0 & (R - 1)] = kRoot;
+    return s0;
+}
+
+// The last position of a document is final after the run reaches it.
+template <int R>
+__device__ __forceinline__ void finish_doc(const UniParams &P, const UGeo &g, const long long *best,
+                                           const uint32_t *bk) {
+    const uint32_t s = (uint32_t)g.de & (R - 1);
+    back_at(P, g.de) = best[s] == kNeg ? 0u : bk[s];
+}
+
+template <int R>
+__global__ void __launch_bounds__(kUniThreads) k_uni_fwd(UniParams P, unsigned long long n_chunks) {
+    __shared__ int4 lut[256];
+    load_uni_lut(P, lut);
+    __syncthreads();
+    const unsigned long long k = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= n_chunks) return;
+    const UGeo g = uni_geo(P, k);
+    long long best[R];
+    uint32_t bk[R];
+    const uint64_t from = run_from(P, g);
+    const uint64_t s0 = start_run<R>(P, g, from, best, bk);
+    uint32_t *gb = P.gback + k * (unsigned long long)P.grec;
+    uint32_t cross[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // guard positions with an edge reaching cs or beyond
+    const bool exact = from == g.ds;
+    if (s0 >= g.cs && !exact) atomicOr(&P.st->err, UERR_SPAN);   // a guard of continuation bytes only
+    if (g.first && is_cont(byte_at(P, g.ds))) atomicOr(&P.st->err, UERR_CONT_START);
+    uni_run<R>(
+        P, lut, best, bk, from, g.ce, g.de,
+        [&](uint64_t i, uint32_t bp) {
+            if (i >= g.cs) {
+                if (i != g.ds) back_at(P, i) = bp;
+            } else if (!exact) {
+                gb[i - from] = bp;
+            }
+        },
+        [&](uint64_t i, uint64_t j) {
+            if (i < g.cs && j >= g.cs && !exact) {
+                const uint32_t o = (uint32_t)(i - from);
+                cross[o >> 5] |= 1u << (o & 31);
+            }
+        });
+    if (!exact)
+        for (uint32_t w = 0; w < (P.guard >> 5); w++) gb[P.guard + w] = cross[w];
+    if (g.last) finish_doc<R>(P, g, best, bk);
+}
+
+// Whether chunk k's guard run (its record gr: back pointers over [cs - G,
+// cs), then the crossing bits) agrees with the true back pointers up to a
+// constant at cs.  Only positions with an edge reaching cs or beyond
+// (crossing) influence the chunk.  Every reachable crossing position's chain
+// must step like the true chain until all chains meet at one position z the
+// true recurrence reaches; then their values are the true ones plus one
+// constant.  A position of the last E bytes the run did not reach must be
+// unreachable in truth too (its edges were never explored).
+__device__ bool guard_agrees(const UniParams &P, const uint32_t *gr, uint64_t cs) {
+    const uint64_t from = cs - P.guard;
+    uint32_t mk[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // marked offsets (G <= 256)
+    int n = 0;
+    for (uint32_t o = P.guard - P.E; o < P.guard; o++) {
+        if (gr[o] == 0) {
+            if (back_at(P, from + o) != 0) return false;
+        } else if ((gr[P.guard + (o >> 5)] >> (o & 31)) & 1u) {
+            mk[o >> 5] |= 1u << (o & 31);
+            ++n;
+        }
+    }
+    if (n == 0) return false;
+    for (int o = (int)P.guard - 1; o >= 0; o--) {
+        if (!((mk[o >> 5] >> (o & 31)) & 1u)) continue;
+        if (n == 1) return back_at(P, from + o) != 0;   // z: reachable in truth
+        mk[o >> 5] &= ~(1u << (o & 31));
+        const uint32_t v = gr[o];
+        if (v == kRoot || back_at(P, from + o) != v) return false;
+        const int po = o - (int)(v >> 24);
+        if (po < 0) return false;
+        if ((mk[po >> 5] >> (po & 31)) & 1u) --n;
+        else mk[po >> 5] |= 1u << (po & 31);
+    }
+    return false;
+}
+
+constexpr int kFwdWarps = 8;                 // warps per CTA of the warp-per-chunk kernels
+constexpr int kEdgeStride = 65;              // a lane's edge row: one word per length 0..63, odd stride (banks)
+constexpr uint32_t kUnkNode = 0xFFFFFFFFu;   // edge row entry of an <unk> edge
+constexpr size_t kWarpEdgeBytes = 32 * kEdgeStride * sizeof(uint32_t);
+
+// The recurrence's ring of 64 values and back pointers for spans E <= 63,
+// held by a warp in registers: lane l holds the positions base + l (mod 32),
+// half h those with ((pos - base) >> 5) & 1 == h.
+struct WarpRing {
+    long long r0, r1;
+    uint32_t p0, p1;
+    uint64_t base;
+};
+
+__device__ __forceinline__ void ring_start(WarpRing &R, uint64_t base, uint64_t s0, int lane) {
+    R.r0 = R.r1 = kNeg;
+    R.p0 = R.p1 = 0;
+    R.base = base;
+    const uint64_t o = s0 - base;
+    if (o < 64 && lane == (int)(o & 31)) {
+        if (o >> 5) { R.r1 = 0; R.p1 = kRoot; } else { R.r0 = 0; R.p0 = kRoot; }
+    }
+}
+
+// Back pointer of a final position held by this lane (0 if unreachable).
+__device__ __forceinline__ uint32_t ring_final(const WarpRing &R, uint64_t pos) {
+    const bool hi = ((pos - R.base) >> 5) & 1;
+    const long long v = hi ? R.r1 : R.r0;
+    return v == kNeg ? 0u : (hi ? R.p1 : R.p0);
+}
+
+// One warp's edges in shared memory: row l (lane l's position), entry len =
+// the trie node of the token of that length (kUnkNode for <unk>); a 64-bit
+// mask per lane says which entries are edges.
+struct EdgeBuf {
+    uint32_t *node;
+};
+
+// The recurrence over positions [from, to) of a document ending at de, by one
+// warp ((from - base) a multiple of 32), 32 positions at a time.  Walk: every
+// lane walks the trie from its position (reachable or not) and records its
+// edges by length in shared memory, with a 64-bit mask of their lengths; cross(m, bits) receives, per batch m, which positions have
+// an edge reaching cs or beyond.  Recurrence: the batch's positions in order;
+// the value of source s comes from its owner lane, and every lane relaxes the
+// (at most two) positions among the next 63 that it owns, through s's edge of
+// that length.  sink(q, bp) receives every final position.
+template <typename Sink, typename Cross>
+__device__ void warp_dp(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRing &R, uint64_t from,
+                        uint64_t to, uint64_t de, uint64_t cs, Sink sink, Cross cross) {
+    const int lane = threadIdx.x & 31;
+    uint32_t *row = eb.node + lane * kEdgeStride;
+    for (uint64_t b0 = from; b0 < to; b0 += 32) {
+        const uint32_t m = (uint32_t)((b0 - R.base) >> 5);
+        const uint64_t q = b0 + lane;
+        unsigned long long mask = 0;
+        bool crossing = false;
+        if (q < to) {
+            const uint32_t c0 = byte_at(P, q);
+            if (!is_cont(c0)) {
+                const int4 r = lut[c0];
+                if (r.x >= 0) {
+                    int32_t node = r.x;
+                    uint32_t y = (uint32_t)r.y;
+                    uint32_t len = 1;
+                    for (;;) {
+                        const uint64_t j = q + len;
+                        const uint32_t nb = j < de ? byte_at(P, j) : 0u;
+                        if ((y & kTermBit) && (j == de || !is_cont(nb))) {
+                            row[len] = (uint32_t)node;
+                            mask |= 1ull << len;
+                            crossing |= j >= cs;
+                        }
+                        const uint32_t base = y & ~kTermBit;
+                        if (j >= de || base == 0 || len >= P.E) break;
+                        const int32_t t = (int32_t)(base + nb);
+                        const int2 v = __ldg(P.slot + t);
+                        if (v.x != node) break;
+                        node = t;
+                        y = (uint32_t)v.y;
+                        ++len;
+                    }
+                }
+                if (mask == 0) {   // <unk> to the next character boundary
+                    uint64_t j = q + 1;
+                    while (j < de && is_cont(byte_at(P, j)) && j - q <= P.E) ++j;
+                    if (j - q > P.E) {
+                        atomicOr(&P.st->err, UERR_SPAN);
+                        j = q + P.E;
+                    }
+                    row[j - q] = kUnkNode;
+                    mask = 1ull << (j - q);
+                    crossing = j >= cs;
+                }
+            }
+        }
+        cross((uint32_t)((b0 - from) >> 5), __ballot_sync(kFull, crossing && q < cs));
+        __syncwarp();
+        const uint32_t h = m & 1u;
+        uint32_t fin = 0;
+        const uint32_t nsrc = (uint32_t)(to - b0 < 32 ? to - b0 : 32);
+        for (uint32_t s = 0; s < nsrc; s++) {
+            const long long b = __shfl_sync(kFull, h ? R.r1 : R.r0, s);
+            const uint32_t bp = __shfl_sync(kFull, h ? R.p1 : R.p0, s);
+            const unsigned long long M = __shfl_sync(kFull, mask, s);
+            if (lane == (int)s) {   // position b0 + s is final: free its slot
+                fin = b == kNeg ? 0u : bp;
+                if (h) { R.r1 = kNeg; R.p1 = 0; } else { R.r0 = kNeg; R.p0 = 0; }
+            }
+            if (b == kNeg || M == 0) continue;
+            uint32_t o = ((uint32_t)lane - s) & 31u;
+            if (o == 0) o = 32;
+#pragma unroll
+            for (int u = 0; u < 2; u++, o += 32) {
+                if (o > 63 || !((M >> o) & 1ull)) continue;
+                const uint32_t nd = eb.node[s * kEdgeStride + o];
+                long long sc;
+                uint32_t nbp;
+                if (nd == kUnkNode) {
+                    sc = P.unk;
+                    nbp = (o << 24) | kUnkTid;
+                } else {
+                    const Leaf lf = P.leaf[nd];
+                    sc = lf.score;
+                    nbp = (o << 24) | (uint32_t)lf.tid;
+                }
+                const long long cand = b + sc;
+                if ((((32u * m + s + o) >> 5) & 1u) != 0u) {
+                    if (cand > R.r1) { R.r1 = cand; R.p1 = nbp; }
+                } else {
+                    if (cand > R.r0) { R.r0 = cand; R.p0 = nbp; }
+                }
+            }
+        }
+        __syncwarp();
+        if (q < to) sink(q, fin);
+    }
+}
+
+// Warp-per-chunk speculative forward run (spans E <= 63): k_uni_fwd's work,
+// one warp per chunk.
+__global__ void __launch_bounds__(kFwdWarps * 32) k_uni_fwd_warp(UniParams P, unsigned long long n_chunks) {
+    __shared__ int4 lut[256];
+    extern __shared__ uint32_t s_nodes[];   // kFwdWarps edge tables
+    load_uni_lut(P, lut);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const unsigned long long k = (unsigned long long)blockIdx.x * kFwdWarps + w;
+    if (k >= n_chunks) return;
+    const UGeo g = uni_geo(P, k);
+    const uint64_t from = run_from(P, g);
+    const bool exact = from == g.ds;
+    if (g.first && lane == 0 && is_cont(byte_at(P, g.ds))) atomicOr(&P.st->err, UERR_CONT_START);
+    const uint64_t s0 = exact ? g.ds : next_boundary(P, from, g.de);
+    if (!exact && (s0 >= g.cs || s0 - from >= 64) && lane == 0) atomicOr(&P.st->err, UERR_SPAN);
+    WarpRing R;
+    ring_start(R, from, s0, lane);
+    uint32_t *gb = P.gback + k * (unsigned long long)P.grec;
+    const EdgeBuf eb{s_nodes + w * 32 * kEdgeStride};
+    warp_dp(
+        P, lut, eb, R, from, g.ce, g.de, g.cs,
+        [&](uint64_t q, uint32_t bp) {
+            if (q >= g.cs) {
+                if (q != g.ds) back_at(P, q) = bp;
+            } else if (!exact) {
+                gb[q - from] = bp;
+            }
+        },
+        [&](uint32_t m, unsigned bits) {
+            if (!exact && m < (P.guard >> 5) && lane == 0) gb[P.guard + m] = bits;
+        });
+    if (g.last && lane == (int)((g.de - from) & 31)) back_at(P, g.de) = ring_final(R, g.de);
+}
+
+__global__ void __launch_bounds__(256) k_uni_check(UniParams P, unsigned long long n_chunks) {
+    const unsigned long long k = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= n_chunks) return;
+    const UGeo g = uni_geo(P, k);
+    if (g.cs - g.ds <= P.guard) return;   // exact run
+    if (!guard_agrees(P, P.gback + k * (unsigned long long)P.grec, g.cs)) {
+        const uint32_t old = atomicOr(P.fflag + (k >> 5), 1u << (k & 31));
+        P.st->any_fflag = 1u;
+        if (!((old >> (k & 31)) & 1u)) {   // not listed yet (an overflowed run lists itself)
+            const uint32_t i = atomicAdd(&P.st->flist_len, 1u);
+            if (i < P.flist_cap) P.flist[i] = (uint32_t)k;
+        }
+    }
+}
+
+__device__ __forceinline__ bool flag_bit(const uint32_t *flag, unsigned long long k) {
+    return (flag[k >> 5] >> (k & 31)) & 1u;
+}
+
+// Next set bit of a chunk bitmap in [k, end) (end if none); one warp scans
+// 32 words per step, all lanes get the answer.
+__device__ __forceinline__ unsigned long long warp_next_flag(const uint32_t *flag, unsigned long long k,
+                                                             unsigned long long end, int lane) {
+    while (k < end) {
+        const unsigned long long w0 = k >> 5;
+        const unsigned long long w = w0 + lane;
+        uint32_t bits = (w << 5) < end ? flag[w] : 0u;
+        if (lane == 0) bits &= ~0u << (k & 31);
+        if (((w + 1) << 5) > end) bits &= (end & 31) ? ((1u << (end & 31)) - 1u) : ~0u;
+        const unsigned m = __ballot_sync(kFull, bits != 0);
+        if (m) {
+            const int l = __ffs(m) - 1;
+            const uint32_t b = __shfl_sync(kFull, bits, l);
+            return ((w0 + l) << 5) + (__ffs(b) - 1);
+        }
+        k = (w0 + 32) << 5;
+    }
+    return end;
+}
+
+// Previous set bit of a chunk bitmap in [begin, k] (or ~0 if none).
+__device__ __forceinline__ unsigned long long warp_prev_flag(const uint32_t *flag, long long k, long long begin,
+                                                             int lane) {
+    while (k >= begin) {
+        const long long w0 = k >> 5;
+        const long long w = w0 - lane;
+        uint32_t bits = (w >= 0 && ((w << 5) + 31) >= begin) ? flag[w] : 0u;
+        if (lane == 0 && (k & 31) != 31) bits &= (2u << (k & 31)) - 1u;
+        if (w >= 0 && (w << 5) < begin) bits &= ~0u << (begin & 31);
+        const unsigned m = __ballot_sync(kFull, bits != 0);
+        if (m) {
+            const int l = __ffs(m) - 1;
+            const uint32_t b = __shfl_sync(kFull, bits, l);
+            return (unsigned long long)(((w0 - l) << 5) + (31 - __clz(b)));
+        }
+        k = ((w0 - 32) << 5) + 31;
+    }
+    return ~0ull;
+}
+
+// One warp per document; lane 0 does the runs.  For each flagged chunk f (in
+// order) the recurrence is re-run from chunk f-1's start -- f-1 is correct:
+// it passed its check, or the previous chain ended on it -- through chunk f
+// and on through the chunks after it until one passes its check against the
+// repaired back pointers (or the document ends).
+template <int R>
+__global__ void __launch_bounds__(128) k_uni_frepair(UniParams P) {
+    __shared__ int4 lut[256];
+    load_uni_lut(P, lut);
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const uint32_t d = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (d >= P.n_docs) return;
+    const unsigned long long c0 = P.chunk_start[d], c1 = P.chunk_start[d + 1];
+    unsigned long long f = warp_next_flag(P.fflag, c0, c1, lane);
+    uint32_t reruns = 0;
+    while (f < c1) {
+        unsigned long long m = f;
+        if (lane == 0) {
+            long long best[R];
+            uint32_t bk[R];
+            // the state at f's start: from f-1's run start, or exact from the
+            // document start when f lies within G bytes of it
+            const UGeo gf = uni_geo(P, f);
+            const UGeo gp = gf.cs - gf.ds <= P.guard ? gf : uni_geo(P, f - 1);
+            const uint64_t from = run_from(P, gp);
+            start_run<R>(P, gp, from, best, bk);
+            uni_run<R>(P, lut, best, bk, from, gf.cs, gf.de, [](uint64_t, uint32_t) {}, [](uint64_t, uint64_t) {});
+            for (;;) {
+                const UGeo g = uni_geo(P, m);
+                uni_run<R>(
+                    P, lut, best, bk, g.cs, g.ce, g.de, [&](uint64_t i, uint32_t bp) {
+                        if (i != g.ds) back_at(P, i) = bp;
+                    },
+                    [](uint64_t, uint64_t) {});
+                ++reruns;
+                ++m;
+                if (g.last) {
+                    finish_doc<R>(P, g, best, bk);
+                    break;
+                }
+                if (g.ce - g.ds <= P.guard || guard_agrees(P, P.gback + m * (unsigned long long)P.grec, g.ce))
+                    break;
+            }
+        }
+        m = __shfl_sync(kFull, m, 0);
+        f = warp_next_flag(P.fflag, m + 1, c1, lane);   // chunk m is correct now
+    }
+    if (lane == 0 && reruns) atomicAdd(&P.st->fwd_repairs, reruns);
+}
+
+// The state at flagged chunk f's start: f-1's run start (or the document
+// start when f lies within G bytes of it) and the run up to f's start.
+__device__ __forceinline__ void warp_prefix(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRing &R,
+                                            const UGeo &gf, unsigned long long f) {
+    const int lane = threadIdx.x & 31;
+    const UGeo gp = gf.cs - gf.ds <= P.guard ? gf : uni_geo(P, f - 1);
+    const uint64_t from = run_from(P, gp);
+    ring_start(R, from, from == gp.ds ? gp.ds : next_boundary(P, from, gp.de), lane);
+    warp_dp(P, lut, eb, R, from, gf.cs, gf.de, 0, [](uint64_t, uint32_t) {}, [](uint32_t, unsigned) {});
+}
+
+// Run chunk g (its start state in R), writing its true back pointers.
+__device__ __forceinline__ void warp_chunk(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRing &R,
+                                           const UGeo &g) {
+    warp_dp(
+        P, lut, eb, R, g.cs, g.ce, g.de, 0,
+        [&](uint64_t q, uint32_t bp) {
+            if (q != g.ds) back_at(P, q) = bp;
+        },
+        [](uint32_t, unsigned) {});
+    if (g.last && (int)(threadIdx.x & 31) == (int)((g.de - R.base) & 31)) back_at(P, g.de) = ring_final(R, g.de);
+    __syncwarp();
+}
+
+// Whether chunk m + 1 (which starts where g ends) is right given the true
+// back pointers before it; lane 0 checks, every lane gets the answer.
+__device__ __forceinline__ bool warp_next_ok(const UniParams &P, const UGeo &g, unsigned long long m) {
+    bool ok = false;
+    if ((threadIdx.x & 31) == 0)
+        ok = g.ce - g.ds <= P.guard || guard_agrees(P, P.gback + (m + 1) * (unsigned long long)P.grec, g.ce);
+    return __shfl_sync(kFull, ok, 0);
+}
+
+// Parallel repair (spans E <= 63): one warp per listed flagged chunk f re-runs
+// f from f-1's run start and writes f's back pointers -- right whenever f-1
+// is -- and records in okn whether f + 1 then passes its check.
+__global__ void __launch_bounds__(kFwdWarps * 32) k_uni_fix_a(UniParams P) {
+    __shared__ int4 lut[256];
+    extern __shared__ uint32_t s_nodes[];
+    load_uni_lut(P, lut);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t n = min(P.st->flist_len, P.flist_cap);
+    const EdgeBuf eb{s_nodes + w * 32 * kEdgeStride};
+    for (uint32_t i = blockIdx.x * kFwdWarps + w; i < n; i += gridDim.x * kFwdWarps) {
+        const unsigned long long f = P.flist[i];
+        const UGeo gf = uni_geo(P, f);
+        WarpRing R;
+        warp_prefix(P, lut, eb, R, gf, f);
+        warp_chunk(P, lut, eb, R, gf);
+        const bool ok = gf.last || warp_next_ok(P, gf, f);
+        if (ok && lane == 0) atomicOr(P.okn + (f >> 5), 1u << (f & 31));
+    }
+}
+
+// Sequential repair per document (spans E <= 63), one warp per document, in
+// order over the flagged chunks.  Flagged chunk f was repaired by k_uni_fix_a
+// from f-1's state, which is right here (everything before f is).  If okn
+// says f + 1 passes against f's new back pointers and f + 1 is not flagged
+// itself, nothing is left to do.  Otherwise the warp re-runs from f's state
+// through the chunks after f until one passes its check and kept its own
+// run's back pointers (k_uni_fix_a rewrote every listed chunk).
+__global__ void __launch_bounds__(128) k_uni_frepair_warp(UniParams P) {
+    __shared__ int4 lut[256];
+    extern __shared__ uint32_t s_nodes[];   // 4 edge tables
+    load_uni_lut(P, lut);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t d = blockIdx.x * 4 + w;
+    if (d >= P.n_docs) return;
+    const EdgeBuf eb{s_nodes + w * 32 * kEdgeStride};
+    const unsigned long long c0 = P.chunk_start[d], c1 = P.chunk_start[d + 1];
+    unsigned long long f = warp_next_flag(P.fflag, c0, c1, lane);
+    uint32_t reruns = 0;
+    while (f < c1) {
+        const UGeo gf = uni_geo(P, f);
+        const bool fast = flag_bit(P.okn, f) && (gf.last || !flag_bit(P.fflag, f + 1));
+        unsigned long long m = f + 1;
+        if (!fast) {
+            WarpRing R;
+            warp_prefix(P, lut, eb, R, gf, f);
+            m = f;
+            for (;;) {
+                const UGeo g = uni_geo(P, m);
+                warp_chunk(P, lut, eb, R, g);
+                ++reruns;
+                if (g.last || (!flag_bit(P.fflag, m + 1) && warp_next_ok(P, g, m))) break;
+                ++m;
+            }
+            ++m;
+        }
+        f = warp_next_flag(P.fflag, m, c1, lane);   // chunks before m are right
+    }
+    if (lane == 0 && reruns) atomicAdd(&P.st->fwd_repairs, reruns);
+}
+
+// ------------------------------------------------------------ backtrack ---
+
+// Walk the back-pointer chain of chunk g from position x (>= ce, on the
+// chain of a reachable position): tokens starting in [cs, ce) are counted
+// (and written through put, last first); returns the chain's last position
+// at or after cs (the document start when the chunk is the first).
+template <typename Put>
+__device__ __forceinline__ uint64_t walk_chunk(const UniParams &P, const UGeo &g, uint64_t x, uint32_t *cnt,
+                                               Put put) {
+    uint32_t c = 0;
+    while (x != g.ds) {
+        const uint32_t v = back_at(P, x);
+        const uint64_t nx = x - (v >> 24);
+        if ((v >> 24) == 0 || nx < g.cs) break;   // unreachable or a run start: only on rejected input
+        put(c, v);
+        ++c;
+        x = nx;
+    }
+    *cnt = c;
+    return x;
+}
+
+__global__ void __launch_bounds__(256) k_uni_bspec(UniParams P, unsigned long long n_chunks) {
+    const unsigned long long k = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= n_chunks) return;
+    const UGeo g = uni_geo(P, k);
+    uint64_t x = g.de;
+    if (!g.last) {
+        x = min(g.ce + P.ahead, g.de);
+        while (x > g.ce && back_at(P, x) == 0) --x;
+        // down the chain to its last position at or after ce
+        for (;;) {
+            const uint32_t v = back_at(P, x);
+            if ((v >> 24) == 0) break;
+            const uint64_t nx = x - (v >> 24);
+            if (nx < g.ce) break;
+            x = nx;
+        }
+    }
+    uint32_t c;
+    const uint64_t b = walk_chunk(P, g, x, &c, [](uint32_t, uint32_t) {});
+    P.sx[k] = (uint32_t)(x - g.cs);
+    P.bot[k] = (uint32_t)(b - g.cs);
+    P.count[k] = c;
+}
+
+// chunk k's chain is the true path when it passes through the true sx, the
+// next chunk's bot (true once that chunk is)
+__global__ void __launch_bounds__(256) k_uni_bcheck(UniParams P, unsigned long long n_chunks) {
+    const unsigned long long k = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k + 1 >= n_chunks) return;
+    const UGeo g = uni_geo(P, k);
+    if (g.last) return;
+    if ((uint64_t)P.bot[k + 1] + P.chunk != (uint64_t)P.sx[k]) {   // both relative to their chunk starts
+        atomicOr(P.bflag + (k >> 5), 1u << (k & 31));
+        P.st->any_bflag = 1u;
+    }
+}
+
+// Parallel re-walk: one thread per flagged chunk k walks it again from the
+// next chunk's bot -- right whenever that chunk is -- and records in okp
+// whether the chunk before k is then right too (not flagged, and its sx is
+// k's new bot).
+__global__ void __launch_bounds__(256) k_uni_bfix_a(UniParams P, unsigned long long n_chunks) {
+    const unsigned long long k = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k + 1 >= n_chunks || !flag_bit(P.bflag, k)) return;
+    const UGeo g = uni_geo(P, k);
+    const uint64_t x = g.ce + P.bot[k + 1];
+    uint32_t c;
+    const uint64_t b = walk_chunk(P, g, x, &c, [](uint32_t, uint32_t) {});
+    P.sx[k] = (uint32_t)(x - g.cs);
+    P.bot[k] = (uint32_t)(b - g.cs);
+    P.count[k] = c;
+    if (!g.first && !flag_bit(P.bflag, k - 1) && (uint64_t)P.bot[k] + P.chunk == (uint64_t)P.sx[k - 1])
+        atomicOr(P.okp + (k >> 5), 1u << (k & 31));
+}
+
+// One warp per document, right to left over the flagged chunks (everything
+// to the right of the current one is right).  A flagged chunk k whose
+// successor is not flagged was re-walked from a right bot by k_uni_bfix_a;
+// with okp the chunk before it is right as well.  Otherwise k is walked again
+// and so is every chunk before it until one that is not flagged and whose sx
+// equals the new bot.
+__global__ void __launch_bounds__(128) k_uni_brepair(UniParams P) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t d = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (d >= P.n_docs) return;
+    const long long c0 = (long long)P.chunk_start[d], c1 = (long long)P.chunk_start[d + 1];
+    if (c1 - c0 < 2) return;
+    unsigned long long f = warp_prev_flag(P.bflag, c1 - 2, c0, lane);
+    uint32_t rewalks = 0;
+    while (f != ~0ull) {
+        long long k = (long long)f;
+        const bool fast = !flag_bit(P.bflag, (unsigned long long)k + 1) && flag_bit(P.okp, (unsigned long long)k);
+        if (!fast) {
+            if (lane == 0) {
+                for (;;) {
+                    const UGeo g = uni_geo(P, (unsigned long long)k);
+                    const uint64_t x = g.ce + P.bot[k + 1];   // the next chunk starts at ce
+                    uint32_t c;
+                    const uint64_t b = walk_chunk(P, g, x, &c, [](uint32_t, uint32_t) {});
+                    P.sx[k] = (uint32_t)(x - g.cs);
+                    P.bot[k] = (uint32_t)(b - g.cs);
+                    P.count[k] = c;
+                    ++rewalks;
+                    if (k == c0 || (!flag_bit(P.bflag, (unsigned long long)k - 1) &&
+                                    (uint64_t)P.bot[k] + P.chunk == (uint64_t)P.sx[k - 1]))
+                        break;
+                    --k;
+                }
+            }
+            k = __shfl_sync(kFull, k, 0);
+        }
+        // chunk k - 1 is right now (or k is the document's first chunk)
+        f = (k - 2 >= c0) ? warp_prev_flag(P.bflag, k - 2, c0, lane) : ~0ull;
+    }
+    if (lane == 0 && rewalks) atomicAdd(&P.st->bwd_repairs, rewalks);
+}
+
+// ----------------------------------------------------------------- emit ---
+
+constexpr int kUniEmitThreads = 256;
+
+// Exclusive scan of the chunk counts: tiles of 256 chunks taken in ticket
+// order, each publishing its sum and then its inclusive prefix, the next
+// looking back over 32 predecessors per round (bounded wait).  Then every
+// chunk walks its chain from its true sx and writes its ids, last first.
+__global__ void __launch_bounds__(kUniEmitThreads) k_uni_emit(UniParams P, unsigned long long n_chunks) {
+    __shared__ uint32_t s_w[kUniEmitThreads / 32];
+    __shared__ unsigned long long s_tile, s_off;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned long long ntiles = (n_chunks + kUniEmitThreads - 1) / kUniEmitThreads;
+    if (tid == 0) s_tile = atomicAdd(&P.st->ticket, 1u);
+    __syncthreads();
+    const unsigned long long t = s_tile;
+    if (t >= ntiles) return;
+    const unsigned long long k = t * kUniEmitThreads + tid;
+    const bool live = k < n_chunks;
+    const uint32_t cnt = live ? P.count[k] : 0u;
+    const uint32_t incl = warp_incl_sum(cnt, lane);
+    if (lane == 31) s_w[warp] = incl;
+    __syncthreads();
+    uint32_t wpre = 0, tsum = 0;
+#pragma unroll
+    for (int w = 0; w < kUniEmitThreads / 32; w++) {
+        if (w < warp) wpre += s_w[w];
+        tsum += s_w[w];
+    }
+    if (warp == 0) {
+        unsigned long long off = 0;
+        if (t > 0) {
+            if (lane == 0) st_relaxed(P.status + t, 1ull | ((unsigned long long)tsum << 2));
+            long long jhi = (long long)t - 1;
+            unsigned spins = 0;
+            for (;;) {
+                const long long j = jhi - lane;
+                const unsigned long long w = (j >= 0) ? ld_l2(P.status + j) : 2ull;
+                const uint32_t fl = (uint32_t)(w & 3ull);
+                const unsigned incl_m = __ballot_sync(kFull, fl == 2);
+                const int li = incl_m ? __ffs(incl_m) - 1 : 31;
+                const unsigned need = (li == 31) ? kFull : ((2u << li) - 1u);
+                if (__ballot_sync(kFull, fl == 0) & need) {
+                    if (++spins > kUniSpinLimit) {
+                        if (lane == 0) atomicOr(&P.st->err, UERR_TIMEOUT);
+                        break;
+                    }
+                    if (spins > 32) __nanosleep(64);
+                    continue;
+                }
+                unsigned long long v = (lane <= li) ? (w >> 2) : 0ull;
+#pragma unroll
+                for (int dd = 16; dd > 0; dd >>= 1) v += __shfl_xor_sync(kFull, v, dd);
+                off += v;
+                if (incl_m) break;
+                jhi -= 32;
+            }
+        }
+        if (lane == 0) {
+            st_relaxed(P.status + t, 2ull | ((off + tsum) << 2));
+            if (t == ntiles - 1) P.st->total = off + tsum;
+            s_off = off;
+        }
+    }
+    __syncthreads();
+    if (!live) return;
+    const unsigned long long o = s_off + wpre + incl - cnt;
+    P.prefix[k] = o;
+    const UGeo g = uni_geo(P, k);
+    const unsigned long long last = o + cnt - 1;
+    uint32_t c;
+    walk_chunk(P, g, g.cs + P.sx[k], &c, [&](uint32_t r, uint32_t v) {
+        const unsigned long long w = last - r;
+        if (w < P.cap) {
+            const uint32_t id = v & 0x00FFFFFFu;
+            P.ids[w] = id == kUnkTid ? P.unk_id : (int32_t)id;
+        }
+    });
+}
+
+__global__ void k_uni_docoff(UniParams P, unsigned long long n_chunks) {
+    const uint64_t d = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
+    if (d > P.n_docs) return;
+    const unsigned long long c = P.chunk_start[d];
+    P.id_off[d] = c < n_chunks ? P.prefix[c] : P.st->total;
+}
+
+// Per trie slot: the score (fixed-point units) and id of its token.
+__global__ void k_uni_leaf(const int32_t *tid, unsigned long long n_slots, const long long *units, Leaf *leaf) {
+    const unsigned long long s = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x;
+    if (s >= n_slots) return;
+    const int32_t t = tid[s];
+    Leaf l;
+    l.score = t >= 0 ? units[t] : 0;
+    l.tid = t;
+    l.pad = 0;
+    leaf[s] = l;
+}
+
+__global__ void k_uni_copy(const uint8_t *src, uint8_t *dst, uint32_t n) {
+    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
+}
+
+}  // namespace
+}  // namespace bpe
+
+using namespace bpe;
+
+namespace {
+// Smallest q >= 0 with v * 2^q an integer (v finite): v = M * 2^(e - 53)
+// with M the 53-bit mantissa; its trailing zeros lower the need.
+int fraction_bits(double v) {
+    if (v == 0.0) return 0;
+    int e = 0;
+    const double m = std::frexp(std::fabs(v), &e);   // |v| = m * 2^e, m in [0.5, 1)
+    const uint64_t M = (uint64_t)std::ldexp(m, 53);
+    int tz = 0;
+    while (!((M >> tz) & 1ull)) ++tz;
+    return std::max(0, 53 - tz - e);
+}
+}  // namespace
+
+extern "C" int unigram_create(bpe_ctx *ctx, const bpe_trie *trie, const double *h_scores, uint32_t n_scores,
+                              int32_t unk_id, double unk_score, bpe_unigram **out) {
+    if (!ctx) return BPE_ERR_INVALID_ARG;
+    if (!trie || !out || (n_scores && !h_scores)) return fail(ctx, BPE_ERR_INVALID_ARG, "unigram_create: null pointer");
+    *out = nullptr;
+    if (trie->device != ctx->device) return fail(ctx, BPE_ERR_INVALID_ARG, "unigram_create: trie on another device");
+    if (n_scores != trie->n_tok)
+        return fail(ctx, BPE_ERR_INVALID_ARG, "unigram_create: %u scores for %u tokens", n_scores, trie->n_tok);
+    if (trie->n_tok > 0xFFFFFEu) return fail(ctx, BPE_ERR_INVALID_ARG, "unigram_create: more than 16,777,214 tokens");
+    if (trie->max_len > 255) return fail(ctx, BPE_ERR_INVALID_ARG, "unigram_create: a token longer than 255 bytes");
+    int q = 0;
+    for (uint32_t t = 0; t <= n_scores; t++) {
+        const double v = t < n_scores ? h_scores[t] : unk_score;
+        if (!std::isfinite(v)) return fail(ctx, BPE_ERR_INVALID_ARG, "unigram_create: score %u is not finite", t);
+        q = std::max(q, fraction_bits(v));
+    }
+    if (q > 62) return fail(ctx, BPE_ERR_INVALID_ARG, "unigram_create: scores need %d fraction bits (at most 62)", q);
+    std::vector<long long> units(std::max<uint32_t>(n_scores, 1));
+    long long max_abs = 0;
+    const double lim = std::ldexp(1.0, 62);
+    for (uint32_t t = 0; t <= n_scores; t++) {
+        const double v = std::ldexp(t < n_scores ? h_scores[t] : unk_score, q);
+        if (std::fabs(v) >= lim)
+            return fail(ctx, BPE_ERR_INVALID_ARG, "unigram_create: score %u too large for 2^-%d units", t, q);
+        const long long u = (long long)v;
+        max_abs = std::max(max_abs, u < 0 ? -u : u);
+        if (t < n_scores) units[t] = u;
+    }
+    BPE_CUDA(ctx, cudaSetDevice(ctx->device), "cudaSetDevice");
+    bpe_unigram *m = new bpe_unigram;
+    m->ctx = ctx;
+    m->trie = trie;
+    m->device = ctx->device;
+    m->unk_id = unk_id;
+    m->unk = (long long)std::ldexp(unk_score, q);
+    m->max_abs = max_abs;
+    m->q = q;
+    m->span = trie->max_len <= 63 ? 63u : 255u;
+    void *d_units = nullptr;
+    cudaError_t e = cudaMalloc(&m->d_leaf, sizeof(Leaf) * std::max<uint64_t>(trie->n_slots, 1));
+    if (e == cudaSuccess) e = cudaMalloc(&d_units, sizeof(long long) * units.size());
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(d_units, units.data(), sizeof(long long) * units.size(), cudaMemcpyHostToDevice, ctx->stream);
+    if (e == cudaSuccess && trie->n_slots) {
+        k_uni_leaf<<<(unsigned)((trie->n_slots + 255) / 256), 256, 0, ctx->stream>>>(
+            trie->d_tid, trie->n_slots, (const long long *)d_units, (Leaf *)m->d_leaf);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+    if (d_units) cudaFree(d_units);
+    if (e != cudaSuccess) {
+        unigram_free(m);
+        return cuda_fail(ctx, e, "unigram_create");
+    }
+    *out = m;
+    return BPE_OK;
+}
+
+extern "C" void unigram_free(bpe_unigram *model) {
+    if (!model) return;
+    if (model->d_leaf) cudaFree(model->d_leaf);
+    delete model;
+}
+
+extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint8_t *d_bytes,
+                              const uint64_t *d_doc_off, uint32_t n_docs, int32_t *d_ids_out, uint64_t ids_capacity,
+                              uint64_t *d_id_off_out, uint64_t *n_ids) {
+    if (!ctx) return BPE_ERR_INVALID_ARG;
+    if (!model || !n_ids) return fail(ctx, BPE_ERR_INVALID_ARG, "unigram_encode: null model or n_ids");
+    if (model->device != ctx->device) return fail(ctx, BPE_ERR_INVALID_ARG, "unigram_encode: model on another device");
+    if (n_docs && (!d_doc_off || !d_bytes)) return fail(ctx, BPE_ERR_INVALID_ARG, "unigram_encode: null input");
+    if (ids_capacity && !d_ids_out) return fail(ctx, BPE_ERR_INVALID_ARG, "unigram_encode: null ids with capacity");
+    BPE_CUDA(ctx, cudaSetDevice(ctx->device), "cudaSetDevice");
+    cudaStream_t s = ctx->stream;
+    stats_reset(ctx);
+    *n_ids = 0;
+    if (n_docs == 0) {
+        if (d_id_off_out) BPE_CUDA(ctx, cudaMemsetAsync(d_id_off_out, 0, 8, s), "id_off");
+        BPE_CUDA(ctx, cudaStreamSynchronize(s), "sync");
+        return BPE_OK;
+    }
+    const bpe_trie *trie = model->trie;
+    const uint32_t R = model->span == 63 ? 64u : 256u;
+    const uint32_t C = std::max<uint32_t>(ctx->uni_chunk ? (uint32_t)ctx->uni_chunk : kUniDefaultChunk, 256u);
+    int rc;
+    void *cstart, *state, *pin;
+    if ((rc = ensure(ctx, S_UNI_START, ((uint64_t)n_docs + 1) * 8, &cstart)) ||
+        (rc = ensure(ctx, S_UNI_STATE, sizeof(UniState), &state)) || (rc = ensure_pinned(ctx, sizeof(UniState), &pin)))
+        return rc;
+    UniState *h = (UniState *)pin;
+    const bool profile = ctx->profile != 0;
+    if (profile && (rc = ensure_events(ctx, 4))) return rc;
+
+    UniParams P{};
+    P.bytes = d_bytes;
+    P.doc_off = d_doc_off;
+    P.n_docs = n_docs;
+    P.chunk = C;
+    P.guard = R == 64 ? 128u : 256u;
+    P.grec = P.guard + P.guard / 32;
+    P.E = model->span;
+    P.ahead = R;
+    P.chunk_start = (const unsigned long long *)cstart;
+    P.slot = trie->d_slot;
+    P.root = trie->d_root;
+    P.leaf = (const Leaf *)model->d_leaf;
+    P.unk = model->unk;
+    P.unk_id = model->unk_id;
+    P.ids = d_ids_out;
+    P.cap = ids_capacity;
+    P.st = (UniState *)state;
+
+    BPE_CUDA(ctx, cudaMemsetAsync(state, 0, sizeof(UniState), s), "state clear");
+    k_uni_index<<<1, 1024, 0, s>>>(P, (unsigned long long *)cstart);
+    BPE_CUDA(ctx, cudaGetLastError(), "k_uni_index launch");
+    k_uni_copy<<<1, 128, 0, s>>>((const uint8_t *)state, (uint8_t *)h, (uint32_t)sizeof(UniState));
+    BPE_CUDA(ctx, cudaStreamSynchronize(s), "chunk index sync");
+    if (h->err & UERR_OOB)
+        return fail(ctx, BPE_ERR_INVALID_ARG, "unigram_encode: document offsets descend at document %u", h->bad_doc);
+    const unsigned long long nc = h->n_chunks;
+    if (nc == 0) {
+        if (d_id_off_out) BPE_CUDA(ctx, cudaMemsetAsync(d_id_off_out, 0, ((uint64_t)n_docs + 1) * 8, s), "id_off");
+        BPE_CUDA(ctx, cudaStreamSynchronize(s), "sync");
+        return BPE_OK;
+    }
+    if ((unsigned __int128)h->max_doc * (unsigned __int128)(model->max_abs + 1) >= ((unsigned __int128)1 << 62))
+        return fail(ctx, BPE_ERR_INVALID_ARG,
+                    "unigram_encode: a document of %llu bytes could overflow 64-bit sums of 2^-%d units",
+                    (unsigned long long)h->max_doc, model->q);
+    P.text_lo = h->text_lo;
+    const uint64_t words = (nc + 31) / 32, tiles = (nc + kUniEmitThreads - 1) / kUniEmitThreads;
+    void *back, *gback, *info, *flag, *prefix, *status;
+    if ((rc = ensure(ctx, S_UNI_BACK, (h->span + 1) * 4, &back)) ||
+        (rc = ensure(ctx, S_UNI_GBACK, nc * (uint64_t)P.grec * 4, &gback)) ||
+        (rc = ensure(ctx, S_UNI_CHUNK, nc * 12, &info)) || (rc = ensure(ctx, S_UNI_FLAG, words * 16 + nc * 4, &flag)) ||
+        (rc = ensure(ctx, S_UNI_PREFIX, nc * 8 + ((uint64_t)n_docs + 1) * 8, &prefix)) ||
+        (rc = ensure(ctx, S_UNI_STATUS, tiles * 8, &status)))
+        return rc;
+    P.back = (uint32_t *)back;
+    P.gback = (uint32_t *)gback;
+    P.sx = (uint32_t *)info;
+    P.bot = P.sx + nc;
+    P.count = P.bot + nc;
+    P.fflag = (uint32_t *)flag;
+    P.bflag = P.fflag + words;
+    P.okn = P.bflag + words;
+    P.okp = P.okn + words;
+    P.flist = P.okp + words;
+    P.flist_cap = (uint32_t)std::min<unsigned long long>(nc, 0xFFFFFFFFull);
+    P.prefix = (unsigned long long *)prefix;
+    P.status = (unsigned long long *)status;
+    P.id_off = d_id_off_out ? (unsigned long long *)d_id_off_out : P.prefix + nc;
+    BPE_CUDA(ctx, cudaMemsetAsync(flag, 0, words * 16, s), "flag clear");
+    BPE_CUDA(ctx, cudaMemsetAsync(status, 0, tiles * 8, s), "status clear");
+
+    const unsigned grid_c = (unsigned)((nc + kUniThreads - 1) / kUniThreads);
+    const unsigned grid_c256 = (unsigned)((nc + 255) / 256);
+    const unsigned grid_d = (n_docs + 3) / 4;   // one warp per document
+    if (profile) cudaEventRecord(ctx->events[0], s);
+    const size_t warp_smem = kFwdWarps * kWarpEdgeBytes, rep_smem = 4 * kWarpEdgeBytes;
+    if (R == 64) {
+        BPE_CUDA(ctx, cudaFuncSetAttribute(k_uni_fwd_warp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)warp_smem),
+                 "k_uni_fwd_warp smem");
+        BPE_CUDA(ctx, cudaFuncSetAttribute(k_uni_fix_a, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)warp_smem),
+                 "k_uni_fix_a smem");
+        k_uni_fwd_warp<<<(unsigned)((nc + kFwdWarps - 1) / kFwdWarps), kFwdWarps * 32, warp_smem, s>>>(P, nc);
+    }
+    else k_uni_fwd<256><<<grid_c, kUniThreads, 0, s>>>(P, nc);
+    if (profile) cudaEventRecord(ctx->events[1], s);
+    k_uni_check<<<grid_c256, 256, 0, s>>>(P, nc);
+    if (R == 64) {
+        k_uni_fix_a<<<(unsigned)std::max(1, ctx->sm_count * 3), kFwdWarps * 32, warp_smem, s>>>(P);
+        k_uni_frepair_warp<<<grid_d, 128, rep_smem, s>>>(P);
+    } else {
+        k_uni_frepair<256><<<grid_d, 128, 0, s>>>(P);
+    }
+    k_uni_bspec<<<grid_c256, 256, 0, s>>>(P, nc);
+    k_uni_bcheck<<<grid_c256, 256, 0, s>>>(P, nc);
+    k_uni_bfix_a<<<grid_c256, 256, 0, s>>>(P, nc);
+    k_uni_brepair<<<grid_d, 128, 0, s>>>(P);
+    if (profile) cudaEventRecord(ctx->events[2], s);
+    k_uni_emit<<<(unsigned)tiles, kUniEmitThreads, 0, s>>>(P, nc);
+    if (profile) cudaEventRecord(ctx->events[3], s);
+    k_uni_docoff<<<(unsigned)((n_docs + 1 + 255) / 256), 256, 0, s>>>(P, nc);
+    BPE_CUDA(ctx, cudaGetLastError(), "unigram_encode launch");
+    k_uni_copy<<<1, 128, 0, s>>>((const uint8_t *)state, (uint8_t *)h, (uint32_t)sizeof(UniState));
+    BPE_CUDA(ctx, cudaStreamSynchronize(s), "unigram_encode sync");
+    if (h->err & UERR_CONT_START)
+        return fail(ctx, BPE_ERR_INVALID_ARG, "unigram_encode: a document starts with a UTF-8 continuation byte");
+    if (h->err & UERR_SPAN)
+        return fail(ctx, BPE_ERR_INVALID_ARG,
+                    "unigram_encode: a run of %u continuation bytes needs an edge longer than %u bytes", P.E, P.E);
+    if (h->err & UERR_TIMEOUT) return fail(ctx, BPE_ERR_TIMEOUT, "unigram_encode: look-back wait gave up");
+
+    const uint64_t total = h->total;
+    *n_ids = total;
+    const int a = stats_slot(ctx, "unigram_fwd"), b = stats_slot(ctx, "unigram_fix"), c = stats_slot(ctx, "unigram_emit");
+    ctx->stats.k[a].launches = 1;
+    ctx->stats.k[b].launches = R == 64 ? 7 : 6;
+    ctx->stats.k[c].launches = 1;
+    ctx->stats.k[a].bytes = (double)h->span;
+    ctx->stats.k[b].bytes = (double)h->fwd_repairs * C + (double)h->bwd_repairs;   // chunks re-run, chunks re-walked
+    ctx->stats.k[c].bytes = 4.0 * (double)total;
+    ctx->stats.kernel_launches = R == 64 ? 13 : 12;
+    if (profile) {
+        float x = 0, y = 0, z = 0;
+        cudaEventElapsedTime(&x, ctx->events[0], ctx->events[1]);
+        cudaEventElapsedTime(&y, ctx->events[1], ctx->events[2]);
+        cudaEventElapsedTime(&z, ctx->events[2], ctx->events[3]);
+        ctx->stats.k[a].ms = x;
+        ctx->stats.k[b].ms = y;
+        ctx->stats.k[c].ms = z;
+        cudaGetLastError();
+    }
+    if (total > ids_capacity)
+        return fail(ctx, BPE_ERR_CAPACITY, "unigram_encode: %llu ids exceed the capacity %llu",
+                    (unsigned long long)total, (unsigned long long)ids_capacity);
+    return BPE_OK;
+}

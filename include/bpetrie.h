@@ -1,5 +1,6 @@
 /*
- * bpetrie.h -- byte-level BPE training and greedy trie encoding on one GPU.
+ * bpetrie.h -- byte-level BPE training, greedy trie encoding and Unigram
+ * (Viterbi) encoding on one GPU.
  *
  * C ABI of libbpetrie.so (sm_103a).  Plain pointers and sizes only.
  *
@@ -110,6 +111,8 @@ const char *bpe_last_error(const bpe_ctx *ctx);
  *                          step tests the parent's bit and loads the child's
  *                          base|TERM; built on a trie's first use (n_slots x
  *                          64 bytes, kept until trie_free)
+ *   BPE_OPT_UNI_CHUNK    bytes per chunk of unigram_encode (256 .. 4096, a
+ *                        multiple of 64; 0 = default 512)
  *   BPE_OPT_PERSISTENT   1 = with BPE_MERGE_TWO_PASS, the merge loop runs as one cooperative
  *                        launch per window of merges (all CTAs resident,
  *                        phases separated by grid barriers) instead of a CUDA
@@ -122,7 +125,8 @@ enum {
     BPE_OPT_TRAIN_WORDS = 5,
     BPE_OPT_MERGE = 6,
     BPE_OPT_PERSISTENT = 7,
-    BPE_OPT_TRIE_LAYOUT = 8
+    BPE_OPT_TRIE_LAYOUT = 8,
+    BPE_OPT_UNI_CHUNK = 9
 };
 enum { BPE_TRIE_DOUBLE_ARRAY = 0, BPE_TRIE_BITMAP = 1 };
 enum { BPE_MERGE_TWO_PASS = 0, BPE_MERGE_LOOKBACK = 1, BPE_MERGE_TILES = 2 };
@@ -184,11 +188,13 @@ int bpe_train(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_me
  * child = base[node] + byte, valid when check[child] == node; token id kept
  * in the node) over a vocabulary, and upload it to the context's device.
  * Token t is the byte string h_vocab_bytes[h_vocab_off[t] .. h_vocab_off[t+1]);
- * the id of a token is its index.  Every single byte 0..255 must be a token
- * (byte-level vocabularies always are; greedy matching then never fails);
- * when two tokens have the same bytes the lower id is kept.  Empty strings
- * are ignored.  The trie is usable with any context on the same device.
- * Errors: INVALID_ARG (missing single byte, offsets not ascending), OOM, CUDA. */
+ * the id of a token is its index.  Greedy encoding (trie_encode and the calls
+ * built on it) needs every single byte 0..255 to be a token -- byte-level
+ * vocabularies always are, and greedy matching then never fails -- and rejects
+ * a trie without; Unigram encoding does not.  When two tokens have the same
+ * bytes the lower id is kept.  Empty strings are ignored.  The trie is usable
+ * with any context on the same device.
+ * Errors: INVALID_ARG (offsets not ascending), OOM, CUDA. */
 int trie_build(bpe_ctx *ctx, const uint8_t *h_vocab_bytes, const uint64_t *h_vocab_off,
                uint32_t n_tok, bpe_trie **out);
 
@@ -289,6 +295,47 @@ int trie_encode_host(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *h_bytes,
 int trie_encode_noalloc(const bpe_trie *trie, const uint8_t *d_bytes, const uint64_t *d_doc_off,
                         uint32_t n_docs, int32_t *d_ids_out, uint64_t ids_capacity,
                         uint64_t *d_id_off_out, uint64_t *n_ids, void *cuda_stream);
+
+/* --------------------------------------------------------- Unigram ------ */
+
+/* Unigram (Viterbi) encoding ([UNIGRAM] "Unigram tokenization": the most
+ * likely segmentation, best[j] = max over tokens t = bytes[i..j) of best[i] +
+ * score(t), with best[0] = 0, then a backtrack from the end) over the same
+ * double-array trie.  Per document, exactly as that recurrence states:
+ *   - a position that holds a UTF-8 continuation byte (10xxxxxx) starts no
+ *     token, and a token counts only when it ends at a character boundary
+ *     (the document end or a byte that is not a continuation byte);
+ *   - a reachable position from which no token counts is followed by one
+ *     unk_id spanning to the next character boundary, scored unk_score;
+ *   - on equal scores the path whose last token starts earliest wins (the
+ *     strict comparison of the recurrence, positions taken in order).
+ *
+ * unigram_create: a model bound to ctx's device and to trie (which must
+ * outlive it).  h_scores: trie's n_tok f64 scores (host), one per token id.
+ * The GPU sums scores exactly in 64-bit fixed point: with q the smallest
+ * exponent for which every score and unk_score times 2^q is an integer, q
+ * must be at most 62 and every |score| * 2^q below 2^62 (any float32 value of
+ * magnitude at least 2^-39 qualifies).  Sums are then exact, so the result
+ * equals the recurrence evaluated in f64 whenever that evaluation rounds
+ * nothing.  Errors: INVALID_ARG (bad
+ * pointer, a score that is not finite or not representable as above, more
+ * than 16,777,214 tokens, a token longer than 255 bytes), OOM, CUDA.
+ *
+ * unigram_encode: inputs and outputs as trie_encode (d_doc_off: n_docs+1
+ * ascending offsets; ids_capacity; d_id_off_out nullable; *n_ids = total,
+ * BPE_ERR_CAPACITY with the required size when it exceeds the capacity).
+ * A token or an <unk> span longer than the model's span limit (63 bytes when
+ * the longest token has at most 63 bytes, else 255) returns INVALID_ARG, as
+ * does a document whose length times the largest |score| * 2^q reaches 2^62.
+ * Blocks until done.  Errors: INVALID_ARG, CAPACITY, OOM, TIMEOUT, CUDA.
+ * unigram_free releases the model (NULL is ignored). */
+typedef struct bpe_unigram bpe_unigram;
+int unigram_create(bpe_ctx *ctx, const bpe_trie *trie, const double *h_scores, uint32_t n_scores,
+                   int32_t unk_id, double unk_score, bpe_unigram **out);
+int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint8_t *d_bytes, const uint64_t *d_doc_off,
+                   uint32_t n_docs, int32_t *d_ids_out, uint64_t ids_capacity, uint64_t *d_id_off_out,
+                   uint64_t *n_ids);
+void unigram_free(bpe_unigram *model);
 
 #ifdef __cplusplus
 }

@@ -202,7 +202,8 @@ def substring_vocab(text: np.ndarray, n_tok: int = BATCH_VOCAB_SIZE,
 
 def unigram_scores(n_tok: int, seed: int = UNIGRAM_SCORE_SEED) -> np.ndarray:
     """Seeded synthetic Unigram log-probabilities (float64, one per token):
-    a Zipf law over a random ranking of the tokens, normalised to sum 1."""
+    a Zipf law over a random ranking of the tokens, normalised to sum 1,
+    each value a float32."""
     out = np.empty(max(n_tok, 1), dtype=np.float64)
     if _load().syn_unigram_scores(n_tok, seed, _ptr(out)) != 0:
         raise ValueError("unigram scores need n_tok >= 1")

@@ -306,7 +306,8 @@ double syn_exp_export(double x) { return syn_exp(x); }
 /*
  * Synthetic Unigram log-probabilities for n_tok tokens: a Zipf law over a
  * seeded random ranking, score[t] = ln(1 / ((rank(t) + 1) * H)) with H the
- * harmonic number of n_tok, so that exp(score) sums to 1.  Returns 0 on
+ * harmonic number of n_tok, so that exp(score) sums to 1, each rounded to a
+ * float32 value (the precision Unigram models store scores in).  Returns 0 on
  * success, -1 when n_tok is 0.
  */
 int syn_unigram_scores(uint32_t n_tok, uint64_t seed, double *score) {
@@ -322,7 +323,7 @@ int syn_unigram_scores(uint32_t n_tok, uint64_t seed, double *score) {
     double H = 0.0;
     for (uint32_t k = n_tok; k > 0; k--) H += 1.0 / (double)k;
     const double lnH = syn_ln(H);
-    for (uint32_t t = 0; t < n_tok; t++) score[t] = -(lnH + syn_ln((double)rank[t] + 1.0));
+    for (uint32_t t = 0; t < n_tok; t++) score[t] = (double)(float)-(lnH + syn_ln((double)rank[t] + 1.0));
     free(rank);
     return 0;
 }

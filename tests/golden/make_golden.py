@@ -16,6 +16,10 @@ Workloads (see ``synth`` for the text recipe):
          as large_merges.npy: rows of left, right, count)
   enc    1 GiB text, greedy encode with the vocabulary learned on ``large``
   batch  512 documents, 250,000-token substring vocabulary, per-document ids
+  unigram      the batch documents and vocabulary, Viterbi ids under the
+               synthetic scores (synth.unigram_scores; <unk> = the vocabulary
+               size, scored synth.unigram_unk_score)
+  unigram_doc  the first 64 MiB of the enc text as one document, same model
 """
 from __future__ import annotations
 
@@ -116,6 +120,43 @@ def encode_record(name: str, merges_large: np.ndarray | None) -> dict:
     }
 
 
+UNIGRAM_DOC_BYTES = 64 << 20
+
+
+def unigram_record(name: str) -> dict:
+    big = synth.corpus("large")
+    vb, voff = synth.substring_vocab(big)
+    del big
+    if name == "unigram":
+        text, doc_off = synth.batch_documents()
+    else:
+        text = synth.corpus("enc", UNIGRAM_DOC_BYTES)
+        doc_off = np.array([0, text.size], dtype=np.uint64)
+    n_tok = int(voff.size - 1)
+    scores = synth.unigram_scores(n_tok)
+    unk = synth.unigram_unk_score(scores)
+    trie = oracle.Trie(vb, voff)
+    t0 = time.time()
+    ids, id_off = trie.unigram_encode(text, scores, n_tok, unk, doc_off)
+    dt = time.time() - t0
+    return {
+        "text_bytes": int(text.size),
+        "text_sha256": sha(text),
+        "n_docs": int(doc_off.size - 1),
+        "vocab_size": n_tok,
+        "vocab_sha256": sha(np.asarray(vb, dtype=np.uint8)),
+        "scores_sha256": sha(np.asarray(scores, dtype=np.float64)),
+        "unk_id": n_tok,
+        "unk_score": unk,
+        "n_ids": int(ids.size),
+        "n_unk": int((ids == n_tok).sum()),
+        "ids_sha256": sha(ids.astype(np.int32)),
+        "ids_head": ids[:16].tolist(),
+        "id_off_sha256": sha(id_off.astype(np.uint64)),
+        "oracle_seconds": round(dt, 2),
+    }
+
+
 def main(names):
     data = {}
     if os.path.exists(OUT):
@@ -131,6 +172,8 @@ def main(names):
                 # (left, right, count) as uint32 for consumers that need the table
                 np.save(os.path.join(os.path.dirname(OUT), "large_merges.npy"),
                         merges[:, [0, 1, 3]].astype(np.uint32))
+        elif name.startswith("unigram"):
+            rec = unigram_record(name)
         else:
             rec = encode_record(name, merges_large)
         data[name] = rec

@@ -110,12 +110,16 @@ def test_double_array_duplicates_keep_lowest_id():
     assert da_longest(lc, lb, lt, b"xq", 0, 2) == (ord("x"), 1)
 
 
-def test_layout_rejects_missing_single_byte():
+def test_layout_without_a_single_byte():
+    """A vocabulary missing byte 0xFF lays out (Unigram encoding accepts it);
+    the root's slot for 0xFF is then no token of the root."""
     toks = [bytes([b]) for b in range(255)] + [b"ab"]
     vb, off = vocab_arrays(toks)
-    with pytest.raises(_capi.BpeError) as e:
-        _capi.trie_layout(vb, off)
-    assert e.value.code == -1
+    check, base, tid = _capi.trie_layout(vb, off)
+    rb = int(base.view(np.uint32)[0] & 0x7FFFFFFF)
+    for b in range(255):
+        assert check[rb + b] == 0 and tid[rb + b] == b
+    assert check[rb + 255] != 0 or tid[rb + 255] < 0
 
 
 def test_layout_large_substring_vocab_sampled():

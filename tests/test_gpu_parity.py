@@ -436,8 +436,10 @@ def test_encode_capacity_error(ctx):
 
 def test_encode_rejects_bad_inputs(ctx):
     import bpe_trie_encode_gb300 as bt
-    with pytest.raises(bt.BpeError):
-        ctx.trie_build(*vocab_arrays([b"a", b"b"]))
+    partial = ctx.trie_build(*vocab_arrays([b"a", b"b"]))   # builds (Unigram can use it); greedy refuses it
+    with pytest.raises(bt.BpeError) as e:
+        ctx.encode(partial, dev_u8(b"ab"))
+    assert e.value.name == "INVALID_ARG"
     trie = ctx.trie_build(*vocab_arrays([bytes([b]) for b in range(256)]))
     with pytest.raises(bt.BpeError) as e:
         ctx.encode(trie, dev_u8(b"abcdef"), torch.tensor([0, 4, 2], dtype=torch.int64, device="cuda"))
