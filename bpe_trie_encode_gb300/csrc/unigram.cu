@@ -60,6 +60,8 @@ struct bpe_unigram {
     int q = 0;                  // units are 2^-q
     uint32_t span = 0;          // E: longest edge (token or <unk>) the kernels take
     void *d_leaf = nullptr;     // per trie slot: {score units, token id}
+    void *d_fslot = nullptr;    // per trie slot: {check, base|TERM, score units (int32), token id};
+                                // only when every |score| < 2^29 units (the warp kernels need it)
 };
 
 namespace bpe {
@@ -68,6 +70,7 @@ namespace {
 constexpr int kUniThreads = 128;
 constexpr uint32_t kRoot = 0x00FFFFFFu;    // speculative start (length 0 never occurs otherwise)
 constexpr uint32_t kUnkTid = 0x00FFFFFFu;
+constexpr uint32_t kNoTid = 0x00FFFFFEu;     // a token whose id the emit pass looks up from its bytes
 constexpr long long kNeg = -0x7FFFFFFFFFFFFFFFll - 1;   // -inf
 constexpr uint32_t kUniDefaultChunk = 512;
 constexpr unsigned kUniSpinLimit = 1u << 22;
@@ -106,9 +109,11 @@ struct UniParams {
     const int2 *slot;
     const int4 *root;
     const Leaf *leaf;
+    const int4 *fslot;  // the slots with their token's score and id (warp kernels)
     long long unk;
     int32_t unk_id;
     unsigned long long text_lo;   // doc_off[0]
+    unsigned long long text_end;  // doc_off[n_docs]
     uint32_t *back;     // per position (offset from text_lo), span + 1 words
     uint32_t *gback;    // per chunk grec words: the guard's back pointers and crossing bits
     uint32_t *fflag, *bflag;   // bitmaps over chunks
@@ -138,6 +143,16 @@ __device__ __forceinline__ void load_uni_lut(const UniParams &P, int4 *lut) {
         int4 r = P.root[c];
         if (__ldg(&P.slot[r.x].x) != 0) r.x = -1;
         lut[c] = r;
+    }
+}
+
+// The same with each depth-1 node's score (int32 units) and token id:
+// {slot or -1, base|TERM, score, tid}.
+__device__ __forceinline__ void load_fat_lut(const UniParams &P, int4 *lut) {
+    for (int c = threadIdx.x; c < 256; c += blockDim.x) {
+        const int32_t x = P.root[c].x;
+        const int4 f = P.fslot[x];
+        lut[c] = make_int4(f.x == 0 ? x : -1, f.y, f.z, f.w);
     }
 }
 
@@ -174,12 +189,13 @@ __device__ __forceinline__ UGeo uni_geo(const UniParams &P, unsigned long long k
 // reaches it: its back pointer goes to sink(i, bp).  A reachable character
 // start then relaxes every token that ends at a character boundary (trie
 // walk) or, when there is none, the <unk> edge to the next boundary; every
-// relaxed edge i -> j is reported to edge(i, j).  Each loop iteration takes
+// relaxed edge i -> j is reported to edge(i, j).  Back pointers carry the
+// token id (kIds) or kNoTid, as the warp kernels write them.  Each loop iteration takes
 // one trie step on every lane (finalising a position first where a walk has
 // ended), so the lanes of a warp do not wait for each other's long walks.  A
 // run of E continuation bytes could only be crossed by a longer edge: it
 // raises UERR_SPAN (whichever run sees its last E bytes).
-template <int R, typename Sink, typename Edge>
+template <int R, bool kIds = true, typename Sink, typename Edge>
 __device__ __forceinline__ void uni_run(const UniParams &P, const int4 *lut, long long *best, uint32_t *bk,
                                         uint64_t from, uint64_t to, uint64_t de, Sink sink, Edge edge) {
     uint32_t cont_run = 0;
@@ -237,7 +253,7 @@ __device__ __forceinline__ void uni_run(const UniParams &P, const int4 *lut, lon
         const uint32_t nb = j < de ? byte_at(P, j) : 0u;
         if ((y & kTermBit) && (j == de || !is_cont(nb))) {
             const Leaf lf = P.leaf[node];
-            relax(j, b + lf.score, (len << 24) | (uint32_t)lf.tid);
+            relax(j, b + lf.score, (len << 24) | (kIds ? (uint32_t)lf.tid : kNoTid));
             matched = true;
         }
         const uint32_t base = y & ~kTermBit;
@@ -428,148 +444,197 @@ __device__ bool guard_agrees(const UniParams &P, const uint32_t *gr, uint64_t cs
 
 constexpr int kFwdWarps = 8;                 // warps per CTA of the warp-per-chunk kernels
 constexpr int kEdgeStride = 65;              // a lane's edge row: one word per length 0..63, odd stride (banks)
-constexpr uint32_t kUnkNode = 0xFFFFFFFFu;   // edge row entry of an <unk> edge
-constexpr size_t kWarpEdgeBytes = 32 * kEdgeStride * sizeof(uint32_t);
+constexpr size_t kWarpEdgeBytes = 32 * kEdgeStride * sizeof(int32_t) + 128;   // rows, then staged text
 
-// The recurrence's ring of 64 values and back pointers for spans E <= 63,
-// held by a warp in registers: lane l holds the positions base + l (mod 32),
-// half h those with ((pos - base) >> 5) & 1 == h.
+constexpr int32_t kNeg32 = -0x7FFFFFFF - 1;   // unreachable (relative values)
+constexpr int32_t kSpread = 1 << 30;          // relative values stay within +-kSpread (else the run is redone)
+constexpr int kTextStage = 128;               // bytes of text a warp stages per batch (32 positions + 63 + 1)
+
+// The recurrence's window for spans E <= 63, held by a warp in registers.
+// Only values of positions at most 63 apart are ever compared, so they are
+// kept as int32 relative to the window's best, rebased every batch: with
+// |score| < 2^29 and every value within 2^30 of 0 no sum wraps, and a value
+// beyond that reports a spread (the run is redone exactly).  Before source s
+// of the batch at b0, lane t holds in A the position b0 + t if t >= s, else
+// b0 + 32 + t -- the one its length o1 = (t - s - 1) mod 32 + 1 edge reaches --
+// and in B the position 32 further on (lengths o1 + 32).  When lane s is the
+// source its A is final and B moves into A.  With each value, the source of
+// its best edge as an offset from base (bit 31: the edge is <unk>); the
+// edge's length is the distance to it.
 struct WarpRing {
-    long long r0, r1;
-    uint32_t p0, p1;
-    uint64_t base;
+    int32_t a, b;
+    uint32_t sa, sb;
+    uint64_t base, b0;
 };
 
 __device__ __forceinline__ void ring_start(WarpRing &R, uint64_t base, uint64_t s0, int lane) {
-    R.r0 = R.r1 = kNeg;
-    R.p0 = R.p1 = 0;
-    R.base = base;
+    R.a = R.b = kNeg32;
+    R.sa = R.sb = 0;
+    R.base = R.b0 = base;
     const uint64_t o = s0 - base;
-    if (o < 64 && lane == (int)(o & 31)) {
-        if (o >> 5) { R.r1 = 0; R.p1 = kRoot; } else { R.r0 = 0; R.p0 = kRoot; }
+    if (o < 64 && lane == (int)(o & 31)) {   // the start is its own source: length 0
+        if (o >> 5) { R.b = 0; R.sb = (uint32_t)o; } else { R.a = 0; R.sa = (uint32_t)o; }
     }
 }
 
-// Back pointer of a final position held by this lane (0 if unreachable).
-__device__ __forceinline__ uint32_t ring_final(const WarpRing &R, uint64_t pos) {
-    const bool hi = ((pos - R.base) >> 5) & 1;
-    const long long v = hi ? R.r1 : R.r0;
-    return v == kNeg ? 0u : (hi ? R.p1 : R.p0);
+// Back pointer of position pos given its value and source.
+__device__ __forceinline__ uint32_t ring_bp(const WarpRing &R, uint64_t pos, int32_t v, uint32_t src) {
+    if (v == kNeg32) return 0u;
+    const uint32_t len = ((uint32_t)(pos - R.base) - src) & 0x7FFFFFFFu;
+    return len == 0 ? kRoot : (len << 24) | ((src >> 31) ? kUnkTid : kNoTid);
 }
 
-// One warp's edges in shared memory: row l (lane l's position), entry len =
-// the trie node of the token of that length (kUnkNode for <unk>); a 64-bit
-// mask per lane says which entries are edges.
+// After a run: back pointer of the first position at or after its end that
+// this lane holds (the document end, when the run ended there).
+__device__ __forceinline__ uint32_t ring_final(const WarpRing &R, uint64_t pos) {
+    return ring_bp(R, pos, R.a, R.sa);
+}
+
+// One warp's shared memory: its edge rows (row l: lane l's position, entry
+// len = the score, int32 units, of the edge of that length) and its text.
 struct EdgeBuf {
-    uint32_t *node;
+    int32_t *score;
+    uint8_t *text;
 };
 
 // The recurrence over positions [from, to) of a document ending at de, by one
-// warp ((from - base) a multiple of 32), 32 positions at a time.  Walk: every
-// lane walks the trie from its position (reachable or not) and records its
-// edges by length in shared memory, with a 64-bit mask of their lengths; cross(m, bits) receives, per batch m, which positions have
-// an edge reaching cs or beyond.  Recurrence: the batch's positions in order;
-// the value of source s comes from its owner lane, and every lane relaxes the
-// (at most two) positions among the next 63 that it owns, through s's edge of
-// that length.  sink(q, bp) receives every final position.
+// warp (from = R.b0), 32 positions at a time, on the slots that carry their
+// token's score (fslot; lut: the depth-1 nodes).  Walk: every lane walks the
+// trie from its position (reachable or not) over the batch's text staged in
+// shared memory, records its edges' scores by length in its row and their
+// lengths as bit masks (1..32, 33..63); cross(m, bits) receives, per batch m,
+// which positions have an edge reaching cs or beyond.  Recurrence: the
+// batch's positions in order; source s's value comes from lane s, and every
+// lane relaxes its o1 and o1 + 32 targets (a bit of s's masks rotated by
+// s + 1) from shared memory and shuffles only.  A back pointer holds the
+// length and kNoTid (the emit pass finds the id from the token's bytes) or
+// kUnkTid.  sink(q, bp) receives every final position.  Returns whether the
+// values spread beyond kSpread (then the run is incomplete).
 template <typename Sink, typename Cross>
-__device__ void warp_dp(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRing &R, uint64_t from,
+__device__ bool warp_dp(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRing &R, uint64_t from,
                         uint64_t to, uint64_t de, uint64_t cs, Sink sink, Cross cross) {
     const int lane = threadIdx.x & 31;
-    uint32_t *row = eb.node + lane * kEdgeStride;
+    const uint32_t mybit = 1u << lane;
+    int32_t *row = eb.score + lane * kEdgeStride;
+    bool spread = false;
     for (uint64_t b0 = from; b0 < to; b0 += 32) {
-        const uint32_t m = (uint32_t)((b0 - R.base) >> 5);
+        // stage text [b0, b0 + 128) (what lies before the text's end)
+#pragma unroll
+        for (int i = 0; i < kTextStage / 32; i++) {
+            const uint64_t p = b0 + i * 32 + lane;
+            eb.text[i * 32 + lane] = p < P.text_end ? byte_at(P, p) : 0u;
+        }
+        __syncwarp();
         const uint64_t q = b0 + lane;
-        unsigned long long mask = 0;
-        bool crossing = false;
+        unsigned long long M = 0;   // bit len: an edge of that length
+        bool crossing = false, unk = false;
         if (q < to) {
-            const uint32_t c0 = byte_at(P, q);
+            const uint32_t dlen = de - q < 64 ? (uint32_t)(de - q) : 64u;   // bytes to the document end (capped)
+            const uint32_t lim = min(dlen, P.E);
+            const uint32_t csr = q >= cs ? 0u : cs - q < 64 ? (uint32_t)(cs - q) : 64u;
+            const uint8_t *tx = eb.text + lane;
+            const uint32_t c0 = tx[0];
             if (!is_cont(c0)) {
                 const int4 r = lut[c0];
                 if (r.x >= 0) {
                     int32_t node = r.x;
                     uint32_t y = (uint32_t)r.y;
+                    int32_t sc = r.z;
                     uint32_t len = 1;
                     for (;;) {
-                        const uint64_t j = q + len;
-                        const uint32_t nb = j < de ? byte_at(P, j) : 0u;
-                        if ((y & kTermBit) && (j == de || !is_cont(nb))) {
-                            row[len] = (uint32_t)node;
-                            mask |= 1ull << len;
-                            crossing |= j >= cs;
+                        const uint32_t nb = len < dlen ? tx[len] : 0u;
+                        if ((y & kTermBit) && (len == dlen || !is_cont(nb))) {
+                            row[len] = sc;
+                            M |= 1ull << len;
+                            crossing |= len >= csr;
                         }
                         const uint32_t base = y & ~kTermBit;
-                        if (j >= de || base == 0 || len >= P.E) break;
+                        if (len >= lim || base == 0) break;
                         const int32_t t = (int32_t)(base + nb);
-                        const int2 v = __ldg(P.slot + t);
+                        const int4 v = __ldg(P.fslot + t);
                         if (v.x != node) break;
                         node = t;
                         y = (uint32_t)v.y;
+                        sc = v.z;
                         ++len;
                     }
                 }
-                if (mask == 0) {   // <unk> to the next character boundary
-                    uint64_t j = q + 1;
-                    while (j < de && is_cont(byte_at(P, j)) && j - q <= P.E) ++j;
-                    if (j - q > P.E) {
+                if (M == 0) {   // <unk> to the next character boundary
+                    uint32_t len = 1;
+                    while (len < dlen && len <= P.E && is_cont(len < kTextStage - lane ? tx[len] : byte_at(P, q + len)))
+                        ++len;
+                    if (len > P.E) {
                         atomicOr(&P.st->err, UERR_SPAN);
-                        j = q + P.E;
+                        len = P.E;
                     }
-                    row[j - q] = kUnkNode;
-                    mask = 1ull << (j - q);
-                    crossing = j >= cs;
+                    row[len] = (int32_t)P.unk;
+                    M = 1ull << len;
+                    unk = true;
+                    crossing = len >= csr;
                 }
             }
         }
         cross((uint32_t)((b0 - from) >> 5), __ballot_sync(kFull, crossing && q < cs));
-        __syncwarp();
-        const uint32_t h = m & 1u;
-        uint32_t fin = 0;
-        const uint32_t nsrc = (uint32_t)(to - b0 < 32 ? to - b0 : 32);
-        for (uint32_t s = 0; s < nsrc; s++) {
-            const long long b = __shfl_sync(kFull, h ? R.r1 : R.r0, s);
-            const uint32_t bp = __shfl_sync(kFull, h ? R.p1 : R.p0, s);
-            const unsigned long long M = __shfl_sync(kFull, mask, s);
-            if (lane == (int)s) {   // position b0 + s is final: free its slot
-                fin = b == kNeg ? 0u : bp;
-                if (h) { R.r1 = kNeg; R.p1 = 0; } else { R.r0 = kNeg; R.p0 = 0; }
+        const uint32_t X = (uint32_t)(M >> 1), Y = (uint32_t)(M >> 33);
+        const uint32_t xrot = __funnelshift_l(X, X, lane + 1), yrot = __funnelshift_l(Y, Y, lane + 1);
+        const uint32_t mycode = ((uint32_t)(q - R.base) & 0x7FFFFFFFu) | ((uint32_t)unk << 31);
+        // rebase: the window's best reachable value becomes 0
+        const int32_t mx = __reduce_max_sync(kFull, max(R.a, R.b));
+        if (mx != kNeg32) {
+            if (R.a != kNeg32) {
+                const long long v = (long long)R.a - mx;
+                spread |= v < -kSpread;
+                R.a = (int32_t)max(v, (long long)-kSpread);
             }
-            if (b == kNeg || M == 0) continue;
-            uint32_t o = ((uint32_t)lane - s) & 31u;
-            if (o == 0) o = 32;
-#pragma unroll
-            for (int u = 0; u < 2; u++, o += 32) {
-                if (o > 63 || !((M >> o) & 1ull)) continue;
-                const uint32_t nd = eb.node[s * kEdgeStride + o];
-                long long sc;
-                uint32_t nbp;
-                if (nd == kUnkNode) {
-                    sc = P.unk;
-                    nbp = (o << 24) | kUnkTid;
-                } else {
-                    const Leaf lf = P.leaf[nd];
-                    sc = lf.score;
-                    nbp = (o << 24) | (uint32_t)lf.tid;
-                }
-                const long long cand = b + sc;
-                if ((((32u * m + s + o) >> 5) & 1u) != 0u) {
-                    if (cand > R.r1) { R.r1 = cand; R.p1 = nbp; }
-                } else {
-                    if (cand > R.r0) { R.r0 = cand; R.p0 = nbp; }
-                }
+            if (R.b != kNeg32) {
+                const long long v = (long long)R.b - mx;
+                spread |= v < -kSpread;
+                R.b = (int32_t)max(v, (long long)-kSpread);
             }
         }
         __syncwarp();
-        if (q < to) sink(q, fin);
+        int32_t fv = kNeg32;
+        uint32_t fs = 0;
+        const uint32_t nsrc = (uint32_t)(to - b0 < 32 ? to - b0 : 32);
+        uint32_t o1 = lane == 0 ? 32u : (uint32_t)lane;   // this lane's length o1 from source 0
+        const int32_t *srow = eb.score;
+        for (uint32_t s = 0; s < nsrc; s++, o1 = o1 == 1 ? 32u : o1 - 1, srow += kEdgeStride) {
+            const int32_t b = __shfl_sync(kFull, R.a, s);
+            const uint32_t xr = __shfl_sync(kFull, xrot, s);
+            const uint32_t yr = __shfl_sync(kFull, yrot, s);
+            const uint32_t code = __shfl_sync(kFull, mycode, s);
+            if (lane == (int)s) {   // position b0 + s is final; the next window position moves in
+                fv = R.a;
+                fs = R.sa;
+                R.a = R.b;
+                R.sa = R.sb;
+                R.b = kNeg32;
+                R.sb = 0;
+            }
+            if (b == kNeg32) continue;
+            if (xr & mybit) {
+                const int32_t cand = b + srow[o1];
+                if (cand > R.a) { R.a = cand; R.sa = code; }
+            }
+            if (yr & mybit) {
+                const int32_t cand = b + srow[o1 + 32];
+                if (cand > R.b) { R.b = cand; R.sb = code; }
+            }
+        }
+        spread |= fv != kNeg32 && (fv < -kSpread || fv > kSpread);   // every source value stayed in range
+        __syncwarp();
+        if (q < to) sink(q, ring_bp(R, q, fv, fs));
+        R.b0 = b0 + 32;
     }
+    return __any_sync(kFull, spread);
 }
 
 // Warp-per-chunk speculative forward run (spans E <= 63): k_uni_fwd's work,
 // one warp per chunk.
 __global__ void __launch_bounds__(kFwdWarps * 32) k_uni_fwd_warp(UniParams P, unsigned long long n_chunks) {
     __shared__ int4 lut[256];
-    extern __shared__ uint32_t s_nodes[];   // kFwdWarps edge tables
-    load_uni_lut(P, lut);
+    extern __shared__ int32_t s_rows[];   // kFwdWarps edge tables
+    load_fat_lut(P, lut);
     __syncthreads();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const unsigned long long k = (unsigned long long)blockIdx.x * kFwdWarps + w;
@@ -583,8 +648,8 @@ __global__ void __launch_bounds__(kFwdWarps * 32) k_uni_fwd_warp(UniParams P, un
     WarpRing R;
     ring_start(R, from, s0, lane);
     uint32_t *gb = P.gback + k * (unsigned long long)P.grec;
-    const EdgeBuf eb{s_nodes + w * 32 * kEdgeStride};
-    warp_dp(
+    const EdgeBuf eb{s_rows + w * (kWarpEdgeBytes / 4), (uint8_t *)(s_rows + w * (kWarpEdgeBytes / 4) + 32 * kEdgeStride)};
+    const bool sp = warp_dp(
         P, lut, eb, R, from, g.ce, g.de, g.cs,
         [&](uint64_t q, uint32_t bp) {
             if (q >= g.cs) {
@@ -596,6 +661,12 @@ __global__ void __launch_bounds__(kFwdWarps * 32) k_uni_fwd_warp(UniParams P, un
         [&](uint32_t m, unsigned bits) {
             if (!exact && m < (P.guard >> 5) && lane == 0) gb[P.guard + m] = bits;
         });
+    if (sp && lane == 0) {   // values spread too far for 32 bits: the chunk is redone
+        atomicOr(P.fflag + (k >> 5), 1u << (k & 31));
+        P.st->any_fflag = 1u;
+        const uint32_t i = atomicAdd(&P.st->flist_len, 1u);
+        if (i < P.flist_cap) P.flist[i] = (uint32_t)k;
+    }
     if (g.last && lane == (int)((g.de - from) & 31)) back_at(P, g.de) = ring_final(R, g.de);
 }
 
@@ -713,18 +784,18 @@ __global__ void __launch_bounds__(128) k_uni_frepair(UniParams P) {
 // The state at flagged chunk f's start: f-1's run start (or the document
 // start when f lies within G bytes of it) and the run up to f's start.
 __device__ __forceinline__ void warp_prefix(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRing &R,
-                                            const UGeo &gf, unsigned long long f) {
+                                            const UGeo &gf, unsigned long long f, bool *sp) {
     const int lane = threadIdx.x & 31;
     const UGeo gp = gf.cs - gf.ds <= P.guard ? gf : uni_geo(P, f - 1);
     const uint64_t from = run_from(P, gp);
     ring_start(R, from, from == gp.ds ? gp.ds : next_boundary(P, from, gp.de), lane);
-    warp_dp(P, lut, eb, R, from, gf.cs, gf.de, 0, [](uint64_t, uint32_t) {}, [](uint32_t, unsigned) {});
+    *sp |= warp_dp(P, lut, eb, R, from, gf.cs, gf.de, 0, [](uint64_t, uint32_t) {}, [](uint32_t, unsigned) {});
 }
 
 // Run chunk g (its start state in R), writing its true back pointers.
 __device__ __forceinline__ void warp_chunk(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRing &R,
-                                           const UGeo &g) {
-    warp_dp(
+                                           const UGeo &g, bool *sp) {
+    *sp |= warp_dp(
         P, lut, eb, R, g.cs, g.ce, g.de, 0,
         [&](uint64_t q, uint32_t bp) {
             if (q != g.ds) back_at(P, q) = bp;
@@ -748,20 +819,53 @@ __device__ __forceinline__ bool warp_next_ok(const UniParams &P, const UGeo &g, 
 // is -- and records in okn whether f + 1 then passes its check.
 __global__ void __launch_bounds__(kFwdWarps * 32) k_uni_fix_a(UniParams P) {
     __shared__ int4 lut[256];
-    extern __shared__ uint32_t s_nodes[];
-    load_uni_lut(P, lut);
+    extern __shared__ int32_t s_rows[];
+    load_fat_lut(P, lut);
     __syncthreads();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint32_t n = min(P.st->flist_len, P.flist_cap);
-    const EdgeBuf eb{s_nodes + w * 32 * kEdgeStride};
+    const EdgeBuf eb{s_rows + w * (kWarpEdgeBytes / 4), (uint8_t *)(s_rows + w * (kWarpEdgeBytes / 4) + 32 * kEdgeStride)};
     for (uint32_t i = blockIdx.x * kFwdWarps + w; i < n; i += gridDim.x * kFwdWarps) {
         const unsigned long long f = P.flist[i];
         const UGeo gf = uni_geo(P, f);
         WarpRing R;
-        warp_prefix(P, lut, eb, R, gf, f);
-        warp_chunk(P, lut, eb, R, gf);
-        const bool ok = gf.last || warp_next_ok(P, gf, f);
+        bool sp = false;
+        warp_prefix(P, lut, eb, R, gf, f, &sp);
+        warp_chunk(P, lut, eb, R, gf, &sp);
+        const bool ok = !sp && (gf.last || warp_next_ok(P, gf, f));
         if (ok && lane == 0) atomicOr(P.okn + (f >> 5), 1u << (f & 31));
+    }
+}
+
+// The chain of k_uni_frepair_warp run by one thread on a private 64-bit ring
+// (back pointers in the warp kernels' format): from f's state through at
+// least chunk wend, then on until a chunk passes its check; returns the chunk
+// after the chain.
+__device__ unsigned long long thread_chain(const UniParams &P, const int4 *lut, const UGeo &gf, unsigned long long f,
+                                           unsigned long long wend) {
+    long long best[64];
+    uint32_t bk[64];
+    const UGeo gp = gf.cs - gf.ds <= P.guard ? gf : uni_geo(P, f - 1);
+    const uint64_t from = run_from(P, gp);
+    start_run<64>(P, gp, from, best, bk);
+    uni_run<64, false>(P, lut, best, bk, from, gf.cs, gf.de, [](uint64_t, uint32_t) {}, [](uint64_t, uint64_t) {});
+    unsigned long long m = f;
+    for (;;) {
+        const UGeo g = uni_geo(P, m);
+        uni_run<64, false>(
+            P, lut, best, bk, g.cs, g.ce, g.de,
+            [&](uint64_t i, uint32_t bp) {
+                if (i != g.ds) back_at(P, i) = bp;
+            },
+            [](uint64_t, uint64_t) {});
+        ++m;
+        if (g.last) {
+            finish_doc<64>(P, g, best, bk);
+            return m;
+        }
+        if (m > wend && !flag_bit(P.fflag, m) &&
+            (g.ce - g.ds <= P.guard || guard_agrees(P, P.gback + m * (unsigned long long)P.grec, g.ce)))
+            return m;
     }
 }
 
@@ -774,13 +878,13 @@ __global__ void __launch_bounds__(kFwdWarps * 32) k_uni_fix_a(UniParams P) {
 // run's back pointers (k_uni_fix_a rewrote every listed chunk).
 __global__ void __launch_bounds__(128) k_uni_frepair_warp(UniParams P) {
     __shared__ int4 lut[256];
-    extern __shared__ uint32_t s_nodes[];   // 4 edge tables
-    load_uni_lut(P, lut);
+    extern __shared__ int32_t s_rows[];   // 4 edge tables
+    load_fat_lut(P, lut);
     __syncthreads();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint32_t d = blockIdx.x * 4 + w;
     if (d >= P.n_docs) return;
-    const EdgeBuf eb{s_nodes + w * 32 * kEdgeStride};
+    const EdgeBuf eb{s_rows + w * (kWarpEdgeBytes / 4), (uint8_t *)(s_rows + w * (kWarpEdgeBytes / 4) + 32 * kEdgeStride)};
     const unsigned long long c0 = P.chunk_start[d], c1 = P.chunk_start[d + 1];
     unsigned long long f = warp_next_flag(P.fflag, c0, c1, lane);
     uint32_t reruns = 0;
@@ -790,16 +894,22 @@ __global__ void __launch_bounds__(128) k_uni_frepair_warp(UniParams P) {
         unsigned long long m = f + 1;
         if (!fast) {
             WarpRing R;
-            warp_prefix(P, lut, eb, R, gf, f);
+            bool sp = false;
+            warp_prefix(P, lut, eb, R, gf, f, &sp);
             m = f;
             for (;;) {
                 const UGeo g = uni_geo(P, m);
-                warp_chunk(P, lut, eb, R, g);
+                warp_chunk(P, lut, eb, R, g, &sp);
                 ++reruns;
                 if (g.last || (!flag_bit(P.fflag, m + 1) && warp_next_ok(P, g, m))) break;
                 ++m;
             }
+            const unsigned long long wend = m;   // last chunk the warp rewrote
             ++m;
+            if (sp) {   // values spread beyond 32 bits: lane 0 redoes the chain (through wend at least) in 64 bits
+                if (lane == 0) m = thread_chain(P, lut, gf, f, wend);
+                m = __shfl_sync(kFull, m, 0);
+            }
         }
         f = warp_next_flag(P.fflag, m, c1, lane);   // chunks before m are right
     }
@@ -810,8 +920,9 @@ __global__ void __launch_bounds__(128) k_uni_frepair_warp(UniParams P) {
 
 // Walk the back-pointer chain of chunk g from position x (>= ce, on the
 // chain of a reachable position): tokens starting in [cs, ce) are counted
-// (and written through put, last first); returns the chain's last position
-// at or after cs (the document start when the chunk is the first).
+// (and passed to put(rank, back pointer, start), last first); returns the
+// chain's last position at or after cs (the document start when the chunk is
+// the first).
 template <typename Put>
 __device__ __forceinline__ uint64_t walk_chunk(const UniParams &P, const UGeo &g, uint64_t x, uint32_t *cnt,
                                                Put put) {
@@ -820,7 +931,7 @@ __device__ __forceinline__ uint64_t walk_chunk(const UniParams &P, const UGeo &g
         const uint32_t v = back_at(P, x);
         const uint64_t nx = x - (v >> 24);
         if ((v >> 24) == 0 || nx < g.cs) break;   // unreachable or a run start: only on rejected input
-        put(c, v);
+        put(c, v, nx);
         ++c;
         x = nx;
     }
@@ -846,7 +957,7 @@ __global__ void __launch_bounds__(256) k_uni_bspec(UniParams P, unsigned long lo
         }
     }
     uint32_t c;
-    const uint64_t b = walk_chunk(P, g, x, &c, [](uint32_t, uint32_t) {});
+    const uint64_t b = walk_chunk(P, g, x, &c, [](uint32_t, uint32_t, uint64_t) {});
     P.sx[k] = (uint32_t)(x - g.cs);
     P.bot[k] = (uint32_t)(b - g.cs);
     P.count[k] = c;
@@ -875,7 +986,7 @@ __global__ void __launch_bounds__(256) k_uni_bfix_a(UniParams P, unsigned long l
     const UGeo g = uni_geo(P, k);
     const uint64_t x = g.ce + P.bot[k + 1];
     uint32_t c;
-    const uint64_t b = walk_chunk(P, g, x, &c, [](uint32_t, uint32_t) {});
+    const uint64_t b = walk_chunk(P, g, x, &c, [](uint32_t, uint32_t, uint64_t) {});
     P.sx[k] = (uint32_t)(x - g.cs);
     P.bot[k] = (uint32_t)(b - g.cs);
     P.count[k] = c;
@@ -906,7 +1017,7 @@ __global__ void __launch_bounds__(128) k_uni_brepair(UniParams P) {
                     const UGeo g = uni_geo(P, (unsigned long long)k);
                     const uint64_t x = g.ce + P.bot[k + 1];   // the next chunk starts at ce
                     uint32_t c;
-                    const uint64_t b = walk_chunk(P, g, x, &c, [](uint32_t, uint32_t) {});
+                    const uint64_t b = walk_chunk(P, g, x, &c, [](uint32_t, uint32_t, uint64_t) {});
                     P.sx[k] = (uint32_t)(x - g.cs);
                     P.bot[k] = (uint32_t)(b - g.cs);
                     P.count[k] = c;
@@ -926,6 +1037,14 @@ __global__ void __launch_bounds__(128) k_uni_brepair(UniParams P) {
 }
 
 // ----------------------------------------------------------------- emit ---
+
+// Id of the token bytes[start, start + len) (a token: its path exists).
+__device__ __forceinline__ int32_t token_id(const UniParams &P, uint64_t start, uint32_t len) {
+    int32_t node = __ldg(&P.root[byte_at(P, start)].x);
+    for (uint32_t i = 1; i < len; i++)
+        node = (int32_t)(((uint32_t)__ldg(&P.fslot[node].y) & ~kTermBit) + byte_at(P, start + i));
+    return __ldg(&P.fslot[node].w);
+}
 
 constexpr int kUniEmitThreads = 256;
 
@@ -996,11 +1115,11 @@ __global__ void __launch_bounds__(kUniEmitThreads) k_uni_emit(UniParams P, unsig
     const UGeo g = uni_geo(P, k);
     const unsigned long long last = o + cnt - 1;
     uint32_t c;
-    walk_chunk(P, g, g.cs + P.sx[k], &c, [&](uint32_t r, uint32_t v) {
+    walk_chunk(P, g, g.cs + P.sx[k], &c, [&](uint32_t r, uint32_t v, uint64_t start) {
         const unsigned long long w = last - r;
         if (w < P.cap) {
             const uint32_t id = v & 0x00FFFFFFu;
-            P.ids[w] = id == kUnkTid ? P.unk_id : (int32_t)id;
+            P.ids[w] = id == kUnkTid ? P.unk_id : id == kNoTid ? token_id(P, start, v >> 24) : (int32_t)id;
         }
     });
 }
@@ -1010,6 +1129,16 @@ __global__ void k_uni_docoff(UniParams P, unsigned long long n_chunks) {
     if (d > P.n_docs) return;
     const unsigned long long c = P.chunk_start[d];
     P.id_off[d] = c < n_chunks ? P.prefix[c] : P.st->total;
+}
+
+// Per trie slot: {check, base|TERM, score (int32 units), id} (scores that fit).
+__global__ void k_uni_fat(const int2 *slot, const int32_t *tid, unsigned long long n_slots, const long long *units,
+                          int4 *fslot) {
+    const unsigned long long s = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x;
+    if (s >= n_slots) return;
+    const int2 v = slot[s];
+    const int32_t t = tid[s];
+    fslot[s] = make_int4(v.x, v.y, t >= 0 ? (int32_t)units[t] : 0, t);
 }
 
 // Per trie slot: the score (fixed-point units) and id of its token.
@@ -1095,6 +1224,14 @@ extern "C" int unigram_create(bpe_ctx *ctx, const bpe_trie *trie, const double *
             trie->d_tid, trie->n_slots, (const long long *)d_units, (Leaf *)m->d_leaf);
         e = cudaGetLastError();
     }
+    if (e == cudaSuccess && trie->n_slots && max_abs < (1ll << 29)) {   // the warp kernels' 32-bit sums
+        e = cudaMalloc(&m->d_fslot, sizeof(int4) * trie->n_slots);
+        if (e == cudaSuccess) {
+            k_uni_fat<<<(unsigned)((trie->n_slots + 255) / 256), 256, 0, ctx->stream>>>(
+                trie->d_slot, trie->d_tid, trie->n_slots, (const long long *)d_units, (int4 *)m->d_fslot);
+            e = cudaGetLastError();
+        }
+    }
     if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
     if (d_units) cudaFree(d_units);
     if (e != cudaSuccess) {
@@ -1108,6 +1245,7 @@ extern "C" int unigram_create(bpe_ctx *ctx, const bpe_trie *trie, const double *
 extern "C" void unigram_free(bpe_unigram *model) {
     if (!model) return;
     if (model->d_leaf) cudaFree(model->d_leaf);
+    if (model->d_fslot) cudaFree(model->d_fslot);
     delete model;
 }
 
@@ -1153,6 +1291,7 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
     P.slot = trie->d_slot;
     P.root = trie->d_root;
     P.leaf = (const Leaf *)model->d_leaf;
+    P.fslot = (const int4 *)model->d_fslot;
     P.unk = model->unk;
     P.unk_id = model->unk_id;
     P.ids = d_ids_out;
@@ -1177,6 +1316,7 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
                     "unigram_encode: a document of %llu bytes could overflow 64-bit sums of 2^-%d units",
                     (unsigned long long)h->max_doc, model->q);
     P.text_lo = h->text_lo;
+    P.text_end = h->text_lo + h->span;
     const uint64_t words = (nc + 31) / 32, tiles = (nc + kUniEmitThreads - 1) / kUniEmitThreads;
     void *back, *gback, *info, *flag, *prefix, *status;
     if ((rc = ensure(ctx, S_UNI_BACK, (h->span + 1) * 4, &back)) ||
@@ -1207,19 +1347,27 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
     const unsigned grid_d = (n_docs + 3) / 4;   // one warp per document
     if (profile) cudaEventRecord(ctx->events[0], s);
     const size_t warp_smem = kFwdWarps * kWarpEdgeBytes, rep_smem = 4 * kWarpEdgeBytes;
-    if (R == 64) {
+    // spans up to 63 bytes and 32-bit scores: the warp-per-chunk kernels;
+    // otherwise one thread per chunk with a private ring
+    const bool warp = R == 64 && model->d_fslot;
+    if (warp) {
         BPE_CUDA(ctx, cudaFuncSetAttribute(k_uni_fwd_warp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)warp_smem),
                  "k_uni_fwd_warp smem");
         BPE_CUDA(ctx, cudaFuncSetAttribute(k_uni_fix_a, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)warp_smem),
                  "k_uni_fix_a smem");
         k_uni_fwd_warp<<<(unsigned)((nc + kFwdWarps - 1) / kFwdWarps), kFwdWarps * 32, warp_smem, s>>>(P, nc);
+    } else if (R == 64) {
+        k_uni_fwd<64><<<grid_c, kUniThreads, 0, s>>>(P, nc);
+    } else {
+        k_uni_fwd<256><<<grid_c, kUniThreads, 0, s>>>(P, nc);
     }
-    else k_uni_fwd<256><<<grid_c, kUniThreads, 0, s>>>(P, nc);
     if (profile) cudaEventRecord(ctx->events[1], s);
     k_uni_check<<<grid_c256, 256, 0, s>>>(P, nc);
-    if (R == 64) {
+    if (warp) {
         k_uni_fix_a<<<(unsigned)std::max(1, ctx->sm_count * 3), kFwdWarps * 32, warp_smem, s>>>(P);
         k_uni_frepair_warp<<<grid_d, 128, rep_smem, s>>>(P);
+    } else if (R == 64) {
+        k_uni_frepair<64><<<grid_d, 128, 0, s>>>(P);
     } else {
         k_uni_frepair<256><<<grid_d, 128, 0, s>>>(P);
     }
@@ -1245,12 +1393,12 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
     *n_ids = total;
     const int a = stats_slot(ctx, "unigram_fwd"), b = stats_slot(ctx, "unigram_fix"), c = stats_slot(ctx, "unigram_emit");
     ctx->stats.k[a].launches = 1;
-    ctx->stats.k[b].launches = R == 64 ? 7 : 6;
+    ctx->stats.k[b].launches = warp ? 7 : 6;
     ctx->stats.k[c].launches = 1;
     ctx->stats.k[a].bytes = (double)h->span;
     ctx->stats.k[b].bytes = (double)h->fwd_repairs * C + (double)h->bwd_repairs;   // chunks re-run, chunks re-walked
     ctx->stats.k[c].bytes = 4.0 * (double)total;
-    ctx->stats.kernel_launches = R == 64 ? 13 : 12;
+    ctx->stats.kernel_launches = warp ? 13 : 12;
     if (profile) {
         float x = 0, y = 0, z = 0;
         cudaEventElapsedTime(&x, ctx->events[0], ctx->events[1]);

@@ -164,6 +164,31 @@ def test_many_edges_per_position(ctx):
     check_unigram(ctx, vb, off, scores, len(toks), -40.0, docs, chunk=256)
 
 
+@pytest.mark.parametrize("seed", range(3))
+def test_wide_scores_thread_path(ctx, seed):
+    """Scores beyond 32-bit units take the per-thread kernels (same answers)."""
+    rng = random.Random(100 + seed)
+    toks, _ = random_model(rng, 300)
+    scores = [float(-rng.randint(1, 3) * 1_000_000_007) for _ in toks]   # integers above 2^31
+    vb, off = vocab_arrays(toks)
+    docs = [b"".join(rng.choice(ALPHA) for _ in range(rng.choice([1, 700, 2000]))) for _ in range(6)]
+    check_unigram(ctx, vb, off, scores, len(toks), -9e9, docs, chunk=256)
+
+
+def test_spread_beyond_32_bits(ctx):
+    """Scores near 2^28 units and runs of unknown characters push a window's
+    values more than 2^30 apart: those runs are redone in 64 bits."""
+    vb, off = vocab_arrays([b"a", b"b", b"ab", b"ba"])
+    sc = [-1.0, float(-(1 << 28)), -3.0, float(-(1 << 28) + 5)]
+    rng = random.Random(8)
+    docs = []
+    for _ in range(6):
+        parts = [rng.choice([b"a" * rng.randint(1, 400), b"z" * rng.randint(1, 300), b"ab" * rng.randint(1, 200),
+                             "ş".encode() * rng.randint(1, 100)]) for _ in range(rng.randint(2, 10))]
+        docs.append(b"".join(parts))
+    check_unigram(ctx, vb, off, sc, 4, float(-(1 << 28) - 7), docs, chunk=256)
+
+
 def test_long_tokens_wide_ring(ctx):
     """Tokens of up to 200 bytes take the 255-byte span (256-entry ring)."""
     rng = random.Random(9)
