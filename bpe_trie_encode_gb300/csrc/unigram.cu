@@ -442,9 +442,16 @@ __device__ bool guard_agrees(const UniParams &P, const uint32_t *gr, uint64_t cs
     return false;
 }
 
+// Guard bytes before a chunk for spans <= 63 (64 leaves the back-pointer
+// chains too little room to meet: most chunks then need a repair; 128 almost
+// none).
+constexpr uint32_t kGuard64 = 128;
+
 constexpr int kFwdWarps = 8;                 // warps per CTA of the warp-per-chunk kernels
-constexpr int kEdgeStride = 65;              // a lane's edge row: one word per length 0..63, odd stride (banks)
-constexpr size_t kWarpEdgeBytes = 32 * kEdgeStride * sizeof(int32_t) + 128;   // rows, then staged text
+constexpr int kEdgeStride = 33;              // a lane's edge row: lengths 1..32, odd stride (banks)
+constexpr int kLongRows = 16;                // rows for lengths 33..63, claimed per batch by the lanes that need one
+// per warp: 32 rows, the long rows, the long-row counter, the staged text
+constexpr size_t kWarpEdgeBytes = (32 * kEdgeStride + kLongRows * 32 + 4) * sizeof(int32_t) + 128;
 
 constexpr int32_t kNeg32 = -0x7FFFFFFF - 1;   // unreachable (relative values)
 constexpr int32_t kSpread = 1 << 30;          // relative values stay within +-kSpread (else the run is redone)
@@ -491,18 +498,25 @@ __device__ __forceinline__ uint32_t ring_final(const WarpRing &R, uint64_t pos) 
 }
 
 // One warp's shared memory: its edge rows (row l: lane l's position, entry
-// len = the score, int32 units, of the edge of that length) and its text.
+// len - 1 = the score, int32 units, of its edge of length len <= 32), a few
+// rows for lengths 33..63 (entry len - 33) claimed by the lanes that have
+// such an edge, and its text.
 struct EdgeBuf {
     int32_t *score;
+    int32_t *lrow;
+    int *lcount;
     uint8_t *text;
+    __device__ EdgeBuf(int32_t *base)
+        : score(base), lrow(base + 32 * kEdgeStride), lcount((int *)(base + 32 * kEdgeStride + kLongRows * 32)),
+          text((uint8_t *)(base + 32 * kEdgeStride + kLongRows * 32 + 4)) {}
 };
 
 // The recurrence over positions [from, to) of a document ending at de, by one
 // warp (from = R.b0), 32 positions at a time, on the slots that carry their
 // token's score (fslot; lut: the depth-1 nodes).  Walk: every lane walks the
 // trie from its position (reachable or not) over the batch's text staged in
-// shared memory, records its edges' scores by length in its row and their
-// lengths as bit masks (1..32, 33..63); cross(m, bits) receives, per batch m,
+// shared memory, records its edges' scores by length in its row (a long row
+// for lengths over 32) and their lengths as bit masks (1..32, 33..63); cross(m, bits) receives, per batch m,
 // which positions have an edge reaching cs or beyond.  Recurrence: the
 // batch's positions in order; source s's value comes from lane s, and every
 // lane relaxes its o1 and o1 + 32 targets (a bit of s's masks rotated by
@@ -524,7 +538,9 @@ __device__ bool warp_dp(const UniParams &P, const int4 *lut, const EdgeBuf &eb, 
             const uint64_t p = b0 + i * 32 + lane;
             eb.text[i * 32 + lane] = p < P.text_end ? byte_at(P, p) : 0u;
         }
+        if (lane == 0) *eb.lcount = 0;
         __syncwarp();
+        int lr = -1;   // this lane's long row
         const uint64_t q = b0 + lane;
         unsigned long long M = 0;   // bit len: an edge of that length
         bool crossing = false, unk = false;
@@ -544,7 +560,13 @@ __device__ bool warp_dp(const UniParams &P, const int4 *lut, const EdgeBuf &eb, 
                     for (;;) {
                         const uint32_t nb = len < dlen ? tx[len] : 0u;
                         if ((y & kTermBit) && (len == dlen || !is_cont(nb))) {
-                            row[len] = sc;
+                            if (len <= 32) {
+                                row[len - 1] = sc;
+                            } else {
+                                if (lr < 0) lr = atomicAdd(eb.lcount, 1);
+                                if (lr < kLongRows) eb.lrow[lr * 32 + (len - 33)] = sc;
+                                else spread = true;   // no long row left: the run is redone exactly
+                            }
                             M |= 1ull << len;
                             crossing |= len >= csr;
                         }
@@ -567,7 +589,13 @@ __device__ bool warp_dp(const UniParams &P, const int4 *lut, const EdgeBuf &eb, 
                         atomicOr(&P.st->err, UERR_SPAN);
                         len = P.E;
                     }
-                    row[len] = (int32_t)P.unk;
+                    if (len <= 32) {
+                        row[len - 1] = (int32_t)P.unk;
+                    } else {
+                        lr = atomicAdd(eb.lcount, 1);
+                        if (lr < kLongRows) eb.lrow[lr * 32 + (len - 33)] = (int32_t)P.unk;
+                        else spread = true;
+                    }
                     M = 1ull << len;
                     unk = true;
                     crossing = len >= csr;
@@ -603,6 +631,7 @@ __device__ bool warp_dp(const UniParams &P, const int4 *lut, const EdgeBuf &eb, 
             const uint32_t xr = __shfl_sync(kFull, xrot, s);
             const uint32_t yr = __shfl_sync(kFull, yrot, s);
             const uint32_t code = __shfl_sync(kFull, mycode, s);
+            const int slr = yr ? __shfl_sync(kFull, lr, s) : 0;   // s's long row (lengths 33..63)
             if (lane == (int)s) {   // position b0 + s is final; the next window position moves in
                 fv = R.a;
                 fs = R.sa;
@@ -613,11 +642,11 @@ __device__ bool warp_dp(const UniParams &P, const int4 *lut, const EdgeBuf &eb, 
             }
             if (b == kNeg32) continue;
             if (xr & mybit) {
-                const int32_t cand = b + srow[o1];
+                const int32_t cand = b + srow[o1 - 1];
                 if (cand > R.a) { R.a = cand; R.sa = code; }
             }
-            if (yr & mybit) {
-                const int32_t cand = b + srow[o1 + 32];
+            if ((yr & mybit) && slr < kLongRows) {   // length o1 + 32
+                const int32_t cand = b + eb.lrow[slr * 32 + (o1 - 1)];
                 if (cand > R.b) { R.b = cand; R.sb = code; }
             }
         }
@@ -631,7 +660,7 @@ __device__ bool warp_dp(const UniParams &P, const int4 *lut, const EdgeBuf &eb, 
 
 // Warp-per-chunk speculative forward run (spans E <= 63): k_uni_fwd's work,
 // one warp per chunk.
-__global__ void __launch_bounds__(kFwdWarps * 32) k_uni_fwd_warp(UniParams P, unsigned long long n_chunks) {
+__global__ void __launch_bounds__(kFwdWarps * 32, 4) k_uni_fwd_warp(UniParams P, unsigned long long n_chunks) {
     __shared__ int4 lut[256];
     extern __shared__ int32_t s_rows[];   // kFwdWarps edge tables
     load_fat_lut(P, lut);
@@ -648,7 +677,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32) k_uni_fwd_warp(UniParams P, un
     WarpRing R;
     ring_start(R, from, s0, lane);
     uint32_t *gb = P.gback + k * (unsigned long long)P.grec;
-    const EdgeBuf eb{s_rows + w * (kWarpEdgeBytes / 4), (uint8_t *)(s_rows + w * (kWarpEdgeBytes / 4) + 32 * kEdgeStride)};
+    const EdgeBuf eb(s_rows + w * (kWarpEdgeBytes / 4));
     const bool sp = warp_dp(
         P, lut, eb, R, from, g.ce, g.de, g.cs,
         [&](uint64_t q, uint32_t bp) {
@@ -824,7 +853,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32) k_uni_fix_a(UniParams P) {
     __syncthreads();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint32_t n = min(P.st->flist_len, P.flist_cap);
-    const EdgeBuf eb{s_rows + w * (kWarpEdgeBytes / 4), (uint8_t *)(s_rows + w * (kWarpEdgeBytes / 4) + 32 * kEdgeStride)};
+    const EdgeBuf eb(s_rows + w * (kWarpEdgeBytes / 4));
     for (uint32_t i = blockIdx.x * kFwdWarps + w; i < n; i += gridDim.x * kFwdWarps) {
         const unsigned long long f = P.flist[i];
         const UGeo gf = uni_geo(P, f);
@@ -884,7 +913,7 @@ __global__ void __launch_bounds__(128) k_uni_frepair_warp(UniParams P) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint32_t d = blockIdx.x * 4 + w;
     if (d >= P.n_docs) return;
-    const EdgeBuf eb{s_rows + w * (kWarpEdgeBytes / 4), (uint8_t *)(s_rows + w * (kWarpEdgeBytes / 4) + 32 * kEdgeStride)};
+    const EdgeBuf eb(s_rows + w * (kWarpEdgeBytes / 4));
     const unsigned long long c0 = P.chunk_start[d], c1 = P.chunk_start[d + 1];
     unsigned long long f = warp_next_flag(P.fflag, c0, c1, lane);
     uint32_t reruns = 0;
@@ -1283,7 +1312,7 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
     P.doc_off = d_doc_off;
     P.n_docs = n_docs;
     P.chunk = C;
-    P.guard = R == 64 ? 128u : 256u;
+    P.guard = R == 64 ? kGuard64 : 256u;
     P.grec = P.guard + P.guard / 32;
     P.E = model->span;
     P.ahead = R;
@@ -1346,7 +1375,7 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
     const unsigned grid_c256 = (unsigned)((nc + 255) / 256);
     const unsigned grid_d = (n_docs + 3) / 4;   // one warp per document
     if (profile) cudaEventRecord(ctx->events[0], s);
-    const size_t warp_smem = kFwdWarps * kWarpEdgeBytes, rep_smem = 4 * kWarpEdgeBytes;
+    const size_t rep_smem = 4 * kWarpEdgeBytes, warp_smem = kFwdWarps * kWarpEdgeBytes;
     // spans up to 63 bytes and 32-bit scores: the warp-per-chunk kernels;
     // otherwise one thread per chunk with a private ring
     const bool warp = R == 64 && model->d_fslot;
