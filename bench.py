@@ -285,6 +285,41 @@ def extra_legs(args, ctx, dev, stream, flush, d_text, d_sym, n_merges, peak, pea
         "ms_per_step": round(ms_bm / args.steps, 3), "n_ids": int(r2[0].numel()),
         "vs_double_array": round(ms_all / ms_bm, 3),
         "workload": "the batch encode above with 64-byte bitmap nodes instead of the double array"}
+    # Unigram (Viterbi) encoding of the same batch on the same trie, synthetic scores
+    scores = synth.unigram_scores(voff.size - 1)
+    unk = synth.unigram_unk_score(scores)
+    model = ctx.unigram(trie, scores, voff.size - 1, unk)
+    ms_u, kern = 0.0, {}
+    ctx.set_option(bt.BPE_OPT_PROFILE, 1)
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        (r3, _), ms = timed(stream, lambda: (ctx.unigram_encode(model, d_data, d_off, ids_out=ids), None))
+        if i >= args.warmup:
+            ms_u += ms
+            for k2, v in ctx.stats().items():
+                if k2 != "kernel_launches":
+                    a = kern.setdefault(k2, {"launches": 0, "bytes": 0.0, "ms": 0.0})
+                    for f in ("launches", "bytes", "ms"):
+                        a[f] += v[f]
+    ctx.set_option(bt.BPE_OPT_PROFILE, 0)
+    fwd = kern.get("unigram_fwd", {"ms": 0.0, "launches": 1})
+    fwd_ms = fwd["ms"] / max(fwd["launches"], 1)
+    out["unigram_batch"] = {
+        "value": round(args.steps * data.size / (ms_u / 1e3) / 1e9, 3), "unit": "GB/s",
+        "ms_per_step": round(ms_u / args.steps, 3), "n_ids": int(r3[0].numel()),
+        "workload": "the batch documents, most likely segmentation (Viterbi) under synthetic Zipf "
+                    "log-probabilities (float32) for the 250,000 tokens",
+        "kernels": {k2: {"launches": v["launches"], "ms": round(v["ms"], 3)} for k2, v in kern.items()},
+        # the forward recurrence is bound by dependent trie-walk loads and integer
+        # issue (ncu: ALU pipe ~48 %, issue ~56 % active), not by DRAM: its
+        # algorithmic traffic -- text read, 4-byte back pointer per byte written --
+        # over its duration is a small fraction of the copy bandwidth
+        "fwd_hbm": {"bound": "latency/alu", "achieved": round(5.0 * data.size / (fwd_ms / 1e3) / 1e9, 1),
+                    "peak": peak, "unit": "GB/s", "frac": round(5.0 * data.size / (fwd_ms / 1e3) / 1e9 / peak, 4),
+                    "peak_kind": f"of {peak_kind}", "algorithmic_bytes_per_byte": 5.0},
+    }
+    model.close()
     return out
 
 
