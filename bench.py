@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the extra legs (word-frequency, large, batch)")
+    ap.add_argument("--leg", choices=["unigram"], default=None,
+                    help="run only that leg and print its JSON (profiling)")
     return ap.parse_args()
 
 
@@ -285,7 +287,18 @@ def extra_legs(args, ctx, dev, stream, flush, d_text, d_sym, n_merges, peak, pea
         "ms_per_step": round(ms_bm / args.steps, 3), "n_ids": int(r2[0].numel()),
         "vs_double_array": round(ms_all / ms_bm, 3),
         "workload": "the batch encode above with 64-byte bitmap nodes instead of the double array"}
-    # Unigram (Viterbi) encoding of the same batch on the same trie, synthetic scores
+    out["unigram_batch"] = unigram_leg(args, ctx, stream, flush, trie, voff, d_data, d_off, ids, peak, peak_kind)
+    return out
+
+
+def unigram_leg(args, ctx, stream, flush, trie, voff, d_data, d_off, ids, peak, peak_kind):
+    """Unigram (Viterbi) encoding of the batch documents on the batch trie,
+    synthetic float32 Zipf log-probabilities; W warm-up and K timed steps,
+    the L2 flushed before each."""
+    import torch
+
+    import bpe_trie_encode_gb300 as bt
+    import synth
     scores = synth.unigram_scores(voff.size - 1)
     unk = synth.unigram_unk_score(scores)
     model = ctx.unigram(trie, scores, voff.size - 1, unk)
@@ -303,23 +316,51 @@ def extra_legs(args, ctx, dev, stream, flush, d_text, d_sym, n_merges, peak, pea
                     for f in ("launches", "bytes", "ms"):
                         a[f] += v[f]
     ctx.set_option(bt.BPE_OPT_PROFILE, 0)
+    model.close()
+    nbytes = d_data.numel()
     fwd = kern.get("unigram_fwd", {"ms": 0.0, "launches": 1})
     fwd_ms = fwd["ms"] / max(fwd["launches"], 1)
-    out["unigram_batch"] = {
-        "value": round(args.steps * data.size / (ms_u / 1e3) / 1e9, 3), "unit": "GB/s",
+    fwd_gbs = 5.0 * nbytes / (fwd_ms / 1e3) / 1e9 if fwd_ms else 0.0
+    return {
+        "value": round(args.steps * nbytes / (ms_u / 1e3) / 1e9, 3), "unit": "GB/s",
         "ms_per_step": round(ms_u / args.steps, 3), "n_ids": int(r3[0].numel()),
         "workload": "the batch documents, most likely segmentation (Viterbi) under synthetic Zipf "
                     "log-probabilities (float32) for the 250,000 tokens",
         "kernels": {k2: {"launches": v["launches"], "ms": round(v["ms"], 3)} for k2, v in kern.items()},
         # the forward recurrence is bound by dependent trie-walk loads and integer
-        # issue (ncu: ALU pipe ~48 %, issue ~56 % active), not by DRAM: its
+        # issue (ncu: ALU pipe ~53 %, issue ~72 % active), not by DRAM: its
         # algorithmic traffic -- text read, 4-byte back pointer per byte written --
         # over its duration is a small fraction of the copy bandwidth
-        "fwd_hbm": {"bound": "latency/alu", "achieved": round(5.0 * data.size / (fwd_ms / 1e3) / 1e9, 1),
-                    "peak": peak, "unit": "GB/s", "frac": round(5.0 * data.size / (fwd_ms / 1e3) / 1e9 / peak, 4),
-                    "peak_kind": f"of {peak_kind}", "algorithmic_bytes_per_byte": 5.0},
+        "fwd_hbm": {"bound": "latency/alu", "achieved": round(fwd_gbs, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(fwd_gbs / peak, 4), "peak_kind": f"of {peak_kind}",
+                    "algorithmic_bytes_per_byte": 5.0},
     }
-    model.close()
+
+
+def run_unigram_only(args):
+    """bench.py --leg unigram: only the Unigram leg (profiling and quick runs)."""
+    import numpy as np
+    import torch
+
+    import bpe_trie_encode_gb300 as bt
+    import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    ctx = bt.Context(0)
+    peak, peak_kind = peaks()
+    big = synth.corpus("large")
+    vb, voff = synth.substring_vocab(big)
+    del big
+    data, doc_off = synth.batch_documents()
+    trie = ctx.trie_build(vb, voff)
+    d_data = torch.from_numpy(data).to(dev)
+    d_off = torch.from_numpy(doc_off.astype(np.int64)).to(dev)
+    ids = torch.empty(data.size, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = unigram_leg(args, ctx, torch.cuda.current_stream(dev), flush, trie, voff, d_data, d_off, ids, peak,
+                      peak_kind)
+    out = {"leg": "unigram_batch", **out}
+    ctx.close()
     return out
 
 
@@ -658,7 +699,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.impl == "reference":
+    if args.leg == "unigram":
+        out = run_unigram_only(args) if rank == 0 else None
+    elif args.impl == "reference":
         out = run_reference(args, rank, world)
     else:
         import torch

@@ -624,13 +624,13 @@ __device__ bool warp_dp(const UniParams &P, const int4 *lut, const EdgeBuf &eb, 
         int32_t fv = kNeg32;
         uint32_t fs = 0;
         const uint32_t nsrc = (uint32_t)(to - b0 < 32 ? to - b0 : 32);
-        uint32_t o1 = lane == 0 ? 32u : (uint32_t)lane;   // this lane's length o1 from source 0
-        const int32_t *srow = eb.score;
-        for (uint32_t s = 0; s < nsrc; s++, o1 = o1 == 1 ? 32u : o1 - 1, srow += kEdgeStride) {
+        const bool anylong = __any_sync(kFull, Y != 0u);   // some edge over 32 bytes (rare)
+        // source s of the batch; o1 = this lane's length to reach its A position
+        auto source = [&](uint32_t s, uint32_t o1) {
             const int32_t b = __shfl_sync(kFull, R.a, s);
             const uint32_t xr = __shfl_sync(kFull, xrot, s);
-            const uint32_t yr = __shfl_sync(kFull, yrot, s);
             const uint32_t code = __shfl_sync(kFull, mycode, s);
+            const uint32_t yr = anylong ? __shfl_sync(kFull, yrot, s) : 0u;
             const int slr = yr ? __shfl_sync(kFull, lr, s) : 0;   // s's long row (lengths 33..63)
             if (lane == (int)s) {   // position b0 + s is final; the next window position moves in
                 fv = R.a;
@@ -638,17 +638,23 @@ __device__ bool warp_dp(const UniParams &P, const int4 *lut, const EdgeBuf &eb, 
                 R.a = R.b;
                 R.sa = R.sb;
                 R.b = kNeg32;
-                R.sb = 0;
             }
-            if (b == kNeg32) continue;
+            if (b == kNeg32) return;
             if (xr & mybit) {
-                const int32_t cand = b + srow[o1 - 1];
+                const int32_t cand = b + eb.score[s * kEdgeStride + (o1 - 1)];
                 if (cand > R.a) { R.a = cand; R.sa = code; }
             }
             if ((yr & mybit) && slr < kLongRows) {   // length o1 + 32
                 const int32_t cand = b + eb.lrow[slr * 32 + (o1 - 1)];
                 if (cand > R.b) { R.b = cand; R.sb = code; }
             }
+        };
+        const uint32_t o10 = lane == 0 ? 32u : (uint32_t)lane;   // this lane's length o1 from source 0
+        if (nsrc == 32) {
+#pragma unroll
+            for (uint32_t s = 0; s < 32; s++) source(s, ((o10 - 1u - s) & 31u) + 1u);
+        } else {
+            for (uint32_t s = 0; s < nsrc; s++) source(s, ((o10 - 1u - s) & 31u) + 1u);
         }
         spread |= fv != kNeg32 && (fv < -kSpread || fv > kSpread);   // every source value stayed in range
         __syncwarp();
