@@ -22,6 +22,7 @@ enum Slot {
     S_ENC_SBITS, S_HOST_IN0, S_HOST_IN1, S_HOST_OUT0, S_HOST_OUT1, S_HOST_OFF0, S_HOST_OFF1,
     S_W_BSUM, S_W_START, S_W_OCCSLOT, S_W_TABLE, S_W_UID, S_W_UINFO, S_W_SYM, S_W_OUTOFF,
     S_UNI_START, S_UNI_STATE, S_UNI_BACK, S_UNI_GBACK, S_UNI_CHUNK, S_UNI_FLAG, S_UNI_PREFIX, S_UNI_STATUS,
+    S_UNI_TSTART,
     S_NUM
 };
 

@@ -115,6 +115,7 @@ struct UniParams {
     unsigned long long text_lo;   // doc_off[0]
     unsigned long long text_end;  // doc_off[n_docs]
     uint32_t *back;     // per position (offset from text_lo), span + 1 words
+    uint32_t *tstart;   // per id: its token's start for k_uni_ids (null: emit looks ids up itself)
     uint32_t *gback;    // per chunk grec words: the guard's back pointers and crossing bits
     uint32_t *fflag, *bflag;   // bitmaps over chunks
     uint32_t *okn;             // bitmap: a flagged chunk's parallel repair was valid for its successor too
@@ -816,11 +817,54 @@ __global__ void __launch_bounds__(128) k_uni_frepair(UniParams P) {
     if (lane == 0 && reruns) atomicAdd(&P.st->fwd_repairs, reruns);
 }
 
-// The state at flagged chunk f's start: f-1's run start (or the document
-// start when f lies within G bytes of it) and the run up to f's start.
+// Where the true back-pointer chains of every reachable crossing position
+// of chunk f (its guard record gr: crossing bits; the chunk before it right)
+// meet, within the G bytes before cs; ~0 if they do not.  Every such
+// position's best path passes through it, so the recurrence started there
+// (value 0, nothing else reachable) gives those positions their true values
+// plus one constant -- and the chunk its true back pointers.
+__device__ uint64_t true_meet(const UniParams &P, const uint32_t *gr, uint64_t cs) {
+    const uint64_t from = cs - P.guard;
+    uint32_t mk[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    int n = 0;
+    for (uint32_t o = P.guard - P.E; o < P.guard; o++)
+        if (((gr[P.guard + (o >> 5)] >> (o & 31)) & 1u) && back_at(P, from + o) != 0) {
+            mk[o >> 5] |= 1u << (o & 31);
+            ++n;
+        }
+    if (n == 0) return ~0ull;
+    for (int o = (int)P.guard - 1; o >= 0; o--) {
+        if (!((mk[o >> 5] >> (o & 31)) & 1u)) continue;
+        if (n == 1) return from + (uint64_t)o;
+        mk[o >> 5] &= ~(1u << (o & 31));
+        const uint32_t v = back_at(P, from + o);
+        const int po = o - (int)(v >> 24);
+        if ((v >> 24) == 0 || po < 0) return ~0ull;
+        if ((mk[po >> 5] >> (po & 31)) & 1u) --n;
+        else mk[po >> 5] |= 1u << (po & 31);
+    }
+    return ~0ull;
+}
+
+// The state at flagged chunk f's start, the chunk before it being right:
+// from where the true chains of f's crossing positions meet when they do
+// (a few tokens back), else from f-1's run start (or the document start when
+// f lies within G bytes of it).
 __device__ __forceinline__ void warp_prefix(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRing &R,
                                             const UGeo &gf, unsigned long long f, bool *sp) {
     const int lane = threadIdx.x & 31;
+    if (gf.cs - gf.ds > P.guard) {
+        uint64_t z = 0;
+        if (lane == 0) z = true_meet(P, P.gback + f * (unsigned long long)P.grec, gf.cs);
+        z = __shfl_sync(kFull, z, 0);
+        if (z != ~0ull) {
+            const uint64_t base = gf.cs - ((gf.cs - z + 31) & ~31ull);   // batches stay aligned to cs
+            ring_start(R, base, z, lane);
+            *sp |= warp_dp(P, lut, eb, R, base, gf.cs, gf.de, 0, [](uint64_t, uint32_t) {},
+                           [](uint32_t, unsigned) {});
+            return;
+        }
+    }
     const UGeo gp = gf.cs - gf.ds <= P.guard ? gf : uni_geo(P, f - 1);
     const uint64_t from = run_from(P, gp);
     ring_start(R, from, from == gp.ds ? gp.ds : next_boundary(P, from, gp.de), lane);
@@ -1154,9 +1198,26 @@ __global__ void __launch_bounds__(kUniEmitThreads) k_uni_emit(UniParams P, unsig
         const unsigned long long w = last - r;
         if (w < P.cap) {
             const uint32_t id = v & 0x00FFFFFFu;
-            P.ids[w] = id == kUnkTid ? P.unk_id : id == kNoTid ? token_id(P, start, v >> 24) : (int32_t)id;
+            if (id == kNoTid && P.tstart) {   // the id is looked up by k_uni_ids, one thread per id
+                P.ids[w] = (int32_t)(v >> 24);
+                P.tstart[w] = (uint32_t)(start - P.text_lo);
+            } else {
+                P.ids[w] = id == kUnkTid ? P.unk_id : id == kNoTid ? token_id(P, start, v >> 24) : (int32_t)id;
+                if (P.tstart) P.tstart[w] = 0xFFFFFFFFu;
+            }
         }
     });
+}
+
+// The ids k_uni_emit left to look up: ids[w] holds the token's length and
+// tstart[w] its start (offset from text_lo; all ones: the id is final).
+__global__ void __launch_bounds__(256) k_uni_ids(UniParams P) {
+    const unsigned long long n = min(P.st->total, P.cap);
+    for (unsigned long long w = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x; w < n;
+         w += (unsigned long long)gridDim.x * blockDim.x) {
+        const uint32_t s = P.tstart[w];
+        if (s != 0xFFFFFFFFu) P.ids[w] = token_id(P, P.text_lo + s, (uint32_t)P.ids[w]);
+    }
 }
 
 __global__ void k_uni_docoff(UniParams P, unsigned long long n_chunks) {
@@ -1360,6 +1421,16 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
         (rc = ensure(ctx, S_UNI_PREFIX, nc * 8 + ((uint64_t)n_docs + 1) * 8, &prefix)) ||
         (rc = ensure(ctx, S_UNI_STATUS, tiles * 8, &status)))
         return rc;
+    // spans up to 63 bytes and 32-bit scores: the warp-per-chunk kernels;
+    // otherwise one thread per chunk with a private ring
+    const bool warp = R == 64 && model->d_fslot;
+    if (warp && h->span < 0xFFFFFFFFull) {   // ids looked up by one thread each after the emit pass
+        void *tst;
+        if ((rc = ensure(ctx, S_UNI_TSTART, std::max<uint64_t>(std::min<uint64_t>(ids_capacity, h->span + 1), 1) * 4,
+                         &tst)))
+            return rc;
+        P.tstart = (uint32_t *)tst;
+    }
     P.back = (uint32_t *)back;
     P.gback = (uint32_t *)gback;
     P.sx = (uint32_t *)info;
@@ -1382,9 +1453,6 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
     const unsigned grid_d = (n_docs + 3) / 4;   // one warp per document
     if (profile) cudaEventRecord(ctx->events[0], s);
     const size_t rep_smem = 4 * kWarpEdgeBytes, warp_smem = kFwdWarps * kWarpEdgeBytes;
-    // spans up to 63 bytes and 32-bit scores: the warp-per-chunk kernels;
-    // otherwise one thread per chunk with a private ring
-    const bool warp = R == 64 && model->d_fslot;
     if (warp) {
         BPE_CUDA(ctx, cudaFuncSetAttribute(k_uni_fwd_warp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)warp_smem),
                  "k_uni_fwd_warp smem");
@@ -1412,6 +1480,7 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
     k_uni_brepair<<<grid_d, 128, 0, s>>>(P);
     if (profile) cudaEventRecord(ctx->events[2], s);
     k_uni_emit<<<(unsigned)tiles, kUniEmitThreads, 0, s>>>(P, nc);
+    if (P.tstart) k_uni_ids<<<(unsigned)std::max(1, ctx->sm_count * 8), 256, 0, s>>>(P);
     if (profile) cudaEventRecord(ctx->events[3], s);
     k_uni_docoff<<<(unsigned)((n_docs + 1 + 255) / 256), 256, 0, s>>>(P, nc);
     BPE_CUDA(ctx, cudaGetLastError(), "unigram_encode launch");
@@ -1433,7 +1502,7 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
     ctx->stats.k[a].bytes = (double)h->span;
     ctx->stats.k[b].bytes = (double)h->fwd_repairs * C + (double)h->bwd_repairs;   // chunks re-run, chunks re-walked
     ctx->stats.k[c].bytes = 4.0 * (double)total;
-    ctx->stats.kernel_launches = warp ? 13 : 12;
+    ctx->stats.kernel_launches = (warp ? 13 : 12) + (P.tstart ? 1 : 0);
     if (profile) {
         float x = 0, y = 0, z = 0;
         cudaEventElapsedTime(&x, ctx->events[0], ctx->events[1]);
