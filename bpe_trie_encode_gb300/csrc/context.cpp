@@ -127,6 +127,14 @@ extern "C" void bpe_ctx_destroy(bpe_ctx *ctx) {
     if (!ctx) return;
     cudaSetDevice(ctx->device);
     cudaStreamSynchronize(ctx->stream);
+    if (ctx->pipe_stream) trie_stream_close(ctx->pipe_stream);
+    if (ctx->pipe_h2d) cudaStreamSynchronize(ctx->pipe_h2d);
+    if (ctx->pipe_d2h) cudaStreamSynchronize(ctx->pipe_d2h);
+    for (auto ev : ctx->pipe_ev)
+        if (ev) cudaEventDestroy(ev);
+    if (ctx->pipe_h2d) cudaStreamDestroy(ctx->pipe_h2d);
+    if (ctx->pipe_d2h) cudaStreamDestroy(ctx->pipe_d2h);
+    if (ctx->pipe_pinned) cudaFreeHost(ctx->pipe_pinned);
     if (ctx->graph.exec) cudaGraphExecDestroy(ctx->graph.exec);
     for (auto &s : ctx->scratch)
         if (s.p) cudaFree(s.p);

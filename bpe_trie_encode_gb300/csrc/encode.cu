@@ -1091,6 +1091,10 @@ extern "C" int trie_stream_push(bpe_stream *st, const uint8_t *d_bytes, uint64_t
 }
 
 namespace bpe {
+void stream_reset(bpe_stream *st) {
+    if (st) st->carry = 0;
+}
+
 // The slice already sits in device memory with at least the trie's longest
 // token length of writable bytes before it: the carry goes there, so the
 // slice itself is not copied.

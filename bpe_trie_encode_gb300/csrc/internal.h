@@ -66,6 +66,16 @@ struct bpe_ctx {
     std::vector<cudaEvent_t> events;
     bpe_stats stats{};
     uint64_t pretok_launches = 0;   // running count of pre-tokenize launches
+    // host pipeline of trie_encode_host, created on first use and kept: its
+    // two copy streams, six events, pinned staging, and the streaming state
+    // for documents longer than a slice (for one trie and longest-token length)
+    cudaStream_t pipe_h2d = nullptr, pipe_d2h = nullptr;
+    cudaEvent_t pipe_ev[6] = {};
+    void *pipe_pinned = nullptr;
+    size_t pipe_pinned_cap = 0;
+    bpe_stream *pipe_stream = nullptr;
+    const bpe_trie *pipe_trie = nullptr;
+    uint32_t pipe_max_len = 0;
 };
 
 namespace bpe {
@@ -92,6 +102,9 @@ int stats_slot(bpe_ctx *ctx, const char *name);
 
 // The bitmap-node layout of a trie, built on its first use (kept with the trie).
 int trie_bitmap_nodes(bpe_ctx *ctx, const bpe_trie *trie);
+
+// Forget a stream's carried bytes (start a new document).
+void stream_reset(bpe_stream *st);
 
 // Streaming push of a slice with writable headroom of the trie's longest
 // token length before it (the carried bytes are placed there).

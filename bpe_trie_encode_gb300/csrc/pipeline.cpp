@@ -23,27 +23,36 @@ struct Unit {
     uint64_t stage;     // a group: where its id offsets land in the pinned staging area
 };
 
-struct Pipe {   // streams, events and pinned staging of one call
-    cudaStream_t h2d = nullptr, d2h = nullptr;
-    cudaEvent_t in_ready[2] = {}, computed[2] = {}, out_free[2] = {};
-    uint64_t *h_off = nullptr;     // 2 slots x (max_nd + 1) rebased document offsets
-    uint64_t *h_ioff = nullptr;    // id offsets of every group
-    bpe_stream *stream = nullptr;
-    ~Pipe() {
-        if (h2d) cudaStreamSynchronize(h2d);
-        if (d2h) cudaStreamSynchronize(d2h);
-        for (int i = 0; i < 2; i++) {
-            if (in_ready[i]) cudaEventDestroy(in_ready[i]);
-            if (computed[i]) cudaEventDestroy(computed[i]);
-            if (out_free[i]) cudaEventDestroy(out_free[i]);
-        }
-        if (h2d) cudaStreamDestroy(h2d);
-        if (d2h) cudaStreamDestroy(d2h);
-        if (h_off) cudaFreeHost(h_off);
-        if (h_ioff) cudaFreeHost(h_ioff);
-        if (stream) trie_stream_close(stream);
+// Waits for the pipeline's copy streams on every exit, so no copy still reads
+// or writes the caller's host buffers after the call returns.
+struct PipeSync {
+    bpe_ctx *ctx;
+    ~PipeSync() {
+        if (ctx->pipe_h2d) cudaStreamSynchronize(ctx->pipe_h2d);
+        if (ctx->pipe_d2h) cudaStreamSynchronize(ctx->pipe_d2h);
     }
 };
+
+// The context's pipeline resources, created on first use; pinned staging of
+// at least `pinned` bytes (grown x1.5).
+int pipe_resources(bpe_ctx *ctx, size_t pinned) {
+    if (!ctx->pipe_h2d) BPE_CUDA(ctx, cudaStreamCreateWithFlags(&ctx->pipe_h2d, cudaStreamNonBlocking), "h2d stream");
+    if (!ctx->pipe_d2h) BPE_CUDA(ctx, cudaStreamCreateWithFlags(&ctx->pipe_d2h, cudaStreamNonBlocking), "d2h stream");
+    for (auto &ev : ctx->pipe_ev)
+        if (!ev) BPE_CUDA(ctx, cudaEventCreateWithFlags(&ev, cudaEventDisableTiming), "event");
+    if (ctx->pipe_pinned_cap < pinned) {
+        if (ctx->pipe_pinned) {
+            BPE_CUDA(ctx, cudaStreamSynchronize(ctx->pipe_d2h), "d2h sync");
+            cudaFreeHost(ctx->pipe_pinned);
+            ctx->pipe_pinned = nullptr;
+            ctx->pipe_pinned_cap = 0;
+        }
+        const size_t cap = std::max(pinned, ctx->pipe_pinned_cap + ctx->pipe_pinned_cap / 2);
+        BPE_CUDA(ctx, cudaMallocHost(&ctx->pipe_pinned, cap), "pinned staging");
+        ctx->pipe_pinned_cap = cap;
+    }
+    return BPE_OK;
+}
 
 constexpr uint64_t kDefaultSlice = 128ull << 20;
 
@@ -93,7 +102,7 @@ extern "C" int trie_encode_host(bpe_ctx *ctx, const bpe_trie *trie, const uint8_
         d = e;
     }
 
-    Pipe pp;
+    PipeSync guard{ctx};
     const uint64_t id_slots = max_bytes + trie->max_len + 16;   // one id per byte, plus a carried tail
     const uint64_t head = ((uint64_t)trie->max_len + 15) & ~15ull;   // room for a slice's carried bytes
     void *din[2], *dout[2], *doff[2];
@@ -104,16 +113,15 @@ extern "C" int trie_encode_host(bpe_ctx *ctx, const bpe_trie *trie, const uint8_
         (rc = ensure(ctx, S_HOST_OFF0, ((uint64_t)max_nd + 1) * 16, &doff[0])) ||
         (rc = ensure(ctx, S_HOST_OFF1, ((uint64_t)max_nd + 1) * 16, &doff[1])))
         return rc;
-    BPE_CUDA(ctx, cudaStreamCreateWithFlags(&pp.h2d, cudaStreamNonBlocking), "h2d stream");
-    BPE_CUDA(ctx, cudaStreamCreateWithFlags(&pp.d2h, cudaStreamNonBlocking), "d2h stream");
-    for (int i = 0; i < 2; i++) {
-        BPE_CUDA(ctx, cudaEventCreateWithFlags(&pp.in_ready[i], cudaEventDisableTiming), "event");
-        BPE_CUDA(ctx, cudaEventCreateWithFlags(&pp.computed[i], cudaEventDisableTiming), "event");
-        BPE_CUDA(ctx, cudaEventCreateWithFlags(&pp.out_free[i], cudaEventDisableTiming), "event");
-        BPE_CUDA(ctx, cudaEventRecord(pp.out_free[i], pp.d2h), "event");
-    }
-    BPE_CUDA(ctx, cudaMallocHost(&pp.h_off, 2 * ((size_t)max_nd + 1) * 8), "pinned offsets");
-    BPE_CUDA(ctx, cudaMallocHost(&pp.h_ioff, std::max<size_t>(stage, 1) * 8), "pinned id offsets");
+    const size_t n_off = 2 * ((size_t)max_nd + 1), n_ioff = std::max<size_t>(stage, 1);
+    if ((rc = pipe_resources(ctx, (n_off + n_ioff) * 8))) return rc;
+    struct {
+        cudaStream_t h2d, d2h;
+        cudaEvent_t *in_ready, *computed, *out_free;
+        uint64_t *h_off, *h_ioff;
+    } pp{ctx->pipe_h2d, ctx->pipe_d2h, ctx->pipe_ev, ctx->pipe_ev + 2, ctx->pipe_ev + 4,
+         (uint64_t *)ctx->pipe_pinned, (uint64_t *)ctx->pipe_pinned + n_off};
+    for (int i = 0; i < 2; i++) BPE_CUDA(ctx, cudaEventRecord(pp.out_free[i], pp.d2h), "event");
 
     cudaStream_t cs = ctx->stream;
     const size_t noff = (size_t)max_nd + 1;
@@ -145,8 +153,19 @@ extern "C" int trie_encode_host(bpe_ctx *ctx, const bpe_trie *trie, const uint8_
         BPE_CUDA(ctx, cudaStreamWaitEvent(cs, pp.out_free[sl], 0), "wait output slot");
         uint64_t n = 0;
         if (u.slice) {
-            if (u.first && !pp.stream && (rc = trie_stream_open(ctx, trie, &pp.stream))) return rc;
-            rc = stream_push_in_place(pp.stream, (uint8_t *)din[sl] + head, u.b1 - u.b0, u.last ? 1 : 0,
+            if (u.first) {   // the context's streaming state, reopened for another trie
+                if (ctx->pipe_stream && (ctx->pipe_trie != trie || ctx->pipe_max_len != trie->max_len)) {
+                    trie_stream_close(ctx->pipe_stream);
+                    ctx->pipe_stream = nullptr;
+                }
+                if (!ctx->pipe_stream) {
+                    if ((rc = trie_stream_open(ctx, trie, &ctx->pipe_stream))) return rc;
+                    ctx->pipe_trie = trie;
+                    ctx->pipe_max_len = trie->max_len;
+                }
+                stream_reset(ctx->pipe_stream);
+            }
+            rc = stream_push_in_place(ctx->pipe_stream, (uint8_t *)din[sl] + head, u.b1 - u.b0, u.last ? 1 : 0,
                                       (int32_t *)dout[sl], id_slots, &n);
         } else {
             rc = trie_encode(ctx, trie, (const uint8_t *)din[sl], (const uint64_t *)doff[sl], u.nd,
