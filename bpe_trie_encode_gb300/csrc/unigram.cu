@@ -72,7 +72,7 @@ constexpr uint32_t kRoot = 0x00FFFFFFu;    // speculative start (length 0 never 
 constexpr uint32_t kUnkTid = 0x00FFFFFFu;
 constexpr uint32_t kNoTid = 0x00FFFFFEu;     // a token whose id the emit pass looks up from its bytes
 constexpr long long kNeg = -0x7FFFFFFFFFFFFFFFll - 1;   // -inf
-constexpr uint32_t kUniDefaultChunk = 512;
+constexpr uint32_t kUniDefaultChunk = 768;   // measured on the batch workload: 512 3.90 ms, 768 3.69, 1024 3.99, 2048 4.73
 constexpr unsigned kUniSpinLimit = 1u << 22;
 enum : uint32_t { UERR_SPAN = 8u, UERR_OOB = 4u, UERR_TIMEOUT = 2u, UERR_CONT_START = 16u };
 

@@ -112,7 +112,7 @@ const char *bpe_last_error(const bpe_ctx *ctx);
  *                          base|TERM; built on a trie's first use (n_slots x
  *                          64 bytes, kept until trie_free)
  *   BPE_OPT_UNI_CHUNK    bytes per chunk of unigram_encode (256 .. 4096, a
- *                        multiple of 64; 0 = default 512)
+ *                        multiple of 64; 0 = default 768)
  *   BPE_OPT_PERSISTENT   1 = with BPE_MERGE_TWO_PASS, the merge loop runs as one cooperative
  *                        launch per window of merges (all CTAs resident,
  *                        phases separated by grid barriers) instead of a CUDA
