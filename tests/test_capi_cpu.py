@@ -51,8 +51,11 @@ def test_null_arguments_rejected():
     assert lib.bpe_ctx_set_option(None, 1, 0) == -1
     assert lib.bpe_train(None, None, 0, 0, None, None, None, None) == -1
     assert lib.trie_encode(None, None, None, None, 0, None, 0, None, None) == -1
+    assert lib.unigram_create(None, None, None, 0, 0, 0.0, None) == -1
+    assert lib.unigram_encode(None, None, None, None, 0, None, 0, None, None) == -1
     lib.bpe_ctx_destroy(None)
     lib.trie_free(None)
+    lib.unigram_free(None)
 
 
 def da_longest(check, base, tid, data: bytes, p: int, end: int):
