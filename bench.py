@@ -287,14 +287,17 @@ def extra_legs(args, ctx, dev, stream, flush, d_text, d_sym, n_merges, peak, pea
         "ms_per_step": round(ms_bm / args.steps, 3), "n_ids": int(r2[0].numel()),
         "vs_double_array": round(ms_all / ms_bm, 3),
         "workload": "the batch encode above with 64-byte bitmap nodes instead of the double array"}
-    out["unigram_batch"] = unigram_leg(args, ctx, stream, flush, trie, voff, d_data, d_off, ids, peak, peak_kind)
+    out["unigram_batch"] = unigram_leg(args, ctx, stream, flush, trie, voff, d_data, d_off, ids, peak, peak_kind,
+                                       vb=vb, data=data, doc_off=doc_off)
     return out
 
 
-def unigram_leg(args, ctx, stream, flush, trie, voff, d_data, d_off, ids, peak, peak_kind):
+def unigram_leg(args, ctx, stream, flush, trie, voff, d_data, d_off, ids, peak, peak_kind, vb=None, data=None,
+                doc_off=None):
     """Unigram (Viterbi) encoding of the batch documents on the batch trie,
     synthetic float32 Zipf log-probabilities; W warm-up and K timed steps,
-    the L2 flushed before each."""
+    the L2 flushed before each.  With the host copies of the vocabulary and
+    documents, the oracle is timed on the first 8 documents (rank 0)."""
     import torch
 
     import bpe_trie_encode_gb300 as bt
@@ -321,9 +324,20 @@ def unigram_leg(args, ctx, stream, flush, trie, voff, d_data, d_off, ids, peak, 
     fwd = kern.get("unigram_fwd", {"ms": 0.0, "launches": 1})
     fwd_ms = fwd["ms"] / max(fwd["launches"], 1)
     fwd_gbs = 5.0 * nbytes / (fwd_ms / 1e3) / 1e9 if fwd_ms else 0.0
+    cpu = None
+    if vb is not None and not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:
+        import oracle
+        n8 = int(doc_off[8])
+        t0 = time.perf_counter()
+        oracle.Trie(vb, voff).unigram_encode(data[:n8], scores, voff.size - 1, unk, doc_off[:9])
+        dt = time.perf_counter() - t0
+        cpu = {"value": round(n8 / dt / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"the first 8 documents ({n8} B), same model, single thread, {cpu_model()}",
+               "seconds": round(dt, 2)}
     return {
         "value": round(args.steps * nbytes / (ms_u / 1e3) / 1e9, 3), "unit": "GB/s",
         "ms_per_step": round(ms_u / args.steps, 3), "n_ids": int(r3[0].numel()),
+        "cpu_baseline": cpu,
         "workload": "the batch documents, most likely segmentation (Viterbi) under synthetic Zipf "
                     "log-probabilities (float32) for the 250,000 tokens",
         "kernels": {k2: {"launches": v["launches"], "ms": round(v["ms"], 3)} for k2, v in kern.items()},
@@ -358,7 +372,7 @@ def run_unigram_only(args):
     ids = torch.empty(data.size, dtype=torch.int32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     out = unigram_leg(args, ctx, torch.cuda.current_stream(dev), flush, trie, voff, d_data, d_off, ids, peak,
-                      peak_kind)
+                      peak_kind, vb=vb, data=data, doc_off=doc_off)
     out = {"leg": "unigram_batch", **out}
     ctx.close()
     return out
