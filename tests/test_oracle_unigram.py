@@ -181,3 +181,52 @@ def test_scores_are_log_probabilities():
     assert np.array_equal(s, s.astype(np.float32).astype(np.float64))
     assert np.array_equal(s, synth.unigram_scores(5000))
     assert len(np.unique(s)) == s.size
+
+
+def test_best_score_equals_shortest_path():
+    """With scores <= 0 the best segmentation is a shortest path from 0 to n
+    over positions (edge weight -score), found here by scipy's Dijkstra on
+    texts of a few thousand bytes -- beyond what brute force enumerates.
+    Scores are multiples of 1/8, so every sum is exact in either order."""
+    from scipy.sparse import csr_matrix
+    from scipy.sparse.csgraph import dijkstra
+    rng = random.Random(21)
+    for trial in range(12):
+        tokens = []
+        while len(tokens) < 200:
+            t = b"".join(rng.choice([b"a", b"b", b"c", "ı".encode(), "ş".encode()])
+                         for _ in range(rng.randint(1, 5)))
+            if rng.random() < 0.1:
+                t = t[: rng.randint(1, len(t))]
+            tokens.append(t)
+        scores = [-rng.randint(1, 80) / 8.0 for _ in tokens]
+        unk_score = -20.0
+        text = b"".join(rng.choice([b"a", b"b", b"c", b"d", "ı".encode(), "ş".encode()])
+                        for _ in range(rng.randint(500, 3000)))
+        n = len(text)
+        first = {}
+        for t, tok in enumerate(tokens):
+            first.setdefault(tok, t)
+        rows, cols, w = [], [], []
+        for i in range(n):
+            if cont(text[i]):
+                continue
+            matched = False
+            for L in range(1, 16):
+                j = i + L
+                if j > n:
+                    break
+                t = first.get(text[i:j])
+                if t is not None and (j == n or not cont(text[j])):
+                    rows.append(i); cols.append(j); w.append(-scores[t]); matched = True
+            if not matched:
+                j = i + 1
+                while j < n and cont(text[j]):
+                    j += 1
+                rows.append(i); cols.append(j); w.append(-unk_score)
+        # every weight is at least 1/8: none vanishes from the sparse matrix
+        g = csr_matrix((w, (rows, cols)), shape=(n + 1, n + 1))
+        dist = dijkstra(g, directed=True, indices=0)[n]
+        T = oracle.Trie(*vocab(tokens))
+        ids, _ = T.unigram_encode(text, scores, len(tokens), unk_score)
+        assert path_score(ids.tolist(), tokens, scores, len(tokens), unk_score) == -dist
