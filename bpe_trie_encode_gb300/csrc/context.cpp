@@ -176,6 +176,9 @@ extern "C" int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value) {
     case BPE_OPT_PERSISTENT:
         ctx->persistent = value ? 1 : 0;
         return BPE_OK;
+    case BPE_OPT_TEST_STALL_TILE:
+        ctx->test_stall_tile = value < 0 ? -1 : value;
+        return BPE_OK;
     case BPE_OPT_UNI_CHUNK:
         if (value != 0 && (value < 256 || value > 4096 || value % 64))
             return fail(ctx, BPE_ERR_INVALID_ARG, "unigram chunk %lld not 0 or in 256..4096 in steps of 64",

@@ -60,6 +60,7 @@ struct bpe_ctx {
     int persistent = 0;
     int trie_layout = 0;   // BPE_TRIE_*
     int uni_chunk = 0;     // unigram_encode chunk bytes (0: default)
+    long long test_stall_tile = -1;   // BPE_OPT_TEST_STALL_TILE
     // cached graph of merge iterations
     bpe::TrainGraph graph;
     // profiling events (grown on demand)

@@ -112,10 +112,12 @@ struct UniParams {
     const int4 *fslot;  // the slots with their token's score and id (warp kernels)
     long long unk;
     int32_t unk_id;
+    unsigned long long stall_tile;   // testing: this emit tile never publishes (~0: none)
     unsigned long long text_lo;   // doc_off[0]
     unsigned long long text_end;  // doc_off[n_docs]
     uint32_t *back;     // per position (offset from text_lo), span + 1 words
     uint32_t *tstart;   // per id: its token's start for k_uni_ids (null: emit looks ids up itself)
+    unsigned long long tstart_n;   // its entries
     uint32_t *gback;    // per chunk grec words: the guard's back pointers and crossing bits
     uint32_t *fflag, *bflag;   // bitmaps over chunks
     uint32_t *okn;             // bitmap: a flagged chunk's parallel repair was valid for its successor too
@@ -1155,7 +1157,7 @@ __global__ void __launch_bounds__(kUniEmitThreads) k_uni_emit(UniParams P, unsig
     if (warp == 0) {
         unsigned long long off = 0;
         if (t > 0) {
-            if (lane == 0) st_relaxed(P.status + t, 1ull | ((unsigned long long)tsum << 2));
+            if (lane == 0 && t != P.stall_tile) st_relaxed(P.status + t, 1ull | ((unsigned long long)tsum << 2));
             long long jhi = (long long)t - 1;
             unsigned spins = 0;
             for (;;) {
@@ -1182,7 +1184,7 @@ __global__ void __launch_bounds__(kUniEmitThreads) k_uni_emit(UniParams P, unsig
             }
         }
         if (lane == 0) {
-            st_relaxed(P.status + t, 2ull | ((off + tsum) << 2));
+            if (t != P.stall_tile) st_relaxed(P.status + t, 2ull | ((off + tsum) << 2));
             if (t == ntiles - 1) P.st->total = off + tsum;
             s_off = off;
         }
@@ -1198,12 +1200,12 @@ __global__ void __launch_bounds__(kUniEmitThreads) k_uni_emit(UniParams P, unsig
         const unsigned long long w = last - r;
         if (w < P.cap) {
             const uint32_t id = v & 0x00FFFFFFu;
-            if (id == kNoTid && P.tstart) {   // the id is looked up by k_uni_ids, one thread per id
+            if (id == kNoTid && P.tstart && w < P.tstart_n) {   // the id is looked up by k_uni_ids, one thread per id
                 P.ids[w] = (int32_t)(v >> 24);
                 P.tstart[w] = (uint32_t)(start - P.text_lo);
             } else {
                 P.ids[w] = id == kUnkTid ? P.unk_id : id == kNoTid ? token_id(P, start, v >> 24) : (int32_t)id;
-                if (P.tstart) P.tstart[w] = 0xFFFFFFFFu;
+                if (P.tstart && w < P.tstart_n) P.tstart[w] = 0xFFFFFFFFu;
             }
         }
     });
@@ -1212,7 +1214,7 @@ __global__ void __launch_bounds__(kUniEmitThreads) k_uni_emit(UniParams P, unsig
 // The ids k_uni_emit left to look up: ids[w] holds the token's length and
 // tstart[w] its start (offset from text_lo; all ones: the id is final).
 __global__ void __launch_bounds__(256) k_uni_ids(UniParams P) {
-    const unsigned long long n = min(P.st->total, P.cap);
+    const unsigned long long n = min(min(P.st->total, P.cap), P.tstart_n);
     for (unsigned long long w = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x; w < n;
          w += (unsigned long long)gridDim.x * blockDim.x) {
         const uint32_t s = P.tstart[w];
@@ -1390,6 +1392,7 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
     P.fslot = (const int4 *)model->d_fslot;
     P.unk = model->unk;
     P.unk_id = model->unk_id;
+    P.stall_tile = ctx->test_stall_tile >= 0 ? (unsigned long long)ctx->test_stall_tile : ~0ull;
     P.ids = d_ids_out;
     P.cap = ids_capacity;
     P.st = (UniState *)state;
@@ -1426,9 +1429,8 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
     const bool warp = R == 64 && model->d_fslot;
     if (warp && h->span < 0xFFFFFFFFull) {   // ids looked up by one thread each after the emit pass
         void *tst;
-        if ((rc = ensure(ctx, S_UNI_TSTART, std::max<uint64_t>(std::min<uint64_t>(ids_capacity, h->span + 1), 1) * 4,
-                         &tst)))
-            return rc;
+        P.tstart_n = std::max<uint64_t>(std::min<uint64_t>(ids_capacity, h->span + 1), 1);
+        if ((rc = ensure(ctx, S_UNI_TSTART, P.tstart_n * 4, &tst))) return rc;
         P.tstart = (uint32_t *)tst;
     }
     P.back = (uint32_t *)back;

@@ -113,6 +113,11 @@ const char *bpe_last_error(const bpe_ctx *ctx);
  *                          64 bytes, kept until trie_free)
  *   BPE_OPT_UNI_CHUNK    bytes per chunk of unigram_encode (256 .. 4096, a
  *                        multiple of 64; 0 = default 768)
+ *   BPE_OPT_TEST_STALL_TILE  testing only: in unigram_encode the scan tile
+ *                        with this ticket never publishes its prefix, so the
+ *                        tiles after it wait until their bounded wait gives up
+ *                        and the call returns BPE_ERR_TIMEOUT (the context
+ *                        stays usable); -1 = off (default)
  *   BPE_OPT_PERSISTENT   1 = with BPE_MERGE_TWO_PASS, the merge loop runs as one cooperative
  *                        launch per window of merges (all CTAs resident,
  *                        phases separated by grid barriers) instead of a CUDA
@@ -126,7 +131,8 @@ enum {
     BPE_OPT_MERGE = 6,
     BPE_OPT_PERSISTENT = 7,
     BPE_OPT_TRIE_LAYOUT = 8,
-    BPE_OPT_UNI_CHUNK = 9
+    BPE_OPT_UNI_CHUNK = 9,
+    BPE_OPT_TEST_STALL_TILE = 10
 };
 enum { BPE_TRIE_DOUBLE_ARRAY = 0, BPE_TRIE_BITMAP = 1 };
 enum { BPE_MERGE_TWO_PASS = 0, BPE_MERGE_LOOKBACK = 1, BPE_MERGE_TILES = 2 };

@@ -251,6 +251,27 @@ def test_errors(ctx):
     check_unigram(ctx, vb, off, [-1.0, -1.0], 2, -9.0, [b"a" + b"\x80" * 40 + b"b"])
 
 
+def test_bounded_wait_times_out(ctx):
+    """A scan tile that never publishes: the tiles after it give up their
+    bounded wait, the call returns TIMEOUT, and the context keeps working."""
+    import bpe_trie_encode_gb300 as bt
+    from bpe_trie_encode_gb300 import _capi
+    rng = random.Random(12)
+    toks, scores = random_model(rng, 300)
+    vb, off = vocab_arrays(toks)
+    data = b"".join(rng.choice(ALPHA) for _ in range(400_000))   # about 2,000 chunks: 8 scan tiles
+    trie = ctx.trie_build(vb, off)
+    model = ctx.unigram(trie, scores, len(toks), -30.0)
+    ctx.set_option(_capi.BPE_OPT_TEST_STALL_TILE, 1)
+    try:
+        with pytest.raises(bt.BpeError) as e:
+            ctx.unigram_encode(model, dev_u8(data))
+        assert e.value.name == "TIMEOUT"
+    finally:
+        ctx.set_option(_capi.BPE_OPT_TEST_STALL_TILE, -1)
+    check_unigram(ctx, vb, off, scores, len(toks), -30.0, [data[:50_000]])
+
+
 def unigram_workload(ctx, golden, name, data, doc_off, vb, off):
     g = golden[name]
     assert sha(data) == g["text_sha256"]
