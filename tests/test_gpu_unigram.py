@@ -211,6 +211,17 @@ def test_unknown_characters(ctx):
     assert (got == 4).sum() > 0
 
 
+def test_many_small_documents(ctx):
+    """20,000 documents of 0..60 bytes: the per-document index, repair and
+    offset kernels over many documents, most of them one chunk or empty."""
+    rng = random.Random(31)
+    toks, scores = random_model(rng, 500)
+    vb, off = vocab_arrays(toks)
+    docs = [b"".join(rng.choice(ALPHA) for _ in range(rng.choice([0, 0, 1, 2, 7, 20, 60])))
+            for _ in range(20_000)]
+    check_unigram(ctx, vb, off, scores, len(toks), -30.0, docs, chunk=256)
+
+
 def test_degenerate_inputs(ctx):
     vb, off = vocab_arrays([b"a", b"b"])
     check_unigram(ctx, vb, off, [-1.0, -1.0], 2, -9.0, [b""])
