@@ -518,6 +518,7 @@ def run_ours(args, rank, world, local_rank):
             h_ioff_buf = torch.empty(enc["h_off"].numel(), dtype=torch.int64)
         tr_ms = en_ms = 0.0
         d2h_ids = 0
+        en_steps = []
         for i in range(args.warmup + args.steps):
             flush.fill_(1)
             torch.cuda.synchronize(dev)
@@ -536,13 +537,17 @@ def run_ours(args, rank, world, local_rank):
             if i >= args.warmup:
                 tr_ms += a.elapsed_time(b)
                 en_ms += b.elapsed_time(c)
+                en_steps.append(round(b.elapsed_time(c), 2))
         (tr_ms, en_ms), (e2e_merges, e2e_bytes) = reduce_ranks(
             [tr_ms, en_ms], [args.steps * m.shape[0], args.steps * enc["bytes"] if enc else 0], world, dev)
         e2e = {"value": round(throughput(e2e_merges, tr_ms), 2), "unit": "merges/s",
                "h2d_bytes_per_step": int(text.size + (enc["bytes"] + enc["h_off"].numel() * 8 if enc else 0)),
                "d2h_bytes_per_step": int(h_merges_bytes + d2h_ids)}
         if enc:
-            e2e["encode"] = {"value": round(throughput(e2e_bytes, en_ms) / 1e9, 3), "unit": "GB/s"}
+            e2e["encode"] = {"value": round(throughput(e2e_bytes, en_ms) / 1e9, 3), "unit": "GB/s",
+                             "steps_ms": en_steps,   # rank 0's; some steps stall
+                             "median_GBs": round(enc["bytes"] / (sorted(en_steps)[len(en_steps) // 2] / 1e3) / 1e9, 3)
+                             if en_steps else None}
 
     # ---- extra legs: the word-frequency trainer (same merges), the large
     # training workload, the batch encode workload

@@ -54,7 +54,7 @@ struct bpe_ctx {
     int table_log2 = 0;
     int use_graph = 1;
     int profile = 0;
-    int chunk = 128;
+    int chunk = 256;   // trie_encode bytes per chunk (measured best on both encode workloads)
     int train_words = 0;
     int merge_mode = 0;   // BPE_MERGE_*
     int persistent = 0;

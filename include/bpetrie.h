@@ -84,7 +84,8 @@ const char *bpe_last_error(const bpe_ctx *ctx);
  *                        bpe_train / trie_encode so bpe_last_stats() reports
  *                        per-kernel device time (implies host launches)
  *   BPE_OPT_CHUNK        trie_encode bytes per chunk (64..256, multiple
- *                        of 32; default 128)
+ *                        of 32; default 256; chunks shorter than a few of
+ *                        the vocabulary's longest tokens resynchronise badly)
  *   BPE_OPT_TRAIN_WORDS  1 = bpe_train runs the merge loop over distinct
  *                        words weighted by their number of occurrences
  *                        (the same merges and final stream: no count or merge

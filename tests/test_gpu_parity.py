@@ -266,7 +266,7 @@ def check_encode(ctx, vb, off, docs, chunk=None):
         ids, id_off = ctx.encode(trie, dev_u8(data) if data else torch.empty(0, dtype=torch.uint8, device="cuda"),
                                  torch.from_numpy(doc_off).cuda())
     finally:
-        ctx.set_option(bt.BPE_OPT_CHUNK, 128)
+        ctx.set_option(bt.BPE_OPT_CHUNK, 256)
     wids, woff = oracle.Trie(vb, off).encode(data, doc_off.astype(np.uint64))
     assert np.array_equal(ids.cpu().numpy(), wids)
     assert np.array_equal(id_off.cpu().numpy().astype(np.uint64), woff)
