@@ -5,42 +5,51 @@
 // trie node, [UNIGRAM] "Baseline" and "Bitmap and inline packing").
 //
 // The recurrence is sequential along a document; the GPU splits every
-// document into chunks of C bytes, one thread per chunk, and makes the
-// sequential result exact by speculation and repair.  Scores are summed in
-// 64-bit fixed point, so sums are associative and a path's decisions do not
-// depend on the constant its values start from.
+// document into chunks of C bytes and makes the sequential result exact by
+// speculation and repair.  Scores are summed in fixed point, so sums are
+// associative and a path's decisions do not depend on the constant its
+// values start from.
 //
-//   k_uni_index   first chunk of every document, longest document
-//   k_uni_fwd     each thread runs the recurrence from the first character
-//                 boundary G bytes before its chunk (value 0 there, nothing
-//                 reachable before) through its chunk, and stores the back
-//                 pointer (token length, id) of every position: those of the
-//                 chunk in the output array, those of the guard privately.
-//   k_uni_check   the chunk's guard ran the recurrence from a wrong start
-//                 value, but if the back-pointer chains of every reachable
-//                 position of the last E bytes before the chunk (E = longest
-//                 edge) meet at one position z, and the guard's back pointers
-//                 equal the previous chunk's from z on, the guard's values
-//                 there are the true ones plus one constant -- and so are the
-//                 chunk's.  A chunk for which that fails is flagged.
-//   k_uni_frepair one thread per document with a flagged chunk re-runs the
-//                 recurrence, in order, from the chunk before each flagged
-//                 one through the chunks after it until a chunk passes the
-//                 check against the repaired back pointers.
-//   k_uni_bspec   each thread backtracks speculatively from a reachable
-//                 position H bytes past its chunk's end; back-pointer chains
-//                 merge, so where the chain first steps to or below the
-//                 chunk's end (sx) is usually where the true path does.  It
-//                 counts the tokens starting in the chunk and records the
-//                 chain's last position in the chunk (bot).
-//   k_uni_brepair the true sx of a chunk is the next chunk's bot (the
-//                 document end for the last chunk); one thread per document
-//                 re-walks, right to left, the chunks where they differ.
-//   k_uni_emit    exclusive scan of the counts (decoupled look-back) and a
-//                 walk of every chunk from its true sx that writes its ids.
-//   k_uni_docoff  per-document id offsets.
+//   k_uni_index    first chunk of every document, longest document
+//   k_uni_fwd_warp one warp per chunk runs the recurrence from the first
+//                  character boundary G bytes before its chunk (value 0
+//                  there, nothing reachable before) through its chunk: lanes
+//                  walk the trie from 32 positions at once into shared
+//                  memory, then relax them in order with the window of values
+//                  in registers (int32, relative to the window's best).  It
+//                  stores the back pointer of every position: the chunk's in
+//                  the output array, the guard's in a private record with the
+//                  guard positions whose edges reach the chunk ("crossing").
+//                  (k_uni_fwd: the same with one thread per chunk and a
+//                  64-bit ring, for spans over 63 bytes or wide scores.)
+//   k_uni_check    the guard ran from a wrong start value, but if the chains
+//                  of the reachable crossing positions step like the true
+//                  chains (the previous chunk's back pointers) until they
+//                  meet at one position the true recurrence reaches, their
+//                  values are the true ones plus one constant -- and so are
+//                  the chunk's.  A chunk for which that fails is flagged.
+//   k_uni_fix_a    one warp per flagged chunk re-runs it from its
+//                  predecessor's state (right when the predecessor is) and
+//                  notes whether the next chunk then passes its check;
+//   k_uni_frepair_warp  one warp per document keeps those results where they
+//                  hold and re-runs chains of chunks where they do not.
+//   k_uni_bspec    each thread backtracks speculatively from a reachable
+//                  position past its chunk's end; back-pointer chains merge,
+//                  so where the chain enters the chunk (sx) is usually where
+//                  the true path does.  It counts the chunk's tokens and
+//                  records where the chain leaves it (bot).
+//   k_uni_bcheck, k_uni_bfix_a, k_uni_brepair  the true sx of a chunk is the
+//                  next chunk's bot (the document end for the last chunk):
+//                  chunks where they differ are walked again, in parallel
+//                  where the next chunk is right, right to left otherwise.
+//   k_uni_emit     exclusive scan of the counts (decoupled look-back) and a
+//                  walk of every chunk from its true sx that writes its ids;
+//   k_uni_ids      one thread per id finds the ids the warp kernels left to
+//                  the token's bytes.
+//   k_uni_docoff   per-document id offsets.
 //
-// A back pointer is (length << 24) | id, id 0xFFFFFF for <unk>; 0 marks an
+// A back pointer is (length << 24) | id, with id 0xFFFFFF for <unk> and
+// kNoTid where the id is found from the token's bytes; 0 marks an
 // unreachable position and kRoot the start of a speculative run.
 #include <algorithm>
 #include <cmath>
