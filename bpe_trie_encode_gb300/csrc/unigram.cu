@@ -523,155 +523,187 @@ struct EdgeBuf {
           text((uint8_t *)(base + 32 * kEdgeStride + kLongRows * 32 + 4)) {}
 };
 
+// What one lane's walk of a batch leaves for the recurrence: its edge
+// lengths as masks (1..32, 33..63), its long row, whether its only edge is
+// <unk>, whether an edge reaches cs, and whether a long row was missing.
+struct WalkOut {
+    uint32_t X, Y;
+    int lr;
+    bool unk, crossing, spread;
+};
+
+// Walk: every lane walks the trie from its position b0 + lane (reachable or
+// not) over the batch's text staged in shared memory, and records its edges'
+// scores by length in its row (a long row for lengths over 32).
+__device__ __forceinline__ WalkOut walk_batch(const UniParams &P, const int4 *lut, const EdgeBuf &eb, uint64_t b0,
+                                              uint64_t to, uint64_t de, uint64_t cs) {
+    const int lane = threadIdx.x & 31;
+    int32_t *row = eb.score + lane * kEdgeStride;
+    // stage text [b0, b0 + 128) (what lies before the text's end)
+#pragma unroll
+    for (int i = 0; i < kTextStage / 32; i++) {
+        const uint64_t p = b0 + i * 32 + lane;
+        eb.text[i * 32 + lane] = p < P.text_end ? byte_at(P, p) : 0u;
+    }
+    if (lane == 0) *eb.lcount = 0;
+    __syncwarp();
+    WalkOut w{0u, 0u, -1, false, false, false};
+    const uint64_t q = b0 + lane;
+    unsigned long long M = 0;   // bit len: an edge of that length
+    if (q < to) {
+        const uint32_t dlen = de - q < 64 ? (uint32_t)(de - q) : 64u;   // bytes to the document end (capped)
+        const uint32_t lim = min(dlen, P.E);
+        const uint32_t csr = q >= cs ? 0u : cs - q < 64 ? (uint32_t)(cs - q) : 64u;
+        const uint8_t *tx = eb.text + lane;
+        const uint32_t c0 = tx[0];
+        if (!is_cont(c0)) {
+            const int4 r = lut[c0];
+            if (r.x >= 0) {
+                int32_t node = r.x;
+                uint32_t y = (uint32_t)r.y;
+                int32_t sc = r.z;
+                uint32_t len = 1;
+                for (;;) {
+                    const uint32_t nb = len < dlen ? tx[len] : 0u;
+                    if ((y & kTermBit) && (len == dlen || !is_cont(nb))) {
+                        if (len <= 32) {
+                            row[len - 1] = sc;
+                        } else {
+                            if (w.lr < 0) w.lr = atomicAdd(eb.lcount, 1);
+                            if (w.lr < kLongRows) eb.lrow[w.lr * 32 + (len - 33)] = sc;
+                            else w.spread = true;   // no long row left: the run is redone exactly
+                        }
+                        M |= 1ull << len;
+                        w.crossing |= len >= csr;
+                    }
+                    const uint32_t base = y & ~kTermBit;
+                    if (len >= lim || base == 0) break;
+                    const int32_t t = (int32_t)(base + nb);
+                    const int4 v = __ldg(P.fslot + t);
+                    if (v.x != node) break;
+                    node = t;
+                    y = (uint32_t)v.y;
+                    sc = v.z;
+                    ++len;
+                }
+            }
+            if (M == 0) {   // <unk> to the next character boundary
+                uint32_t len = 1;
+                while (len < dlen && len <= P.E && is_cont(len < kTextStage - lane ? tx[len] : byte_at(P, q + len)))
+                    ++len;
+                if (len > P.E) {
+                    atomicOr(&P.st->err, UERR_SPAN);
+                    len = P.E;
+                }
+                if (len <= 32) {
+                    row[len - 1] = (int32_t)P.unk;
+                } else {
+                    w.lr = atomicAdd(eb.lcount, 1);
+                    if (w.lr < kLongRows) eb.lrow[w.lr * 32 + (len - 33)] = (int32_t)P.unk;
+                    else w.spread = true;
+                }
+                M = 1ull << len;
+                w.unk = true;
+                w.crossing = len >= csr;
+            }
+        }
+    }
+    w.X = (uint32_t)(M >> 1);
+    w.Y = (uint32_t)(M >> 33);
+    return w;
+}
+
+// Recurrence over the batch at b0 (= R.b0) from the walk's rows in eb and
+// this lane's walk results: the batch's positions in order; source s's value
+// comes from lane s, and every lane relaxes its o1 and o1 + 32 targets (a bit
+// of s's masks rotated by s + 1) from shared memory and shuffles only.
+// sink(q, bp) receives every final position.  Returns whether this lane saw
+// a value beyond kSpread.
+template <typename Sink>
+__device__ __forceinline__ bool dp_batch(const EdgeBuf &eb, WarpRing &R, uint64_t b0, uint64_t to, const WalkOut &w,
+                                         Sink sink) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t mybit = 1u << lane;
+    const uint64_t q = b0 + lane;
+    bool spread = false;
+    const uint32_t xrot = __funnelshift_l(w.X, w.X, lane + 1), yrot = __funnelshift_l(w.Y, w.Y, lane + 1);
+    const uint32_t mycode = ((uint32_t)(q - R.base) & 0x7FFFFFFFu) | ((uint32_t)w.unk << 31);
+    const int lr = w.lr;
+    // rebase: the window's best reachable value becomes 0
+    const int32_t mx = __reduce_max_sync(kFull, max(R.a, R.b));
+    if (mx != kNeg32) {
+        if (R.a != kNeg32) {
+            const long long v = (long long)R.a - mx;
+            spread |= v < -kSpread;
+            R.a = (int32_t)max(v, (long long)-kSpread);
+        }
+        if (R.b != kNeg32) {
+            const long long v = (long long)R.b - mx;
+            spread |= v < -kSpread;
+            R.b = (int32_t)max(v, (long long)-kSpread);
+        }
+    }
+    __syncwarp();
+    int32_t fv = kNeg32;
+    uint32_t fs = 0;
+    const uint32_t nsrc = (uint32_t)(to - b0 < 32 ? to - b0 : 32);
+    const bool anylong = __any_sync(kFull, w.Y != 0u);   // some edge over 32 bytes (rare)
+    // source s of the batch; o1 = this lane's length to reach its A position
+    auto source = [&](uint32_t s, uint32_t o1) {
+        const int32_t b = __shfl_sync(kFull, R.a, s);
+        const uint32_t xr = __shfl_sync(kFull, xrot, s);
+        const uint32_t code = __shfl_sync(kFull, mycode, s);
+        const uint32_t yr = anylong ? __shfl_sync(kFull, yrot, s) : 0u;
+        const int slr = yr ? __shfl_sync(kFull, lr, s) : 0;   // s's long row (lengths 33..63)
+        if (lane == (int)s) {   // position b0 + s is final; the next window position moves in
+            fv = R.a;
+            fs = R.sa;
+            R.a = R.b;
+            R.sa = R.sb;
+            R.b = kNeg32;
+        }
+        if (b == kNeg32) return;
+        if (xr & mybit) {
+            const int32_t cand = b + eb.score[s * kEdgeStride + (o1 - 1)];
+            if (cand > R.a) { R.a = cand; R.sa = code; }
+        }
+        if ((yr & mybit) && slr < kLongRows) {   // length o1 + 32
+            const int32_t cand = b + eb.lrow[slr * 32 + (o1 - 1)];
+            if (cand > R.b) { R.b = cand; R.sb = code; }
+        }
+    };
+    const uint32_t o10 = lane == 0 ? 32u : (uint32_t)lane;   // this lane's length o1 from source 0
+    if (nsrc == 32) {
+#pragma unroll
+        for (uint32_t s = 0; s < 32; s++) source(s, ((o10 - 1u - s) & 31u) + 1u);
+    } else {
+        for (uint32_t s = 0; s < nsrc; s++) source(s, ((o10 - 1u - s) & 31u) + 1u);
+    }
+    spread |= fv != kNeg32 && (fv < -kSpread || fv > kSpread);   // every source value stayed in range
+    __syncwarp();
+    if (q < to) sink(q, ring_bp(R, q, fv, fs));
+    R.b0 = b0 + 32;
+    return spread;
+}
+
 // The recurrence over positions [from, to) of a document ending at de, by one
 // warp (from = R.b0), 32 positions at a time, on the slots that carry their
-// token's score (fslot; lut: the depth-1 nodes).  Walk: every lane walks the
-// trie from its position (reachable or not) over the batch's text staged in
-// shared memory, records its edges' scores by length in its row (a long row
-// for lengths over 32) and their lengths as bit masks (1..32, 33..63); cross(m, bits) receives, per batch m,
-// which positions have an edge reaching cs or beyond.  Recurrence: the
-// batch's positions in order; source s's value comes from lane s, and every
-// lane relaxes its o1 and o1 + 32 targets (a bit of s's masks rotated by
-// s + 1) from shared memory and shuffles only.  A back pointer holds the
+// token's score (fslot; lut: the depth-1 nodes): a walk, then the
+// recurrence, per batch.  cross(m, bits) receives, per batch m, which
+// positions have an edge reaching cs or beyond.  A back pointer holds the
 // length and kNoTid (the emit pass finds the id from the token's bytes) or
-// kUnkTid.  sink(q, bp) receives every final position.  Returns whether the
-// values spread beyond kSpread (then the run is incomplete).
+// kUnkTid.  Returns whether the values spread beyond kSpread or a long row
+// was missing (then the run is incomplete).
 template <typename Sink, typename Cross>
 __device__ bool warp_dp(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRing &R, uint64_t from,
                         uint64_t to, uint64_t de, uint64_t cs, Sink sink, Cross cross) {
     const int lane = threadIdx.x & 31;
-    const uint32_t mybit = 1u << lane;
-    int32_t *row = eb.score + lane * kEdgeStride;
     bool spread = false;
     for (uint64_t b0 = from; b0 < to; b0 += 32) {
-        // stage text [b0, b0 + 128) (what lies before the text's end)
-#pragma unroll
-        for (int i = 0; i < kTextStage / 32; i++) {
-            const uint64_t p = b0 + i * 32 + lane;
-            eb.text[i * 32 + lane] = p < P.text_end ? byte_at(P, p) : 0u;
-        }
-        if (lane == 0) *eb.lcount = 0;
-        __syncwarp();
-        int lr = -1;   // this lane's long row
-        const uint64_t q = b0 + lane;
-        unsigned long long M = 0;   // bit len: an edge of that length
-        bool crossing = false, unk = false;
-        if (q < to) {
-            const uint32_t dlen = de - q < 64 ? (uint32_t)(de - q) : 64u;   // bytes to the document end (capped)
-            const uint32_t lim = min(dlen, P.E);
-            const uint32_t csr = q >= cs ? 0u : cs - q < 64 ? (uint32_t)(cs - q) : 64u;
-            const uint8_t *tx = eb.text + lane;
-            const uint32_t c0 = tx[0];
-            if (!is_cont(c0)) {
-                const int4 r = lut[c0];
-                if (r.x >= 0) {
-                    int32_t node = r.x;
-                    uint32_t y = (uint32_t)r.y;
-                    int32_t sc = r.z;
-                    uint32_t len = 1;
-                    for (;;) {
-                        const uint32_t nb = len < dlen ? tx[len] : 0u;
-                        if ((y & kTermBit) && (len == dlen || !is_cont(nb))) {
-                            if (len <= 32) {
-                                row[len - 1] = sc;
-                            } else {
-                                if (lr < 0) lr = atomicAdd(eb.lcount, 1);
-                                if (lr < kLongRows) eb.lrow[lr * 32 + (len - 33)] = sc;
-                                else spread = true;   // no long row left: the run is redone exactly
-                            }
-                            M |= 1ull << len;
-                            crossing |= len >= csr;
-                        }
-                        const uint32_t base = y & ~kTermBit;
-                        if (len >= lim || base == 0) break;
-                        const int32_t t = (int32_t)(base + nb);
-                        const int4 v = __ldg(P.fslot + t);
-                        if (v.x != node) break;
-                        node = t;
-                        y = (uint32_t)v.y;
-                        sc = v.z;
-                        ++len;
-                    }
-                }
-                if (M == 0) {   // <unk> to the next character boundary
-                    uint32_t len = 1;
-                    while (len < dlen && len <= P.E && is_cont(len < kTextStage - lane ? tx[len] : byte_at(P, q + len)))
-                        ++len;
-                    if (len > P.E) {
-                        atomicOr(&P.st->err, UERR_SPAN);
-                        len = P.E;
-                    }
-                    if (len <= 32) {
-                        row[len - 1] = (int32_t)P.unk;
-                    } else {
-                        lr = atomicAdd(eb.lcount, 1);
-                        if (lr < kLongRows) eb.lrow[lr * 32 + (len - 33)] = (int32_t)P.unk;
-                        else spread = true;
-                    }
-                    M = 1ull << len;
-                    unk = true;
-                    crossing = len >= csr;
-                }
-            }
-        }
-        cross((uint32_t)((b0 - from) >> 5), __ballot_sync(kFull, crossing && q < cs));
-        const uint32_t X = (uint32_t)(M >> 1), Y = (uint32_t)(M >> 33);
-        const uint32_t xrot = __funnelshift_l(X, X, lane + 1), yrot = __funnelshift_l(Y, Y, lane + 1);
-        const uint32_t mycode = ((uint32_t)(q - R.base) & 0x7FFFFFFFu) | ((uint32_t)unk << 31);
-        // rebase: the window's best reachable value becomes 0
-        const int32_t mx = __reduce_max_sync(kFull, max(R.a, R.b));
-        if (mx != kNeg32) {
-            if (R.a != kNeg32) {
-                const long long v = (long long)R.a - mx;
-                spread |= v < -kSpread;
-                R.a = (int32_t)max(v, (long long)-kSpread);
-            }
-            if (R.b != kNeg32) {
-                const long long v = (long long)R.b - mx;
-                spread |= v < -kSpread;
-                R.b = (int32_t)max(v, (long long)-kSpread);
-            }
-        }
-        __syncwarp();
-        int32_t fv = kNeg32;
-        uint32_t fs = 0;
-        const uint32_t nsrc = (uint32_t)(to - b0 < 32 ? to - b0 : 32);
-        const bool anylong = __any_sync(kFull, Y != 0u);   // some edge over 32 bytes (rare)
-        // source s of the batch; o1 = this lane's length to reach its A position
-        auto source = [&](uint32_t s, uint32_t o1) {
-            const int32_t b = __shfl_sync(kFull, R.a, s);
-            const uint32_t xr = __shfl_sync(kFull, xrot, s);
-            const uint32_t code = __shfl_sync(kFull, mycode, s);
-            const uint32_t yr = anylong ? __shfl_sync(kFull, yrot, s) : 0u;
-            const int slr = yr ? __shfl_sync(kFull, lr, s) : 0;   // s's long row (lengths 33..63)
-            if (lane == (int)s) {   // position b0 + s is final; the next window position moves in
-                fv = R.a;
-                fs = R.sa;
-                R.a = R.b;
-                R.sa = R.sb;
-                R.b = kNeg32;
-            }
-            if (b == kNeg32) return;
-            if (xr & mybit) {
-                const int32_t cand = b + eb.score[s * kEdgeStride + (o1 - 1)];
-                if (cand > R.a) { R.a = cand; R.sa = code; }
-            }
-            if ((yr & mybit) && slr < kLongRows) {   // length o1 + 32
-                const int32_t cand = b + eb.lrow[slr * 32 + (o1 - 1)];
-                if (cand > R.b) { R.b = cand; R.sb = code; }
-            }
-        };
-        const uint32_t o10 = lane == 0 ? 32u : (uint32_t)lane;   // this lane's length o1 from source 0
-        if (nsrc == 32) {
-#pragma unroll
-            for (uint32_t s = 0; s < 32; s++) source(s, ((o10 - 1u - s) & 31u) + 1u);
-        } else {
-            for (uint32_t s = 0; s < nsrc; s++) source(s, ((o10 - 1u - s) & 31u) + 1u);
-        }
-        spread |= fv != kNeg32 && (fv < -kSpread || fv > kSpread);   // every source value stayed in range
-        __syncwarp();
-        if (q < to) sink(q, ring_bp(R, q, fv, fs));
-        R.b0 = b0 + 32;
+        const WalkOut w = walk_batch(P, lut, eb, b0, to, de, cs);
+        cross((uint32_t)((b0 - from) >> 5), __ballot_sync(kFull, w.crossing && b0 + lane < cs));
+        spread |= w.spread;
+        spread |= dp_batch(eb, R, b0, to, w, sink);
     }
     return __any_sync(kFull, spread);
 }
@@ -907,13 +939,14 @@ __device__ __forceinline__ bool warp_next_ok(const UniParams &P, const UGeo &g, 
 // Parallel repair (spans E <= 63): one warp per listed flagged chunk f re-runs
 // f from f-1's run start and writes f's back pointers -- right whenever f-1
 // is -- and records in okn whether f + 1 then passes its check.
-__global__ void __launch_bounds__(kFwdWarps * 32) k_uni_fix_a(UniParams P) {
+__global__ void __launch_bounds__(kFwdWarps * 32) k_uni_fix_a(UniParams P, uint32_t coop_max) {
     __shared__ int4 lut[256];
     extern __shared__ int32_t s_rows[];
+    const uint32_t n = min(P.st->flist_len, P.flist_cap);
+    if (n <= coop_max) return;   // k_uni_fix_coop runs them, a CTA each
     load_fat_lut(P, lut);
     __syncthreads();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const uint32_t n = min(P.st->flist_len, P.flist_cap);
     const EdgeBuf eb(s_rows + w * (kWarpEdgeBytes / 4));
     for (uint32_t i = blockIdx.x * kFwdWarps + w; i < n; i += gridDim.x * kFwdWarps) {
         const unsigned long long f = P.flist[i];
@@ -924,6 +957,93 @@ __global__ void __launch_bounds__(kFwdWarps * 32) k_uni_fix_a(UniParams P) {
         warp_chunk(P, lut, eb, R, gf, &sp);
         const bool ok = !sp && (gf.last || warp_next_ok(P, gf, f));
         if (ok && lane == 0) atomicOr(P.okn + (f >> 5), 1u << (f & 31));
+    }
+}
+
+// Cooperative parallel repair (spans E <= 63), used when the flagged chunks
+// are no more than the CTAs: one CTA per listed flagged chunk f runs what
+// k_uni_fix_a's warp runs (from where f's crossing chains truly meet, else
+// from f-1's run start, through f's end).  Eight warps walk the trie for
+// eight batches at a time into shared-memory buffers while a ninth runs the
+// recurrence over the eight walked before, so the run costs about the
+// recurrence's latency instead of a walk's chain of dependent trie loads per
+// batch.
+constexpr int kCoopWalkers = 8;
+constexpr int kCoopBufWords = (kWarpEdgeBytes + 32 * 16) / 4;   // edge buffer + each lane's walk result
+
+__global__ void __launch_bounds__((kCoopWalkers + 1) * 32) k_uni_fix_coop(UniParams P) {
+    __shared__ int4 lut[256];
+    __shared__ unsigned long long s_from, s_start;
+    extern __shared__ int32_t s_buf[];
+    load_fat_lut(P, lut);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const bool dp = w == kCoopWalkers;
+    const uint32_t n = min(P.st->flist_len, P.flist_cap);
+    if (n > gridDim.x) return;   // k_uni_fix_a runs them, a warp each
+    for (uint32_t i = blockIdx.x; i < n; i += gridDim.x) {
+        const unsigned long long f = P.flist[i];
+        const UGeo gf = uni_geo(P, f);
+        if (dp && lane == 0) {
+            uint64_t z = ~0ull;
+            if (gf.cs - gf.ds > P.guard) z = true_meet(P, P.gback + f * (unsigned long long)P.grec, gf.cs);
+            if (z != ~0ull) {
+                s_from = gf.cs - ((gf.cs - z + 31) & ~31ull);   // batches stay aligned to cs
+                s_start = z;
+            } else {
+                const UGeo gp = gf.cs - gf.ds <= P.guard ? gf : uni_geo(P, f - 1);
+                const uint64_t from = run_from(P, gp);
+                s_from = from;
+                s_start = from == gp.ds ? gp.ds : next_boundary(P, from, gp.de);
+            }
+        }
+        __syncthreads();
+        const uint64_t from = s_from;
+        const uint32_t npre = (uint32_t)((gf.cs - from + 31) >> 5);
+        const uint32_t nb = npre + (uint32_t)((gf.ce - gf.cs + 31) >> 5);
+        const uint32_t nr = (nb + kCoopWalkers - 1) / kCoopWalkers;
+        // batch k: the prefix's batches up to cs, then the chunk's
+        auto batch_b0 = [&](uint32_t k) { return k < npre ? from + 32ull * k : gf.cs + 32ull * (k - npre); };
+        auto batch_to = [&](uint32_t k) { return k < npre ? gf.cs : gf.ce; };
+        WarpRing R;
+        bool sp = false;
+        if (dp) ring_start(R, from, s_start, lane);
+        for (uint32_t r = 0; r <= nr; r++) {   // round r: walk group r, recurrence over group r - 1
+            if (!dp) {
+                const uint32_t k = r * kCoopWalkers + w;
+                if (k < nb) {
+                    int32_t *base = s_buf + ((r & 1) * kCoopWalkers + w) * kCoopBufWords;
+                    const WalkOut wo = walk_batch(P, lut, EdgeBuf(base), batch_b0(k), batch_to(k), gf.de, 0);
+                    ((uint4 *)(base + kWarpEdgeBytes / 4))[lane] =
+                        make_uint4(wo.X, wo.Y, (uint32_t)wo.lr, (uint32_t)wo.unk | ((uint32_t)wo.spread << 1));
+                }
+            } else if (r > 0) {
+                const uint32_t k1 = min(nb, r * kCoopWalkers);
+                for (uint32_t k = (r - 1) * kCoopWalkers; k < k1; k++) {
+                    const int32_t *base = s_buf + (((r - 1) & 1) * kCoopWalkers + (k % kCoopWalkers)) * kCoopBufWords;
+                    const uint4 v = ((const uint4 *)(base + kWarpEdgeBytes / 4))[lane];
+                    WalkOut wo;
+                    wo.X = v.x;
+                    wo.Y = v.y;
+                    wo.lr = (int)v.z;
+                    wo.unk = v.w & 1u;
+                    wo.spread = (v.w >> 1) & 1u;
+                    wo.crossing = false;
+                    sp |= wo.spread;
+                    sp |= dp_batch(EdgeBuf(const_cast<int32_t *>(base)), R, batch_b0(k), batch_to(k), wo,
+                                   [&](uint64_t q, uint32_t bp) {
+                                       if (q >= gf.cs && q != gf.ds) back_at(P, q) = bp;
+                                   });
+                }
+            }
+            __syncthreads();
+        }
+        if (dp) {
+            if (gf.last && lane == (int)((gf.de - R.base) & 31)) back_at(P, gf.de) = ring_final(R, gf.de);
+            __syncwarp();
+            sp = __any_sync(kFull, sp);
+            const bool ok = !sp && (gf.last || warp_next_ok(P, gf, f));
+            if (ok && lane == 0) atomicOr(P.okn + (f >> 5), 1u << (f & 31));
+        }
     }
 }
 
@@ -1464,11 +1584,14 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
     const unsigned grid_d = (n_docs + 3) / 4;   // one warp per document
     if (profile) cudaEventRecord(ctx->events[0], s);
     const size_t rep_smem = 4 * kWarpEdgeBytes, warp_smem = kFwdWarps * kWarpEdgeBytes;
+    const size_t coop_smem = 2 * kCoopWalkers * kCoopBufWords * sizeof(int32_t);
     if (warp) {
         BPE_CUDA(ctx, cudaFuncSetAttribute(k_uni_fwd_warp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)warp_smem),
                  "k_uni_fwd_warp smem");
         BPE_CUDA(ctx, cudaFuncSetAttribute(k_uni_fix_a, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)warp_smem),
                  "k_uni_fix_a smem");
+        BPE_CUDA(ctx, cudaFuncSetAttribute(k_uni_fix_coop, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)coop_smem),
+                 "k_uni_fix_coop smem");
         k_uni_fwd_warp<<<(unsigned)((nc + kFwdWarps - 1) / kFwdWarps), kFwdWarps * 32, warp_smem, s>>>(P, nc);
     } else if (R == 64) {
         k_uni_fwd<64><<<grid_c, kUniThreads, 0, s>>>(P, nc);
@@ -1478,7 +1601,9 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
     if (profile) cudaEventRecord(ctx->events[1], s);
     k_uni_check<<<grid_c256, 256, 0, s>>>(P, nc);
     if (warp) {
-        k_uni_fix_a<<<(unsigned)std::max(1, ctx->sm_count * 3), kFwdWarps * 32, warp_smem, s>>>(P);
+        const unsigned coop_grid = (unsigned)std::max(1, ctx->sm_count * 2);
+        k_uni_fix_coop<<<coop_grid, (kCoopWalkers + 1) * 32, coop_smem, s>>>(P);
+        k_uni_fix_a<<<(unsigned)std::max(1, ctx->sm_count * 3), kFwdWarps * 32, warp_smem, s>>>(P, coop_grid);
         k_uni_frepair_warp<<<grid_d, 128, rep_smem, s>>>(P);
     } else if (R == 64) {
         k_uni_frepair<64><<<grid_d, 128, 0, s>>>(P);

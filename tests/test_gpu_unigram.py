@@ -134,6 +134,14 @@ def test_repairs_parity_runs(ctx):
     assert ctx.stats()["unigram_fix"]["bytes"] > 0
 
 
+def test_repairs_many_flagged(ctx):
+    """The same parity runs over about 1,200 chunks of 256 bytes, more flagged
+    chunks than the cooperative repair has CTAs: the warp-per-chunk repair
+    takes them."""
+    vb, off = vocab_arrays([b"a", b"aa"])
+    check_unigram(ctx, vb, off, [-1.0, -1.5], 2, -30.0, [b"a" * 200001, b"a" * 100000, b"a" * 3], chunk=256)
+
+
 def test_repairs_mixed(ctx):
     """Runs of 'a' between ordinary text: repairs start and stop inside documents."""
     rng = random.Random(3)
