@@ -226,9 +226,10 @@ struct ByteWin {
 
 // Greedy longest-match parse of the tokens that start in [p, ce) of a
 // document ending at de.  Every loop iteration takes one trie step on every
-// lane -- from the root through the shared LUT, or from a node through the
-// double array -- so the lanes of a warp run the same instructions whatever
-// their token lengths; a token ends when a step fails.  Positions are kept
+// lane through the double array, so the lanes of a warp run the same
+// instructions whatever their token lengths; a token ends when a step fails,
+// and the next token's first step (through the shared LUT) is taken in the
+// same iteration, from the byte that failed when the token ended there.  Positions are kept
 // as 32-bit offsets from the chunk start cs (p >= cs; a parse never runs
 // 2^31 bytes past it).
 //   MODE 0 (speculative): mark token starts in bits (offsets from cs) and,
@@ -259,27 +260,30 @@ __device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 
         }
     }
     ByteWin byte{P.bytes + cs};
-    int32_t node = -1;            // -1: at the root
+    int32_t node = 0;
     uint32_t y = 0, blen = 0;     // base|TERM of node; length of the best token so far
     int32_t bnode = -1, btid = 0; // best token: its slot (id in tid[]) or, at depth 1, its id
     uint32_t q = p;
+    // a token's first step, through the shared LUT (every byte is a token)
+    auto root_step = [&](uint32_t ch) {
+        const int4 r = lut[ch];
+        node = r.x;
+        y = (uint32_t)r.y;
+        btid = r.z;
+        blen = 1;
+        bnode = -1;
+        q = p + 1;
+    };
+    if (p < ce) root_step(byte(p));
     while (p < ce) {
-        const bool root = node < 0;
         const uint32_t base = y & ~kTermBit;
+        const bool load = q < de && base != 0;
         bool ok = false;
         int32_t nt = 0;
-        uint32_t ny = 0;
-        if (q < de && (root || base != 0)) {
-            const uint32_t ch = byte(q);
-            if (root) {
-                const int4 r = lut[ch];
-                nt = r.x;
-                ny = (uint32_t)r.y;
-                btid = r.z;
-                ok = true;
-            } else {
-                ok = trie_step<L>(P, node, base, ch, &nt, &ny);
-            }
+        uint32_t ny = 0, ch = 0;
+        if (load) {
+            ch = byte(q);
+            ok = trie_step<L>(P, node, base, ch, &nt, &ny);
         }
         if (ok) {
             node = nt;
@@ -287,9 +291,9 @@ __device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 
             ++q;
             if (ny & kTermBit) {
                 blen = q - p;
-                bnode = root ? -1 : nt;
+                bnode = nt;
             }
-        } else {   // the token [p, p + blen) ends here (every byte is a token: blen >= 1)
+        } else {   // the token [p, p + blen) ends here; the next one starts in the same step
             if (MODE == 0) {
                 bits[(p >> 5) * kBS] |= 1u << (p & 31);
                 if (sid) sid[c] = bnode >= 0 ? (int32_t)(0x80000000u | (uint32_t)bnode) : btid;
@@ -297,6 +301,7 @@ __device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 
             if (kWrite && o < P.cap) P.ids[o] = bnode >= 0 ? __ldg(P.tid + bnode) : btid;
             ++o;
             ++c;
+            const bool at_q = load && p + blen == q;   // the failed byte starts the next token
             p += blen;
             if (kMeet && p < ce) {
                 if ((bits[(p >> 5) * kBS] >> (p & 31)) & 1u) {
@@ -304,11 +309,7 @@ __device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 
                     break;
                 }
             }
-            node = -1;
-            y = 0;
-            blen = 0;
-            bnode = -1;
-            q = p;
+            if (p < ce) root_step(at_q ? ch : byte(p));
         }
     }
     *cnt = c;
