@@ -28,9 +28,13 @@
 //                  meet at one position the true recurrence reaches, their
 //                  values are the true ones plus one constant -- and so are
 //                  the chunk's.  A chunk for which that fails is flagged.
-//   k_uni_fix_a    one warp per flagged chunk re-runs it from its
+//   k_uni_fix_coop one CTA per flagged chunk re-runs it from its
 //                  predecessor's state (right when the predecessor is) and
-//                  notes whether the next chunk then passes its check;
+//                  notes whether the next chunk then passes its check; eight
+//                  warps walk the trie for eight batches at once while a
+//                  ninth runs the recurrence.  (k_uni_fix_a: the same with
+//                  one warp per chunk, when more chunks are flagged than
+//                  the cooperative kernel has CTAs.)
 //   k_uni_frepair_warp  one warp per document keeps those results where they
 //                  hold and re-runs chains of chunks where they do not.
 //   k_uni_bspec    each thread backtracks speculatively from a reachable
@@ -889,29 +893,36 @@ __device__ uint64_t true_meet(const UniParams &P, const uint32_t *gr, uint64_t c
     return ~0ull;
 }
 
-// The state at flagged chunk f's start, the chunk before it being right:
-// from where the true chains of f's crossing positions meet when they do
-// (a few tokens back), else from f-1's run start (or the document start when
-// f lies within G bytes of it).
-__device__ __forceinline__ void warp_prefix(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRing &R,
-                                            const UGeo &gf, unsigned long long f, bool *sp) {
-    const int lane = threadIdx.x & 31;
+// Where a re-run of flagged chunk f starts, the chunk before it being right:
+// where the true chains of f's crossing positions meet when they do (a few
+// tokens back; the ring's base then lies a whole number of batches before
+// cs), else f-1's run start (or the document start when f lies within G
+// bytes of it).  Returns the ring's base; *s0 = the start position.
+__device__ uint64_t repair_from(const UniParams &P, const UGeo &gf, unsigned long long f, uint64_t *s0) {
     if (gf.cs - gf.ds > P.guard) {
-        uint64_t z = 0;
-        if (lane == 0) z = true_meet(P, P.gback + f * (unsigned long long)P.grec, gf.cs);
-        z = __shfl_sync(kFull, z, 0);
+        const uint64_t z = true_meet(P, P.gback + f * (unsigned long long)P.grec, gf.cs);
         if (z != ~0ull) {
-            const uint64_t base = gf.cs - ((gf.cs - z + 31) & ~31ull);   // batches stay aligned to cs
-            ring_start(R, base, z, lane);
-            *sp |= warp_dp(P, lut, eb, R, base, gf.cs, gf.de, 0, [](uint64_t, uint32_t) {},
-                           [](uint32_t, unsigned) {});
-            return;
+            *s0 = z;
+            return gf.cs - ((gf.cs - z + 31) & ~31ull);
         }
     }
     const UGeo gp = gf.cs - gf.ds <= P.guard ? gf : uni_geo(P, f - 1);
     const uint64_t from = run_from(P, gp);
-    ring_start(R, from, from == gp.ds ? gp.ds : next_boundary(P, from, gp.de), lane);
-    *sp |= warp_dp(P, lut, eb, R, from, gf.cs, gf.de, 0, [](uint64_t, uint32_t) {}, [](uint32_t, unsigned) {});
+    *s0 = from == gp.ds ? gp.ds : next_boundary(P, from, gp.de);
+    return from;
+}
+
+// The state at flagged chunk f's start, the chunk before it being right (the
+// run from repair_from up to cs).
+__device__ __forceinline__ void warp_prefix(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRing &R,
+                                            const UGeo &gf, unsigned long long f, bool *sp) {
+    const int lane = threadIdx.x & 31;
+    uint64_t base = 0, s0 = 0;
+    if (lane == 0) base = repair_from(P, gf, f, &s0);
+    base = __shfl_sync(kFull, base, 0);
+    s0 = __shfl_sync(kFull, s0, 0);
+    ring_start(R, base, s0, lane);
+    *sp |= warp_dp(P, lut, eb, R, base, gf.cs, gf.de, 0, [](uint64_t, uint32_t) {}, [](uint32_t, unsigned) {});
 }
 
 // Run chunk g (its start state in R), writing its true back pointers.
@@ -984,17 +995,9 @@ __global__ void __launch_bounds__((kCoopWalkers + 1) * 32) k_uni_fix_coop(UniPar
         const unsigned long long f = P.flist[i];
         const UGeo gf = uni_geo(P, f);
         if (dp && lane == 0) {
-            uint64_t z = ~0ull;
-            if (gf.cs - gf.ds > P.guard) z = true_meet(P, P.gback + f * (unsigned long long)P.grec, gf.cs);
-            if (z != ~0ull) {
-                s_from = gf.cs - ((gf.cs - z + 31) & ~31ull);   // batches stay aligned to cs
-                s_start = z;
-            } else {
-                const UGeo gp = gf.cs - gf.ds <= P.guard ? gf : uni_geo(P, f - 1);
-                const uint64_t from = run_from(P, gp);
-                s_from = from;
-                s_start = from == gp.ds ? gp.ds : next_boundary(P, from, gp.de);
-            }
+            uint64_t s0;
+            s_from = repair_from(P, gf, f, &s0);
+            s_start = s0;
         }
         __syncthreads();
         const uint64_t from = s_from;
