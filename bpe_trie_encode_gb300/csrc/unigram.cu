@@ -1083,12 +1083,13 @@ __device__ unsigned long long thread_chain(const UniParams &P, const int4 *lut, 
 }
 
 // Sequential repair per document (spans E <= 63), one warp per document, in
-// order over the flagged chunks.  Flagged chunk f was repaired by k_uni_fix_a
-// from f-1's state, which is right here (everything before f is).  If okn
-// says f + 1 passes against f's new back pointers and f + 1 is not flagged
-// itself, nothing is left to do.  Otherwise the warp re-runs from f's state
-// through the chunks after f until one passes its check and kept its own
-// run's back pointers (k_uni_fix_a rewrote every listed chunk).
+// order over the flagged chunks.  Flagged chunk f was repaired by the
+// parallel pass (k_uni_fix_coop or k_uni_fix_a) from f-1's state, which is
+// right here (everything before f is).  If okn says f + 1 passes against f's
+// new back pointers and f + 1 is not flagged itself, nothing is left to do.
+// Otherwise the warp re-runs from f's state through the chunks after f until
+// one passes its check and kept its own run's back pointers (the parallel
+// pass rewrote every listed chunk).
 __global__ void __launch_bounds__(128) k_uni_frepair_warp(UniParams P) {
     __shared__ int4 lut[256];
     extern __shared__ int32_t s_rows[];   // 4 edge tables
