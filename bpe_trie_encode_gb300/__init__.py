@@ -24,8 +24,8 @@ import torch
 from . import _capi
 from ._capi import (BPE_MAX_MERGES, BPE_MERGE_LOOKBACK, BPE_MERGE_TILES, BPE_MERGE_TWO_PASS,  # noqa: F401
                     BPE_OPT_CHUNK, BPE_OPT_GRAPH, BPE_OPT_MERGE, BPE_OPT_PERSISTENT, BPE_OPT_PROFILE,
-                    BPE_OPT_TABLE_LOG2, BPE_OPT_TRAIN_WORDS, BPE_OPT_TRIE_LAYOUT, BPE_OPT_UNI_CHUNK, BPE_TRIE_BITMAP,
-                    BPE_TRIE_DOUBLE_ARRAY, BPE_WORD_START, BpeError)
+                    BPE_OPT_SPARSE_MERGE, BPE_OPT_TABLE_LOG2, BPE_OPT_TRAIN_WORDS, BPE_OPT_TRIE_LAYOUT,
+                    BPE_OPT_UNI_CHUNK, BPE_TRIE_BITMAP, BPE_TRIE_DOUBLE_ARRAY, BPE_WORD_START, BpeError)
 
 __all__ = ["Context", "Trie", "Unigram", "BpeError", "vocab_from_merges", "BPE_WORD_START", "BPE_MAX_MERGES"]
 

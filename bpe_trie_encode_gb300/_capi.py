@@ -22,7 +22,7 @@ BPE_WORD_START = 0x10000
 BPE_MAX_MERGES = 65280
 BPE_OPT_TABLE_LOG2, BPE_OPT_GRAPH, BPE_OPT_PROFILE, BPE_OPT_CHUNK, BPE_OPT_TRAIN_WORDS = 1, 2, 3, 4, 5
 BPE_OPT_MERGE, BPE_OPT_PERSISTENT, BPE_OPT_TRIE_LAYOUT, BPE_OPT_UNI_CHUNK = 6, 7, 8, 9
-BPE_OPT_TEST_STALL_TILE = 10
+BPE_OPT_TEST_STALL_TILE, BPE_OPT_SPARSE_MERGE = 10, 11
 BPE_TRIE_DOUBLE_ARRAY, BPE_TRIE_BITMAP = 0, 1
 BPE_MERGE_TWO_PASS, BPE_MERGE_LOOKBACK, BPE_MERGE_TILES = 0, 1, 2
 

@@ -50,6 +50,7 @@ int ensure(bpe_ctx *ctx, Slot s, size_t bytes, void **out) {
         sc.p = p;
         sc.cap = want;
         ctx->graph.key.clear();                    // pointers changed: recapture
+        ctx->graph_sparse.key.clear();
     }
     *out = sc.p;
     return BPE_OK;
@@ -136,6 +137,7 @@ extern "C" void bpe_ctx_destroy(bpe_ctx *ctx) {
     if (ctx->pipe_d2h) cudaStreamDestroy(ctx->pipe_d2h);
     if (ctx->pipe_pinned) cudaFreeHost(ctx->pipe_pinned);
     if (ctx->graph.exec) cudaGraphExecDestroy(ctx->graph.exec);
+    if (ctx->graph_sparse.exec) cudaGraphExecDestroy(ctx->graph_sparse.exec);
     for (auto &s : ctx->scratch)
         if (s.p) cudaFree(s.p);
     for (auto ev : ctx->events) cudaEventDestroy(ev);
@@ -175,6 +177,9 @@ extern "C" int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value) {
         return BPE_OK;
     case BPE_OPT_PERSISTENT:
         ctx->persistent = value ? 1 : 0;
+        return BPE_OK;
+    case BPE_OPT_SPARSE_MERGE:
+        ctx->sparse_merge = value ? 1 : 0;
         return BPE_OK;
     case BPE_OPT_TEST_STALL_TILE:
         ctx->test_stall_tile = value < 0 ? -1 : value;

@@ -23,6 +23,7 @@ enum Slot {
     S_W_BSUM, S_W_START, S_W_OCCSLOT, S_W_TABLE, S_W_UID, S_W_UINFO, S_W_SYM, S_W_OUTOFF,
     S_UNI_START, S_UNI_STATE, S_UNI_BACK, S_UNI_GBACK, S_UNI_CHUNK, S_UNI_FLAG, S_UNI_PREFIX, S_UNI_STATUS,
     S_UNI_TSTART,
+    S_SPARSE_OCC,
     S_NUM
 };
 
@@ -58,11 +59,13 @@ struct bpe_ctx {
     int train_words = 0;
     int merge_mode = 0;   // BPE_MERGE_*
     int persistent = 0;
+    int sparse_merge = 1;   // BPE_OPT_SPARSE_MERGE
     int trie_layout = 0;   // BPE_TRIE_*
     int uni_chunk = 0;     // unigram_encode chunk bytes (0: default)
     long long test_stall_tile = -1;   // BPE_OPT_TEST_STALL_TILE
     // cached graph of merge iterations
     bpe::TrainGraph graph;
+    bpe::TrainGraph graph_sparse;   // the same for occurrence-driven merge windows
     // profiling events (grown on demand)
     std::vector<cudaEvent_t> events;
     bpe_stats stats{};

@@ -92,6 +92,12 @@ struct TrainState {
     uint32_t ticket[2];       // tile tickets, by merge parity
     uint32_t msum_done;       // k_msum CTAs finished (the last one scans)
     uint32_t gactive[2];      // gapped tiles: tiles in use, by merge parity
+    // occurrence-driven merges (merge sparse_from on): the stream sits in
+    // buf[scur] as slen symbols, tombstones included
+    uint32_t sparse_from;     // 0xFFFFFFFF: none
+    uint32_t scur;
+    unsigned long long slen, live, tombs;
+    uint32_t occ_n[2];        // occurrences listed, by merge parity
     // grid barrier of the persistent merge loop: kBarGroups arrival counters,
     // the groups' counter and the release generation, each on its own
     // 128-byte line so arrivals and polling do not queue at one L2 slice
@@ -118,6 +124,12 @@ struct TrainParams {
     uint32_t *gcarry;            // summary pass: merge flag entering each tile
     unsigned long long *goff;    // summary pass: output offset of each tile (compacting merges)
     uint32_t gtiles;
+    // occurrence-driven merges: each merge's occurrences as (i, j) position
+    // pairs, by merge parity; compaction tiles' live counts and offsets
+    uint32_t *occ[2];
+    uint32_t occ_cap;
+    uint32_t *ctile;
+    unsigned long long *coff;
 };
 
 __device__ __forceinline__ unsigned long long pack_best(uint32_t count, uint32_t key) {
@@ -1282,6 +1294,168 @@ __device__ __forceinline__ void argmax_into(const TrainParams &p, uint32_t k, un
     }
 }
 
+// ------------------------------------------------ occurrence-driven merges ---
+//
+// Once the best pair is rare, rewriting the whole stream per merge costs far
+// more than the merge changes.  From merge sparse_from on (chosen by the
+// host), a merge instead
+//   k_sscan     reads the stream once and, for each occurrence (i, j) of the
+//               pair that merges (j: the next live position after i), applies
+//               the exact count deltas from the old stream and lists (i, j);
+//   k_sargmax   (the next merge's first kernel) writes new_id at i and a
+//               tombstone at j for every listed occurrence, then runs that
+//               merge's argmax.
+// A pair is a live symbol and the next live one after it (tombstones are
+// skipped); the stream is compacted when tombstones pass a quarter of it
+// (k_ccount, k_cscan, k_cscatter, k_cdone at the start of a window) and once
+// at the end.
+//
+// Count deltas of one occurrence (i, j) that merges, taken from the old
+// stream (p: the live position before i when i has no WORD_START; q: the
+// live position after j when it has none):
+//   own pair (l, r): -1 (for l != r all occurrences merge, so one thread
+//       subtracts the whole count instead);
+//   left edge (p, i): -(s[p], l), +(s[p]', new) where s[p]' = new when p is
+//       the right half of another merging occurrence -- the edge between two
+//       occurrences is counted by the right one;
+//   right edge (j, q), unless q starts a merging occurrence: -(r, s[q]),
+//       +(new, s[q]).
+// For l == r only starts with an odd number of consecutive valid starts
+// ending at them merge (leftmost first); the right half of the previous
+// merging start and the next merging start are then exactly the cases the
+// two tests above check.
+constexpr uint32_t kTomb = 0xFFFFFFFFu;   // never a symbol: bits 17..31 of a symbol are 0
+constexpr uint32_t kNoSparse = 0xFFFFFFFFu;
+constexpr int kSparseThreads = 256;
+constexpr uint64_t kSparseDiv = 64;   // automatic switch: best count below n / kSparseDiv
+
+__device__ __forceinline__ uint32_t sym_id(uint32_t x) { return x & 0xFFFFu; }
+
+__device__ __forceinline__ uint64_t next_live(const uint32_t *s, uint64_t a, uint64_t n) {
+    uint64_t b = a + 1;
+    while (b < n && __ldg(s + b) == kTomb) ++b;
+    return b;
+}
+
+// The live position before a, or -1.
+__device__ __forceinline__ long long prev_live(const uint32_t *s, uint64_t a) {
+    long long b = (long long)a - 1;
+    while (b >= 0 && __ldg(s + b) == kTomb) --b;
+    return b;
+}
+
+// Position i holds l (live): if (i, next live) is an occurrence that merges,
+// apply its count deltas and list it.
+__device__ void sparse_occurrence(const TrainParams &p, const Table &T, const uint32_t *s, uint64_t n, uint64_t i,
+                                  uint32_t l, uint32_t r, uint32_t nid, uint32_t k) {
+    const uint64_t j = next_live(s, i, n);
+    if (j >= n) return;
+    const uint32_t sj = __ldg(s + j);
+    if (sym_id(sj) != r || (sj & kWordStart)) return;
+    const uint32_t si = __ldg(s + i);
+    if (l == r) {   // merges when the run of valid starts ending at i is odd
+        uint32_t c = 1;
+        uint64_t x = i;
+        for (;;) {
+            if (__ldg(s + x) & kWordStart) break;
+            const long long pp = prev_live(s, x);
+            if (pp < 0 || sym_id(__ldg(s + pp)) != l) break;
+            ++c;
+            x = (uint64_t)pp;
+        }
+        if (!(c & 1u)) return;
+        global_add(T, pair_key(l, r), 0xFFFFFFFFu);
+    }
+    if (!(si & kWordStart)) {
+        const long long pp = prev_live(s, i);
+        if (pp >= 0) {
+            const uint32_t sp = __ldg(s + pp);
+            bool pocc = false;   // p is the right half of a merging occurrence
+            if (sym_id(sp) == r && !(sp & kWordStart)) {
+                const long long p2 = prev_live(s, (uint64_t)pp);
+                pocc = p2 >= 0 && sym_id(__ldg(s + p2)) == l;
+            }
+            global_add(T, pair_key(sp, l), 0xFFFFFFFFu);
+            global_add(T, pair_key(pocc ? nid : sp, nid), 1u);
+        }
+    }
+    const uint64_t q = next_live(s, j, n);
+    if (q < n) {
+        const uint32_t sq = __ldg(s + q);
+        if (!(sq & kWordStart)) {
+            bool qocc = false;   // q starts a merging occurrence
+            if (sym_id(sq) == l) {
+                const uint64_t q2 = next_live(s, q, n);
+                qocc = q2 < n && sym_id(__ldg(s + q2)) == r && !(__ldg(s + q2) & kWordStart);
+            }
+            if (!qocc) {
+                global_add(T, pair_key(r, sq), 0xFFFFFFFFu);
+                global_add(T, pair_key(nid, sq), 1u);
+            }
+        }
+    }
+    const uint32_t x = atomicAdd(&p.st->occ_n[k & 1], 1u);
+    if (x < p.occ_cap) {
+        p.occ[k & 1][2 * (uint64_t)x] = (uint32_t)i;
+        p.occ[k & 1][2 * (uint64_t)x + 1] = (uint32_t)j;
+    } else {
+        atomicOr(&p.st->err, DERR_OOB);   // the list is sized by a count no later merge exceeds
+    }
+}
+
+__global__ void __launch_bounds__(kSparseThreads) k_sscan(TrainParams p, uint32_t it) {
+    TrainState *st = p.st;
+    const uint32_t k = st->k_base + it;
+    if (k >= st->n_merges || st->err || k < st->sparse_from) return;
+    const unsigned long long bw = __ldcg(p.best + k);
+    const uint32_t cnt = (uint32_t)(bw >> 32);
+    if (cnt == 0) return;
+    const uint32_t key = ~(uint32_t)bw, l = key >> 16, r = key & 0xFFFFu, nid = 256u + k;
+    const uint32_t *s = p.buf[st->scur];
+    const uint64_t n = st->slen;
+    const Table T = table_of(p);
+    if (l != r && blockIdx.x == 0 && threadIdx.x == 0) global_add(T, key, 0u - cnt);   // its count ends at 0
+    const uint64_t nq = (n + 3) / 4;   // the buffer is padded: a quad past n is readable
+    for (uint64_t x = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; x < nq; x += (uint64_t)gridDim.x * blockDim.x) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(s) + x);
+        const uint32_t a[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            if (sym_id(a[e]) != l || a[e] == kTomb || 4 * x + e >= n) continue;
+            sparse_occurrence(p, T, s, n, 4 * x + e, l, r, nid, k);
+        }
+    }
+}
+
+// Apply merge k-1's listed occurrences (when it was occurrence-driven), then
+// merge k's argmax.
+__global__ void __launch_bounds__(kArgmaxThreads) k_sargmax(TrainParams p, uint32_t it) {
+    __shared__ unsigned long long sbest[kArgmaxThreads / 32];
+    TrainState *st = p.st;
+    const uint32_t k = st->k_base + it;
+    const uint32_t sf = st->sparse_from;
+    if (k >= 1 && sf != kNoSparse && k - 1 >= sf && k - 1 < st->n_merges) {
+        const uint32_t m = min(st->occ_n[(k - 1) & 1], p.occ_cap);
+        uint32_t *s = p.buf[st->scur];
+        const uint32_t nid = 256u + (k - 1);
+        const uint32_t *L = p.occ[(k - 1) & 1];
+        for (uint32_t x = blockIdx.x * blockDim.x + threadIdx.x; x < m; x += gridDim.x * blockDim.x) {
+            const uint32_t i = L[2 * (uint64_t)x], j = L[2 * (uint64_t)x + 1];
+            s[i] = nid | (s[i] & kWordStart);
+            s[j] = kTomb;
+        }
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            st->live -= m;
+            st->tombs += m;
+            p.nhist[k] = st->live;
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0 && sf != kNoSparse && k >= sf) st->occ_n[k & 1] = 0;   // merge k lists here
+    if (k == 0 || k >= st->n_merges || st->err) return;
+    if ((__ldcg(p.best + k - 1) >> 32) == 0) return;   // training has stopped
+    argmax_into(p, k, sbest);
+}
+
 __global__ void __launch_bounds__(kMergeThreads, 4) k_train_loop(TrainParams p, uint32_t k_begin, uint32_t k_end) {
     extern __shared__ uint32_t dsm[];
     __shared__ MergeShared sh;
@@ -1707,8 +1881,8 @@ __global__ void k_ginit(uint32_t *len0, uint32_t T, unsigned long long n) {
     }
 }
 
-// Exclusive scan of the tiles' live counts (one CTA).
-__global__ void __launch_bounds__(1024) k_gscan(const uint32_t *len, uint32_t T, unsigned long long *off) {
+// Exclusive scan of T u32 counts into u64 offsets by one CTA of 1,024 threads.
+__device__ __forceinline__ void exclusive_scan_1024(const uint32_t *len, uint32_t T, unsigned long long *off) {
     __shared__ unsigned long long s_w[32];
     __shared__ unsigned long long s_carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1737,6 +1911,11 @@ __global__ void __launch_bounds__(1024) k_gscan(const uint32_t *len, uint32_t T,
     }
 }
 
+// Exclusive scan of the tiles' live counts (one CTA).
+__global__ void __launch_bounds__(1024) k_gscan(const uint32_t *len, uint32_t T, unsigned long long *off) {
+    exclusive_scan_1024(len, T, off);
+}
+
 // The contiguous stream: tile t's live symbols to out + off[t].
 __global__ void k_gcopy(const uint32_t *buf, const uint32_t *len, const unsigned long long *off, uint32_t *out) {
     const uint32_t t = blockIdx.x, l = len[t];
@@ -1745,6 +1924,101 @@ __global__ void k_gcopy(const uint32_t *buf, const uint32_t *len, const unsigned
 }
 
 __global__ void k_advance(TrainState *st, uint32_t by) { st->k_base += by; }
+
+// Compaction of the tombstoned stream, in tiles of kCTile positions: live
+// counts per tile, their exclusive scan, then each tile's live symbols in
+// order.  Without force, all four kernels run only when tombstones exceed a
+// quarter of the stream (the same test in each: nothing they read changes
+// before k_cdone).
+constexpr int kCTile = 4096;
+constexpr int kCThreads = 256;
+constexpr int kCItems = kCTile / kCThreads;
+
+__device__ __forceinline__ bool compact_now(const TrainState *st, int force) {
+    return force || (st->sparse_from != kNoSparse && st->tombs * 4 > st->slen);
+}
+
+__global__ void __launch_bounds__(kCThreads) k_ccount(TrainParams p, int force) {
+    __shared__ uint32_t s_w[kCThreads / 32];
+    const TrainState *st = p.st;
+    if (!compact_now(st, force)) return;
+    const uint64_t n = st->slen, base = (uint64_t)blockIdx.x * kCTile;
+    if (base >= n) return;
+    const uint32_t *s = p.buf[st->scur];
+    uint32_t c = 0;
+    for (int t = threadIdx.x; t < kCTile; t += kCThreads) {
+        const uint64_t i = base + t;
+        c += (i < n && s[i] != kTomb) ? 1u : 0u;
+    }
+    c = __reduce_add_sync(kFull, c);
+    if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = c;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t tot = 0;
+        for (int w = 0; w < kCThreads / 32; w++) tot += s_w[w];
+        p.ctile[blockIdx.x] = tot;
+    }
+}
+
+__global__ void __launch_bounds__(1024) k_cscan(TrainParams p, int force) {
+    const TrainState *st = p.st;
+    if (!compact_now(st, force)) return;
+    const uint32_t T = (uint32_t)((st->slen + kCTile - 1) / kCTile);
+    exclusive_scan_1024(p.ctile, T, p.coff);
+}
+
+// out: the other buffer (then k_cdone switches to it), or the caller's.
+__global__ void __launch_bounds__(kCThreads) k_cscatter(TrainParams p, uint32_t *out, int force) {
+    __shared__ uint32_t s_w[kCThreads / 32];
+    const TrainState *st = p.st;
+    if (!compact_now(st, force)) return;
+    const uint64_t n = st->slen, base = (uint64_t)blockIdx.x * kCTile;
+    if (base >= n) return;
+    const uint32_t *s = p.buf[st->scur];
+    if (!out) out = p.buf[st->scur ^ 1u];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t v[kCItems];
+    uint32_t c = 0;
+#pragma unroll
+    for (int e = 0; e < kCItems; e++) {
+        const uint64_t i = base + (uint64_t)kCItems * tid + e;
+        v[e] = i < n ? s[i] : kTomb;
+        c += v[e] != kTomb ? 1u : 0u;
+    }
+    uint32_t x = c;   // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_w[warp] = x;
+    __syncthreads();
+    uint32_t wpre = 0;
+    for (int w = 0; w < warp; w++) wpre += s_w[w];
+    uint64_t o = p.coff[blockIdx.x] + wpre + x - c;
+#pragma unroll
+    for (int e = 0; e < kCItems; e++)
+        if (v[e] != kTomb) out[o++] = v[e];
+}
+
+__global__ void k_cdone(TrainParams p, int force) {
+    TrainState *st = p.st;
+    if (!compact_now(st, force)) return;
+    st->slen = st->live;
+    st->tombs = 0;
+    if (!force) st->scur ^= 1u;
+}
+
+// Occurrence-driven merges from merge k on; the stream is in buf[k & 1].
+__global__ void k_sparse_begin(TrainParams p, uint32_t k) {
+    TrainState *st = p.st;
+    st->sparse_from = k;
+    st->scur = k & 1u;
+    st->slen = st->n[k & 1];
+    st->live = st->slen;
+    st->tombs = 0;
+    st->occ_n[0] = st->occ_n[1] = 0;
+}
 
 uint32_t ceil_log2(uint64_t x) {
     uint32_t l = 0;
@@ -1758,6 +2032,7 @@ struct Launch {
     size_t count_smem, merge_smem, gmerge_smem, gsum_smem;
     unsigned gmerge_grid;
     int mode;   // BPE_MERGE_TWO_PASS, BPE_MERGE_LOOKBACK or BPE_MERGE_TILES
+    unsigned sscan_grid, ctile_grid;   // occurrence-driven merges: scan CTAs, compaction tiles
 };
 
 constexpr size_t kGmergeSmem = (size_t)(kGapStage + kMergeTile + 2 * kDeltaSlots) * sizeof(uint32_t);
@@ -1835,6 +2110,57 @@ int get_graph(bpe_ctx *ctx, const Launch &L, cudaGraphExec_t *out) {
     return BPE_OK;
 }
 
+// Compaction of the tombstoned stream: when due (force 0, into the other
+// buffer), or always into out (force 1).
+void launch_compaction(const Launch &L, uint32_t *out, int force, cudaStream_t s) {
+    k_ccount<<<L.ctile_grid, kCThreads, 0, s>>>(L.p, force);
+    k_cscan<<<1, 1024, 0, s>>>(L.p, force);
+    k_cscatter<<<L.ctile_grid, kCThreads, 0, s>>>(L.p, out, force);
+    k_cdone<<<1, 1, 0, s>>>(L.p, force);
+}
+
+// A window compacts after its first k_sargmax has applied the previous
+// merge's occurrences (their positions are in the current buffer).
+void launch_sparse_iteration(const Launch &L, uint32_t it, bool compact, cudaStream_t s) {
+    k_sargmax<<<L.argmax_grid, kArgmaxThreads, 0, s>>>(L.p, it);
+    if (compact) launch_compaction(L, nullptr, 0, s);
+    k_sscan<<<L.sscan_grid, kSparseThreads, 0, s>>>(L.p, it);
+}
+
+// Capture (or reuse) a graph of one occurrence-driven window: kGraphIters
+// merges (compaction when due after the first one's apply), the k_base
+// advance.
+int get_sparse_graph(bpe_ctx *ctx, const Launch &L, cudaGraphExec_t *out) {
+    std::vector<uintptr_t> key = {
+        (uintptr_t)L.p.buf[0], (uintptr_t)L.p.buf[1], (uintptr_t)L.p.tslot, (uintptr_t)L.p.tmask,
+        (uintptr_t)L.p.dkey, (uintptr_t)L.p.dcnt, (uintptr_t)L.p.dcap, (uintptr_t)L.p.best,
+        (uintptr_t)L.p.nhist, (uintptr_t)L.p.dhist, (uintptr_t)L.p.st, (uintptr_t)L.p.occ[0],
+        (uintptr_t)L.p.occ[1], (uintptr_t)L.p.occ_cap, (uintptr_t)L.p.ctile, (uintptr_t)L.p.coff,
+        (uintptr_t)L.sscan_grid, (uintptr_t)L.ctile_grid, (uintptr_t)L.argmax_grid};
+    TrainGraph &G = ctx->graph_sparse;
+    if (G.exec && G.key == key) {
+        *out = G.exec;
+        return BPE_OK;
+    }
+    if (G.exec) {
+        cudaGraphExecDestroy(G.exec);
+        G.exec = nullptr;
+    }
+    cudaStream_t cs = ctx->capture_stream;
+    BPE_CUDA(ctx, cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal), "begin capture");
+    for (uint32_t i = 0; i < kGraphIters; i++) launch_sparse_iteration(L, i, i == 0, cs);
+    k_advance<<<1, 1, 0, cs>>>(L.p.st, kGraphIters);
+    cudaGraph_t g = nullptr;
+    cudaError_t e = cudaStreamEndCapture(cs, &g);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "end capture");
+    e = cudaGraphInstantiate(&G.exec, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "graph instantiate");
+    G.key = key;
+    *out = G.exec;
+    return BPE_OK;
+}
+
 int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_merges, uint32_t table_log2,
                bpe_merge *h_merges_out, uint32_t *n_done, uint32_t *d_symbols_final, uint64_t *n_final,
                bool *table_full) {
@@ -1872,6 +2198,16 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
                  "k_train_loop occupancy");
         if (pb < 1) return fail(ctx, BPE_ERR_CUDA, "bpe_train: the persistent merge loop does not fit on an SM");
     }
+    // occurrence-driven merges: automatic (1) or from merge 0 (2); positions are 32-bit
+    const int sparse_mode = ctx->sparse_merge;
+    const bool sparse_ok = sparse_mode && mode == BPE_MERGE_TWO_PASS && !persistent && n > 0 &&
+                           n + kPadSymbols < 0xFFFFFFFFull;
+    void *occ = nullptr;
+    uint64_t occ_cap = 0;   // a merge's occurrences never exceed the count that started the mode
+    if (sparse_ok) {
+        occ_cap = (sparse_mode == 2 ? n / 2 : n / kSparseDiv) + 1;
+        if ((rc = ensure(ctx, S_SPARSE_OCC, occ_cap * 16, &occ))) return rc;
+    }
     // persistent: every CTA resident (at least one per SM, for the argmax);
     // otherwise one range per CTA, at most as many ranges as tiles
     const uint64_t range_grid =
@@ -1897,6 +2233,7 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     h_state->n_merges = n_merges;
     h_state->n[0] = n;
     h_state->gactive[0] = (uint32_t)ntiles;
+    h_state->sparse_from = kNoSparse;
     h_nhist[0] = n;
     BPE_CUDA(ctx, cudaMemcpyAsync(state, h_state, sizeof *h_state, cudaMemcpyHostToDevice, s), "state upload");
     BPE_CUDA(ctx, cudaMemcpyAsync(nhist, h_nhist, 8, cudaMemcpyHostToDevice, s), "nhist upload");
@@ -1941,6 +2278,13 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     L.p.nhist = (unsigned long long *)nhist;
     L.p.dhist = (uint32_t *)dhist;
     L.p.st = (TrainState *)state;
+    L.p.occ[0] = (uint32_t *)occ;
+    L.p.occ[1] = occ ? (uint32_t *)occ + 2 * occ_cap : nullptr;
+    L.p.occ_cap = (uint32_t)occ_cap;
+    L.p.ctile = (uint32_t *)st0;                  // the look-back status words are unused here
+    L.p.coff = (unsigned long long *)st1;
+    L.sscan_grid = (unsigned)ctx->sm_count * (2048 / kSparseThreads);
+    L.ctile_grid = (unsigned)std::max<uint64_t>(1, ntiles);
     const uint64_t count_work = (n + kCountTile - 1) / kCountTile;
     L.count_grid = (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(count_work, (uint64_t)ctx->sm_count * cb));
     // look-back: one tile per CTA (spare CTAs exit); two passes: one range per CTA
@@ -1955,8 +2299,9 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     std::vector<cudaEvent_t> poll_ev(kInFlight);
     for (int i = 0; i < kInFlight; i++) poll_ev[i] = ctx->events[n_prof + i];
 
-    cudaGraphExec_t exec = nullptr;
+    cudaGraphExec_t exec = nullptr, sexec = nullptr;
     if (graph && !persistent && (rc = get_graph(ctx, L, &exec))) return rc;
+    if (graph && sparse_ok && (rc = get_sparse_graph(ctx, L, &sexec))) return rc;
     if (gapped) k_ginit<<<(unsigned)((ntiles + 255) / 256), 256, 0, s>>>(L.p.glen[0], (uint32_t)ntiles, n);
     if (profile) BPE_CUDA(ctx, cudaEventRecord(ctx->events[0], s), "event");
     k_count<<<L.count_grid, kCountThreads, L.count_smem, s>>>(L.p);
@@ -1965,17 +2310,39 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     // Launch windows of G merges; keep at most kInFlight windows queued so a
     // stop (a merge with count 0) is noticed without a full drain.
     uint32_t launched = 0;
-    uint64_t window = 0;
-    bool stopped = false;
+    uint64_t window = 0, sparse_windows = 0;
+    bool stopped = false, sparse_on = false;
+    uint32_t k_sparse = 0;   // first occurrence-driven merge
+    auto sparse_begin = [&](uint32_t k) {
+        k_sparse_begin<<<1, 1, 0, s>>>(L.p, k);
+        sparse_on = true;
+        k_sparse = k;
+    };
+    if (sparse_ok && sparse_mode == 2) sparse_begin(0);
     while (launched < n_merges && !stopped) {
         if (window >= (uint64_t)kInFlight) {
             const int slot = (int)(window % kInFlight);
             BPE_CUDA(ctx, cudaEventSynchronize(poll_ev[slot]), "poll sync");
-            if ((h_poll[slot] >> 32) == 0) stopped = true;
+            const uint64_t c = h_poll[slot] >> 32;   // best count of an earlier merge: later ones are no larger
+            if (c == 0) stopped = true;
             if (stopped) break;
+            if (sparse_ok && !sparse_on && c * kSparseDiv < n) sparse_begin(launched);
         }
         uint32_t end = std::min<uint32_t>(n_merges, launched + G);
-        if (persistent) {
+        if (sparse_on) {
+            ++sparse_windows;
+            if (graph) {
+                BPE_CUDA(ctx, cudaGraphLaunch(sexec, s), "graph launch");
+            } else {
+                for (uint32_t k = launched; k < end; k++) {
+                    k_sargmax<<<L.argmax_grid, kArgmaxThreads, 0, s>>>(L.p, k);
+                    if (k == launched) launch_compaction(L, nullptr, 0, s);
+                    if (profile) cudaEventRecord(ctx->events[2 + 2 * (size_t)k], s);
+                    k_sscan<<<L.sscan_grid, kSparseThreads, 0, s>>>(L.p, k);
+                    if (profile) cudaEventRecord(ctx->events[3 + 2 * (size_t)k], s);
+                }
+            }
+        } else if (persistent) {
             void *args[] = {&L.p, &launched, &end};
             BPE_CUDA(ctx, cudaLaunchCooperativeKernel((const void *)k_train_loop, L.merge_grid, kMergeThreads, args,
                                                       L.merge_smem, s),
@@ -1998,6 +2365,9 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
         launched = end;
         window++;
     }
+    // the last occurrence-driven merge's occurrences (k_base is launched after
+    // the graphs' advances, 0 with host launches)
+    if (sparse_on) k_sargmax<<<L.argmax_grid, kArgmaxThreads, 0, s>>>(L.p, graph ? 0u : launched);
     BPE_CUDA(ctx, cudaMemcpyAsync(h_state, state, sizeof *h_state, cudaMemcpyDeviceToHost, s), "state read");
     BPE_CUDA(ctx, cudaMemcpyAsync(h_best, best, (uint64_t)n_merges * 8, cudaMemcpyDeviceToHost, s), "best read");
     BPE_CUDA(ctx, cudaMemcpyAsync(h_nhist, nhist, ((uint64_t)n_merges + 1) * 8, cudaMemcpyDeviceToHost, s),
@@ -2024,8 +2394,12 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     *n_done = done;
     const uint64_t nf = h_nhist[done];
     if (n_final) *n_final = nf;
+    const bool sparse_final = sparse_on && done > k_sparse;   // the stream holds tombstones
     if (d_symbols_final) {
-        if (gapped) {   // gather the tiles' live symbols
+        if (sparse_final) {
+            launch_compaction(L, d_symbols_final, 1, s);
+            BPE_CUDA(ctx, cudaGetLastError(), "compaction launch");
+        } else if (gapped) {   // gather the tiles' live symbols
             void *goff;
             if ((rc = ensure(ctx, S_W_OUTOFF, ntiles * 8, &goff))) return rc;
             k_gscan<<<1, 1024, 0, s>>>(L.p.glen[done & 1], (uint32_t)ntiles, (unsigned long long *)goff);
@@ -2042,9 +2416,16 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     // statistics: algorithmic bytes per kernel family and (profiled) device time
     stats_reset(ctx);
     const uint64_t per_merge = lookback ? 2 : 3;
+    const uint64_t full_windows = window - sparse_windows;
+    const uint32_t full_merges = sparse_on ? std::min(k_sparse, launched) : launched;
     ctx->stats.kernel_launches =
         1 + (gapped ? 1 : 0) + (d_symbols_final && gapped ? 2 : 0) +
-        (persistent ? (uint64_t)window : graph ? (uint64_t)window * (per_merge * kGraphIters + 1) : per_merge * launched);
+        (persistent ? (uint64_t)window
+                    : graph ? full_windows * (per_merge * kGraphIters + 1) : per_merge * full_merges) +
+        (sparse_on ? 2 + sparse_windows * 4 + (graph ? sparse_windows * (2 * kGraphIters + 1)
+                                                      : 2 * (uint64_t)(launched - full_merges)) +
+                         (sparse_final && d_symbols_final ? 4 : 0)
+                   : 0);
     const int sc = stats_slot(ctx, "pair_count"), sa = stats_slot(ctx, "argmax"), sm = stats_slot(ctx, "merge_compact");
     ctx->stats.k[sc].launches = 1;
     ctx->stats.k[sc].bytes = 4.0 * (double)n;
@@ -2055,7 +2436,9 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     }
     for (uint32_t k = 0; k < done; k++) {
         ctx->stats.k[sm].launches++;
-        ctx->stats.k[sm].bytes += 4.0 * (double)h_nhist[k] + 4.0 * (double)h_nhist[k + 1];
+        // an occurrence-driven merge reads the stream once (its few writes aside)
+        ctx->stats.k[sm].bytes += sparse_on && k >= k_sparse ? 4.0 * (double)h_nhist[k]
+                                                             : 4.0 * (double)h_nhist[k] + 4.0 * (double)h_nhist[k + 1];
     }
     if (profile) {
         float x = 0;

@@ -122,7 +122,16 @@ const char *bpe_last_error(const bpe_ctx *ctx);
  *   BPE_OPT_PERSISTENT   1 = with BPE_MERGE_TWO_PASS, the merge loop runs as one cooperative
  *                        launch per window of merges (all CTAs resident,
  *                        phases separated by grid barriers) instead of a CUDA
- *                        graph of per-phase kernels; default 0 */
+ *                        graph of per-phase kernels; default 0
+ *   BPE_OPT_SPARSE_MERGE 1 = with BPE_MERGE_TWO_PASS, once the best pair's
+ *                        count falls below 1/64 of the input length the
+ *                        merge loop stops rewriting the stream: each merge
+ *                        reads it once to find the pair's occurrences, then
+ *                        rewrites only those (the right symbol becomes a
+ *                        tombstone; the stream is compacted when tombstones
+ *                        pass a quarter of it, and at the end); same
+ *                        results; default 1.  0 = every merge rewrites the
+ *                        whole stream */
 enum {
     BPE_OPT_TABLE_LOG2 = 1,
     BPE_OPT_GRAPH = 2,
@@ -133,7 +142,8 @@ enum {
     BPE_OPT_PERSISTENT = 7,
     BPE_OPT_TRIE_LAYOUT = 8,
     BPE_OPT_UNI_CHUNK = 9,
-    BPE_OPT_TEST_STALL_TILE = 10
+    BPE_OPT_TEST_STALL_TILE = 10,
+    BPE_OPT_SPARSE_MERGE = 11
 };
 enum { BPE_TRIE_DOUBLE_ARRAY = 0, BPE_TRIE_BITMAP = 1 };
 enum { BPE_MERGE_TWO_PASS = 0, BPE_MERGE_LOOKBACK = 1, BPE_MERGE_TILES = 2 };

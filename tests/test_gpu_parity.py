@@ -156,6 +156,45 @@ def test_train_merge_variants_agree(ctx, golden, case, mode):
         ctx.set_option(bt.BPE_OPT_PERSISTENT, 0)
 
 
+@pytest.mark.parametrize("mode", ["off", "always", "always-eager"])
+@pytest.mark.parametrize("case", ["runs", "random", "alternating", "tiny", "med"])
+def test_train_sparse_modes_agree(ctx, golden, case, mode):
+    # occurrence-driven merges (tombstones, exact deltas, compaction) from
+    # merge 0 on, with graphs and with host launches, and the full-stream
+    # merge alone, give the oracle's merges and final stream; the default
+    # (automatic switch) runs in every other training test
+    import bpe_trie_encode_gb300 as bt
+    ctx.set_option(bt.BPE_OPT_SPARSE_MERGE, 0 if mode == "off" else 2)
+    ctx.set_option(bt.BPE_OPT_GRAPH, 0 if mode == "always-eager" else 1)
+    try:
+        if case == "runs":
+            text = b" ".join(b"a" * n for n in list(range(1, 40)) + [1001, 4097, 64, 65]) + b"aaaa bbbb abab" * 3
+            check_train(ctx, oracle.pretokenize(text), 60)
+            check_train(ctx, oracle.pretokenize(b"a" * 1_000_001 + b" " + b"a" * 4097 + b".bb" + b"b" * 4097), 12)
+        elif case == "random":
+            for seed in range(4):
+                rng = random.Random(200 + seed)
+                alphabet = [b"ab", b"aab ", b"aab c.", b"abc a.\n1"][seed]
+                check_train(ctx, oracle.pretokenize(rand_bytes(rng, 9000 + 4096 * seed, alphabet)), 150)
+        elif case == "alternating":
+            check_train(ctx, oracle.pretokenize(b"ab" * 50000 + b" " + b"ba" * 777), 40)
+        elif case == "tiny":
+            m, f = ctx.train(dev_sym(oracle.pretokenize(synth.corpus("tiny"))), 256)
+            assert sha(m.astype(np.uint32)) == golden["tiny"]["merges_sha256"]
+            assert sha(host_u32(f)) == golden["tiny"]["final_sha256"]
+        else:
+            g = golden["med"]
+            sym = ctx.pretokenize(dev_u8(synth.corpus("med")))
+            m, f = ctx.train(sym, g["n_merges"])
+            assert sha(m.astype(np.uint32)) == g["merges_sha256"] and sha(host_u32(f)) == g["final_sha256"]
+            for k in (1, 100, 1000):
+                _, fk = ctx.train(sym, k)
+                assert sha(host_u32(fk)) == g["checkpoints"][str(k)]["sha256"], k
+    finally:
+        ctx.set_option(bt.BPE_OPT_SPARSE_MERGE, 1)
+        ctx.set_option(bt.BPE_OPT_GRAPH, 1)
+
+
 def test_train_alternating_and_ties(ctx):
     check_train(ctx, oracle.pretokenize(b"ab" * 50000 + b" " + b"ba" * 777), 20)
     check_train(ctx, oracle.pretokenize(b"ab cd ef gh ba dc fe hg"), 10)
