@@ -1418,11 +1418,13 @@ __global__ void __launch_bounds__(kSparseThreads) k_sscan(TrainParams p, uint32_
     const uint64_t nq = (n + 3) / 4;   // the buffer is padded: a quad past n is readable
     for (uint64_t x = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; x < nq; x += (uint64_t)gridDim.x * blockDim.x) {
         const uint4 v = __ldg(reinterpret_cast<const uint4 *>(s) + x);
-        const uint32_t a[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-            if (sym_id(a[e]) != l || a[e] == kTomb || 4 * x + e >= n) continue;
-            sparse_occurrence(p, T, s, n, 4 * x + e, l, r, nid, k);
+        // positions of the quad holding l (rare): one call site for all four
+        uint32_t m = (sym_id(v.x) == l && v.x != kTomb ? 1u : 0u) | (sym_id(v.y) == l && v.y != kTomb ? 2u : 0u) |
+                     (sym_id(v.z) == l && v.z != kTomb ? 4u : 0u) | (sym_id(v.w) == l && v.w != kTomb ? 8u : 0u);
+        while (m) {
+            const uint32_t e = __ffs(m) - 1;
+            m &= m - 1;
+            if (4 * x + e < n) sparse_occurrence(p, T, s, n, 4 * x + e, l, r, nid, k);
         }
     }
 }
@@ -2427,6 +2429,7 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
                          (sparse_final && d_symbols_final ? 4 : 0)
                    : 0);
     const int sc = stats_slot(ctx, "pair_count"), sa = stats_slot(ctx, "argmax"), sm = stats_slot(ctx, "merge_compact");
+    const int ss = sparse_on ? stats_slot(ctx, "merge_scan") : sm;   // occurrence-driven merges: the scan
     ctx->stats.k[sc].launches = 1;
     ctx->stats.k[sc].bytes = 4.0 * (double)n;
     const uint32_t ran = std::min<uint32_t>(n_merges, done + 1);   // the argmax that found 0 ran too
@@ -2435,10 +2438,10 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
         ctx->stats.k[sa].bytes += 8.0 * (double)h_dhist[k];
     }
     for (uint32_t k = 0; k < done; k++) {
-        ctx->stats.k[sm].launches++;
-        // an occurrence-driven merge reads the stream once (its few writes aside)
-        ctx->stats.k[sm].bytes += sparse_on && k >= k_sparse ? 4.0 * (double)h_nhist[k]
-                                                             : 4.0 * (double)h_nhist[k] + 4.0 * (double)h_nhist[k + 1];
+        // an occurrence-driven merge reads the live stream once (its few writes aside)
+        const bool sp = sparse_on && k >= k_sparse;
+        ctx->stats.k[sp ? ss : sm].launches++;
+        ctx->stats.k[sp ? ss : sm].bytes += sp ? 4.0 * (double)h_nhist[k] : 4.0 * (double)h_nhist[k] + 4.0 * (double)h_nhist[k + 1];
     }
     if (profile) {
         float x = 0;
@@ -2450,7 +2453,7 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
                 ctx->stats.k[sa].ms += a;
             if (k < done &&
                 cudaEventElapsedTime(&b, ctx->events[2 + 2 * (size_t)k], ctx->events[3 + 2 * (size_t)k]) == cudaSuccess)
-                ctx->stats.k[sm].ms += b;
+                ctx->stats.k[sparse_on && k >= k_sparse ? ss : sm].ms += b;
         }
         cudaGetLastError();
     }
