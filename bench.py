@@ -577,8 +577,8 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "vocab": vocab_check},
         "train": {"value": round(value, 2), "unit": "merges/s", "ms_per_step": round(train_ms / args.steps, 3),
-                  "roofline": roofline(kern, ["pair_count", "merge_compact"], peak, peak_kind, traffic)},
-        "roofline": roofline(kern, ["pair_count", "merge_compact"], peak, peak_kind, traffic),
+                  "roofline": roofline(kern, ["pair_count", "merge_compact", "merge_scan", "argmax"], peak, peak_kind, traffic)},
+        "roofline": roofline(kern, ["pair_count", "merge_compact", "merge_scan", "argmax"], peak, peak_kind, traffic),
         "gpu_launches": acc["launches"],
         "timing": ("value, e2e: CUDA-graph replay as a caller runs it; roofline and kernels: per-kernel CUDA "
                    "events on the launching stream in a separate profiled pass of the same steps"),
