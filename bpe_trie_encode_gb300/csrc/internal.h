@@ -59,7 +59,7 @@ struct bpe_ctx {
     int train_words = 0;
     int merge_mode = 0;   // BPE_MERGE_*
     int persistent = 0;
-    int sparse_merge = 1;   // BPE_OPT_SPARSE_MERGE
+    int sparse_merge = 0;   // BPE_OPT_SPARSE_MERGE
     int trie_layout = 0;   // BPE_TRIE_*
     int uni_chunk = 0;     // unigram_encode chunk bytes (0: default)
     long long test_stall_tile = -1;   // BPE_OPT_TEST_STALL_TILE

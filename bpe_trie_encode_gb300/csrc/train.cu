@@ -1915,7 +1915,32 @@ __device__ __forceinline__ void exclusive_scan_1024(const uint32_t *len, uint32_
 
 // Exclusive scan of the tiles' live counts (one CTA).
 __global__ void __launch_bounds__(1024) k_gscan(const uint32_t *len, uint32_t T, unsigned long long *off) {
-    exclusive_scan_1024(len, T, off);
+    __shared__ unsigned long long s_w[32];
+    __shared__ unsigned long long s_carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s_carry = 0;
+    __syncthreads();
+    for (uint32_t base = 0; base < T; base += 1024) {
+        const uint32_t t = base + tid;
+        const unsigned long long v = t < T ? len[t] : 0ull;
+        unsigned long long x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_w[warp] = x;
+        __syncthreads();
+        unsigned long long wpre = 0, tot = 0;
+        for (int w = 0; w < 32; w++) {
+            if (w < warp) wpre += s_w[w];
+            tot += s_w[w];
+        }
+        if (t < T) off[t] = s_carry + wpre + x - v;
+        __syncthreads();
+        if (tid == 0) s_carry += tot;
+        __syncthreads();
+    }
 }
 
 // The contiguous stream: tile t's live symbols to out + off[t].

@@ -123,15 +123,15 @@ const char *bpe_last_error(const bpe_ctx *ctx);
  *                        launch per window of merges (all CTAs resident,
  *                        phases separated by grid barriers) instead of a CUDA
  *                        graph of per-phase kernels; default 0
- *   BPE_OPT_SPARSE_MERGE 1 = with BPE_MERGE_TWO_PASS, once the best pair's
- *                        count falls below 1/64 of the input length the
- *                        merge loop stops rewriting the stream: each merge
- *                        reads it once to find the pair's occurrences, then
- *                        rewrites only those (the right symbol becomes a
- *                        tombstone; the stream is compacted when tombstones
- *                        pass a quarter of it, and at the end); same
- *                        results; default 1.  0 = every merge rewrites the
- *                        whole stream */
+ *   BPE_OPT_SPARSE_MERGE occurrence-driven merges (with BPE_MERGE_TWO_PASS;
+ *                        same results): a merge reads the stream once to
+ *                        find the pair's occurrences and rewrites only those
+ *                        (the right symbol becomes a tombstone; the stream
+ *                        is compacted when tombstones pass a quarter of it,
+ *                        and at the end).  0 = off, every merge rewrites the
+ *                        whole stream (default); 1 = from the first window
+ *                        after the best pair's count falls below 1/64 of the
+ *                        input length; 2 = from merge 0 */
 enum {
     BPE_OPT_TABLE_LOG2 = 1,
     BPE_OPT_GRAPH = 2,

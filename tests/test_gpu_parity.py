@@ -156,15 +156,15 @@ def test_train_merge_variants_agree(ctx, golden, case, mode):
         ctx.set_option(bt.BPE_OPT_PERSISTENT, 0)
 
 
-@pytest.mark.parametrize("mode", ["off", "always", "always-eager"])
+@pytest.mark.parametrize("mode", ["auto", "always", "always-eager"])
 @pytest.mark.parametrize("case", ["runs", "random", "alternating", "tiny", "med"])
 def test_train_sparse_modes_agree(ctx, golden, case, mode):
     # occurrence-driven merges (tombstones, exact deltas, compaction) from
-    # merge 0 on, with graphs and with host launches, and the full-stream
-    # merge alone, give the oracle's merges and final stream; the default
-    # (automatic switch) runs in every other training test
+    # merge 0 on, with graphs and with host launches, and after the automatic
+    # switch, give the oracle's merges and final stream (every other training
+    # test runs with the mode off, the default)
     import bpe_trie_encode_gb300 as bt
-    ctx.set_option(bt.BPE_OPT_SPARSE_MERGE, 0 if mode == "off" else 2)
+    ctx.set_option(bt.BPE_OPT_SPARSE_MERGE, 1 if mode == "auto" else 2)
     ctx.set_option(bt.BPE_OPT_GRAPH, 0 if mode == "always-eager" else 1)
     try:
         if case == "runs":
@@ -191,7 +191,7 @@ def test_train_sparse_modes_agree(ctx, golden, case, mode):
                 _, fk = ctx.train(sym, k)
                 assert sha(host_u32(fk)) == g["checkpoints"][str(k)]["sha256"], k
     finally:
-        ctx.set_option(bt.BPE_OPT_SPARSE_MERGE, 1)
+        ctx.set_option(bt.BPE_OPT_SPARSE_MERGE, 0)
         ctx.set_option(bt.BPE_OPT_GRAPH, 1)
 
 
