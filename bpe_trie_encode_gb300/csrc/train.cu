@@ -2409,6 +2409,8 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
     }
     if (h_state->err & DERR_TIMEOUT)
         return fail(ctx, BPE_ERR_TIMEOUT, "bpe_train: a look-back or grid-barrier wait gave up");
+    if (h_state->err & DERR_OOB)
+        return fail(ctx, BPE_ERR_CHECKED_OOB, "bpe_train: a merge's occurrences overflowed their list");
     uint32_t done = 0;
     while (done < n_merges && (h_best[done] >> 32) != 0) done++;
     for (uint32_t k = 0; k < done; k++) {
