@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the extra legs (word-frequency, large, batch)")
+    ap.add_argument("--sparse-merge", type=int, choices=[0, 1, 2], default=0,
+                    help="BPE_OPT_SPARSE_MERGE for the full-stream training leg (0 = off, the library default)")
     ap.add_argument("--leg", choices=["unigram"], default=None,
                     help="run only that leg and print its JSON (profiling)")
     return ap.parse_args()
@@ -411,6 +413,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     ctx = bt.Context(local_rank)
+    ctx.set_option(bt.BPE_OPT_SPARSE_MERGE, args.sparse_merge)
     g = golden()
     peak, peak_kind = peaks()
     n_merges = args.merges or TRAIN[args.train]
@@ -575,7 +578,7 @@ def run_ours(args, rank, world, local_rank):
                    "train_corpus_bytes": int(text.size), "n_merges": n_merges,
                    "l2": "flushed between steps (256 MiB write)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "vocab": vocab_check},
+                   "vocab": vocab_check, "sparse_merge": args.sparse_merge},
         "train": {"value": round(value, 2), "unit": "merges/s", "ms_per_step": round(train_ms / args.steps, 3),
                   "roofline": roofline(kern, ["pair_count", "merge_compact", "merge_scan", "argmax"], peak, peak_kind, traffic)},
         "roofline": roofline(kern, ["pair_count", "merge_compact", "merge_scan", "argmax"], peak, peak_kind, traffic),
