@@ -2225,14 +2225,13 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
                  "k_train_loop occupancy");
         if (pb < 1) return fail(ctx, BPE_ERR_CUDA, "bpe_train: the persistent merge loop does not fit on an SM");
     }
-    // occurrence-driven merges: automatic (1) or from merge 0 (2); positions are 32-bit
-    const int sparse_mode = ctx->sparse_merge;
-    const bool sparse_ok = sparse_mode && mode == BPE_MERGE_TWO_PASS && !persistent && n > 0 &&
+    // occurrence-driven merges once the best count is rare; positions are 32-bit
+    const bool sparse_ok = ctx->sparse_merge && mode == BPE_MERGE_TWO_PASS && !persistent && n > 0 &&
                            n + kPadSymbols < 0xFFFFFFFFull;
     void *occ = nullptr;
     uint64_t occ_cap = 0;   // a merge's occurrences never exceed the count that started the mode
     if (sparse_ok) {
-        occ_cap = (sparse_mode == 2 ? n / 2 : n / kSparseDiv) + 1;
+        occ_cap = n / kSparseDiv + 1;
         if ((rc = ensure(ctx, S_SPARSE_OCC, occ_cap * 16, &occ))) return rc;
     }
     // persistent: every CTA resident (at least one per SM, for the argmax);
@@ -2345,7 +2344,6 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
         sparse_on = true;
         k_sparse = k;
     };
-    if (sparse_ok && sparse_mode == 2) sparse_begin(0);
     while (launched < n_merges && !stopped) {
         if (window >= (uint64_t)kInFlight) {
             const int slot = (int)(window % kInFlight);
