@@ -1307,8 +1307,8 @@ __device__ __forceinline__ void argmax_into(const TrainParams &p, uint32_t k, un
 //               merge's argmax.
 // A pair is a live symbol and the next live one after it (tombstones are
 // skipped); the stream is compacted when tombstones pass a quarter of it
-// (k_ccount, k_cscan, k_cscatter, k_cdone at the start of a window) and once
-// at the end.
+// (k_ccount, k_cscan, k_cscatter, k_cdone, once per window of merges, after
+// its first k_sargmax has applied the previous merge) and once at the end.
 //
 // Count deltas of one occurrence (i, j) that merges, taken from the old
 // stream (p: the live position before i when i has no WORD_START; q: the
