@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the extra legs (word-frequency, large, batch)")
-    ap.add_argument("--sparse-merge", type=int, choices=[0, 1], default=0,
+    ap.add_argument("--sparse-merge", type=int, choices=[0, 1, 2], default=0,
                     help="BPE_OPT_SPARSE_MERGE for the full-stream training leg (0 = off, the library default)")
     ap.add_argument("--leg", choices=["unigram"], default=None,
                     help="run only that leg and print its JSON (profiling)")

@@ -179,8 +179,8 @@ extern "C" int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value) {
         ctx->persistent = value ? 1 : 0;
         return BPE_OK;
     case BPE_OPT_SPARSE_MERGE:
-        if (value < 0 || value > 1)
-            return fail(ctx, BPE_ERR_INVALID_ARG, "sparse merge mode %lld is not 0 or 1", (long long)value);
+        if (value < 0 || value > 2)
+            return fail(ctx, BPE_ERR_INVALID_ARG, "sparse merge mode %lld is not 0, 1 or 2", (long long)value);
         ctx->sparse_merge = (int)value;
         return BPE_OK;
     case BPE_OPT_TEST_STALL_TILE:

@@ -1321,9 +1321,9 @@ __device__ __forceinline__ void argmax_into(const TrainParams &p, uint32_t k, un
 //   right edge (j, q), unless q starts a merging occurrence: -(r, s[q]),
 //       +(new, s[q]).
 // For l == r only starts with an odd number of consecutive valid starts
-// ending at them merge (leftmost first); the right half of the previous
-// merging start and the next merging start are then exactly the cases the
-// two tests above check.
+// ending at them merge (leftmost first), and the first start of each run
+// walks the run; the right half of the previous merging start and the next
+// merging start are then exactly the cases the two tests above check.
 constexpr uint32_t kTomb = 0xFFFFFFFFu;   // never a symbol: bits 17..31 of a symbol are 0
 constexpr uint32_t kNoSparse = 0xFFFFFFFFu;
 constexpr int kSparseThreads = 256;
@@ -1344,28 +1344,11 @@ __device__ __forceinline__ long long prev_live(const uint32_t *s, uint64_t a) {
     return b;
 }
 
-// Position i holds l (live): if (i, next live) is an occurrence that merges,
-// apply its count deltas and list it.
-__device__ void sparse_occurrence(const TrainParams &p, const Table &T, const uint32_t *s, uint64_t n, uint64_t i,
-                                  uint32_t l, uint32_t r, uint32_t nid, uint32_t k) {
-    const uint64_t j = next_live(s, i, n);
-    if (j >= n) return;
-    const uint32_t sj = __ldg(s + j);
-    if (sym_id(sj) != r || (sj & kWordStart)) return;
+// The count deltas of an occurrence (i, j) that merges, and its list entry.
+__device__ void occurrence_deltas(const TrainParams &p, const Table &T, const uint32_t *s, uint64_t n, uint64_t i,
+                                  uint64_t j, uint32_t l, uint32_t r, uint32_t nid, uint32_t k) {
     const uint32_t si = __ldg(s + i);
-    if (l == r) {   // merges when the run of valid starts ending at i is odd
-        uint32_t c = 1;
-        uint64_t x = i;
-        for (;;) {
-            if (__ldg(s + x) & kWordStart) break;
-            const long long pp = prev_live(s, x);
-            if (pp < 0 || sym_id(__ldg(s + pp)) != l) break;
-            ++c;
-            x = (uint64_t)pp;
-        }
-        if (!(c & 1u)) return;
-        global_add(T, pair_key(l, r), 0xFFFFFFFFu);
-    }
+    if (l == r) global_add(T, pair_key(l, r), 0xFFFFFFFFu);
     if (!(si & kWordStart)) {
         const long long pp = prev_live(s, i);
         if (pp >= 0) {
@@ -1400,6 +1383,41 @@ __device__ void sparse_occurrence(const TrainParams &p, const Table &T, const ui
         p.occ[k & 1][2 * (uint64_t)x + 1] = (uint32_t)j;
     } else {
         atomicOr(&p.st->err, DERR_OOB);   // the list is sized by a count no later merge exceeds
+    }
+}
+
+// Whether live position x starts a pair with id r next: *y = the next live position.
+__device__ __forceinline__ bool valid_start(const uint32_t *s, uint64_t n, uint64_t x, uint32_t r, uint64_t *y) {
+    *y = next_live(s, x, n);
+    return *y < n && sym_id(__ldg(s + *y)) == r && !(__ldg(s + *y) & kWordStart);
+}
+
+// Position i holds l (live).  For l != r: if (i, next live) is an
+// occurrence, it merges.  For l == r only the first valid start of a run of
+// consecutive valid starts proceeds: it walks the run and handles the starts
+// that merge (every second one, leftmost first), so a run of length L costs
+// O(L) steps in one thread.
+__device__ void sparse_occurrence(const TrainParams &p, const Table &T, const uint32_t *s, uint64_t n, uint64_t i,
+                                  uint32_t l, uint32_t r, uint32_t nid, uint32_t k) {
+    uint64_t j;
+    if (!valid_start(s, n, i, r, &j)) return;
+    if (l != r) {
+        occurrence_deltas(p, T, s, n, i, j, l, r, nid, k);
+        return;
+    }
+    if (!(__ldg(s + i) & kWordStart)) {
+        const long long pp = prev_live(s, i);
+        if (pp >= 0 && sym_id(__ldg(s + pp)) == l) return;   // a valid start precedes i: not the run's first
+    }
+    uint64_t x = i, y = j;
+    for (;;) {
+        occurrence_deltas(p, T, s, n, x, y, l, r, nid, k);
+        const uint64_t z = next_live(s, y, n);   // the next start that may merge
+        if (z >= n || sym_id(__ldg(s + z)) != l || (__ldg(s + z) & kWordStart)) break;
+        uint64_t w;
+        if (!valid_start(s, n, z, r, &w)) break;
+        x = z;
+        y = w;
     }
 }
 
@@ -2225,13 +2243,15 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
                  "k_train_loop occupancy");
         if (pb < 1) return fail(ctx, BPE_ERR_CUDA, "bpe_train: the persistent merge loop does not fit on an SM");
     }
-    // occurrence-driven merges once the best count is rare; positions are 32-bit
-    const bool sparse_ok = ctx->sparse_merge && mode == BPE_MERGE_TWO_PASS && !persistent && n > 0 &&
+    // occurrence-driven merges once the best count is rare (1) or from merge 0
+    // (2); positions are 32-bit
+    const int sparse_mode = ctx->sparse_merge;
+    const bool sparse_ok = sparse_mode && mode == BPE_MERGE_TWO_PASS && !persistent && n > 0 &&
                            n + kPadSymbols < 0xFFFFFFFFull;
     void *occ = nullptr;
     uint64_t occ_cap = 0;   // a merge's occurrences never exceed the count that started the mode
     if (sparse_ok) {
-        occ_cap = n / kSparseDiv + 1;
+        occ_cap = (sparse_mode == 2 ? n / 2 : n / kSparseDiv) + 1;
         if ((rc = ensure(ctx, S_SPARSE_OCC, occ_cap * 16, &occ))) return rc;
     }
     // persistent: every CTA resident (at least one per SM, for the argmax);
@@ -2344,6 +2364,7 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
         sparse_on = true;
         k_sparse = k;
     };
+    if (sparse_ok && sparse_mode == 2) sparse_begin(0);
     while (launched < n_merges && !stopped) {
         if (window >= (uint64_t)kInFlight) {
             const int slot = (int)(window % kInFlight);

@@ -131,7 +131,7 @@ const char *bpe_last_error(const bpe_ctx *ctx);
  *                        and at the end).  0 = off, every merge rewrites the
  *                        whole stream (default); 1 = from the first window
  *                        after the best pair's count falls below 1/64 of the
- *                        input length */
+ *                        input length; 2 = from merge 0 */
 enum {
     BPE_OPT_TABLE_LOG2 = 1,
     BPE_OPT_GRAPH = 2,

@@ -156,17 +156,19 @@ def test_train_merge_variants_agree(ctx, golden, case, mode):
         ctx.set_option(bt.BPE_OPT_PERSISTENT, 0)
 
 
-@pytest.mark.parametrize("mode", ["auto", "auto-eager"])
+@pytest.mark.parametrize("mode", ["auto", "auto-eager", "always", "always-eager"])
 @pytest.mark.parametrize("case", ["runs", "random", "alternating", "tiny", "med"])
 def test_train_sparse_modes_agree(ctx, golden, case, mode):
     # occurrence-driven merges (tombstones, exact deltas, compaction) after
-    # the automatic switch, with graphs and with host launches, give the
-    # oracle's merges and final stream (every other training test runs with
-    # the mode off, the default); the switch comes at the first poll (merge
-    # 96), so the longer cases are the ones that exercise it
+    # the automatic switch and from merge 0, with graphs and with host
+    # launches, give the oracle's merges and final stream (every other
+    # training test runs with the mode off, the default); the automatic
+    # switch comes at the first poll (merge 96), so only the longer cases
+    # exercise it, while merge 0 on puts million-symbol runs through the
+    # l == r walk
     import bpe_trie_encode_gb300 as bt
-    ctx.set_option(bt.BPE_OPT_SPARSE_MERGE, 1)
-    ctx.set_option(bt.BPE_OPT_GRAPH, 0 if mode == "auto-eager" else 1)
+    ctx.set_option(bt.BPE_OPT_SPARSE_MERGE, 2 if mode.startswith("always") else 1)
+    ctx.set_option(bt.BPE_OPT_GRAPH, 0 if mode.endswith("eager") else 1)
     try:
         if case == "runs":
             text = b" ".join(b"a" * n for n in list(range(1, 40)) + [1001, 4097, 64, 65]) + b"aaaa bbbb abab" * 3
