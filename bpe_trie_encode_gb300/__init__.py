@@ -22,7 +22,8 @@ import numpy as np
 import torch
 
 from . import _capi
-from ._capi import (BPE_MAX_MERGES, BPE_MERGE_LOOKBACK, BPE_MERGE_TILES, BPE_MERGE_TWO_PASS,  # noqa: F401
+from ._capi import (BPE_MAX_MERGES, BPE_MERGE_LISTS, BPE_MERGE_LOOKBACK, BPE_MERGE_TILES,  # noqa: F401
+                    BPE_MERGE_TWO_PASS, BPE_OPT_LIST_FRONTIER, BPE_OPT_LIST_TAIL,
                     BPE_OPT_CHUNK, BPE_OPT_GRAPH, BPE_OPT_MERGE, BPE_OPT_PERSISTENT, BPE_OPT_PROFILE,
                     BPE_OPT_SPARSE_MERGE, BPE_OPT_TABLE_LOG2, BPE_OPT_TRAIN_WORDS, BPE_OPT_TRIE_LAYOUT,
                     BPE_OPT_UNI_CHUNK, BPE_TRIE_BITMAP, BPE_TRIE_DOUBLE_ARRAY, BPE_WORD_START, BpeError)
@@ -188,6 +189,24 @@ class Context:
         _capi.check(self._h, rc)
         return ids_out[: n_ids.value], id_off[: n_docs + 1]
 
+    def decode(self, merges, ids: torch.Tensor) -> torch.Tensor:
+        """Bytes of ids or symbols (int32 CUDA tensor; WORD_START ignored)
+        under the vocabulary of ``merges``: a uint8 CUDA tensor."""
+        ids = _need_cuda(ids, torch.int32, "ids", self.device)
+        arr, n = _merge_array(merges)
+        n_bytes = ctypes.c_uint64(0)
+        ptr = ctypes.c_void_p(ids.data_ptr() if ids.numel() else 0)
+        self._sync_stream()
+        rc = self.lib.bpe_decode(self._h, arr, n, ptr, ids.numel(), None, 0, ctypes.byref(n_bytes))
+        if rc not in (0, -6):
+            _capi.check(self._h, rc)
+        out = torch.empty(max(n_bytes.value, 1), dtype=torch.uint8, device=self.device)
+        if ids.numel():
+            _capi.check(self._h, self.lib.bpe_decode(self._h, arr, n, ptr, ids.numel(),
+                                                     ctypes.c_void_p(out.data_ptr()), out.numel(),
+                                                     ctypes.byref(n_bytes)))
+        return out[: n_bytes.value]
+
 
     def unigram(self, trie: Trie, scores, unk_id: int, unk_score: float) -> "Unigram":
         """A Unigram (Viterbi) model over ``trie``: one f64 score per token
@@ -317,14 +336,29 @@ class Stream:
             pass
 
 
+def _merge_array(merges):
+    """(n, 4) uint32 rows (left, right, new_id, count) as a bpe_merge array."""
+    m = np.ascontiguousarray(np.asarray(merges, dtype=np.uint32).reshape(-1, 4))
+    arr = (_capi.bpe_merge * max(m.shape[0], 1))()
+    if m.shape[0]:
+        ctypes.memmove(arr, m.ctypes.data, m.nbytes)
+    return arr, m.shape[0]
+
+
 def vocab_from_merges(merges):
-    """Token byte strings of ids 0 .. 255 + len(merges) (host bookkeeping for
-    trie_build): bytes(b) = [b], bytes(256 + k) = bytes(left) + bytes(right).
-    Returns (uint8 array, uint64 offsets)."""
-    m = np.asarray(merges, dtype=np.uint32).reshape(-1, 4)
-    toks = [bytes([b]) for b in range(256)]
-    for l, r in m[:, :2].tolist():
-        toks.append(toks[l] + toks[r])
-    off = np.zeros(len(toks) + 1, dtype=np.uint64)
-    off[1:] = np.cumsum([len(t) for t in toks])
-    return np.frombuffer(b"".join(toks), dtype=np.uint8), off
+    """Token byte strings of ids 0 .. 255 + len(merges), through the library's
+    bpe_vocab_from_merges (host only).  Returns (uint8 array, uint64 offsets),
+    the layout ``Context.trie_build`` takes."""
+    lib = _capi.load()
+    arr, n = _merge_array(merges)
+    n_bytes = ctypes.c_uint64(0)
+    rc = lib.bpe_vocab_from_merges(arr, n, None, 0, None, ctypes.byref(n_bytes))
+    if rc not in (0, -6):
+        raise BpeError(rc, "bpe_vocab_from_merges: malformed merge table")
+    vb = np.empty(max(n_bytes.value, 1), dtype=np.uint8)
+    off = np.empty(257 + n, dtype=np.uint64)
+    rc = lib.bpe_vocab_from_merges(arr, n, ctypes.c_void_p(vb.ctypes.data), vb.size,
+                                   ctypes.c_void_p(off.ctypes.data), ctypes.byref(n_bytes))
+    if rc != 0:
+        raise BpeError(rc, "bpe_vocab_from_merges failed")
+    return vb[: n_bytes.value], off

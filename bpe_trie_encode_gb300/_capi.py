@@ -22,9 +22,9 @@ BPE_WORD_START = 0x10000
 BPE_MAX_MERGES = 65280
 BPE_OPT_TABLE_LOG2, BPE_OPT_GRAPH, BPE_OPT_PROFILE, BPE_OPT_CHUNK, BPE_OPT_TRAIN_WORDS = 1, 2, 3, 4, 5
 BPE_OPT_MERGE, BPE_OPT_PERSISTENT, BPE_OPT_TRIE_LAYOUT, BPE_OPT_UNI_CHUNK = 6, 7, 8, 9
-BPE_OPT_TEST_STALL_TILE, BPE_OPT_SPARSE_MERGE = 10, 11
+BPE_OPT_TEST_STALL_TILE, BPE_OPT_SPARSE_MERGE, BPE_OPT_LIST_FRONTIER, BPE_OPT_LIST_TAIL = 10, 11, 12, 13
 BPE_TRIE_DOUBLE_ARRAY, BPE_TRIE_BITMAP = 0, 1
-BPE_MERGE_TWO_PASS, BPE_MERGE_LOOKBACK, BPE_MERGE_TILES = 0, 1, 2
+BPE_MERGE_TWO_PASS, BPE_MERGE_LOOKBACK, BPE_MERGE_TILES, BPE_MERGE_LISTS = 0, 1, 2, 3
 
 # every symbol the header declares (checked by the tests)
 EXPORTS = [
@@ -33,6 +33,7 @@ EXPORTS = [
     "trie_build", "trie_layout", "trie_info", "trie_free", "trie_encode",
     "trie_encode_noalloc", "trie_stream_open", "trie_stream_push", "trie_stream_close",
     "trie_encode_host", "unigram_create", "unigram_encode", "unigram_free",
+    "bpe_vocab_from_merges", "bpe_decode",
 ]
 
 
@@ -95,6 +96,8 @@ def load() -> ctypes.CDLL:
             "unigram_create": (i32, [vp, vp, vp, u32, ctypes.c_int32, ctypes.c_double, P(vp)]),
             "unigram_encode": (i32, [vp, vp, vp, vp, u32, vp, u64, vp, P(u64)]),
             "unigram_free": (None, [vp]),
+            "bpe_vocab_from_merges": (i32, [vp, u32, vp, u64, vp, P(u64)]),
+            "bpe_decode": (i32, [vp, vp, u32, vp, u64, vp, u64, P(u64)]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

@@ -51,6 +51,7 @@ int ensure(bpe_ctx *ctx, Slot s, size_t bytes, void **out) {
         sc.cap = want;
         ctx->graph.key.clear();                    // pointers changed: recapture
         ctx->graph_sparse.key.clear();
+        ctx->graph_lists.key.clear();
     }
     *out = sc.p;
     return BPE_OK;
@@ -138,6 +139,7 @@ extern "C" void bpe_ctx_destroy(bpe_ctx *ctx) {
     if (ctx->pipe_pinned) cudaFreeHost(ctx->pipe_pinned);
     if (ctx->graph.exec) cudaGraphExecDestroy(ctx->graph.exec);
     if (ctx->graph_sparse.exec) cudaGraphExecDestroy(ctx->graph_sparse.exec);
+    if (ctx->graph_lists.exec) cudaGraphExecDestroy(ctx->graph_lists.exec);
     for (auto &s : ctx->scratch)
         if (s.p) cudaFree(s.p);
     for (auto ev : ctx->events) cudaEventDestroy(ev);
@@ -166,7 +168,8 @@ extern "C" int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value) {
         ctx->train_words = value ? 1 : 0;
         return BPE_OK;
     case BPE_OPT_MERGE:
-        if (value != BPE_MERGE_TILES && value != BPE_MERGE_LOOKBACK && value != BPE_MERGE_TWO_PASS)
+        if (value != BPE_MERGE_TILES && value != BPE_MERGE_LOOKBACK && value != BPE_MERGE_TWO_PASS &&
+            value != BPE_MERGE_LISTS)
             return fail(ctx, BPE_ERR_INVALID_ARG, "unknown merge variant %lld", (long long)value);
         ctx->merge_mode = (int)value;
         return BPE_OK;
@@ -182,6 +185,16 @@ extern "C" int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value) {
         if (value < 0 || value > 2)
             return fail(ctx, BPE_ERR_INVALID_ARG, "sparse merge mode %lld is not 0, 1 or 2", (long long)value);
         ctx->sparse_merge = (int)value;
+        return BPE_OK;
+    case BPE_OPT_LIST_FRONTIER:
+        if (value < 0 || value > 8192)
+            return fail(ctx, BPE_ERR_INVALID_ARG, "list frontier %lld outside 0..8192", (long long)value);
+        ctx->list_frontier = (int)value;
+        return BPE_OK;
+    case BPE_OPT_LIST_TAIL:
+        if (value < -1 || value > 2048)
+            return fail(ctx, BPE_ERR_INVALID_ARG, "list tail %lld outside -1..2048", (long long)value);
+        ctx->list_tail = (int)value;
         return BPE_OK;
     case BPE_OPT_TEST_STALL_TILE:
         ctx->test_stall_tile = value < 0 ? -1 : value;

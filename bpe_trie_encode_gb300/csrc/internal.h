@@ -24,6 +24,9 @@ enum Slot {
     S_UNI_START, S_UNI_STATE, S_UNI_BACK, S_UNI_GBACK, S_UNI_CHUNK, S_UNI_FLAG, S_UNI_PREFIX, S_UNI_STATUS,
     S_UNI_TSTART,
     S_SPARSE_OCC,
+    S_DEC_TOK, S_DEC_OFF, S_DEC_BSUM, S_DEC_STATE,
+    S_L_STATE, S_L_OCC, S_L_EKEY, S_L_ECNT, S_L_ELEN, S_L_EOFF, S_L_VLEN, S_L_BFILL, S_L_EBEST, S_L_FRONT,
+    S_L_HSLOT, S_L_HCNT, S_L_HENT, S_L_NS, S_L_CAND, S_L_APP, S_L_REC, S_L_CSTAT, S_L_KMODE,
     S_NUM
 };
 
@@ -57,15 +60,18 @@ struct bpe_ctx {
     int profile = 0;
     int chunk = 256;   // trie_encode bytes per chunk (measured best on both encode workloads)
     int train_words = 0;
-    int merge_mode = 0;   // BPE_MERGE_*
+    int merge_mode = BPE_MERGE_LISTS;   // BPE_MERGE_*
     int persistent = 0;
     int sparse_merge = 0;   // BPE_OPT_SPARSE_MERGE
+    int list_frontier = 0;  // BPE_OPT_LIST_FRONTIER (0: default)
+    int list_tail = -1;     // BPE_OPT_LIST_TAIL (-1: default)
     int trie_layout = 0;   // BPE_TRIE_*
     int uni_chunk = 0;     // unigram_encode chunk bytes (0: default)
     long long test_stall_tile = -1;   // BPE_OPT_TEST_STALL_TILE
     // cached graph of merge iterations
     bpe::TrainGraph graph;
     bpe::TrainGraph graph_sparse;   // the same for occurrence-driven merge windows
+    bpe::TrainGraph graph_lists;    // the same for the occurrence-list merge loop
     // profiling events (grown on demand)
     std::vector<cudaEvent_t> events;
     bpe_stats stats{};
@@ -106,6 +112,12 @@ int stats_slot(bpe_ctx *ctx, const char *name);
 
 // The bitmap-node layout of a trie, built on its first use (kept with the trie).
 int trie_bitmap_nodes(bpe_ctx *ctx, const bpe_trie *trie);
+
+// The merge loop over per-pair occurrence lists (train_lists.cu).  Needs
+// byte-level input (ids < 256); *not_bytes is set, with nothing done, when a
+// symbol is not one.
+int train_lists(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_merges, bpe_merge *h_merges_out,
+                uint32_t *n_done, uint32_t *d_symbols_final, uint64_t *n_final, bool *not_bytes);
 
 // Forget a stream's carried bytes (start a new document).
 void stream_reset(bpe_stream *st);

@@ -2226,7 +2226,8 @@ int train_once(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_m
         return rc;
     int cb, mb;
     if ((rc = occupancy(ctx, &cb, &mb))) return rc;
-    const int mode = ctx->merge_mode;
+    // the list loop hands input it cannot take (ids past one byte) to the two-pass loop
+    const int mode = ctx->merge_mode == BPE_MERGE_LISTS ? (int)BPE_MERGE_TWO_PASS : ctx->merge_mode;
     const bool lookback = mode == BPE_MERGE_LOOKBACK, gapped = mode == BPE_MERGE_TILES;
     const bool profile = ctx->profile != 0;
     const bool graph = ctx->use_graph && !profile;
@@ -3107,6 +3108,13 @@ extern "C" int bpe_train(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, ui
             BPE_CUDA(ctx, cudaStreamSynchronize(ctx->stream), "final sync");
         }
         return BPE_OK;
+    }
+    if (ctx->merge_mode == BPE_MERGE_LISTS && !ctx->train_words) {
+        bool not_bytes = false;
+        const int rc = train_lists(ctx, d_symbols, n, n_merges, h_merges_out, n_done, d_symbols_final, n_final,
+                                   &not_bytes);
+        if (rc != BPE_OK || !not_bytes) return rc;
+        // ids beyond one byte: the full-stream loop with the hash-table count
     }
     uint32_t lg = ctx->table_log2;
     const bool automatic = (lg == 0);

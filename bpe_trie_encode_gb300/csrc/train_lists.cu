@@ -1,0 +1,1877 @@
+// train_lists.cu -- the BPE merge loop driven by per-pair occurrence lists.
+//
+// [GPU-BPE] "What is this?" and "What it does" 2.-3.: count every adjacent
+// pair inside a word, take the most frequent (ties: lowest left id, then
+// lowest right id), replace its occurrences left to right without overlap by
+// a new symbol, repeat.  The pages rescan and compact the whole stream for
+// every merge.  Here a merge touches only the pair's occurrences:
+//
+//   * Every pair occurrence ever formed is recorded once, in the list of its
+//     pair.  An occurrence of (a, b) can only form in the merge that creates
+//     the younger of a and b (or before the first merge): a position's id
+//     only ever grows, and its right neighbour changes only when the position
+//     itself merges.  So each pair's list is written in one merge and only
+//     loses members afterwards; a merge reads its pair's list and skips the
+//     entries that no longer hold the pair.
+//   * Positions are stable.  A merged pair keeps its left position, which
+//     takes the new id; the positions of the right token are marked dead.  A
+//     live position's token length is the length of its id's byte string, so
+//     the next live position is p + len(id); the last byte of a multi-byte
+//     token stores the distance back to the token's first position, so the
+//     previous live position is found from p - 1 in one step.
+//   * Counts are kept exactly: a merge subtracts the pairs it destroys
+//     (through the per-position entry index of the pair starting there) and
+//     creates new entries, with their lists, for the pairs it forms.  New
+//     pairs always contain the new id, so they are new entries.
+//   * The argmax scans a frontier: all entries whose count reached a
+//     threshold T when they were last looked at.  Counts only fall after an
+//     entry is created, and the best count never rises, so while the
+//     frontier's best is at least T it is the global best; otherwise every
+//     entry is rescanned into a new frontier with a lower threshold.
+//   * The stream is compacted once, at the end (decoupled look-back).
+//
+// Kernels:
+//   k_bcount     pair counts of the input (byte ids): per CTA a direct-indexed
+//                table of 65,536 16-bit counters in shared memory, 128-bit
+//                loads, flushed to the global counts when a counter nears its
+//                limit and at the end
+//   k_lbase      one CTA: the byte-pair entries (key, list offsets by scan),
+//                the argmax of merge 0 and the first frontier
+//   k_bfill      the working copy of the stream, each position's pair entry and
+//                the pair lists (per tile: ranks in shared memory, one global
+//                reservation per distinct pair)
+//   k_lscan      per merge: the pair's live occurrences; count deltas; new
+//                pairs grouped per CTA round and registered in a per-merge
+//                hash; the last CTA creates the new entries and lists, and
+//                finds the next merge's pair in the frontier
+//   k_lapply     per merge: new ids, dead marks and back distances; new pairs
+//                into their lists; a full rescan when the frontier ran dry
+//   k_lcompact   the live symbols in order (warp scans, decoupled look-back)
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace bpe {
+namespace {
+
+constexpr uint32_t kDead = 0x80000000u;       // dead position; bits 0..29: distance back to its token's head
+constexpr uint32_t kDistMask = 0x3FFFFFFFu;
+constexpr uint32_t kNone = 0xFFFFFFFFu;
+constexpr uint32_t kBadBits = 0xFFFEFF00u;    // bits a byte-level input symbol never has
+constexpr uint32_t kBaseEntries = 65536;      // entry (l << 8) | r for byte pairs
+constexpr int kBcThreads = 1024;
+constexpr int kBcQuads = 4;                   // 128-bit loads per thread and step
+constexpr uint32_t kBcLimit = 0x7FFFu;        // a counter at this value asks for a flush
+constexpr size_t kBcSmem = 32768 * sizeof(uint32_t);   // 65,536 16-bit counters
+constexpr int kBfThreads = 1024;
+constexpr int kBfItems = 8;                   // positions per thread and tile
+constexpr int kBfTile = kBfThreads * kBfItems;
+constexpr size_t kBfSmem = 32768 * sizeof(uint32_t) + kBfTile * sizeof(uint16_t) + kBfTile * sizeof(uint32_t);
+constexpr int kLsThreads = 256;
+constexpr int kLsItems = 4;                   // list entries per thread and round
+constexpr int kLsRound = kLsThreads * kLsItems;
+constexpr int kLsRecCap = 2 * kLsRound;       // staged new pairs per round
+constexpr int kLsHash = 2 * kLsRecCap;        // per-round distinct new pairs (shared hash, at most half full)
+constexpr int kLaThreads = 256;
+constexpr int kTlThreads = 512;
+constexpr int kTlList = 4096;                 // longest list the single-CTA tail takes
+constexpr int kTlRecCap = 2 * kTlList;        // new pairs of one tail merge (two per occurrence at most)
+constexpr int kTlHash = kTlRecCap;            // distinct new pairs of a tail merge never exceed its pairs
+constexpr uint32_t kTlBudget = 512;           // merges per tail launch
+constexpr int kSlots = 8;                     // (tail, scan, apply) slots per captured graph
+constexpr int kCpThreads = 256;
+constexpr int kCpItems = 32;                  // 8 coalesced 128-bit loads per thread
+constexpr int kCpTile = kCpThreads * kCpItems;
+constexpr uint32_t kHashProbes = 4096;
+constexpr unsigned kSpinLimit = 1u << 22;
+constexpr int kInFlight = 3;
+constexpr uint32_t kFfInit = 224;             // frontier threshold: ff / 256 of the last count
+enum : uint32_t { LERR_BADINPUT = 16u, LERR_ENTRIES = 32u, LERR_LISTS = 64u, LERR_HASH = 128u, LERR_RECORDS = 256u };
+
+struct LState {
+    uint32_t k_cur, n_merges, err, D;           // k_cur: the next merge; D: entries in use
+    unsigned long long occ_top;                  // list storage in use
+    uint32_t T, fn, fvalid, fcur;                // frontier: threshold, size, valid, buffer
+    uint32_t ff;                                 // next threshold = ff / 256 of the last merge's count
+    uint32_t cmax;                               // largest count of the input
+    uint32_t pad0;
+    uint32_t ticket[2], ticket4[2];              // last-CTA tickets of k_lscan / k_lapply, by merge parity
+    uint32_t napp[2], nrec[2], nns[2];           // per merge parity: occurrences, new-pair records, new slots
+    unsigned long long rebuilds;
+    unsigned long long live;                     // compaction: symbols kept
+    uint32_t cp_ticket, tail_len;                // tail_len: longest list the tail kernel takes (0: off)
+    unsigned long long tail_merges, multi_merges;
+};
+
+struct LP {
+    const uint32_t *in;
+    uint64_t n;
+    uint32_t *sym, *pe, *occ;
+    unsigned long long occ_cap;
+    uint32_t *ekey, *ecnt, *ellen;
+    unsigned long long *eloff;
+    uint32_t dcap;
+    uint32_t *vlen;        // byte length of every id (65,536)
+    uint32_t *bfill;       // k_bfill: per byte pair, list slots handed out
+    unsigned long long *best;   // per merge: count << 32 | ~key (0: stop)
+    uint32_t *ebest;       // per merge: its entry
+    uint2 *fr[2];          // argmax frontier: {entry, key}, two buffers
+    uint32_t fcap;
+    unsigned long long *hslot;   // per-merge hash: (k + 1) << 32 | key
+    uint32_t *hcnt, *hent;
+    uint32_t hmask;
+    uint32_t *ns[2];       // slots claimed by a merge, by parity
+    uint32_t *app[2];      // per merge parity: left positions of merging occurrences
+    uint4 *rec[2];         // per merge parity: new pairs {slot, rank, position, 0}
+    uint32_t app_cap, rec_cap;
+    unsigned long long *cand;   // k_lapply rescan: per CTA {best, entry}
+    unsigned long long *cstat;  // compaction: per tile status
+    uint8_t *kmode;        // per merge: 1 = run by the tail, 2 = by the multi-CTA kernels
+    LState *st;
+};
+
+__device__ __forceinline__ unsigned long long pack(uint32_t count, uint32_t key) {
+    return ((unsigned long long)count << 32) | (unsigned long long)(~key);
+}
+__device__ __forceinline__ uint32_t sid(uint32_t s) { return s & 0xFFFFu; }
+__device__ __forceinline__ uint32_t base_key(uint32_t e) { return ((e >> 8) << 16) | (e & 0xFFu); }
+
+// The live position before live position p (p > 0), and its symbol.
+__device__ __forceinline__ uint32_t prev_live(const uint32_t *sym, uint32_t p, uint32_t *sa) {
+    const uint32_t x = p - 1, sx = __ldcg(sym + x);
+    if (!(sx & kDead)) {
+        *sa = sx;
+        return x;
+    }
+    const uint32_t a = x - (sx & kDistMask);
+    *sa = __ldcg(sym + a);
+    return a;
+}
+
+// Programmatic dependent launch: a kernel of the merge loop lets the next
+// one be scheduled as soon as it starts, and waits for the previous one (all
+// its memory operations) before touching anything it wrote.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Largest (packed, entry) pair of a block; result in every thread.
+template <int THREADS>
+__device__ __forceinline__ void block_max2(unsigned long long &v, uint32_t &e, unsigned long long *sv, uint32_t *se) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+        const unsigned long long ov = __shfl_xor_sync(kFull, v, d);
+        const uint32_t oe = __shfl_xor_sync(kFull, e, d);
+        if (ov > v) {
+            v = ov;
+            e = oe;
+        }
+    }
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    __syncthreads();
+    if (lane == 0) {
+        sv[w] = v;
+        se[w] = e;
+    }
+    __syncthreads();
+    if (w == 0) {
+        v = lane < THREADS / 32 ? sv[lane] : 0ull;
+        e = lane < THREADS / 32 ? se[lane] : kNone;
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+            const unsigned long long ov = __shfl_xor_sync(kFull, v, d);
+            const uint32_t oe = __shfl_xor_sync(kFull, e, d);
+            if (ov > v) {
+                v = ov;
+                e = oe;
+            }
+        }
+        if (lane == 0) {
+            sv[0] = v;
+            se[0] = e;
+        }
+    }
+    __syncthreads();
+    v = sv[0];
+    e = se[0];
+    __syncthreads();
+}
+
+// Exclusive block scan of 32-bit values; *total receives the sum.
+template <int THREADS>
+__device__ __forceinline__ uint32_t block_excl(uint32_t v, uint32_t *sw, uint32_t *total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t incl = warp_incl_sum(v, lane);
+    __syncthreads();
+    if (lane == 31) sw[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        const uint32_t x = lane < THREADS / 32 ? sw[lane] : 0u;
+        const uint32_t xi = warp_incl_sum(x, lane);
+        if (lane < THREADS / 32) sw[lane] = xi - x;
+        if (lane == 31) sw[32] = xi;
+    }
+    __syncthreads();
+    const uint32_t r = sw[w] + incl - v;
+    *total = sw[32];
+    __syncthreads();
+    return r;
+}
+
+// ---------------------------------------------------------- pair count ---
+
+// Add the pairs of one quad of symbols a[0..4) (a[4] = the next symbol, or
+// kWordStart when none) to the 16-bit counters.
+__device__ __forceinline__ void bc_quad(uint32_t *cnt, const uint32_t *a, uint32_t nvalid, uint32_t &bad,
+                                        bool &hot) {
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        if ((uint32_t)i < nvalid) bad |= a[i] & kBadBits;
+        if ((uint32_t)i + 1 <= nvalid && !(a[i + 1] & kWordStart)) {
+            const uint32_t e = ((a[i] & 0xFFu) << 8) | (a[i + 1] & 0xFFu);
+            const uint32_t sh = (e & 1u) << 4;
+            const uint32_t old = atomicAdd(cnt + (e >> 1), 1u << sh);
+            hot |= ((old >> sh) & 0xFFFFu) == kBcLimit;
+        }
+    }
+}
+
+__device__ __forceinline__ void bc_flush(uint32_t *cnt, uint32_t *g) {
+    for (int w = threadIdx.x; w < 32768; w += kBcThreads) {
+        const uint32_t x = cnt[w];
+        if (x) {
+            if (x & 0xFFFFu) atomicAdd(g + 2 * w, x & 0xFFFFu);
+            if (x >> 16) atomicAdd(g + 2 * w + 1, x >> 16);
+            cnt[w] = 0;
+        }
+    }
+}
+
+// Counts of the pairs (i, i+1), i+1 < n, whose right symbol has no
+// WORD_START, by entry (l << 8) | r; LERR_BADINPUT when a symbol is not a
+// byte id (with or without WORD_START).  One CTA per contiguous range of
+// quads; VEC: the input is 16-byte aligned.
+template <bool VEC>
+__global__ void __launch_bounds__(kBcThreads, 1) k_bcount(LP P) {
+    extern __shared__ uint32_t bcnt[];
+    __shared__ int s_hot;
+    const uint64_t n = P.n, nq = n / 4;   // full quads; the tail is done by CTA 0
+    const uint32_t *in = P.in;
+    for (int w = threadIdx.x; w < 32768; w += kBcThreads) bcnt[w] = 0;
+    if (threadIdx.x == 0) s_hot = 0;
+    __syncthreads();
+    const uint64_t per = (nq + gridDim.x - 1) / gridDim.x;
+    const uint64_t q0 = (uint64_t)blockIdx.x * per, q1 = min(nq, q0 + per);
+    uint32_t bad = 0;
+    const int lane = threadIdx.x & 31;
+    constexpr uint64_t kStep = (uint64_t)kBcThreads * kBcQuads;   // quads per CTA step
+    // quad of thread t, slot u in a step: q = base + u * kBcThreads + t (a warp's lanes are consecutive)
+    uint4 cur[kBcQuads], nxt[kBcQuads];
+    uint32_t cnx[kBcQuads], nnx[kBcQuads];
+    auto load = [&](uint64_t base, uint4 *v, uint32_t *nx) {
+#pragma unroll
+        for (int u = 0; u < kBcQuads; u++) {
+            const uint64_t q = base + (uint64_t)u * kBcThreads + threadIdx.x;
+            if (q < q1) {
+                if (VEC) {
+                    v[u] = __ldcs(reinterpret_cast<const uint4 *>(in) + q);
+                } else {
+                    v[u] = make_uint4(in[4 * q], in[4 * q + 1], in[4 * q + 2], in[4 * q + 3]);
+                }
+                // lanes 0..30 take the next quad's first symbol from their neighbour
+                nx[u] = (lane == 31 || q + 1 >= q1) ? (4 * q + 4 < n ? __ldcs(in + 4 * q + 4) : kWordStart) : 0u;
+            } else {
+                v[u] = make_uint4(0, 0, 0, 0);
+                nx[u] = kWordStart;
+            }
+        }
+    };
+    if (q0 < q1) load(q0, cur, cnx);
+    for (uint64_t base = q0; base < q1; base += kStep) {
+        const bool more = base + kStep < q1;
+        if (more) load(base + kStep, nxt, nnx);   // in flight while this step counts
+        bool hot = false;
+#pragma unroll
+        for (int u = 0; u < kBcQuads; u++) {
+            const uint64_t q = base + (uint64_t)u * kBcThreads + threadIdx.x;
+            const uint32_t right = __shfl_down_sync(kFull, cur[u].x, 1);
+            if (q < q1) {
+                const uint32_t a[5] = {cur[u].x, cur[u].y, cur[u].z, cur[u].w,
+                                       (lane == 31 || q + 1 >= q1) ? cnx[u] : right};
+                bc_quad(bcnt, a, 4, bad, hot);
+            }
+        }
+        if (hot) s_hot = 1;
+        __syncthreads();
+        if (s_hot) {   // a counter passed kBcLimit: at most kStep * 4 more adds before the next check
+            bc_flush(bcnt, P.ecnt);
+            __syncthreads();
+            if (threadIdx.x == 0) s_hot = 0;
+            __syncthreads();
+        }
+        if (more) {
+#pragma unroll
+            for (int u = 0; u < kBcQuads; u++) {
+                cur[u] = nxt[u];
+                cnx[u] = nnx[u];
+            }
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {   // the tail after the last full quad
+        for (uint64_t i = 4 * nq; i < n; i++) {
+            const uint32_t s = in[i];
+            bad |= s & kBadBits;
+            if (i + 1 < n && !(in[i + 1] & kWordStart)) {
+                const uint32_t e = ((s & 0xFFu) << 8) | (in[i + 1] & 0xFFu);
+                atomicAdd(bcnt + (e >> 1), 1u << ((e & 1u) << 4));
+            }
+        }
+    }
+    __syncthreads();
+    bc_flush(bcnt, P.ecnt);
+    if (bad) atomicOr(&P.st->err, LERR_BADINPUT);
+}
+
+// ----------------------------------------------------------- list base ---
+
+// One CTA of 1,024 threads over the 65,536 byte-pair entries: keys, list
+// lengths and offsets (exclusive scan of the counts), the argmax of merge 0
+// and the frontier it starts with; byte ids have length 1.
+__global__ void __launch_bounds__(1024) k_lbase(LP P) {
+    __shared__ uint32_t sw[33];
+    __shared__ unsigned long long sv[32];
+    __shared__ uint32_t se[32];
+    __shared__ uint32_t s_fn, s_over;
+    LState *st = P.st;
+    constexpr int kPer = kBaseEntries / 1024;
+    const uint32_t e0 = threadIdx.x * kPer;
+    uint32_t sum = 0;
+    unsigned long long bv = 0;
+    uint32_t be = kNone;
+    for (int j = 0; j < kPer; j++) {
+        const uint32_t e = e0 + j, c = P.ecnt[e];
+        sum += c;
+        if (c) {
+            const unsigned long long v = pack(c, base_key(e));
+            if (v > bv) {
+                bv = v;
+                be = e;
+            }
+        }
+    }
+    uint32_t total;
+    uint32_t off = block_excl<1024>(sum, sw, &total);
+    for (int j = 0; j < kPer; j++) {
+        const uint32_t e = e0 + j, c = P.ecnt[e];
+        P.ekey[e] = base_key(e);
+        P.ellen[e] = c;
+        P.eloff[e] = off;
+        P.bfill[e] = 0;
+        off += c;
+    }
+    for (uint32_t i = threadIdx.x; i < 65536; i += 1024) P.vlen[i] = i < 256 ? 1u : 0u;
+    block_max2<1024>(bv, be, sv, se);
+    // the largest count is the argmax's; the frontier: entries at or above its threshold
+    const unsigned long long cm = bv >> 32;
+    const uint32_t T = max(1u, (uint32_t)((cm * kFfInit) >> 8));
+    if (threadIdx.x == 0) {
+        s_fn = 0;
+        s_over = 0;
+    }
+    __syncthreads();
+    for (int j = 0; j < kPer; j++) {
+        const uint32_t e = e0 + j;
+        if (P.ecnt[e] >= T) {
+            const uint32_t i = atomicAdd(&s_fn, 1u);
+            if (i < P.fcap) P.fr[0][i] = make_uint2(e, base_key(e));
+            else s_over = 1;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        st->D = kBaseEntries;
+        st->occ_top = total;
+        st->cmax = (uint32_t)cm;
+        st->T = T;
+        st->fn = min(s_fn, P.fcap);
+        st->fvalid = s_over ? 0u : 1u;
+        st->fcur = 0;
+        st->ff = kFfInit;
+        P.best[0] = cm ? bv : 0ull;
+        P.ebest[0] = be;
+    }
+}
+
+// ------------------------------------------------------------ list fill ---
+
+// The working stream (input copy), every position's pair entry (kNone when
+// no pair starts there) and the byte-pair lists.  A tile of kBfTile
+// positions ranks its pairs per entry in shared memory, takes one
+// reservation per distinct entry from the global cursor, then writes.
+__global__ void __launch_bounds__(kBfThreads, 1) k_bfill(LP P) {
+    extern __shared__ uint32_t bsm[];
+    uint32_t *cnt = bsm;                                          // 65,536 16-bit counters, later tile slots
+    uint16_t *tkeys = reinterpret_cast<uint16_t *>(bsm + 32768);  // distinct entries of the tile
+    uint32_t *tbase = bsm + 32768 + kBfTile / 2;                  // their first list slot
+    __shared__ uint32_t s_nt;
+    uint16_t *c16 = reinterpret_cast<uint16_t *>(cnt);
+    const uint64_t n = P.n;
+    for (int w = threadIdx.x; w < 32768; w += kBfThreads) cnt[w] = 0;
+    if (threadIdx.x == 0) s_nt = 0;
+    __syncthreads();
+    const uint64_t ntiles = (n + kBfTile - 1) / kBfTile;
+    for (uint64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const uint64_t p0 = t * kBfTile + (uint64_t)threadIdx.x * kBfItems;   // this thread's positions
+        uint32_t a[kBfItems + 1];
+#pragma unroll
+        for (int j = 0; j <= kBfItems; j++) a[j] = (p0 + j < n) ? __ldg(P.in + p0 + j) : kWordStart;
+        uint32_t ent[kBfItems], rank[kBfItems];
+#pragma unroll
+        for (int j = 0; j < kBfItems; j++) {
+            ent[j] = kNone;
+            rank[j] = 0;
+            const uint64_t p = p0 + j;
+            if (p < n) {
+                P.sym[p] = a[j];
+                if (p + 1 < n && !(a[j + 1] & kWordStart)) {
+                    const uint32_t e = ((a[j] & 0xFFu) << 8) | (a[j + 1] & 0xFFu);
+                    const uint32_t sh = (e & 1u) << 4;
+                    const uint32_t old = (atomicAdd(cnt + (e >> 1), 1u << sh) >> sh) & 0xFFFFu;
+                    if (old == 0) {
+                        const uint32_t i = atomicAdd(&s_nt, 1u);
+                        tkeys[i] = (uint16_t)e;
+                    }
+                    ent[j] = e;
+                    rank[j] = old;
+                }
+                P.pe[p] = ent[j];
+            }
+        }
+        __syncthreads();
+        const uint32_t nt = s_nt;
+        for (uint32_t i = threadIdx.x; i < nt; i += kBfThreads) {
+            const uint32_t e = tkeys[i];
+            const uint32_t c = c16[e];
+            tbase[i] = (uint32_t)P.eloff[e] + atomicAdd(P.bfill + e, c);
+        }
+        __syncthreads();
+        for (uint32_t i = threadIdx.x; i < nt; i += kBfThreads) c16[tkeys[i]] = (uint16_t)i;   // entry -> tile slot
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < kBfItems; j++)
+            if (ent[j] != kNone) P.occ[tbase[c16[ent[j]]] + rank[j]] = (uint32_t)(p0 + j);
+        __syncthreads();
+        for (uint32_t i = threadIdx.x; i < nt; i += kBfThreads) c16[tkeys[i]] = 0;
+        if (threadIdx.x == 0) s_nt = 0;
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------- merge ---
+//
+// The merge to run is st->k_cur.  A merge whose list holds at most
+// st->tail_len entries is run by k_ltail (one CTA, phases separated by
+// __syncthreads, many merges per launch); a longer one by k_lscan + k_lapply
+// (every SM), after which k_ltail resumes.  Counts never grow after a pair is
+// created, so late merges are small and the tail takes almost all of them.
+
+// Claim or find key's slot in the per-merge hash (tag = merge + 1).
+__device__ uint32_t hash_slot(const LP &P, uint32_t key, uint32_t tag, uint32_t par) {
+    uint32_t h = fmix32(key) & P.hmask;
+    const unsigned long long want = ((unsigned long long)tag << 32) | key;
+    for (uint32_t probe = 1; probe <= kHashProbes; ++probe) {
+        unsigned long long cur = __ldcg(P.hslot + h);
+        if ((uint32_t)(cur >> 32) != tag) {
+            // left by an earlier merge: free for this one.  Only this merge's
+            // claims write the slot, so a failed claim returns this merge's tag.
+            const unsigned long long old = atomicCAS(P.hslot + h, cur, want);
+            if (old == cur) {
+                const uint32_t i = atomicAdd(&P.st->nns[par], 1u);
+                P.ns[par][i] = h;   // at most P.hmask / 2 + 1 distinct keys per merge: in bounds
+                return h;
+            }
+            cur = old;
+        }
+        if (cur == want) return h;
+        h = (h + probe) & P.hmask;   // the same probe sequence for every thread
+    }
+    atomicOr(&P.st->err, LERR_HASH);
+    return kNone;
+}
+
+struct MergeCtx {
+    uint32_t k, par, tag, l, r, nid, es, vl, vr;
+    uint64_t n;
+    bool last;   // the last merge of the call: its new pairs are never used
+};
+
+__device__ __forceinline__ void merge_ctx(const LP &P, MergeCtx &M, uint32_t k, unsigned long long bw, uint32_t es) {
+    const uint32_t key = ~(uint32_t)bw;
+    M.k = k;
+    M.par = k & 1u;
+    M.tag = k + 1;
+    M.l = key >> 16;
+    M.r = key & 0xFFFFu;
+    M.nid = 256u + k;
+    M.es = es;
+    M.vl = __ldcg(P.vlen + M.l);
+    M.vr = __ldcg(P.vlen + M.r);
+    M.n = P.n;
+    M.last = k + 1 >= P.st->n_merges;
+}
+
+// Where a merge's outputs are staged (shared memory): the left positions of
+// merging occurrences and the new pairs (key, position).  Past the capacity
+// they go straight to the global records (direct) -- only k_lscan allows
+// that; k_ltail's capacities cover a whole merge, anything more is an error.
+struct Stage {
+    uint32_t *app, *rkey, *rpos;
+    uint32_t *na, *nr;
+    uint32_t app_cap, rec_cap;
+    bool direct;
+};
+
+// One merging occurrence's outputs directly to global memory, each new
+// pair's rank taken from its global slot.
+__device__ void emit_direct_app(const LP &P, const MergeCtx &M, uint32_t p) {
+    const uint32_t i = atomicAdd(&P.st->napp[M.par], 1u);
+    if (i < P.app_cap) P.app[M.par][i] = p;
+    else atomicOr(&P.st->err, LERR_RECORDS);
+}
+__device__ void emit_direct_rec(const LP &P, const MergeCtx &M, uint32_t key, uint32_t pos) {
+    const uint32_t h = hash_slot(P, key, M.tag, M.par);
+    if (h == kNone) return;
+    const uint32_t rank = atomicAdd(P.hcnt + h, 1u);
+    const uint32_t i = atomicAdd(&P.st->nrec[M.par], 1u);
+    if (i < P.rec_cap) P.rec[M.par][i] = make_uint4(h, rank, pos, 0u);
+    else atomicOr(&P.st->err, LERR_RECORDS);
+}
+
+__device__ __forceinline__ void emit_app(const LP &P, const MergeCtx &M, const Stage &S, uint32_t p) {
+    const uint32_t i = atomicAdd(S.na, 1u);
+    if (i < S.app_cap) S.app[i] = p;
+    else if (S.direct) emit_direct_app(P, M, p);
+    else atomicOr(&P.st->err, LERR_RECORDS);
+}
+__device__ __forceinline__ void emit_rec(const LP &P, const MergeCtx &M, const Stage &S, uint32_t key, uint32_t pos) {
+    const uint32_t i = atomicAdd(S.nr, 1u);
+    if (i < S.rec_cap) {
+        S.rkey[i] = key;
+        S.rpos[i] = pos;
+    } else if (S.direct) {
+        emit_direct_rec(P, M, key, pos);
+    } else {
+        atomicOr(&P.st->err, LERR_RECORDS);
+    }
+}
+
+// Deltas and outputs of one merging occurrence (p, q): sp is p's symbol, a
+// p's left neighbour (kNone: none) with symbol sa and pair entry ea, pocc
+// whether a is the right half of another merging occurrence (then a2 is
+// that occurrence's left position), b the position after q's token with
+// symbol sb, eq the entry of the pair (q, b), qocc whether b starts another
+// merging occurrence.  The pair (a, p) loses a count and (a or a2, new)
+// forms; the pair (q, b) loses a count and (new, b) forms -- except where
+// two occurrences meet, which the right one of them handles.  The staged
+// record is p with p's WORD_START in bit 31.
+__device__ __forceinline__ void occurrence(const LP &P, const MergeCtx &M, const Stage &S, uint32_t p, uint32_t sp,
+                                           uint32_t a, uint32_t sa, uint32_t ea, bool pocc, uint32_t a2, uint32_t b,
+                                           uint32_t sb, uint32_t eq, bool qocc) {
+    const uint32_t rec = p | ((sp & kWordStart) ? kDead : 0u);
+    if (M.last) {
+        emit_app(P, M, S, rec);
+        return;
+    }
+    if (a != kNone) {
+        if (ea != M.es) atomicSub(P.ecnt + ea, 1u);
+        if (pocc) emit_rec(P, M, S, (M.nid << 16) | M.nid, a2);
+        else emit_rec(P, M, S, (sid(sa) << 16) | M.nid, a);
+    }
+    if (b < M.n && !(sb & kWordStart) && !qocc) {
+        if (eq != M.es) atomicSub(P.ecnt + eq, 1u);
+        emit_rec(P, M, S, (M.nid << 16) | sid(sb), p);
+    }
+    emit_app(P, M, S, rec);
+}
+
+// Whether position x (a live head or n) holds id want, without WORD_START
+// unless ws_ok.
+__device__ __forceinline__ bool holds(const LP &P, uint64_t n, uint32_t x, uint32_t want, bool ws_ok, uint32_t *sx) {
+    if (x >= n) return false;
+    const uint32_t s = __ldcg(P.sym + x);
+    *sx = s;
+    return !(s & kDead) && sid(s) == want && (ws_ok || !(s & kWordStart));
+}
+
+// A list entry p: when it still holds the pair, its deltas and outputs (for
+// l == r, the whole run of valid starts, walked from its first one).  Once
+// sym[p] is known every neighbour position but a dead left one is known too
+// (token lengths come from the ids), so their loads are issued together.
+__device__ void list_entry(const LP &P, const MergeCtx &M, const Stage &S, uint32_t p) {
+    if (p >= M.n) return;
+    const uint32_t sp = __ldcg(P.sym + p);
+    if ((sp & kDead) || sid(sp) != M.l) return;
+    const uint32_t q = p + M.vl, b = q + M.vr;
+    if (q >= M.n) return;
+    const bool left = !(sp & kWordStart) && p > 0;
+    const uint32_t sq = __ldcg(P.sym + q);
+    const uint32_t eq = __ldcg(P.pe + q);                       // used only when (q, b) is a pair
+    const uint32_t sx = left ? __ldcg(P.sym + p - 1) : kDead;   // p's left neighbour, or its last byte
+    const uint32_t ex = left ? __ldcg(P.pe + p - 1) : kNone;
+    const uint32_t sb = b < M.n ? __ldcg(P.sym + b) : kWordStart;
+    if ((sq & kDead) || sid(sq) != M.r || (sq & kWordStart)) return;
+    uint32_t a = kNone, sa = 0, ea = kNone;
+    if (left) {
+        if (!(sx & kDead)) {
+            a = p - 1;
+            sa = sx;
+            ea = ex;
+        } else {
+            a = p - 1 - (sx & kDistMask);
+            sa = __ldcg(P.sym + a);
+            ea = __ldcg(P.pe + a);
+        }
+    }
+    if (M.l != M.r) {
+        bool pocc = false;
+        uint32_t a2 = kNone;
+        if (a != kNone && a > 0 && sid(sa) == M.r && !(sa & kWordStart)) {
+            uint32_t sa2;
+            a2 = prev_live(P.sym, a, &sa2);
+            pocc = sid(sa2) == M.l;
+        }
+        uint32_t sc;
+        const bool qocc = b < M.n && !(sb & kWordStart) && sid(sb) == M.l && holds(P, M.n, b + M.vl, M.r, false, &sc);
+        occurrence(P, M, S, p, sp, a, sa, ea, pocc, a2, b, sb, eq, qocc);
+        return;
+    }
+    // l == r (so vl == vr): only the first valid start of a run proceeds; it
+    // merges (x, x + v), (x + 2v, x + 3v), ... while the next start is valid
+    if (a != kNone && sid(sa) == M.l) return;
+    uint32_t x = p, sxx = sp, la = a, lsa = sa, lea = ea, la2 = kNone;
+    uint32_t z = b, sz = sb, ez = eq;
+    bool first = true;
+    for (;;) {
+        // (x, x + v) merges; z = x + 2v follows it
+        uint32_t sw = kWordStart, sn = kWordStart, en = kNone;
+        bool more = false;
+        if (z < M.n && !(sz & kWordStart) && sid(sz) == M.l && z + M.vl < M.n) {
+            sw = __ldcg(P.sym + z + M.vl);
+            more = !(sw & kDead) && sid(sw) == M.r && !(sw & kWordStart);
+        }
+        if (more && z + M.vl + M.vr < M.n) {
+            sn = __ldcg(P.sym + z + M.vl + M.vr);
+            en = __ldcg(P.pe + z + M.vl);
+        }
+        occurrence(P, M, S, x, sxx, la, lsa, lea, !first, la2, z, sz, ez, more);
+        if (!more) break;
+        la = x + M.vl;   // the next start's left neighbour is this occurrence's right half
+        la2 = x;
+        lsa = 0;
+        lea = M.es;      // the pair there is (l, l): its count is cleared whole
+        first = false;
+        x = z;
+        sxx = sz;
+        z = x + M.vl + M.vr;
+        sz = sn;
+        ez = en;
+    }
+}
+
+// Count decrements of a warp, one atomic per distinct entry: every lane
+// passes its entry (kNone: none) and the lanes holding the same one add up.
+__device__ __forceinline__ void warp_dec(const LP &P, uint32_t e) {
+    const unsigned peers = __match_any_sync(kFull, e);
+    if (e != kNone && (threadIdx.x & 31) == __ffs(peers) - 1) atomicSub(P.ecnt + e, (uint32_t)__popc(peers));
+}
+
+// Staging of a warp: each lane appends n (0..2) values; one shared atomic per
+// warp reserves the slots.  Past the capacity the values go to *over (the
+// caller handles them one by one).
+__device__ __forceinline__ uint32_t warp_reserve(uint32_t *counter, uint32_t n) {
+    const int lane = threadIdx.x & 31;
+    uint32_t incl = warp_incl_sum(n, lane);
+    const uint32_t total = __shfl_sync(kFull, incl, 31);
+    uint32_t base = 0;
+    if (lane == 31 && total) base = atomicAdd(counter, total);
+    base = __shfl_sync(kFull, base, 31);
+    return base + incl - n;
+}
+
+// J list entries per thread (entries x0, x0 + stride, ...), advanced stage by
+// stage so that each stage's loads for all J are in flight together: the
+// entries, their symbols, their neighbours, dead left neighbours, then the
+// rare second-level checks; then per entry slot the count decrements (one
+// atomic per distinct entry and warp) and the staged outputs (one shared
+// reservation per warp).  l == r merges take the one-entry path (their runs
+// are walked in order).  Called by whole warps.
+template <int J>
+__device__ __forceinline__ void list_batch(const LP &P, const MergeCtx &M, const Stage &S, unsigned long long lb,
+                                           uint32_t len, uint32_t x0, uint32_t stride) {
+    // slots of this warp that hold any entry (x0 is lane-consecutive, so the
+    // warp's first lane decides); the others skip every stage
+    const uint32_t w0 = __shfl_sync(kFull, x0, 0);
+    const int jmax = w0 >= len ? 0 : (int)min((uint32_t)J, (len - w0 + stride - 1) / stride);
+    if (jmax == 0) return;
+    uint32_t p[J], sp[J];
+#pragma unroll
+    for (int j = 0; j < J; j++) {
+        const uint32_t x = x0 + j * stride;
+        p[j] = j < jmax && x < len ? __ldcg(P.occ + lb + x) : kNone;
+    }
+    if (M.l == M.r) {
+#pragma unroll
+        for (int j = 0; j < J; j++)
+            if (p[j] != kNone) list_entry(P, M, S, p[j]);
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < J; j++) sp[j] = j < jmax && p[j] < M.n ? __ldcg(P.sym + p[j]) : kDead;
+    uint32_t sq[J], eq[J], sx[J], ex[J], sb[J];
+    bool ok[J], left[J];
+#pragma unroll
+    for (int j = 0; j < J; j++) {
+        ok[j] = !(sp[j] & kDead) && sid(sp[j]) == M.l && p[j] + M.vl < M.n;
+        left[j] = ok[j] && !(sp[j] & kWordStart) && p[j] > 0;
+        const uint32_t q = p[j] + M.vl, b = q + M.vr;
+        sq[j] = ok[j] ? __ldcg(P.sym + q) : kDead;
+        eq[j] = ok[j] ? __ldcg(P.pe + q) : kNone;
+        sx[j] = left[j] ? __ldcg(P.sym + p[j] - 1) : kDead;
+        ex[j] = left[j] ? __ldcg(P.pe + p[j] - 1) : kNone;
+        sb[j] = ok[j] && b < M.n ? __ldcg(P.sym + b) : kWordStart;
+    }
+    uint32_t a[J], sa[J], ea[J];
+#pragma unroll
+    for (int j = 0; j < J; j++) {
+        ok[j] = ok[j] && !(sq[j] & kDead) && sid(sq[j]) == M.r && !(sq[j] & kWordStart);
+        a[j] = kNone;
+        sa[j] = 0;
+        ea[j] = kNone;
+        if (ok[j] && left[j]) {
+            if (!(sx[j] & kDead)) {
+                a[j] = p[j] - 1;
+                sa[j] = sx[j];
+                ea[j] = ex[j];
+            } else {
+                a[j] = p[j] - 1 - (sx[j] & kDistMask);
+                sa[j] = __ldcg(P.sym + a[j]);
+                ea[j] = __ldcg(P.pe + a[j]);
+            }
+        }
+    }
+    // second-level checks, all slots at once: is a the right half of another
+    // occurrence (its left neighbour holds l), does b start one (b + vl holds r)
+    uint32_t a2[J], s2[J], sc[J];
+    bool np[J], nq[J];
+#pragma unroll
+    for (int j = 0; j < J; j++) {
+        const uint32_t b = p[j] + M.vl + M.vr;
+        np[j] = ok[j] && a[j] != kNone && a[j] > 0 && sid(sa[j]) == M.r && !(sa[j] & kWordStart);
+        nq[j] = ok[j] && b < M.n && !(sb[j] & kWordStart) && sid(sb[j]) == M.l && b + M.vl < M.n;
+        a2[j] = np[j] ? a[j] - 1 : kNone;
+        s2[j] = np[j] ? __ldcg(P.sym + a2[j]) : 0u;
+        sc[j] = nq[j] ? __ldcg(P.sym + b + M.vl) : kDead;
+    }
+#pragma unroll
+    for (int j = 0; j < J; j++) {
+        if (np[j] && (s2[j] & kDead)) {
+            a2[j] -= s2[j] & kDistMask;
+            s2[j] = __ldcg(P.sym + a2[j]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < J; j++) {
+        if (j >= jmax || !__ballot_sync(kFull, ok[j])) continue;   // uniform in the warp
+        // this slot's outputs: decrements d1, d2; new pairs (k1, q1), (k2, q2); the record
+        uint32_t d1 = kNone, d2 = kNone, k1 = 0, q1 = kNone, k2 = 0, q2 = kNone;
+        if (ok[j] && !M.last) {
+            const bool pocc = np[j] && sid(s2[j]) == M.l;
+            const bool qocc = nq[j] && !(sc[j] & kDead) && sid(sc[j]) == M.r && !(sc[j] & kWordStart);
+            const uint32_t b = p[j] + M.vl + M.vr;
+            if (a[j] != kNone) {
+                if (ea[j] != M.es) d1 = ea[j];
+                k1 = pocc ? ((M.nid << 16) | M.nid) : ((sid(sa[j]) << 16) | M.nid);
+                q1 = pocc ? a2[j] : a[j];
+            }
+            if (b < M.n && !(sb[j] & kWordStart) && !qocc) {
+                if (eq[j] != M.es) d2 = eq[j];
+                k2 = (M.nid << 16) | sid(sb[j]);
+                q2 = p[j];
+            }
+        }
+        warp_dec(P, d1);
+        warp_dec(P, d2);
+        const uint32_t nrec = (q1 != kNone ? 1u : 0u) + (q2 != kNone ? 1u : 0u);
+        uint32_t ro = warp_reserve(S.nr, nrec);
+        const uint32_t ao = warp_reserve(S.na, ok[j] ? 1u : 0u);
+        if (q1 != kNone) {
+            if (ro < S.rec_cap) {
+                S.rkey[ro] = k1;
+                S.rpos[ro] = q1;
+            } else if (S.direct) {
+                emit_direct_rec(P, M, k1, q1);
+            } else {
+                atomicOr(&P.st->err, LERR_RECORDS);
+            }
+            ++ro;
+        }
+        if (q2 != kNone) {
+            if (ro < S.rec_cap) {
+                S.rkey[ro] = k2;
+                S.rpos[ro] = q2;
+            } else if (S.direct) {
+                emit_direct_rec(P, M, k2, q2);
+            } else {
+                atomicOr(&P.st->err, LERR_RECORDS);
+            }
+        }
+        if (ok[j]) {
+            const uint32_t rec = p[j] | ((sp[j] & kWordStart) ? kDead : 0u);
+            if (ao < S.app_cap) S.app[ao] = rec;
+            else if (S.direct) emit_direct_app(P, M, rec);
+            else atomicOr(&P.st->err, LERR_RECORDS);
+        }
+    }
+}
+
+// list_batch with the fewest slots per thread that covers the avail entries
+// from this round's first one (the stages are unrolled over the slots, so
+// idle slots would still cost issue).
+template <int JMAX>
+__device__ __forceinline__ void list_scan(const LP &P, const MergeCtx &M, const Stage &S, unsigned long long lb,
+                                          uint32_t len, uint32_t x0, uint32_t stride, uint32_t avail) {
+    const uint32_t need = (avail + stride - 1) / stride;
+    if (need <= 1) list_batch<1>(P, M, S, lb, len, x0, stride);
+    else if (need <= 2 || JMAX < 4) list_batch<(JMAX < 2 ? JMAX : 2)>(P, M, S, lb, len, x0, stride);
+    else if (need <= 4 || JMAX < 8) list_batch<(JMAX < 4 ? JMAX : 4)>(P, M, S, lb, len, x0, stride);
+    else list_batch<JMAX>(P, M, S, lb, len, x0, stride);
+}
+
+// Group the staged new pairs by key in a shared hash (lanes with equal keys
+// agree within the warp first): rslot[i] = local slot << 16 | rank among its
+// key (rslot may be rkey itself: each i is read, then written, by one
+// thread).  hkey must hold kNone and hcnt 0 in every slot; the slots taken
+// are listed in used[0 .. *nused).
+template <int THREADS, int HASH>
+__device__ __forceinline__ void group_pairs(const uint32_t *rkey, uint32_t *rslot, uint32_t nr, uint32_t *hkey,
+                                            uint32_t *hcnt, uint16_t *used, uint32_t *nused) {
+    const int lane = threadIdx.x & 31;
+    for (uint32_t i0 = 0; i0 < nr; i0 += THREADS) {
+        const uint32_t i = i0 + threadIdx.x;
+        const bool act = i < nr;
+        const uint32_t k2 = act ? rkey[i] : kNone;
+        const unsigned peers = __match_any_sync(kFull, k2);
+        const int leader = __ffs(peers) - 1;
+        uint32_t ls = 0, lbase = 0;
+        if (act && lane == leader) {
+            uint32_t h = fmix32(k2) & (HASH - 1);
+            // at most HASH distinct keys: triangular probing over a power of
+            // two visits every slot, so a free one is reached within HASH probes
+            for (int probe = 1; probe <= HASH; ++probe) {
+                const uint32_t cur = atomicCAS(hkey + h, kNone, k2);
+                if (cur == kNone) {
+                    const uint32_t u = atomicAdd(nused, 1u);
+                    used[u] = (uint16_t)h;
+                    break;
+                }
+                if (cur == k2) break;
+                h = (h + probe) & (HASH - 1);
+            }
+            ls = h;
+            lbase = atomicAdd(hcnt + h, (uint32_t)__popc(peers));
+        }
+        ls = __shfl_sync(kFull, ls, leader);
+        lbase = __shfl_sync(kFull, lbase, leader);
+        if (act) rslot[i] = (ls << 16) | (lbase + __popc(peers & ((1u << lane) - 1u)));
+    }
+}
+
+// Shared staging of one k_lscan round.
+struct LsShared {
+    uint32_t app[kLsRound];
+    uint32_t rkey[kLsRecCap], rpos[kLsRecCap], rslot[kLsRecCap];
+    uint32_t hkey[kLsHash], hcnt[kLsHash], hglob[kLsHash], hbase[kLsHash];
+    uint16_t used[kLsHash];
+    uint32_t na, nr, nused, abase, rbase;
+    uint32_t last;
+    uint32_t sw[33];
+};
+
+// The merge st->k_cur, when the multi-CTA kernels run it: it exists, has a
+// pair, and its list is too long for the tail.  *bw, *es: its pair and entry.
+__device__ __forceinline__ bool multi_merge(const LP &P, uint32_t *k, unsigned long long *bw, uint32_t *es) {
+    LState *st = P.st;
+    *k = __ldcg(&st->k_cur);
+    if (*k >= st->n_merges || __ldcg(&st->err)) return false;
+    *bw = __ldcg(P.best + *k);
+    if ((*bw >> 32) == 0) return false;
+    *es = __ldcg(P.ebest + *k);
+    return __ldcg(P.ellen + *es) > __ldcg(&st->tail_len);
+}
+
+// The last k_lscan CTA: entries and lists for the merge's new pairs (the
+// ones at or above the frontier threshold join the frontier), the merged
+// pair's count to 0, the new id's length, the counters of the next merge.
+__device__ void lscan_finish(const LP &P, const MergeCtx &M, LsShared &S) {
+    LState *st = P.st;
+    // state written by the other CTAs of this launch: read past L1
+    const uint32_t nns = min(__ldcg(&st->nns[M.par]), P.hmask + 1);
+    const uint32_t D0 = __ldcg(&st->D);
+    unsigned long long top = __ldcg(&st->occ_top);
+    const bool fvalid0 = __ldcg(&st->fvalid) != 0;
+    const uint32_t T = __ldcg(&st->T), fcur = __ldcg(&st->fcur);
+    uint32_t fn = __ldcg(&st->fn);
+    bool fover = false;
+    if (D0 + nns > P.dcap) {
+        if (threadIdx.x == 0) atomicOr(&st->err, LERR_ENTRIES);
+        return;
+    }
+    for (uint32_t c0 = 0; c0 < nns; c0 += kLsThreads) {
+        const uint32_t i = c0 + threadIdx.x;
+        uint32_t h = 0, c = 0, key = 0;
+        if (i < nns) {
+            h = __ldcg(P.ns[M.par] + i);
+            c = __ldcg(P.hcnt + h);
+            key = (uint32_t)__ldcg(P.hslot + h);
+        }
+        uint32_t tot;
+        const uint32_t off = block_excl<kLsThreads>(c, S.sw, &tot);
+        if (i < nns) {
+            const uint32_t e = D0 + i;
+            P.ekey[e] = key;
+            P.ecnt[e] = c;
+            P.ellen[e] = c;
+            P.eloff[e] = top + off;
+            P.hent[h] = e;
+            P.hcnt[h] = 0;
+        }
+        const bool inf = i < nns && fvalid0 && c >= T;
+        uint32_t ftot;
+        const uint32_t fo = block_excl<kLsThreads>(inf ? 1u : 0u, S.sw, &ftot);
+        if (inf && fn + fo < P.fcap) P.fr[fcur][fn + fo] = make_uint2(D0 + i, key);
+        if (fn + ftot > P.fcap) fover = true;
+        fn = min(fn + ftot, P.fcap);
+        top += tot;
+    }
+    if (top > P.occ_cap) {
+        if (threadIdx.x == 0) atomicOr(&st->err, LERR_LISTS);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        st->D = D0 + nns;
+        st->occ_top = top;
+        st->fn = fn;
+        if (fover) st->fvalid = 0;
+        P.ecnt[M.es] = 0;
+        P.vlen[M.nid] = M.vl + M.vr;
+        const uint32_t nx = (M.par ^ 1u);
+        st->ticket[nx] = 0;
+        st->napp[nx] = 0;
+        st->nrec[nx] = 0;
+        st->nns[nx] = 0;
+    }
+}
+
+__global__ void __launch_bounds__(kLsThreads, 2) k_lscan(LP P) {
+    extern __shared__ __align__(16) unsigned char lsm[];
+    LsShared &S = *reinterpret_cast<LsShared *>(lsm);
+    LState *st = P.st;
+    pdl_launch();
+    pdl_wait();
+    uint32_t k, es;
+    unsigned long long bw;
+    if (!multi_merge(P, &k, &bw, &es)) return;
+    MergeCtx M;
+    merge_ctx(P, M, k, bw, es);
+    const Stage G{S.app, S.rkey, S.rpos, &S.na, &S.nr, (uint32_t)kLsRound, (uint32_t)kLsRecCap, true};
+    const uint32_t len = __ldcg(P.ellen + es);
+    const unsigned long long lb = __ldcg(P.eloff + es);
+    const uint32_t nrounds = (len + kLsRound - 1) / kLsRound;
+    if (threadIdx.x == 0) {
+        S.na = 0;
+        S.nr = 0;
+        S.nused = 0;
+    }
+    for (int i = threadIdx.x; i < kLsHash; i += kLsThreads) {
+        S.hkey[i] = kNone;
+        S.hcnt[i] = 0;
+    }
+    __syncthreads();
+    for (uint32_t rd = blockIdx.x; rd < nrounds; rd += gridDim.x) {
+        // 1. the round's list entries (independent chains, kLsItems per thread)
+        list_scan<kLsItems>(P, M, G, lb, len, rd * kLsRound + threadIdx.x, kLsThreads, len - rd * kLsRound);
+        __syncthreads();
+        // 2. new pairs ranked per distinct key in shared memory
+        const uint32_t nr = min(S.nr, (uint32_t)kLsRecCap);
+        group_pairs<kLsThreads, kLsHash>(S.rkey, S.rslot, nr, S.hkey, S.hcnt, S.used, &S.nused);
+        __syncthreads();
+        // 3. one global slot and rank reservation per distinct key
+        const uint32_t nu = S.nused;
+        for (uint32_t u = threadIdx.x; u < nu; u += kLsThreads) {
+            const uint32_t h = S.used[u];
+            const uint32_t g = hash_slot(P, S.hkey[h], M.tag, M.par);
+            S.hglob[h] = g;
+            S.hbase[h] = g == kNone ? 0u : atomicAdd(P.hcnt + g, S.hcnt[h]);
+        }
+        if (threadIdx.x == 0) {
+            const uint32_t na = min(S.na, (uint32_t)kLsRound);
+            S.abase = atomicAdd(&st->napp[M.par], na);
+            S.rbase = atomicAdd(&st->nrec[M.par], nr);
+        }
+        __syncthreads();
+        // 4. write out
+        const uint32_t na = min(S.na, (uint32_t)kLsRound);
+        for (uint32_t i = threadIdx.x; i < na; i += kLsThreads) {
+            const uint32_t o = S.abase + i;
+            if (o < P.app_cap) P.app[M.par][o] = S.app[i];
+            else atomicOr(&st->err, LERR_RECORDS);
+        }
+        for (uint32_t i = threadIdx.x; i < nr; i += kLsThreads) {
+            const uint32_t rs = S.rslot[i], h = rs >> 16;
+            const uint32_t g = S.hglob[h];
+            const uint32_t o = S.rbase + i;
+            if (g != kNone && o < P.rec_cap) P.rec[M.par][o] = make_uint4(g, S.hbase[h] + (rs & 0xFFFFu), S.rpos[i], 0u);
+            else if (g != kNone) atomicOr(&st->err, LERR_RECORDS);
+        }
+        __syncthreads();
+        for (uint32_t u = threadIdx.x; u < nu; u += kLsThreads) {
+            const uint32_t h = S.used[u];
+            S.hkey[h] = kNone;
+            S.hcnt[h] = 0;
+        }
+        if (threadIdx.x == 0) {
+            S.na = 0;
+            S.nr = 0;
+            S.nused = 0;
+        }
+        __syncthreads();
+    }
+    // the last CTA to finish completes the merge
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) S.last = atomicAdd(&st->ticket[M.par], 1u) == gridDim.x - 1 ? 1u : 0u;
+    __syncthreads();
+    if (!S.last) return;
+    __threadfence();
+    lscan_finish(P, M, S);
+}
+
+// One CTA: every entry rescanned into a new frontier (threshold ff / 256 of
+// the count of merge k) and the argmax of merge k + 1.  Counts are read four
+// at a time; a key only for a count that can win or join the frontier.
+// Returns the winner in *bv, *be (every thread).
+template <int THREADS>
+__device__ void rescan(const LP &P, uint32_t k, unsigned long long *sv, uint32_t *se, uint32_t *s_fn,
+                       unsigned long long *out_bv, uint32_t *out_be) {
+    LState *st = P.st;
+    const uint32_t D = __ldcg(&st->D), fnext = __ldcg(&st->fcur) ^ 1u, ff = __ldcg(&st->ff);
+    const uint32_t ck = (uint32_t)(__ldcg(P.best + k) >> 32);
+    const uint32_t T = max(1u, (uint32_t)(((unsigned long long)ck * ff) >> 8));
+    __syncthreads();
+    if (threadIdx.x == 0) *s_fn = 0;
+    __syncthreads();
+    unsigned long long bv = 0;
+    uint32_t be = kNone;
+    const uint32_t D4 = (D + 3) / 4;   // dcap is a multiple of 4: the last load stays in bounds
+#pragma unroll 4
+    for (uint32_t i = threadIdx.x; i < D4; i += THREADS) {
+        const uint4 c4 = __ldcg(reinterpret_cast<const uint4 *>(P.ecnt) + i);
+        const uint32_t cs[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const uint32_t e = 4 * i + j, c = cs[j];
+            if (e >= D || c == 0 || (c < T && c < (uint32_t)(bv >> 32))) continue;
+            const uint32_t key = __ldcg(P.ekey + e);
+            const unsigned long long v = pack(c, key);
+            if (v > bv) {
+                bv = v;
+                be = e;
+            }
+            if (c >= T) {
+                const uint32_t f = atomicAdd(s_fn, 1u);
+                if (f < P.fcap) P.fr[fnext][f] = make_uint2(e, key);
+            }
+        }
+    }
+    block_max2<THREADS>(bv, be, sv, se);
+    if (threadIdx.x == 0) {
+        P.best[k + 1] = bv;
+        P.ebest[k + 1] = be;
+        const uint32_t nf = *s_fn;
+        st->fcur = fnext;
+        st->fn = min(nf, P.fcap);
+        st->fvalid = nf > P.fcap ? 0u : 1u;
+        st->T = T;
+        if (nf > P.fcap) st->ff = (ff + 256u) / 2u;
+        st->rebuilds++;
+    }
+    *out_bv = bv;
+    *out_be = be;
+    __syncthreads();
+}
+
+// Per merge (multi-CTA): new ids, dead marks and back distances; new pairs
+// into their lists; then the next merge's pair: every CTA takes a slice of
+// the frontier, the last one combines the slices' maxima (or, when the
+// frontier cannot decide, rescans every entry) and advances st->k_cur.
+__global__ void __launch_bounds__(kLaThreads) k_lapply(LP P) {
+    __shared__ uint32_t s_last, s_fn;
+    __shared__ unsigned long long sv[32];
+    __shared__ uint32_t se[32];
+    LState *st = P.st;
+    pdl_launch();
+    pdl_wait();
+    uint32_t k, es;
+    unsigned long long bw;
+    if (!multi_merge(P, &k, &bw, &es)) return;
+    const uint32_t key = ~(uint32_t)bw, l = key >> 16, r = key & 0xFFFFu, nid = 256u + k, par = k & 1u;
+    const uint32_t vl = __ldcg(P.vlen + l), vr = __ldcg(P.vlen + r);
+    const uint32_t na = min(__ldcg(&st->napp[par]), P.app_cap), nr = min(__ldcg(&st->nrec[par]), P.rec_cap);
+    const uint32_t stride = gridDim.x * kLaThreads;
+    for (uint32_t i = blockIdx.x * kLaThreads + threadIdx.x; i < na; i += stride) {
+        const uint32_t rc = __ldcg(P.app[par] + i), p = rc & ~kDead;
+        const uint32_t q = p + vl, last = q + vr - 1;
+        P.sym[p] = nid | ((rc & kDead) ? kWordStart : 0u);
+        P.sym[q] = kDead | (q - p);
+        if (last != q) P.sym[last] = kDead | (last - p);
+    }
+    for (uint32_t i = blockIdx.x * kLaThreads + threadIdx.x; i < nr; i += stride) {
+        const uint4 rc = __ldcg(P.rec[par] + i);
+        const uint32_t e = __ldcg(P.hent + rc.x);
+        P.occ[__ldcg(P.eloff + e) + rc.y] = rc.z;
+        P.pe[rc.z] = e;
+    }
+    const bool more = k + 1 < st->n_merges;
+    // the frontier's best (every count of merge k is final)
+    unsigned long long bv = 0;
+    uint32_t be = kNone;
+    if (more) {
+        const uint32_t fn = __ldcg(&st->fn), fcur = __ldcg(&st->fcur);
+        for (uint32_t i = blockIdx.x * kLaThreads + threadIdx.x; i < fn; i += stride) {
+            const uint2 f = __ldcg(P.fr[fcur] + i);
+            const uint32_t c = __ldcg(P.ecnt + f.x);
+            if (c) {
+                const unsigned long long v = pack(c, f.y);
+                if (v > bv) {
+                    bv = v;
+                    be = f.x;
+                }
+            }
+        }
+        block_max2<kLaThreads>(bv, be, sv, se);
+    }
+    if (threadIdx.x == 0) {
+        P.cand[2 * blockIdx.x] = bv;
+        P.cand[2 * blockIdx.x + 1] = be;
+        __threadfence();
+        s_last = atomicAdd(&st->ticket4[par], 1u) == gridDim.x - 1 ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (more) {
+        bv = 0;
+        be = kNone;
+        for (uint32_t b = threadIdx.x; b < gridDim.x; b += kLaThreads) {
+            const unsigned long long v = __ldcg(P.cand + 2 * b);
+            if (v > bv) {
+                bv = v;
+                be = (uint32_t)__ldcg(P.cand + 2 * b + 1);
+            }
+        }
+        block_max2<kLaThreads>(bv, be, sv, se);
+        if (__ldcg(&st->fvalid) && (uint32_t)(bv >> 32) >= __ldcg(&st->T)) {
+            if (threadIdx.x == 0) {
+                P.best[k + 1] = bv;
+                P.ebest[k + 1] = be;
+            }
+        } else {
+            rescan<kLaThreads>(P, k, sv, se, &s_fn, &bv, &be);
+        }
+    }
+    if (threadIdx.x == 0) {
+        st->ticket4[par] = 0;
+        st->multi_merges++;
+        P.kmode[k] = 2;
+        st->k_cur = k + 1;   // every CTA has read k_cur: each took a ticket after it
+    }
+}
+
+// ----------------------------------------------------------------- tail ---
+
+// Shared state of k_ltail: one merge's staging, its new-pair hash, and the
+// loop's copy of the merge state.
+struct TlShared {
+    uint32_t app[kTlList];
+    uint32_t rkey[kTlRecCap], rpos[kTlRecCap];   // rkey becomes the local slot and rank once grouped
+    uint32_t hkey[kTlHash], hcnt[kTlHash], hoff[kTlHash];   // after allocation: hcnt = entry, hoff = list start
+    uint16_t used[kTlHash];
+    uint32_t na, nr, nused, fn_scratch;
+    uint32_t sw[33];
+    unsigned long long sv[32];
+    uint32_t se[32];
+};
+
+// Up to `budget` consecutive merges from st->k_cur in one CTA, while their
+// lists hold at most st->tail_len entries: the same steps as k_lscan +
+// k_lapply, the new pairs grouped in shared memory (no global hash), the
+// phases separated by __syncthreads.
+__global__ void __launch_bounds__(kTlThreads, 1) k_ltail(LP P, uint32_t budget) {
+    extern __shared__ __align__(16) unsigned char tsm[];
+    TlShared &S = *reinterpret_cast<TlShared *>(tsm);
+    LState *st = P.st;
+    pdl_launch();
+    pdl_wait();
+    const uint32_t tail_len = st->tail_len;
+    if (!tail_len || st->err) return;
+    uint32_t k = st->k_cur;
+    const uint32_t n_merges = st->n_merges;
+    uint32_t D = st->D, fn = st->fn, fcur = st->fcur, fvalid = st->fvalid, T = st->T;
+    unsigned long long top = st->occ_top;
+    for (int i = threadIdx.x; i < kTlHash; i += kTlThreads) {
+        S.hkey[i] = kNone;
+        S.hcnt[i] = 0;
+    }
+    if (threadIdx.x == 0) {
+        S.na = 0;
+        S.nr = 0;
+        S.nused = 0;
+    }
+    __syncthreads();
+    uint32_t done = 0;
+    const Stage G{S.app, S.rkey, S.rpos, &S.na, &S.nr, (uint32_t)kTlList, (uint32_t)kTlRecCap, false};
+    unsigned long long bw = k < n_merges ? __ldcg(P.best + k) : 0ull;   // then carried from each argmax
+    uint32_t es = k < n_merges ? __ldcg(P.ebest + k) : kNone;
+    while (done < budget && k < n_merges) {
+        if ((bw >> 32) == 0) break;
+        // the pair's list and both token lengths, loaded together
+        const uint32_t key = ~(uint32_t)bw;
+        const uint32_t len = __ldcg(P.ellen + es);
+        const unsigned long long lb = __ldcg(P.eloff + es);
+        const uint32_t vl = __ldcg(P.vlen + (key >> 16)), vr = __ldcg(P.vlen + (key & 0xFFFFu));
+        if (len > tail_len) break;   // the multi-CTA kernels take it
+        MergeCtx M;
+        M.k = k;
+        M.par = k & 1u;
+        M.tag = k + 1;
+        M.l = key >> 16;
+        M.r = key & 0xFFFFu;
+        M.nid = 256u + k;
+        M.es = es;
+        M.vl = vl;
+        M.vr = vr;
+        M.n = P.n;
+        M.last = k + 1 >= n_merges;
+        // scan: at most kTlList entries, kTlList / kTlThreads independent chains per thread
+        list_scan<kTlList / kTlThreads>(P, M, G, lb, len, threadIdx.x, kTlThreads, len);
+        __syncthreads();
+        const uint32_t nr = min(S.nr, (uint32_t)kTlRecCap), na = min(S.na, (uint32_t)kTlList);
+        group_pairs<kTlThreads, kTlHash>(S.rkey, S.rkey, nr, S.hkey, S.hcnt, S.used, &S.nused);
+        __syncthreads();
+        // entries and lists of the new pairs; the frontier takes those at or above T
+        const uint32_t nu = S.nused;
+        if (D + nu > P.dcap) {
+            if (threadIdx.x == 0) atomicOr(&st->err, LERR_ENTRIES);
+            break;
+        }
+        bool fover = false;
+        for (uint32_t c0 = 0; c0 < nu; c0 += kTlThreads) {
+            const uint32_t u = c0 + threadIdx.x;
+            uint32_t h = 0, c = 0;
+            if (u < nu) {
+                h = S.used[u];
+                c = S.hcnt[h];
+            }
+            // one scan for both: list offsets (high half) and frontier slots (low
+            // half); a tail merge has at most kTlRecCap new pairs, so neither overflows
+            const bool inf = u < nu && fvalid && c >= T;
+            uint32_t tot2;
+            const uint32_t o2 = block_excl<kTlThreads>((c << 16) | (inf ? 1u : 0u), S.sw, &tot2);
+            const uint32_t off = o2 >> 16, fo = o2 & 0xFFFFu, tot = tot2 >> 16, ftot = tot2 & 0xFFFFu;
+            if (u < nu) {
+                const uint32_t e = D + u, key = S.hkey[h];
+                P.ekey[e] = key;
+                P.ecnt[e] = c;
+                P.ellen[e] = c;
+                P.eloff[e] = top + off;
+                S.hcnt[h] = e;
+                S.hoff[h] = (uint32_t)(top + off);
+                if (inf && fn + fo < P.fcap) P.fr[fcur][fn + fo] = make_uint2(e, key);
+            }
+            if (fn + ftot > P.fcap) fover = true;
+            fn = min(fn + ftot, P.fcap);
+            top += tot;
+        }
+        if (fover) fvalid = 0;
+        D += nu;
+        if (top > P.occ_cap) {
+            if (threadIdx.x == 0) atomicOr(&st->err, LERR_LISTS);
+            break;
+        }
+        if (threadIdx.x == 0) {
+            P.ecnt[es] = 0;
+            P.vlen[M.nid] = M.vl + M.vr;
+        }
+        __syncthreads();
+        // apply: new ids, dead marks, back distances; new pairs into their lists
+        for (uint32_t i = threadIdx.x; i < na; i += kTlThreads) {
+            const uint32_t rc = S.app[i], p = rc & ~kDead;
+            const uint32_t q = p + M.vl, last = q + M.vr - 1;
+            P.sym[p] = M.nid | ((rc & kDead) ? kWordStart : 0u);
+            P.sym[q] = kDead | (q - p);
+            if (last != q) P.sym[last] = kDead | (last - p);
+        }
+        for (uint32_t i = threadIdx.x; i < nr; i += kTlThreads) {
+            const uint32_t rs = S.rkey[i], h = rs >> 16, pos = S.rpos[i];
+            P.occ[S.hoff[h] + (rs & 0xFFFFu)] = pos;
+            P.pe[pos] = S.hcnt[h];
+        }
+        __syncthreads();
+        for (uint32_t u = threadIdx.x; u < nu; u += kTlThreads) {
+            const uint32_t h = S.used[u];
+            S.hkey[h] = kNone;
+            S.hcnt[h] = 0;
+        }
+        if (threadIdx.x == 0) {
+            S.na = 0;
+            S.nr = 0;
+            S.nused = 0;
+        }
+        // the next merge's pair from the frontier, or a rescan of every entry
+        if (!M.last) {
+            unsigned long long bv = 0;
+            uint32_t be = kNone;
+            // four frontier entries per step, their loads in flight together
+            for (uint32_t i0 = 0; i0 < fn; i0 += 4 * kTlThreads) {
+                uint2 f[4];
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const uint32_t i = i0 + j * kTlThreads + threadIdx.x;
+                    f[j] = i < fn ? __ldcg(P.fr[fcur] + i) : make_uint2(kNone, 0u);
+                }
+                uint32_t c[4];
+#pragma unroll
+                for (int j = 0; j < 4; j++) c[j] = f[j].x != kNone ? __ldcg(P.ecnt + f[j].x) : 0u;
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    if (c[j]) {
+                        const unsigned long long v = pack(c[j], f[j].y);
+                        if (v > bv) {
+                            bv = v;
+                            be = f[j].x;
+                        }
+                    }
+                }
+            }
+            block_max2<kTlThreads>(bv, be, S.sv, S.se);
+            if (fvalid && (uint32_t)(bv >> 32) >= T) {
+                if (threadIdx.x == 0) {
+                    P.best[k + 1] = bv;
+                    P.ebest[k + 1] = be;
+                }
+            } else {
+                // the rescan works on the global state: hand over the loop's copy first
+                if (threadIdx.x == 0) {
+                    st->D = D;
+                    st->fn = fn;
+                    st->fcur = fcur;
+                    st->fvalid = fvalid;
+                    st->T = T;
+                }
+                __syncthreads();
+                rescan<kTlThreads>(P, k, S.sv, S.se, &S.fn_scratch, &bv, &be);
+                fn = __ldcg(&st->fn);
+                fcur = __ldcg(&st->fcur);
+                fvalid = __ldcg(&st->fvalid);
+                T = __ldcg(&st->T);
+            }
+            bw = bv;
+            es = be;
+        }
+        if (threadIdx.x == 0) P.kmode[k] = 1;
+        __syncthreads();
+        ++k;
+        ++done;
+    }
+    if (threadIdx.x == 0 && done) {
+        st->k_cur = k;
+        st->D = D;
+        st->occ_top = top;
+        st->fn = fn;
+        st->fcur = fcur;
+        st->fvalid = fvalid;
+        st->T = T;
+        st->tail_merges += done;
+        for (int x = 0; x < 2; x++) {   // the multi-CTA kernels' counters start clean
+            st->ticket[x] = 0;
+            st->ticket4[x] = 0;
+            st->napp[x] = 0;
+            st->nrec[x] = 0;
+            st->nns[x] = 0;
+        }
+    }
+}
+
+// ----------------------------------------------------------- compaction ---
+
+// The live symbols (bit 31 clear) in position order ([GPU-BPE] "What it
+// does" 3.: warp-level exclusive scans and decoupled look-back across CTAs).
+// A tile of kCpTile positions is read with coalesced 128-bit loads (warp w,
+// load j, lane L: positions 1024w + 128j + 4L .. +3); the live counts are
+// scanned per load with __shfl_up_sync and across warps in shared memory; the
+// tile's output offset comes from a warp-wide look-back over 32 predecessor
+// tiles per round trip (ticket order, bounded waits); survivors are staged
+// in shared memory in order and written out coalesced.
+__global__ void __launch_bounds__(kCpThreads) k_lcompact(LP P, uint32_t *out) {
+    constexpr int kLoads = kCpItems / 4;
+    __shared__ uint32_t s_tile, s_off, s_n;
+    __shared__ uint32_t s_warp[kCpThreads / 32 + 1];
+    __shared__ __align__(16) uint32_t stage[kCpTile];
+    LState *st = P.st;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (threadIdx.x == 0) s_tile = atomicAdd(&st->cp_ticket, 1u);
+    __syncthreads();
+    const uint32_t t = s_tile;
+    const uint64_t n = P.n, wbase = (uint64_t)t * kCpTile + (uint64_t)w * (kCpTile / (kCpThreads / 32));
+    uint4 v[kLoads];
+    uint32_t cnt[kLoads];
+#pragma unroll
+    for (int j = 0; j < kLoads; j++) {
+        const uint64_t p = wbase + 128u * j + 4u * lane;
+        if (p + 4 <= n) {
+            v[j] = __ldcs(reinterpret_cast<const uint4 *>(P.sym + p));
+        } else {
+            v[j].x = p < n ? P.sym[p] : kDead;
+            v[j].y = p + 1 < n ? P.sym[p + 1] : kDead;
+            v[j].z = p + 2 < n ? P.sym[p + 2] : kDead;
+            v[j].w = p + 3 < n ? P.sym[p + 3] : kDead;
+        }
+        cnt[j] = ((v[j].x & kDead) ? 0u : 1u) + ((v[j].y & kDead) ? 0u : 1u) + ((v[j].z & kDead) ? 0u : 1u) +
+                 ((v[j].w & kDead) ? 0u : 1u);
+    }
+    // offsets inside the warp, in position order (load, lane, item)
+    uint32_t off[kLoads], run = 0;
+#pragma unroll
+    for (int j = 0; j < kLoads; j++) {
+        const uint32_t incl = warp_incl_sum(cnt[j], lane);
+        off[j] = run + incl - cnt[j];
+        run += __shfl_sync(kFull, incl, 31);
+    }
+    if (lane == 0) s_warp[w] = run;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t a = 0;
+        for (int i = 0; i < kCpThreads / 32; i++) {
+            const uint32_t x = s_warp[i];
+            s_warp[i] = a;
+            a += x;
+        }
+        s_warp[kCpThreads / 32] = a;
+    }
+    __syncthreads();
+    const uint32_t total = s_warp[kCpThreads / 32];
+    // the tile's offset: status word flag << 62 | value (1: the tile's count, 2: inclusive prefix)
+    unsigned long long *cs = P.cstat;
+    if (w == 0) {
+        uint32_t excl = 0;
+        if (t == 0) {
+            if (lane == 0) st_relaxed(cs, (2ull << 62) | total);
+        } else {
+            if (lane == 0) st_relaxed(cs + t, (1ull << 62) | total);
+            int64_t j = (int64_t)t - 1;
+            unsigned spins = 0;
+            for (;;) {
+                const int64_t idx = j - lane;
+                const unsigned long long x = idx >= 0 ? ld_relaxed(cs + idx) : (2ull << 62);
+                const uint32_t f = (uint32_t)(x >> 62);
+                const unsigned pm = __ballot_sync(kFull, f == 2), zm = __ballot_sync(kFull, f == 0);
+                const int fp = pm ? __ffs(pm) - 1 : 32;   // nearest predecessor with its prefix
+                const unsigned need = fp == 32 ? kFull : (fp == 31 ? kFull : ((2u << fp) - 1u));
+                if (zm & need) {
+                    if (++spins > kSpinLimit) {
+                        if (lane == 0) atomicOr(&st->err, DERR_TIMEOUT);
+                        break;
+                    }
+                    continue;
+                }
+                uint32_t val = lane <= fp ? (uint32_t)(x & 0xFFFFFFFFull) : 0u;
+#pragma unroll
+                for (int d = 16; d > 0; d >>= 1) val += __shfl_xor_sync(kFull, val, d);
+                excl += val;
+                if (fp < 32) break;
+                j -= 32;
+            }
+            if (lane == 0) st_relaxed(cs + t, (2ull << 62) | (unsigned long long)(excl + total));
+        }
+        if (lane == 0) {
+            s_off = excl;
+            s_n = total;
+        }
+    }
+    // survivors into the stage, in order
+    const uint32_t wo = s_warp[w];
+#pragma unroll
+    for (int j = 0; j < kLoads; j++) {
+        uint32_t o = wo + off[j];
+        if (!(v[j].x & kDead)) stage[o++] = v[j].x;
+        if (!(v[j].y & kDead)) stage[o++] = v[j].y;
+        if (!(v[j].z & kDead)) stage[o++] = v[j].z;
+        if (!(v[j].w & kDead)) stage[o++] = v[j].w;
+    }
+    __syncthreads();
+    const uint32_t base = s_off, cnt_all = s_n;
+    for (uint32_t i = threadIdx.x; i < cnt_all; i += kCpThreads) out[(uint64_t)base + i] = stage[i];
+    if (t == gridDim.x - 1 && threadIdx.x == 0) st->live = (unsigned long long)base + cnt_all;
+}
+
+// ---------------------------------------------------------------- host ---
+
+struct LBuffers {
+    LP p;
+    unsigned scan_grid, apply_grid;
+};
+
+// Launch with programmatic dependent launch allowed (pdl): the kernel may be
+// scheduled while the one before it runs; it waits for it in griddepcontrol.
+template <typename... Args>
+cudaError_t launch(void (*kern)(Args...), unsigned grid, unsigned block, size_t smem, cudaStream_t s, bool pdl,
+                   Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? at : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// One slot: the tail from st->k_cur, then the multi-CTA pair for a merge the
+// tail left (each returns at once when it has nothing to do).  Each kernel
+// overlaps its launch with the one before (pdl) except the first of a
+// window; profiled slots record an event after each kernel instead (under
+// stream capture an external record becomes an event node of the graph).
+void launch_slot(const LBuffers &B, cudaStream_t s, const cudaEvent_t *ev, bool first) {
+    const bool pdl = !ev;
+    launch(k_ltail, 1, kTlThreads, sizeof(TlShared), s, pdl && !first, B.p, kTlBudget);
+    if (ev) cudaEventRecordWithFlags(ev[0], s, cudaEventRecordExternal);
+    launch(k_lscan, B.scan_grid, kLsThreads, sizeof(LsShared), s, pdl, B.p);
+    if (ev) cudaEventRecordWithFlags(ev[1], s, cudaEventRecordExternal);
+    launch(k_lapply, B.apply_grid, kLaThreads, 0, s, pdl, B.p);
+    if (ev) cudaEventRecordWithFlags(ev[2], s, cudaEventRecordExternal);
+}
+
+// Capture (or reuse) the graph of kSlots slots; with events (profiling), an
+// event before the first kernel and after every kernel.
+int get_graph(bpe_ctx *ctx, const LBuffers &B, const cudaEvent_t *ev, cudaGraphExec_t *out) {
+    std::vector<uintptr_t> key = {
+        3u, (uintptr_t)B.p.sym, (uintptr_t)B.p.pe, (uintptr_t)B.p.occ, (uintptr_t)B.p.occ_cap, (uintptr_t)B.p.ekey,
+        (uintptr_t)B.p.ecnt, (uintptr_t)B.p.ellen, (uintptr_t)B.p.eloff, (uintptr_t)B.p.dcap, (uintptr_t)B.p.vlen,
+        (uintptr_t)B.p.best, (uintptr_t)B.p.ebest, (uintptr_t)B.p.fr[0], (uintptr_t)B.p.fr[1], (uintptr_t)B.p.fcap,
+        (uintptr_t)B.p.hslot, (uintptr_t)B.p.hcnt, (uintptr_t)B.p.hent, (uintptr_t)B.p.hmask, (uintptr_t)B.p.ns[0],
+        (uintptr_t)B.p.ns[1], (uintptr_t)B.p.app[0], (uintptr_t)B.p.app[1], (uintptr_t)B.p.rec[0],
+        (uintptr_t)B.p.rec[1], (uintptr_t)B.p.app_cap, (uintptr_t)B.p.rec_cap, (uintptr_t)B.p.cand,
+        (uintptr_t)B.p.st, (uintptr_t)B.p.n, (uintptr_t)B.p.kmode, (uintptr_t)B.scan_grid, (uintptr_t)B.apply_grid,
+        (uintptr_t)(ev ? ev[0] : nullptr)};
+    TrainGraph &G = ctx->graph_lists;
+    if (G.exec && G.key == key) {
+        *out = G.exec;
+        return BPE_OK;
+    }
+    if (G.exec) {
+        cudaGraphExecDestroy(G.exec);
+        G.exec = nullptr;
+    }
+    cudaStream_t cs = ctx->capture_stream;
+    BPE_CUDA(ctx, cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal), "begin capture");
+    if (ev) cudaEventRecordWithFlags(ev[0], cs, cudaEventRecordExternal);
+    for (int i = 0; i < kSlots; i++) launch_slot(B, cs, ev ? ev + 1 + 3 * i : nullptr, i == 0);
+    cudaGraph_t g = nullptr;
+    cudaError_t e = cudaStreamEndCapture(cs, &g);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "end capture");
+    e = cudaGraphInstantiate(&G.exec, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "graph instantiate");
+    G.key = key;
+    *out = G.exec;
+    return BPE_OK;
+}
+
+uint64_t align_up(uint64_t x) { return (x + 255) & ~uint64_t(255); }
+
+}  // namespace
+
+int train_lists(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_merges, bpe_merge *h_merges_out,
+                uint32_t *n_done, uint32_t *d_symbols_final, uint64_t *n_final, bool *not_bytes) {
+    *not_bytes = false;
+    cudaStream_t s = ctx->stream;
+    const bool profile = ctx->profile != 0;
+    const bool graph = ctx->use_graph || profile;   // profiling times the graph's kernels with event nodes
+    int rc;
+    // ---- state, counts, entries, lists, stream
+    const uint32_t fcap = ctx->list_frontier ? (uint32_t)ctx->list_frontier : 8192u;
+    const uint32_t tail_len = ctx->list_tail < 0 ? (uint32_t)kTlList : std::min<uint32_t>(ctx->list_tail, kTlList);
+    const uint32_t hbits = 18;   // per-merge hash: <= 2 * 65,536 + 1 distinct new pairs, at most half full
+    const uint64_t dcap = (uint64_t)kBaseEntries + (1u << 17) + 64ull * n_merges;
+    const uint64_t occ_cap = 3 * n + 16;   // byte pairs (< n) + two new pairs per merged occurrence (< n in all)
+    void *state, *sym, *pe, *occ, *ekey, *ecnt, *ellen, *eloff, *vlen, *bfill, *best, *ebest, *fr, *hslot, *hcnt,
+        *hent, *ns, *cand, *kmode;
+    const unsigned scan_grid = (unsigned)ctx->sm_count * 2, apply_grid = (unsigned)ctx->sm_count * 2;
+    if ((rc = ensure(ctx, S_L_STATE, sizeof(LState), &state)) || (rc = ensure(ctx, S_TRAIN_BUF0, n * 4 + 64, &sym)) ||
+        (rc = ensure(ctx, S_TRAIN_BUF1, n * 4 + 64, &pe)) || (rc = ensure(ctx, S_L_OCC, occ_cap * 4, &occ)) ||
+        (rc = ensure(ctx, S_L_EKEY, dcap * 4, &ekey)) || (rc = ensure(ctx, S_L_ECNT, dcap * 4, &ecnt)) ||
+        (rc = ensure(ctx, S_L_ELEN, dcap * 4, &ellen)) || (rc = ensure(ctx, S_L_EOFF, dcap * 8, &eloff)) ||
+        (rc = ensure(ctx, S_L_VLEN, 65536 * 4, &vlen)) || (rc = ensure(ctx, S_L_BFILL, 65536 * 4, &bfill)) ||
+        (rc = ensure(ctx, S_BEST, ((uint64_t)n_merges + 1) * 8, &best)) ||
+        (rc = ensure(ctx, S_L_EBEST, ((uint64_t)n_merges + 1) * 4, &ebest)) ||
+        (rc = ensure(ctx, S_L_FRONT, 2ull * fcap * 8, &fr)) ||
+        (rc = ensure(ctx, S_L_HSLOT, (8ull << hbits), &hslot)) || (rc = ensure(ctx, S_L_HCNT, (4ull << hbits), &hcnt)) ||
+        (rc = ensure(ctx, S_L_HENT, (4ull << hbits), &hent)) || (rc = ensure(ctx, S_L_NS, 2ull * (4ull << hbits), &ns)) ||
+        (rc = ensure(ctx, S_L_CAND, 16ull * apply_grid, &cand)) || (rc = ensure(ctx, S_L_KMODE, n_merges + 16, &kmode)))
+        return rc;
+    void *pin;
+    const size_t pin_bytes = (kInFlight + 2) * sizeof(LState) + ((uint64_t)n_merges + 1) * 8 + n_merges + 16;
+    if ((rc = ensure_pinned(ctx, pin_bytes, &pin))) return rc;
+    LState *h_state = (LState *)pin;
+    LState *h_poll = h_state + 1;
+    unsigned long long *h_best = (unsigned long long *)(h_poll + kInFlight);
+    uint8_t *h_kmode = (uint8_t *)(h_best + n_merges + 1);
+    BPE_CUDA(ctx, cudaStreamSynchronize(s), "train: stream sync");
+    memset(h_state, 0, sizeof *h_state);
+    h_state->n_merges = n_merges;
+    h_state->tail_len = tail_len;
+    BPE_CUDA(ctx, cudaMemcpyAsync(state, h_state, sizeof *h_state, cudaMemcpyHostToDevice, s), "state upload");
+    BPE_CUDA(ctx, cudaMemsetAsync(ecnt, 0, kBaseEntries * 4, s), "count clear");
+    BPE_CUDA(ctx, cudaMemsetAsync(best, 0, ((uint64_t)n_merges + 1) * 8, s), "best clear");
+    BPE_CUDA(ctx, cudaMemsetAsync(kmode, 0, n_merges + 16, s), "mode clear");
+    BPE_CUDA(ctx, cudaMemsetAsync(hslot, 0, 8ull << hbits, s), "hash clear");
+    BPE_CUDA(ctx, cudaMemsetAsync(hcnt, 0, 4ull << hbits, s), "hash count clear");
+
+    LBuffers B;
+    LP &P = B.p;
+    memset(&P, 0, sizeof P);
+    P.in = d_symbols;
+    P.n = n;
+    P.sym = (uint32_t *)sym;
+    P.pe = (uint32_t *)pe;
+    P.occ = (uint32_t *)occ;
+    P.occ_cap = occ_cap;
+    P.ekey = (uint32_t *)ekey;
+    P.ecnt = (uint32_t *)ecnt;
+    P.ellen = (uint32_t *)ellen;
+    P.eloff = (unsigned long long *)eloff;
+    P.dcap = (uint32_t)dcap;
+    P.vlen = (uint32_t *)vlen;
+    P.bfill = (uint32_t *)bfill;
+    P.best = (unsigned long long *)best;
+    P.ebest = (uint32_t *)ebest;
+    P.fr[0] = (uint2 *)fr;
+    P.fr[1] = (uint2 *)fr + fcap;
+    P.fcap = fcap;
+    P.hslot = (unsigned long long *)hslot;
+    P.hcnt = (uint32_t *)hcnt;
+    P.hent = (uint32_t *)hent;
+    P.hmask = (1u << hbits) - 1;
+    P.ns[0] = (uint32_t *)ns;
+    P.ns[1] = (uint32_t *)ns + (1u << hbits);
+    P.cand = (unsigned long long *)cand;
+    P.kmode = (uint8_t *)kmode;
+    P.st = (LState *)state;
+    B.scan_grid = scan_grid;
+    B.apply_grid = apply_grid;
+
+    // ---- events: 0 before the count, 1 after it, 2 after the fill, 3 and 4
+    // around the compaction; then 1 + 3 * kSlots for the profiled graph
+    constexpr size_t kFixedEv = 5, kSlotEv = 1 + 3 * kSlots;
+    if ((rc = ensure_events(ctx, kFixedEv + kSlotEv + kInFlight))) return rc;
+    const cudaEvent_t *slot_ev = profile ? &ctx->events[kFixedEv] : nullptr;
+    std::vector<cudaEvent_t> poll_ev(kInFlight);
+    for (int i = 0; i < kInFlight; i++) poll_ev[i] = ctx->events[kFixedEv + kSlotEv + i];
+    auto ev = [&](size_t i) {
+        if (profile) cudaEventRecord(ctx->events[i], s);
+    };
+
+    // ---- pair counts and the base entries
+    BPE_CUDA(ctx, cudaFuncSetAttribute(k_bcount<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBcSmem),
+             "k_bcount smem attribute");
+    BPE_CUDA(ctx, cudaFuncSetAttribute(k_bcount<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBcSmem),
+             "k_bcount smem attribute");
+    BPE_CUDA(ctx, cudaFuncSetAttribute(k_bfill, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBfSmem),
+             "k_bfill smem attribute");
+    BPE_CUDA(ctx, cudaFuncSetAttribute(k_lscan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(LsShared)),
+             "k_lscan smem attribute");
+    BPE_CUDA(ctx, cudaFuncSetAttribute(k_ltail, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(TlShared)),
+             "k_ltail smem attribute");
+    // one shared-memory carveout for the three kernels of the loop, so the
+    // SMs need not be reconfigured between them
+    BPE_CUDA(ctx, cudaFuncSetAttribute(k_ltail, cudaFuncAttributePreferredSharedMemoryCarveout, 100), "carveout");
+    BPE_CUDA(ctx, cudaFuncSetAttribute(k_lscan, cudaFuncAttributePreferredSharedMemoryCarveout, 100), "carveout");
+    BPE_CUDA(ctx, cudaFuncSetAttribute(k_lapply, cudaFuncAttributePreferredSharedMemoryCarveout, 100), "carveout");
+    const uint64_t nq = n / 4;
+    const unsigned bc_grid =
+        (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(ctx->sm_count, (nq + 4095) / 4096));
+    ev(0);
+    if (((uintptr_t)d_symbols & 15) == 0) k_bcount<true><<<bc_grid, kBcThreads, kBcSmem, s>>>(P);
+    else k_bcount<false><<<bc_grid, kBcThreads, kBcSmem, s>>>(P);
+    ev(1);
+    k_lbase<<<1, 1024, 0, s>>>(P);
+    BPE_CUDA(ctx, cudaGetLastError(), "count launch");
+    BPE_CUDA(ctx, cudaMemcpyAsync(h_state, state, sizeof *h_state, cudaMemcpyDeviceToHost, s), "state read");
+    BPE_CUDA(ctx, cudaStreamSynchronize(s), "count sync");
+    if (h_state->err & LERR_BADINPUT) {
+        *not_bytes = true;
+        return BPE_OK;
+    }
+    // merge records: a merge's occurrences never exceed the largest input count
+    const uint64_t cmax = std::max<uint64_t>(h_state->cmax, 1);
+    void *app, *rec;
+    if ((rc = ensure(ctx, S_L_APP, 2 * align_up(cmax * 4), &app)) ||
+        (rc = ensure(ctx, S_L_REC, 2 * align_up(2 * cmax * 16), &rec)))
+        return rc;
+    P.app[0] = (uint32_t *)app;
+    P.app[1] = (uint32_t *)((char *)app + align_up(cmax * 4));
+    P.rec[0] = (uint4 *)rec;
+    P.rec[1] = (uint4 *)((char *)rec + align_up(2 * cmax * 16));
+    P.app_cap = (uint32_t)cmax;
+    P.rec_cap = (uint32_t)(2 * cmax);
+    const unsigned bf_grid = (unsigned)std::max<uint64_t>(
+        1, std::min<uint64_t>(ctx->sm_count, (n + kBfTile - 1) / kBfTile));
+    k_bfill<<<bf_grid, kBfThreads, kBfSmem, s>>>(P);
+    BPE_CUDA(ctx, cudaGetLastError(), "fill launch");
+    ev(2);
+
+    // ---- the merge loop: graph windows of kSlots slots (or host launches),
+    // polled kInFlight windows behind; every slot completes at least one merge
+    // until the loop ends, so a poll without progress is an internal error
+    cudaGraphExec_t exec = nullptr;
+    if (graph && (rc = get_graph(ctx, B, slot_ev, &exec))) return rc;
+    uint64_t window = 0;
+    double ms_tail = 0, ms_scan = 0, ms_apply = 0;
+    uint32_t last_k = 0xFFFFFFFFu;
+    for (;;) {
+        if (window >= (uint64_t)kInFlight) {   // the state after the window launched kInFlight ago
+            const int slot = (int)(window % kInFlight);
+            BPE_CUDA(ctx, cudaEventSynchronize(poll_ev[slot]), "poll sync");
+            const LState &h = h_poll[slot];
+            if (h.err || h.k_cur >= n_merges) break;
+            if (h.k_cur == last_k) break;   // a whole window without a merge: a count of 0 stopped training
+            last_k = h.k_cur;
+        }
+        if (graph) {
+            BPE_CUDA(ctx, cudaGraphLaunch(exec, s), "graph launch");
+        } else {
+            for (int i = 0; i < kSlots; i++) launch_slot(B, s, nullptr, i == 0);
+        }
+        BPE_CUDA(ctx, cudaGetLastError(), "train launch");
+        const int slot = (int)(window % kInFlight);
+        BPE_CUDA(ctx, cudaMemcpyAsync(h_poll + slot, state, sizeof(LState), cudaMemcpyDeviceToHost, s), "poll copy");
+        BPE_CUDA(ctx, cudaEventRecord(poll_ev[slot], s), "poll event");
+        if (profile) {   // this window's kernel times (event nodes of the graph)
+            BPE_CUDA(ctx, cudaEventSynchronize(poll_ev[slot]), "profile sync");
+            for (int i = 0; i < kSlots; i++) {
+                float a = 0, b = 0, c = 0;
+                const cudaEvent_t *e3 = slot_ev + 1 + 3 * i;
+                cudaEventElapsedTime(&a, i ? slot_ev[3 * i] : slot_ev[0], e3[0]);
+                cudaEventElapsedTime(&b, e3[0], e3[1]);
+                cudaEventElapsedTime(&c, e3[1], e3[2]);
+                ms_tail += a;
+                ms_scan += b;
+                ms_apply += c;
+            }
+            cudaGetLastError();
+        }
+        window++;
+        if (window > (uint64_t)n_merges + 2 * kInFlight + 2) break;   // at least one merge per window until the end
+    }
+    BPE_CUDA(ctx, cudaMemcpyAsync(h_state, state, sizeof *h_state, cudaMemcpyDeviceToHost, s), "state read");
+    BPE_CUDA(ctx, cudaMemcpyAsync(h_best, best, (uint64_t)n_merges * 8, cudaMemcpyDeviceToHost, s), "best read");
+    BPE_CUDA(ctx, cudaMemcpyAsync(h_kmode, kmode, n_merges, cudaMemcpyDeviceToHost, s), "mode read");
+    BPE_CUDA(ctx, cudaStreamSynchronize(s), "train sync");
+    if (h_state->err & (LERR_ENTRIES | LERR_LISTS | LERR_HASH | LERR_RECORDS | DERR_OOB))
+        return fail(ctx, BPE_ERR_CHECKED_OOB, "bpe_train: occurrence-list capacity exceeded (error bits 0x%x)",
+                    h_state->err);
+    uint32_t done = 0;
+    while (done < n_merges && (h_best[done] >> 32) != 0) done++;
+    if (h_state->k_cur != done)
+        return fail(ctx, BPE_ERR_CHECKED_OOB, "bpe_train: the merge loop stopped at merge %u of %u", h_state->k_cur,
+                    done);
+    for (uint32_t k = 0; k < done; k++) {
+        const uint32_t key = ~(uint32_t)h_best[k];
+        h_merges_out[k].left = key >> 16;
+        h_merges_out[k].right = key & 0xFFFFu;
+        h_merges_out[k].new_id = 256u + k;
+        h_merges_out[k].count = (uint32_t)(h_best[k] >> 32);
+    }
+    *n_done = done;
+    // ---- the final stream
+    uint64_t nf = n;
+    void *cst = nullptr;
+    const uint64_t ntiles = (n + kCpTile - 1) / kCpTile;
+    if (d_symbols_final || n_final) {
+        if ((rc = ensure(ctx, S_L_CSTAT, ntiles * 8, &cst))) return rc;
+        P.cstat = (unsigned long long *)cst;
+        BPE_CUDA(ctx, cudaMemsetAsync(cst, 0, ntiles * 8, s), "status clear");
+        BPE_CUDA(ctx, cudaMemsetAsync(&P.st->cp_ticket, 0, 4, s), "ticket clear");
+        uint32_t *out = d_symbols_final ? d_symbols_final : P.pe;   // length only: the pair entries are done with
+        ev(3);
+        k_lcompact<<<(unsigned)ntiles, kCpThreads, 0, s>>>(P, out);
+        BPE_CUDA(ctx, cudaGetLastError(), "compaction launch");
+        ev(4);
+        BPE_CUDA(ctx, cudaMemcpyAsync(h_state, state, sizeof *h_state, cudaMemcpyDeviceToHost, s), "state read");
+        BPE_CUDA(ctx, cudaStreamSynchronize(s), "final sync");
+        if (h_state->err & DERR_TIMEOUT) return fail(ctx, BPE_ERR_TIMEOUT, "bpe_train: a look-back wait gave up");
+        nf = h_state->live;
+    }
+    if (n_final) *n_final = nf;
+
+    // ---- statistics: algorithmic bytes per kernel family (per merged
+    // occurrence: the scan reads its list entry, its two symbols, both
+    // neighbours and their pair entries and stages three outputs; the apply
+    // rewrites three symbol words and files two new pairs) and, profiled,
+    // device time between the event nodes around each kernel
+    stats_reset(ctx);
+    const int sc = stats_slot(ctx, "pair_count"), sb = stats_slot(ctx, "list_build"),
+              st_ = stats_slot(ctx, "merge_tail"), ss = stats_slot(ctx, "merge_scan"),
+              sa = stats_slot(ctx, "merge_apply"), sp = stats_slot(ctx, "compact");
+    ctx->stats.kernel_launches = 3 + window * 3 * kSlots + ((d_symbols_final || n_final) ? 1 : 0);
+    ctx->stats.k[sc].launches = 1;
+    ctx->stats.k[sc].bytes = 4.0 * (double)n;
+    ctx->stats.k[sb].launches = 2;
+    ctx->stats.k[sb].bytes = 16.0 * (double)n;   // read the input, write the stream, pair entries and lists
+    // launches of the merge families: the merges each ran (their kernels are
+    // launched once per slot, and return at once when the merge is not theirs)
+    for (uint32_t k = 0; k < done; k++) {
+        const double c = (double)(uint32_t)(h_best[k] >> 32);
+        ctx->stats.k[h_kmode[k] == 1 ? st_ : ss].launches++;
+        if (h_kmode[k] != 1) ctx->stats.k[sa].launches++;
+        if (h_kmode[k] == 1) {
+            ctx->stats.k[st_].bytes += c * (4 + 24 + 12 + 12 + 32);
+        } else {
+            ctx->stats.k[ss].bytes += c * (4 + 24 + 4 + 32);
+            ctx->stats.k[sa].bytes += c * (12 + 32 + 16);
+        }
+    }
+    if (d_symbols_final || n_final) {
+        ctx->stats.k[sp].launches = 1;
+        ctx->stats.k[sp].bytes = 4.0 * (double)n + 4.0 * (double)nf;
+    }
+    if (profile) {
+        float x = 0;
+        if (cudaEventElapsedTime(&x, ctx->events[0], ctx->events[1]) == cudaSuccess) ctx->stats.k[sc].ms = x;
+        if (cudaEventElapsedTime(&x, ctx->events[1], ctx->events[2]) == cudaSuccess) ctx->stats.k[sb].ms = x;
+        ctx->stats.k[st_].ms = ms_tail;
+        ctx->stats.k[ss].ms = ms_scan;
+        ctx->stats.k[sa].ms = ms_apply;
+        if ((d_symbols_final || n_final) && cudaEventElapsedTime(&x, ctx->events[3], ctx->events[4]) == cudaSuccess)
+            ctx->stats.k[sp].ms = x;
+        cudaGetLastError();
+    }
+    return BPE_OK;
+}
+
+}  // namespace bpe

@@ -91,9 +91,17 @@ const char *bpe_last_error(const bpe_ctx *ctx);
  *                        (the same merges and final stream: no count or merge
  *                        crosses a WORD_START); 0 = over the full symbol
  *                        stream (default)
- *   BPE_OPT_MERGE        full-stream merge and compaction (all give the same
- *                        results):
- *                        BPE_MERGE_TWO_PASS (default): per merge, range
+ *   BPE_OPT_MERGE        the merge loop (all give the same results):
+ *                        BPE_MERGE_LISTS (default): every pair occurrence
+ *                          is filed, when it forms, in its pair's list; a
+ *                          merge reads only its pair's list, rewrites those
+ *                          positions in place (the right token's positions
+ *                          marked dead) and keeps counts by exact deltas; the
+ *                          argmax scans a frontier of the highest counts;
+ *                          the stream is compacted once at the end.  Needs
+ *                          byte-level input (ids < 256, bits 17-31 zero);
+ *                          other input runs BPE_MERGE_TWO_PASS
+ *                        BPE_MERGE_TWO_PASS: per merge, range
  *                          summaries (the last CTA scans them into offsets),
  *                          then each range merges and compacts; no CTA waits
  *                          on another
@@ -131,7 +139,14 @@ const char *bpe_last_error(const bpe_ctx *ctx);
  *                        and at the end).  0 = off, every merge rewrites the
  *                        whole stream (default); 1 = from the first window
  *                        after the best pair's count falls below 1/64 of the
- *                        input length; 2 = from merge 0 */
+ *                        input length; 2 = from merge 0
+ *   BPE_OPT_LIST_FRONTIER  testing: the occurrence-list loop's argmax
+ *                        frontier capacity (1 .. 8192; 0 = default 8192);
+ *                        small values force its overflow and rescan paths
+ *   BPE_OPT_LIST_TAIL    the occurrence-list loop runs a merge whose list
+ *                        holds at most this many entries in one CTA, many
+ *                        merges per launch (0 = every merge on all SMs;
+ *                        -1 = default 2048; at most 2048) */
 enum {
     BPE_OPT_TABLE_LOG2 = 1,
     BPE_OPT_GRAPH = 2,
@@ -143,10 +158,12 @@ enum {
     BPE_OPT_TRIE_LAYOUT = 8,
     BPE_OPT_UNI_CHUNK = 9,
     BPE_OPT_TEST_STALL_TILE = 10,
-    BPE_OPT_SPARSE_MERGE = 11
+    BPE_OPT_SPARSE_MERGE = 11,
+    BPE_OPT_LIST_FRONTIER = 12,
+    BPE_OPT_LIST_TAIL = 13
 };
 enum { BPE_TRIE_DOUBLE_ARRAY = 0, BPE_TRIE_BITMAP = 1 };
-enum { BPE_MERGE_TWO_PASS = 0, BPE_MERGE_LOOKBACK = 1, BPE_MERGE_TILES = 2 };
+enum { BPE_MERGE_TWO_PASS = 0, BPE_MERGE_LOOKBACK = 1, BPE_MERGE_TILES = 2, BPE_MERGE_LISTS = 3 };
 int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value);
 
 /* Statistics of the last bpe_train or trie_encode call on this context.
@@ -198,6 +215,39 @@ int bpe_pretokenize(bpe_ctx *ctx, const uint8_t *d_bytes, uint64_t n, uint32_t *
 int bpe_train(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_merges,
               bpe_merge *h_merges_out, uint32_t *n_done,
               uint32_t *d_symbols_final, uint64_t *n_final);
+
+/* -------------------------------------------------------- vocabulary --- */
+
+/* The vocabulary a merge table defines ([GPU-BPE] "What is this?": each
+ * merge gives its pair one new symbol; "Host architecture", 1.: the
+ * vocabulary, as byte strings, is what the trie is compiled from).  Token
+ * b < 256 is the single byte b; token 256 + k is merge k's left token's bytes
+ * followed by its right token's bytes.  Host only, needs no GPU.
+ *
+ * h_merges: n_merges entries as bpe_train writes them (merge k must have
+ * new_id 256 + k and left, right < 256 + k).  h_bytes_out: bytes_capacity
+ * bytes; h_off_out: 257 + n_merges uint64 offsets, token t being
+ * h_bytes_out[h_off_out[t] .. h_off_out[t+1]) -- the layout trie_build takes.
+ * *n_bytes receives the total; when it exceeds bytes_capacity nothing is
+ * written and BPE_ERR_CAPACITY is returned (call with capacity 0 to size the
+ * buffer).  Errors: INVALID_ARG (malformed table, null pointer), ID_OVERFLOW,
+ * CAPACITY. */
+int bpe_vocab_from_merges(const bpe_merge *h_merges, uint32_t n_merges, uint8_t *h_bytes_out,
+                          uint64_t bytes_capacity, uint64_t *h_off_out, uint64_t *n_bytes);
+
+/* Ids or symbols back to bytes on the device: the concatenation of the byte
+ * strings (as bpe_vocab_from_merges defines them) of d_ids[0 .. n_ids).  Bits
+ * 0-15 of each value are the id and WORD_START (bit 16) is ignored, so a
+ * symbol stream from bpe_pretokenize / bpe_train and the int32 ids of
+ * trie_encode with the same vocabulary both decode; decode(encode(x)) == x.
+ *
+ * d_ids: n_ids uint32 (device); d_bytes_out: bytes_capacity bytes (device).
+ * *n_bytes (host) receives the total; when it exceeds bytes_capacity nothing
+ * is written and BPE_ERR_CAPACITY is returned with the required size.  Blocks
+ * until done.  Errors: INVALID_ARG (malformed table, a value with bits above
+ * 16 or an id past 255 + n_merges), ID_OVERFLOW, CAPACITY, OOM, CUDA. */
+int bpe_decode(bpe_ctx *ctx, const bpe_merge *h_merges, uint32_t n_merges, const uint32_t *d_ids,
+               uint64_t n_ids, uint8_t *d_bytes_out, uint64_t bytes_capacity, uint64_t *n_bytes);
 
 /* ---------------------------------------------------------------- trie --- */
 

@@ -139,3 +139,44 @@ def test_layout_large_substring_vocab_sampled():
     rng = random.Random(3)
     for p in rng.sample(range(len(d)), 3000):
         assert da_longest(lc, lb, lt, d, p, len(d)) == ref.longest_match(d, p)
+
+
+def test_vocab_from_merges_matches_oracle():
+    """bpe_vocab_from_merges (the library, host only) against the oracle's
+    vocabulary on the tiny workload's merge table and on the large corpus's
+    stored table (32,000 merges)."""
+    import bpe_trie_encode_gb300 as bt
+    sym = oracle.pretokenize(synth.corpus("tiny"))
+    m, _ = oracle.train_words(sym, 256)
+    tables = [m, m[:0], m[:1]]
+    lm = os.path.join(ROOT, "tests", "golden", "large_merges.npy")
+    if os.path.exists(lm):
+        lr = np.load(lm).astype(np.uint32)
+        big = np.zeros((lr.shape[0], 4), dtype=np.uint32)
+        big[:, :2] = lr[:, :2]
+        big[:, 2] = 256 + np.arange(lr.shape[0], dtype=np.uint32)
+        big[:, 3] = lr[:, 2]
+        tables.append(big)
+    for t in tables:
+        vb, off = bt.vocab_from_merges(t)
+        wb, woff = oracle.vocab_from_merges(t)
+        assert np.array_equal(off, woff.astype(np.uint64))
+        assert np.array_equal(vb, wb)
+
+
+def test_vocab_from_merges_rejects_malformed_tables():
+    lib = _capi.load()
+    n = ctypes.c_uint64(0)
+
+    def call(rows):
+        arr = (_capi.bpe_merge * len(rows))(*[_capi.bpe_merge(*r) for r in rows])
+        return lib.bpe_vocab_from_merges(arr, len(rows), None, 0, None, ctypes.byref(n))
+
+    assert call([(97, 98, 256, 1)]) == -6            # valid: CAPACITY with the size
+    assert n.value == 256 + 2
+    assert call([(97, 98, 257, 1)]) == -1            # new_id must be 256 + k
+    assert call([(97, 256, 256, 1)]) == -1           # an id no earlier merge made
+    assert call([(97, 98, 256, 1), (256, 256, 257, 1)]) == -6
+    assert n.value == 256 + 2 + 4
+    assert lib.bpe_vocab_from_merges(None, 1, None, 0, None, ctypes.byref(n)) == -1
+    assert lib.bpe_decode(None, None, 0, None, 0, None, 0, None) == -1

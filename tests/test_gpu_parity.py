@@ -121,15 +121,15 @@ def test_train_identical_runs_cross_tiles(ctx, n):
     check_train(ctx, oracle.pretokenize(text), 12)
 
 
-@pytest.mark.parametrize("mode", ["lookback", "tiles", "persistent"])
+@pytest.mark.parametrize("mode", ["two_pass", "lookback", "tiles", "persistent"])
 @pytest.mark.parametrize("case", ["runs", "random", "tiny", "med"])
 def test_train_merge_variants_agree(ctx, golden, case, mode):
-    # the single-pass merge (decoupled look-back), the gapped-tile merge and
-    # the persistent two-pass loop give the same merges and stream as the
-    # default two-pass merge
+    # the full-stream loops -- two-pass merge, single-pass merge (decoupled
+    # look-back), gapped tiles, persistent two-pass -- give the same merges
+    # and stream as the default occurrence-list loop
     import bpe_trie_encode_gb300 as bt
     ctx.set_option(bt.BPE_OPT_MERGE, {"lookback": bt.BPE_MERGE_LOOKBACK, "tiles": bt.BPE_MERGE_TILES,
-                                      "persistent": bt.BPE_MERGE_TWO_PASS}[mode])
+                                      "persistent": bt.BPE_MERGE_TWO_PASS, "two_pass": bt.BPE_MERGE_TWO_PASS}[mode])
     ctx.set_option(bt.BPE_OPT_PERSISTENT, 1 if mode == "persistent" else 0)
     try:
         if case == "runs":
@@ -152,23 +152,29 @@ def test_train_merge_variants_agree(ctx, golden, case, mode):
                 _, fk = ctx.train(sym, k)
                 assert sha(host_u32(fk)) == g["checkpoints"][str(k)]["sha256"], k
     finally:
-        ctx.set_option(bt.BPE_OPT_MERGE, bt.BPE_MERGE_TWO_PASS)
+        ctx.set_option(bt.BPE_OPT_MERGE, bt.BPE_MERGE_LISTS)
         ctx.set_option(bt.BPE_OPT_PERSISTENT, 0)
 
 
 @pytest.mark.parametrize("mode", ["auto", "auto-eager", "always", "always-eager"])
 @pytest.mark.parametrize("case", ["runs", "random", "alternating", "tiny", "med"])
 def test_train_sparse_modes_agree(ctx, golden, case, mode):
-    # occurrence-driven merges (tombstones, exact deltas, compaction) after
-    # the automatic switch and from merge 0, with graphs and with host
-    # launches, give the oracle's merges and final stream (every other
-    # training test runs with the mode off, the default); the automatic
-    # switch comes at the first poll (merge 96), so only the longer cases
-    # exercise it, while merge 0 on puts million-symbol runs through the
-    # l == r walk
+    # the two-pass loop's occurrence-driven merges (tombstones, exact
+    # deltas, compaction) after the automatic switch and from merge 0, with
+    # graphs and with host launches, give the oracle's merges and final
+    # stream; the automatic switch comes at the first poll (merge 96), so
+    # only the longer cases exercise it, while merge 0 on puts million-symbol
+    # runs through the l == r walk.  Where the mode must have engaged, the
+    # call's statistics show its scan kernel.
     import bpe_trie_encode_gb300 as bt
+    ctx.set_option(bt.BPE_OPT_MERGE, bt.BPE_MERGE_TWO_PASS)
     ctx.set_option(bt.BPE_OPT_SPARSE_MERGE, 2 if mode.startswith("always") else 1)
     ctx.set_option(bt.BPE_OPT_GRAPH, 0 if mode.endswith("eager") else 1)
+
+    def engaged():
+        st = ctx.stats()
+        return st.get("merge_scan", {}).get("launches", 0) > 0
+
     try:
         if case == "runs":
             text = b" ".join(b"a" * n for n in list(range(1, 40)) + [1001, 4097, 64, 65]) + b"aaaa bbbb abab" * 3
@@ -179,16 +185,22 @@ def test_train_sparse_modes_agree(ctx, golden, case, mode):
                 rng = random.Random(200 + seed)
                 alphabet = [b"ab", b"aab ", b"aab c.", b"abc a.\n1"][seed]
                 check_train(ctx, oracle.pretokenize(rand_bytes(rng, 9000 + 4096 * seed, alphabet)), 150)
+            if mode.startswith("always"):
+                assert engaged()
         elif case == "alternating":
             check_train(ctx, oracle.pretokenize(b"ab" * 50000 + b" " + b"ba" * 777), 40)
+            if mode.startswith("always"):
+                assert engaged()
         elif case == "tiny":
             m, f = ctx.train(dev_sym(oracle.pretokenize(synth.corpus("tiny"))), 256)
             assert sha(m.astype(np.uint32)) == golden["tiny"]["merges_sha256"]
             assert sha(host_u32(f)) == golden["tiny"]["final_sha256"]
+            assert engaged()   # the best count falls below 1/64 of the input within the first windows
         else:
             g = golden["med"]
             sym = ctx.pretokenize(dev_u8(synth.corpus("med")))
             m, f = ctx.train(sym, g["n_merges"])
+            assert engaged()
             assert sha(m.astype(np.uint32)) == g["merges_sha256"] and sha(host_u32(f)) == g["final_sha256"]
             for k in (1, 100, 1000):
                 _, fk = ctx.train(sym, k)
@@ -196,6 +208,72 @@ def test_train_sparse_modes_agree(ctx, golden, case, mode):
     finally:
         ctx.set_option(bt.BPE_OPT_SPARSE_MERGE, 0)
         ctx.set_option(bt.BPE_OPT_GRAPH, 1)
+        ctx.set_option(bt.BPE_OPT_MERGE, bt.BPE_MERGE_LISTS)
+
+
+@pytest.mark.parametrize("fcap", [1, 2, 7, 64])
+def test_train_lists_small_frontier(ctx, golden, fcap):
+    # the occurrence-list loop with a tiny argmax frontier: it overflows and
+    # is rescanned over and over, and still gives the oracle's merges
+    import bpe_trie_encode_gb300 as bt
+    ctx.set_option(bt.BPE_OPT_LIST_FRONTIER, fcap)
+    try:
+        rng = random.Random(fcap)
+        check_train(ctx, oracle.pretokenize(rand_bytes(rng, 20000, b"abcde fgh.")), 300)
+        m, f = ctx.train(dev_sym(oracle.pretokenize(synth.corpus("tiny"))), 256)
+        assert sha(m.astype(np.uint32)) == golden["tiny"]["merges_sha256"]
+        assert sha(host_u32(f)) == golden["tiny"]["final_sha256"]
+    finally:
+        ctx.set_option(bt.BPE_OPT_LIST_FRONTIER, 0)
+
+
+@pytest.mark.parametrize("tail", [0, 1, 64, -1])
+def test_train_lists_tail_modes(ctx, golden, tail):
+    # merges on all SMs only (0), a single-CTA tail that takes only lists of
+    # one or 64 entries (mixing the two paths merge by merge), and the default
+    import bpe_trie_encode_gb300 as bt
+    ctx.set_option(bt.BPE_OPT_LIST_TAIL, tail)
+    try:
+        rng = random.Random(300 + tail)
+        check_train(ctx, oracle.pretokenize(rand_bytes(rng, 30000, b"aab c.")), 200)
+        # late merges of this text have short lists: the default tail takes some, none when off
+        tail_merges = ctx.stats()["merge_tail"]["launches"]
+        if tail == 0:
+            assert tail_merges == 0
+        elif tail == -1:
+            assert tail_merges > 0
+        check_train(ctx, oracle.pretokenize(b"a" * 5001 + b" " + b"ab" * 3000 + b" " + b"a" * 7), 30)
+        g = golden["med"]
+        sym = ctx.pretokenize(dev_u8(synth.corpus("med")))
+        m, f = ctx.train(sym, g["n_merges"])
+        assert sha(m.astype(np.uint32)) == g["merges_sha256"] and sha(host_u32(f)) == g["final_sha256"]
+    finally:
+        ctx.set_option(bt.BPE_OPT_LIST_TAIL, -1)
+
+
+def test_train_lists_unaligned_and_wide_ids(ctx):
+    # an input that starts 4 bytes into an allocation (the count's scalar
+    # path), an input without WORD_START at position 0, and ids past one byte
+    # (handed to the two-pass loop) all match the oracle
+    sym = oracle.pretokenize(synth.corpus("tiny", 30000))
+    d = dev_sym(np.concatenate([np.array([7], dtype=np.uint32), sym]))
+    m, f = ctx.train(d[1:], 100)
+    wm, wf = oracle.train_stream(sym, 100)
+    assert np.array_equal(m, wm) and np.array_equal(host_u32(f), wf)
+    s2 = sym.copy()
+    s2[0] &= ~np.uint32(WS)
+    check_train(ctx, s2, 80)
+    wide = sym.copy()
+    wide[::7] = (wide[::7] & np.uint32(WS)) | np.uint32(65000)   # no merge of these 50 makes id 65000
+    check_train(ctx, wide, 50)
+
+
+def test_train_lists_long_runs(ctx):
+    # runs of one symbol (l == r merges walk each run once from its first
+    # valid start) next to runs of a merged token, odd and even lengths
+    parts = [b"a" * n for n in (1, 2, 3, 4, 5, 31, 32, 33, 1000, 1001, 65537)]
+    text = b" ".join(parts) + b" " + b"ab" * 3001 + b"." + b"aab" * 999 + b" " + b"abab" * 777
+    check_train(ctx, oracle.pretokenize(text), 40)
 
 
 def test_train_alternating_and_ties(ctx):
@@ -224,6 +302,7 @@ def test_train_table_full_is_reported(ctx):
     rng = np.random.default_rng(5)
     data = rng.integers(97, 123, 200000, dtype=np.uint8)   # ~676 distinct pairs ... grows
     sym = oracle.pretokenize(data)
+    ctx.set_option(bt.BPE_OPT_MERGE, bt.BPE_MERGE_TWO_PASS)   # the loop with the sized hash table
     ctx.set_option(bt.BPE_OPT_TABLE_LOG2, 12)
     try:
         with pytest.raises(bt.BpeError) as e:
@@ -231,6 +310,7 @@ def test_train_table_full_is_reported(ctx):
         assert e.value.name == "TABLE_FULL"
     finally:
         ctx.set_option(bt.BPE_OPT_TABLE_LOG2, 0)
+        ctx.set_option(bt.BPE_OPT_MERGE, bt.BPE_MERGE_LISTS)
     check_train(ctx, sym[:5000], 30)   # the context is still usable
 
 
@@ -250,7 +330,9 @@ def test_train_launch_modes_agree(ctx, golden, mode):
     assert sha(host_u32(f)) == g["final_sha256"]
     if mode == "profile":
         st = ctx.stats()
-        assert st["pair_count"]["ms"] > 0 and st["merge_compact"]["launches"] == 256
+        # every merge ran either in the single-CTA tail or on all SMs (scan + apply)
+        assert st["pair_count"]["ms"] > 0 and st["merge_tail"]["launches"] + st["merge_scan"]["launches"] == 256
+        assert st["merge_apply"]["launches"] == st["merge_scan"]["launches"] and st["compact"]["launches"] == 1
 
 
 def train_workload(ctx, golden, name, checkpoints):
@@ -605,3 +687,36 @@ def test_words_tiny_med_workloads(words_ctx, golden):
 
 def test_words_large_workload(words_ctx, golden):
     train_workload(words_ctx, golden, "large", [1000])
+
+
+# ------------------------------------------------------------------ decode --
+def test_decode_streams_and_ids(ctx):
+    """bpe_decode against the oracle's decode: a trained stream (symbols with
+    WORD_START bits) and greedy ids decode to the corpus; empty input; an id
+    outside the vocabulary and a short output are reported."""
+    import bpe_trie_encode_gb300 as bt
+    text = synth.corpus("tiny", 40_000)
+    sym = oracle.pretokenize(text)
+    m, fin = oracle.train_words(sym, 200)
+    vb, voff = oracle.vocab_from_merges(m)
+    got = ctx.decode(m, dev_sym(fin)).cpu().numpy()
+    assert np.array_equal(got, text)
+    assert oracle.decode(fin & np.uint32(0xFFFF), vb, voff) == text.tobytes()
+    other = synth.lexicon("tiny").corpus(9, 30_000)
+    ids, _ = oracle.Trie(vb, voff).encode(other)
+    d_ids = torch.from_numpy(np.ascontiguousarray(ids, dtype=np.int32)).cuda()
+    assert np.array_equal(ctx.decode(m, d_ids).cpu().numpy(), other)
+    assert ctx.decode(m, d_ids[:0]).numel() == 0
+    bad = d_ids.clone()
+    bad[17] = 256 + m.shape[0]
+    with pytest.raises(bt.BpeError) as e:
+        ctx.decode(m, bad)
+    assert e.value.name == "INVALID_ARG"
+    import ctypes
+    from bpe_trie_encode_gb300 import _capi
+    arr = (_capi.bpe_merge * m.shape[0]).from_buffer_copy(np.ascontiguousarray(m).tobytes())
+    out = torch.empty(10, dtype=torch.uint8, device="cuda")
+    n = ctypes.c_uint64(0)
+    rc = _capi.load().bpe_decode(ctx._h, arr, m.shape[0], ctypes.c_void_p(d_ids.data_ptr()), d_ids.numel(),
+                                 ctypes.c_void_p(out.data_ptr()), 10, ctypes.byref(n))
+    assert rc == -6 and n.value == other.size
