@@ -2,26 +2,32 @@
 """Benchmark: BPE training merges/s and trie-encode GB/s on one GB300.
 
 One step is one pass of the whole hot path over one batch of synthetic input:
-  train leg   pre-tokenize the medium corpus (16 MiB, seed 1, 20,000-word
-              Turkish-mix lexicon) and run 4,096 merges (pair count, argmax,
-              merge, compaction per merge)
+  train leg   pre-tokenize the large corpus (256 MiB, seed 2, 50,000-word
+              Turkish-mix lexicon) and run 32,000 merges through the default
+              full-stream loop (pair count, argmax, merge of the pair's
+              occurrences) and the final compaction of the stream
   encode leg  greedy longest-match encode of 1 GiB of fresh text (seed 3) with
-              the 32,256-token vocabulary learned on the large corpus (trained
-              on the GPU during set-up, checked against the oracle's table)
-``value`` is the train leg's merges/s (the medium training workload is the
-headline configuration); the encode leg is reported in ``encode``.  Inputs are
-resident in HBM when the timed region starts; L2 is flushed between steps.
-The timed steps replay merge windows from CUDA graphs, as a caller runs them.
-Kernel durations (roofline, per-kernel table) come from the same steps run
-again with a CUDA event recorded after every kernel on the launching stream
-(the library's profile option, host launches).
+              the 32,256-token vocabulary learned on the large corpus (the
+              oracle's stored table, hash-checked)
+``value`` is the train leg's merges/s (the large training workload: the
+largest training configuration, the one the metric's per-kernel figures are
+asked for); the encode leg is reported in ``encode``.  Inputs are resident in
+HBM when the timed region starts; L2 is flushed between steps.  The timed
+steps replay the merge loop from CUDA graphs as a caller runs it.
+
+Kernel figures (``rooflines``, ``kernels``) come from the same steps run again
+with the library's profile option: a CUDA event on the launching stream around
+each kernel that runs alone (pair count, list build, compaction, encode), and
+event nodes inside the merge loop's graph (its kernels then run without the
+launch overlap of the timed replay, so their sum exceeds the replayed loop).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-``--impl reference`` times the CPU oracle (single-threaded C) on the same
-workload: each step runs the oracle's training on the medium corpus and its
-greedy encode on a 64 MiB sample of the encode text.
-N > 1 (torchrun) runs independent replicas, one per GPU ("weak" scaling).
+``--impl reference`` times the CPU oracle (single-threaded C, pinned to one
+core) on the same workload: each step pre-tokenizes the large corpus and runs
+the word-frequency oracle's first merges, then its greedy encode of a 64 MiB
+sample of the encode text.  N > 1 (torchrun) runs independent replicas, one
+per GPU ("weak" scaling).
 """
 from __future__ import annotations
 
@@ -41,6 +47,7 @@ sys.path.insert(0, ROOT)
 METRIC = "BPE train merges/s + trie_encode GB/s on 1 GB300; % of HBM roofline"
 TRAIN = {"tiny": 256, "med": 4096, "large": 32000}
 ENC_REF_SAMPLE = 64 << 20
+REF_MERGES = 200          # word-frequency oracle merges per reference step (a bounded sample)
 
 
 def parse():
@@ -49,15 +56,17 @@ def parse():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--train", default="med", choices=sorted(TRAIN))
+    ap.add_argument("--train", default="large", choices=sorted(TRAIN))
     ap.add_argument("--encode", default="enc", choices=["enc", "batch", "none"])
     ap.add_argument("--merges", type=int, default=None, help="override the merge count (profiling cases)")
     ap.add_argument("--encode-bytes", type=int, default=None, help="encode only a prefix (profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-extra", action="store_true", help="skip the extra legs (word-frequency, large, batch)")
+    ap.add_argument("--no-extra", action="store_true", help="skip the extra legs (word-frequency, other sizes, batch)")
+    ap.add_argument("--merge-mode", type=int, choices=[0, 1, 2, 3], default=3,
+                    help="BPE_OPT_MERGE for the train leg (3 = occurrence lists, the library default)")
     ap.add_argument("--sparse-merge", type=int, choices=[0, 1, 2], default=0,
-                    help="BPE_OPT_SPARSE_MERGE for the full-stream training leg (0 = off, the library default)")
+                    help="BPE_OPT_SPARSE_MERGE (two-pass loop only)")
     ap.add_argument("--leg", choices=["unigram"], default=None,
                     help="run only that leg and print its JSON (profiling)")
     return ap.parse_args()
@@ -174,22 +183,25 @@ def traffic_record():
     return out
 
 
-def roofline(stats: dict, families: list[str], peak: float, peak_kind: str, traffic: dict):
-    fam = max(families, key=lambda f: stats.get(f, {}).get("ms", 0.0))
-    s = stats[fam]
-    achieved = s["bytes"] / (s["ms"] / 1e3) / 1e9 if s["ms"] > 0 else 0.0
-    per_launch_bytes = s["bytes"] / max(s["launches"], 1)
+def kernel_roofline(stats: dict, fam: str, peak: float, peak_kind: str, traffic: dict, bound: str = "hbm"):
+    """Roofline entry of one kernel family from the profiled pass: algorithmic
+    bytes per launch (the method's bytes, the library's stats) over the
+    average launch duration; ``traffic`` from a committed ncu record of that
+    kernel, scaled to this launch's algorithmic bytes, or null."""
+    s = stats.get(fam)
+    if not s or not s["launches"] or s["ms"] <= 0:
+        return None
+    achieved = s["bytes"] / (s["ms"] / 1e3) / 1e9
+    per_launch_bytes = s["bytes"] / s["launches"]
     t = traffic.get(fam)
     tr = None
     if t:
-        # ncu measured a (possibly smaller) case: scale its DRAM bytes by the
-        # algorithmic bytes of that case to this launch's algorithmic bytes
         tr = t["dram_bytes"] * per_launch_bytes / t["algorithmic_bytes"] if t.get("scale") else t["dram_bytes"]
-    return {"kernel": fam, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+    return {"kernel": fam, "bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_kind": f"of {peak_kind}",
             "traffic": round(tr, 1) if tr is not None else None,
             "algorithmic_bytes_per_launch": round(per_launch_bytes, 1),
-            "avg_launch_ms": round(s["ms"] / max(s["launches"], 1), 6)}
+            "avg_launch_ms": round(s["ms"] / s["launches"], 6), "launches": s["launches"]}
 
 
 def timed(stream, fn):
@@ -203,77 +215,100 @@ def timed(stream, fn):
     return r, a.elapsed_time(b)
 
 
-def extra_legs(args, ctx, dev, stream, flush, d_text, d_sym, n_merges, peak, peak_kind):
+def add_stats(acc: dict, st: dict):
+    for k, v in st.items():
+        if k == "kernel_launches":
+            continue
+        a = acc.setdefault(k, {"launches": 0, "bytes": 0.0, "ms": 0.0})
+        for f in ("launches", "bytes", "ms"):
+            a[f] += v[f]
+
+
+def train_leg(args, ctx, stream, flush, name, steps, warmup):
+    """W warm-up and K timed runs of pre-tokenize + full-stream training of a
+    named corpus (final stream included), L2 flushed before each; then one
+    profiled run for the kernel split."""
+    import torch
+
+    import bpe_trie_encode_gb300 as bt
+    import synth
+    text = synth.corpus(name)
+    d_text = torch.from_numpy(text).to(stream.device)
+    d_sym = torch.empty(text.size, dtype=torch.int32, device=stream.device)
+    n_merges = TRAIN[name]
+    ms_all, merges, steps_ms = 0.0, 0, []
+    for i in range(warmup + steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        (m, _), ms = timed(stream, lambda: ctx.train(ctx.pretokenize(d_text, out=d_sym), n_merges))
+        if i >= warmup:
+            ms_all += ms
+            merges += m.shape[0]
+            steps_ms.append(round(ms, 3))
+    ctx.set_option(bt.BPE_OPT_PROFILE, 1)
+    ctx.train(ctx.pretokenize(d_text, out=d_sym), n_merges)
+    kern = {}
+    add_stats(kern, ctx.stats())
+    ctx.set_option(bt.BPE_OPT_PROFILE, 0)
+    return {"value": round(merges / (ms_all / 1e3), 2), "unit": "merges/s", "ms_per_step": round(ms_all / steps, 3),
+            "us_per_merge": round(1e3 * ms_all / max(merges, 1), 3), "steps_ms": steps_ms,
+            "workload": f"{name} training: {text.size} B corpus, {n_merges} merges, full stream",
+            "kernels": {k: {"launches": v["launches"], "ms": round(v["ms"], 3)} for k, v in kern.items()}}
+
+
+def extra_legs(args, ctx, dev, stream, flush, peak, peak_kind):
     import numpy as np
     import torch
 
     import bpe_trie_encode_gb300 as bt
     import synth
     out = {}
-    # word-frequency training of the same medium corpus
+    # the medium (16 MiB, 4,096 merges) and tiny (64 KiB, 256 merges) training workloads, full stream
+    out["train_med"] = train_leg(args, ctx, stream, flush, "med", args.steps, args.warmup)
+    out["train_tiny"] = train_leg(args, ctx, stream, flush, "tiny", args.steps, args.warmup)
+    # word-frequency training (the same merges) of the medium and large corpora
     ctx.set_option(bt.BPE_OPT_TRAIN_WORDS, 1)
-    ms_all, merges, kern = 0.0, 0, {}
-    for prof in (False, True):   # timed graph replay, then one profiled step for the kernel split
-        ctx.set_option(bt.BPE_OPT_PROFILE, 1 if prof else 0)
-        for i in range(1 if prof else args.warmup + args.steps):
-            flush.fill_(1)
-            torch.cuda.synchronize()
-            (m, _), ms = timed(stream, lambda: (ctx.pretokenize(d_text, out=d_sym),
-                                                ctx.train(d_sym, n_merges, final=False))[1])
-            if prof:
-                for k2, v in ctx.stats().items():
-                    if k2 != "kernel_launches":
-                        a = kern.setdefault(k2, {"launches": 0, "ms": 0.0})
-                        a["launches"] += v["launches"]
-                        a["ms"] += v["ms"]
-            elif i >= args.warmup:
-                ms_all += ms
-                merges += m.shape[0]
-    out["train_words"] = {"value": round(merges / (ms_all / 1e3), 2), "unit": "merges/s",
-                          "ms_per_step": round(ms_all / args.steps, 3),
-                          "workload": f"{args.train} training by distinct words (identical merges)",
-                          "kernels": {k2: {"launches": v["launches"], "ms": round(v["ms"], 3)} for k2, v in kern.items()}}
-    # the large training workload (256 MiB, 32,000 merges), word-frequency path, one timed run
-    big = synth.corpus("large")
-    d_big = torch.from_numpy(big).to(dev)
-    d_bsym = torch.empty(big.size, dtype=torch.int32, device=dev)
-    ctx.set_option(bt.BPE_OPT_PROFILE, 0)
-    ctx.pretokenize(d_big, out=d_bsym)
-    ctx.train(d_bsym, 200, final=False)          # warm-up
-    flush.fill_(1)
-    torch.cuda.synchronize()
-    (m, _), ms = timed(stream, lambda: (ctx.pretokenize(d_big, out=d_bsym), ctx.train(d_bsym, 32000, final=False))[1])
-    out["train_large_words"] = {"value": round(m.shape[0] / (ms / 1e3), 2), "unit": "merges/s", "ms": round(ms, 3),
-                                "workload": f"large training: {big.size} B corpus, {m.shape[0]} merges, distinct words"}
+    for name in ("med", "large"):
+        text = synth.corpus(name)
+        d_text = torch.from_numpy(text).to(dev)
+        d_sym = torch.empty(text.size, dtype=torch.int32, device=dev)
+        ctx.train(ctx.pretokenize(d_text, out=d_sym), 200, final=False)   # warm-up
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        (m, _), ms = timed(stream, lambda: ctx.train(ctx.pretokenize(d_text, out=d_sym), TRAIN[name], final=False))
+        out[f"train_{name}_words"] = {"value": round(m.shape[0] / (ms / 1e3), 2), "unit": "merges/s",
+                                      "ms": round(ms, 3),
+                                      "workload": f"{name} training by distinct words: {text.size} B corpus, "
+                                                  f"{m.shape[0]} merges (the full-stream merges)"}
+        del d_text, d_sym
     ctx.set_option(bt.BPE_OPT_TRAIN_WORDS, 0)
-    del d_bsym
     # the batch encode workload: 512 documents, 250,000-token substring vocabulary
+    big = synth.corpus("large")
     vb, voff = synth.substring_vocab(big)
-    del big, d_big
+    del big
     data, doc_off = synth.batch_documents()
     trie = ctx.trie_build(vb, voff)
     d_data = torch.from_numpy(data).to(dev)
     d_off = torch.from_numpy(doc_off.astype(np.int64)).to(dev)
     ids = torch.empty(data.size, dtype=torch.int32, device=dev)
-    ctx.set_option(bt.BPE_OPT_PROFILE, 1)
-    ms_all, kern = 0.0, {}
+    ms_all = 0.0
     for i in range(args.warmup + args.steps):
         flush.fill_(1)
         torch.cuda.synchronize()
         (r, _), ms = timed(stream, lambda: (ctx.encode(trie, d_data, d_off, ids_out=ids), None))
         if i >= args.warmup:
             ms_all += ms
-            for k2, v in ctx.stats().items():
-                if k2 != "kernel_launches":
-                    a = kern.setdefault(k2, {"launches": 0, "bytes": 0.0, "ms": 0.0})
-                    for f in ("launches", "bytes", "ms"):
-                        a[f] += v[f]
+    ctx.set_option(bt.BPE_OPT_PROFILE, 1)
+    ctx.encode(trie, d_data, d_off, ids_out=ids)
+    kern = {}
+    add_stats(kern, ctx.stats())
     ctx.set_option(bt.BPE_OPT_PROFILE, 0)
     out["encode_batch"] = {"value": round(args.steps * data.size / (ms_all / 1e3) / 1e9, 3), "unit": "GB/s",
                            "ms_per_step": round(ms_all / args.steps, 3),
                            "workload": f"{doc_off.size - 1} documents, {data.size} B, 250,000-token substring vocabulary",
                            "n_ids": int(r[0].numel()), "trie": trie.info(),
-                           "roofline": roofline(kern, ["encode_spec", "encode_emit"], peak, peak_kind, {})}
+                           "rooflines": {f: kernel_roofline(kern, f, peak, peak_kind, {})
+                                         for f in ("encode_spec", "encode_emit")}}
     # the same batch through the bitmap-node trie layout, against the double array above
     ctx.set_option(bt.BPE_OPT_TRIE_LAYOUT, bt.BPE_TRIE_BITMAP)
     ms_bm = 0.0
@@ -291,7 +326,41 @@ def extra_legs(args, ctx, dev, stream, flush, d_text, d_sym, n_merges, peak, pea
         "workload": "the batch encode above with 64-byte bitmap nodes instead of the double array"}
     out["unigram_batch"] = unigram_leg(args, ctx, stream, flush, trie, voff, d_data, d_off, ids, peak, peak_kind,
                                        vb=vb, data=data, doc_off=doc_off)
+    out["unigram_doc"] = unigram_doc_leg(args, ctx, stream, flush, trie, voff)
     return out
+
+
+def unigram_doc_leg(args, ctx, stream, flush, trie, voff):
+    """Unigram encoding of one 64 MiB document (the first 64 MiB of the
+    encode text) on the batch trie: the single-document case."""
+    import torch
+
+    import bpe_trie_encode_gb300 as bt
+    import synth
+    scores = synth.unigram_scores(voff.size - 1)
+    unk = synth.unigram_unk_score(scores)
+    model = ctx.unigram(trie, scores, voff.size - 1, unk)
+    text = synth.corpus("enc", 64 << 20)
+    d = torch.from_numpy(text).to(stream.device)
+    ids = torch.empty(text.size, dtype=torch.int32, device=stream.device)
+    ms_all = 0.0
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        (r, _), ms = timed(stream, lambda: (ctx.unigram_encode(model, d, ids_out=ids), None))
+        if i >= args.warmup:
+            ms_all += ms
+    ctx.set_option(bt.BPE_OPT_PROFILE, 1)
+    ctx.unigram_encode(model, d, ids_out=ids)
+    kern = {}
+    add_stats(kern, ctx.stats())
+    ctx.set_option(bt.BPE_OPT_PROFILE, 0)
+    model.close()
+    return {"value": round(args.steps * text.size / (ms_all / 1e3) / 1e9, 3), "unit": "GB/s",
+            "ms_per_step": round(ms_all / args.steps, 3), "n_ids": int(r[0].numel()),
+            "workload": f"one document of {text.size} B (the encode text's first 64 MiB), Viterbi under "
+                        "synthetic Zipf log-probabilities, 250,000-token substring vocabulary",
+            "kernels": {k: {"launches": v["launches"], "ms": round(v["ms"], 3)} for k, v in kern.items()}}
 
 
 def unigram_leg(args, ctx, stream, flush, trie, voff, d_data, d_off, ids, peak, peak_kind, vb=None, data=None,
@@ -413,8 +482,8 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     ctx = bt.Context(local_rank)
+    ctx.set_option(bt.BPE_OPT_MERGE, args.merge_mode)
     ctx.set_option(bt.BPE_OPT_SPARSE_MERGE, args.sparse_merge)
-    g = golden()
     peak, peak_kind = peaks()
     n_merges = args.merges or TRAIN[args.train]
 
@@ -444,19 +513,20 @@ def run_ours(args, rank, world, local_rank):
             wl = "512 documents of >= 64 KiB (seed 4), 250,000-token substring vocabulary"
         trie = ctx.trie_build(vb, voff)
         h_enc = torch.from_numpy(etext).pin_memory()
-        enc = {"trie": trie, "vb": vb, "voff": voff, "h": h_enc, "d": h_enc.to(dev), "h_off": torch.from_numpy(doc_off).pin_memory(),
-               "d_off": torch.from_numpy(doc_off).to(dev), "workload": wl, "bytes": int(etext.size),
+        enc = {"trie": trie, "vb": vb, "voff": voff, "h": h_enc, "d": h_enc.to(dev),
+               "h_off": torch.from_numpy(doc_off).pin_memory(), "d_off": torch.from_numpy(doc_off).to(dev),
+               "workload": wl, "bytes": int(etext.size),
                "ids": torch.empty(int(etext.size), dtype=torch.int32, device=dev)}
         del etext
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(timed: bool, acc: dict):
+    def step(timed_step: bool, acc: dict):
         flush.fill_(1)                         # L2 flush between steps (> 129 MB written)
         e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         e0.record(stream)
         ctx.pretokenize(d_text, out=d_sym)
-        m, _ = ctx.train(d_sym, n_merges, final=False)
+        m, fin = ctx.train(d_sym, n_merges)    # the merge table and the final stream
         st_train = ctx.stats()
         e1.record(stream)
         st_enc = None
@@ -467,25 +537,25 @@ def run_ours(args, rank, world, local_rank):
             st_enc = ctx.stats()
         e2.record(stream)
         torch.cuda.synchronize(dev)
-        if timed:
+        if timed_step:
             acc["train_ms"] += e0.elapsed_time(e1)
             acc["enc_ms"] += e1.elapsed_time(e2)
+            acc["steps_ms"].append(round(e0.elapsed_time(e1), 3))
             acc["merges"] += m.shape[0]
             acc["launches"] += 1 + st_train["kernel_launches"] + (st_enc["kernel_launches"] if st_enc else 0)
-            for st in (st_train, st_enc):
-                for k, v in (st or {}).items():
-                    if k == "kernel_launches":
-                        continue
-                    a = acc["kern"].setdefault(k, {"launches": 0, "bytes": 0.0, "ms": 0.0})
-                    for f in ("launches", "bytes", "ms"):
-                        a[f] += v[f]
+            add_stats(acc["kern"], st_train)
+            add_stats(acc["kern"], st_enc or {})
             acc["n_ids"] = n_ids
+            acc["n_final"] = int(fin.numel())
+
+    def fresh():
+        return {"train_ms": 0.0, "enc_ms": 0.0, "merges": 0, "launches": 0, "kern": {}, "n_ids": 0,
+                "steps_ms": [], "n_final": 0}
 
     # timed steps: graph replay, as a caller runs it
-    dummy = {"train_ms": 0, "enc_ms": 0, "merges": 0, "launches": 0, "kern": {}}
     for _ in range(args.warmup):
-        step(False, dummy)
-    acc = {"train_ms": 0.0, "enc_ms": 0.0, "merges": 0, "launches": 0, "kern": {}, "n_ids": 0}
+        step(False, fresh())
+    acc = fresh()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -498,15 +568,14 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     clk = clocks.stop() if clocks else None
-    # per-kernel device time for the roofline: the same steps again with a
-    # CUDA event after every kernel on the launching stream (host launches)
+    # per-kernel device time: the same steps again with the profile option
     ctx.set_option(bt.BPE_OPT_PROFILE, 1)
-    prof = {"train_ms": 0.0, "enc_ms": 0.0, "merges": 0, "launches": 0, "kern": {}, "n_ids": 0}
-    step(False, dummy)
+    prof = fresh()
+    step(False, prof)
     for _ in range(max(1, min(args.steps, 2))):
         step(True, prof)
     ctx.set_option(bt.BPE_OPT_PROFILE, 0)
-    acc["kern"] = prof["kern"]
+    kern = prof["kern"]
 
     (train_ms, enc_ms), (merges_total, enc_bytes_total) = reduce_ranks(
         [acc["train_ms"], acc["enc_ms"]], [acc["merges"], enc["bytes"] * args.steps if enc else 0], world, dev)
@@ -529,7 +598,7 @@ def run_ours(args, rank, world, local_rank):
             a.record(stream)
             dt = h_text.to(dev, non_blocking=True)
             ctx.pretokenize(dt, out=d_sym)
-            m, _ = ctx.train(d_sym, n_merges, final=False)     # merge table returns to host
+            m, _ = ctx.train(d_sym, n_merges, final=False)     # the merge table returns to the host
             b.record(stream)
             if enc:   # host buffers in and out through trie_encode_host (copies overlap the encode)
                 h_ids, h_io = bt.encode_host(ctx, enc["trie"], enc["h"], enc["h_off"], ids_out=h_ids_buf,
@@ -548,15 +617,15 @@ def run_ours(args, rank, world, local_rank):
                "d2h_bytes_per_step": int(h_merges_bytes + d2h_ids)}
         if enc:
             e2e["encode"] = {"value": round(throughput(e2e_bytes, en_ms) / 1e9, 3), "unit": "GB/s",
-                             "steps_ms": en_steps,   # rank 0's; some steps stall
+                             "steps_ms": en_steps,
                              "median_GBs": round(enc["bytes"] / (sorted(en_steps)[len(en_steps) // 2] / 1e3) / 1e9, 3)
                              if en_steps else None}
 
-    # ---- extra legs: the word-frequency trainer (same merges), the large
-    # training workload, the batch encode workload
+    # ---- extra legs: other training sizes, the word-frequency trainer (same
+    # merges), the batch encode workload, Unigram
     extra = {}
     if not args.no_extra:
-        extra = extra_legs(args, ctx, dev, stream, flush, d_text, d_sym, n_merges, peak, peak_kind)
+        extra = extra_legs(args, ctx, dev, stream, flush, peak, peak_kind)
 
     # ---- CPU baseline: the oracle as it stands, rank 0, N == 1 only
     cpu = None
@@ -566,25 +635,35 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return None
     traffic = traffic_record()
-    kern = acc["kern"]
+    loop = ("merge_tail", "merge_scan", "merge_apply")
+    loop_ms = sum(kern.get(f, {"ms": 0.0})["ms"] for f in loop)
+    rooflines = {f: kernel_roofline(kern, f, peak, peak_kind, traffic)
+                 for f in ("pair_count", "list_build", "compact", "encode_spec", "encode_emit") + loop}
+    # the timed step's dominant kernel: the merge loop's tail (most merges run there)
+    dom = max((f for f in rooflines if rooflines[f]), key=lambda f: kern[f]["ms"])
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "merges/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round((train_ms + enc_ms) / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
         "data": "synthetic (seeded generator)",
-        "config": {"workload": f"{args.train} training: {text.size} B corpus, {n_merges} merges; "
-                               f"encode leg: {enc['workload'] if enc else 'none'}",
+        "config": {"workload": f"{args.train} training: {text.size} B corpus, {n_merges} merges, full stream "
+                               f"(final compaction included); encode leg: {enc['workload'] if enc else 'none'}",
                    "train_corpus_bytes": int(text.size), "n_merges": n_merges,
                    "l2": "flushed between steps (256 MiB write)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "vocab": vocab_check, "sparse_merge": args.sparse_merge},
+                   "vocab": vocab_check, "merge_mode": args.merge_mode, "sparse_merge": args.sparse_merge},
         "train": {"value": round(value, 2), "unit": "merges/s", "ms_per_step": round(train_ms / args.steps, 3),
-                  "roofline": roofline(kern, ["pair_count", "merge_compact", "merge_scan", "argmax"], peak, peak_kind, traffic)},
-        "roofline": roofline(kern, ["pair_count", "merge_compact", "merge_scan", "argmax"], peak, peak_kind, traffic),
+                  "us_per_merge": round(1e3 * train_ms / max(merges_total, 1), 3), "steps_ms": acc["steps_ms"],
+                  "n_final": acc["n_final"]},
+        "roofline": rooflines[dom],
+        "rooflines": rooflines,
         "gpu_launches": acc["launches"],
-        "timing": ("value, e2e: CUDA-graph replay as a caller runs it; roofline and kernels: per-kernel CUDA "
-                   "events on the launching stream in a separate profiled pass of the same steps"),
+        "timing": ("value, e2e: CUDA events around each step, the merge loop replayed from CUDA graphs with "
+                   "programmatic dependent launch; kernels and rooflines: a separate profiled pass of the same "
+                   "steps (events around each stand-alone kernel, event nodes between the merge loop's kernels, "
+                   "which then run without launch overlap)"),
+        "profiled_merge_loop_ms_per_step": round(loop_ms / max(1, min(args.steps, 2)), 3),
         "kernels": {k: {"launches": v["launches"], "ms": round(v["ms"], 3),
                         "GB/s": round(v["bytes"] / (v["ms"] / 1e3) / 1e9, 1) if v["ms"] else None}
                     for k, v in kern.items()},
@@ -597,34 +676,80 @@ def run_ours(args, rank, world, local_rank):
         gbs = throughput(enc_bytes_total, enc_ms) / 1e9
         out["encode"] = {"value": round(gbs, 3), "unit": "GB/s", "ms_per_step": round(enc_ms / args.steps, 3),
                          "workload": enc["workload"], "n_ids": acc["n_ids"],
-                         "roofline": roofline(kern, ["encode_spec", "encode_emit"], peak, peak_kind, traffic)}
+                         "rooflines": {f: rooflines[f] for f in ("encode_spec", "encode_emit")}}
     return out
 
 
+class one_core:
+    """Pin this process to one host core while the oracle runs (the pages'
+    measurement method: single-threaded, one pinned core), restoring the
+    previous affinity afterwards."""
+
+    def __enter__(self):
+        self.before = None
+        self.core = None
+        try:
+            self.before = os.sched_getaffinity(0)
+            self.core = max(self.before)
+            os.sched_setaffinity(0, {self.core})
+        except (AttributeError, OSError):
+            pass
+        return self
+
+    def __exit__(self, *exc):
+        if self.before is not None:
+            try:
+                os.sched_setaffinity(0, self.before)
+            except OSError:
+                pass
+        return False
+
+    def info(self) -> dict:
+        return {"affinity": [self.core] if self.core is not None else None, "nproc": os.cpu_count(),
+                "cpu_model": cpu_model()}
+
+
 def cpu_baseline(args, text, enc, n_merges):
-    """The oracle as it stands, single-threaded, on a bounded sample: the full
-    training workload (about 10 s of CPU) and the first 64 MiB of the encode
-    text with the same vocabulary."""
-    import numpy as np
-
+    """The oracle as it stands, single-threaded and pinned to one core, on
+    bounded samples: the word-frequency form on the headline workload's first
+    merges (``value``); the full-stream form (like for like with the GPU loop)
+    on the tiny workload in full and on the medium workload's first merges;
+    and the greedy encode of the first 64 MiB of the encode text."""
     import oracle
+    import synth
 
-    t0 = time.perf_counter()
-    sym = oracle.pretokenize(text)
-    m, _ = oracle.train_words(sym, n_merges)
-    dt = time.perf_counter() - t0
-    out = {"value": round(m.shape[0] / dt, 2), "unit": "merges/s", "cores": 1, "kind": "oracle",
-           "sample": f"{args.train} training, full ({text.size} B, {n_merges} merges), "
-                     f"word-frequency oracle, single thread, {cpu_model()}",
-           "seconds": round(dt, 2)}
-    if enc:
-        sample = enc["h"][:ENC_REF_SAMPLE].numpy()
-        trie = oracle.Trie(enc["vb"], enc["voff"])
+    with one_core() as pin:
         t0 = time.perf_counter()
-        trie.encode(sample)
+        sym = oracle.pretokenize(text)
+        m, _ = oracle.train_words(sym, min(REF_MERGES, n_merges))
         dt = time.perf_counter() - t0
-        out["encode"] = {"value": round(sample.size / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
-                         "sample": f"first {sample.size} B of the encode text, same vocabulary"}
+        out = {"value": round(m.shape[0] / dt, 3), "unit": "merges/s", "cores": 1, "kind": "oracle",
+               "sample": f"{args.train} training, pre-tokenize + the first {m.shape[0]} merges "
+                         f"({text.size} B corpus), word-frequency oracle, single thread",
+               "seconds": round(dt, 2), **pin.info()}
+        tiny = oracle.pretokenize(synth.corpus("tiny"))
+        t0 = time.perf_counter()
+        mt, _ = oracle.train_stream(tiny, TRAIN["tiny"])
+        dt = time.perf_counter() - t0
+        out["full_stream_tiny"] = {"value": round(mt.shape[0] / dt, 2), "unit": "merges/s",
+                                   "ms_per_merge": round(1e3 * dt / max(mt.shape[0], 1), 3),
+                                   "sample": f"tiny training in full ({tiny.size} symbols, {mt.shape[0]} merges), "
+                                             "full-stream oracle"}
+        med = oracle.pretokenize(synth.corpus("med"))
+        t0 = time.perf_counter()
+        mm, _ = oracle.train_stream(med, 4)
+        dt = time.perf_counter() - t0
+        out["full_stream_med"] = {"value": round(mm.shape[0] / dt, 4), "unit": "merges/s",
+                                  "sample": f"medium training, the first {mm.shape[0]} merges of {med.size} "
+                                            "symbols, full-stream oracle (each merge costs about the same)"}
+        if enc:
+            sample = enc["h"][:ENC_REF_SAMPLE].numpy()
+            trie = oracle.Trie(enc["vb"], enc["voff"])
+            t0 = time.perf_counter()
+            trie.encode(sample)
+            dt = time.perf_counter() - t0
+            out["encode"] = {"value": round(sample.size / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+                             "sample": f"first {sample.size} B of the encode text, same vocabulary"}
     return out
 
 
@@ -668,13 +793,15 @@ def encode_reference_sample(args):
 
 # ---------------------------------------------------------- reference -------
 def run_reference(args, rank, world):
-    import numpy as np
-
+    """The CPU oracle on the same workload, pinned to one core: each step
+    pre-tokenizes the training corpus and runs the word-frequency oracle's
+    first merges (a bounded sample), then its greedy encode of a 64 MiB sample
+    of the encode text."""
     import oracle
     import synth
     if rank != 0:
         return None
-    n_merges = TRAIN[args.train]
+    n_merges = min(REF_MERGES, TRAIN[args.train])
     text = synth.corpus(args.train)
     enc = None
     if args.encode != "none":
@@ -690,26 +817,29 @@ def run_reference(args, rank, world):
         t2 = time.perf_counter()
         return t1 - t0, t2 - t1, m.shape[0]
 
-    for _ in range(args.warmup):
-        step()
-    tr = en = 0.0
-    merges = 0
-    for _ in range(args.steps):
-        a, b, m = step()
-        tr += a
-        en += b
-        merges += m
+    with one_core() as pin:
+        for _ in range(args.warmup):
+            step()
+        tr = en = 0.0
+        merges = 0
+        for _ in range(args.steps):
+            a, b, m = step()
+            tr += a
+            en += b
+            merges += m
     value = merges / tr
-    out = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "merges/s", "n_gpus": world,
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "merges/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round((tr + en) / args.steps * 1e3, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
            "data": "synthetic (seeded generator)",
-           "config": {"workload": f"{args.train} training: {text.size} B corpus, {n_merges} merges; "
-                                  f"encode leg: {args.encode} ({'64 MiB sample' if args.encode == 'enc' else '64 documents'})",
+           "config": {"workload": f"{args.train} training: {text.size} B corpus, pre-tokenize + the first "
+                                  f"{n_merges} merges per step; encode leg: {args.encode} "
+                                  f"({'64 MiB sample' if args.encode == 'enc' else '64 documents'})",
                       "parallelism": "CPU oracle, rank 0 only"},
-           "cpu_baseline": {"value": round(value, 2), "unit": "merges/s", "cores": 1, "kind": "oracle",
-                            "sample": f"full {args.train} training per step, single-threaded C oracle, {cpu_model()}"},
-           "e2e": {"value": round(value, 2), "unit": "merges/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+           "cpu_baseline": {"value": round(value, 3), "unit": "merges/s", "cores": 1, "kind": "oracle",
+                            "sample": f"{args.train} training, pre-tokenize + the first {n_merges} merges per "
+                                      "step, word-frequency oracle, single thread", **pin.info()},
+           "e2e": {"value": round(value, 3), "unit": "merges/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     if enc:
         out["encode"] = {"value": round(args.steps * enc[1].size / en / 1e9, 4), "unit": "GB/s",
                          "sample_bytes": int(enc[1].size)}
