@@ -26,7 +26,7 @@ enum Slot {
     S_SPARSE_OCC,
     S_DEC_TOK, S_DEC_OFF, S_DEC_BSUM, S_DEC_STATE,
     S_L_STATE, S_L_OCC, S_L_EKEY, S_L_ECNT, S_L_ELEN, S_L_EOFF, S_L_VLEN, S_L_BFILL, S_L_EBEST, S_L_FRONT,
-    S_L_HSLOT, S_L_HCNT, S_L_HENT, S_L_NS, S_L_CAND, S_L_APP, S_L_REC, S_L_CSTAT, S_L_KMODE,
+    S_L_HSLOT, S_L_HCNT, S_L_HENT, S_L_NS, S_L_CAND, S_L_APP, S_L_REC, S_L_CSTAT, S_L_KMODE, S_L_CBAR, S_L_CTILE,
     S_NUM
 };
 

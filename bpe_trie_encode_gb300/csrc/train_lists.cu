@@ -64,7 +64,6 @@ constexpr uint32_t kBadBits = 0xFFFEFF00u;    // bits a byte-level input symbol 
 constexpr uint32_t kBaseEntries = 65536;      // entry (l << 8) | r for byte pairs
 constexpr int kBcThreads = 1024;
 constexpr int kBcQuads = 4;                   // 128-bit loads per thread and step
-constexpr uint32_t kBcLimit = 0x7FFFu;        // a counter at this value asks for a flush
 constexpr size_t kBcSmem = 32768 * sizeof(uint32_t);   // 65,536 16-bit counters
 constexpr int kBfThreads = 1024;
 constexpr int kBfItems = 8;                   // positions per thread and tile
@@ -82,9 +81,8 @@ constexpr int kTlRecCap = 2 * kTlList;        // new pairs of one tail merge (tw
 constexpr int kTlHash = kTlRecCap;            // distinct new pairs of a tail merge never exceed its pairs
 constexpr uint32_t kTlBudget = 512;           // merges per tail launch
 constexpr int kSlots = 8;                     // (tail, scan, apply) slots per captured graph
-constexpr int kCpThreads = 256;
-constexpr int kCpItems = 32;                  // 8 coalesced 128-bit loads per thread
-constexpr int kCpTile = kCpThreads * kCpItems;
+constexpr int kCsThreads = 512;
+constexpr uint32_t kCsRound = 16u << 20;      // compaction round: 64 MB of symbols, resident in L2 between passes
 constexpr uint32_t kHashProbes = 4096;
 constexpr unsigned kSpinLimit = 1u << 22;
 constexpr int kInFlight = 3;
@@ -128,7 +126,9 @@ struct LP {
     uint4 *rec[2];         // per merge parity: new pairs {slot, rank, position, 0}
     uint32_t app_cap, rec_cap;
     unsigned long long *cand;   // k_lapply rescan: per CTA {best, entry}
-    unsigned long long *cstat;  // compaction: per tile status
+    uint32_t *ctot;        // compaction: per CTA slice counts, two rounds
+    uint32_t *ctile;       // compaction: per warp tile live counts, two rounds
+    uint32_t *cbar;        // compaction: grid barrier words
     uint8_t *kmode;        // per merge: 1 = run by the tail, 2 = by the multi-CTA kernels
     LState *st;
 };
@@ -222,20 +222,13 @@ __device__ __forceinline__ uint32_t block_excl(uint32_t v, uint32_t *sw, uint32_
 
 // ---------------------------------------------------------- pair count ---
 
-// Add the pairs of one quad of symbols a[0..4) (a[4] = the next symbol, or
-// kWordStart when none) to the 16-bit counters.
-__device__ __forceinline__ void bc_quad(uint32_t *cnt, const uint32_t *a, uint32_t nvalid, uint32_t &bad,
-                                        bool &hot) {
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        if ((uint32_t)i < nvalid) bad |= a[i] & kBadBits;
-        if ((uint32_t)i + 1 <= nvalid && !(a[i + 1] & kWordStart)) {
-            const uint32_t e = ((a[i] & 0xFFu) << 8) | (a[i + 1] & 0xFFu);
-            const uint32_t sh = (e & 1u) << 4;
-            const uint32_t old = atomicAdd(cnt + (e >> 1), 1u << sh);
-            hot |= ((old >> sh) & 0xFFFFu) == kBcLimit;
-        }
-    }
+// The pair (a, b), counted when b has no WORD_START: 16-bit counter of entry
+// (l << 8) | r is half r & 1 of word (l << 7) | (r >> 1).  The old word is
+// OR-ed into hot: bit 14 or 30 set means a counter has reached 16,384.
+__device__ __forceinline__ void bc_pair(uint32_t *cnt, uint32_t a, uint32_t b, uint32_t &hot) {
+    const uint32_t w = ((a << 7) & 0x7F80u) | ((b >> 1) & 0x7Fu);
+    const uint32_t inc = (b & 1u) ? 0x10000u : 1u;
+    if (!(b & kWordStart)) hot |= atomicAdd(cnt + w, inc);
 }
 
 __device__ __forceinline__ void bc_flush(uint32_t *cnt, uint32_t *g) {
@@ -252,7 +245,12 @@ __device__ __forceinline__ void bc_flush(uint32_t *cnt, uint32_t *g) {
 // Counts of the pairs (i, i+1), i+1 < n, whose right symbol has no
 // WORD_START, by entry (l << 8) | r; LERR_BADINPUT when a symbol is not a
 // byte id (with or without WORD_START).  One CTA per contiguous range of
-// quads; VEC: the input is 16-byte aligned.
+// quads (four symbols); a step loads kBcQuads 128-bit quads per thread
+// (warp-contiguous, the next step's in flight while this one counts), takes
+// each quad's following symbol from the next lane, and adds 16 pairs per
+// thread to the shared counters.  A step adds at most 16,384 to a counter,
+// so flushing after any step in which a counter reached 16,384 keeps every
+// counter below 32,769.  VEC: the input is 16-byte aligned.
 template <bool VEC>
 __global__ void __launch_bounds__(kBcThreads, 1) k_bcount(LP P) {
     extern __shared__ uint32_t bcnt[];
@@ -263,49 +261,53 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bcount(LP P) {
     if (threadIdx.x == 0) s_hot = 0;
     __syncthreads();
     const uint64_t per = (nq + gridDim.x - 1) / gridDim.x;
-    const uint64_t q0 = (uint64_t)blockIdx.x * per, q1 = min(nq, q0 + per);
+    const uint64_t q0 = (uint64_t)blockIdx.x * per;
+    // this CTA's quads, relative to q0 (a range is far below 2^32 quads)
+    const uint32_t nr = (uint32_t)(q0 < nq ? min(per, nq - q0) : 0);
+    const uint4 *in4 = reinterpret_cast<const uint4 *>(in) + q0;
+    const uint32_t *ins = in + 4 * q0;
+    const bool has_next = q0 + nr < nq || 4 * nq < n;   // a symbol follows the range's last quad
     uint32_t bad = 0;
     const int lane = threadIdx.x & 31;
-    constexpr uint64_t kStep = (uint64_t)kBcThreads * kBcQuads;   // quads per CTA step
-    // quad of thread t, slot u in a step: q = base + u * kBcThreads + t (a warp's lanes are consecutive)
+    constexpr uint32_t kStep = (uint32_t)kBcThreads * kBcQuads;   // quads per CTA step
     uint4 cur[kBcQuads], nxt[kBcQuads];
     uint32_t cnx[kBcQuads], nnx[kBcQuads];
-    auto load = [&](uint64_t base, uint4 *v, uint32_t *nx) {
+    // quad of thread t, slot u: base + u * kBcThreads + t; lane 31 (and the
+    // range's last quad) loads the following symbol itself
+    auto load = [&](uint32_t base, uint4 *v, uint32_t *nx) {
 #pragma unroll
         for (int u = 0; u < kBcQuads; u++) {
-            const uint64_t q = base + (uint64_t)u * kBcThreads + threadIdx.x;
-            if (q < q1) {
-                if (VEC) {
-                    v[u] = __ldcs(reinterpret_cast<const uint4 *>(in) + q);
-                } else {
-                    v[u] = make_uint4(in[4 * q], in[4 * q + 1], in[4 * q + 2], in[4 * q + 3]);
-                }
-                // lanes 0..30 take the next quad's first symbol from their neighbour
-                nx[u] = (lane == 31 || q + 1 >= q1) ? (4 * q + 4 < n ? __ldcs(in + 4 * q + 4) : kWordStart) : 0u;
-            } else {
-                v[u] = make_uint4(0, 0, 0, 0);
-                nx[u] = kWordStart;
-            }
+            const uint32_t q = base + u * kBcThreads + threadIdx.x;
+            const bool in_range = q < nr;
+            if (VEC) v[u] = in_range ? __ldcs(in4 + q) : make_uint4(0, 0, 0, 0);
+            else
+                v[u] = in_range ? make_uint4(ins[4 * q], ins[4 * q + 1], ins[4 * q + 2], ins[4 * q + 3])
+                                : make_uint4(0, 0, 0, 0);
+            nx[u] = kWordStart;
+            if (in_range && (lane == 31 || q + 1 == nr) && (q + 1 < nr || has_next)) nx[u] = __ldcs(ins + 4 * q + 4);
         }
     };
-    if (q0 < q1) load(q0, cur, cnx);
-    for (uint64_t base = q0; base < q1; base += kStep) {
-        const bool more = base + kStep < q1;
+    if (nr) load(0, cur, cnx);
+    for (uint32_t base = 0; base < nr; base += kStep) {
+        const bool more = base + kStep < nr;
         if (more) load(base + kStep, nxt, nnx);   // in flight while this step counts
-        bool hot = false;
+        uint32_t hot = 0;
 #pragma unroll
         for (int u = 0; u < kBcQuads; u++) {
-            const uint64_t q = base + (uint64_t)u * kBcThreads + threadIdx.x;
+            const uint32_t q = base + u * kBcThreads + threadIdx.x;
             const uint32_t right = __shfl_down_sync(kFull, cur[u].x, 1);
-            if (q < q1) {
-                const uint32_t a[5] = {cur[u].x, cur[u].y, cur[u].z, cur[u].w,
-                                       (lane == 31 || q + 1 >= q1) ? cnx[u] : right};
-                bc_quad(bcnt, a, 4, bad, hot);
+            const uint32_t nx = (lane == 31 || q + 1 == nr) ? cnx[u] : right;
+            if (q < nr) {
+                bad |= cur[u].x | cur[u].y | cur[u].z | cur[u].w;
+                bc_pair(bcnt, cur[u].x, cur[u].y, hot);
+                bc_pair(bcnt, cur[u].y, cur[u].z, hot);
+                bc_pair(bcnt, cur[u].z, cur[u].w, hot);
+                bc_pair(bcnt, cur[u].w, nx, hot);
             }
         }
-        if (hot) s_hot = 1;
+        if (hot & 0x40004000u) s_hot = 1;
         __syncthreads();
-        if (s_hot) {   // a counter passed kBcLimit: at most kStep * 4 more adds before the next check
+        if (s_hot) {
             bc_flush(bcnt, P.ecnt);
             __syncthreads();
             if (threadIdx.x == 0) s_hot = 0;
@@ -320,18 +322,15 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bcount(LP P) {
         }
     }
     if (blockIdx.x == 0 && threadIdx.x == 0) {   // the tail after the last full quad
+        uint32_t hot = 0;
         for (uint64_t i = 4 * nq; i < n; i++) {
-            const uint32_t s = in[i];
-            bad |= s & kBadBits;
-            if (i + 1 < n && !(in[i + 1] & kWordStart)) {
-                const uint32_t e = ((s & 0xFFu) << 8) | (in[i + 1] & 0xFFu);
-                atomicAdd(bcnt + (e >> 1), 1u << ((e & 1u) << 4));
-            }
+            bad |= in[i];
+            if (i + 1 < n) bc_pair(bcnt, in[i], in[i + 1], hot);
         }
     }
     __syncthreads();
     bc_flush(bcnt, P.ecnt);
-    if (bad) atomicOr(&P.st->err, LERR_BADINPUT);
+    if (bad & kBadBits) atomicOr(&P.st->err, LERR_BADINPUT);
 }
 
 // ----------------------------------------------------------- list base ---
@@ -1416,114 +1415,209 @@ __global__ void __launch_bounds__(kTlThreads, 1) k_ltail(LP P, uint32_t budget) 
 
 // ----------------------------------------------------------- compaction ---
 
-// The live symbols (bit 31 clear) in position order ([GPU-BPE] "What it
-// does" 3.: warp-level exclusive scans and decoupled look-back across CTAs).
-// A tile of kCpTile positions is read with coalesced 128-bit loads (warp w,
-// load j, lane L: positions 1024w + 128j + 4L .. +3); the live counts are
-// scanned per load with __shfl_up_sync and across warps in shared memory; the
-// tile's output offset comes from a warp-wide look-back over 32 predecessor
-// tiles per round trip (ticket order, bounded waits); survivors are staged
-// in shared memory in order and written out coalesced.
-__global__ void __launch_bounds__(kCpThreads) k_lcompact(LP P, uint32_t *out) {
-    constexpr int kLoads = kCpItems / 4;
-    __shared__ uint32_t s_tile, s_off, s_n;
-    __shared__ uint32_t s_warp[kCpThreads / 32 + 1];
-    __shared__ __align__(16) uint32_t stage[kCpTile];
-    LState *st = P.st;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    if (threadIdx.x == 0) s_tile = atomicAdd(&st->cp_ticket, 1u);
-    __syncthreads();
-    const uint32_t t = s_tile;
-    const uint64_t n = P.n, wbase = (uint64_t)t * kCpTile + (uint64_t)w * (kCpTile / (kCpThreads / 32));
-    uint4 v[kLoads];
-    uint32_t cnt[kLoads];
-#pragma unroll
-    for (int j = 0; j < kLoads; j++) {
-        const uint64_t p = wbase + 128u * j + 4u * lane;
-        if (p + 4 <= n) {
-            v[j] = __ldcs(reinterpret_cast<const uint4 *>(P.sym + p));
-        } else {
-            v[j].x = p < n ? P.sym[p] : kDead;
-            v[j].y = p + 1 < n ? P.sym[p + 1] : kDead;
-            v[j].z = p + 2 < n ? P.sym[p + 2] : kDead;
-            v[j].w = p + 3 < n ? P.sym[p + 3] : kDead;
-        }
-        cnt[j] = ((v[j].x & kDead) ? 0u : 1u) + ((v[j].y & kDead) ? 0u : 1u) + ((v[j].z & kDead) ? 0u : 1u) +
-                 ((v[j].w & kDead) ? 0u : 1u);
-    }
-    // offsets inside the warp, in position order (load, lane, item)
-    uint32_t off[kLoads], run = 0;
-#pragma unroll
-    for (int j = 0; j < kLoads; j++) {
-        const uint32_t incl = warp_incl_sum(cnt[j], lane);
-        off[j] = run + incl - cnt[j];
-        run += __shfl_sync(kFull, incl, 31);
-    }
-    if (lane == 0) s_warp[w] = run;
+// Grid barrier of a cooperative launch with a bounded wait (false, and
+// DERR_TIMEOUT in *err, when it gives up).  Two levels: CTA b arrives at
+// counter b % kGbGroups; the last arrival of a group arrives at the top
+// counter, whose last arrival bumps the generation the others poll.  Every
+// word sits on its own 128-byte line: bar[32 * g] for group g, bar[32 *
+// kGbGroups] the top counter, bar[32 * (kGbGroups + 1)] the generation.
+constexpr int kGbGroups = 16;
+constexpr size_t kGbWords = 32 * (kGbGroups + 2);
+__device__ __forceinline__ bool grid_barrier(uint32_t *bar, uint32_t *err, int *s_ok) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        uint32_t a = 0;
-        for (int i = 0; i < kCpThreads / 32; i++) {
-            const uint32_t x = s_warp[i];
-            s_warp[i] = a;
-            a += x;
+        uint32_t *top = bar + 32 * kGbGroups, *gen_w = top + 32;
+        const uint32_t G = gridDim.x, g = blockIdx.x % kGbGroups;
+        const uint32_t ngroups = G < (uint32_t)kGbGroups ? G : (uint32_t)kGbGroups;
+        const uint32_t gsize = (G - g + kGbGroups - 1) / kGbGroups;   // CTAs b < G with b % kGbGroups == g
+        const uint32_t gen = ld_acquire_u32(gen_w);
+        __threadfence();
+        int ok = 1;
+        if (atomicAdd(bar + 32 * g, 1u) == gsize - 1) {
+            atomicExch(bar + 32 * g, 0u);
+            if (atomicAdd(top, 1u) == ngroups - 1) {
+                atomicExch(top, 0u);
+                __threadfence();
+                st_release_u32(gen_w, gen + 1);
+            }
         }
-        s_warp[kCpThreads / 32] = a;
+        unsigned spins = 0;
+        while (ld_acquire_u32(gen_w) == gen) {
+            if (++spins > kSpinLimit) {
+                atomicOr(err, DERR_TIMEOUT);
+                ok = 0;
+                break;
+            }
+            if (spins > 4) __nanosleep(64);
+        }
+        __threadfence();
+        *s_ok = ok;
     }
     __syncthreads();
-    const uint32_t total = s_warp[kCpThreads / 32];
-    // the tile's offset: status word flag << 62 | value (1: the tile's count, 2: inclusive prefix)
-    unsigned long long *cs = P.cstat;
-    if (w == 0) {
-        uint32_t excl = 0;
-        if (t == 0) {
-            if (lane == 0) st_relaxed(cs, (2ull << 62) | total);
-        } else {
-            if (lane == 0) st_relaxed(cs + t, (1ull << 62) | total);
-            int64_t j = (int64_t)t - 1;
-            unsigned spins = 0;
-            for (;;) {
-                const int64_t idx = j - lane;
-                const unsigned long long x = idx >= 0 ? ld_relaxed(cs + idx) : (2ull << 62);
-                const uint32_t f = (uint32_t)(x >> 62);
-                const unsigned pm = __ballot_sync(kFull, f == 2), zm = __ballot_sync(kFull, f == 0);
-                const int fp = pm ? __ffs(pm) - 1 : 32;   // nearest predecessor with its prefix
-                const unsigned need = fp == 32 ? kFull : (fp == 31 ? kFull : ((2u << fp) - 1u));
-                if (zm & need) {
-                    if (++spins > kSpinLimit) {
-                        if (lane == 0) atomicOr(&st->err, DERR_TIMEOUT);
-                        break;
-                    }
-                    continue;
-                }
-                uint32_t val = lane <= fp ? (uint32_t)(x & 0xFFFFFFFFull) : 0u;
+    return *s_ok != 0;
+}
+
+__device__ __forceinline__ uint32_t live4(uint4 v) {
+    return 4u - ((v.x >> 31) + (v.y >> 31) + (v.z >> 31) + (v.w >> 31));
+}
+
+// The live symbols (bit 31 clear) in position order ([GPU-BPE] "What it
+// does" 3.: warp-level exclusive scans of the keep flags, offsets across
+// CTAs, a scatter).  One cooperative launch (all CTAs resident) walks the
+// stream in rounds of kCsRound positions, small enough to stay in L2 between
+// the round's two passes, so HBM sees each symbol read once and each
+// survivor written once.  A round is split into warp tiles of 512 positions
+// (four 128-bit loads per lane), dealt out as contiguous slices, one per CTA:
+//   pass 1  every warp counts the live symbols of its tiles (loads kept in
+//           L2) and records each tile's count; each CTA publishes its total;
+//   barrier (grid-wide, bounded wait)
+//   pass 2  each CTA adds up the totals of the CTAs before it (its output
+//           offset) and of all CTAs (the round's total); one warp scans the
+//           slice's tile counts into tile offsets; then every warp, on its
+//           own, re-reads its tiles from L2, places each lane's survivors
+//           with a __shfl_up_sync scan, stages them in a warp-private shared
+//           buffer and writes them out coalesced.
+// The decoupled look-back of the single-pass form is not used here: with
+// every CTA resident and working through tiles in step, each tile read the
+// status words of all the tiles before it in its step, and that traffic on a
+// few L2 lines, not HBM, set the pace.
+__global__ void __launch_bounds__(kCsThreads) k_lcompact(LP P, uint32_t *out) {
+    constexpr int kWarps = kCsThreads / 32;
+    constexpr uint32_t kWT = 512;                       // positions per warp tile
+    constexpr uint32_t kMaxTiles = kCsRound / kWT;      // warp tiles of a round
+    __shared__ __align__(16) uint32_t stage[kWarps][kWT];
+    __shared__ uint32_t s_toff[2048];                   // a slice's tile offsets (a slice has at most 2,048 tiles)
+    // two tiles per warp and step (tiles t and t + kWarps): eight loads in flight per lane
+    __shared__ uint32_t s_warp[kWarps];
+    __shared__ unsigned long long s_red[kWarps][2];
+    __shared__ int s_ok;
+    LState *st = P.st;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint64_t n = P.n;
+    const uint32_t G = gridDim.x, c = blockIdx.x;
+    uint64_t out_base = 0;   // survivors of the earlier rounds (the same in every CTA)
+    uint32_t par = 0;
+    auto load = [&](uint64_t i, uint64_t end) -> uint4 {   // four positions, dead past end
+        if (i + 4 <= end) return __ldcg(reinterpret_cast<const uint4 *>(P.sym + i));
+        uint4 v;
+        v.x = i < end ? __ldcg(P.sym + i) : kDead;
+        v.y = i + 1 < end ? __ldcg(P.sym + i + 1) : kDead;
+        v.z = i + 2 < end ? __ldcg(P.sym + i + 2) : kDead;
+        v.w = i + 3 < end ? __ldcg(P.sym + i + 3) : kDead;
+        return v;
+    };
+    for (uint64_t r0 = 0; r0 < n; r0 += kCsRound, par ^= 1u) {
+        const uint64_t rend = min(n, r0 + kCsRound);
+        const uint32_t nt = (uint32_t)((rend - r0 + kWT - 1) / kWT);   // warp tiles of the round
+        const uint32_t per = (nt + G - 1) / G;                          // tiles per slice
+        const uint32_t w0 = min(nt, c * per), w1 = min(nt, w0 + per);  // this CTA's tiles
+        uint32_t *tcnt = P.ctile + (uint64_t)par * kMaxTiles;
+        // pass 1: live count of each of the slice's tiles
+        uint32_t cta = 0;
+        for (uint32_t t = w0 + w; t < w1; t += 2 * kWarps) {
+            const bool two = t + kWarps < w1;
+            const uint64_t b = r0 + (uint64_t)t * kWT + 4 * lane, b2 = b + (uint64_t)kWarps * kWT;
+            uint4 v[8];
 #pragma unroll
-                for (int d = 16; d > 0; d >>= 1) val += __shfl_xor_sync(kFull, val, d);
-                excl += val;
-                if (fp < 32) break;
-                j -= 32;
+            for (int j = 0; j < 4; j++) {
+                v[j] = load(b + 128 * j, rend);
+                v[4 + j] = two ? load(b2 + 128 * j, rend) : make_uint4(kDead, kDead, kDead, kDead);
             }
-            if (lane == 0) st_relaxed(cs + t, (2ull << 62) | (unsigned long long)(excl + total));
+            uint32_t k = live4(v[0]) + live4(v[1]) + live4(v[2]) + live4(v[3]);
+            uint32_t k2 = live4(v[4]) + live4(v[5]) + live4(v[6]) + live4(v[7]);
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) {
+                k += __shfl_xor_sync(kFull, k, d);
+                k2 += __shfl_xor_sync(kFull, k2, d);
+            }
+            if (lane == 0) {
+                tcnt[t] = k;
+                if (two) tcnt[t + kWarps] = k2;
+            }
+            cta += k + k2;
+        }
+        if (lane == 0) s_warp[w] = cta;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            uint32_t a = 0;
+            for (int i = 0; i < kWarps; i++) a += s_warp[i];
+            P.ctot[par * G + c] = a;
+        }
+        if (!grid_barrier(P.cbar, &st->err, &s_ok)) return;
+        // pass 2: this CTA's offset and the round's total
+        unsigned long long before = 0, all = 0;
+        for (uint32_t i = threadIdx.x; i < G; i += kCsThreads) {
+            const uint32_t v = __ldcg(P.ctot + par * G + i);
+            all += v;
+            if (i < c) before += v;
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+            before += __shfl_xor_sync(kFull, before, d);
+            all += __shfl_xor_sync(kFull, all, d);
         }
         if (lane == 0) {
-            s_off = excl;
-            s_n = total;
+            s_red[w][0] = before;
+            s_red[w][1] = all;
         }
-    }
-    // survivors into the stage, in order
-    const uint32_t wo = s_warp[w];
+        // the slice's tile offsets (warp 0, 32 tiles per step)
+        if (w == 0) {
+            uint32_t carry = 0;
+            for (uint32_t t0 = w0; t0 < w1; t0 += 32) {
+                const uint32_t t = t0 + lane;
+                const uint32_t k = t < w1 ? __ldcg(tcnt + t) : 0u;
+                const uint32_t incl = warp_incl_sum(k, lane);
+                if (t < w1) s_toff[t - w0] = carry + incl - k;
+                carry += __shfl_sync(kFull, incl, 31);
+            }
+        }
+        __syncthreads();
+        before = 0;
+        all = 0;
+        for (int i = 0; i < kWarps; i++) {
+            before += s_red[i][0];
+            all += s_red[i][1];
+        }
+        const uint64_t cbase = out_base + before;
+        // every warp compacts its tiles on its own
+        uint4 nv[4];
+        const uint32_t tw = w0 + w;
+        if (tw < w1)
 #pragma unroll
-    for (int j = 0; j < kLoads; j++) {
-        uint32_t o = wo + off[j];
-        if (!(v[j].x & kDead)) stage[o++] = v[j].x;
-        if (!(v[j].y & kDead)) stage[o++] = v[j].y;
-        if (!(v[j].z & kDead)) stage[o++] = v[j].z;
-        if (!(v[j].w & kDead)) stage[o++] = v[j].w;
+            for (int j = 0; j < 4; j++) nv[j] = load(r0 + (uint64_t)tw * kWT + 4 * lane + 128 * j, rend);
+        for (uint32_t t = tw; t < w1; t += kWarps) {
+            uint4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) v[j] = nv[j];
+            if (t + kWarps < w1)   // the warp's next tile is in flight meanwhile
+#pragma unroll
+                for (int j = 0; j < 4; j++) nv[j] = load(r0 + (uint64_t)(t + kWarps) * kWT + 4 * lane + 128 * j, rend);
+            uint32_t off[4], run = 0;
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const uint32_t k = live4(v[j]);
+                const uint32_t incl = warp_incl_sum(k, lane);
+                off[j] = run + incl - k;
+                run += __shfl_sync(kFull, incl, 31);
+            }
+            uint32_t *sg = stage[w];
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                uint32_t o = off[j];
+                if (!(v[j].x & kDead)) sg[o++] = v[j].x;
+                if (!(v[j].y & kDead)) sg[o++] = v[j].y;
+                if (!(v[j].z & kDead)) sg[o++] = v[j].z;
+                if (!(v[j].w & kDead)) sg[o++] = v[j].w;
+            }
+            __syncwarp();
+            uint32_t *dst = out + cbase + s_toff[t - w0];
+            for (uint32_t i = lane; i < run; i += 32) __stcs(dst + i, sg[i]);
+            __syncwarp();
+        }
+        out_base += all;
+        __syncthreads();   // s_toff and s_red are rewritten by the next round
     }
-    __syncthreads();
-    const uint32_t base = s_off, cnt_all = s_n;
-    for (uint32_t i = threadIdx.x; i < cnt_all; i += kCpThreads) out[(uint64_t)base + i] = stage[i];
-    if (t == gridDim.x - 1 && threadIdx.x == 0) st->live = (unsigned long long)base + cnt_all;
+    if (c == 0 && threadIdx.x == 0) st->live = out_base;
 }
 
 // ---------------------------------------------------------------- host ---
@@ -1810,21 +1904,32 @@ int train_lists(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_
     *n_done = done;
     // ---- the final stream
     uint64_t nf = n;
-    void *cst = nullptr;
-    const uint64_t ntiles = (n + kCpTile - 1) / kCpTile;
     if (d_symbols_final || n_final) {
-        if ((rc = ensure(ctx, S_L_CSTAT, ntiles * 8, &cst))) return rc;
-        P.cstat = (unsigned long long *)cst;
-        BPE_CUDA(ctx, cudaMemsetAsync(cst, 0, ntiles * 8, s), "status clear");
-        BPE_CUDA(ctx, cudaMemsetAsync(&P.st->cp_ticket, 0, 4, s), "ticket clear");
+        int cpb = 1;
+        BPE_CUDA(ctx, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cpb, k_lcompact, kCsThreads, 0),
+                 "k_lcompact occupancy");
+        // every CTA resident: a cooperative launch (the grid barrier needs it)
+        const unsigned cp_grid = (unsigned)ctx->sm_count * (unsigned)std::max(cpb, 1);
+        if ((kCsRound / 512 + cp_grid - 1) / cp_grid > 2048)   // a slice's tile offsets fit the shared table
+            return fail(ctx, BPE_ERR_CUDA, "bpe_train: %u CTAs are too few for the compaction", cp_grid);
+        void *ctot, *cbar, *ctile;
+        if ((rc = ensure(ctx, S_L_CSTAT, 2ull * cp_grid * 4, &ctot)) ||
+            (rc = ensure(ctx, S_L_CBAR, kGbWords * 4, &cbar)) ||
+            (rc = ensure(ctx, S_L_CTILE, 2ull * (kCsRound / 512) * 4, &ctile)))
+            return rc;
+        P.ctot = (uint32_t *)ctot;
+        P.ctile = (uint32_t *)ctile;
+        P.cbar = (uint32_t *)cbar;
+        BPE_CUDA(ctx, cudaMemsetAsync(cbar, 0, kGbWords * 4, s), "barrier clear");
         uint32_t *out = d_symbols_final ? d_symbols_final : P.pe;   // length only: the pair entries are done with
         ev(3);
-        k_lcompact<<<(unsigned)ntiles, kCpThreads, 0, s>>>(P, out);
-        BPE_CUDA(ctx, cudaGetLastError(), "compaction launch");
+        void *cargs[] = {&P, &out};
+        BPE_CUDA(ctx, cudaLaunchCooperativeKernel((const void *)k_lcompact, cp_grid, kCsThreads, cargs, 0, s),
+                 "compaction launch");
         ev(4);
         BPE_CUDA(ctx, cudaMemcpyAsync(h_state, state, sizeof *h_state, cudaMemcpyDeviceToHost, s), "state read");
         BPE_CUDA(ctx, cudaStreamSynchronize(s), "final sync");
-        if (h_state->err & DERR_TIMEOUT) return fail(ctx, BPE_ERR_TIMEOUT, "bpe_train: a look-back wait gave up");
+        if (h_state->err & DERR_TIMEOUT) return fail(ctx, BPE_ERR_TIMEOUT, "bpe_train: a grid barrier wait gave up");
         nf = h_state->live;
     }
     if (n_final) *n_final = nf;
