@@ -235,15 +235,18 @@ struct ByteWin {
 //   MODE 0 (speculative): mark token starts in bits (offsets from cs) and,
 //          when sid is not null, store each token to sid[0 ...]: its id when
 //          it is one byte long (from the root LUT), else 0x80000000 | its
-//          trie slot, so the id lookup leaves the parse's critical path
+//          trie slot, so the id lookup leaves the parse's critical path.
+//          Tokens gather in the thread's column of shared memory (stage,
+//          stride kBS) and go out eight at a time as one whole 32-byte
+//          sector (sid is 32-byte aligned); the caller flushes the rest
 //   MODE 1 (resync): stop early where a token start is already marked
 //   MODE 2 (emit): write ids to ids[o ...] (below cap)
 //   MODE 3 (emit head): MODE 2's writes, stopping like MODE 1
-// Returns the position after the last token; *cnt = tokens parsed (MODE 1
-// and 3: tokens up to the meeting point, *met = whether it met the marked
-// path).
+// Returns the position after the last token as an offset from cs; *cnt =
+// tokens parsed (MODE 1 and 3: tokens up to the meeting point, *met = whether
+// it met the marked path).
 template <int MODE, int L = 0>
-__device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 *lut, uint64_t p_abs, uint64_t ce_abs,
+__device__ __forceinline__ uint32_t parse_tokens(const EncParams &P, const int4 *lut, uint64_t p_abs, uint64_t ce_abs,
                                                  uint64_t de_abs, uint64_t cs, uint32_t *bits, uint32_t *cnt,
                                                  unsigned long long o, bool *met, int32_t *sid = nullptr) {
     constexpr bool kMeet = MODE == 1 || MODE == 3, kWrite = MODE == 2 || MODE == 3;
@@ -256,7 +259,7 @@ __device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 
         if ((bits[(p >> 5) * kBS] >> (p & 31)) & 1u) {
             *met = true;
             *cnt = 0;
-            return p_abs;
+            return p;
         }
     }
     ByteWin byte{P.bytes + cs};
@@ -264,6 +267,8 @@ __device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 
     uint32_t y = 0, blen = 0;     // base|TERM of node; length of the best token so far
     int32_t bnode = -1, btid = 0; // best token: its slot (id in tid[]) or, at depth 1, its id
     uint32_t q = p;
+    uint32_t bw = 0;              // MODE 0: token starts in the word of the current token's start
+    uint32_t *const stage = bits - 8 * kBS;   // MODE 0: the eight staged tokens sit just before bits
     // a token's first step, through the shared LUT (every byte is a token)
     auto root_step = [&](uint32_t ch) {
         const int4 r = lut[ch];
@@ -295,14 +300,25 @@ __device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 
             }
         } else {   // the token [p, p + blen) ends here; the next one starts in the same step
             if (MODE == 0) {
-                bits[(p >> 5) * kBS] |= 1u << (p & 31);
-                if (sid) sid[c] = bnode >= 0 ? (int32_t)(0x80000000u | (uint32_t)bnode) : btid;
+                bw |= 1u << (p & 31);
+                if (sid) {
+                    stage[(c & 7u) * kBS] = bnode >= 0 ? 0x80000000u | (uint32_t)bnode : (uint32_t)btid;
+                    if ((c & 7u) == 7u) {   // a whole sector
+                        uint4 *d = reinterpret_cast<uint4 *>(sid + (c & ~7u));
+                        d[0] = make_uint4(stage[0], stage[kBS], stage[2 * kBS], stage[3 * kBS]);
+                        d[1] = make_uint4(stage[4 * kBS], stage[5 * kBS], stage[6 * kBS], stage[7 * kBS]);
+                    }
+                }
             }
             if (kWrite && o < P.cap) P.ids[o] = bnode >= 0 ? __ldg(P.tid + bnode) : btid;
             ++o;
             ++c;
             const bool at_q = load && p + blen == q;   // the failed byte starts the next token
             p += blen;
+            if (MODE == 0 && ((p ^ (p - blen)) >> 5)) {   // the next token starts in a later word
+                bits[((p - blen) >> 5) * kBS] = bw;
+                bw = 0;
+            }
             if (kMeet && p < ce) {
                 if ((bits[(p >> 5) * kBS] >> (p & 31)) & 1u) {
                     *met = true;
@@ -312,11 +328,16 @@ __device__ __forceinline__ uint64_t parse_tokens(const EncParams &P, const int4 
             if (p < ce) root_step(at_q ? ch : byte(p));
         }
     }
+    if (MODE == 0 && bw) bits[((p - blen) >> 5) * kBS] = bw;   // the last token's word
     *cnt = c;
-    return cs + p;
+    return p;
 }
 
-__host__ __device__ __forceinline__ size_t spec_smem_for(uint32_t C) { return (size_t)kSpecThreads * (C / 32) * 4; }
+// k_spec's dynamic shared memory: the token-start bitmaps, then 8 staged
+// tokens per thread (both one column per thread)
+__host__ __device__ __forceinline__ size_t spec_smem_for(uint32_t C) {
+    return (size_t)kSpecThreads * (C / 32) * 4 + (size_t)kSpecThreads * 8 * 4;
+}
 __host__ __device__ __forceinline__ size_t emit_smem_for(uint32_t C) { return (size_t)kEmitThreads * (C / 32) * 4; }
 // Stored speculative ids take 4 bytes per input byte; above this the emit
 // pass re-parses instead (also when the allocation fails).
@@ -373,59 +394,61 @@ __global__ void __launch_bounds__(1024) k_chunk_index(EncParams P, unsigned long
 
 template <int L>
 __global__ void __launch_bounds__(kSpecThreads, 8) k_spec(EncParams P, unsigned long long n_chunks, uint64_t text_end) {
-    extern __shared__ uint32_t s_bits[];   // kSpecThreads x (C/32) token-start bitmaps
+    extern __shared__ uint32_t s_bits[];   // 8 staged tokens, then the C/32-word token-start bitmap: a column per thread
     __shared__ int4 lut[256];
-    __shared__ unsigned long long s_exit[kSpecThreads];
+    __shared__ uint32_t s_exit[kSpecThreads];   // each chunk's spec exit, from its start
     const int tid = threadIdx.x;
     const uint32_t words = P.chunk >> 5;
-    uint32_t *bits = s_bits + tid;
+    uint32_t *stage = s_bits + tid, *bits = stage + 8 * kBS;
     const long long k = (long long)blockIdx.x * (kSpecThreads - 1) + tid - 1;
     const bool live = k >= 0 && (unsigned long long)k < n_chunks;
     load_lut(P, lut);
 
-    ChunkGeo g{0, 0, 0, true};
-    if (live) g = chunk_geo(P, (unsigned long long)k);
     __syncthreads();
 
-    uint32_t spec_count = 0;
-    uint64_t spec_exit = 0;
+    uint32_t spec_count = 0, spec_rel = 0;
     if (live) {
+        const ChunkGeo g = chunk_geo(P, (unsigned long long)k);
         for (uint32_t w = 0; w < words; w++) bits[w * kBS] = 0;
         int32_t *sid = P.sids ? P.sids + (size_t)k * P.chunk : nullptr;
-        spec_exit = parse_tokens<0, L>(P, lut, g.cs, g.ce, g.de, g.cs, bits, &spec_count, 0, nullptr, sid);
+        spec_rel = parse_tokens<0, L>(P, lut, g.cs, g.ce, g.de, g.cs, bits, &spec_count, 0, nullptr, sid);
+        if (sid)   // the last partial sector
+            for (uint32_t i = spec_count & ~7u; i < spec_count; i++) sid[i] = (int32_t)stage[(i & 7u) * kBS];
         if (P.sbits)
             for (uint32_t w = 0; w < words; w++) P.sbits[(size_t)k * words + w] = bits[w * kBS];
     }
-    s_exit[tid] = spec_exit;
+    s_exit[tid] = spec_rel;
     __syncthreads();
     if (!live || tid == 0) return;   // the halo thread only supplied its exit
 
-    uint32_t count;
-    uint64_t exit;
+    // the geometry again: reloaded rather than held in registers through the parse
+    const ChunkGeo g = chunk_geo(P, (unsigned long long)k);
+    uint32_t count, exit_rel;
     if (g.doc_first) {
         count = spec_count;
-        exit = spec_exit;
+        exit_rel = spec_rel;
     } else {
         // re-parse from the nominal entry (previous chunk's spec exit) until the
         // two paths meet; from there the rest of the chunk is the spec path
         bool met = false;
         uint32_t c = 0;
-        const uint64_t q = parse_tokens<1, L>(P, lut, s_exit[tid - 1], g.ce, g.de, g.cs, bits, &c, 0, &met);
+        const uint32_t q =
+            parse_tokens<1, L>(P, lut, (g.cs - P.chunk) + s_exit[tid - 1], g.ce, g.de, g.cs, bits, &c, 0, &met);
         if (met) {
-            const uint32_t o = (uint32_t)(q - g.cs);
+            const uint32_t o = q;
             uint32_t rest = __popc(bits[(o >> 5) * kBS] >> (o & 31));
             for (uint32_t w = (o >> 5) + 1; w < words; w++) rest += __popc(bits[w * kBS]);
             c += rest;
-            exit = spec_exit;
+            exit_rel = spec_rel;
         } else {
-            exit = q;
+            exit_rel = q;
         }
         count = c;
     }
     P.count[k] = count;
-    P.exit_rel[k] = (uint32_t)(exit - g.cs);
-    P.spec_rel[k] = (uint32_t)(spec_exit - g.cs);
-    if (exit != spec_exit) {
+    P.exit_rel[k] = exit_rel;
+    P.spec_rel[k] = spec_rel;
+    if (exit_rel != spec_rel) {
         atomicOr(P.flag + (k >> 5), 1u << (k & 31));
         P.st->any_flag = 1u;
         const uint32_t i = atomicAdd(&P.st->flist_len, 1u);
@@ -665,9 +688,8 @@ __global__ void __launch_bounds__(kEmitThreads) k_emit(EncParams P, unsigned lon
         }
         const uint64_t e = g.doc_first ? g.cs : (g.cs - P.chunk) + P.exit_rel[k - 1];
         bool met = false;
-        const uint64_t q = parse_tokens<3, L>(P, lut, e, g.ce, g.de, g.cs, bits, &c_head, o, &met);
-        if (met) {   // spec tokens before offset q - cs are skipped
-            const uint32_t off = (uint32_t)(q - g.cs);
+        const uint32_t off = parse_tokens<3, L>(P, lut, e, g.ce, g.de, g.cs, bits, &c_head, o, &met);
+        if (met) {   // spec tokens before offset off are skipped
             uint32_t before = 0;
             for (uint32_t w = 0; w < (off >> 5); w++) before += __popc(bits[w * kBS]);
             before += __popc(bits[(off >> 5) * kBS] & ((1u << (off & 31)) - 1u));
@@ -936,15 +958,16 @@ extern "C" int trie_encode(bpe_ctx *ctx, const bpe_trie *trie, const uint8_t *d_
     const uint64_t total = h->total;
     *n_ids = total;
 
-    // statistics: the spec parse and the emit pass each read the input once;
-    // emit writes 4 bytes per id
+    // statistics, in the encode's algorithmic bytes (the input once, 4 bytes
+    // per id and 8 per document offset): the spec parse is charged the input,
+    // the emit pass the ids and offsets it writes
     const int a = stats_slot(ctx, "encode_spec"), b = stats_slot(ctx, "encode_emit");
     ctx->stats.k[a].launches = 1;
     ctx->stats.k[b].launches = 1;
     const uint64_t in_bytes = h->span;
     ctx->stats.kernel_launches = 6;
     ctx->stats.k[a].bytes = (double)in_bytes;
-    ctx->stats.k[b].bytes = (double)in_bytes + 4.0 * (double)total;
+    ctx->stats.k[b].bytes = 4.0 * (double)total + 8.0 * ((double)n_docs + 1.0);
     if (profile) {
         float x = 0, y = 0, z = 0;
         cudaEventElapsedTime(&x, ctx->events[2], ctx->events[3]);

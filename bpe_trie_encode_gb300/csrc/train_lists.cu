@@ -1801,11 +1801,6 @@ int train_lists(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_
              "k_lscan smem attribute");
     BPE_CUDA(ctx, cudaFuncSetAttribute(k_ltail, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(TlShared)),
              "k_ltail smem attribute");
-    // one shared-memory carveout for the three kernels of the loop, so the
-    // SMs need not be reconfigured between them
-    BPE_CUDA(ctx, cudaFuncSetAttribute(k_ltail, cudaFuncAttributePreferredSharedMemoryCarveout, 100), "carveout");
-    BPE_CUDA(ctx, cudaFuncSetAttribute(k_lscan, cudaFuncAttributePreferredSharedMemoryCarveout, 100), "carveout");
-    BPE_CUDA(ctx, cudaFuncSetAttribute(k_lapply, cudaFuncAttributePreferredSharedMemoryCarveout, 100), "carveout");
     const uint64_t nq = n / 4;
     const unsigned bc_grid =
         (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(ctx->sm_count, (nq + 4095) / 4096));
