@@ -5,10 +5,11 @@ stream and device pointers by an application that owns all device memory, or
 a latency-critical path that must not pay the synchronisation of cudaFree.
 For them the library offers one entry point whose scratch is a fixed array
 compiled into the library.  This test calls it through the C ABI and checks
-it against trie_encode, bit for bit, on two calls in a row (the second on a
-smaller, different input, so stale contents of the shared array would show),
-and checks that an input beyond its stated maximum is refused.  It lives in
-a file of its own that pytest collects last.
+it against trie_encode and the oracle's greedy encode, bit for bit, on two
+calls in a row (the second on a smaller, different input, so stale contents
+of the shared array would show), and checks that inputs beyond either stated
+maximum (documents, chunks) are refused before any write.  It lives in a file
+of its own that pytest collects last.
 """
 import ctypes
 
@@ -49,6 +50,7 @@ def test_noalloc_encode_matches_trie_encode():
     merges, _ = oracle.train_words(oracle.pretokenize(synth.corpus("tiny")), 256)
     vb, off = oracle.vocab_from_merges(merges)
     trie = ctx.trie_build(vb, off)
+    otrie = oracle.Trie(vb, off)
     lex = synth.lexicon("tiny")
     inputs = [
         [lex.corpus(100 + d, 40000 + 977 * d).tobytes() for d in range(40)],       # ~1.9 MB, 40 docs
@@ -62,6 +64,9 @@ def test_noalloc_encode_matches_trie_encode():
         assert rc == 0
         assert torch.equal(ids, want_ids)
         assert torch.equal(id_off, want_off)
+        o_ids, o_off = otrie.encode(b"".join(docs), doc_off.cpu().numpy())
+        assert np.array_equal(ids.cpu().numpy(), o_ids)
+        assert np.array_equal(id_off.cpu().numpy().astype(np.uint64), o_off)
 
     # documents whose parses flip parity at their first byte flag one chunk
     # each: the repair runs from the flag list, then past its capacity
@@ -80,4 +85,21 @@ def test_noalloc_encode_matches_trie_encode():
     many = torch.zeros(65538, dtype=torch.int64, device="cuda")
     rc, _, id_off = _noalloc(lib, trie, data, many, 16)
     assert rc == -1 and int(id_off[0]) == -7
+
+    # within the document limit but beyond the chunk limit: 65,536 documents
+    # of 1,025 bytes take 9 chunks of 128 bytes each, 589,824 > 524,288
+    big = torch.full((65536 * 1025,), ord("a"), dtype=torch.uint8, device="cuda")
+    big_off = torch.arange(0, 65537, dtype=torch.int64, device="cuda") * 1025
+    rc, ids, id_off = _noalloc(lib, trie, big, big_off, 64)
+    assert rc == -1 and ids.numel() == 0
+    assert bool((id_off == -7).all())
+    # one document fewer is still refused (589,815 chunks); at 58,254
+    # documents (524,286 chunks) the same bytes are accepted
+    rc, _, _ = _noalloc(lib, trie, big, big_off[:65536], 64)
+    assert rc == -1
+    ok_off = big_off[:58255]
+    rc, ids, id_off = _noalloc(lib, trie, big, ok_off, big.numel())
+    assert rc == 0
+    want_ids, want_off = ctx.encode(trie, big, ok_off)
+    assert torch.equal(ids, want_ids) and torch.equal(id_off, want_off)
     ctx.close()
