@@ -303,8 +303,14 @@ def extra_legs(args, ctx, dev, stream, flush, peak, peak_kind):
     kern = {}
     add_stats(kern, ctx.stats())
     ctx.set_option(bt.BPE_OPT_PROFILE, 0)
+    call_bytes = data.size + 4 * int(r[0].numel()) + 8 * doc_off.size
+    call_gbs = call_bytes / (ms_all / args.steps / 1e3) / 1e9
     out["encode_batch"] = {"value": round(args.steps * data.size / (ms_all / 1e3) / 1e9, 3), "unit": "GB/s",
                            "ms_per_step": round(ms_all / args.steps, 3),
+                           "roofline": {"kernel": "trie_encode (whole call)", "bound": "hbm",
+                                        "achieved": round(call_gbs, 1), "peak": peak, "unit": "GB/s",
+                                        "frac": round(call_gbs / peak, 4), "peak_kind": f"of {peak_kind}",
+                                        "algorithmic_bytes_per_call": int(call_bytes)},
                            "workload": f"{doc_off.size - 1} documents, {data.size} B, 250,000-token substring vocabulary",
                            "n_ids": int(r[0].numel()), "trie": trie.info(),
                            "rooflines": {f: kernel_roofline(kern, f, peak, peak_kind, {})
@@ -588,6 +594,17 @@ def run_ours(args, rank, world, local_rank):
         if enc:   # pinned host outputs of the end-to-end encode
             h_ids_buf = torch.empty(enc["bytes"], dtype=torch.int32, pin_memory=True)
             h_ioff_buf = torch.empty(enc["h_off"].numel(), dtype=torch.int64)
+        link = None
+        if enc:   # the host link's own copy speed in this run: what bounds the end-to-end encode
+            n_cp = max(acc["n_ids"], 1)
+            h2d, d2h = [], []
+            for _ in range(3):
+                _, ms = timed(stream, lambda: enc["d"].copy_(enc["h"], non_blocking=True))
+                h2d.append(enc["bytes"] / (ms / 1e3) / 1e9)
+                _, ms = timed(stream, lambda: h_ids_buf[:n_cp].copy_(enc["ids"][:n_cp], non_blocking=True))
+                d2h.append(4 * n_cp / (ms / 1e3) / 1e9)
+            link = {"h2d_GBs": round(sorted(h2d)[1], 1), "d2h_GBs": round(sorted(d2h)[1], 1),
+                    "copy_bound_ms": round(max(enc["bytes"] / sorted(h2d)[1], 4 * n_cp / sorted(d2h)[1]) / 1e6, 3)}
         tr_ms = en_ms = 0.0
         d2h_ids = 0
         en_steps = []
@@ -619,7 +636,10 @@ def run_ours(args, rank, world, local_rank):
             e2e["encode"] = {"value": round(throughput(e2e_bytes, en_ms) / 1e9, 3), "unit": "GB/s",
                              "steps_ms": en_steps,
                              "median_GBs": round(enc["bytes"] / (sorted(en_steps)[len(en_steps) // 2] / 1e3) / 1e9, 3)
-                             if en_steps else None}
+                             if en_steps else None,
+                             "mean_over_median": round((sum(en_steps) / len(en_steps)) /
+                                                       sorted(en_steps)[len(en_steps) // 2], 3) if en_steps else None,
+                             "host_link": link}
 
     # ---- extra legs: other training sizes, the word-frequency trainer (same
     # merges), the batch encode workload, Unigram
@@ -674,8 +694,16 @@ def run_ours(args, rank, world, local_rank):
     out.update(extra)
     if enc:
         gbs = throughput(enc_bytes_total, enc_ms) / 1e9
+        # the whole call against HBM: its algorithmic bytes are the input once,
+        # 4 per id and 8 per document offset
+        call_bytes = enc["bytes"] + 4 * acc["n_ids"] + 8 * enc["h_off"].numel()
+        call_gbs = call_bytes / (enc_ms / args.steps / 1e3) / 1e9
         out["encode"] = {"value": round(gbs, 3), "unit": "GB/s", "ms_per_step": round(enc_ms / args.steps, 3),
                          "workload": enc["workload"], "n_ids": acc["n_ids"],
+                         "roofline": {"kernel": "trie_encode (whole call)", "bound": "hbm",
+                                      "achieved": round(call_gbs, 1), "peak": peak, "unit": "GB/s",
+                                      "frac": round(call_gbs / peak, 4), "peak_kind": f"of {peak_kind}",
+                                      "algorithmic_bytes_per_call": int(call_bytes)},
                          "rooflines": {f: rooflines[f] for f in ("encode_spec", "encode_emit")}}
     return out
 
