@@ -192,8 +192,8 @@ extern "C" int bpe_ctx_set_option(bpe_ctx *ctx, int option, int64_t value) {
         ctx->list_frontier = (int)value;
         return BPE_OK;
     case BPE_OPT_LIST_TAIL:
-        if (value < -1 || value > 2048)
-            return fail(ctx, BPE_ERR_INVALID_ARG, "list tail %lld outside -1..2048", (long long)value);
+        if (value < -1 || value > 4096)
+            return fail(ctx, BPE_ERR_INVALID_ARG, "list tail %lld outside -1..4096", (long long)value);
         ctx->list_tail = (int)value;
         return BPE_OK;
     case BPE_OPT_TEST_STALL_TILE:

@@ -146,7 +146,7 @@ const char *bpe_last_error(const bpe_ctx *ctx);
  *   BPE_OPT_LIST_TAIL    the occurrence-list loop runs a merge whose list
  *                        holds at most this many entries in one CTA, many
  *                        merges per launch (0 = every merge on all SMs;
- *                        -1 = default 2048; at most 2048) */
+ *                        -1 = default 4096; at most 4096) */
 enum {
     BPE_OPT_TABLE_LOG2 = 1,
     BPE_OPT_GRAPH = 2,
