@@ -679,10 +679,9 @@ def run_ours(args, rank, world, local_rank):
         "roofline": rooflines[dom],
         "rooflines": rooflines,
         "gpu_launches": acc["launches"],
-        "timing": ("value, e2e: CUDA events around each step, the merge loop replayed from CUDA graphs with "
-                   "programmatic dependent launch; kernels and rooflines: a separate profiled pass of the same "
-                   "steps (events around each stand-alone kernel, event nodes between the merge loop's kernels, "
-                   "which then run without launch overlap)"),
+        "timing": ("value, e2e: CUDA events around each step, the merge loop replayed from CUDA graphs; "
+                   "kernels and rooflines: a separate profiled pass of the same "
+                   "steps (events around each stand-alone kernel, event nodes between the merge loop's kernels)"),
         "profiled_merge_loop_ms_per_step": round(loop_ms / max(1, min(args.steps, 2)), 3),
         "kernels": {k: {"launches": v["launches"], "ms": round(v["ms"], 3),
                         "GB/s": round(v["bytes"] / (v["ms"] / 1e3) / 1e9, 1) if v["ms"] else None}

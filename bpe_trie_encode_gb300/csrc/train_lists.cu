@@ -151,12 +151,6 @@ __device__ __forceinline__ uint32_t prev_live(const uint32_t *sym, uint32_t p, u
     return a;
 }
 
-// Programmatic dependent launch: a kernel of the merge loop lets the next
-// one be scheduled as soon as it starts, and waits for the previous one (all
-// its memory operations) before touching anything it wrote.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
 // Largest (packed, entry) pair of a block; result in every thread.
 template <int THREADS>
 __device__ __forceinline__ void block_max2(unsigned long long &v, uint32_t &e, unsigned long long *sv, uint32_t *se) {
@@ -977,8 +971,6 @@ __global__ void __launch_bounds__(kLsThreads, 2) k_lscan(LP P) {
     extern __shared__ __align__(16) unsigned char lsm[];
     LsShared &S = *reinterpret_cast<LsShared *>(lsm);
     LState *st = P.st;
-    pdl_launch();
-    pdl_wait();
     uint32_t k, es;
     unsigned long long bw;
     if (!multi_merge(P, &k, &bw, &es)) return;
@@ -1120,8 +1112,6 @@ __global__ void __launch_bounds__(kLaThreads) k_lapply(LP P) {
     __shared__ unsigned long long sv[32];
     __shared__ uint32_t se[32];
     LState *st = P.st;
-    pdl_launch();
-    pdl_wait();
     uint32_t k, es;
     unsigned long long bw;
     if (!multi_merge(P, &k, &bw, &es)) return;
@@ -1221,8 +1211,6 @@ __global__ void __launch_bounds__(kTlThreads, 1) k_ltail(LP P, uint32_t budget) 
     extern __shared__ __align__(16) unsigned char tsm[];
     TlShared &S = *reinterpret_cast<TlShared *>(tsm);
     LState *st = P.st;
-    pdl_launch();
-    pdl_wait();
     const uint32_t tail_len = st->tail_len;
     if (!tail_len || st->err) return;
     uint32_t k = st->k_cur;
@@ -1627,36 +1615,18 @@ struct LBuffers {
     unsigned scan_grid, apply_grid;
 };
 
-// Launch with programmatic dependent launch allowed (pdl): the kernel may be
-// scheduled while the one before it runs; it waits for it in griddepcontrol.
-template <typename... Args>
-cudaError_t launch(void (*kern)(Args...), unsigned grid, unsigned block, size_t smem, cudaStream_t s, bool pdl,
-                   Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = pdl ? at : nullptr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, args...);
-}
-
 // One slot: the tail from st->k_cur, then the multi-CTA pair for a merge the
-// tail left (each returns at once when it has nothing to do).  Each kernel
-// overlaps its launch with the one before (pdl) except the first of a
-// window; profiled slots record an event after each kernel instead (under
-// stream capture an external record becomes an event node of the graph).
-void launch_slot(const LBuffers &B, cudaStream_t s, const cudaEvent_t *ev, bool first) {
-    const bool pdl = !ev;
-    launch(k_ltail, 1, kTlThreads, sizeof(TlShared), s, pdl && !first, B.p, kTlBudget);
+// tail left (each returns at once when it has nothing to do), in plain
+// stream order.  (Programmatic dependent launch, which lets a kernel be
+// scheduled while the one before it still runs, made the large workload's
+// loop 21% slower.)  Profiled slots record an event after each kernel
+// (under stream capture an external record becomes an event node).
+void launch_slot(const LBuffers &B, cudaStream_t s, const cudaEvent_t *ev) {
+    k_ltail<<<1, kTlThreads, sizeof(TlShared), s>>>(B.p, kTlBudget);
     if (ev) cudaEventRecordWithFlags(ev[0], s, cudaEventRecordExternal);
-    launch(k_lscan, B.scan_grid, kLsThreads, sizeof(LsShared), s, pdl, B.p);
+    k_lscan<<<B.scan_grid, kLsThreads, sizeof(LsShared), s>>>(B.p);
     if (ev) cudaEventRecordWithFlags(ev[1], s, cudaEventRecordExternal);
-    launch(k_lapply, B.apply_grid, kLaThreads, 0, s, pdl, B.p);
+    k_lapply<<<B.apply_grid, kLaThreads, 0, s>>>(B.p);
     if (ev) cudaEventRecordWithFlags(ev[2], s, cudaEventRecordExternal);
 }
 
@@ -1684,7 +1654,7 @@ int get_graph(bpe_ctx *ctx, const LBuffers &B, const cudaEvent_t *ev, cudaGraphE
     cudaStream_t cs = ctx->capture_stream;
     BPE_CUDA(ctx, cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal), "begin capture");
     if (ev) cudaEventRecordWithFlags(ev[0], cs, cudaEventRecordExternal);
-    for (int i = 0; i < kSlots; i++) launch_slot(B, cs, ev ? ev + 1 + 3 * i : nullptr, i == 0);
+    for (int i = 0; i < kSlots; i++) launch_slot(B, cs, ev ? ev + 1 + 3 * i : nullptr);
     cudaGraph_t g = nullptr;
     cudaError_t e = cudaStreamEndCapture(cs, &g);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "end capture");
@@ -1854,7 +1824,7 @@ int train_lists(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_
         if (graph) {
             BPE_CUDA(ctx, cudaGraphLaunch(exec, s), "graph launch");
         } else {
-            for (int i = 0; i < kSlots; i++) launch_slot(B, s, nullptr, i == 0);
+            for (int i = 0; i < kSlots; i++) launch_slot(B, s, nullptr);
         }
         BPE_CUDA(ctx, cudaGetLastError(), "train launch");
         const int slot = (int)(window % kInFlight);
