@@ -28,7 +28,9 @@
 //     entry is created, and the best count never rises, so while the
 //     frontier's best is at least T it is the global best; otherwise every
 //     entry is rescanned into a new frontier with a lower threshold.
-//   * The stream is compacted once, at the end (decoupled look-back).
+//   * A position's symbol and the entry of the pair starting there share one
+//     8-byte cell, so the neighbours of an occurrence cost one load each.
+//   * The stream is compacted once, at the end.
 //
 // Kernels:
 //   k_bcount     pair counts of the input (byte ids): per CTA a direct-indexed
@@ -46,7 +48,11 @@
 //                finds the next merge's pair in the frontier
 //   k_lapply     per merge: new ids, dead marks and back distances; new pairs
 //                into their lists; a full rescan when the frontier ran dry
-//   k_lcompact   the live symbols in order (warp scans, decoupled look-back)
+//   k_ltail      per merge while the lists are short (at most 4,096
+//                entries): k_lscan + k_lapply's steps in one CTA, up to 512
+//                merges per launch
+//   k_lcompact   the live symbols in order (one cooperative launch: tile
+//                counts, a grid barrier, then per-warp compaction)
 #include <algorithm>
 #include <cstring>
 #include <vector>
@@ -82,7 +88,7 @@ constexpr int kTlHash = kTlRecCap;            // distinct new pairs of a tail me
 constexpr uint32_t kTlBudget = 512;           // merges per tail launch
 constexpr int kSlots = 8;                     // (tail, scan, apply) slots per captured graph
 constexpr int kCsThreads = 512;
-constexpr uint32_t kCsRound = 16u << 20;      // compaction round: 64 MB of symbols, resident in L2 between passes
+constexpr uint32_t kCsRound = 8u << 20;       // compaction round: 64 MB of cells, resident in L2 between passes
 constexpr uint32_t kHashProbes = 4096;
 constexpr unsigned kSpinLimit = 1u << 22;
 constexpr int kInFlight = 3;
@@ -107,7 +113,8 @@ struct LState {
 struct LP {
     const uint32_t *in;
     uint64_t n;
-    uint32_t *sym, *pe, *occ;
+    uint2 *cell;           // per position: x = symbol or dead mark, y = entry of the pair starting there
+    uint32_t *occ;
     unsigned long long occ_cap;
     uint32_t *ekey, *ecnt, *ellen;
     unsigned long long *eloff;
@@ -139,15 +146,19 @@ __device__ __forceinline__ unsigned long long pack(uint32_t count, uint32_t key)
 __device__ __forceinline__ uint32_t sid(uint32_t s) { return s & 0xFFFFu; }
 __device__ __forceinline__ uint32_t base_key(uint32_t e) { return ((e >> 8) << 16) | (e & 0xFFu); }
 
+// A position's symbol (or dead mark), and its whole cell.
+__device__ __forceinline__ uint32_t ld_sym(const uint2 *cell, uint32_t x) { return __ldcg(&cell[x].x); }
+__device__ __forceinline__ uint2 ld_cell(const uint2 *cell, uint32_t x) { return __ldcg(cell + x); }
+
 // The live position before live position p (p > 0), and its symbol.
-__device__ __forceinline__ uint32_t prev_live(const uint32_t *sym, uint32_t p, uint32_t *sa) {
-    const uint32_t x = p - 1, sx = __ldcg(sym + x);
+__device__ __forceinline__ uint32_t prev_live(const uint2 *cell, uint32_t p, uint32_t *sa) {
+    const uint32_t x = p - 1, sx = ld_sym(cell, x);
     if (!(sx & kDead)) {
         *sa = sx;
         return x;
     }
     const uint32_t a = x - (sx & kDistMask);
-    *sa = __ldcg(sym + a);
+    *sa = ld_sym(cell, a);
     return a;
 }
 
@@ -427,7 +438,6 @@ __global__ void __launch_bounds__(kBfThreads, 1) k_bfill(LP P) {
             rank[j] = 0;
             const uint64_t p = p0 + j;
             if (p < n) {
-                P.sym[p] = a[j];
                 if (p + 1 < n && !(a[j + 1] & kWordStart)) {
                     const uint32_t e = ((a[j] & 0xFFu) << 8) | (a[j + 1] & 0xFFu);
                     const uint32_t sh = (e & 1u) << 4;
@@ -439,7 +449,7 @@ __global__ void __launch_bounds__(kBfThreads, 1) k_bfill(LP P) {
                     ent[j] = e;
                     rank[j] = old;
                 }
-                P.pe[p] = ent[j];
+                P.cell[p] = make_uint2(a[j], ent[j]);
             }
         }
         __syncthreads();
@@ -593,7 +603,7 @@ __device__ __forceinline__ void occurrence(const LP &P, const MergeCtx &M, const
 // unless ws_ok.
 __device__ __forceinline__ bool holds(const LP &P, uint64_t n, uint32_t x, uint32_t want, bool ws_ok, uint32_t *sx) {
     if (x >= n) return false;
-    const uint32_t s = __ldcg(P.sym + x);
+    const uint32_t s = ld_sym(P.cell, x);
     *sx = s;
     return !(s & kDead) && sid(s) == want && (ws_ok || !(s & kWordStart));
 }
@@ -604,16 +614,15 @@ __device__ __forceinline__ bool holds(const LP &P, uint64_t n, uint32_t x, uint3
 // (token lengths come from the ids), so their loads are issued together.
 __device__ void list_entry(const LP &P, const MergeCtx &M, const Stage &S, uint32_t p) {
     if (p >= M.n) return;
-    const uint32_t sp = __ldcg(P.sym + p);
+    const uint32_t sp = ld_sym(P.cell, p);
     if ((sp & kDead) || sid(sp) != M.l) return;
     const uint32_t q = p + M.vl, b = q + M.vr;
     if (q >= M.n) return;
     const bool left = !(sp & kWordStart) && p > 0;
-    const uint32_t sq = __ldcg(P.sym + q);
-    const uint32_t eq = __ldcg(P.pe + q);                       // used only when (q, b) is a pair
-    const uint32_t sx = left ? __ldcg(P.sym + p - 1) : kDead;   // p's left neighbour, or its last byte
-    const uint32_t ex = left ? __ldcg(P.pe + p - 1) : kNone;
-    const uint32_t sb = b < M.n ? __ldcg(P.sym + b) : kWordStart;
+    const uint2 cq = ld_cell(P.cell, q);                                          // eq: used only when (q, b) is a pair
+    const uint2 cx = left ? ld_cell(P.cell, p - 1) : make_uint2(kDead, kNone);   // p's left neighbour, or its last byte
+    const uint32_t sq = cq.x, eq = cq.y, sx = cx.x, ex = cx.y;
+    const uint32_t sb = b < M.n ? ld_sym(P.cell, b) : kWordStart;
     if ((sq & kDead) || sid(sq) != M.r || (sq & kWordStart)) return;
     uint32_t a = kNone, sa = 0, ea = kNone;
     if (left) {
@@ -623,8 +632,9 @@ __device__ void list_entry(const LP &P, const MergeCtx &M, const Stage &S, uint3
             ea = ex;
         } else {
             a = p - 1 - (sx & kDistMask);
-            sa = __ldcg(P.sym + a);
-            ea = __ldcg(P.pe + a);
+            const uint2 ca = ld_cell(P.cell, a);
+            sa = ca.x;
+            ea = ca.y;
         }
     }
     if (M.l != M.r) {
@@ -632,7 +642,7 @@ __device__ void list_entry(const LP &P, const MergeCtx &M, const Stage &S, uint3
         uint32_t a2 = kNone;
         if (a != kNone && a > 0 && sid(sa) == M.r && !(sa & kWordStart)) {
             uint32_t sa2;
-            a2 = prev_live(P.sym, a, &sa2);
+            a2 = prev_live(P.cell, a, &sa2);
             pocc = sid(sa2) == M.l;
         }
         uint32_t sc;
@@ -651,12 +661,12 @@ __device__ void list_entry(const LP &P, const MergeCtx &M, const Stage &S, uint3
         uint32_t sw = kWordStart, sn = kWordStart, en = kNone;
         bool more = false;
         if (z < M.n && !(sz & kWordStart) && sid(sz) == M.l && z + M.vl < M.n) {
-            sw = __ldcg(P.sym + z + M.vl);
+            sw = ld_sym(P.cell, z + M.vl);
             more = !(sw & kDead) && sid(sw) == M.r && !(sw & kWordStart);
         }
         if (more && z + M.vl + M.vr < M.n) {
-            sn = __ldcg(P.sym + z + M.vl + M.vr);
-            en = __ldcg(P.pe + z + M.vl);
+            sn = ld_sym(P.cell, z + M.vl + M.vr);
+            en = __ldcg(&P.cell[z + M.vl].y);
         }
         occurrence(P, M, S, x, sxx, la, lsa, lea, !first, la2, z, sz, ez, more);
         if (!more) break;
@@ -721,7 +731,7 @@ __device__ __forceinline__ void list_batch(const LP &P, const MergeCtx &M, const
         return;
     }
 #pragma unroll
-    for (int j = 0; j < J; j++) sp[j] = j < jmax && p[j] < M.n ? __ldcg(P.sym + p[j]) : kDead;
+    for (int j = 0; j < J; j++) sp[j] = j < jmax && p[j] < M.n ? ld_sym(P.cell, p[j]) : kDead;
     uint32_t sq[J], eq[J], sx[J], ex[J], sb[J];
     bool ok[J], left[J];
 #pragma unroll
@@ -729,11 +739,13 @@ __device__ __forceinline__ void list_batch(const LP &P, const MergeCtx &M, const
         ok[j] = !(sp[j] & kDead) && sid(sp[j]) == M.l && p[j] + M.vl < M.n;
         left[j] = ok[j] && !(sp[j] & kWordStart) && p[j] > 0;
         const uint32_t q = p[j] + M.vl, b = q + M.vr;
-        sq[j] = ok[j] ? __ldcg(P.sym + q) : kDead;
-        eq[j] = ok[j] ? __ldcg(P.pe + q) : kNone;
-        sx[j] = left[j] ? __ldcg(P.sym + p[j] - 1) : kDead;
-        ex[j] = left[j] ? __ldcg(P.pe + p[j] - 1) : kNone;
-        sb[j] = ok[j] && b < M.n ? __ldcg(P.sym + b) : kWordStart;
+        const uint2 cq = ok[j] ? ld_cell(P.cell, q) : make_uint2(kDead, kNone);
+        const uint2 cx = left[j] ? ld_cell(P.cell, p[j] - 1) : make_uint2(kDead, kNone);
+        sq[j] = cq.x;
+        eq[j] = cq.y;
+        sx[j] = cx.x;
+        ex[j] = cx.y;
+        sb[j] = ok[j] && b < M.n ? ld_sym(P.cell, b) : kWordStart;
     }
     uint32_t a[J], sa[J], ea[J];
 #pragma unroll
@@ -749,8 +761,9 @@ __device__ __forceinline__ void list_batch(const LP &P, const MergeCtx &M, const
                 ea[j] = ex[j];
             } else {
                 a[j] = p[j] - 1 - (sx[j] & kDistMask);
-                sa[j] = __ldcg(P.sym + a[j]);
-                ea[j] = __ldcg(P.pe + a[j]);
+                const uint2 ca = ld_cell(P.cell, a[j]);
+                sa[j] = ca.x;
+                ea[j] = ca.y;
             }
         }
     }
@@ -764,14 +777,14 @@ __device__ __forceinline__ void list_batch(const LP &P, const MergeCtx &M, const
         np[j] = ok[j] && a[j] != kNone && a[j] > 0 && sid(sa[j]) == M.r && !(sa[j] & kWordStart);
         nq[j] = ok[j] && b < M.n && !(sb[j] & kWordStart) && sid(sb[j]) == M.l && b + M.vl < M.n;
         a2[j] = np[j] ? a[j] - 1 : kNone;
-        s2[j] = np[j] ? __ldcg(P.sym + a2[j]) : 0u;
-        sc[j] = nq[j] ? __ldcg(P.sym + b + M.vl) : kDead;
+        s2[j] = np[j] ? ld_sym(P.cell, a2[j]) : 0u;
+        sc[j] = nq[j] ? ld_sym(P.cell, b + M.vl) : kDead;
     }
 #pragma unroll
     for (int j = 0; j < J; j++) {
         if (np[j] && (s2[j] & kDead)) {
             a2[j] -= s2[j] & kDistMask;
-            s2[j] = __ldcg(P.sym + a2[j]);
+            s2[j] = ld_sym(P.cell, a2[j]);
         }
     }
 #pragma unroll
@@ -1122,15 +1135,15 @@ __global__ void __launch_bounds__(kLaThreads) k_lapply(LP P) {
     for (uint32_t i = blockIdx.x * kLaThreads + threadIdx.x; i < na; i += stride) {
         const uint32_t rc = __ldcg(P.app[par] + i), p = rc & ~kDead;
         const uint32_t q = p + vl, last = q + vr - 1;
-        P.sym[p] = nid | ((rc & kDead) ? kWordStart : 0u);
-        P.sym[q] = kDead | (q - p);
-        if (last != q) P.sym[last] = kDead | (last - p);
+        P.cell[p].x = nid | ((rc & kDead) ? kWordStart : 0u);
+        P.cell[q].x = kDead | (q - p);
+        if (last != q) P.cell[last].x = kDead | (last - p);
     }
     for (uint32_t i = blockIdx.x * kLaThreads + threadIdx.x; i < nr; i += stride) {
         const uint4 rc = __ldcg(P.rec[par] + i);
         const uint32_t e = __ldcg(P.hent + rc.x);
         P.occ[__ldcg(P.eloff + e) + rc.y] = rc.z;
-        P.pe[rc.z] = e;
+        P.cell[rc.z].y = e;
     }
     const bool more = k + 1 < st->n_merges;
     // the frontier's best (every count of merge k is final)
@@ -1306,14 +1319,14 @@ __global__ void __launch_bounds__(kTlThreads, 1) k_ltail(LP P, uint32_t budget) 
         for (uint32_t i = threadIdx.x; i < na; i += kTlThreads) {
             const uint32_t rc = S.app[i], p = rc & ~kDead;
             const uint32_t q = p + M.vl, last = q + M.vr - 1;
-            P.sym[p] = M.nid | ((rc & kDead) ? kWordStart : 0u);
-            P.sym[q] = kDead | (q - p);
-            if (last != q) P.sym[last] = kDead | (last - p);
+            P.cell[p].x = M.nid | ((rc & kDead) ? kWordStart : 0u);
+            P.cell[q].x = kDead | (q - p);
+            if (last != q) P.cell[last].x = kDead | (last - p);
         }
         for (uint32_t i = threadIdx.x; i < nr; i += kTlThreads) {
             const uint32_t rs = S.rkey[i], h = rs >> 16, pos = S.rpos[i];
             P.occ[S.hoff[h] + (rs & 0xFFFFu)] = pos;
-            P.pe[pos] = S.hcnt[h];
+            P.cell[pos].y = S.hcnt[h];
         }
         __syncthreads();
         for (uint32_t u = threadIdx.x; u < nu; u += kTlThreads) {
@@ -1453,9 +1466,10 @@ __device__ __forceinline__ uint32_t live4(uint4 v) {
 // does" 3.: warp-level exclusive scans of the keep flags, offsets across
 // CTAs, a scatter).  One cooperative launch (all CTAs resident) walks the
 // stream in rounds of kCsRound positions, small enough to stay in L2 between
-// the round's two passes, so HBM sees each symbol read once and each
-// survivor written once.  A round is split into warp tiles of 512 positions
-// (four 128-bit loads per lane), dealt out as contiguous slices, one per CTA:
+// the round's two passes, so HBM sees each cell read once and each survivor
+// written once.  A round is split into warp tiles of 512 positions (eight
+// 128-bit loads per lane: four positions' cells per two loads), dealt out as
+// contiguous slices, one per CTA:
 //   pass 1  every warp counts the live symbols of its tiles (loads kept in
 //           L2) and records each tile's count; each CTA publishes its total;
 //   barrier (grid-wide, bounded wait)
@@ -1475,7 +1489,6 @@ __global__ void __launch_bounds__(kCsThreads) k_lcompact(LP P, uint32_t *out) {
     constexpr uint32_t kMaxTiles = kCsRound / kWT;      // warp tiles of a round
     __shared__ __align__(16) uint32_t stage[kWarps][kWT];
     __shared__ uint32_t s_toff[2048];                   // a slice's tile offsets (a slice has at most 2,048 tiles)
-    // two tiles per warp and step (tiles t and t + kWarps): eight loads in flight per lane
     __shared__ uint32_t s_warp[kWarps];
     __shared__ unsigned long long s_red[kWarps][2];
     __shared__ int s_ok;
@@ -1485,13 +1498,17 @@ __global__ void __launch_bounds__(kCsThreads) k_lcompact(LP P, uint32_t *out) {
     const uint32_t G = gridDim.x, c = blockIdx.x;
     uint64_t out_base = 0;   // survivors of the earlier rounds (the same in every CTA)
     uint32_t par = 0;
-    auto load = [&](uint64_t i, uint64_t end) -> uint4 {   // four positions, dead past end
-        if (i + 4 <= end) return __ldcg(reinterpret_cast<const uint4 *>(P.sym + i));
+    auto load = [&](uint64_t i, uint64_t end) -> uint4 {   // four positions' symbols (two 128-bit loads), dead past end
+        if (i + 4 <= end) {
+            const uint4 *c = reinterpret_cast<const uint4 *>(P.cell + i);
+            const uint4 u0 = __ldcg(c), u1 = __ldcg(c + 1);
+            return make_uint4(u0.x, u0.z, u1.x, u1.z);
+        }
         uint4 v;
-        v.x = i < end ? __ldcg(P.sym + i) : kDead;
-        v.y = i + 1 < end ? __ldcg(P.sym + i + 1) : kDead;
-        v.z = i + 2 < end ? __ldcg(P.sym + i + 2) : kDead;
-        v.w = i + 3 < end ? __ldcg(P.sym + i + 3) : kDead;
+        v.x = i < end ? ld_sym(P.cell, (uint32_t)i) : kDead;
+        v.y = i + 1 < end ? ld_sym(P.cell, (uint32_t)(i + 1)) : kDead;
+        v.z = i + 2 < end ? ld_sym(P.cell, (uint32_t)(i + 2)) : kDead;
+        v.w = i + 3 < end ? ld_sym(P.cell, (uint32_t)(i + 3)) : kDead;
         return v;
     };
     for (uint64_t r0 = 0; r0 < n; r0 += kCsRound, par ^= 1u) {
@@ -1502,27 +1519,16 @@ __global__ void __launch_bounds__(kCsThreads) k_lcompact(LP P, uint32_t *out) {
         uint32_t *tcnt = P.ctile + (uint64_t)par * kMaxTiles;
         // pass 1: live count of each of the slice's tiles
         uint32_t cta = 0;
-        for (uint32_t t = w0 + w; t < w1; t += 2 * kWarps) {
-            const bool two = t + kWarps < w1;
-            const uint64_t b = r0 + (uint64_t)t * kWT + 4 * lane, b2 = b + (uint64_t)kWarps * kWT;
-            uint4 v[8];
+        for (uint32_t t = w0 + w; t < w1; t += kWarps) {   // eight 128-bit loads in flight per lane
+            const uint64_t b = r0 + (uint64_t)t * kWT + 4 * lane;
+            uint4 v[4];
 #pragma unroll
-            for (int j = 0; j < 4; j++) {
-                v[j] = load(b + 128 * j, rend);
-                v[4 + j] = two ? load(b2 + 128 * j, rend) : make_uint4(kDead, kDead, kDead, kDead);
-            }
+            for (int j = 0; j < 4; j++) v[j] = load(b + 128 * j, rend);
             uint32_t k = live4(v[0]) + live4(v[1]) + live4(v[2]) + live4(v[3]);
-            uint32_t k2 = live4(v[4]) + live4(v[5]) + live4(v[6]) + live4(v[7]);
 #pragma unroll
-            for (int d = 16; d > 0; d >>= 1) {
-                k += __shfl_xor_sync(kFull, k, d);
-                k2 += __shfl_xor_sync(kFull, k2, d);
-            }
-            if (lane == 0) {
-                tcnt[t] = k;
-                if (two) tcnt[t + kWarps] = k2;
-            }
-            cta += k + k2;
+            for (int d = 16; d > 0; d >>= 1) k += __shfl_xor_sync(kFull, k, d);
+            if (lane == 0) tcnt[t] = k;
+            cta += k;
         }
         if (lane == 0) s_warp[w] = cta;
         __syncthreads();
@@ -1567,9 +1573,10 @@ __global__ void __launch_bounds__(kCsThreads) k_lcompact(LP P, uint32_t *out) {
             all += s_red[i][1];
         }
         const uint64_t cbase = out_base + before;
-        // every warp compacts its tiles on its own
+        // every warp compacts its tiles on its own (without an output, only
+        // the length is wanted: nothing to do)
         uint4 nv[4];
-        const uint32_t tw = w0 + w;
+        const uint32_t tw = out ? w0 + w : w1;
         if (tw < w1)
 #pragma unroll
             for (int j = 0; j < 4; j++) nv[j] = load(r0 + (uint64_t)tw * kWT + 4 * lane + 128 * j, rend);
@@ -1634,7 +1641,7 @@ void launch_slot(const LBuffers &B, cudaStream_t s, const cudaEvent_t *ev) {
 // event before the first kernel and after every kernel.
 int get_graph(bpe_ctx *ctx, const LBuffers &B, const cudaEvent_t *ev, cudaGraphExec_t *out) {
     std::vector<uintptr_t> key = {
-        3u, (uintptr_t)B.p.sym, (uintptr_t)B.p.pe, (uintptr_t)B.p.occ, (uintptr_t)B.p.occ_cap, (uintptr_t)B.p.ekey,
+        3u, (uintptr_t)B.p.cell, (uintptr_t)B.p.occ, (uintptr_t)B.p.occ_cap, (uintptr_t)B.p.ekey,
         (uintptr_t)B.p.ecnt, (uintptr_t)B.p.ellen, (uintptr_t)B.p.eloff, (uintptr_t)B.p.dcap, (uintptr_t)B.p.vlen,
         (uintptr_t)B.p.best, (uintptr_t)B.p.ebest, (uintptr_t)B.p.fr[0], (uintptr_t)B.p.fr[1], (uintptr_t)B.p.fcap,
         (uintptr_t)B.p.hslot, (uintptr_t)B.p.hcnt, (uintptr_t)B.p.hent, (uintptr_t)B.p.hmask, (uintptr_t)B.p.ns[0],
@@ -1683,11 +1690,11 @@ int train_lists(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_
     const uint32_t hbits = 18;   // per-merge hash: <= 2 * 65,536 + 1 distinct new pairs, at most half full
     const uint64_t dcap = (uint64_t)kBaseEntries + (1u << 17) + 64ull * n_merges;
     const uint64_t occ_cap = 3 * n + 16;   // byte pairs (< n) + two new pairs per merged occurrence (< n in all)
-    void *state, *sym, *pe, *occ, *ekey, *ecnt, *ellen, *eloff, *vlen, *bfill, *best, *ebest, *fr, *hslot, *hcnt,
+    void *state, *cell, *occ, *ekey, *ecnt, *ellen, *eloff, *vlen, *bfill, *best, *ebest, *fr, *hslot, *hcnt,
         *hent, *ns, *cand, *kmode;
     const unsigned scan_grid = (unsigned)ctx->sm_count * 2, apply_grid = (unsigned)ctx->sm_count * 2;
-    if ((rc = ensure(ctx, S_L_STATE, sizeof(LState), &state)) || (rc = ensure(ctx, S_TRAIN_BUF0, n * 4 + 64, &sym)) ||
-        (rc = ensure(ctx, S_TRAIN_BUF1, n * 4 + 64, &pe)) || (rc = ensure(ctx, S_L_OCC, occ_cap * 4, &occ)) ||
+    if ((rc = ensure(ctx, S_L_STATE, sizeof(LState), &state)) || (rc = ensure(ctx, S_TRAIN_BUF0, n * 8 + 64, &cell)) ||
+        (rc = ensure(ctx, S_L_OCC, occ_cap * 4, &occ)) ||
         (rc = ensure(ctx, S_L_EKEY, dcap * 4, &ekey)) || (rc = ensure(ctx, S_L_ECNT, dcap * 4, &ecnt)) ||
         (rc = ensure(ctx, S_L_ELEN, dcap * 4, &ellen)) || (rc = ensure(ctx, S_L_EOFF, dcap * 8, &eloff)) ||
         (rc = ensure(ctx, S_L_VLEN, 65536 * 4, &vlen)) || (rc = ensure(ctx, S_L_BFILL, 65536 * 4, &bfill)) ||
@@ -1721,8 +1728,7 @@ int train_lists(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_
     memset(&P, 0, sizeof P);
     P.in = d_symbols;
     P.n = n;
-    P.sym = (uint32_t *)sym;
-    P.pe = (uint32_t *)pe;
+    P.cell = (uint2 *)cell;
     P.occ = (uint32_t *)occ;
     P.occ_cap = occ_cap;
     P.ekey = (uint32_t *)ekey;
@@ -1886,7 +1892,7 @@ int train_lists(bpe_ctx *ctx, const uint32_t *d_symbols, uint64_t n, uint32_t n_
         P.ctile = (uint32_t *)ctile;
         P.cbar = (uint32_t *)cbar;
         BPE_CUDA(ctx, cudaMemsetAsync(cbar, 0, kGbWords * 4, s), "barrier clear");
-        uint32_t *out = d_symbols_final ? d_symbols_final : P.pe;   // length only: the pair entries are done with
+        uint32_t *out = d_symbols_final;   // null: the length only
         ev(3);
         void *cargs[] = {&P, &out};
         BPE_CUDA(ctx, cudaLaunchCooperativeKernel((const void *)k_lcompact, cp_grid, kCsThreads, cargs, 0, s),
