@@ -22,6 +22,9 @@
 //                  guard positions whose edges reach the chunk ("crossing").
 //                  (k_uni_fwd: the same with one thread per chunk and a
 //                  64-bit ring, for spans over 63 bytes or wide scores.)
+//   k_uni_fwd_wide the chunks whose 32-bit window spread (values more than
+//                  2^30 units apart: many short tokens under scores of a fine
+//                  unit) run again, a warp each, with 64-bit values.
 //   k_uni_check    the guard ran from a wrong start value, but if the chains
 //                  of the reachable crossing positions step like the true
 //                  chains (the previous chunk's back pointers) until they
@@ -107,6 +110,7 @@ struct UniState {
     uint32_t bad_doc;
     uint32_t fwd_repairs, bwd_repairs;   // chunks re-run by the repair passes
     uint32_t flist_len;
+    uint32_t wlist_len;   // chunks whose 32-bit window spread, for the wide re-run
 };
 
 struct UniParams {
@@ -137,6 +141,7 @@ struct UniParams {
     uint32_t *okp;             // bitmap: a flagged chunk's parallel re-walk was valid for its predecessor too
     uint32_t *flist;           // flagged chunks (unordered; flist_cap entries kept)
     uint32_t flist_cap;
+    uint32_t *wlist;           // chunks to run again in 64 bits (unordered; flist_cap entries kept)
     uint32_t *sx, *bot, *count;   // per chunk (sx, bot relative to the chunk start)
     unsigned long long *prefix;
     unsigned long long *status;
@@ -484,14 +489,27 @@ constexpr int kTextStage = 128;               // bytes of text a warp stages per
 // source its A is final and B moves into A.  With each value, the source of
 // its best edge as an offset from base (bit 31: the edge is <unk>); the
 // edge's length is the distance to it.
-struct WarpRing {
-    int32_t a, b;
+//
+// WideRing holds the same window in 64 bits, not rebased: it is what a run
+// takes when the 32-bit window spread (values of a window more than 2^30
+// units apart: many short tokens under scores of a fine unit), and it never
+// spreads (a document's sums stay far below 2^62 units).
+template <typename V>
+struct WarpRingT {
+    V a, b;
     uint32_t sa, sb;
     uint64_t base, b0;
 };
+using WarpRing = WarpRingT<int32_t>;
+using WideRing = WarpRingT<long long>;
+constexpr long long kNeg64 = -0x7FFFFFFFFFFFFFFFll - 1;   // unreachable (wide values)
+template <typename V> __device__ __forceinline__ V ring_neg();
+template <> __device__ __forceinline__ int32_t ring_neg<int32_t>() { return kNeg32; }
+template <> __device__ __forceinline__ long long ring_neg<long long>() { return kNeg64; }
 
-__device__ __forceinline__ void ring_start(WarpRing &R, uint64_t base, uint64_t s0, int lane) {
-    R.a = R.b = kNeg32;
+template <typename V>
+__device__ __forceinline__ void ring_start(WarpRingT<V> &R, uint64_t base, uint64_t s0, int lane) {
+    R.a = R.b = ring_neg<V>();
     R.sa = R.sb = 0;
     R.base = R.b0 = base;
     const uint64_t o = s0 - base;
@@ -501,15 +519,17 @@ __device__ __forceinline__ void ring_start(WarpRing &R, uint64_t base, uint64_t 
 }
 
 // Back pointer of position pos given its value and source.
-__device__ __forceinline__ uint32_t ring_bp(const WarpRing &R, uint64_t pos, int32_t v, uint32_t src) {
-    if (v == kNeg32) return 0u;
+template <typename V>
+__device__ __forceinline__ uint32_t ring_bp(const WarpRingT<V> &R, uint64_t pos, V v, uint32_t src) {
+    if (v == ring_neg<V>()) return 0u;
     const uint32_t len = ((uint32_t)(pos - R.base) - src) & 0x7FFFFFFFu;
     return len == 0 ? kRoot : (len << 24) | ((src >> 31) ? kUnkTid : kNoTid);
 }
 
 // After a run: back pointer of the first position at or after its end that
 // this lane holds (the document end, when the run ended there).
-__device__ __forceinline__ uint32_t ring_final(const WarpRing &R, uint64_t pos) {
+template <typename V>
+__device__ __forceinline__ uint32_t ring_final(const WarpRingT<V> &R, uint64_t pos) {
     return ring_bp(R, pos, R.a, R.sa);
 }
 
@@ -533,7 +553,7 @@ struct EdgeBuf {
 struct WalkOut {
     uint32_t X, Y;
     int lr;
-    bool unk, crossing, spread;
+    bool unk, crossing, norow;
 };
 
 // Walk: every lane walks the trie from its position b0 + lane (reachable or
@@ -575,7 +595,7 @@ __device__ __forceinline__ WalkOut walk_batch(const UniParams &P, const int4 *lu
                         } else {
                             if (w.lr < 0) w.lr = atomicAdd(eb.lcount, 1);
                             if (w.lr < kLongRows) eb.lrow[w.lr * 32 + (len - 33)] = sc;
-                            else w.spread = true;   // no long row left: the run is redone exactly
+                            else w.norow = true;   // no long row left: the run is redone exactly
                         }
                         M |= 1ull << len;
                         w.crossing |= len >= csr;
@@ -604,7 +624,7 @@ __device__ __forceinline__ WalkOut walk_batch(const UniParams &P, const int4 *lu
                 } else {
                     w.lr = atomicAdd(eb.lcount, 1);
                     if (w.lr < kLongRows) eb.lrow[w.lr * 32 + (len - 33)] = (int32_t)P.unk;
-                    else w.spread = true;
+                    else w.norow = true;
                 }
                 M = 1ull << len;
                 w.unk = true;
@@ -622,10 +642,12 @@ __device__ __forceinline__ WalkOut walk_batch(const UniParams &P, const int4 *lu
 // comes from lane s, and every lane relaxes its o1 and o1 + 32 targets (a bit
 // of s's masks rotated by s + 1) from shared memory and shuffles only.
 // sink(q, bp) receives every final position.  Returns whether this lane saw
-// a value beyond kSpread.
-template <typename Sink>
-__device__ __forceinline__ bool dp_batch(const EdgeBuf &eb, WarpRing &R, uint64_t b0, uint64_t to, const WalkOut &w,
-                                         Sink sink) {
+// a value beyond kSpread (never in a wide ring).
+template <typename V, typename Sink>
+__device__ __forceinline__ bool dp_batch(const EdgeBuf &eb, WarpRingT<V> &R, uint64_t b0, uint64_t to,
+                                         const WalkOut &w, Sink sink) {
+    constexpr bool kNarrow = sizeof(V) == 4;
+    const V neg = ring_neg<V>();
     const int lane = threadIdx.x & 31;
     const uint32_t mybit = 1u << lane;
     const uint64_t q = b0 + lane;
@@ -633,28 +655,29 @@ __device__ __forceinline__ bool dp_batch(const EdgeBuf &eb, WarpRing &R, uint64_
     const uint32_t xrot = __funnelshift_l(w.X, w.X, lane + 1), yrot = __funnelshift_l(w.Y, w.Y, lane + 1);
     const uint32_t mycode = ((uint32_t)(q - R.base) & 0x7FFFFFFFu) | ((uint32_t)w.unk << 31);
     const int lr = w.lr;
-    // rebase: the window's best reachable value becomes 0
-    const int32_t mx = __reduce_max_sync(kFull, max(R.a, R.b));
-    if (mx != kNeg32) {
-        if (R.a != kNeg32) {
-            const long long v = (long long)R.a - mx;
-            spread |= v < -kSpread;
-            R.a = (int32_t)max(v, (long long)-kSpread);
-        }
-        if (R.b != kNeg32) {
-            const long long v = (long long)R.b - mx;
-            spread |= v < -kSpread;
-            R.b = (int32_t)max(v, (long long)-kSpread);
+    if constexpr (kNarrow) {   // rebase: the window's best reachable value becomes 0
+        const int32_t mx = __reduce_max_sync(kFull, max((int32_t)R.a, (int32_t)R.b));
+        if (mx != kNeg32) {
+            if (R.a != kNeg32) {
+                const long long v = (long long)R.a - mx;
+                spread |= v < -kSpread;
+                R.a = (V)max(v, (long long)-kSpread);
+            }
+            if (R.b != kNeg32) {
+                const long long v = (long long)R.b - mx;
+                spread |= v < -kSpread;
+                R.b = (V)max(v, (long long)-kSpread);
+            }
         }
     }
     __syncwarp();
-    int32_t fv = kNeg32;
+    V fv = neg;
     uint32_t fs = 0;
     const uint32_t nsrc = (uint32_t)(to - b0 < 32 ? to - b0 : 32);
     const bool anylong = __any_sync(kFull, w.Y != 0u);   // some edge over 32 bytes (rare)
     // source s of the batch; o1 = this lane's length to reach its A position
     auto source = [&](uint32_t s, uint32_t o1) {
-        const int32_t b = __shfl_sync(kFull, R.a, s);
+        const V b = __shfl_sync(kFull, R.a, s);
         const uint32_t xr = __shfl_sync(kFull, xrot, s);
         const uint32_t code = __shfl_sync(kFull, mycode, s);
         const uint32_t yr = anylong ? __shfl_sync(kFull, yrot, s) : 0u;
@@ -664,15 +687,15 @@ __device__ __forceinline__ bool dp_batch(const EdgeBuf &eb, WarpRing &R, uint64_
             fs = R.sa;
             R.a = R.b;
             R.sa = R.sb;
-            R.b = kNeg32;
+            R.b = neg;
         }
-        if (b == kNeg32) return;
+        if (b == neg) return;
         if (xr & mybit) {
-            const int32_t cand = b + eb.score[s * kEdgeStride + (o1 - 1)];
+            const V cand = b + (V)eb.score[s * kEdgeStride + (o1 - 1)];
             if (cand > R.a) { R.a = cand; R.sa = code; }
         }
         if ((yr & mybit) && slr < kLongRows) {   // length o1 + 32
-            const int32_t cand = b + eb.lrow[slr * 32 + (o1 - 1)];
+            const V cand = b + (V)eb.lrow[slr * 32 + (o1 - 1)];
             if (cand > R.b) { R.b = cand; R.sb = code; }
         }
     };
@@ -683,7 +706,7 @@ __device__ __forceinline__ bool dp_batch(const EdgeBuf &eb, WarpRing &R, uint64_
     } else {
         for (uint32_t s = 0; s < nsrc; s++) source(s, ((o10 - 1u - s) & 31u) + 1u);
     }
-    spread |= fv != kNeg32 && (fv < -kSpread || fv > kSpread);   // every source value stayed in range
+    if constexpr (kNarrow) spread |= fv != neg && (fv < -kSpread || fv > kSpread);   // every source value stayed in range
     __syncwarp();
     if (q < to) sink(q, ring_bp(R, q, fv, fs));
     R.b0 = b0 + 32;
@@ -696,43 +719,40 @@ __device__ __forceinline__ bool dp_batch(const EdgeBuf &eb, WarpRing &R, uint64_
 // recurrence, per batch.  cross(m, bits) receives, per batch m, which
 // positions have an edge reaching cs or beyond.  A back pointer holds the
 // length and kNoTid (the emit pass finds the id from the token's bytes) or
-// kUnkTid.  Returns whether the values spread beyond kSpread or a long row
-// was missing (then the run is incomplete).
-template <typename Sink, typename Cross>
-__device__ bool warp_dp(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRing &R, uint64_t from,
-                        uint64_t to, uint64_t de, uint64_t cs, Sink sink, Cross cross) {
+// kUnkTid.  Returns 0 when the run is complete, else kRunLongRows when a
+// long row was missing, kRunSpread when the values spread beyond kSpread
+// (both: the run is incomplete).
+constexpr uint32_t kRunLongRows = 1u, kRunSpread = 2u;
+template <typename V, typename Sink, typename Cross>
+__device__ uint32_t warp_dp(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRingT<V> &R, uint64_t from,
+                            uint64_t to, uint64_t de, uint64_t cs, Sink sink, Cross cross) {
     const int lane = threadIdx.x & 31;
-    bool spread = false;
+    bool rows = false, spread = false;
     for (uint64_t b0 = from; b0 < to; b0 += 32) {
         const WalkOut w = walk_batch(P, lut, eb, b0, to, de, cs);
         cross((uint32_t)((b0 - from) >> 5), __ballot_sync(kFull, w.crossing && b0 + lane < cs));
-        spread |= w.spread;
+        rows |= w.norow;
         spread |= dp_batch(eb, R, b0, to, w, sink);
     }
-    return __any_sync(kFull, spread);
+    return (__any_sync(kFull, rows) ? kRunLongRows : 0u) | (__any_sync(kFull, spread) ? kRunSpread : 0u);
 }
 
-// Warp-per-chunk speculative forward run (spans E <= 63): k_uni_fwd's work,
-// one warp per chunk.
-__global__ void __launch_bounds__(kFwdWarps * 32, 4) k_uni_fwd_warp(UniParams P, unsigned long long n_chunks) {
-    __shared__ int4 lut[256];
-    extern __shared__ int32_t s_rows[];   // kFwdWarps edge tables
-    load_fat_lut(P, lut);
-    __syncthreads();
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const unsigned long long k = (unsigned long long)blockIdx.x * kFwdWarps + w;
-    if (k >= n_chunks) return;
+// The speculative forward run of chunk k by one warp (spans E <= 63):
+// k_uni_fwd's work.  Returns warp_dp's code (0: complete).
+template <typename V>
+__device__ __forceinline__ uint32_t fwd_chunk(const UniParams &P, const int4 *lut, const EdgeBuf &eb,
+                                              unsigned long long k) {
+    const int lane = threadIdx.x & 31;
     const UGeo g = uni_geo(P, k);
     const uint64_t from = run_from(P, g);
     const bool exact = from == g.ds;
     if (g.first && lane == 0 && is_cont(byte_at(P, g.ds))) atomicOr(&P.st->err, UERR_CONT_START);
     const uint64_t s0 = exact ? g.ds : next_boundary(P, from, g.de);
     if (!exact && (s0 >= g.cs || s0 - from >= 64) && lane == 0) atomicOr(&P.st->err, UERR_SPAN);
-    WarpRing R;
+    WarpRingT<V> R;
     ring_start(R, from, s0, lane);
     uint32_t *gb = P.gback + k * (unsigned long long)P.grec;
-    const EdgeBuf eb(s_rows + w * (kWarpEdgeBytes / 4));
-    const bool sp = warp_dp(
+    const uint32_t code = warp_dp(
         P, lut, eb, R, from, g.ce, g.de, g.cs,
         [&](uint64_t q, uint32_t bp) {
             if (q >= g.cs) {
@@ -744,13 +764,58 @@ __global__ void __launch_bounds__(kFwdWarps * 32, 4) k_uni_fwd_warp(UniParams P,
         [&](uint32_t m, unsigned bits) {
             if (!exact && m < (P.guard >> 5) && lane == 0) gb[P.guard + m] = bits;
         });
-    if (sp && lane == 0) {   // values spread too far for 32 bits: the chunk is redone
-        atomicOr(P.fflag + (k >> 5), 1u << (k & 31));
-        P.st->any_fflag = 1u;
-        const uint32_t i = atomicAdd(&P.st->flist_len, 1u);
-        if (i < P.flist_cap) P.flist[i] = (uint32_t)k;
-    }
     if (g.last && lane == (int)((g.de - from) & 31)) back_at(P, g.de) = ring_final(R, g.de);
+    return code;
+}
+
+// A chunk whose run is incomplete for want of a long row: flagged, so the
+// repair passes run it again.
+__device__ __forceinline__ void flag_chunk(const UniParams &P, unsigned long long k) {
+    atomicOr(P.fflag + (k >> 5), 1u << (k & 31));
+    P.st->any_fflag = 1u;
+    const uint32_t i = atomicAdd(&P.st->flist_len, 1u);
+    if (i < P.flist_cap) P.flist[i] = (uint32_t)k;
+}
+
+// Warp-per-chunk speculative forward run in 32-bit windows; a chunk whose
+// window spread is listed for k_uni_fwd_wide.
+__global__ void __launch_bounds__(kFwdWarps * 32, 4) k_uni_fwd_warp(UniParams P, unsigned long long n_chunks) {
+    __shared__ int4 lut[256];
+    extern __shared__ int32_t s_rows[];   // kFwdWarps edge tables
+    load_fat_lut(P, lut);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const unsigned long long k = (unsigned long long)blockIdx.x * kFwdWarps + w;
+    if (k >= n_chunks) return;
+    const EdgeBuf eb(s_rows + w * (kWarpEdgeBytes / 4));
+    const uint32_t code = fwd_chunk<int32_t>(P, lut, eb, k);
+    if (lane == 0) {
+        if (code & kRunLongRows) {
+            flag_chunk(P, k);
+        } else if (code & kRunSpread) {
+            const uint32_t i = atomicAdd(&P.st->wlist_len, 1u);
+            if (i < P.flist_cap) P.wlist[i] = (uint32_t)k;
+            else flag_chunk(P, k);
+        }
+    }
+}
+
+// The listed chunks' forward runs again, in 64-bit windows (a warp each, all
+// in parallel): their results replace the spread ones entirely.
+__global__ void __launch_bounds__(kFwdWarps * 32) k_uni_fwd_wide(UniParams P) {
+    __shared__ int4 lut[256];
+    extern __shared__ int32_t s_rows[];
+    const uint32_t n = min(P.st->wlist_len, P.flist_cap);
+    if (n == 0) return;
+    load_fat_lut(P, lut);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const EdgeBuf eb(s_rows + w * (kWarpEdgeBytes / 4));
+    for (uint32_t i = blockIdx.x * kFwdWarps + w; i < n; i += gridDim.x * kFwdWarps) {
+        const unsigned long long k = P.wlist[i];
+        const uint32_t code = fwd_chunk<long long>(P, lut, eb, k);
+        if (code && lane == 0) flag_chunk(P, k);
+    }
 }
 
 __global__ void __launch_bounds__(256) k_uni_check(UniParams P, unsigned long long n_chunks) {
@@ -913,22 +978,24 @@ __device__ uint64_t repair_from(const UniParams &P, const UGeo &gf, unsigned lon
 }
 
 // The state at flagged chunk f's start, the chunk before it being right (the
-// run from repair_from up to cs).
-__device__ __forceinline__ void warp_prefix(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRing &R,
-                                            const UGeo &gf, unsigned long long f, bool *sp) {
+// run from repair_from up to cs).  *code collects warp_dp's codes.
+template <typename V>
+__device__ __forceinline__ void warp_prefix(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRingT<V> &R,
+                                            const UGeo &gf, unsigned long long f, uint32_t *code) {
     const int lane = threadIdx.x & 31;
     uint64_t base = 0, s0 = 0;
     if (lane == 0) base = repair_from(P, gf, f, &s0);
     base = __shfl_sync(kFull, base, 0);
     s0 = __shfl_sync(kFull, s0, 0);
     ring_start(R, base, s0, lane);
-    *sp |= warp_dp(P, lut, eb, R, base, gf.cs, gf.de, 0, [](uint64_t, uint32_t) {}, [](uint32_t, unsigned) {});
+    *code |= warp_dp(P, lut, eb, R, base, gf.cs, gf.de, 0, [](uint64_t, uint32_t) {}, [](uint32_t, unsigned) {});
 }
 
 // Run chunk g (its start state in R), writing its true back pointers.
-__device__ __forceinline__ void warp_chunk(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRing &R,
-                                           const UGeo &g, bool *sp) {
-    *sp |= warp_dp(
+template <typename V>
+__device__ __forceinline__ void warp_chunk(const UniParams &P, const int4 *lut, const EdgeBuf &eb, WarpRingT<V> &R,
+                                           const UGeo &g, uint32_t *code) {
+    *code |= warp_dp(
         P, lut, eb, R, g.cs, g.ce, g.de, 0,
         [&](uint64_t q, uint32_t bp) {
             if (q != g.ds) back_at(P, q) = bp;
@@ -963,10 +1030,16 @@ __global__ void __launch_bounds__(kFwdWarps * 32) k_uni_fix_a(UniParams P, uint3
         const unsigned long long f = P.flist[i];
         const UGeo gf = uni_geo(P, f);
         WarpRing R;
-        bool sp = false;
-        warp_prefix(P, lut, eb, R, gf, f, &sp);
-        warp_chunk(P, lut, eb, R, gf, &sp);
-        const bool ok = !sp && (gf.last || warp_next_ok(P, gf, f));
+        uint32_t code = 0;
+        warp_prefix(P, lut, eb, R, gf, f, &code);
+        warp_chunk(P, lut, eb, R, gf, &code);
+        if (code == kRunSpread) {   // the 32-bit window spread: the same run in 64 bits
+            WideRing W;
+            code = 0;
+            warp_prefix(P, lut, eb, W, gf, f, &code);
+            warp_chunk(P, lut, eb, W, gf, &code);
+        }
+        const bool ok = !code && (gf.last || warp_next_ok(P, gf, f));
         if (ok && lane == 0) atomicOr(P.okn + (f >> 5), 1u << (f & 31));
     }
 }
@@ -1008,7 +1081,7 @@ __global__ void __launch_bounds__((kCoopWalkers + 1) * 32) k_uni_fix_coop(UniPar
         auto batch_b0 = [&](uint32_t k) { return k < npre ? from + 32ull * k : gf.cs + 32ull * (k - npre); };
         auto batch_to = [&](uint32_t k) { return k < npre ? gf.cs : gf.ce; };
         WarpRing R;
-        bool sp = false;
+        bool rows = false, sp = false;
         if (dp) ring_start(R, from, s_start, lane);
         for (uint32_t r = 0; r <= nr; r++) {   // round r: walk group r, recurrence over group r - 1
             if (!dp) {
@@ -1017,7 +1090,7 @@ __global__ void __launch_bounds__((kCoopWalkers + 1) * 32) k_uni_fix_coop(UniPar
                     int32_t *base = s_buf + ((r & 1) * kCoopWalkers + w) * kCoopBufWords;
                     const WalkOut wo = walk_batch(P, lut, EdgeBuf(base), batch_b0(k), batch_to(k), gf.de, 0);
                     ((uint4 *)(base + kWarpEdgeBytes / 4))[lane] =
-                        make_uint4(wo.X, wo.Y, (uint32_t)wo.lr, (uint32_t)wo.unk | ((uint32_t)wo.spread << 1));
+                        make_uint4(wo.X, wo.Y, (uint32_t)wo.lr, (uint32_t)wo.unk | ((uint32_t)wo.norow << 1));
                 }
             } else if (r > 0) {
                 const uint32_t k1 = min(nb, r * kCoopWalkers);
@@ -1029,9 +1102,9 @@ __global__ void __launch_bounds__((kCoopWalkers + 1) * 32) k_uni_fix_coop(UniPar
                     wo.Y = v.y;
                     wo.lr = (int)v.z;
                     wo.unk = v.w & 1u;
-                    wo.spread = (v.w >> 1) & 1u;
+                    wo.norow = (v.w >> 1) & 1u;
                     wo.crossing = false;
-                    sp |= wo.spread;
+                    rows |= wo.norow;
                     sp |= dp_batch(EdgeBuf(const_cast<int32_t *>(base)), R, batch_b0(k), batch_to(k), wo,
                                    [&](uint64_t q, uint32_t bp) {
                                        if (q >= gf.cs && q != gf.ds) back_at(P, q) = bp;
@@ -1043,8 +1116,17 @@ __global__ void __launch_bounds__((kCoopWalkers + 1) * 32) k_uni_fix_coop(UniPar
         if (dp) {
             if (gf.last && lane == (int)((gf.de - R.base) & 31)) back_at(P, gf.de) = ring_final(R, gf.de);
             __syncwarp();
+            rows = __any_sync(kFull, rows);
             sp = __any_sync(kFull, sp);
-            const bool ok = !sp && (gf.last || warp_next_ok(P, gf, f));
+            if (sp && !rows) {   // the 32-bit window spread: this warp runs the chunk again in 64 bits
+                WideRing W;      // (the walkers' buffers are idle until every warp reaches the next chunk)
+                uint32_t code = 0;
+                const EdgeBuf eb(s_buf);
+                warp_prefix(P, lut, eb, W, gf, f, &code);
+                warp_chunk(P, lut, eb, W, gf, &code);
+                sp = code != 0;
+            }
+            const bool ok = !rows && !sp && (gf.last || warp_next_ok(P, gf, f));
             if (ok && lane == 0) atomicOr(P.okn + (f >> 5), 1u << (f & 31));
         }
     }
@@ -1082,6 +1164,30 @@ __device__ unsigned long long thread_chain(const UniParams &P, const int4 *lut, 
     }
 }
 
+// A chain of k_uni_frepair_warp by the warp: from flagged chunk f's state,
+// chunks f, f + 1, ... through at least chunk `through`, until one whose
+// successor is not flagged and passes its check against the new back
+// pointers (or the document ends); *last = the chain's last chunk.  Returns
+// warp_dp's codes.
+template <typename V>
+__device__ uint32_t warp_chain(const UniParams &P, const int4 *lut, const EdgeBuf &eb, const UGeo &gf,
+                               unsigned long long f, unsigned long long through, unsigned long long *last,
+                               uint32_t *reruns) {
+    WarpRingT<V> R;
+    uint32_t code = 0;
+    warp_prefix(P, lut, eb, R, gf, f, &code);
+    unsigned long long m = f;
+    for (;;) {
+        const UGeo g = uni_geo(P, m);
+        warp_chunk(P, lut, eb, R, g, &code);
+        ++*reruns;
+        if (g.last || (m >= through && !flag_bit(P.fflag, m + 1) && warp_next_ok(P, g, m))) break;
+        ++m;
+    }
+    *last = m;
+    return code;
+}
+
 // Sequential repair per document (spans E <= 63), one warp per document, in
 // order over the flagged chunks.  Flagged chunk f was repaired by the
 // parallel pass (k_uni_fix_coop or k_uni_fix_a) from f-1's state, which is
@@ -1107,20 +1213,14 @@ __global__ void __launch_bounds__(128) k_uni_frepair_warp(UniParams P) {
         const bool fast = flag_bit(P.okn, f) && (gf.last || !flag_bit(P.fflag, f + 1));
         unsigned long long m = f + 1;
         if (!fast) {
-            WarpRing R;
-            bool sp = false;
-            warp_prefix(P, lut, eb, R, gf, f, &sp);
-            m = f;
-            for (;;) {
-                const UGeo g = uni_geo(P, m);
-                warp_chunk(P, lut, eb, R, g, &sp);
-                ++reruns;
-                if (g.last || (!flag_bit(P.fflag, m + 1) && warp_next_ok(P, g, m))) break;
-                ++m;
-            }
-            const unsigned long long wend = m;   // last chunk the warp rewrote
-            ++m;
-            if (sp) {   // values spread beyond 32 bits: lane 0 redoes the chain (through wend at least) in 64 bits
+            // after a call whose forward windows spread, chains go 64-bit at once
+            const bool wide = __ldcg(&P.st->wlist_len) != 0;
+            unsigned long long wend = f;   // last chunk the warp rewrote
+            uint32_t code = wide ? kRunSpread : warp_chain<int32_t>(P, lut, eb, gf, f, f, &wend, &reruns);
+            if (code == kRunSpread)   // the 32-bit window spread: the chain in 64 bits, through wend at least
+                code = warp_chain<long long>(P, lut, eb, gf, f, wend, &wend, &reruns);
+            m = wend + 1;
+            if (code) {   // a long row was missing: lane 0 redoes the chain (through wend at least) on its own ring
                 if (lane == 0) m = thread_chain(P, lut, gf, f, wend);
                 m = __shfl_sync(kFull, m, 0);
             }
@@ -1507,7 +1607,7 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
         return rc;
     UniState *h = (UniState *)pin;
     const bool profile = ctx->profile != 0;
-    if (profile && (rc = ensure_events(ctx, 4))) return rc;
+    if (profile && (rc = ensure_events(ctx, 5))) return rc;
 
     UniParams P{};
     P.bytes = d_bytes;
@@ -1553,7 +1653,7 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
     void *back, *gback, *info, *flag, *prefix, *status;
     if ((rc = ensure(ctx, S_UNI_BACK, (h->span + 1) * 4, &back)) ||
         (rc = ensure(ctx, S_UNI_GBACK, nc * (uint64_t)P.grec * 4, &gback)) ||
-        (rc = ensure(ctx, S_UNI_CHUNK, nc * 12, &info)) || (rc = ensure(ctx, S_UNI_FLAG, words * 16 + nc * 4, &flag)) ||
+        (rc = ensure(ctx, S_UNI_CHUNK, nc * 12, &info)) || (rc = ensure(ctx, S_UNI_FLAG, words * 16 + nc * 8, &flag)) ||
         (rc = ensure(ctx, S_UNI_PREFIX, nc * 8 + ((uint64_t)n_docs + 1) * 8, &prefix)) ||
         (rc = ensure(ctx, S_UNI_STATUS, tiles * 8, &status)))
         return rc;
@@ -1577,6 +1677,7 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
     P.okp = P.okn + words;
     P.flist = P.okp + words;
     P.flist_cap = (uint32_t)std::min<unsigned long long>(nc, 0xFFFFFFFFull);
+    P.wlist = P.flist + nc;
     P.prefix = (unsigned long long *)prefix;
     P.status = (unsigned long long *)status;
     P.id_off = d_id_off_out ? (unsigned long long *)d_id_off_out : P.prefix + nc;
@@ -1596,7 +1697,10 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
                  "k_uni_fix_a smem");
         BPE_CUDA(ctx, cudaFuncSetAttribute(k_uni_fix_coop, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)coop_smem),
                  "k_uni_fix_coop smem");
+        BPE_CUDA(ctx, cudaFuncSetAttribute(k_uni_fwd_wide, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)warp_smem),
+                 "k_uni_fwd_wide smem");
         k_uni_fwd_warp<<<(unsigned)((nc + kFwdWarps - 1) / kFwdWarps), kFwdWarps * 32, warp_smem, s>>>(P, nc);
+        k_uni_fwd_wide<<<(unsigned)std::max(1, ctx->sm_count * 2), kFwdWarps * 32, warp_smem, s>>>(P);
     } else if (R == 64) {
         k_uni_fwd<64><<<grid_c, kUniThreads, 0, s>>>(P, nc);
     } else {
@@ -1614,6 +1718,7 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
     } else {
         k_uni_frepair<256><<<grid_d, 128, 0, s>>>(P);
     }
+    if (profile) cudaEventRecord(ctx->events[4], s);
     k_uni_bspec<<<grid_c256, 256, 0, s>>>(P, nc);
     k_uni_bcheck<<<grid_c256, 256, 0, s>>>(P, nc);
     k_uni_bfix_a<<<grid_c256, 256, 0, s>>>(P, nc);
@@ -1635,21 +1740,32 @@ extern "C" int unigram_encode(bpe_ctx *ctx, const bpe_unigram *model, const uint
 
     const uint64_t total = h->total;
     *n_ids = total;
+    // families, one pass each per call (launches counts passes): the forward
+    // pass (with the wide re-run), its checks and repairs, the backward pass
+    // (speculative backtrack, checks, re-walks), the emit pass
     const int a = stats_slot(ctx, "unigram_fwd"), b = stats_slot(ctx, "unigram_fix"), c = stats_slot(ctx, "unigram_emit");
+    const int bk = stats_slot(ctx, "unigram_back");
     ctx->stats.k[a].launches = 1;
-    ctx->stats.k[b].launches = warp ? 7 : 6;
+    ctx->stats.k[b].launches = 1;
+    ctx->stats.k[bk].launches = 1;
     ctx->stats.k[c].launches = 1;
+    const int wd = stats_slot(ctx, "unigram_wide");   // chunks whose forward run took 64-bit windows
+    ctx->stats.k[wd].launches = h->wlist_len;
+    ctx->stats.k[wd].bytes = (double)h->wlist_len * C;
     ctx->stats.k[a].bytes = (double)h->span;
-    ctx->stats.k[b].bytes = (double)h->fwd_repairs * C + (double)h->bwd_repairs;   // chunks re-run, chunks re-walked
+    ctx->stats.k[b].bytes = (double)h->fwd_repairs * C;   // chunks re-run
+    ctx->stats.k[bk].bytes = 4.0 * (double)h->span;        // back pointers read by the backtrack
     ctx->stats.k[c].bytes = 4.0 * (double)total;
-    ctx->stats.kernel_launches = (warp ? 13 : 12) + (P.tstart ? 1 : 0);
+    ctx->stats.kernel_launches = (warp ? 15 : 12) + (P.tstart ? 1 : 0);
     if (profile) {
-        float x = 0, y = 0, z = 0;
+        float x = 0, y = 0, z = 0, u = 0;
         cudaEventElapsedTime(&x, ctx->events[0], ctx->events[1]);
-        cudaEventElapsedTime(&y, ctx->events[1], ctx->events[2]);
+        cudaEventElapsedTime(&y, ctx->events[1], ctx->events[4]);
+        cudaEventElapsedTime(&u, ctx->events[4], ctx->events[2]);
         cudaEventElapsedTime(&z, ctx->events[2], ctx->events[3]);
         ctx->stats.k[a].ms = x;
         ctx->stats.k[b].ms = y;
+        ctx->stats.k[bk].ms = u;
         ctx->stats.k[c].ms = z;
         cudaGetLastError();
     }

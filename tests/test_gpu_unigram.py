@@ -322,3 +322,26 @@ def test_long_document(ctx, golden, batch_vocab):
     """One 64 MiB document: every chunk but the first few runs speculatively."""
     data = synth.corpus("enc", 64 << 20)
     unigram_workload(ctx, golden, "unigram_doc", data, np.array([0, data.size], dtype=np.uint64), *batch_vocab)
+
+
+def test_wide_windows(ctx):
+    """Scores of a fine unit with many short tokens: a 63-byte window's values
+    lie more than 2^30 units apart, so the forward runs (and the repairs of
+    the parity runs) take 64-bit windows; the result is still exact."""
+    # unit 2^-23 (from b's score); every score within the warp kernels' 2^29 units
+    sc = [float(np.float32(x)) for x in (-20.0, -30.5, -1.0000001)]
+    assert sc[2] != -1.0
+    vb, off = vocab_arrays([b"a", b"aa", b"b"])
+    docs = [b"a" * 5000, b"ab" * 3000, b"b" * 700, b"a" * 40001, b""]
+    check_unigram(ctx, vb, off, sc, 3, -40.0, docs, chunk=256)
+    assert ctx.stats()["unigram_wide"]["launches"] > 0
+    # the smoke's model: the tiny corpus's 64 merges, Zipf scores over 320 tokens
+    merges, _ = oracle.train_words(oracle.pretokenize(synth.corpus("tiny", 32 * 1024)), 64)
+    vb, off = oracle.vocab_from_merges(merges)
+    n_tok = off.size - 1
+    scores = synth.unigram_scores(n_tok)
+    unk = synth.unigram_unk_score(scores)
+    lex = synth.lexicon("tiny")
+    docs = [lex.corpus(7, 16 * 1024).tobytes()] + [lex.corpus(20 + d, 3000 + 997 * d).tobytes() for d in range(6)]
+    check_unigram(ctx, vb, off, scores, n_tok, unk, docs)
+    assert ctx.stats()["unigram_wide"]["launches"] > 0
