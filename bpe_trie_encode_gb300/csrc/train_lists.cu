@@ -65,8 +65,6 @@ namespace {
 
 constexpr uint32_t kDead = 0x80000000u;       // dead position; bits 0..29: distance back to its token's head
 constexpr uint32_t kDistMask = 0x3FFFFFFFu;
-constexpr uint32_t kNear = 0x40000000u;       // a last byte's dead mark that carries its head's symbol (see last_mark)
-constexpr uint32_t kNearDist = 0x1FFFu;
 constexpr uint32_t kNone = 0xFFFFFFFFu;
 constexpr uint32_t kBadBits = 0xFFFEFF00u;    // bits a byte-level input symbol never has
 constexpr uint32_t kBaseEntries = 65536;      // entry (l << 8) | r for byte pairs
@@ -148,18 +146,6 @@ __device__ __forceinline__ unsigned long long pack(uint32_t count, uint32_t key)
 __device__ __forceinline__ uint32_t sid(uint32_t s) { return s & 0xFFFFu; }
 __device__ __forceinline__ uint32_t base_key(uint32_t e) { return ((e >> 8) << 16) | (e & 0xFFu); }
 
-// The dead mark of a multi-byte token's last byte, d bytes after its head,
-// whose symbol is hs: when d fits 13 bits it also holds hs in bits 13..29
-// (kNear), and the cell's y then mirrors the head's pair entry, so a reader
-// standing at the next token finds its left neighbour without loading the
-// head; otherwise the distance alone.  Other dead positions hold the
-// distance alone; only last bytes are ever read for it.
-__device__ __forceinline__ uint32_t last_mark(uint32_t hs, uint32_t d) {
-    return d <= kNearDist ? kDead | kNear | ((hs & 0x1FFFFu) << 13) | d : kDead | d;
-}
-__device__ __forceinline__ uint32_t dead_dist(uint32_t w) { return (w & kNear) ? (w & kNearDist) : (w & kDistMask); }
-__device__ __forceinline__ uint32_t near_head(uint32_t w) { return (w >> 13) & 0x1FFFFu; }
-
 // A position's symbol (or dead mark), and its whole cell.
 __device__ __forceinline__ uint32_t ld_sym(const uint2 *cell, uint32_t x) { return __ldcg(&cell[x].x); }
 __device__ __forceinline__ uint2 ld_cell(const uint2 *cell, uint32_t x) { return __ldcg(cell + x); }
@@ -171,8 +157,8 @@ __device__ __forceinline__ uint32_t prev_live(const uint2 *cell, uint32_t p, uin
         *sa = sx;
         return x;
     }
-    const uint32_t a = x - dead_dist(sx);
-    *sa = (sx & kNear) ? near_head(sx) : ld_sym(cell, a);
+    const uint32_t a = x - (sx & kDistMask);
+    *sa = ld_sym(cell, a);
     return a;
 }
 
@@ -540,13 +526,11 @@ __device__ __forceinline__ void merge_ctx(const LP &P, MergeCtx &M, uint32_t k, 
 }
 
 // Where a merge's outputs are staged (shared memory): the left positions of
-// merging occurrences and the new pairs (key, position, and the last byte of
-// the token at that position, whose cell mirrors the pair's entry: kNone
-// when there is none to keep).  Past the capacity
+// merging occurrences and the new pairs (key, position).  Past the capacity
 // they go straight to the global records (direct) -- only k_lscan allows
 // that; k_ltail's capacities cover a whole merge, anything more is an error.
 struct Stage {
-    uint32_t *app, *rkey, *rpos, *rmir;
+    uint32_t *app, *rkey, *rpos;
     uint32_t *na, *nr;
     uint32_t app_cap, rec_cap;
     bool direct;
@@ -559,12 +543,12 @@ __device__ void emit_direct_app(const LP &P, const MergeCtx &M, uint32_t p) {
     if (i < P.app_cap) P.app[M.par][i] = p;
     else atomicOr(&P.st->err, LERR_RECORDS);
 }
-__device__ void emit_direct_rec(const LP &P, const MergeCtx &M, uint32_t key, uint32_t pos, uint32_t mir) {
+__device__ void emit_direct_rec(const LP &P, const MergeCtx &M, uint32_t key, uint32_t pos) {
     const uint32_t h = hash_slot(P, key, M.tag, M.par);
     if (h == kNone) return;
     const uint32_t rank = atomicAdd(P.hcnt + h, 1u);
     const uint32_t i = atomicAdd(&P.st->nrec[M.par], 1u);
-    if (i < P.rec_cap) P.rec[M.par][i] = make_uint4(h, rank, pos, mir);
+    if (i < P.rec_cap) P.rec[M.par][i] = make_uint4(h, rank, pos, 0u);
     else atomicOr(&P.st->err, LERR_RECORDS);
 }
 
@@ -574,15 +558,13 @@ __device__ __forceinline__ void emit_app(const LP &P, const MergeCtx &M, const S
     else if (S.direct) emit_direct_app(P, M, p);
     else atomicOr(&P.st->err, LERR_RECORDS);
 }
-__device__ __forceinline__ void emit_rec(const LP &P, const MergeCtx &M, const Stage &S, uint32_t key, uint32_t pos,
-                                         uint32_t mir) {
+__device__ __forceinline__ void emit_rec(const LP &P, const MergeCtx &M, const Stage &S, uint32_t key, uint32_t pos) {
     const uint32_t i = atomicAdd(S.nr, 1u);
     if (i < S.rec_cap) {
         S.rkey[i] = key;
         S.rpos[i] = pos;
-        S.rmir[i] = mir;
     } else if (S.direct) {
-        emit_direct_rec(P, M, key, pos, mir);
+        emit_direct_rec(P, M, key, pos);
     } else {
         atomicOr(&P.st->err, LERR_RECORDS);
     }
@@ -596,9 +578,7 @@ __device__ __forceinline__ void emit_rec(const LP &P, const MergeCtx &M, const S
 // merging occurrence.  The pair (a, p) loses a count and (a or a2, new)
 // forms; the pair (q, b) loses a count and (new, b) forms -- except where
 // two occurrences meet, which the right one of them handles.  The staged
-// record is p with p's WORD_START in bit 31.  A new pair's entry is mirrored
-// at the last byte of its left token: p - 1 for (a or a2, new), b - 1 for
-// (new, b).
+// record is p with p's WORD_START in bit 31.
 __device__ __forceinline__ void occurrence(const LP &P, const MergeCtx &M, const Stage &S, uint32_t p, uint32_t sp,
                                            uint32_t a, uint32_t sa, uint32_t ea, bool pocc, uint32_t a2, uint32_t b,
                                            uint32_t sb, uint32_t eq, bool qocc) {
@@ -609,12 +589,12 @@ __device__ __forceinline__ void occurrence(const LP &P, const MergeCtx &M, const
     }
     if (a != kNone) {
         if (ea != M.es) atomicSub(P.ecnt + ea, 1u);
-        if (pocc) emit_rec(P, M, S, (M.nid << 16) | M.nid, a2, p - 1);
-        else emit_rec(P, M, S, (sid(sa) << 16) | M.nid, a, p - 1);
+        if (pocc) emit_rec(P, M, S, (M.nid << 16) | M.nid, a2);
+        else emit_rec(P, M, S, (sid(sa) << 16) | M.nid, a);
     }
     if (b < M.n && !(sb & kWordStart) && !qocc) {
         if (eq != M.es) atomicSub(P.ecnt + eq, 1u);
-        emit_rec(P, M, S, (M.nid << 16) | sid(sb), p, b - 1);
+        emit_rec(P, M, S, (M.nid << 16) | sid(sb), p);
     }
     emit_app(P, M, S, rec);
 }
@@ -649,10 +629,6 @@ __device__ void list_entry(const LP &P, const MergeCtx &M, const Stage &S, uint3
         if (!(sx & kDead)) {
             a = p - 1;
             sa = sx;
-            ea = ex;
-        } else if (sx & kNear) {   // the head's symbol in the mark, its pair entry mirrored in the cell
-            a = p - 1 - (sx & kNearDist);
-            sa = near_head(sx);
             ea = ex;
         } else {
             a = p - 1 - (sx & kDistMask);
@@ -783,10 +759,6 @@ __device__ __forceinline__ void list_batch(const LP &P, const MergeCtx &M, const
                 a[j] = p[j] - 1;
                 sa[j] = sx[j];
                 ea[j] = ex[j];
-            } else if (sx[j] & kNear) {   // the head's symbol in the mark, its pair entry mirrored in the cell
-                a[j] = p[j] - 1 - (sx[j] & kNearDist);
-                sa[j] = near_head(sx[j]);
-                ea[j] = ex[j];
             } else {
                 a[j] = p[j] - 1 - (sx[j] & kDistMask);
                 const uint2 ca = ld_cell(P.cell, a[j]);
@@ -811,8 +783,8 @@ __device__ __forceinline__ void list_batch(const LP &P, const MergeCtx &M, const
 #pragma unroll
     for (int j = 0; j < J; j++) {
         if (np[j] && (s2[j] & kDead)) {
-            a2[j] -= dead_dist(s2[j]);
-            s2[j] = (s2[j] & kNear) ? near_head(s2[j]) : ld_sym(P.cell, a2[j]);
+            a2[j] -= s2[j] & kDistMask;
+            s2[j] = ld_sym(P.cell, a2[j]);
         }
     }
 #pragma unroll
@@ -840,15 +812,12 @@ __device__ __forceinline__ void list_batch(const LP &P, const MergeCtx &M, const
         const uint32_t nrec = (q1 != kNone ? 1u : 0u) + (q2 != kNone ? 1u : 0u);
         uint32_t ro = warp_reserve(S.nr, nrec);
         const uint32_t ao = warp_reserve(S.na, ok[j] ? 1u : 0u);
-        // mirrors: the last byte before p for (a or a2, new), the new token's for (new, b)
-        const uint32_t m1 = p[j] - 1, m2 = p[j] + M.vl + M.vr - 1;
         if (q1 != kNone) {
             if (ro < S.rec_cap) {
                 S.rkey[ro] = k1;
                 S.rpos[ro] = q1;
-                S.rmir[ro] = m1;
             } else if (S.direct) {
-                emit_direct_rec(P, M, k1, q1, m1);
+                emit_direct_rec(P, M, k1, q1);
             } else {
                 atomicOr(&P.st->err, LERR_RECORDS);
             }
@@ -858,9 +827,8 @@ __device__ __forceinline__ void list_batch(const LP &P, const MergeCtx &M, const
             if (ro < S.rec_cap) {
                 S.rkey[ro] = k2;
                 S.rpos[ro] = q2;
-                S.rmir[ro] = m2;
             } else if (S.direct) {
-                emit_direct_rec(P, M, k2, q2, m2);
+                emit_direct_rec(P, M, k2, q2);
             } else {
                 atomicOr(&P.st->err, LERR_RECORDS);
             }
@@ -930,7 +898,7 @@ __device__ __forceinline__ void group_pairs(const uint32_t *rkey, uint32_t *rslo
 // Shared staging of one k_lscan round.
 struct LsShared {
     uint32_t app[kLsRound];
-    uint32_t rkey[kLsRecCap], rpos[kLsRecCap], rmir[kLsRecCap], rslot[kLsRecCap];
+    uint32_t rkey[kLsRecCap], rpos[kLsRecCap], rslot[kLsRecCap];
     uint32_t hkey[kLsHash], hcnt[kLsHash], hglob[kLsHash], hbase[kLsHash];
     uint16_t used[kLsHash];
     uint32_t na, nr, nused, abase, rbase;
@@ -1022,7 +990,7 @@ __global__ void __launch_bounds__(kLsThreads, 2) k_lscan(LP P) {
     if (!multi_merge(P, &k, &bw, &es)) return;
     MergeCtx M;
     merge_ctx(P, M, k, bw, es);
-    const Stage G{S.app, S.rkey, S.rpos, S.rmir, &S.na, &S.nr, (uint32_t)kLsRound, (uint32_t)kLsRecCap, true};
+    const Stage G{S.app, S.rkey, S.rpos, &S.na, &S.nr, (uint32_t)kLsRound, (uint32_t)kLsRecCap, true};
     const uint32_t len = __ldcg(P.ellen + es);
     const unsigned long long lb = __ldcg(P.eloff + es);
     const uint32_t nrounds = (len + kLsRound - 1) / kLsRound;
@@ -1069,8 +1037,7 @@ __global__ void __launch_bounds__(kLsThreads, 2) k_lscan(LP P) {
             const uint32_t rs = S.rslot[i], h = rs >> 16;
             const uint32_t g = S.hglob[h];
             const uint32_t o = S.rbase + i;
-            if (g != kNone && o < P.rec_cap)
-                P.rec[M.par][o] = make_uint4(g, S.hbase[h] + (rs & 0xFFFFu), S.rpos[i], S.rmir[i]);
+            if (g != kNone && o < P.rec_cap) P.rec[M.par][o] = make_uint4(g, S.hbase[h] + (rs & 0xFFFFu), S.rpos[i], 0u);
             else if (g != kNone) atomicOr(&st->err, LERR_RECORDS);
         }
         __syncthreads();
@@ -1169,17 +1136,15 @@ __global__ void __launch_bounds__(kLaThreads) k_lapply(LP P) {
     for (uint32_t i = blockIdx.x * kLaThreads + threadIdx.x; i < na; i += stride) {
         const uint32_t rc = __ldcg(P.app[par] + i), p = rc & ~kDead;
         const uint32_t q = p + vl, last = q + vr - 1;
-        const uint32_t hs = nid | ((rc & kDead) ? kWordStart : 0u);
-        P.cell[p].x = hs;
-        P.cell[q].x = last != q ? kDead | (q - p) : last_mark(hs, q - p);
-        if (last != q) P.cell[last].x = last_mark(hs, last - p);
+        P.cell[p].x = nid | ((rc & kDead) ? kWordStart : 0u);
+        P.cell[q].x = kDead | (q - p);
+        if (last != q) P.cell[last].x = kDead | (last - p);
     }
     for (uint32_t i = blockIdx.x * kLaThreads + threadIdx.x; i < nr; i += stride) {
         const uint4 rc = __ldcg(P.rec[par] + i);
         const uint32_t e = __ldcg(P.hent + rc.x);
         P.occ[__ldcg(P.eloff + e) + rc.y] = rc.z;
         P.cell[rc.z].y = e;
-        P.cell[rc.w].y = e;   // the mirror at the last byte of the pair's left token (rc.z itself for one byte)
     }
     const bool more = k + 1 < st->n_merges;
     // the frontier's best (every count of merge k is final)
@@ -1243,7 +1208,7 @@ __global__ void __launch_bounds__(kLaThreads) k_lapply(LP P) {
 // loop's copy of the merge state.
 struct TlShared {
     uint32_t app[kTlList];
-    uint32_t rkey[kTlRecCap], rpos[kTlRecCap], rmir[kTlRecCap];   // rkey becomes the local slot and rank once grouped
+    uint32_t rkey[kTlRecCap], rpos[kTlRecCap];   // rkey becomes the local slot and rank once grouped
     uint32_t hkey[kTlHash], hcnt[kTlHash];   // after allocation: hcnt = entry, hkey = its list start
     uint16_t used[kTlHash];
     uint32_t na, nr, nused, fn_scratch;
@@ -1251,7 +1216,9 @@ struct TlShared {
     unsigned long long sv[32];
     uint32_t se[32];
 };
-static_assert(sizeof(TlShared) <= 227 * 1024, "k_ltail's shared state must fit one CTA");
+// (kept well below the SM's 228 KB: what it leaves is the L1 that holds the
+// tail's gathers in flight; 32 KB more made the loop 21% slower)
+static_assert(sizeof(TlShared) <= 164 * 1024 - 1024, "k_ltail's shared state fits the 164 KB carveout");
 
 // Up to `budget` consecutive merges from st->k_cur in one CTA, while their
 // lists hold at most st->tail_len entries: the same steps as k_lscan +
@@ -1278,7 +1245,7 @@ __global__ void __launch_bounds__(kTlThreads, 1) k_ltail(LP P, uint32_t budget) 
     }
     __syncthreads();
     uint32_t done = 0;
-    const Stage G{S.app, S.rkey, S.rpos, S.rmir, &S.na, &S.nr, (uint32_t)kTlList, (uint32_t)kTlRecCap, false};
+    const Stage G{S.app, S.rkey, S.rpos, &S.na, &S.nr, (uint32_t)kTlList, (uint32_t)kTlRecCap, false};
     unsigned long long bw = k < n_merges ? __ldcg(P.best + k) : 0ull;   // then carried from each argmax
     uint32_t es = k < n_merges ? __ldcg(P.ebest + k) : kNone;
     while (done < budget && k < n_merges) {
@@ -1356,16 +1323,14 @@ __global__ void __launch_bounds__(kTlThreads, 1) k_ltail(LP P, uint32_t budget) 
         for (uint32_t i = threadIdx.x; i < na; i += kTlThreads) {
             const uint32_t rc = S.app[i], p = rc & ~kDead;
             const uint32_t q = p + M.vl, last = q + M.vr - 1;
-            const uint32_t hs = M.nid | ((rc & kDead) ? kWordStart : 0u);
-            P.cell[p].x = hs;
-            P.cell[q].x = last != q ? kDead | (q - p) : last_mark(hs, q - p);
-            if (last != q) P.cell[last].x = last_mark(hs, last - p);
+            P.cell[p].x = M.nid | ((rc & kDead) ? kWordStart : 0u);
+            P.cell[q].x = kDead | (q - p);
+            if (last != q) P.cell[last].x = kDead | (last - p);
         }
         for (uint32_t i = threadIdx.x; i < nr; i += kTlThreads) {
             const uint32_t rs = S.rkey[i], h = rs >> 16, pos = S.rpos[i];
             P.occ[S.hkey[h] + (rs & 0xFFFFu)] = pos;
             P.cell[pos].y = S.hcnt[h];
-            P.cell[S.rmir[i]].y = S.hcnt[h];   // the mirror at the last byte of the pair's left token
         }
         __syncthreads();
         for (uint32_t u = threadIdx.x; u < nu; u += kTlThreads) {
