@@ -661,6 +661,10 @@ def run_ours(args, rank, world, local_rank):
                  for f in ("pair_count", "list_build", "compact", "encode_spec", "encode_emit") + loop}
     # the timed step's dominant kernel: the merge loop's tail (most merges run there)
     dom = max((f for f in rooflines if rooflines[f]), key=lambda f: kern[f]["ms"])
+    for f in loop:   # what the HBM fraction of the merge kernels means
+        if rooflines.get(f):
+            rooflines[f]["note"] = ("latency-bound: a chain of dependent gathers and barriers per merge "
+                                    "(one CTA for the tail); HBM is nearly idle")
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "merges/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
