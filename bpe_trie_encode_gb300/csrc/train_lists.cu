@@ -44,10 +44,11 @@
 //                reservation per distinct pair)
 //   k_lscan      per merge: the pair's live occurrences; count deltas; new
 //                pairs grouped per CTA round and registered in a per-merge
-//                hash; the last CTA creates the new entries and lists, and
-//                finds the next merge's pair in the frontier
+//                hash; the last CTA creates the new entries and lists
 //   k_lapply     per merge: new ids, dead marks and back distances; new pairs
-//                into their lists; a full rescan when the frontier ran dry
+//                into their lists; every CTA takes a slice of the frontier
+//                and the last one combines them into the next merge's pair
+//                (a full rescan when the frontier ran dry)
 //   k_ltail      per merge while the lists are short (at most 4,096
 //                entries): k_lscan + k_lapply's steps in one CTA, up to 512
 //                merges per launch
