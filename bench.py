@@ -527,7 +527,10 @@ def run_ours(args, rank, world, local_rank):
         enc = {"trie": trie, "vb": vb, "voff": voff, "h": h_enc, "d": h_enc.to(dev),
                "h_off": torch.from_numpy(doc_off).pin_memory(), "d_off": torch.from_numpy(doc_off).to(dev),
                "workload": wl, "bytes": int(etext.size),
-               "ids": torch.empty(int(etext.size), dtype=torch.int32, device=dev)}
+               "ids": torch.empty(int(etext.size), dtype=torch.int32, device=dev),
+               # the end-to-end leg's host outputs, pinned at set-up next to its inputs
+               "h_ids": torch.empty(int(etext.size), dtype=torch.int32, pin_memory=True),
+               "h_ioff": torch.empty(doc_off.size, dtype=torch.int64)}
         del etext
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -597,8 +600,7 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_e2e:
         h_merges_bytes = n_merges * 16
         if enc:   # pinned host outputs of the end-to-end encode
-            h_ids_buf = torch.empty(enc["bytes"], dtype=torch.int32, pin_memory=True)
-            h_ioff_buf = torch.empty(enc["h_off"].numel(), dtype=torch.int64)
+            h_ids_buf, h_ioff_buf = enc["h_ids"], enc["h_ioff"]
         link = None
         if enc:   # the host link's own copy speed in this run: what bounds the end-to-end encode
             n_cp = max(acc["n_ids"], 1)
