@@ -93,7 +93,7 @@ constexpr uint32_t kCsRound = 8u << 20;       // compaction round: 64 MB of cell
 constexpr uint32_t kHashProbes = 4096;
 constexpr unsigned kSpinLimit = 1u << 22;
 constexpr int kInFlight = 3;
-constexpr uint32_t kFfInit = 240;             // frontier threshold: ff / 256 of the last count
+constexpr uint32_t kFfInit = 224;             // frontier threshold: ff / 256 of the last count
 enum : uint32_t { LERR_BADINPUT = 16u, LERR_ENTRIES = 32u, LERR_LISTS = 64u, LERR_HASH = 128u, LERR_RECORDS = 256u };
 
 struct LState {
