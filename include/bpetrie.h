@@ -326,9 +326,7 @@ void trie_stream_close(bpe_stream *stream);
  *
  * h_bytes, h_doc_off (n_docs+1 ascending offsets): host input (pinned memory
  * lets the copies overlap the encode); h_ids_out: ids_capacity int32 (host,
- * pinned for the same reason; a large output buffer pinned early in the
- * process, before other large allocations, measured about 5x faster copies
- * than one pinned after them); h_id_off_out (nullable): n_docs+1 uint64.
+ * pinned for the same reason); h_id_off_out (nullable): n_docs+1 uint64.
  * *n_ids receives the total; past ids_capacity nothing is written and
  * BPE_ERR_CAPACITY is returned with the required size.  Blocks until done.
  * Errors: INVALID_ARG, CAPACITY, OOM, TIMEOUT, CUDA. */
