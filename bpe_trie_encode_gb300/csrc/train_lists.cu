@@ -93,7 +93,7 @@ constexpr uint32_t kCsRound = 8u << 20;       // compaction round: 64 MB of cell
 constexpr uint32_t kHashProbes = 4096;
 constexpr unsigned kSpinLimit = 1u << 22;
 constexpr int kInFlight = 3;
-constexpr uint32_t kFfInit = 224;             // frontier threshold: ff / 256 of the last count
+constexpr uint32_t kFfInit = 240;             // frontier threshold: ff / 256 of the last count
 enum : uint32_t { LERR_BADINPUT = 16u, LERR_ENTRIES = 32u, LERR_LISTS = 64u, LERR_HASH = 128u, LERR_RECORDS = 256u };
 
 struct LState {
@@ -1065,9 +1065,8 @@ __global__ void __launch_bounds__(kLsThreads, 2) k_lscan(LP P) {
 }
 
 // One CTA: every entry rescanned into a new frontier (threshold ff / 256 of
-// the count of merge k) and the argmax of merge k + 1.  Counts are read four
-// at a time; a key only for a count that can win or join the frontier.
-// Returns the winner in *bv, *be (every thread).
+// the count of merge k) and the argmax of merge k + 1.  Returns the winner
+// in *bv, *be (every thread).
 template <int THREADS>
 __device__ void rescan(const LP &P, uint32_t k, unsigned long long *sv, uint32_t *se, uint32_t *s_fn,
                        unsigned long long *out_bv, uint32_t *out_be) {
@@ -1081,23 +1080,39 @@ __device__ void rescan(const LP &P, uint32_t k, unsigned long long *sv, uint32_t
     unsigned long long bv = 0;
     uint32_t be = kNone;
     const uint32_t D4 = (D + 3) / 4;   // dcap is a multiple of 4: the last load stays in bounds
-#pragma unroll 4
-    for (uint32_t i = threadIdx.x; i < D4; i += THREADS) {
-        const uint4 c4 = __ldcg(reinterpret_cast<const uint4 *>(P.ecnt) + i);
-        const uint32_t cs[4] = {c4.x, c4.y, c4.z, c4.w};
+    // Counts are read kRsBatch 16-byte loads per thread at a time, all issued
+    // before any is used (the frontier stores below would otherwise keep the
+    // compiler from hoisting the next load).  Most groups of four hold no count
+    // that can join the frontier or lead this thread: one test on their largest
+    // skips them.  A byte pair's key follows from its entry index.
+    constexpr int kRsBatch = 8;
+    for (uint32_t i0 = threadIdx.x; i0 < D4; i0 += kRsBatch * THREADS) {
+        uint4 c4[kRsBatch];
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const uint32_t e = 4 * i + j, c = cs[j];
-            if (e >= D || c == 0 || (c < T && c < (uint32_t)(bv >> 32))) continue;
-            const uint32_t key = __ldcg(P.ekey + e);
-            const unsigned long long v = pack(c, key);
-            if (v > bv) {
-                bv = v;
-                be = e;
-            }
-            if (c >= T) {
-                const uint32_t f = atomicAdd(s_fn, 1u);
-                if (f < P.fcap) P.fr[fnext][f] = make_uint2(e, key);
+        for (int u = 0; u < kRsBatch; u++) {
+            const uint32_t i = i0 + u * THREADS;
+            c4[u] = i < D4 ? __ldcg(reinterpret_cast<const uint4 *>(P.ecnt) + i) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kRsBatch; u++) {
+            const uint32_t m4 = max(max(c4[u].x, c4[u].y), max(c4[u].z, c4[u].w));
+            if (m4 == 0 || (m4 < T && m4 < (uint32_t)(bv >> 32))) continue;
+            const uint32_t i = i0 + u * THREADS;
+            const uint32_t cs[4] = {c4[u].x, c4[u].y, c4[u].z, c4[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const uint32_t e = 4 * i + j, c = cs[j];
+                if (e >= D || c == 0 || (c < T && c < (uint32_t)(bv >> 32))) continue;
+                const uint32_t key = e < kBaseEntries ? base_key(e) : __ldcg(P.ekey + e);
+                const unsigned long long v = pack(c, key);
+                if (v > bv) {
+                    bv = v;
+                    be = e;
+                }
+                if (c >= T) {
+                    const uint32_t f = atomicAdd(s_fn, 1u);
+                    if (f < P.fcap) P.fr[fnext][f] = make_uint2(e, key);
+                }
             }
         }
     }
