@@ -69,3 +69,14 @@ def test_reference_arm_runs_on_rank_zero_only():
     out = bench.run_reference(ns, 0, 2)
     assert out["impl"] == "reference" and out["n_gpus"] == 2 and out["value"] > 0
     assert out["e2e"]["h2d_bytes_per_step"] == 0 and out["cpu_baseline"]["cores"] == 1
+    # the JSON line's contract: the bench line's keys, with this run's own
+    # figures in cpu_baseline and e2e
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config"):
+        assert key in out, key
+    assert out["steps"] == 1 and out["warmup"] == 0 and out["higher_is_better"] is True
+    assert out["vs_baseline"] is None and out["config"]["workload"]
+    cb = out["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["sample"] and cb["value"] == out["value"] and cb["unit"] == out["unit"]
+    e2e = out["e2e"]
+    assert e2e["value"] == out["value"] and e2e["unit"] == out["unit"] and e2e["d2h_bytes_per_step"] == 0
